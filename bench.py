@@ -1,0 +1,330 @@
+#!/usr/bin/env python
+"""Benchmark of the quantized-KV MLA decode step on GB300.
+
+Workload: KV8 decode, 8 sequences x 4096 cached rows, 128 heads sharing one
+576-dim latent cache (fp8 e4m3 + two f32 scales per row, 584 B), one bf16
+query token per sequence and head.  Inputs are synthetic and seeded
+(quantized_kv_cache_kv8_gb300.synth): latent rows N(0,1) x per-channel
+log-normal gains.
+
+One step = the whole hot path for one decode token of every sequence:
+  1. kv8_encode of the 8 new rows (one per sequence, appended at the end of its
+     range of the resident pool),
+  2. kv_attn_decode over all 8 x 4096 rows (split-T partials + merge).
+The cache (19 MB) fits in L2, so a 256 MB buffer is written between timed
+steps (outside the timed events) to flush it.
+
+Metric: cache GB/s = rows read per step x 584 B / step time; rows/s and the
+fraction of the measured HBM copy bandwidth are reported beside it.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--path auto|simt|tensor]
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+B, T, H, D, DV = 8, 4096, 128, 576, 512
+ROW_BYTES = 576 + 2 * 4
+FLOPS_PER_ROW = H * (D + DV) * 2
+SEED = 2
+METRIC = "quantized-KV MLA decode attn: cache GB/s & % of HBM roofline; rows/s"
+WORKLOAD = "KV8 decode: 8 seqs x 4096 rows, 128 heads, 576-dim latent (512+64), bf16 query"
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "sm_max_mhz": 2070.0}, \
+        "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during a region."""
+
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines: list[tuple[float, list[str]]] = []
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        threading.Thread(target=self._read, daemon=True).start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), [x.strip() for x in line.split(",")]))
+
+    def mark(self, begin: bool):
+        if begin:
+            self.t0 = time.time()
+        else:
+            self.t1 = time.time()
+
+    def stop(self):
+        if self.proc is not None:
+            time.sleep(0.1)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if not self.lines:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        inside = [f for t, f in self.lines if self.t0 and self.t1 and self.t0 <= t <= self.t1]
+        window = "timed"
+        if len(inside) < 3:
+            inside = [f for _, f in self.lines]
+            window = "warmup+timed"
+        sm = [float(f[1]) for f in inside if f[1].replace(".", "").isdigit()]
+        mx = [float(f[2]) for f in inside if f[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for f in inside for i in range(4) if len(f) > 5 + i and f[5 + i] == "Active"})
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(inside), "window": window}
+
+
+def make_inputs(torch, kvq):
+    from quantized_kv_cache_kv8_gb300 import synth
+    rows = synth.mla_rows(SEED, B * T)
+    cu = synth.cu_seqlens([T] * B)
+    dev = torch.device("cuda")
+    codes = torch.empty((B * T, D), dtype=torch.uint8, device=dev)
+    scales = torch.empty((B * T, 2), dtype=torch.float32, device=dev)
+    kvq.kv8_encode(torch.from_numpy(rows).to(dev), codes, scales)
+    new_rows = synth.mla_rows(SEED + 100, B)
+    q = synth.queries(SEED + 1, (B, H, D))
+    q_bits = synth.bf16_bits(q)
+    return dict(codes=codes, scales=scales, cu=torch.from_numpy(cu).to(dev), cu_np=cu,
+                dst=torch.from_numpy(cu[1:] - 1).to(dev),
+                x_new_host=torch.from_numpy(new_rows).pin_memory(),
+                q_host=torch.from_numpy(q_bits.view(np.int16)).view(torch.bfloat16).pin_memory())
+
+
+def run_ours(args, rank, world):
+    import torch
+    from quantized_kv_cache_kv8_gb300 import kvq
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    path = {"auto": kvq.PATH_AUTO, "simt": kvq.PATH_SIMT, "tensor": kvq.PATH_TENSOR}[args.path]
+    inp = make_inputs(torch, kvq)
+    stream = torch.cuda.current_stream()
+    dev = torch.device("cuda")
+    x_new = inp["x_new_host"].to(dev)
+    q = inp["q_host"].to(dev)
+    out = torch.empty((B, H, DV), dtype=torch.float32, device=dev)
+    out_host = torch.empty((B, H, DV), dtype=torch.float32).pin_memory()
+    ws = torch.empty(kvq.kv_attn_workspace_size(kvq.KVQ_KV8, B, H, B * T, path=path), dtype=torch.uint8, device=dev)
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+
+    def step(xn, qq):
+        kvq.kv8_encode(xn, inp["codes"], inp["scales"], dst_rows=inp["dst"])
+        kvq.kv_attn_decode(kvq.KVQ_KV8, qq, inp["codes"], inp["scales"], inp["cu"], out, ws, B * T, path=path)
+
+    for _ in range(max(args.warmup, 3)):
+        step(x_new, q)
+        flush.zero_()
+    torch.cuda.synchronize()
+    if kvq.read_device_error(ws) != 0:
+        raise RuntimeError("device error word set during warm-up")
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    sampler.mark(True)
+    for i in range(K):
+        e0, e1, e2 = ev[i]
+        e0.record(stream)
+        kvq.kv8_encode(x_new, inp["codes"], inp["scales"], dst_rows=inp["dst"])
+        e1.record(stream)
+        kvq.kv_attn_decode(kvq.KVQ_KV8, q, inp["codes"], inp["scales"], inp["cu"], out, ws, B * T, path=path)
+        e2.record(stream)
+        flush.zero_()
+    torch.cuda.synchronize()
+    sampler.mark(False)
+    step_ms = sum(e0.elapsed_time(e2) for e0, _, e2 in ev) / K
+    decode_ms = sum(e1.elapsed_time(e2) for _, e1, e2 in ev) / K
+
+    # end to end through the public API: pinned host inputs in, result out, every step
+    e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    for i in range(K):
+        a, b = e2e_ev[i]
+        a.record(stream)
+        x_new.copy_(inp["x_new_host"], non_blocking=True)
+        q.copy_(inp["q_host"], non_blocking=True)
+        step(x_new, q)
+        out_host.copy_(out, non_blocking=True)
+        b.record(stream)
+        flush.zero_()
+    torch.cuda.synchronize()
+    sampler.stop()
+    e2e_ms = sum(a.elapsed_time(b) for a, b in e2e_ev) / K
+    err = kvq.read_device_error(ws)
+    if err != 0:
+        raise RuntimeError(f"device error word {err} after the timed region")
+
+    t = torch.tensor([step_ms, decode_ms, e2e_ms], dtype=torch.float64, device=dev)
+    if dist:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        dist.barrier()
+    step_ms, decode_ms, e2e_ms = t.tolist()
+    if rank != 0:
+        return None
+
+    rows = B * T * world
+    peaks, src = load_peaks()
+    gbs = rows * ROW_BYTES / (step_ms * 1e-3) / 1e9
+    e2e_gbs = rows * ROW_BYTES / (e2e_ms * 1e-3) / 1e9
+    clocks = sampler.summary()
+    # the decode's tensor-core path is bound by the bf16 tensor pipe; the SIMT
+    # path by the fp32 FMA pipe (152 SMs x 128 lanes x 2 flop x max SM clock)
+    used_path = "simt" if path in (kvq.PATH_SIMT, kvq.PATH_AUTO) else "tensor"
+    flops = B * T * FLOPS_PER_ROW
+    achieved_tf = flops / (decode_ms * 1e-3) / 1e12
+    if used_path == "simt":
+        peak = 152 * 128 * 2 * peaks.get("sm_max_mhz", 2070.0) * 1e6 / 1e12
+        roof = {"bound": "alu", "achieved": round(achieved_tf, 3), "peak": round(peak, 2), "unit": "TFLOP/s",
+                "frac": round(achieved_tf / peak, 4), "traffic": None,
+                "peak_source": "derived: 152 SMs x 128 fp32 lanes x 2 x max SM clock (MEASURED_PEAKS sm_max_mhz)",
+                "kernel": "kv_attn_decode (split-T partial + merge)"}
+    else:
+        peak = peaks["bf16_tflops"]
+        roof = {"bound": "tensor", "achieved": round(achieved_tf, 2), "peak": peak, "unit": "TFLOP/s",
+                "frac": round(achieved_tf / peak, 4), "traffic": None, "peak_source": f"bf16_tflops ({src})",
+                "kernel": "kv_attn_decode"}
+    line = {
+        "metric": METRIC, "value": round(gbs, 3), "unit": "GB/s", "n_gpus": world, "steps": K,
+        "warmup": max(args.warmup, 3), "ms_per_step": round(step_ms, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "e4m3 codes, f32 accumulate",
+        "data": "synthetic (seeded N(0,1) x log-normal channel gains; bf16 queries)",
+        "config": {"workload": WORKLOAD, "batch": B, "seq_len": T, "heads": H, "row_bytes": ROW_BYTES,
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "l2": "256 MB buffer written between timed steps (outside the events)", "path": used_path},
+        "rows_per_s": round(rows / (step_ms * 1e-3), 1),
+        "hbm_roof_frac": round(gbs / peaks["hbm_gbs"], 5),
+        "hbm_peak_gbs": peaks["hbm_gbs"], "peak_source": src,
+        "decode_ms": round(decode_ms, 5),
+        "e2e": {"value": round(e2e_gbs, 3), "unit": "GB/s", "ms_per_step": round(e2e_ms, 5),
+                "h2d_bytes_per_step": int(B * D * 4 + B * H * D * 2), "d2h_bytes_per_step": int(B * H * DV * 4)},
+        "gpu_launches": 3 * K,
+        "roofline": roof,
+        "clocks": clocks,
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(seconds=args.cpu_seconds)
+    return line
+
+
+def cpu_baseline(seconds: float = 10.0, sample_seqs: int | None = None, heads: int = H):
+    """The oracle as it stands, single-threaded on the host, on a bounded sample
+    of the same workload: sequences of 4096 rows x `heads` of the 128 heads, as
+    many sequences as fit the time budget (at least one).  The rate is scaled
+    to the metric's unit: rows read once for all 128 heads."""
+    from oracle import oracle as orc
+    from quantized_kv_cache_kv8_gb300 import synth
+    orc.lib()
+    rows = synth.mla_rows(SEED, B * T)
+    q = synth.bf16_to_f32(synth.bf16_bits(synth.queries(SEED + 1, (B, H, D))))
+    cu = synth.cu_seqlens([T] * B)
+    t0 = time.perf_counter()
+    done = 0
+    n_max = sample_seqs or B
+    for b in range(n_max):
+        codes, scales = orc.kv8_encode(rows[cu[b]:cu[b + 1]])
+        xh = orc.kv8_decode(codes, scales)
+        orc.attn_dense(xh, q[b, :heads], 1.0 / math.sqrt(192.0), DV)
+        done += 1
+        if time.perf_counter() - t0 > seconds:
+            break
+    dt = time.perf_counter() - t0
+    gbs = done * T * ROW_BYTES * (heads / H) / dt / 1e9
+    return {"value": round(gbs, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{done} of {B} sequences x {T} rows x {heads} of {H} heads (encode + f64 attention), "
+                      f"{dt:.1f} s; rate scaled to all {H} heads"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    K = max(args.steps, 1)
+    W = max(args.warmup, 0)
+    times = []
+    for i in range(W + K):
+        t0 = time.perf_counter()
+        cpu_baseline(seconds=0.0, sample_seqs=1, heads=8)
+        dt = time.perf_counter() - t0
+        if i >= W:
+            times.append(dt)
+        if sum(times) > 120:
+            K = len(times)
+            break
+    step_s = sum(times) / len(times)
+    gbs = T * ROW_BYTES * (8 / H) / step_s / 1e9
+    return {"impl": "reference", "metric": METRIC, "value": round(gbs, 6), "unit": "GB/s", "n_gpus": 1, "steps": K,
+            "warmup": W, "ms_per_step": round(step_s * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64 (oracle)", "data": "synthetic",
+            "config": {"workload": WORKLOAD + " (each step: one sequence of the batch, 8 of 128 heads)", "batch": B,
+                       "seq_len": T, "heads": H},
+            "cpu_baseline": {"value": round(gbs, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": "per step: 1 of 8 sequences x 4096 rows x 8 of 128 heads; rate scaled "
+                                       "to all heads"},
+            "e2e": {"value": round(gbs, 6), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--path", choices=["auto", "simt", "tensor"], default="auto")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    line = run_reference(args, rank, world) if args.impl == "reference" else run_ours(args, rank, world)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,243 @@
+/*
+ * kvq.h -- C ABI of libkvq: quantized KV cache encoders and attention over an
+ * MLA latent cache (the latent row is both key and value), on one GB300 GPU.
+ *
+ * The pages that define the operations are cited by title:
+ *   [P1] "KV cache quantization: fp8 (KV8) + 4-bit TurboQuant (KV_TQ) on CPU,
+ *         CUDA, and Metal" (colibri pull request 399)
+ *   [P2] "CPU: KV cache quantization -- KV8 (fp8 e4m3) + KV_TQ (rotated-int4 /
+ *         PolarQuant)" (colibri pull request 553)
+ *   [P3] "KV cache: FP16 sliding window + attention sinks, and an optional
+ *         2-bit K / 4-bit V cache scheme (--kv q2k)" (Strata pull request 2318)
+ *
+ * Conventions for every call:
+ *   - Ownership: the caller allocates and owns all memory.  The library
+ *     allocates nothing on the device and frees nothing; scratch space is the
+ *     caller's `workspace`, sized by the matching *_workspace_size call.
+ *   - Pointers are device pointers (any memory the GPU can address), except the
+ *     layout structs, which are read on the host during the call.
+ *   - Execution is asynchronous on `stream` (a cudaStream_t; NULL is the legacy
+ *     default stream).  Nothing is synchronized unless stated.
+ *   - Errors: arguments are validated on the host before any launch and
+ *     reported as a kvq_status; nothing is thrown across the ABI.  A launch
+ *     failure returns KVQ_ERR_CUDA.  Conditions only the device can see (a
+ *     ragged batch larger than the bound it was sized for, a non-monotone
+ *     cu_seqlens) set an error word in the workspace, read with
+ *     kvq_read_device_error; the kernels never trap.
+ *   - The library keeps no global state; calls on different streams with
+ *     different workspaces are independent.
+ *   - Encoders are bit-exact by construction: IEEE f32 arithmetic in a fixed
+ *     order, no fast-math, no fused multiply-add except where the definition
+ *     names one.
+ */
+#ifndef KVQ_H
+#define KVQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum kvq_status {
+    KVQ_OK = 0,
+    KVQ_ERR_ARG = 1,          /* null pointer, negative size, bad enum */
+    KVQ_ERR_SHAPE = 2,        /* a TQ4 block width that is not a power of two >= 2 */
+    KVQ_ERR_WORKSPACE = 3,    /* workspace missing or smaller than required */
+    KVQ_ERR_CUDA = 4,         /* a CUDA launch or runtime call failed */
+    KVQ_ERR_UNSUPPORTED = 5,  /* valid arguments this build has no kernel for */
+    KVQ_ERR_DEVICE = 6        /* the device error word was set (see kvq_read_device_error) */
+} kvq_status;
+
+typedef enum kvq_format { KVQ_KV8 = 1, KVQ_TQ4 = 2 } kvq_format;
+typedef enum kvq_dtype { KVQ_F32 = 0, KVQ_BF16 = 1 } kvq_dtype;
+
+/* Which attention kernel family runs.  AUTO picks the fastest available;
+ * SIMT is the fp32 CUDA-core path (outputs within 1e-5 of exact attention);
+ * TENSOR is the tensor-core path (16-bit operands, within 2e-3). */
+typedef enum kvq_path { KVQ_PATH_AUTO = 0, KVQ_PATH_SIMT = 1, KVQ_PATH_TENSOR = 2 } kvq_path;
+
+/* Row layout of the MLA latent cache.  A row of D = block_dim[0] (+
+ * block_dim[1]) f32 values is split into scale blocks; each block gets one f32
+ * scale ([P1] Summary: "fp8 e4m3 + per-row scale"; two blocks, latent 512 and
+ * rope 64, give the 584-byte KV8 row and the 296-byte TQ4 row behind the
+ * "~3.9x" and "~7.8x" of [P1] Summary).  v_dim leading dims form the value
+ * (must lie in block 0).  seed selects the TQ4 rotation signs. */
+typedef struct kvq_mla_layout {
+    int32_t n_blocks;       /* 1 or 2 */
+    int32_t block_dim[2];   /* widths of the scale blocks; block_dim[1] ignored if n_blocks == 1 */
+    int32_t v_dim;          /* value width, <= block_dim[0] */
+    uint64_t seed;          /* TQ4 sign seed (ignored by KV8) */
+} kvq_mla_layout;
+
+/* Human-readable name of a status. */
+const char* kvq_status_string(kvq_status status);
+
+/* Library version as "major.minor.patch". */
+const char* kvq_version(void);
+
+/* Copies the f32 codebook the kernels use: which = 16 gives the TQ4 levels
+ * (16) and decision thresholds (15); which = 4 gives the K2 levels (4) and
+ * thresholds (3).  Host memory, host call, no GPU needed.  These are the
+ * N(0,1) Lloyd-Max quantizers of [P1] "Why rotated-int4 for the 4-bit tier"
+ * and of [P3] "Why per-channel K and per-token V". */
+kvq_status kvq_codebook(int32_t which, float* levels, float* thresholds);
+
+/* ------------------------------------------------------------------------ */
+/* Producers                                                                */
+/* ------------------------------------------------------------------------ */
+
+/* KV8 encode ([P1] Commits, item 1; [P2] "What's in it").  For every row and
+ * scale block: s = amax/448 (f32 division), code_i = e4m3(x_i / s) with one
+ * round-to-nearest-even, saturating at +-448.  A block whose s is 0 stores
+ * s = 0 and codes 0x00.
+ *   x         [n_rows][D] f32, row-major
+ *   dst_rows  NULL, or device int64 [n_rows]: input row i is stored as pool
+ *             row dst_rows[i] (the decode-step append: one new row per
+ *             sequence, each at the end of its own range)
+ *   codes     pool [*][D] bytes (e4m3 bit patterns), rows written
+ *   scales    pool [*][n_blocks] f32, rows written
+ * Any block widths with D <= 4096.  n_rows == 0 is a no-op. */
+kvq_status kv8_encode(const float* x, int64_t n_rows, const kvq_mla_layout* layout,
+                      const int64_t* dst_rows, uint8_t* codes, float* scales, void* stream);
+
+/* TQ4 (rotated-int4) encode ([P1] "Why rotated-int4 for the 4-bit tier";
+ * [P2] "What's in it").  Per block of n dims (a power of two, 2..1024):
+ *   y = (1/sqrt n) H_n (sigma . x)   (f32 radix-2 FWHT, stages h = 1,2,4,..)
+ *   s = ||x|| / sqrt(n)              (sum of squares in a fixed order: 32
+ *                                     interleaved fma partials, then halving)
+ *   code_i = number of codebook thresholds strictly below y_i / s
+ *   byte j of the block = code_2j | code_(2j+1) << 4
+ * sigma comes from layout->seed: splitmix64 words from state = seed, each
+ * block taking ceil(n/64) words in order, sign i = -1 when bit i%64 of word
+ * i/64 is set.  A block with s == 0 stores s = 0 and codes 0.
+ *   x         [n_rows][D] f32
+ *   dst_rows  NULL, or device int64 [n_rows] destination pool rows (as kv8_encode)
+ *   packed    pool [*][D/2] bytes, rows written (block 0 first)
+ *   scales    pool [*][n_blocks] f32, rows written
+ * Returns KVQ_ERR_SHAPE for a width that is not a power of two >= 2 ([P1]
+ * rebase comment and [P2] review-pass item 1: such rows would all become
+ * inert, so the codec refuses). */
+kvq_status tq4_encode(const float* x, int64_t n_rows, const kvq_mla_layout* layout,
+                      const int64_t* dst_rows, uint8_t* packed, float* scales, void* stream);
+
+/* The TQ4 rotation applied to whole vectors, f32 ([P1] "Ready for review"
+ * comment, finding 2: rotate the query once per head, unrotate the
+ * accumulated context once).  inverse = 0: out = (1/sqrt n) H_n (sigma . in)
+ * per block; inverse = 1: out = sigma . ((1/sqrt n) H_n in).
+ *   in   [n_vecs][D] (f32 or bf16 per in_dtype);  out [n_vecs][D] f32. */
+kvq_status tq4_rotate(const void* in, kvq_dtype in_dtype, int64_t n_vecs, const kvq_mla_layout* layout,
+                      int32_t inverse, float* out, void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* Consumers                                                                */
+/* ------------------------------------------------------------------------ */
+
+/* Bytes of workspace kv_attn_decode needs for at most max_total_rows cached
+ * rows across `batch` sequences.  Returns 0 for invalid arguments. */
+size_t kv_attn_workspace_size(kvq_format fmt, const kvq_mla_layout* layout, int32_t batch,
+                              int32_t n_heads, int64_t max_total_rows, kvq_path path);
+
+/* Ragged decode attention over quantized rows, never reconstructing the cache
+ * ([P2] "What's in it": KV8 dequantizes inline with the row scale factored
+ * out of the score and context sums; TQ4 rotates the query once per head,
+ * dots it with the codebook levels and unrotates the context once).  For
+ * sequence b with rows [cu_seqlens[b], cu_seqlens[b+1]) of the packed pool and
+ * head h:
+ *   z_t = sm_scale * (q_bh . x_hat_t)   over all D dims
+ *   out[b][h][:] = sum_t softmax(z)_t x_hat_t[0:v_dim]
+ * where x_hat is the row's reconstruction (never materialized).  Long
+ * sequences are split into chunks whose partial softmax states are merged
+ * (split-T).  An empty sequence yields zeros.
+ *   q           [batch][n_heads][D] in q_dtype
+ *   codes       packed row pool: KV8 [rows][D] bytes, TQ4 [rows][D/2] bytes
+ *   scales      [rows][n_blocks] f32
+ *   cu_seqlens  [batch+1] int64, device, non-decreasing, cu[0] = 0
+ *   max_total_rows  host-side bound on cu_seqlens[batch] (sizes the launch)
+ *   out         [batch][n_heads][v_dim] f32, written
+ * Supported attention layout: D = 576 as blocks (512, 64) or (576) for KV8,
+ * (512, 64) for TQ4; v_dim = 512.  Others return KVQ_ERR_UNSUPPORTED. */
+kvq_status kv_attn_decode(kvq_format fmt, const kvq_mla_layout* layout,
+                          const void* q, kvq_dtype q_dtype, int32_t batch, int32_t n_heads,
+                          const uint8_t* codes, const float* scales, const int64_t* cu_seqlens,
+                          int64_t max_total_rows, float sm_scale, float* out,
+                          void* workspace, size_t workspace_bytes, kvq_path path, void* stream);
+
+/* Bytes of workspace kv_attn_prefill needs. */
+size_t kv_attn_prefill_workspace_size(kvq_format fmt, const kvq_mla_layout* layout, int32_t n_heads,
+                                      int64_t n_past, int64_t n_new, kvq_path path);
+
+/* Chunked causal prefill of one sequence: first encodes the n_new new rows
+ * into pool rows [n_past, n_past + n_new) (kv8_encode / tq4_encode), then
+ * attends each new token j over pool rows [0, n_past + j] in quantized form,
+ * its own row included (the producer runs before the consumer, [P2] review
+ * thread on the producer loop).
+ *   x_new   [n_new][D] f32
+ *   q       [n_new][n_heads][D] in q_dtype
+ *   codes, scales  the pool, capacity >= n_past + n_new rows; rows
+ *           [0, n_past) are read, rows [n_past, n_past + n_new) written
+ *   out     [n_new][n_heads][v_dim] f32, written */
+kvq_status kv_attn_prefill(kvq_format fmt, const kvq_mla_layout* layout,
+                           const float* x_new, const void* q, kvq_dtype q_dtype,
+                           int64_t n_past, int64_t n_new, int32_t n_heads,
+                           uint8_t* codes, float* scales, float sm_scale, float* out,
+                           void* workspace, size_t workspace_bytes, kvq_path path, void* stream);
+
+/* Reads the device error word of a decode/prefill workspace (synchronizes
+ * `stream`).  Returns 0 when clear, else a kvq_status value; clears it when
+ * `clear` is non-zero. */
+int32_t kvq_read_device_error(void* workspace, int32_t clear, void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* K2/V4 GQA cache with an exact FP16 window ([P3])                          */
+/* ------------------------------------------------------------------------ */
+
+/* [P3] Summary: K at 2 bits with per-channel scales (one fp16 scale per dim
+ * per 32-cell group, a 4-level Lloyd-Max codebook, stored scale = k_gain x
+ * the rule's scale with the codes chosen against the un-gained scale), V at 4
+ * bits per token (q4_0: 32-dim blocks of fp16 d + 16 bytes, value = (code-8)
+ * d, element j < 16 the low nibble of byte j, j >= 16 the high nibble of byte
+ * j-16), and an FP16 overlay holding exact copies of the first n_sink cells
+ * and the last n_window cells (n_slack spare slots, 16 on the page). */
+typedef struct kvq_k2v4_layout {
+    int32_t n_kv_heads;
+    int32_t head_dim;       /* multiple of 32, <= 512 */
+    int32_t group;          /* must be 32 */
+    float k_gain;           /* 1.10 on the page */
+    int32_t n_sink, n_window, n_slack;
+} kvq_k2v4_layout;
+
+/* Encodes whole sequences of n_cells cells (a multiple of 32) and writes the
+ * overlay for the sink and window cells.
+ *   k, v      [batch][n_kv_heads][n_cells][head_dim] f32 (already rotated; the
+ *             Hadamard rotation of the page's cache happens before this call)
+ *   k_codes   [batch][n_kv_heads][capacity][head_dim/4] bytes: dim d is bits
+ *             2(d%4) of byte d/4, code c reads level c of the K2 codebook
+ *   k_scales  [batch][n_kv_heads][capacity/32][head_dim] fp16 bits
+ *   v_blocks  [batch][n_kv_heads][capacity][head_dim/32][18] bytes (q4_0)
+ *   k_win, v_win [batch][n_kv_heads][n_sink+n_window+n_slack][head_dim] fp16
+ * Overlay slot of cell c: c < n_sink -> c; c >= n_cells - n_window ->
+ * n_sink + c mod (n_window + n_slack). */
+kvq_status k2v4_encode(const kvq_k2v4_layout* layout, const float* k, const float* v,
+                       int32_t batch, int64_t n_cells, int64_t capacity,
+                       uint8_t* k_codes, uint16_t* k_scales, uint8_t* v_blocks,
+                       uint16_t* k_win, uint16_t* v_win, void* stream);
+
+size_t kv_attn_decode_k2v4_workspace_size(const kvq_k2v4_layout* layout, int32_t batch,
+                                          int32_t n_q_heads, int64_t n_cells, kvq_path path);
+
+/* GQA decode over the K2/V4 cache: q head h reads kv head h / (n_q_heads /
+ * n_kv_heads); cells in the overlay read fp16 exactly, the rest the bulk.
+ *   q    [batch][n_q_heads][head_dim] f32;  out [batch][n_q_heads][head_dim] f32 */
+kvq_status kv_attn_decode_k2v4(const kvq_k2v4_layout* layout, const float* q, int32_t batch,
+                               int32_t n_q_heads, int64_t n_cells, int64_t capacity,
+                               const uint8_t* k_codes, const uint16_t* k_scales, const uint8_t* v_blocks,
+                               const uint16_t* k_win, const uint16_t* v_win, float sm_scale, float* out,
+                               void* workspace, size_t workspace_bytes, kvq_path path, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVQ_H */

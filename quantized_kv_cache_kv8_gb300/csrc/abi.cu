@@ -1,0 +1,277 @@
+// abi.cu -- the extern "C" entry points declared in include/kvq.h.
+//
+// Every call validates its arguments on the host and only then launches; a
+// failed check returns a status and launches nothing.  No call allocates or
+// frees device memory.
+#include "kvq_internal.cuh"
+
+#include <algorithm>
+#include <math.h>
+
+using namespace kvq;
+
+namespace {
+
+constexpr int kMaxD = 4096;
+
+bool is_pow2_ge2(int n) { return n >= 2 && (n & (n - 1)) == 0; }
+
+kvq_status check_layout(const kvq_mla_layout* L) {
+    if (!L) return KVQ_ERR_ARG;
+    if (L->n_blocks < 1 || L->n_blocks > 2) return KVQ_ERR_ARG;
+    for (int b = 0; b < L->n_blocks; ++b)
+        if (L->block_dim[b] <= 0) return KVQ_ERR_ARG;
+    const int D = L->block_dim[0] + (L->n_blocks > 1 ? L->block_dim[1] : 0);
+    if (D > kMaxD) return KVQ_ERR_UNSUPPORTED;
+    return KVQ_OK;
+}
+
+int row_dim(const kvq_mla_layout* L) { return L->block_dim[0] + (L->n_blocks > 1 ? L->block_dim[1] : 0); }
+
+kvq_status check_tq4_layout(const kvq_mla_layout* L) {
+    kvq_status s = check_layout(L);
+    if (s != KVQ_OK) return s;
+    for (int b = 0; b < L->n_blocks; ++b)
+        if (!is_pow2_ge2(L->block_dim[b])) return KVQ_ERR_SHAPE;
+    for (int b = 0; b < L->n_blocks; ++b)
+        if (L->block_dim[b] > 1024) return KVQ_ERR_UNSUPPORTED;
+    if (row_dim(L) > 1024) return KVQ_ERR_UNSUPPORTED;   // 16 sign words
+    return KVQ_OK;
+}
+
+// The attention kernels are written for the 576-dim MLA latent row.
+kvq_status check_attn_layout(kvq_format fmt, const kvq_mla_layout* L) {
+    kvq_status s = fmt == KVQ_TQ4 ? check_tq4_layout(L) : (fmt == KVQ_KV8 ? check_layout(L) : KVQ_ERR_ARG);
+    if (s != KVQ_OK) return s;
+    if (L->v_dim != 512) return KVQ_ERR_UNSUPPORTED;
+    const bool two = L->n_blocks == 2 && L->block_dim[0] == 512 && L->block_dim[1] == 64;
+    const bool one = L->n_blocks == 1 && L->block_dim[0] == 576;
+    if (fmt == KVQ_TQ4 ? !two : !(two || one)) return KVQ_ERR_UNSUPPORTED;
+    return KVQ_OK;
+}
+
+kvq_status cuda_status(cudaError_t e) { return e == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA; }
+
+kvq_status check_path(kvq_path path) {
+    if (path != KVQ_PATH_AUTO && path != KVQ_PATH_SIMT && path != KVQ_PATH_TENSOR) return KVQ_ERR_ARG;
+    if (path == KVQ_PATH_TENSOR) return KVQ_ERR_UNSUPPORTED;
+    return KVQ_OK;
+}
+
+kvq_status check_k2v4(const kvq_k2v4_layout* L) {
+    if (!L) return KVQ_ERR_ARG;
+    if (L->n_kv_heads <= 0 || L->head_dim <= 0 || L->n_sink < 0 || L->n_window < 0 || L->n_slack < 0)
+        return KVQ_ERR_ARG;
+    if (L->group != 32) return KVQ_ERR_UNSUPPORTED;
+    if (L->head_dim % 32 != 0 || L->head_dim > 512) return KVQ_ERR_UNSUPPORTED;
+    if (!(L->k_gain > 0.0f) || !isfinite(L->k_gain)) return KVQ_ERR_ARG;
+    return KVQ_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* kvq_status_string(kvq_status s) {
+    switch (s) {
+        case KVQ_OK: return "ok";
+        case KVQ_ERR_ARG: return "invalid argument";
+        case KVQ_ERR_SHAPE: return "TQ4 block width is not a power of two >= 2 (rows would all be inert)";
+        case KVQ_ERR_WORKSPACE: return "workspace missing or too small";
+        case KVQ_ERR_CUDA: return "CUDA launch or runtime error";
+        case KVQ_ERR_UNSUPPORTED: return "arguments valid but not supported by this build";
+        case KVQ_ERR_DEVICE: return "device error word set";
+    }
+    return "unknown status";
+}
+
+const char* kvq_version(void) { return "0.1.0"; }
+
+kvq_status kvq_codebook(int32_t which, float* levels, float* thresholds) {
+    if (!levels || !thresholds) return KVQ_ERR_ARG;
+    if (which == 16) {
+        const Codebook16 c = tq4_codebook();
+        for (int k = 0; k < 16; ++k) levels[k] = c.lv[k];
+        for (int k = 0; k < 15; ++k) thresholds[k] = c.th[k];
+        return KVQ_OK;
+    }
+    if (which == 4) {
+        const Codebook4 c = k2_codebook();
+        for (int k = 0; k < 4; ++k) levels[k] = c.lv[k];
+        for (int k = 0; k < 3; ++k) thresholds[k] = c.th[k];
+        return KVQ_OK;
+    }
+    return KVQ_ERR_ARG;
+}
+
+kvq_status kv8_encode(const float* x, int64_t n_rows, const kvq_mla_layout* layout, const int64_t* dst_rows,
+                      uint8_t* codes, float* scales, void* stream) {
+    kvq_status s = check_layout(layout);
+    if (s != KVQ_OK) return s;
+    if (n_rows < 0) return KVQ_ERR_ARG;
+    if (n_rows == 0) return KVQ_OK;
+    if (!x || !codes || !scales) return KVQ_ERR_ARG;
+    return cuda_status(launch_kv8_encode(x, n_rows, *layout, dst_rows, codes, scales, (cudaStream_t)stream));
+}
+
+kvq_status tq4_encode(const float* x, int64_t n_rows, const kvq_mla_layout* layout, const int64_t* dst_rows,
+                      uint8_t* packed, float* scales, void* stream) {
+    kvq_status s = check_tq4_layout(layout);
+    if (s != KVQ_OK) return s;
+    if (n_rows < 0) return KVQ_ERR_ARG;
+    if (n_rows == 0) return KVQ_OK;
+    if (!x || !packed || !scales) return KVQ_ERR_ARG;
+    return cuda_status(launch_tq4_encode(x, n_rows, *layout, dst_rows, packed, scales, (cudaStream_t)stream));
+}
+
+kvq_status tq4_rotate(const void* in, kvq_dtype in_dtype, int64_t n_vecs, const kvq_mla_layout* layout,
+                      int32_t inverse, float* out, void* stream) {
+    kvq_status s = check_tq4_layout(layout);
+    if (s != KVQ_OK) return s;
+    if (n_vecs < 0 || (in_dtype != KVQ_F32 && in_dtype != KVQ_BF16)) return KVQ_ERR_ARG;
+    if (n_vecs == 0) return KVQ_OK;
+    if (!in || !out) return KVQ_ERR_ARG;
+    return cuda_status(launch_tq4_rotate(in, in_dtype, n_vecs, *layout, inverse, out, (cudaStream_t)stream));
+}
+
+size_t kv_attn_workspace_size(kvq_format fmt, const kvq_mla_layout* layout, int32_t batch, int32_t n_heads,
+                              int64_t max_total_rows, kvq_path path) {
+    if (check_attn_layout(fmt, layout) != KVQ_OK || check_path(path) != KVQ_OK) return 0;
+    if (batch < 0 || n_heads < 0 || max_total_rows < 0) return 0;
+    const AttnPlan pl = plan_decode_simt(batch, n_heads, max_total_rows);
+    return kWsHeader + partial_bytes(pl.max_items, n_heads, layout->v_dim);
+}
+
+kvq_status kv_attn_decode(kvq_format fmt, const kvq_mla_layout* layout, const void* q, kvq_dtype q_dtype,
+                          int32_t batch, int32_t n_heads, const uint8_t* codes, const float* scales,
+                          const int64_t* cu_seqlens, int64_t max_total_rows, float sm_scale, float* out,
+                          void* workspace, size_t workspace_bytes, kvq_path path, void* stream) {
+    kvq_status s = check_attn_layout(fmt, layout);
+    if (s != KVQ_OK) return s;
+    if ((s = check_path(path)) != KVQ_OK) return s;
+    if (batch < 0 || n_heads < 0 || max_total_rows < 0 || (q_dtype != KVQ_F32 && q_dtype != KVQ_BF16))
+        return KVQ_ERR_ARG;
+    if (batch > 65535 || n_heads > 65535) return KVQ_ERR_UNSUPPORTED;
+    if (batch == 0 || n_heads == 0) return KVQ_OK;
+    if (!q || !cu_seqlens || !out) return KVQ_ERR_ARG;
+    if (max_total_rows > 0 && (!codes || !scales)) return KVQ_ERR_ARG;
+    if (!isfinite(sm_scale)) return KVQ_ERR_ARG;
+    const size_t need = kv_attn_workspace_size(fmt, layout, batch, n_heads, max_total_rows, path);
+    if (!workspace || workspace_bytes < need) return KVQ_ERR_WORKSPACE;
+    cudaStream_t st = (cudaStream_t)stream;
+    cudaError_t e = cudaMemsetAsync(workspace, 0, sizeof(int32_t), st);
+    if (e != cudaSuccess) return KVQ_ERR_CUDA;
+    const AttnPlan pl = plan_decode_simt(batch, n_heads, max_total_rows);
+    return cuda_status(launch_attn_simt(fmt, *layout, q, q_dtype, batch, n_heads, codes, scales, cu_seqlens, -1, pl,
+                                        sm_scale, out, workspace, st));
+}
+
+static AttnPlan plan_prefill(int64_t n_past, int64_t n_new) {
+    AttnPlan pl{};
+    pl.chunk = std::max<int64_t>(1, n_past + n_new);
+    pl.max_items = n_new;
+    pl.heads_per_cta = 16;
+    return pl;
+}
+
+size_t kv_attn_prefill_workspace_size(kvq_format fmt, const kvq_mla_layout* layout, int32_t n_heads, int64_t n_past,
+                                      int64_t n_new, kvq_path path) {
+    if (check_attn_layout(fmt, layout) != KVQ_OK || check_path(path) != KVQ_OK) return 0;
+    if (n_heads < 0 || n_past < 0 || n_new < 0) return 0;
+    const AttnPlan pl = plan_prefill(n_past, n_new);
+    return kWsHeader + partial_bytes(pl.max_items, n_heads, layout->v_dim);
+}
+
+kvq_status kv_attn_prefill(kvq_format fmt, const kvq_mla_layout* layout, const float* x_new, const void* q,
+                           kvq_dtype q_dtype, int64_t n_past, int64_t n_new, int32_t n_heads, uint8_t* codes,
+                           float* scales, float sm_scale, float* out, void* workspace, size_t workspace_bytes,
+                           kvq_path path, void* stream) {
+    kvq_status s = check_attn_layout(fmt, layout);
+    if (s != KVQ_OK) return s;
+    if ((s = check_path(path)) != KVQ_OK) return s;
+    if (n_past < 0 || n_new < 0 || n_heads < 0 || (q_dtype != KVQ_F32 && q_dtype != KVQ_BF16)) return KVQ_ERR_ARG;
+    if (n_new > 65535 || n_heads > 65535) return KVQ_ERR_UNSUPPORTED;
+    if (n_new == 0 || n_heads == 0) return KVQ_OK;
+    if (!x_new || !q || !codes || !scales || !out) return KVQ_ERR_ARG;
+    if (!isfinite(sm_scale)) return KVQ_ERR_ARG;
+    const size_t need = kv_attn_prefill_workspace_size(fmt, layout, n_heads, n_past, n_new, path);
+    if (!workspace || workspace_bytes < need) return KVQ_ERR_WORKSPACE;
+    cudaStream_t st = (cudaStream_t)stream;
+    const int D = row_dim(layout);
+    const int64_t row_bytes = fmt == KVQ_KV8 ? D : D / 2;
+    cudaError_t e;
+    if (fmt == KVQ_KV8)
+        e = launch_kv8_encode(x_new, n_new, *layout, nullptr, codes + n_past * row_bytes,
+                              scales + n_past * layout->n_blocks, st);
+    else
+        e = launch_tq4_encode(x_new, n_new, *layout, nullptr, codes + n_past * row_bytes,
+                              scales + n_past * layout->n_blocks, st);
+    if (e != cudaSuccess) return KVQ_ERR_CUDA;
+    if ((e = cudaMemsetAsync(workspace, 0, sizeof(int32_t), st)) != cudaSuccess) return KVQ_ERR_CUDA;
+    const AttnPlan pl = plan_prefill(n_past, n_new);
+    return cuda_status(launch_attn_simt(fmt, *layout, q, q_dtype, (int32_t)n_new, n_heads, codes, scales, nullptr,
+                                        n_past, pl, sm_scale, out, workspace, st));
+}
+
+int32_t kvq_read_device_error(void* workspace, int32_t clear, void* stream) {
+    if (!workspace) return KVQ_ERR_ARG;
+    cudaStream_t st = (cudaStream_t)stream;
+    int32_t v = 0;
+    if (cudaMemcpyAsync(&v, workspace, sizeof v, cudaMemcpyDeviceToHost, st) != cudaSuccess) return KVQ_ERR_CUDA;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return KVQ_ERR_CUDA;
+    if (clear && v != 0) {
+        if (cudaMemsetAsync(workspace, 0, sizeof(int32_t), st) != cudaSuccess) return KVQ_ERR_CUDA;
+    }
+    return v;
+}
+
+kvq_status k2v4_encode(const kvq_k2v4_layout* layout, const float* k, const float* v, int32_t batch,
+                       int64_t n_cells, int64_t capacity, uint8_t* k_codes, uint16_t* k_scales, uint8_t* v_blocks,
+                       uint16_t* k_win, uint16_t* v_win, void* stream) {
+    kvq_status s = check_k2v4(layout);
+    if (s != KVQ_OK) return s;
+    if (batch < 0 || n_cells < 0 || capacity < n_cells) return KVQ_ERR_ARG;
+    if (n_cells % 32 != 0 || capacity % 32 != 0) return KVQ_ERR_UNSUPPORTED;
+    if (batch > 65535 || layout->n_kv_heads > 65535 || n_cells / 32 > 0x7fffffff) return KVQ_ERR_UNSUPPORTED;
+    if (batch == 0 || n_cells == 0) return KVQ_OK;
+    if (!k || !v || !k_codes || !k_scales || !v_blocks) return KVQ_ERR_ARG;
+    if ((layout->n_sink + layout->n_window) > 0 && (!k_win || !v_win)) return KVQ_ERR_ARG;
+    return cuda_status(launch_k2v4_encode(*layout, k, v, batch, n_cells, capacity, k_codes, k_scales, v_blocks, k_win,
+                                          v_win, (cudaStream_t)stream));
+}
+
+size_t kv_attn_decode_k2v4_workspace_size(const kvq_k2v4_layout* layout, int32_t batch, int32_t n_q_heads,
+                                          int64_t n_cells, kvq_path path) {
+    if (check_k2v4(layout) != KVQ_OK || check_path(path) != KVQ_OK) return 0;
+    if (batch < 0 || n_q_heads < 0 || n_cells < 0) return 0;
+    const K2V4Plan pl = plan_k2v4(*layout, batch, n_q_heads, n_cells);
+    return kWsHeader + k2v4_partial_bytes(*layout, batch, n_q_heads, pl);
+}
+
+kvq_status kv_attn_decode_k2v4(const kvq_k2v4_layout* layout, const float* q, int32_t batch, int32_t n_q_heads,
+                               int64_t n_cells, int64_t capacity, const uint8_t* k_codes, const uint16_t* k_scales,
+                               const uint8_t* v_blocks, const uint16_t* k_win, const uint16_t* v_win, float sm_scale,
+                               float* out, void* workspace, size_t workspace_bytes, kvq_path path, void* stream) {
+    kvq_status s = check_k2v4(layout);
+    if (s != KVQ_OK) return s;
+    if ((s = check_path(path)) != KVQ_OK) return s;
+    if (batch < 0 || n_q_heads < 0 || n_cells < 0 || capacity < n_cells) return KVQ_ERR_ARG;
+    if (n_q_heads % layout->n_kv_heads != 0) return KVQ_ERR_ARG;
+    if (n_q_heads / layout->n_kv_heads > 8) return KVQ_ERR_UNSUPPORTED;
+    if (n_cells % 32 != 0 || capacity % 32 != 0) return KVQ_ERR_UNSUPPORTED;
+    const int D = layout->head_dim;
+    if (D != 128 && D != 256 && D != 512) return KVQ_ERR_UNSUPPORTED;
+    if (batch > 65535) return KVQ_ERR_UNSUPPORTED;
+    if (batch == 0 || n_q_heads == 0) return KVQ_OK;
+    if (!q || !out || (n_cells > 0 && (!k_codes || !k_scales || !v_blocks))) return KVQ_ERR_ARG;
+    if ((layout->n_sink + layout->n_window) > 0 && (!k_win || !v_win)) return KVQ_ERR_ARG;
+    if (!isfinite(sm_scale)) return KVQ_ERR_ARG;
+    const size_t need = kv_attn_decode_k2v4_workspace_size(layout, batch, n_q_heads, n_cells, path);
+    if (!workspace || workspace_bytes < need) return KVQ_ERR_WORKSPACE;
+    const K2V4Plan pl = plan_k2v4(*layout, batch, n_q_heads, n_cells);
+    return cuda_status(launch_k2v4_decode(*layout, q, batch, n_q_heads, n_cells, capacity, k_codes, k_scales,
+                                          v_blocks, k_win, v_win, sm_scale, out, workspace, pl,
+                                          (cudaStream_t)stream));
+}
+
+}  // extern "C"

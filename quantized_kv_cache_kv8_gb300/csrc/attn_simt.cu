@@ -1,0 +1,474 @@
+// attn_simt.cu -- fp32 CUDA-core attention over quantized MLA rows (the
+// parity path: outputs within 1e-5 of exact attention).
+//
+// Work decomposition (split-T, [P1] Commits item 2: split-T kernels): the rows
+// of every sequence are cut into chunks of `chunk` rows; one CTA handles one
+// (chunk, group of 16 heads) and leaves a partial softmax state (running max
+// m, running sum l, unnormalized context o[512]) per head in the workspace.  A
+// second kernel merges the chunks of each (sequence, head) by log-sum-exp and,
+// for TQ4, unrotates the context once.  Ragged sequences are found on the
+// device from cu_seqlens, so nothing is synchronized with the host.
+//
+// Inside a CTA the consumer never reconstructs a row ([P2] "What's in it"):
+// a tile of 16 rows is decoded to the codes' values only (e4m3 value or TQ4
+// codebook level) and the per-row scales stay separate.  The score of head h
+// and row t is sm_scale * (s_L * (q_L . c_L) + s_R * (q_R . c_R)) and the
+// context weight of row t is p_t * s_L: the scale is factored out of both sums.
+// For TQ4 the query is rotated in shared memory first ([P1] "Ready for
+// review" comment, finding 2).
+#include "kvq_internal.cuh"
+
+#include <algorithm>
+#include <math.h>
+
+namespace kvq {
+namespace {
+
+constexpr int kD = 576, kDL = 512, kDR = 64, kDV = 512;
+constexpr int kHG = 16;   // heads per CTA
+constexpr int kTR = 16;   // rows per tile
+constexpr int kNT = 256;  // threads per CTA
+constexpr int kXS = 580;  // shared-memory row stride in floats (bank spread)
+constexpr int kSmSMs = 152;
+
+struct AttnParams {
+    int32_t n_blocks;
+    int32_t n_seq, n_heads;
+    const void* q;
+    const uint8_t* codes;
+    const float* scales;
+    const int64_t* cu;      // decode: ragged row offsets
+    int64_t prefill_past;   // prefill: >= 0; token b attends rows [0, past + b]
+    int64_t chunk, max_items;
+    float sm_scale;
+    float* ws_o;            // [max_items][n_heads][kDV]
+    float* ws_ml;           // [max_items][n_heads][2]
+    int32_t* err;
+    SignWords signs;
+    float kn[2];
+    float lv[16];
+};
+
+constexpr size_t kSmemFloats = (size_t)kHG * kXS + (size_t)kTR * kXS + kTR * 2 + kTR * kHG + kHG + 16 + 4;
+
+__device__ __forceinline__ void set_err(int32_t* err, int32_t code) { atomicCAS(err, 0, code); }
+
+// Number of chunks of sequence b (0 for an empty or malformed range).
+__device__ __forceinline__ int64_t n_chunks_of(const int64_t* cu, int b, int64_t chunk, int32_t* err) {
+    const int64_t len = cu[b + 1] - cu[b];
+    if (len < 0) {
+        set_err(err, KVQ_ERR_ARG);
+        return 0;
+    }
+    return (len + chunk - 1) / chunk;
+}
+
+// Warp-cooperative search for the sequence owning work item `item`.
+// Returns b (or -1) and the chunk index within b.
+__device__ int find_item(const int64_t* cu, int n_seq, int64_t chunk, int64_t item, int lane, int64_t* ch_out,
+                         int32_t* err) {
+    int64_t base = 0;
+    for (int b0 = 0; b0 < n_seq; b0 += 32) {
+        const int b = b0 + lane;
+        const int64_t n = b < n_seq ? n_chunks_of(cu, b, chunk, err) : 0;
+        int64_t incl = n;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int64_t t = __shfl_up_sync(kFull, incl, o);
+            if (lane >= o) incl += t;
+        }
+        const int64_t total = __shfl_sync(kFull, incl, 31);
+        if (item < base + total) {
+            const int64_t excl = incl - n;
+            const bool mine = b < n_seq && item >= base + excl && item < base + incl;
+            const unsigned mask = __ballot_sync(kFull, mine);
+            const int src = __ffs(mask) - 1;
+            *ch_out = item - base - __shfl_sync(kFull, excl, src);
+            return b0 + src;
+        }
+        base += total;
+    }
+    return -1;
+}
+
+// First work item of sequence b and its chunk count.
+__device__ void seq_items(const int64_t* cu, int b, int64_t chunk, int lane, int64_t* first, int64_t* count,
+                          int32_t* err) {
+    int64_t acc = 0;
+    for (int b0 = 0; b0 < b; b0 += 32) {
+        const int bb = b0 + lane;
+        int64_t n = bb < b ? n_chunks_of(cu, bb, chunk, err) : 0;
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) n += __shfl_xor_sync(kFull, n, o);
+        acc += n;
+    }
+    *first = acc;
+    *count = n_chunks_of(cu, b, chunk, err);
+}
+
+template <bool QBF16>
+__device__ __forceinline__ float load_q(const void* q, int64_t idx) {
+    if (QBF16) return __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(q)[idx]);
+    return reinterpret_cast<const float*>(q)[idx];
+}
+
+template <int FMT, bool QBF16>
+__global__ void __launch_bounds__(kNT, 2) attn_partial_kernel(AttnParams p) {
+    extern __shared__ float4 smem4[];
+    float* qs = reinterpret_cast<float*>(smem4);
+    float* xs = qs + kHG * kXS;
+    float* sc = xs + kTR * kXS;
+    float* P = sc + kTR * 2;
+    float* alpha = P + kTR * kHG;
+    float* lvs = alpha + kHG;
+    int64_t* info = reinterpret_cast<int64_t*>(lvs + 16);
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int64_t item = blockIdx.x;
+    const int h0 = blockIdx.y * kHG;
+    const bool prefill = p.prefill_past >= 0;
+
+    if (warp == 0) {
+        int b = -1;
+        int64_t ch = 0;
+        if (prefill) {
+            if (item < p.n_seq) b = (int)item;
+        } else {
+            b = find_item(p.cu, p.n_seq, p.chunk, item, lane, &ch, p.err);
+        }
+        if (lane == 0) {
+            info[0] = b;
+            info[1] = ch;
+        }
+    }
+    if (tid < 16) lvs[tid] = p.lv[tid];
+    __syncthreads();
+    const int b = (int)info[0];
+    if (b < 0) return;
+    int64_t row0, row1;
+    if (prefill) {
+        row0 = 0;
+        row1 = p.prefill_past + b + 1;
+    } else {
+        const int64_t s = p.cu[b], e = p.cu[b + 1];
+        row0 = s + info[1] * p.chunk;
+        row1 = min(row0 + p.chunk, e);
+    }
+
+    // queries of this head group -> shared memory, f32
+    for (int i = tid; i < kHG * kD; i += kNT) {
+        const int h = i / kD, d = i - h * kD;
+        float v = 0.0f;
+        if (h0 + h < p.n_heads) v = load_q<QBF16>(p.q, ((int64_t)b * p.n_heads + h0 + h) * kD + d);
+        qs[h * kXS + d] = v;
+    }
+    __syncthreads();
+    if (FMT == KVQ_TQ4) {
+        // rotate each head's query once: latent block (512) and rope block (64)
+        for (int hh = warp; hh < kHG; hh += kNT / 32) {
+            float* qh = qs + hh * kXS;
+            float v[16];
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+                const int i = lane + 32 * k;
+                v[k] = sign_neg(p.signs, 0, i) ? -qh[i] : qh[i];
+            }
+            warp_fwht<512>(v, lane);
+#pragma unroll
+            for (int k = 0; k < 16; ++k) qh[lane + 32 * k] = __fmul_rn(v[k], p.kn[0]);
+            float r[2];
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+                const int i = lane + 32 * k;
+                r[k] = sign_neg(p.signs, 1, i) ? -qh[kDL + i] : qh[kDL + i];
+            }
+            warp_fwht<64>(r, lane);
+#pragma unroll
+            for (int k = 0; k < 2; ++k) qh[kDL + lane + 32 * k] = __fmul_rn(r[k], p.kn[1]);
+        }
+        __syncthreads();
+    }
+
+    const int sh = tid >> 4;   // score: head of this thread
+    const int st = tid & 15;   // score: row of this thread
+    float m_run = -INFINITY, l_run = 0.0f;
+    const int cq = tid >> 6;   // context: head quad
+    const int cc = tid & 63;   // context: dims 4cc..4cc+3 and 256+4cc..+3
+    float o[4][8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) o[i][j] = 0.0f;
+
+    for (int64_t t0 = row0; t0 < row1; t0 += kTR) {
+        const int nt = (int)min((int64_t)kTR, row1 - t0);
+        // decode the tile to code values (no scale applied)
+        if (FMT == KVQ_KV8) {
+            const uint32_t* src = reinterpret_cast<const uint32_t*>(p.codes + t0 * kD);
+            for (int w = tid; w < kTR * (kD / 4); w += kNT) {
+                const int r = w / (kD / 4), c4 = (w - r * (kD / 4)) * 4;
+                float4 f = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (r < nt) {
+                    const uint32_t u = __ldg(src + w);
+                    const float2 a = e4m3x2_to_float2((uint16_t)(u & 0xffffu));
+                    const float2 c = e4m3x2_to_float2((uint16_t)(u >> 16));
+                    f = make_float4(a.x, a.y, c.x, c.y);
+                }
+                *reinterpret_cast<float4*>(xs + r * kXS + c4) = f;
+            }
+        } else {
+            const uint32_t* src = reinterpret_cast<const uint32_t*>(p.codes + t0 * (kD / 2));
+            for (int w = tid; w < kTR * (kD / 8); w += kNT) {
+                const int r = w / (kD / 8), c8 = (w - r * (kD / 8)) * 8;
+                float f[8];
+                if (r < nt) {
+                    const uint32_t u = __ldg(src + w);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) f[j] = lvs[(u >> (4 * j)) & 15u];
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) f[j] = 0.0f;
+                }
+                *reinterpret_cast<float4*>(xs + r * kXS + c8) = make_float4(f[0], f[1], f[2], f[3]);
+                *reinterpret_cast<float4*>(xs + r * kXS + c8 + 4) = make_float4(f[4], f[5], f[6], f[7]);
+            }
+        }
+        if (tid < kTR) {
+            float sL = 0.0f, sR = 0.0f;
+            if (tid < nt) {
+                const int64_t row = t0 + tid;
+                if (p.n_blocks == 2) {
+                    sL = p.scales[row * 2];
+                    sR = p.scales[row * 2 + 1];
+                } else {
+                    sL = sR = p.scales[row];
+                }
+            }
+            sc[tid * 2] = sL;
+            sc[tid * 2 + 1] = sR;
+        }
+        __syncthreads();
+
+        // scores and the online softmax of this tile (16 lanes share a head)
+        {
+            const float* qh = qs + sh * kXS;
+            const float* xr = xs + st * kXS;
+            float aL0 = 0.f, aL1 = 0.f, aL2 = 0.f, aL3 = 0.f;
+#pragma unroll 8
+            for (int d = 0; d < kDL; d += 4) {
+                const float4 a = *reinterpret_cast<const float4*>(qh + d);
+                const float4 x = *reinterpret_cast<const float4*>(xr + d);
+                aL0 = fmaf(a.x, x.x, aL0);
+                aL1 = fmaf(a.y, x.y, aL1);
+                aL2 = fmaf(a.z, x.z, aL2);
+                aL3 = fmaf(a.w, x.w, aL3);
+            }
+            float aR0 = 0.f, aR1 = 0.f, aR2 = 0.f, aR3 = 0.f;
+#pragma unroll
+            for (int d = kDL; d < kD; d += 4) {
+                const float4 a = *reinterpret_cast<const float4*>(qh + d);
+                const float4 x = *reinterpret_cast<const float4*>(xr + d);
+                aR0 = fmaf(a.x, x.x, aR0);
+                aR1 = fmaf(a.y, x.y, aR1);
+                aR2 = fmaf(a.z, x.z, aR2);
+                aR3 = fmaf(a.w, x.w, aR3);
+            }
+            const float dotL = (aL0 + aL1) + (aL2 + aL3);
+            const float dotR = (aR0 + aR1) + (aR2 + aR3);
+            const float z = st < nt ? p.sm_scale * (sc[st * 2] * dotL + sc[st * 2 + 1] * dotR) : -INFINITY;
+            float tmax = z;
+#pragma unroll
+            for (int off = 8; off >= 1; off >>= 1) tmax = fmaxf(tmax, __shfl_xor_sync(kFull, tmax, off));
+            const float m_new = fmaxf(m_run, tmax);
+            const float a = m_run == -INFINITY ? 0.0f : expf(m_run - m_new);
+            const float pz = expf(z - m_new);
+            float psum = pz;
+#pragma unroll
+            for (int off = 8; off >= 1; off >>= 1) psum += __shfl_xor_sync(kFull, psum, off);
+            l_run = l_run * a + psum;
+            m_run = m_new;
+            P[st * kHG + sh] = pz * sc[st * 2];
+            if (st == 0) alpha[sh] = a;
+        }
+        __syncthreads();
+
+        // context: o[h][d] = alpha_h * o[h][d] + sum_t P[t][h] * c[t][d]
+        {
+            float al[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) al[i] = alpha[cq * 4 + i];
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < 8; ++j) o[i][j] *= al[i];
+            for (int t = 0; t < nt; ++t) {
+                const float4 xa = *reinterpret_cast<const float4*>(xs + t * kXS + 4 * cc);
+                const float4 xb = *reinterpret_cast<const float4*>(xs + t * kXS + 256 + 4 * cc);
+                const float4 pw = *reinterpret_cast<const float4*>(P + t * kHG + 4 * cq);
+                const float pv[4] = {pw.x, pw.y, pw.z, pw.w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    o[i][0] = fmaf(pv[i], xa.x, o[i][0]);
+                    o[i][1] = fmaf(pv[i], xa.y, o[i][1]);
+                    o[i][2] = fmaf(pv[i], xa.z, o[i][2]);
+                    o[i][3] = fmaf(pv[i], xa.w, o[i][3]);
+                    o[i][4] = fmaf(pv[i], xb.x, o[i][4]);
+                    o[i][5] = fmaf(pv[i], xb.y, o[i][5]);
+                    o[i][6] = fmaf(pv[i], xb.z, o[i][6]);
+                    o[i][7] = fmaf(pv[i], xb.w, o[i][7]);
+                }
+            }
+        }
+        __syncthreads();
+    }
+
+    // partial state of this chunk
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int h = h0 + cq * 4 + i;
+        if (h < p.n_heads) {
+            float* dst = p.ws_o + (item * p.n_heads + h) * kDV;
+            *reinterpret_cast<float4*>(dst + 4 * cc) = make_float4(o[i][0], o[i][1], o[i][2], o[i][3]);
+            *reinterpret_cast<float4*>(dst + 256 + 4 * cc) = make_float4(o[i][4], o[i][5], o[i][6], o[i][7]);
+        }
+    }
+    if (st == 0 && h0 + sh < p.n_heads) {
+        float* ml = p.ws_ml + (item * p.n_heads + h0 + sh) * 2;
+        ml[0] = m_run;
+        ml[1] = l_run;
+    }
+}
+
+template <int FMT>
+__global__ void __launch_bounds__(128) attn_merge_kernel(AttnParams p, float* __restrict__ out) {
+    __shared__ int64_t info[2];
+    __shared__ float ov[kDV];
+    const int h = blockIdx.x, b = blockIdx.y;
+    const int tid = threadIdx.x, lane = tid & 31;
+    const bool prefill = p.prefill_past >= 0;
+    if (tid < 32) {
+        int64_t first = b, count = 1;
+        if (!prefill) seq_items(p.cu, b, p.chunk, lane, &first, &count, p.err);
+        if (lane == 0) {
+            info[0] = first;
+            info[1] = count;
+        }
+    }
+    __syncthreads();
+    const int64_t first = info[0];
+    int64_t count = info[1];
+    if (first + count > p.max_items) {
+        if (tid == 0) set_err(p.err, KVQ_ERR_DEVICE);
+        count = 0;
+    }
+    float M = -INFINITY;
+    for (int64_t c = 0; c < count; ++c) M = fmaxf(M, p.ws_ml[((first + c) * p.n_heads + h) * 2]);
+    float L = 0.0f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int64_t c = 0; c < count; ++c) {
+        const float* ml = p.ws_ml + ((first + c) * p.n_heads + h) * 2;
+        const float w = (M == -INFINITY) ? 0.0f : expf(ml[0] - M);
+        L += w * ml[1];
+        const float4 v = *reinterpret_cast<const float4*>(p.ws_o + ((first + c) * p.n_heads + h) * kDV + 4 * tid);
+        acc.x = fmaf(w, v.x, acc.x);
+        acc.y = fmaf(w, v.y, acc.y);
+        acc.z = fmaf(w, v.z, acc.z);
+        acc.w = fmaf(w, v.w, acc.w);
+    }
+    const float inv = L > 0.0f ? 1.0f / L : 0.0f;
+    acc = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+    float* dst = out + ((int64_t)b * p.n_heads + h) * kDV;
+    if (FMT == KVQ_KV8) {
+        *reinterpret_cast<float4*>(dst + 4 * tid) = acc;
+        return;
+    }
+    *reinterpret_cast<float4*>(ov + 4 * tid) = acc;
+    __syncthreads();
+    if (tid < 32) {
+        // context was accumulated in the rotated domain: unrotate once
+        float v[16];
+#pragma unroll
+        for (int k = 0; k < 16; ++k) v[k] = ov[lane + 32 * k];
+        warp_fwht<512>(v, lane);
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+            const int i = lane + 32 * k;
+            const float y = __fmul_rn(v[k], p.kn[0]);
+            dst[i] = sign_neg(p.signs, 0, i) ? -y : y;
+        }
+    }
+}
+
+template <int FMT, bool QBF16>
+cudaError_t launch_partial(const AttnParams& p, int64_t grid_x, int groups, cudaStream_t stream) {
+    const size_t smem = kSmemFloats * sizeof(float);
+    cudaError_t e = cudaFuncSetAttribute(attn_partial_kernel<FMT, QBF16>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    attn_partial_kernel<FMT, QBF16><<<dim3((unsigned)grid_x, (unsigned)groups), kNT, smem, stream>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+AttnPlan plan_decode_simt(int32_t batch, int32_t n_heads, int64_t max_total_rows) {
+    AttnPlan pl{};
+    pl.heads_per_cta = kHG;
+    const int64_t groups = (n_heads + kHG - 1) / kHG;
+    const int64_t target_items = std::max<int64_t>(1, (int64_t)kSmSMs * 4 / groups);
+    int64_t chunk = (std::max<int64_t>(max_total_rows, 1) + target_items - 1) / target_items;
+    chunk = std::max<int64_t>(kTR, (chunk + kTR - 1) / kTR * kTR);
+    pl.chunk = chunk;
+    pl.max_items = (max_total_rows + chunk - 1) / chunk + batch;
+    return pl;
+}
+
+size_t partial_bytes(int64_t max_items, int32_t n_heads, int32_t v_dim) {
+    return (size_t)max_items * n_heads * (v_dim + 2) * sizeof(float);
+}
+
+cudaError_t launch_attn_simt(kvq_format fmt, const kvq_mla_layout& L, const void* q, kvq_dtype qdt, int32_t n_seq,
+                             int32_t n_heads, const uint8_t* codes, const float* scales, const int64_t* cu_seqlens,
+                             int64_t prefill_past, const AttnPlan& plan, float sm_scale, float* out,
+                             void* workspace, cudaStream_t stream) {
+    if (n_seq == 0 || n_heads == 0) return cudaSuccess;
+    AttnParams p{};
+    p.n_blocks = L.n_blocks;
+    p.n_seq = n_seq;
+    p.n_heads = n_heads;
+    p.q = q;
+    p.codes = codes;
+    p.scales = scales;
+    p.cu = cu_seqlens;
+    p.prefill_past = prefill_past;
+    p.chunk = plan.chunk;
+    p.max_items = plan.max_items;
+    p.sm_scale = sm_scale;
+    char* ws = static_cast<char*>(workspace);
+    p.err = reinterpret_cast<int32_t*>(ws);
+    p.ws_o = reinterpret_cast<float*>(ws + kWsHeader);
+    p.ws_ml = p.ws_o + (size_t)plan.max_items * n_heads * kDV;
+    if (fmt == KVQ_TQ4) {
+        p.signs = tq4_sign_words(L);
+        p.kn[0] = (float)(1.0 / sqrt((double)L.block_dim[0]));
+        p.kn[1] = (float)(1.0 / sqrt((double)L.block_dim[1]));
+        const Codebook16 cb = tq4_codebook();
+        for (int k = 0; k < 16; ++k) p.lv[k] = cb.lv[k];
+    }
+    const int groups = (n_heads + kHG - 1) / kHG;
+    cudaError_t e;
+    if (fmt == KVQ_KV8)
+        e = qdt == KVQ_BF16 ? launch_partial<KVQ_KV8, true>(p, plan.max_items, groups, stream)
+                            : launch_partial<KVQ_KV8, false>(p, plan.max_items, groups, stream);
+    else
+        e = qdt == KVQ_BF16 ? launch_partial<KVQ_TQ4, true>(p, plan.max_items, groups, stream)
+                            : launch_partial<KVQ_TQ4, false>(p, plan.max_items, groups, stream);
+    if (e != cudaSuccess) return e;
+    if (fmt == KVQ_KV8)
+        attn_merge_kernel<KVQ_KV8><<<dim3(n_heads, n_seq), 128, 0, stream>>>(p, out);
+    else
+        attn_merge_kernel<KVQ_TQ4><<<dim3(n_heads, n_seq), 128, 0, stream>>>(p, out);
+    return cudaGetLastError();
+}
+
+}  // namespace kvq

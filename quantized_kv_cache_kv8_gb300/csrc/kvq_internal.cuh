@@ -1,0 +1,169 @@
+// kvq_internal.cuh -- shared device helpers and the launchers behind the C ABI.
+//
+// Page titles cited as in kvq.h: [P1] KV cache quantization: fp8 (KV8) + 4-bit
+// TurboQuant (KV_TQ) on CPU, CUDA, and Metal; [P2] CPU: KV cache quantization
+// -- KV8 (fp8 e4m3) + KV_TQ (rotated-int4 / PolarQuant); [P3] KV cache: FP16
+// sliding window + attention sinks, and an optional 2-bit K / 4-bit V cache
+// scheme (--kv q2k).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <string.h>
+
+#include "kvq.h"
+
+namespace kvq {
+
+constexpr unsigned kFull = 0xffffffffu;
+
+// N(0,1) Lloyd-Max codebooks as f32 bit patterns (levels ascending, then the
+// decision thresholds = f64 midpoints of adjacent levels rounded to f32).
+// Derived by gen_codebook.py (root finding on the centroid and midpoint
+// conditions); the test suite checks them against an independent solver.
+constexpr uint32_t kTq4LevelBits[16] = {
+    0xc02ee2bfu, 0xc0046ac7u, 0xbfcf1c25u, 0xbfa0cc2fu, 0xbf713d39u, 0xbf28215eu, 0xbec6ae44u, 0xbe0379fdu,
+    0x3e0379fdu, 0x3ec6ae44u, 0x3f28215eu, 0x3f713d39u, 0x3fa0cc2fu, 0x3fcf1c25u, 0x40046ac7u, 0x402ee2bfu};
+constexpr uint32_t kTq4ThreshBits[15] = {
+    0xc019a6c3u, 0xbfebf8dau, 0xbfb7f42au, 0xbf8cb566u, 0xbf4caf4bu, 0xbf05bc40u, 0xbe8435a1u, 0x00000000u,
+    0x3e8435a1u, 0x3f05bc40u, 0x3f4caf4bu, 0x3f8cb566u, 0x3fb7f42au, 0x3febf8dau, 0x4019a6c3u};
+constexpr uint32_t kK2LevelBits[4] = {0xbfc1555du, 0xbee7d2c9u, 0x3ee7d2c9u, 0x3fc1555du};
+constexpr uint32_t kK2ThreshBits[3] = {0xbf7b4a0fu, 0x00000000u, 0x3f7b4a0fu};
+
+inline float host_bits_to_float(uint32_t b) {
+    float f;
+    memcpy(&f, &b, sizeof f);
+    return f;
+}
+
+struct Codebook16 {
+    float lv[16];
+    float th[16];   // 15 used; th[15] = +inf pads the branchless search
+};
+struct Codebook4 {
+    float lv[4];
+    float th[4];    // 3 used
+};
+
+Codebook16 tq4_codebook();
+Codebook4 k2_codebook();
+
+// Rotation signs of one TQ4 row: bit i of the D-bit mask (-1 where set).  The
+// words are splitmix64 outputs from state = seed, block b starting at a fresh
+// word ([P1] Commits, item 6: seeded randomized-Hadamard rotation).
+struct SignWords {
+    uint64_t w[16];        // up to 1024 dims
+    int32_t block_word[2]; // first word of each block
+};
+SignWords tq4_sign_words(const kvq_mla_layout& L);
+
+// ---------------------------------------------------------------------------
+// Device helpers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) v = fmaxf(v, __shfl_xor_sync(kFull, v, o));
+    return v;
+}
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) v = __fadd_rn(v, __shfl_xor_sync(kFull, v, o));
+    return v;
+}
+
+// Number of thresholds strictly below u (a sorted list of 15, th[15] = +inf).
+__device__ __forceinline__ int code16(float u, const float* th) {
+    int c = (u > th[7]) ? 8 : 0;
+    c += (u > th[c + 3]) ? 4 : 0;
+    c += (u > th[c + 1]) ? 2 : 0;
+    c += (u > th[c]) ? 1 : 0;
+    return c;
+}
+
+// e4m3 byte -> f32 (exact).  The NaN pattern S.1111.111 is never stored by the
+// encoder; it would read back as NaN here.
+__device__ __forceinline__ float2 e4m3x2_to_float2(uint16_t two) {
+    __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)two, __NV_E4M3);
+    return __half22float2(*reinterpret_cast<__half2*>(&h));
+}
+
+// Warp-held radix-2 FWHT of an n-point block (n a power of two, 2..1024).
+// Lane j holds elements j + 32k in v[k], k < K = max(n/32, 1); for n < 32
+// only lanes j < n hold data.  Stages run in ascending h = 1, 2, 4, ..., n/2,
+// each butterfly mapping (a, b) to (a+b, a-b) in f32 -- the same additions as
+// the plain loop, so the result is bit-identical to it.
+template <int N>
+__device__ __forceinline__ void warp_fwht(float* v, int lane) {
+    constexpr int K = N >= 32 ? N / 32 : 1;
+#pragma unroll
+    for (int h = 1; h < 32 && h < N; h <<= 1) {
+#pragma unroll
+        for (int k = 0; k < K; ++k) {
+            float other = __shfl_xor_sync(kFull, v[k], h);
+            v[k] = (lane & h) ? __fsub_rn(other, v[k]) : __fadd_rn(v[k], other);
+        }
+    }
+#pragma unroll
+    for (int hs = 1; hs < K; hs <<= 1) {
+#pragma unroll
+        for (int k = 0; k < K; ++k) {
+            if ((k & hs) == 0) {
+                float a = v[k], b = v[k + hs];
+                v[k] = __fadd_rn(a, b);
+                v[k + hs] = __fsub_rn(a, b);
+            }
+        }
+    }
+}
+
+__device__ __forceinline__ bool sign_neg(const SignWords& s, int block, int i) {
+    uint64_t w = s.w[s.block_word[block] + (i >> 6)];
+    return (w >> (i & 63)) & 1ull;
+}
+
+// ---------------------------------------------------------------------------
+// Launchers (all asynchronous on `stream`; return cudaGetLastError()).
+// ---------------------------------------------------------------------------
+// dst_rows (device, may be null): input row i goes to pool row dst_rows[i].
+cudaError_t launch_kv8_encode(const float* x, int64_t n_rows, const kvq_mla_layout& L, const int64_t* dst_rows,
+                              uint8_t* codes, float* scales, cudaStream_t stream);
+cudaError_t launch_tq4_encode(const float* x, int64_t n_rows, const kvq_mla_layout& L, const int64_t* dst_rows,
+                              uint8_t* packed, float* scales, cudaStream_t stream);
+cudaError_t launch_tq4_rotate(const void* in, kvq_dtype dt, int64_t n_vecs, const kvq_mla_layout& L, int inverse,
+                              float* out, cudaStream_t stream);
+
+// SIMT attention over the 576 = 512 + 64 latent layout.
+struct AttnPlan {
+    int64_t chunk;        // rows per work item
+    int64_t max_items;    // grid bound
+    int32_t heads_per_cta;
+};
+AttnPlan plan_decode_simt(int32_t batch, int32_t n_heads, int64_t max_total_rows);
+size_t partial_bytes(int64_t max_items, int32_t n_heads, int32_t v_dim);
+constexpr size_t kWsHeader = 256;   // error word + padding
+
+cudaError_t launch_attn_simt(kvq_format fmt, const kvq_mla_layout& L, const void* q, kvq_dtype qdt, int32_t n_seq,
+                             int32_t n_heads, const uint8_t* codes, const float* scales, const int64_t* cu_seqlens,
+                             int64_t prefill_past, const AttnPlan& plan, float sm_scale, float* out,
+                             void* workspace, cudaStream_t stream);
+
+// K2/V4
+cudaError_t launch_k2v4_encode(const kvq_k2v4_layout& L, const float* k, const float* v, int32_t batch,
+                               int64_t n_cells, int64_t cap, uint8_t* k_codes, uint16_t* k_scales,
+                               uint8_t* v_blocks, uint16_t* k_win, uint16_t* v_win, cudaStream_t stream);
+struct K2V4Plan {
+    int64_t chunk;
+    int32_t n_chunks;
+};
+K2V4Plan plan_k2v4(const kvq_k2v4_layout& L, int32_t batch, int32_t n_q_heads, int64_t n_cells);
+size_t k2v4_partial_bytes(const kvq_k2v4_layout& L, int32_t batch, int32_t n_q_heads, const K2V4Plan& p);
+cudaError_t launch_k2v4_decode(const kvq_k2v4_layout& L, const float* q, int32_t batch, int32_t n_q_heads,
+                               int64_t n_cells, int64_t cap, const uint8_t* k_codes, const uint16_t* k_scales,
+                               const uint8_t* v_blocks, const uint16_t* k_win, const uint16_t* v_win,
+                               float sm_scale, float* out, void* workspace, const K2V4Plan& plan,
+                               cudaStream_t stream);
+
+}  // namespace kvq

@@ -1,0 +1,241 @@
+"""Python binding of libkvq's C ABI (include/kvq.h).
+
+Argument marshalling only: every step of the computation runs in the CUDA
+library.  Tensors must be contiguous CUDA tensors of the stated dtypes; the
+calls are asynchronous on the current torch stream (or the one given).  There
+is no CPU path: if the library cannot be built or loaded, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import math
+import threading
+
+import torch
+
+from . import build as _build
+
+KVQ_KV8, KVQ_TQ4 = 1, 2
+KVQ_F32, KVQ_BF16 = 0, 1
+PATH_AUTO, PATH_SIMT, PATH_TENSOR = 0, 1, 2
+SM_SCALE_MLA = 1.0 / math.sqrt(192.0)
+
+
+class KvqError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"{what}: kvq status {status} ({status_string(status)})")
+        self.status = status
+
+
+class MLALayout(C.Structure):
+    _fields_ = [("n_blocks", C.c_int32), ("block_dim", C.c_int32 * 2), ("v_dim", C.c_int32),
+                ("seed", C.c_uint64)]
+
+
+class K2V4Layout(C.Structure):
+    _fields_ = [("n_kv_heads", C.c_int32), ("head_dim", C.c_int32), ("group", C.c_int32),
+                ("k_gain", C.c_float), ("n_sink", C.c_int32), ("n_window", C.c_int32), ("n_slack", C.c_int32)]
+
+
+def mla_layout(block_dims=(512, 64), v_dim=512, seed=0) -> MLALayout:
+    bd = (C.c_int32 * 2)(block_dims[0], block_dims[1] if len(block_dims) > 1 else 0)
+    return MLALayout(len(block_dims), bd, v_dim, seed)
+
+
+def k2v4_layout(n_kv_heads=2, head_dim=256, k_gain=1.10, n_sink=8, n_window=256, n_slack=16) -> K2V4Layout:
+    return K2V4Layout(n_kv_heads, head_dim, 32, k_gain, n_sink, n_window, n_slack)
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def lib():
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = _build.build()
+            L = C.CDLL(path)
+            _declare(L)
+            _lib = L
+    return _lib
+
+
+def _declare(L):
+    P, S, I32, I64 = C.c_void_p, C.c_size_t, C.c_int32, C.c_int64
+    pl, pk = C.POINTER(MLALayout), C.POINTER(K2V4Layout)
+    L.kvq_status_string.restype = C.c_char_p
+    L.kvq_status_string.argtypes = [C.c_int]
+    L.kvq_version.restype = C.c_char_p
+    L.kvq_codebook.restype = C.c_int
+    L.kvq_codebook.argtypes = [I32, P, P]
+    L.kv8_encode.restype = C.c_int
+    L.kv8_encode.argtypes = [P, I64, pl, P, P, P, P]
+    L.tq4_encode.restype = C.c_int
+    L.tq4_encode.argtypes = [P, I64, pl, P, P, P, P]
+    L.tq4_rotate.restype = C.c_int
+    L.tq4_rotate.argtypes = [P, C.c_int, I64, pl, I32, P, P]
+    L.kv_attn_workspace_size.restype = S
+    L.kv_attn_workspace_size.argtypes = [C.c_int, pl, I32, I32, I64, C.c_int]
+    L.kv_attn_decode.restype = C.c_int
+    L.kv_attn_decode.argtypes = [C.c_int, pl, P, C.c_int, I32, I32, P, P, P, I64, C.c_float, P, P, S, C.c_int, P]
+    L.kv_attn_prefill_workspace_size.restype = S
+    L.kv_attn_prefill_workspace_size.argtypes = [C.c_int, pl, I32, I64, I64, C.c_int]
+    L.kv_attn_prefill.restype = C.c_int
+    L.kv_attn_prefill.argtypes = [C.c_int, pl, P, P, C.c_int, I64, I64, I32, P, P, C.c_float, P, P, S, C.c_int, P]
+    L.kvq_read_device_error.restype = I32
+    L.kvq_read_device_error.argtypes = [P, I32, P]
+    L.k2v4_encode.restype = C.c_int
+    L.k2v4_encode.argtypes = [pk, P, P, I32, I64, I64, P, P, P, P, P, P]
+    L.kv_attn_decode_k2v4_workspace_size.restype = S
+    L.kv_attn_decode_k2v4_workspace_size.argtypes = [pk, I32, I32, I64, C.c_int]
+    L.kv_attn_decode_k2v4.restype = C.c_int
+    L.kv_attn_decode_k2v4.argtypes = [pk, P, I32, I32, I64, I64, P, P, P, P, P, C.c_float, P, P, S, C.c_int, P]
+
+
+def status_string(status: int) -> str:
+    return lib().kvq_status_string(status).decode()
+
+
+def version() -> str:
+    return lib().kvq_version().decode()
+
+
+def _ok(status: int, what: str):
+    if status != 0:
+        raise KvqError(status, what)
+
+
+def _ptr(t: torch.Tensor | None, dtype=None, name="tensor"):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    return C.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return C.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _qdtype(q: torch.Tensor) -> int:
+    if q.dtype == torch.float32:
+        return KVQ_F32
+    if q.dtype == torch.bfloat16:
+        return KVQ_BF16
+    raise ValueError("query must be float32 or bfloat16")
+
+
+def codebook(which: int):
+    n = 16 if which == 16 else 4
+    lv = (C.c_float * n)()
+    th = (C.c_float * (n - 1))()
+    _ok(lib().kvq_codebook(which, lv, th), "kvq_codebook")
+    return list(lv), list(th)
+
+
+# -- producers ---------------------------------------------------------------
+
+def kv8_encode(x, codes, scales, layout: MLALayout | None = None, dst_rows=None, stream=None):
+    """Encode rows of x into the pool; row i goes to pool row dst_rows[i] (or i)."""
+    layout = layout or mla_layout()
+    _ok(lib().kv8_encode(_ptr(x, torch.float32, "x"), x.shape[0], C.byref(layout),
+                         _ptr(dst_rows, torch.int64, "dst_rows"), _ptr(codes, torch.uint8, "codes"),
+                         _ptr(scales, torch.float32, "scales"), _stream(stream)), "kv8_encode")
+
+
+def tq4_encode(x, packed, scales, layout: MLALayout | None = None, dst_rows=None, stream=None):
+    layout = layout or mla_layout()
+    _ok(lib().tq4_encode(_ptr(x, torch.float32, "x"), x.shape[0], C.byref(layout),
+                         _ptr(dst_rows, torch.int64, "dst_rows"), _ptr(packed, torch.uint8, "packed"),
+                         _ptr(scales, torch.float32, "scales"), _stream(stream)), "tq4_encode")
+
+
+def tq4_encode_status(x, packed, scales, layout: MLALayout, stream=None) -> int:
+    return lib().tq4_encode(_ptr(x, torch.float32, "x"), x.shape[0], C.byref(layout), None, _ptr(packed),
+                            _ptr(scales), _stream(stream))
+
+
+def tq4_rotate(inp, out, layout: MLALayout | None = None, inverse=False, stream=None):
+    layout = layout or mla_layout()
+    D = layout.block_dim[0] + (layout.block_dim[1] if layout.n_blocks > 1 else 0)
+    n = inp.numel() // D
+    _ok(lib().tq4_rotate(_ptr(inp, None, "in"), _qdtype(inp), n, C.byref(layout), int(inverse),
+                         _ptr(out, torch.float32, "out"), _stream(stream)), "tq4_rotate")
+
+
+# -- consumers ---------------------------------------------------------------
+
+def kv_attn_workspace_size(fmt: int, batch: int, n_heads: int, max_total_rows: int,
+                           layout: MLALayout | None = None, path: int = PATH_AUTO) -> int:
+    layout = layout or mla_layout()
+    return lib().kv_attn_workspace_size(fmt, C.byref(layout), batch, n_heads, max_total_rows, path)
+
+
+def kv_attn_decode(fmt: int, q, codes, scales, cu_seqlens, out, workspace, max_total_rows: int,
+                   sm_scale: float = SM_SCALE_MLA, layout: MLALayout | None = None, path: int = PATH_AUTO,
+                   stream=None):
+    layout = layout or mla_layout()
+    B, H = q.shape[0], q.shape[1]
+    _ok(lib().kv_attn_decode(fmt, C.byref(layout), _ptr(q, None, "q"), _qdtype(q), B, H,
+                             _ptr(codes, torch.uint8, "codes"), _ptr(scales, torch.float32, "scales"),
+                             _ptr(cu_seqlens, torch.int64, "cu_seqlens"), int(max_total_rows), float(sm_scale),
+                             _ptr(out, torch.float32, "out"), _ptr(workspace, torch.uint8, "workspace"),
+                             workspace.numel(), path, _stream(stream)), "kv_attn_decode")
+
+
+def kv_attn_prefill_workspace_size(fmt: int, n_heads: int, n_past: int, n_new: int,
+                                   layout: MLALayout | None = None, path: int = PATH_AUTO) -> int:
+    layout = layout or mla_layout()
+    return lib().kv_attn_prefill_workspace_size(fmt, C.byref(layout), n_heads, n_past, n_new, path)
+
+
+def kv_attn_prefill(fmt: int, x_new, q, codes, scales, n_past: int, out, workspace,
+                    sm_scale: float = SM_SCALE_MLA, layout: MLALayout | None = None, path: int = PATH_AUTO,
+                    stream=None):
+    layout = layout or mla_layout()
+    n_new, H = q.shape[0], q.shape[1]
+    _ok(lib().kv_attn_prefill(fmt, C.byref(layout), _ptr(x_new, torch.float32, "x_new"), _ptr(q, None, "q"),
+                              _qdtype(q), int(n_past), n_new, H, _ptr(codes, torch.uint8, "codes"),
+                              _ptr(scales, torch.float32, "scales"), float(sm_scale), _ptr(out, torch.float32, "out"),
+                              _ptr(workspace, torch.uint8, "workspace"), workspace.numel(), path, _stream(stream)),
+        "kv_attn_prefill")
+
+
+def read_device_error(workspace, clear: bool = True, stream=None) -> int:
+    return lib().kvq_read_device_error(_ptr(workspace, torch.uint8, "workspace"), int(clear), _stream(stream))
+
+
+# -- K2/V4 -------------------------------------------------------------------
+
+def k2v4_encode(layout: K2V4Layout, k, v, k_codes, k_scales, v_blocks, k_win, v_win, capacity: int | None = None,
+                stream=None):
+    B, H, T, D = k.shape
+    cap = T if capacity is None else capacity
+    _ok(lib().k2v4_encode(C.byref(layout), _ptr(k, torch.float32, "k"), _ptr(v, torch.float32, "v"), B, T, cap,
+                          _ptr(k_codes, torch.uint8, "k_codes"), _ptr(k_scales, torch.int16, "k_scales"),
+                          _ptr(v_blocks, torch.uint8, "v_blocks"), _ptr(k_win, torch.int16, "k_win"),
+                          _ptr(v_win, torch.int16, "v_win"), _stream(stream)), "k2v4_encode")
+
+
+def kv_attn_decode_k2v4_workspace_size(layout: K2V4Layout, batch: int, n_q_heads: int, n_cells: int,
+                                       path: int = PATH_AUTO) -> int:
+    return lib().kv_attn_decode_k2v4_workspace_size(C.byref(layout), batch, n_q_heads, n_cells, path)
+
+
+def kv_attn_decode_k2v4(layout: K2V4Layout, q, n_cells: int, k_codes, k_scales, v_blocks, k_win, v_win, out,
+                        workspace, sm_scale: float, capacity: int | None = None, path: int = PATH_AUTO, stream=None):
+    B, Hq, D = q.shape
+    cap = n_cells if capacity is None else capacity
+    _ok(lib().kv_attn_decode_k2v4(C.byref(layout), _ptr(q, torch.float32, "q"), B, Hq, n_cells, cap,
+                                  _ptr(k_codes, torch.uint8, "k_codes"), _ptr(k_scales, torch.int16, "k_scales"),
+                                  _ptr(v_blocks, torch.uint8, "v_blocks"), _ptr(k_win, torch.int16, "k_win"),
+                                  _ptr(v_win, torch.int16, "v_win"), float(sm_scale), _ptr(out, torch.float32, "out"),
+                                  _ptr(workspace, torch.uint8, "workspace"), workspace.numel(), path,
+                                  _stream(stream)), "kv_attn_decode_k2v4")

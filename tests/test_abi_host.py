@@ -1,0 +1,91 @@
+"""The C-ABI library without a GPU: it builds, loads, exports every symbol the
+header declares, and its host-side logic (validation, workspace sizing, the
+codebook constants) behaves.  No call here launches a kernel."""
+import ctypes as C
+import os
+import re
+
+import numpy as np
+import pytest
+
+from conftest import ROOT
+
+
+@pytest.fixture(scope="module")
+def kvq():
+    from quantized_kv_cache_kv8_gb300 import kvq as K
+    K.lib()
+    return K
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "kvq.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s+\**([A-Za-z_][A-Za-z0-9_]*)\s*\(",
+                       src, flags=re.M)
+    return sorted(set(names))
+
+
+def test_every_declared_symbol_is_exported(kvq):
+    names = declared_functions()
+    assert len(names) >= 14, names
+    for n in names:
+        assert hasattr(kvq.lib(), n), n
+
+
+def test_status_strings_and_version(kvq):
+    assert kvq.version() == "0.1.0"
+    for s in range(7):
+        assert kvq.status_string(s)
+
+
+def test_codebook_constants_equal_the_oracle(kvq, oracle):
+    lv, th = kvq.codebook(16)
+    olv, oth = oracle.tq4_codebook()
+    np.testing.assert_array_equal(np.array(lv, np.float32).view(np.uint32), olv.view(np.uint32))
+    np.testing.assert_array_equal(np.array(th, np.float32).view(np.uint32), oth.view(np.uint32))
+    lv, th = kvq.codebook(4)
+    olv, oth = oracle.k2_codebook()
+    np.testing.assert_array_equal(np.array(lv, np.float32).view(np.uint32), olv.view(np.uint32))
+    np.testing.assert_array_equal(np.array(th, np.float32).view(np.uint32), oth.view(np.uint32))
+
+
+def test_tq4_refuses_non_power_of_two_before_launch(kvq):
+    L = kvq.lib()
+    for bd in [(576,), (500, 76), (512, 60)]:
+        lay = kvq.mla_layout(bd, v_dim=min(bd[0], 512))
+        assert L.tq4_encode(None, 4, C.byref(lay), None, None, None, None) == 2
+        assert L.tq4_rotate(None, 0, 4, C.byref(lay), 0, None, None) == 2
+        assert L.kv_attn_workspace_size(2, C.byref(lay), 1, 16, 100, 0) == 0
+        assert L.kv_attn_decode(2, C.byref(lay), None, 0, 1, 16, None, None, None, 100, 0.1, None, None, 0, 0,
+                                None) == 2
+
+
+def test_argument_validation(kvq):
+    L = kvq.lib()
+    lay = kvq.mla_layout()
+    assert L.kv8_encode(None, -1, C.byref(lay), None, None, None, None) == 1
+    assert L.kv8_encode(None, 0, C.byref(lay), None, None, None, None) == 0    # empty is a no-op
+    assert L.kv8_encode(None, 3, C.byref(lay), None, None, None, None) == 1    # null pointers
+    assert L.kv8_encode(None, 3, None, None, None, None, None) == 1
+    # workspace too small is reported before any launch
+    need = kvq.kv_attn_workspace_size(1, 8, 128, 32768)
+    assert need > 0
+    assert L.kv_attn_decode(1, C.byref(lay), C.c_void_p(16), 1, 8, 128, C.c_void_p(16), C.c_void_p(16),
+                            C.c_void_p(16), 32768, 0.07, C.c_void_p(16), C.c_void_p(16), need - 1, 0, None) == 3
+    # unsupported attention layouts
+    odd = kvq.mla_layout((256, 64), v_dim=256)
+    assert kvq.kv_attn_workspace_size(1, 1, 16, 100, layout=odd) == 0
+    k2 = kvq.k2v4_layout()
+    k2.group = 16
+    assert L.k2v4_encode(C.byref(k2), None, None, 1, 64, 64, None, None, None, None, None, None) == 5
+
+
+def test_workspace_sizes_grow_with_work(kvq):
+    a = kvq.kv_attn_workspace_size(1, 8, 128, 32768)
+    b = kvq.kv_attn_workspace_size(1, 32, 128, 2_100_000)
+    assert 0 < a < b
+    p = kvq.kv_attn_prefill_workspace_size(2, 128, 126976, 2048)
+    assert p >= 2048 * 128 * 514 * 4
+    k = kvq.kv_attn_decode_k2v4_workspace_size(kvq.k2v4_layout(), 4, 16, 32768)
+    assert k > 0

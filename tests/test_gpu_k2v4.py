@@ -1,0 +1,88 @@
+"""K2/V4 GQA cache on the GPU against the oracle: encode bit for bit, decode
+within the fp32 tolerance, overlay cells exact."""
+import numpy as np
+import pytest
+import torch
+
+from gpu_common import SIMT_TOL, kvq_module, rel_err, to_dev
+from quantized_kv_cache_kv8_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def kvq():
+    return kvq_module()
+
+
+def gpu_k2v4(kvq, k, v, layout, cap=None):
+    B, H, T, D = k.shape
+    cap = T if cap is None else cap
+    slots = layout.n_sink + layout.n_window + layout.n_slack
+    kc = torch.zeros((B, H, cap, D // 4), dtype=torch.uint8, device="cuda")
+    ks = torch.zeros((B, H, cap // 32, D), dtype=torch.int16, device="cuda")
+    vb = torch.zeros((B, H, cap, D // 32, 18), dtype=torch.uint8, device="cuda")
+    kw = torch.zeros((B, H, slots, D), dtype=torch.int16, device="cuda")
+    vw = torch.zeros((B, H, slots, D), dtype=torch.int16, device="cuda")
+    kvq.k2v4_encode(layout, to_dev(k), to_dev(v), kc, ks, vb, kw, vw, capacity=cap)
+    return kc, ks, vb, kw, vw
+
+
+def oracle_layout(oracle, layout):
+    return oracle.k2v4_layout(layout.n_kv_heads, layout.head_dim, layout.k_gain, layout.n_sink, layout.n_window,
+                              layout.n_slack)
+
+
+def run_case(kvq, oracle, B, H, T, D, Hq, sink, window, seed, full_check=True, pairs=None):
+    layout = kvq.k2v4_layout(H, D, 1.10, sink, window, 16)
+    OL = oracle_layout(oracle, layout)
+    k, v = synth.gqa_kv(seed, B, H, T, D)
+    enc = gpu_k2v4(kvq, k, v, layout)
+    for b in range(B):
+        oenc = oracle.k2v4_encode(k[b], v[b], OL)
+        for name, g, o in zip(("k_codes", "k_scales", "v_blocks", "k_win", "v_win"), enc, oenc):
+            np.testing.assert_array_equal(g[b].cpu().numpy().view(o.dtype), o, err_msg=f"{name} seq {b}")
+    q = synth.queries(seed + 1, (B, Hq, D))
+    out = torch.empty((B, Hq, D), device="cuda")
+    ws = torch.empty(kvq.kv_attn_decode_k2v4_workspace_size(layout, B, Hq, T), dtype=torch.uint8, device="cuda")
+    sm = 1.0 / np.sqrt(D)
+    kvq.kv_attn_decode_k2v4(layout, to_dev(q), T, *enc, out, ws, sm)
+    torch.cuda.synchronize()
+    got = out.cpu().numpy()
+    grp = Hq // H
+    for b in range(B):
+        oenc = oracle.k2v4_encode(k[b], v[b], OL)
+        K, V = oracle.k2v4_reconstruct(*oenc, T, OL)
+        ref = oracle.k2v4_attn(K, V, q[b], sm)
+        for h in range(Hq):
+            if pairs is not None and (b, h) not in pairs:
+                continue
+            assert rel_err(got[b, h], ref[h]) <= SIMT_TOL, (b, h)
+    return got
+
+
+def test_k2v4_small(kvq, oracle):
+    run_case(kvq, oracle, B=2, H=2, T=96, D=128, Hq=16, sink=4, window=16, seed=51)
+
+
+def test_k2v4_window_covers_all(kvq, oracle):
+    """Every cell inside the overlay: output equals attention over fp16 K/V."""
+    B, H, T, D, Hq = 1, 2, 64, 128, 8
+    layout = kvq.k2v4_layout(H, D, 1.10, 8, T, 16)
+    k, v = synth.gqa_kv(61, B, H, T, D)
+    enc = gpu_k2v4(kvq, k, v, layout)
+    q = synth.queries(62, (B, Hq, D))
+    out = torch.empty((B, Hq, D), device="cuda")
+    ws = torch.empty(kvq.kv_attn_decode_k2v4_workspace_size(layout, B, Hq, T), dtype=torch.uint8, device="cuda")
+    kvq.kv_attn_decode_k2v4(layout, to_dev(q), T, *enc, out, ws, 1 / np.sqrt(D))
+    Kf = k[0].astype(np.float16).astype(np.float64)
+    Vf = v[0].astype(np.float16).astype(np.float64)
+    ref = oracle.k2v4_attn(Kf, Vf, q[0], 1 / np.sqrt(D))
+    got = out.cpu().numpy()[0]
+    for h in range(Hq):
+        assert rel_err(got[h], ref[h]) <= SIMT_TOL
+
+
+def test_config5_full_size(kvq, oracle):
+    """4 sequences x 32768 cells, 2 kv heads x 256, 16 query heads, sinks 8, window 256, gain 1.10."""
+    run_case(kvq, oracle, B=4, H=2, T=32768, D=256, Hq=16, sink=8, window=256, seed=5)
