@@ -97,12 +97,22 @@ __global__ void __launch_bounds__(kMaxD) v4_encode_kernel(const float* __restric
     if (dd != 0.0f) c = min(15, __float2int_rz(__fadd_rn(__fdiv_rn(x, dd), 8.5f)));
     const int hi = __shfl_down_sync(kFull, c, 16);
     uint8_t* blk = v_blocks + ((seq * p.cap + cell) * (p.D / 32) + w) * 18;
-    if (lane < 16) blk[2 + lane] = (uint8_t)(c | (hi << 4));
-    if (lane == 0) {
-        const uint16_t hb = __half_as_ushort(__float2half_rn(dd));
-        blk[0] = (uint8_t)(hb & 0xffu);
-        blk[1] = (uint8_t)(hb >> 8);
+    // one byte per lane: lanes 0..15 the packed codes, lanes 16/17 the two
+    // bytes of the little-endian fp16 d
+    const uint16_t hb = __half_as_ushort(__float2half_rn(dd));
+    uint8_t byte = 0;
+    int at_off = -1;
+    if (lane < 16) {
+        byte = (uint8_t)(c | (hi << 4));
+        at_off = 2 + lane;
+    } else if (lane == 16) {
+        byte = (uint8_t)(hb & 0xffu);
+        at_off = 0;
+    } else if (lane == 17) {
+        byte = (uint8_t)(hb >> 8);
+        at_off = 1;
     }
+    if (at_off >= 0) blk[at_off] = byte;
     const int64_t slot = overlay_slot(cell, p);
     if (slot >= 0) {
         const int64_t o = (seq * p.slots + slot) * p.D + tid;
