@@ -164,6 +164,35 @@ kvq_status kv_attn_decode(kvq_format fmt, const kvq_mla_layout* layout,
                           int64_t max_total_rows, float sm_scale, float* out,
                           void* workspace, size_t workspace_bytes, kvq_path path, void* stream);
 
+/* kv_attn_decode for callers that cannot allocate device memory.  The pages
+ * have no counterpart: this is a convenience of this library.
+ *
+ * Who needs it: a caller that records the decode into a CUDA graph while the
+ * stream is being captured (an allocation made then is not part of the graph,
+ * and cudaMalloc synchronizes the whole device), a plugin whose host engine
+ * owns every device allocation, or a real-time loop that must never block in
+ * an allocator.  Such a caller cannot provide kv_attn_decode's workspace.
+ *
+ * Same arguments and results as kv_attn_decode, without workspace: the split-T
+ * scratch lives in a fixed 32 MiB array inside the library's device memory
+ * (held on every GPU that loads the library, until the process exits).  A
+ * request whose kv_attn_workspace_size exceeds 32 MiB returns
+ * KVQ_ERR_WORKSPACE and launches nothing (the scratch grows with the number
+ * of sequences, not their length: 32 MiB covers 128 heads for batches of up
+ * to 51 sequences of any length).  The first call on each device
+ * looks up the array's device address (cudaGetSymbolAddress, which may load
+ * the library's device code); make that first call before any stream
+ * capture.  All calls share the one array, which keeps the last call's
+ * contents: calls that can overlap on the GPU (other streams, other host
+ * threads) race and must be serialized by the caller.  The device error word
+ * of kv_attn_decode is not readable here; a ragged batch larger than
+ * max_total_rows yields zero outputs for the sequences past the bound. */
+kvq_status kv_attn_decode_noalloc(kvq_format fmt, const kvq_mla_layout* layout,
+                                  const void* q, kvq_dtype q_dtype, int32_t batch, int32_t n_heads,
+                                  const uint8_t* codes, const float* scales, const int64_t* cu_seqlens,
+                                  int64_t max_total_rows, float sm_scale, float* out,
+                                  kvq_path path, void* stream);
+
 /* Bytes of workspace kv_attn_prefill needs. */
 size_t kv_attn_prefill_workspace_size(kvq_format fmt, const kvq_mla_layout* layout, int32_t n_heads,
                                       int64_t n_past, int64_t n_new, kvq_path path);

@@ -79,6 +79,8 @@ def _declare(L):
     L.kv_attn_workspace_size.argtypes = [C.c_int, pl, I32, I32, I64, C.c_int]
     L.kv_attn_decode.restype = C.c_int
     L.kv_attn_decode.argtypes = [C.c_int, pl, P, C.c_int, I32, I32, P, P, P, I64, C.c_float, P, P, S, C.c_int, P]
+    L.kv_attn_decode_noalloc.restype = C.c_int
+    L.kv_attn_decode_noalloc.argtypes = [C.c_int, pl, P, C.c_int, I32, I32, P, P, P, I64, C.c_float, P, C.c_int, P]
     L.kv_attn_prefill_workspace_size.restype = S
     L.kv_attn_prefill_workspace_size.argtypes = [C.c_int, pl, I32, I64, I64, C.c_int]
     L.kv_attn_prefill.restype = C.c_int
@@ -188,6 +190,20 @@ def kv_attn_decode(fmt: int, q, codes, scales, cu_seqlens, out, workspace, max_t
                              _ptr(cu_seqlens, torch.int64, "cu_seqlens"), int(max_total_rows), float(sm_scale),
                              _ptr(out, torch.float32, "out"), _ptr(workspace, torch.uint8, "workspace"),
                              workspace.numel(), path, _stream(stream)), "kv_attn_decode")
+
+
+def kv_attn_decode_noalloc(fmt: int, q, codes, scales, cu_seqlens, out, max_total_rows: int,
+                           sm_scale: float = SM_SCALE_MLA, layout: MLALayout | None = None, path: int = PATH_AUTO,
+                           stream=None):
+    """kv_attn_decode without a caller-provided workspace (the library's fixed
+    32 MiB device scratch is used; concurrent calls race)."""
+    layout = layout or mla_layout()
+    B, H = q.shape[0], q.shape[1]
+    _ok(lib().kv_attn_decode_noalloc(fmt, C.byref(layout), _ptr(q, None, "q"), _qdtype(q), B, H,
+                                     _ptr(codes, torch.uint8, "codes"), _ptr(scales, torch.float32, "scales"),
+                                     _ptr(cu_seqlens, torch.int64, "cu_seqlens"), int(max_total_rows),
+                                     float(sm_scale), _ptr(out, torch.float32, "out"), path, _stream(stream)),
+        "kv_attn_decode_noalloc")
 
 
 def kv_attn_prefill_workspace_size(fmt: int, n_heads: int, n_past: int, n_new: int,
