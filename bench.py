@@ -216,7 +216,7 @@ def run_ours(args, rank, world):
     clocks = sampler.summary()
     # the decode's tensor-core path is bound by the bf16 tensor pipe; the SIMT
     # path by the fp32 FMA pipe (152 SMs x 128 lanes x 2 flop x max SM clock)
-    used_path = "simt" if path in (kvq.PATH_SIMT, kvq.PATH_AUTO) else "tensor"
+    used_path = "tensor" if (path == kvq.PATH_TENSOR or (path == kvq.PATH_AUTO and H % 64 == 0)) else "simt"
     flops = B * T * FLOPS_PER_ROW
     achieved_tf = flops / (decode_ms * 1e-3) / 1e12
     if used_path == "simt":
@@ -228,12 +228,14 @@ def run_ours(args, rank, world):
     else:
         peak = peaks["bf16_tflops"]
         roof = {"bound": "tensor", "achieved": round(achieved_tf, 2), "peak": peak, "unit": "TFLOP/s",
-                "frac": round(achieved_tf / peak, 4), "traffic": None, "peak_source": f"bf16_tflops ({src})",
-                "kernel": "kv_attn_decode"}
+                "frac": round(achieved_tf / peak, 4), "traffic": None,
+                "peak_source": f"bf16_tflops ({src}); f16 operands run at the bf16 dense rate",
+                "kernel": "kv_attn_decode (tcgen05 partial + merge)"}
     line = {
         "metric": METRIC, "value": round(gbs, 3), "unit": "GB/s", "n_gpus": world, "steps": K,
         "warmup": max(args.warmup, 3), "ms_per_step": round(step_ms, 5), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "e4m3 codes, f32 accumulate",
+        "scaling": "weak", "vs_baseline": None, "dtype": "e4m3 codes, f16 tensor-core operands, f32 accumulate" if used_path == "tensor"
+        else "e4m3 codes, f32 accumulate",
         "data": "synthetic (seeded N(0,1) x log-normal channel gains; bf16 queries)",
         "config": {"workload": WORKLOAD, "batch": B, "seq_len": T, "heads": H, "row_bytes": ROW_BYTES,
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",

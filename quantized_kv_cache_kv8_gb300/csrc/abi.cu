@@ -54,8 +54,31 @@ kvq_status cuda_status(cudaError_t e) { return e == cudaSuccess ? KVQ_OK : KVQ_E
 
 kvq_status check_path(kvq_path path) {
     if (path != KVQ_PATH_AUTO && path != KVQ_PATH_SIMT && path != KVQ_PATH_TENSOR) return KVQ_ERR_ARG;
-    if (path == KVQ_PATH_TENSOR) return KVQ_ERR_UNSUPPORTED;
     return KVQ_OK;
+}
+
+// The attention family that runs: AUTO takes the tensor-core kernel when it
+// supports the head count, else the SIMT kernel.  K2/V4 has only SIMT.
+kvq_status resolve_path(kvq_path path, const kvq_mla_layout* L, int32_t n_heads, kvq_path* out) {
+    if (path == KVQ_PATH_SIMT) {
+        *out = KVQ_PATH_SIMT;
+        return KVQ_OK;
+    }
+    const bool tc = tc_supported(*L, n_heads);
+    if (path == KVQ_PATH_TENSOR && !tc) return KVQ_ERR_UNSUPPORTED;
+    *out = tc ? KVQ_PATH_TENSOR : KVQ_PATH_SIMT;
+    return KVQ_OK;
+}
+
+kvq_status check_k2v4_path(kvq_path path) {
+    kvq_status s = check_path(path);
+    if (s != KVQ_OK) return s;
+    return path == KVQ_PATH_TENSOR ? KVQ_ERR_UNSUPPORTED : KVQ_OK;
+}
+
+AttnPlan plan_decode(kvq_path resolved, int32_t batch, int32_t n_heads, int64_t max_total_rows) {
+    return resolved == KVQ_PATH_TENSOR ? plan_decode_tc(batch, n_heads, max_total_rows)
+                                       : plan_decode_simt(batch, n_heads, max_total_rows);
 }
 
 kvq_status check_k2v4(const kvq_k2v4_layout* L) {
@@ -138,7 +161,9 @@ size_t kv_attn_workspace_size(kvq_format fmt, const kvq_mla_layout* layout, int3
                               int64_t max_total_rows, kvq_path path) {
     if (check_attn_layout(fmt, layout) != KVQ_OK || check_path(path) != KVQ_OK) return 0;
     if (batch < 0 || n_heads < 0 || max_total_rows < 0) return 0;
-    const AttnPlan pl = plan_decode_simt(batch, n_heads, max_total_rows);
+    kvq_path rp;
+    if (resolve_path(path, layout, n_heads, &rp) != KVQ_OK) return 0;
+    const AttnPlan pl = plan_decode(rp, batch, n_heads, max_total_rows);
     return kWsHeader + partial_bytes(pl.max_items, n_heads, layout->v_dim);
 }
 
@@ -153,6 +178,8 @@ kvq_status kv_attn_decode(kvq_format fmt, const kvq_mla_layout* layout, const vo
         return KVQ_ERR_ARG;
     if (batch > 65535 || n_heads > 65535) return KVQ_ERR_UNSUPPORTED;
     if (batch == 0 || n_heads == 0) return KVQ_OK;
+    kvq_path rp;
+    if ((s = resolve_path(path, layout, n_heads, &rp)) != KVQ_OK) return s;
     if (!q || !cu_seqlens || !out) return KVQ_ERR_ARG;
     if (max_total_rows > 0 && (!codes || !scales)) return KVQ_ERR_ARG;
     if (!isfinite(sm_scale)) return KVQ_ERR_ARG;
@@ -161,7 +188,10 @@ kvq_status kv_attn_decode(kvq_format fmt, const kvq_mla_layout* layout, const vo
     cudaStream_t st = (cudaStream_t)stream;
     cudaError_t e = cudaMemsetAsync(workspace, 0, sizeof(int32_t), st);
     if (e != cudaSuccess) return KVQ_ERR_CUDA;
-    const AttnPlan pl = plan_decode_simt(batch, n_heads, max_total_rows);
+    const AttnPlan pl = plan_decode(rp, batch, n_heads, max_total_rows);
+    if (rp == KVQ_PATH_TENSOR)
+        return cuda_status(launch_attn_tc(fmt, *layout, q, q_dtype, batch, n_heads, codes, scales, cu_seqlens, -1, pl,
+                                          sm_scale, out, workspace, st));
     return cuda_status(launch_attn_simt(fmt, *layout, q, q_dtype, batch, n_heads, codes, scales, cu_seqlens, -1, pl,
                                         sm_scale, out, workspace, st));
 }
@@ -192,6 +222,8 @@ kvq_status kv_attn_prefill(kvq_format fmt, const kvq_mla_layout* layout, const f
     if (n_past < 0 || n_new < 0 || n_heads < 0 || (q_dtype != KVQ_F32 && q_dtype != KVQ_BF16)) return KVQ_ERR_ARG;
     if (n_new > 65535 || n_heads > 65535) return KVQ_ERR_UNSUPPORTED;
     if (n_new == 0 || n_heads == 0) return KVQ_OK;
+    kvq_path rp;
+    if ((s = resolve_path(path, layout, n_heads, &rp)) != KVQ_OK) return s;
     if (!x_new || !q || !codes || !scales || !out) return KVQ_ERR_ARG;
     if (!isfinite(sm_scale)) return KVQ_ERR_ARG;
     const size_t need = kv_attn_prefill_workspace_size(fmt, layout, n_heads, n_past, n_new, path);
@@ -209,6 +241,9 @@ kvq_status kv_attn_prefill(kvq_format fmt, const kvq_mla_layout* layout, const f
     if (e != cudaSuccess) return KVQ_ERR_CUDA;
     if ((e = cudaMemsetAsync(workspace, 0, sizeof(int32_t), st)) != cudaSuccess) return KVQ_ERR_CUDA;
     const AttnPlan pl = plan_prefill(n_past, n_new);
+    if (rp == KVQ_PATH_TENSOR)
+        return cuda_status(launch_attn_tc(fmt, *layout, q, q_dtype, (int32_t)n_new, n_heads, codes, scales, nullptr,
+                                          n_past, pl, sm_scale, out, workspace, st));
     return cuda_status(launch_attn_simt(fmt, *layout, q, q_dtype, (int32_t)n_new, n_heads, codes, scales, nullptr,
                                         n_past, pl, sm_scale, out, workspace, st));
 }
@@ -242,7 +277,7 @@ kvq_status k2v4_encode(const kvq_k2v4_layout* layout, const float* k, const floa
 
 size_t kv_attn_decode_k2v4_workspace_size(const kvq_k2v4_layout* layout, int32_t batch, int32_t n_q_heads,
                                           int64_t n_cells, kvq_path path) {
-    if (check_k2v4(layout) != KVQ_OK || check_path(path) != KVQ_OK) return 0;
+    if (check_k2v4(layout) != KVQ_OK || check_k2v4_path(path) != KVQ_OK) return 0;
     if (batch < 0 || n_q_heads < 0 || n_cells < 0) return 0;
     const K2V4Plan pl = plan_k2v4(*layout, batch, n_q_heads, n_cells);
     return kWsHeader + k2v4_partial_bytes(*layout, batch, n_q_heads, pl);
@@ -254,7 +289,7 @@ kvq_status kv_attn_decode_k2v4(const kvq_k2v4_layout* layout, const float* q, in
                                float* out, void* workspace, size_t workspace_bytes, kvq_path path, void* stream) {
     kvq_status s = check_k2v4(layout);
     if (s != KVQ_OK) return s;
-    if ((s = check_path(path)) != KVQ_OK) return s;
+    if ((s = check_k2v4_path(path)) != KVQ_OK) return s;
     if (batch < 0 || n_q_heads < 0 || n_cells < 0 || capacity < n_cells) return KVQ_ERR_ARG;
     if (n_q_heads % layout->n_kv_heads != 0) return KVQ_ERR_ARG;
     if (n_q_heads / layout->n_kv_heads > 8) return KVQ_ERR_UNSUPPORTED;

@@ -1,0 +1,126 @@
+// attn_common.cuh -- pieces shared by the SIMT and tensor-core attention paths:
+// the parameter block, the device-side enumeration of split-T work items from
+// cu_seqlens, and the partial-state format the merge kernel consumes.
+//
+// Partial state of one work item (a chunk of rows of one sequence) and head h,
+// in natural-log units: m = max_t z_t over the chunk, l = sum_t exp(z_t - m),
+// o[d] = sum_t exp(z_t - m) * x_hat_t[d] (TQ4: in the rotated domain).
+#pragma once
+
+#include "kvq_internal.cuh"
+
+namespace kvq {
+
+constexpr int kMlaD = 576, kMlaDL = 512, kMlaDR = 64, kMlaDV = 512;
+
+struct AttnParams {
+    int32_t n_blocks;
+    int32_t n_seq, n_heads;
+    const void* q;
+    const uint8_t* codes;
+    const float* scales;
+    const int64_t* cu;      // decode: ragged row offsets
+    int64_t prefill_past;   // prefill: >= 0; token b attends rows [0, past + b]
+    int64_t chunk, max_items;
+    float sm_scale;
+    float* ws_o;            // [max_items][n_heads][512]
+    float* ws_ml;           // [max_items][n_heads][2]
+    int32_t* err;
+    SignWords signs;
+    float kn[2];
+    float lv[16];
+};
+
+__device__ __forceinline__ void set_err(int32_t* err, int32_t code) { atomicCAS(err, 0, code); }
+
+// Number of chunks of sequence b (0 for an empty or malformed range).
+__device__ __forceinline__ int64_t n_chunks_of(const int64_t* cu, int b, int64_t chunk, int32_t* err) {
+    const int64_t len = cu[b + 1] - cu[b];
+    if (len < 0) {
+        set_err(err, KVQ_ERR_ARG);
+        return 0;
+    }
+    return (len + chunk - 1) / chunk;
+}
+
+// Warp-cooperative search for the sequence owning work item `item`.
+// Returns b (or -1) and the chunk index within b.
+__device__ __forceinline__ int find_item(const int64_t* cu, int n_seq, int64_t chunk, int64_t item, int lane,
+                                         int64_t* ch_out, int32_t* err) {
+    int64_t base = 0;
+    for (int b0 = 0; b0 < n_seq; b0 += 32) {
+        const int b = b0 + lane;
+        const int64_t n = b < n_seq ? n_chunks_of(cu, b, chunk, err) : 0;
+        int64_t incl = n;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int64_t t = __shfl_up_sync(kFull, incl, o);
+            if (lane >= o) incl += t;
+        }
+        const int64_t total = __shfl_sync(kFull, incl, 31);
+        if (item < base + total) {
+            const int64_t excl = incl - n;
+            const bool mine = b < n_seq && item >= base + excl && item < base + incl;
+            const unsigned mask = __ballot_sync(kFull, mine);
+            const int src = __ffs(mask) - 1;
+            *ch_out = item - base - __shfl_sync(kFull, excl, src);
+            return b0 + src;
+        }
+        base += total;
+    }
+    return -1;
+}
+
+// First work item of sequence b and its chunk count.
+__device__ __forceinline__ void seq_items(const int64_t* cu, int b, int64_t chunk, int lane, int64_t* first,
+                                          int64_t* count, int32_t* err) {
+    int64_t acc = 0;
+    for (int b0 = 0; b0 < b; b0 += 32) {
+        const int bb = b0 + lane;
+        int64_t n = bb < b ? n_chunks_of(cu, bb, chunk, err) : 0;
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) n += __shfl_xor_sync(kFull, n, o);
+        acc += n;
+    }
+    *first = acc;
+    *count = n_chunks_of(cu, b, chunk, err);
+}
+
+// Locates this CTA's work item (warp 0 calls it); returns the sequence (or -1)
+// and the row range [row0, row1) of the chunk.
+__device__ __forceinline__ int locate_item(const AttnParams& p, int64_t item, int lane, int64_t* row0,
+                                           int64_t* row1) {
+    int b = -1;
+    int64_t ch = 0;
+    if (p.prefill_past >= 0) {
+        if (item < p.n_seq) b = (int)item;
+    } else {
+        b = find_item(p.cu, p.n_seq, p.chunk, item, lane, &ch, p.err);
+    }
+    if (b >= 0) {
+        if (p.prefill_past >= 0) {
+            *row0 = 0;
+            *row1 = p.prefill_past + b + 1;
+        } else {
+            const int64_t s = p.cu[b], e = p.cu[b + 1];
+            *row0 = s + ch * p.chunk;
+            *row1 = min(*row0 + p.chunk, e);
+        }
+    }
+    return b;
+}
+
+template <bool QBF16>
+__device__ __forceinline__ float load_q(const void* q, int64_t idx) {
+    if (QBF16) return __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(q)[idx]);
+    return reinterpret_cast<const float*>(q)[idx];
+}
+
+AttnParams make_attn_params(kvq_format fmt, const kvq_mla_layout& L, const void* q, int32_t n_seq, int32_t n_heads,
+                            const uint8_t* codes, const float* scales, const int64_t* cu_seqlens,
+                            int64_t prefill_past, const AttnPlan& plan, float sm_scale, void* workspace);
+
+// LSE merge of the chunk partials into out[n_seq][n_heads][512] (TQ4: unrotated).
+cudaError_t launch_attn_merge(kvq_format fmt, const AttnParams& p, float* out, cudaStream_t stream);
+
+}  // namespace kvq

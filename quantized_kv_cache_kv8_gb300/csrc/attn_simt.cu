@@ -16,7 +16,7 @@
 // context weight of row t is p_t * s_L: the scale is factored out of both sums.
 // For TQ4 the query is rotated in shared memory first ([P1] "Ready for
 // review" comment, finding 2).
-#include "kvq_internal.cuh"
+#include "attn_common.cuh"
 
 #include <algorithm>
 #include <math.h>
@@ -24,93 +24,14 @@
 namespace kvq {
 namespace {
 
-constexpr int kD = 576, kDL = 512, kDR = 64, kDV = 512;
+constexpr int kD = kMlaD, kDL = kMlaDL, kDV = kMlaDV;
 constexpr int kHG = 16;   // heads per CTA
 constexpr int kTR = 16;   // rows per tile
 constexpr int kNT = 256;  // threads per CTA
 constexpr int kXS = 580;  // shared-memory row stride in floats (bank spread)
 constexpr int kSmSMs = 152;
 
-struct AttnParams {
-    int32_t n_blocks;
-    int32_t n_seq, n_heads;
-    const void* q;
-    const uint8_t* codes;
-    const float* scales;
-    const int64_t* cu;      // decode: ragged row offsets
-    int64_t prefill_past;   // prefill: >= 0; token b attends rows [0, past + b]
-    int64_t chunk, max_items;
-    float sm_scale;
-    float* ws_o;            // [max_items][n_heads][kDV]
-    float* ws_ml;           // [max_items][n_heads][2]
-    int32_t* err;
-    SignWords signs;
-    float kn[2];
-    float lv[16];
-};
-
-constexpr size_t kSmemFloats = (size_t)kHG * kXS + (size_t)kTR * kXS + kTR * 2 + kTR * kHG + kHG + 16 + 4;
-
-__device__ __forceinline__ void set_err(int32_t* err, int32_t code) { atomicCAS(err, 0, code); }
-
-// Number of chunks of sequence b (0 for an empty or malformed range).
-__device__ __forceinline__ int64_t n_chunks_of(const int64_t* cu, int b, int64_t chunk, int32_t* err) {
-    const int64_t len = cu[b + 1] - cu[b];
-    if (len < 0) {
-        set_err(err, KVQ_ERR_ARG);
-        return 0;
-    }
-    return (len + chunk - 1) / chunk;
-}
-
-// Warp-cooperative search for the sequence owning work item `item`.
-// Returns b (or -1) and the chunk index within b.
-__device__ int find_item(const int64_t* cu, int n_seq, int64_t chunk, int64_t item, int lane, int64_t* ch_out,
-                         int32_t* err) {
-    int64_t base = 0;
-    for (int b0 = 0; b0 < n_seq; b0 += 32) {
-        const int b = b0 + lane;
-        const int64_t n = b < n_seq ? n_chunks_of(cu, b, chunk, err) : 0;
-        int64_t incl = n;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int64_t t = __shfl_up_sync(kFull, incl, o);
-            if (lane >= o) incl += t;
-        }
-        const int64_t total = __shfl_sync(kFull, incl, 31);
-        if (item < base + total) {
-            const int64_t excl = incl - n;
-            const bool mine = b < n_seq && item >= base + excl && item < base + incl;
-            const unsigned mask = __ballot_sync(kFull, mine);
-            const int src = __ffs(mask) - 1;
-            *ch_out = item - base - __shfl_sync(kFull, excl, src);
-            return b0 + src;
-        }
-        base += total;
-    }
-    return -1;
-}
-
-// First work item of sequence b and its chunk count.
-__device__ void seq_items(const int64_t* cu, int b, int64_t chunk, int lane, int64_t* first, int64_t* count,
-                          int32_t* err) {
-    int64_t acc = 0;
-    for (int b0 = 0; b0 < b; b0 += 32) {
-        const int bb = b0 + lane;
-        int64_t n = bb < b ? n_chunks_of(cu, bb, chunk, err) : 0;
-#pragma unroll
-        for (int o = 16; o >= 1; o >>= 1) n += __shfl_xor_sync(kFull, n, o);
-        acc += n;
-    }
-    *first = acc;
-    *count = n_chunks_of(cu, b, chunk, err);
-}
-
-template <bool QBF16>
-__device__ __forceinline__ float load_q(const void* q, int64_t idx) {
-    if (QBF16) return __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(q)[idx]);
-    return reinterpret_cast<const float*>(q)[idx];
-}
+constexpr size_t kSmemFloats = (size_t)kHG * kXS + (size_t)kTR * kXS + kTR * 2 + kTR * kHG + kHG + 16 + 6;
 
 template <int FMT, bool QBF16>
 __global__ void __launch_bounds__(kNT, 2) attn_partial_kernel(AttnParams p) {
@@ -126,34 +47,20 @@ __global__ void __launch_bounds__(kNT, 2) attn_partial_kernel(AttnParams p) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int64_t item = blockIdx.x;
     const int h0 = blockIdx.y * kHG;
-    const bool prefill = p.prefill_past >= 0;
-
     if (warp == 0) {
-        int b = -1;
-        int64_t ch = 0;
-        if (prefill) {
-            if (item < p.n_seq) b = (int)item;
-        } else {
-            b = find_item(p.cu, p.n_seq, p.chunk, item, lane, &ch, p.err);
-        }
+        int64_t r0 = 0, r1 = 0;
+        const int b = locate_item(p, item, lane, &r0, &r1);
         if (lane == 0) {
             info[0] = b;
-            info[1] = ch;
+            info[1] = r0;
+            info[2] = r1;
         }
     }
     if (tid < 16) lvs[tid] = p.lv[tid];
     __syncthreads();
     const int b = (int)info[0];
     if (b < 0) return;
-    int64_t row0, row1;
-    if (prefill) {
-        row0 = 0;
-        row1 = p.prefill_past + b + 1;
-    } else {
-        const int64_t s = p.cu[b], e = p.cu[b + 1];
-        row0 = s + info[1] * p.chunk;
-        row1 = min(row0 + p.chunk, e);
-    }
+    const int64_t row0 = info[1], row1 = info[2];
 
     // queries of this head group -> shared memory, f32
     for (int i = tid; i < kHG * kD; i += kNT) {
@@ -423,15 +330,9 @@ AttnPlan plan_decode_simt(int32_t batch, int32_t n_heads, int64_t max_total_rows
     return pl;
 }
 
-size_t partial_bytes(int64_t max_items, int32_t n_heads, int32_t v_dim) {
-    return (size_t)max_items * n_heads * (v_dim + 2) * sizeof(float);
-}
-
-cudaError_t launch_attn_simt(kvq_format fmt, const kvq_mla_layout& L, const void* q, kvq_dtype qdt, int32_t n_seq,
-                             int32_t n_heads, const uint8_t* codes, const float* scales, const int64_t* cu_seqlens,
-                             int64_t prefill_past, const AttnPlan& plan, float sm_scale, float* out,
-                             void* workspace, cudaStream_t stream) {
-    if (n_seq == 0 || n_heads == 0) return cudaSuccess;
+AttnParams make_attn_params(kvq_format fmt, const kvq_mla_layout& L, const void* q, int32_t n_seq, int32_t n_heads,
+                            const uint8_t* codes, const float* scales, const int64_t* cu_seqlens,
+                            int64_t prefill_past, const AttnPlan& plan, float sm_scale, void* workspace) {
     AttnParams p{};
     p.n_blocks = L.n_blocks;
     p.n_seq = n_seq;
@@ -447,7 +348,7 @@ cudaError_t launch_attn_simt(kvq_format fmt, const kvq_mla_layout& L, const void
     char* ws = static_cast<char*>(workspace);
     p.err = reinterpret_cast<int32_t*>(ws);
     p.ws_o = reinterpret_cast<float*>(ws + kWsHeader);
-    p.ws_ml = p.ws_o + (size_t)plan.max_items * n_heads * kDV;
+    p.ws_ml = p.ws_o + (size_t)plan.max_items * n_heads * kMlaDV;
     if (fmt == KVQ_TQ4) {
         p.signs = tq4_sign_words(L);
         p.kn[0] = (float)(1.0 / sqrt((double)L.block_dim[0]));
@@ -455,6 +356,20 @@ cudaError_t launch_attn_simt(kvq_format fmt, const kvq_mla_layout& L, const void
         const Codebook16 cb = tq4_codebook();
         for (int k = 0; k < 16; ++k) p.lv[k] = cb.lv[k];
     }
+    return p;
+}
+
+size_t partial_bytes(int64_t max_items, int32_t n_heads, int32_t v_dim) {
+    return (size_t)max_items * n_heads * (v_dim + 2) * sizeof(float);
+}
+
+cudaError_t launch_attn_simt(kvq_format fmt, const kvq_mla_layout& L, const void* q, kvq_dtype qdt, int32_t n_seq,
+                             int32_t n_heads, const uint8_t* codes, const float* scales, const int64_t* cu_seqlens,
+                             int64_t prefill_past, const AttnPlan& plan, float sm_scale, float* out,
+                             void* workspace, cudaStream_t stream) {
+    if (n_seq == 0 || n_heads == 0) return cudaSuccess;
+    const AttnParams p = make_attn_params(fmt, L, q, n_seq, n_heads, codes, scales, cu_seqlens, prefill_past, plan,
+                                          sm_scale, workspace);
     const int groups = (n_heads + kHG - 1) / kHG;
     cudaError_t e;
     if (fmt == KVQ_KV8)
@@ -464,10 +379,14 @@ cudaError_t launch_attn_simt(kvq_format fmt, const kvq_mla_layout& L, const void
         e = qdt == KVQ_BF16 ? launch_partial<KVQ_TQ4, true>(p, plan.max_items, groups, stream)
                             : launch_partial<KVQ_TQ4, false>(p, plan.max_items, groups, stream);
     if (e != cudaSuccess) return e;
+    return launch_attn_merge(fmt, p, out, stream);
+}
+
+cudaError_t launch_attn_merge(kvq_format fmt, const AttnParams& p, float* out, cudaStream_t stream) {
     if (fmt == KVQ_KV8)
-        attn_merge_kernel<KVQ_KV8><<<dim3(n_heads, n_seq), 128, 0, stream>>>(p, out);
+        attn_merge_kernel<KVQ_KV8><<<dim3(p.n_heads, p.n_seq), 128, 0, stream>>>(p, out);
     else
-        attn_merge_kernel<KVQ_TQ4><<<dim3(n_heads, n_seq), 128, 0, stream>>>(p, out);
+        attn_merge_kernel<KVQ_TQ4><<<dim3(p.n_heads, p.n_seq), 128, 0, stream>>>(p, out);
     return cudaGetLastError();
 }
 

@@ -150,6 +150,14 @@ cudaError_t launch_attn_simt(kvq_format fmt, const kvq_mla_layout& L, const void
                              int64_t prefill_past, const AttnPlan& plan, float sm_scale, float* out,
                              void* workspace, cudaStream_t stream);
 
+// Tensor-core attention (tcgen05, 64 heads per CTA).
+bool tc_supported(const kvq_mla_layout& L, int32_t n_heads);
+AttnPlan plan_decode_tc(int32_t batch, int32_t n_heads, int64_t max_total_rows);
+cudaError_t launch_attn_tc(kvq_format fmt, const kvq_mla_layout& L, const void* q, kvq_dtype qdt, int32_t n_seq,
+                           int32_t n_heads, const uint8_t* codes, const float* scales, const int64_t* cu_seqlens,
+                           int64_t prefill_past, const AttnPlan& plan, float sm_scale, float* out, void* workspace,
+                           cudaStream_t stream);
+
 // K2/V4
 cudaError_t launch_k2v4_encode(const kvq_k2v4_layout& L, const float* k, const float* v, int32_t batch,
                                int64_t n_cells, int64_t cap, uint8_t* k_codes, uint16_t* k_scales,

@@ -7,7 +7,7 @@ import numpy as np
 import pytest
 import torch
 
-from gpu_common import SIMT_TOL, gpu_encode, kvq_module, queries, rel_err, to_dev
+from gpu_common import SIMT_TOL, TENSOR_TOL, gpu_encode, kvq_module, queries, rel_err, to_dev
 from quantized_kv_cache_kv8_gb300 import synth
 
 pytestmark = pytest.mark.gpu
@@ -75,14 +75,42 @@ def test_single_scale_kv8_layout(kvq, oracle):
         assert rel_err(got[b, h], r) <= SIMT_TOL
 
 
+@pytest.mark.parametrize("path", ["simt", "tensor"])
 @pytest.mark.parametrize("fmt", [1, 2])
-def test_config2_3_full_size_sampled(kvq, oracle, fmt):
+def test_config2_3_full_size_sampled(kvq, oracle, fmt, path):
     """8 sequences x 4096 rows, 128 heads, bf16 query (KV8 = config 2, TQ4 = config 3)."""
     lens = [4096] * 8
-    x, cu, qv, got, _ = run_decode(kvq, fmt, lens, 128, True, 2 if fmt == 1 else 3, kvq.PATH_SIMT)
-    pairs = [(b, h) for b in range(8) for h in (0, 37, 127)]
-    check_decode(oracle, fmt, x, cu, qv, got, pairs=pairs, seed=2 if fmt == 1 else 3)
+    pth = kvq.PATH_SIMT if path == "simt" else kvq.PATH_TENSOR
+    x, cu, qv, got, _ = run_decode(kvq, fmt, lens, 128, True, 2 if fmt == 1 else 3, pth)
+    pairs = [(b, h) for b in range(8) for h in (0, 37, 64, 127)]
+    check_decode(oracle, fmt, x, cu, qv, got, pairs=pairs, seed=2 if fmt == 1 else 3,
+                 tol=SIMT_TOL if path == "simt" else TENSOR_TOL)
     assert np.all(np.isfinite(got))
+
+
+@pytest.mark.parametrize("fmt", [1, 2])
+@pytest.mark.parametrize("bf16", [False, True])
+def test_tensor_ragged_with_edges(kvq, oracle, fmt, bf16):
+    """Tensor-core path: ragged lengths with an empty, a one-row and tail-tile sequences, 128 heads."""
+    lens = [1, 0, 127, 129, 700, 256, 3000]
+    x, cu, qv, got, ws = run_decode(kvq, fmt, lens, 128, bf16, 13, kvq.PATH_TENSOR)
+    pairs = [(b, h) for b in range(len(lens)) for h in (0, 31, 32, 63, 64, 100, 127)]
+    check_decode(oracle, fmt, x, cu, qv, got, pairs=pairs, seed=13, tol=TENSOR_TOL)
+    assert np.all(got[1] == 0.0)
+    assert np.all(np.isfinite(got))
+    assert kvq.read_device_error(ws) == 0
+
+
+def test_tensor_matches_simt_closely(kvq):
+    """The two kernel families on the same inputs agree to the tensor path's tolerance."""
+    lens = [777, 2048, 5]
+    outs = []
+    for pth in (kvq.PATH_SIMT, kvq.PATH_TENSOR):
+        _, _, _, got, _ = run_decode(kvq, 1, lens, 64, True, 17, pth)
+        outs.append(got)
+    for b in range(3):
+        for h in range(64):
+            assert rel_err(outs[1][b, h], outs[0][b, h]) <= TENSOR_TOL
 
 
 def test_device_error_when_rows_exceed_bound(kvq):
@@ -94,9 +122,11 @@ def test_device_error_when_rows_exceed_bound(kvq):
     assert kvq.read_device_error(ws) == 0             # cleared by the first read
 
 
-@pytest.mark.parametrize("fmt", [1, 2])
-def test_prefill_small(kvq, oracle, fmt):
-    n_past, n_new, H = 200, 37, 16
+@pytest.mark.parametrize("fmt,H,path", [(1, 16, "simt"), (2, 16, "simt"), (1, 64, "tensor"), (2, 64, "tensor")])
+def test_prefill_small(kvq, oracle, fmt, H, path):
+    n_past, n_new = 200, 37
+    pth = kvq.PATH_SIMT if path == "simt" else kvq.PATH_TENSOR
+    tol = SIMT_TOL if path == "simt" else TENSOR_TOL
     layout = kvq.mla_layout(seed=4)
     x_all = synth.mla_rows(31, n_past + n_new)
     row = 576 if fmt == 1 else 288
@@ -107,9 +137,9 @@ def test_prefill_small(kvq, oracle, fmt):
     scales[:n_past] = ps
     qd, qv = queries(32, (n_new, H, 576), False)
     out = torch.empty((n_new, H, 512), device="cuda")
-    ws = torch.empty(kvq.kv_attn_prefill_workspace_size(fmt, H, n_past, n_new, layout), dtype=torch.uint8,
+    ws = torch.empty(kvq.kv_attn_prefill_workspace_size(fmt, H, n_past, n_new, layout, pth), dtype=torch.uint8,
                      device="cuda")
-    kvq.kv_attn_prefill(fmt, to_dev(x_all[n_past:]), qd, codes, scales, n_past, out, ws, SM, layout)
+    kvq.kv_attn_prefill(fmt, to_dev(x_all[n_past:]), qd, codes, scales, n_past, out, ws, SM, layout, pth)
     torch.cuda.synchronize()
     if fmt == 1:
         oc, os_ = oracle.kv8_encode(x_all)
@@ -121,4 +151,4 @@ def test_prefill_small(kvq, oracle, fmt):
     for j in range(n_new):
         ref = oracle.attn_dense(xh[:n_past + j + 1], qv[j], SM, 512)
         for h in range(H):
-            assert rel_err(got[j, h], ref[h]) <= SIMT_TOL, (j, h)
+            assert rel_err(got[j, h], ref[h]) <= tol, (j, h)
