@@ -37,7 +37,8 @@ namespace {
 
 constexpr int kRows = 128;      // rows per tile: the score's M, the context's K
 constexpr int kHC = 64;         // heads per CTA: the MMA N
-constexpr int kThreads = 256;
+constexpr int kWorkers = 256;   // 8 warps: conversion, softmax, epilogue
+constexpr int kThreads = kWorkers + 32;   // + 1 warp whose lane 0 issues every MMA
 constexpr int kSlots = 4;       // f16 staging slots of 128 rows x 64 dims
 constexpr uint32_t kSlotBytes = kRows * 128;
 // query chunk kc (64 dims): rows 0..63 = f16(q) of the 64 heads, rows 64..127 =
@@ -46,13 +47,12 @@ constexpr uint32_t kQChunkBytes = 2 * kHC * 128;
 constexpr uint32_t kOffQ = 0;
 constexpr uint32_t kOffSlot = kOffQ + 9 * kQChunkBytes;
 constexpr uint32_t kOffP = kOffSlot + kSlots * kSlotBytes;
-constexpr uint32_t kOffScale = kOffP + kRows * 128;
-constexpr uint32_t kOffM = kOffScale + kRows * 8;
+constexpr uint32_t kOffM = kOffP + kRows * 128;
 constexpr uint32_t kOffAlpha = kOffM + kHC * 4;
 constexpr uint32_t kOffLut = kOffAlpha + kHC * 4;
 constexpr uint32_t kOffBar = kOffLut + 256 * 4;
-constexpr uint32_t kOffMisc = kOffBar + 8 * 8;   // abort flag, TMEM base, item info, reductions
-constexpr uint32_t kSmemUsed = kOffMisc + 128;
+constexpr uint32_t kOffMisc = kOffBar + 16 * 8;   // abort flag, TMEM base, item info, reductions, TQ4 residuals
+constexpr uint32_t kSmemUsed = kOffMisc + 160;
 constexpr size_t kSmemAlloc = kSmemUsed;          // the base is 1024-aligned (checked at run time)
 static_assert(kSmemAlloc <= 232448, "shared memory budget");
 
@@ -61,9 +61,11 @@ static_assert(kSmemAlloc <= 232448, "shared memory budget");
 constexpr uint32_t kColO = 0, kColSL = 256, kColSR = 384, kTmemCols = 512;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
-constexpr long long kWaitLimit = 1ll << 24;
+constexpr long long kWaitLimit = 1ll << 22;
 
-enum { kBarSlot0 = 0, kBarScore = 4, kBarCtx = 5 };
+// mbarriers: slot full (256 worker arrivals), slot empty (MMA commit), score
+// done, context done (MMA commits), P^T ready (256 worker arrivals)
+enum { kBarFull0 = 0, kBarEmpty0 = 4, kBarScore = 8, kBarCtx = 9, kBarP = 10, kNumBars = 11 };
 
 __host__ __device__ constexpr uint32_t idesc_f16(int M, int N, bool a_mn, bool b_mn) {
     // D f32 (bit 4), A and B f16 (format 0), operand majors, N>>3 at 17, M>>4 at 24
@@ -123,6 +125,30 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
     return false;
 }
 
+// Barrier 1 among the 256 worker threads only (the MMA warp never joins it).
+__device__ __forceinline__ void worker_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+__device__ __forceinline__ bool worker_any(bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.or.pred q, 1, 256, p;\n selp.u32 %0, 1, 0, q;\n}\n"
+        : "=r"(r)
+        : "r"((uint32_t)v)
+        : "memory");
+    return r != 0;
+}
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gmem_src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem_dst)), "l"(gmem_src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
 #define KVQ_R32(v) \
     "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]), "=r"(v[8]), \
         "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]), "=r"(v[16]),   \
@@ -156,26 +182,58 @@ __device__ __forceinline__ uint32_t e4m3x2_to_half2_bits(uint32_t two) {
     return (uint32_t)h.x | ((uint32_t)h.y << 16);
 }
 
-// Decodes dims [64 kc, 64 kc + 64) of the tile's 128 rows to f16 code values in
-// a staging slot (row r = one 128-byte swizzled row).  Rows past the end are 0.
+// The raw bytes one thread converts for one chunk: dims [64 kc, 64 kc + 64) of
+// row (tid / 2), half (tid % 2) of them.  KV8: 32 bytes (a, b); TQ4: 16 (a).
+struct RawChunk {
+    uint4 a, b;
+};
+
+// Each tile is consumed as a fixed stream of 17 chunk steps: the 9 score
+// chunks (dims 0..575), then the 8 context chunks (dims 0..511).  Loads are
+// issued several steps ahead of their use so that DRAM latency overlaps the
+// conversion and the MMAs of the steps in between.
+constexpr int kStepsPerTile = 17;
+
 template <int FMT>
-__device__ __forceinline__ void decode_chunk(const uint8_t* __restrict__ codes, int64_t t0, int nt, int kc,
-                                             unsigned char* slot, const uint32_t* lut, int tid) {
+__device__ __forceinline__ RawChunk load_step(const uint8_t* __restrict__ codes, int64_t row0, int64_t row1,
+                                              int64_t step, int tid) {
+    const int64_t tile = step / kStepsPerTile;
+    const int j = (int)(step - tile * kStepsPerTile);
+    const int kc = j < 9 ? j : j - 9;
+    const int64_t row = row0 + tile * kRows + (tid >> 1);
+    const int half = tid & 1;
+    RawChunk c;
+    c.a = c.b = make_uint4(0u, 0u, 0u, 0u);
+    if (row < row1) {
+        if (FMT == KVQ_KV8) {
+            const uint4* src = reinterpret_cast<const uint4*>(codes + row * kMlaD + kc * 64 + half * 32);
+            c.a = __ldg(src);
+            c.b = __ldg(src + 1);
+        } else {
+            c.a = __ldg(reinterpret_cast<const uint4*>(codes + row * (kMlaD / 2) + kc * 32 + half * 16));
+        }
+    }
+    return c;
+}
+
+// Converts a thread's raw chunk to f16 code values (e4m3 value, or TQ4 level)
+// in a staging slot: row r = one 128-byte swizzled row.  Rows past the tile's
+// end are written as zeros.
+template <int FMT>
+__device__ __forceinline__ void store_chunk(const RawChunk& c, bool valid, unsigned char* slot, const uint32_t* lut,
+                                            int tid) {
     const int r = tid >> 1, half = tid & 1;
     uint32_t w[16];
-    if (r < nt) {
+    if (valid) {
         if (FMT == KVQ_KV8) {
-            const uint4* src = reinterpret_cast<const uint4*>(codes + (t0 + r) * kMlaD + kc * 64 + half * 32);
-            const uint4 a = __ldg(src), b = __ldg(src + 1);
-            const uint32_t in[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+            const uint32_t in[8] = {c.a.x, c.a.y, c.a.z, c.a.w, c.b.x, c.b.y, c.b.z, c.b.w};
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
                 w[2 * i] = e4m3x2_to_half2_bits(in[i] & 0xffffu);
                 w[2 * i + 1] = e4m3x2_to_half2_bits(in[i] >> 16);
             }
         } else {
-            const uint4 a = __ldg(reinterpret_cast<const uint4*>(codes + (t0 + r) * (kMlaD / 2) + kc * 32 + half * 16));
-            const uint32_t in[4] = {a.x, a.y, a.z, a.w};
+            const uint32_t in[4] = {c.a.x, c.a.y, c.a.z, c.a.w};
 #pragma unroll
             for (int i = 0; i < 4; ++i)
 #pragma unroll
@@ -192,14 +250,13 @@ __device__ __forceinline__ void decode_chunk(const uint8_t* __restrict__ codes, 
 }
 
 // TQ4: the f16 rounding residual of each code's level (level - f16(level)),
-// same layout as decode_chunk.  Residuals are below 4e-4 of the level.
-__device__ __forceinline__ void decode_delta_chunk(const uint8_t* __restrict__ codes, int64_t t0, int nt, int kc,
-                                                   unsigned char* slot, const __half* delta, int tid) {
+// same layout as store_chunk.  Residuals are below 4e-4 of the level.
+__device__ __forceinline__ void store_delta_chunk(const RawChunk& c, bool valid, unsigned char* slot,
+                                                  const __half* delta, int tid) {
     const int r = tid >> 1, half = tid & 1;
     uint32_t w[16];
-    if (r < nt) {
-        const uint4 a = __ldg(reinterpret_cast<const uint4*>(codes + (t0 + r) * (kMlaD / 2) + kc * 32 + half * 16));
-        const uint32_t in[4] = {a.x, a.y, a.z, a.w};
+    if (valid) {
+        const uint32_t in[4] = {c.a.x, c.a.y, c.a.z, c.a.w};
 #pragma unroll
         for (int i = 0; i < 4; ++i)
 #pragma unroll
@@ -218,14 +275,17 @@ __device__ __forceinline__ void decode_delta_chunk(const uint8_t* __restrict__ c
             make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
 }
 
-template <int FMT, bool QBF16>
+// LOQ: the query needs its f16 residual rows (f32 queries, or TQ4's rotated
+// queries).  Without them (KV8 with a bf16 query, exact in f16) the residual
+// half of the query area holds a 5-stage cp.async ring of raw code chunks.
+constexpr int kRing = 5;      // stages; chunk k + 4 is copied while chunk k is converted
+template <int FMT, bool QBF16, bool LOQ>
 __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnParams p) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char* sm = smem_raw;
     unsigned char* sQ = sm + kOffQ;
     unsigned char* sSlot = sm + kOffSlot;
     unsigned char* sP = sm + kOffP;
-    float2* sScale = reinterpret_cast<float2*>(sm + kOffScale);
     float* sM = reinterpret_cast<float*>(sm + kOffM);
     float* sAlpha = reinterpret_cast<float*>(sm + kOffAlpha);
     uint32_t* sLut = reinterpret_cast<uint32_t*>(sm + kOffLut);
@@ -234,8 +294,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnParams p) {
     uint32_t* sTmem = reinterpret_cast<uint32_t*>(sm + kOffMisc + 4);
     int* sHasLo = reinterpret_cast<int*>(sm + kOffMisc + 8);
     int64_t* sInfo = reinterpret_cast<int64_t*>(sm + kOffMisc + 16);
-    float* sRed = reinterpret_cast<float*>(sm + kOffMisc + 48);
-    __half* sDelta = reinterpret_cast<__half*>(sm + kOffMisc + 80);   // TQ4: level - f16(level)
+    float* sRed = reinterpret_cast<float*>(sm + kOffMisc + 48);       // 16 floats
+    __half* sDelta = reinterpret_cast<__half*>(sm + kOffMisc + 112);  // TQ4: level - f16(level)
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int64_t item = blockIdx.x;
@@ -258,6 +318,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnParams p) {
     const int b = (int)sInfo[0];
     if (b < 0) return;   // past the last work item: nothing allocated yet
     const int64_t row0 = sInfo[1], row1 = sInfo[2];
+    const int n_tiles = (int)((row1 - row0 + kRows - 1) / kRows);
 
     if (warp == 1) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(sTmem)),
@@ -265,50 +326,120 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnParams p) {
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
     }
     if (tid == 64) {
-        for (int i = 0; i < 6; ++i)
-            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&bars[i])));
+        for (int i = 0; i < kNumBars; ++i) {
+            const uint32_t count = (i < kBarEmpty0 || i == kBarP) ? (uint32_t)kWorkers : 1u;
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(&bars[i])), "r"(count));
+        }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         *sAbort = 0;
         *sHasLo = 0;
     }
     if (tid < kHC) sM[tid] = -INFINITY;
-    if (FMT == KVQ_TQ4) {
+    if (FMT == KVQ_TQ4 && tid < 256) {
         const int lo = tid & 15, hi = tid >> 4;
         const __half2 h2 = __halves2half2(__float2half_rn(p.lv[lo]), __float2half_rn(p.lv[hi]));
         sLut[tid] = *reinterpret_cast<const uint32_t*>(&h2);
         if (tid < 16) sDelta[tid] = __float2half_rn(p.lv[tid] - __half2float(__float2half_rn(p.lv[tid])));
     }
 
-    // reference scale of the chunk: a power of two >= every latent scale, so
-    // that the context weights p * s_L / S_ref stay within f16 range
-    float smax = 0.0f;
-    for (int64_t r = row0 + tid; r < row1; r += kThreads) smax = fmaxf(smax, p.scales[r * p.n_blocks]);
-    smax = warp_max(smax);
-    if (lane == 0) sRed[warp] = smax;
-    // query norm bound of the CTA's heads: fixes one power-of-two prescale
-    // keeping every f16 query element below 2^14
-    float qn = 0.0f;
-    for (int h = warp; h < kHC; h += kThreads / 32) {
-        float ss = 0.0f;
-        for (int d = lane; d < kMlaD; d += 32) {
-            const float v = load_q<QBF16>(p.q, ((int64_t)b * p.n_heads + hbase + h) * kMlaD + d);
-            ss = fmaf(v, v, ss);
+    // workers: the first chunk copies go out now and overlap the query prologue
+    const int wt = tid < kWorkers ? tid : 0;
+    const int wrow = wt >> 1, whalf = wt & 1;
+    int64_t step = 0;
+    // raw ring stage k: the residual half of query chunk k (free when !LOQ)
+    auto ring_ptr = [&](int64_t k) -> unsigned char* {
+        return sQ + (int)(k % kRing) * kQChunkBytes + kHC * 128 + wrow * 64 + whalf * 32;
+    };
+    auto issue_copy = [&](int64_t k) {
+        const int64_t tl = k / kStepsPerTile;
+        const int j = (int)(k - tl * kStepsPerTile);
+        const int kc = j < 9 ? j : j - 9;
+        const int64_t row = row0 + tl * kRows + wrow;
+        if (row < row1) {
+            const uint8_t* src = p.codes + row * kMlaD + kc * 64 + whalf * 32;
+            unsigned char* dst = ring_ptr(k);
+            cp_async16(dst, src);
+            cp_async16(dst + 16, src + 16);
         }
-        qn = fmaxf(qn, sqrtf(warp_sum(ss)));
+        cp_async_commit();
+    };
+    if (!LOQ && tid < kWorkers) {
+        for (int k = 0; k < kRing - 1; ++k) issue_copy(k);
+    }
+    if (tid == 0) {
+        // the first tile's bytes (contiguous rows) into L2
+        const int64_t n = min((int64_t)kRows, row1 - row0);
+        const int row_bytes = FMT == KVQ_KV8 ? kMlaD : kMlaD / 2;
+        prefetch_l2(p.codes + row0 * row_bytes, (uint32_t)(n * row_bytes));
+    }
+    // the raw chunk of step `step`: from the ring (after its copy group lands)
+    // or, with LOQ, straight from global memory (L2-prefetched one tile ahead)
+#define KVQ_NEXT_CHUNK(dst)                                                       \
+    do {                                                                          \
+        if (!LOQ) {                                                               \
+            issue_copy(step + kRing - 1);                                         \
+            cp_async_wait<kRing - 1>();                                           \
+            const uint4* src_ = reinterpret_cast<const uint4*>(ring_ptr(step));   \
+            dst.a = src_[0];                                                      \
+            dst.b = src_[1];                                                      \
+        } else {                                                                  \
+            dst = load_step<FMT>(p.codes, row0, row1, step, wt);                  \
+        }                                                                         \
+        ++step;                                                                   \
+    } while (0)
+
+    // The 64 heads of this CTA are 64 x 576 contiguous query values.
+    const int64_t qbase = ((int64_t)b * p.n_heads + hbase) * kMlaD;
+    constexpr int kQVec = QBF16 ? 8 : 4;                   // values per 16-byte load
+    constexpr int kQLoads = kHC * kMlaD / kQVec;           // 16-byte loads covering the 64 heads
+    // largest |q| (bounds every rotated element too: |q'_i| <= ||q|| <= 24 max|q|)
+    // and the largest latent scale of the chunk
+    float qmax = 0.0f, smax = 0.0f;
+    if (tid < kWorkers) {
+        const uint4* qv = reinterpret_cast<const uint4*>(reinterpret_cast<const char*>(p.q) + qbase * (QBF16 ? 2 : 4));
+        constexpr int kPer = kQLoads / kWorkers;           // 18 (bf16) or 36 (f32): all in flight at once
+        static_assert(kQLoads % kWorkers == 0, "query loads per worker");
+#pragma unroll 6
+        for (int i0 = 0; i0 < kPer; i0 += 6) {
+            uint4 w[6];
+#pragma unroll
+            for (int i = 0; i < 6; ++i) w[i] = __ldg(qv + tid + (i0 + i) * kWorkers);
+#pragma unroll
+            for (int i = 0; i < 6; ++i) {
+                const uint32_t in[4] = {w[i].x, w[i].y, w[i].z, w[i].w};
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    if (QBF16) {
+                        qmax = fmaxf(qmax, fabsf(__uint_as_float(in[k] << 16)));
+                        qmax = fmaxf(qmax, fabsf(__uint_as_float(in[k] & 0xffff0000u)));
+                    } else {
+                        qmax = fmaxf(qmax, fabsf(__uint_as_float(in[k])));
+                    }
+                }
+            }
+        }
+        for (int64_t r = row0 + tid; r < row1; r += kWorkers) smax = fmaxf(smax, p.scales[r * p.n_blocks]);
+        qmax = warp_max(qmax);
+        smax = warp_max(smax);
+        if (lane == 0) {
+            sRed[warp] = qmax;
+            sRed[8 + warp] = smax;
+        }
     }
     tc_before();
     __syncthreads();
     tc_after();
-    float s_max = 0.0f;
-    for (int i = 0; i < 8; ++i) s_max = fmaxf(s_max, sRed[i]);
-    __syncthreads();
-    if (lane == 0) sRed[warp] = qn;
-    __syncthreads();
-    float q_bound = 0.0f;
-    for (int i = 0; i < 8; ++i) q_bound = fmaxf(q_bound, sRed[i]);
+    float q_max = 0.0f, s_max = 0.0f;
+    for (int i = 0; i < 8; ++i) {
+        q_max = fmaxf(q_max, sRed[i]);
+        s_max = fmaxf(s_max, sRed[8 + i]);
+    }
+    const float q_bound = 24.0f * q_max;
     int e_s = 0, e_q = 0;
     if (s_max > 0.0f) frexpf(s_max, &e_s);
     if (q_bound > 0.0f) frexpf(q_bound, &e_q);
+    // context weights p * s_L / S_ref stay within f16 range; queries scaled so
+    // every f16 element stays below 2^14
     const float s_ref = s_max > 0.0f ? ldexpf(1.0f, e_s) : 1.0f;
     const float inv_s_ref = s_max > 0.0f ? ldexpf(1.0f, -e_s) : 1.0f;
     const float q_scale = q_bound > 0.0f ? ldexpf(1.0f, 14 - e_q) : 1.0f;
@@ -318,45 +449,162 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnParams p) {
     // queries -> f16 pair (value, residual) in the score's B layout (K-major,
     // 9 chunks of 64 dims x 128 rows)
     int any_lo = 0;
-    for (int h = warp; h < kHC; h += kThreads / 32) {
-        float v[18];
-        const int64_t qoff = ((int64_t)b * p.n_heads + hbase + h) * kMlaD;
+    if (FMT == KVQ_KV8) {
+        if (tid < kWorkers) {
+            // 8 consecutive dims of one head per step: one 16-byte store of each half
+            const uint4* qv = reinterpret_cast<const uint4*>(reinterpret_cast<const char*>(p.q) + qbase * (QBF16 ? 2 : 4));
+#pragma unroll 3
+            for (int u = tid; u < kHC * kMlaD / 8; u += kWorkers) {
+                float x[8];
+                if (QBF16) {
+                    const uint4 w = __ldg(qv + u);
+                    const uint32_t in[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-        for (int k = 0; k < 18; ++k) v[k] = load_q<QBF16>(p.q, qoff + lane + 32 * k);
-        if (FMT == KVQ_TQ4) {
+                    for (int i = 0; i < 4; ++i) {
+                        x[2 * i] = __uint_as_float(in[i] << 16);
+                        x[2 * i + 1] = __uint_as_float(in[i] & 0xffff0000u);
+                    }
+                } else {
+                    const uint4 w0 = __ldg(qv + 2 * u), w1 = __ldg(qv + 2 * u + 1);
+                    const uint32_t in[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
 #pragma unroll
-            for (int k = 0; k < 16; ++k)
-                if (sign_neg(p.signs, 0, lane + 32 * k)) v[k] = -v[k];
-            warp_fwht<512>(v, lane);
+                    for (int i = 0; i < 8; ++i) x[i] = __uint_as_float(in[i]);
+                }
+                const int e = u * 8, h = e / kMlaD, d = e - h * kMlaD;
+                uint32_t hw[4], lw[4];
 #pragma unroll
-            for (int k = 0; k < 16; ++k) v[k] = __fmul_rn(v[k], p.kn[0]);
-#pragma unroll
-            for (int k = 16; k < 18; ++k)
-                if (sign_neg(p.signs, 1, lane + 32 * (k - 16))) v[k] = -v[k];
-            warp_fwht<64>(v + 16, lane);
-#pragma unroll
-            for (int k = 16; k < 18; ++k) v[k] = __fmul_rn(v[k], p.kn[1]);
+                for (int i = 0; i < 4; ++i) {
+                    const float a0 = x[2 * i] * q_scale, a1 = x[2 * i + 1] * q_scale;
+                    const __half h0 = __float2half_rn(a0), h1 = __float2half_rn(a1);
+                    const __half l0 = __float2half_rn(a0 - __half2float(h0));
+                    const __half l1 = __float2half_rn(a1 - __half2float(h1));
+                    any_lo |= (__half_as_ushort(l0) | __half_as_ushort(l1)) & 0x7fff;
+                    hw[i] = (uint32_t)__half_as_ushort(h0) | ((uint32_t)__half_as_ushort(h1) << 16);
+                    lw[i] = (uint32_t)__half_as_ushort(l0) | ((uint32_t)__half_as_ushort(l1) << 16);
+                }
+                unsigned char* chunk = sQ + (d >> 6) * kQChunkBytes;
+                *reinterpret_cast<uint4*>(chunk + sw128(h, (d & 63) * 2)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                if (LOQ)
+                    *reinterpret_cast<uint4*>(chunk + sw128(kHC + h, (d & 63) * 2)) =
+                        make_uint4(lw[0], lw[1], lw[2], lw[3]);
+            }
         }
+    } else {
+        // TQ4: rotate every head once.  The raw queries of a group of heads are
+        // staged in the (still idle) slot and P^T area, then each warp rotates
+        // its heads with the warp FWHT.
+        constexpr int kGroup = QBF16 ? kHC : kHC / 2;       // 73,728 bytes of raw query per group
+        for (int g0 = 0; g0 < kHC; g0 += kGroup) {
+            if (tid < kWorkers) {
+                const uint4* src = reinterpret_cast<const uint4*>(reinterpret_cast<const char*>(p.q) +
+                                                                   (qbase + (int64_t)g0 * kMlaD) * (QBF16 ? 2 : 4));
+                uint4* dst = reinterpret_cast<uint4*>(sSlot);
+                for (int u = tid; u < kGroup * kMlaD / kQVec; u += kWorkers) dst[u] = __ldg(src + u);
+                worker_sync();
+                for (int hh = warp; hh < kGroup; hh += kWorkers / 32) {
+                    float v[18];
 #pragma unroll
-        for (int k = 0; k < 18; ++k) {
-            const int d = lane + 32 * k;
-            const float x = v[k] * q_scale;
-            const __half hi = __float2half_rn(x);
-            const __half lo = __float2half_rn(x - __half2float(hi));
-            any_lo |= __half_as_ushort(lo) & 0x7fff;
-            unsigned char* chunk = sQ + (d >> 6) * kQChunkBytes;
-            *reinterpret_cast<__half*>(chunk + sw128(h, (d & 63) * 2)) = hi;
-            *reinterpret_cast<__half*>(chunk + sw128(kHC + h, (d & 63) * 2)) = lo;
+                    for (int k = 0; k < 18; ++k) {
+                        const int idx = hh * kMlaD + lane + 32 * k;
+                        v[k] = QBF16 ? __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(sSlot)[idx])
+                                     : reinterpret_cast<const float*>(sSlot)[idx];
+                    }
+#pragma unroll
+                    for (int k = 0; k < 16; ++k)
+                        if (sign_neg(p.signs, 0, lane + 32 * k)) v[k] = -v[k];
+                    warp_fwht<512>(v, lane);
+#pragma unroll
+                    for (int k = 0; k < 16; ++k) v[k] = __fmul_rn(v[k], p.kn[0]);
+#pragma unroll
+                    for (int k = 16; k < 18; ++k)
+                        if (sign_neg(p.signs, 1, lane + 32 * (k - 16))) v[k] = -v[k];
+                    warp_fwht<64>(v + 16, lane);
+#pragma unroll
+                    for (int k = 16; k < 18; ++k) v[k] = __fmul_rn(v[k], p.kn[1]);
+                    const int h = g0 + hh;
+#pragma unroll
+                    for (int k = 0; k < 18; ++k) {
+                        const int d = lane + 32 * k;
+                        const float x = v[k] * q_scale;
+                        const __half hi = __float2half_rn(x);
+                        const __half lo = __float2half_rn(x - __half2float(hi));
+                        any_lo |= __half_as_ushort(lo) & 0x7fff;
+                        unsigned char* chunk = sQ + (d >> 6) * kQChunkBytes;
+                        *reinterpret_cast<__half*>(chunk + sw128(h, (d & 63) * 2)) = hi;
+                        *reinterpret_cast<__half*>(chunk + sw128(kHC + h, (d & 63) * 2)) = lo;
+                    }
+                }
+                worker_sync();
+            }
         }
     }
-    if (any_lo) atomicOr(sHasLo, 1);
+    if (LOQ && any_lo) atomicOr(sHasLo, 1);
     fence_async_smem();
     tc_before();
     __syncthreads();
     tc_after();
-    // a query exact in f16 (bf16 input) needs only the first 64 rows
+    // a query exact in f16 (bf16 input, KV8) needs only the first 64 rows
     const bool has_lo = *sHasLo != 0;
 
+    if (warp == kWorkers / 32) {
+        // ================= MMA warp: lane 0 issues, the rest idle =================
+        if (lane == 0) {
+            const uint32_t id_score = has_lo ? kIdescScore2 : kIdescScore;
+            const uint64_t dq0 = umma_desc(smem_u32(sQ), 16, 1024);
+            const uint64_t dslot0 = umma_desc(smem_u32(sSlot), 16, 1024);
+            const uint64_t dpair0 = umma_desc(smem_u32(sSlot), kSlotBytes, 1024);
+            const uint64_t dp = umma_desc(smem_u32(sP), kSlotBytes, 1024);
+            constexpr uint64_t kQStep = kQChunkBytes >> 4, kSlotStep = kSlotBytes >> 4;
+            uint32_t fills[kSlots] = {0u, 0u, 0u, 0u};
+            bool o_init = false, ok = true;
+            for (int tile = 0; tile < n_tiles && ok; ++tile) {
+                for (int kc = 0; kc < 9 && ok; ++kc) {
+                    const int s = FMT == KVQ_KV8 ? (kc & 3) : (kc & 1) * 2;
+                    ok = mbar_wait(&bars[kBarFull0 + s], fills[s] & 1, sAbort);
+                    ++fills[s];
+                    if (FMT == KVQ_TQ4) {
+                        ok = ok && mbar_wait(&bars[kBarFull0 + s + 1], fills[s + 1] & 1, sAbort);
+                        ++fills[s + 1];
+                    }
+                    tc_after();
+                    const uint32_t d = tmem + (kc < 8 ? kColSL : kColSR);
+                    const uint64_t a = dslot0 + s * kSlotStep, bq = dq0 + kc * kQStep;
+#pragma unroll
+                    for (int ks = 0; ks < 4; ++ks)
+                        umma_f16(d, a + 2 * ks, bq + 2 * ks, id_score, (kc == 0 || kc == 8) ? (ks > 0 ? 1u : 0u) : 1u);
+                    if (FMT == KVQ_TQ4) {
+#pragma unroll
+                        for (int ks = 0; ks < 4; ++ks) umma_f16(d, a + kSlotStep + 2 * ks, bq + 2 * ks, kIdescScore, 1u);
+                    }
+                    umma_commit(&bars[kBarEmpty0 + s]);
+                    if (FMT == KVQ_TQ4) umma_commit(&bars[kBarEmpty0 + s + 1]);
+                    if (kc == 8) umma_commit(&bars[kBarScore]);
+                }
+                ok = ok && mbar_wait(&bars[kBarP], tile & 1, sAbort);
+                tc_after();
+                for (int db = 0; db < 4 && ok; ++db) {
+                    const int s0 = (db & 1) * 2;
+                    ok = mbar_wait(&bars[kBarFull0 + s0], fills[s0] & 1, sAbort) &&
+                         mbar_wait(&bars[kBarFull0 + s0 + 1], fills[s0 + 1] & 1, sAbort);
+                    ++fills[s0];
+                    ++fills[s0 + 1];
+                    tc_after();
+                    const uint32_t d = tmem + kColO + 64 * db;
+                    const uint64_t a = dpair0 + s0 * kSlotStep;
+#pragma unroll
+                    for (int ks = 0; ks < 8; ++ks)
+                        umma_f16(d, a + 128 * ks, dp + 128 * ks, kIdescCtx, (o_init || ks > 0) ? 1u : 0u);
+                    umma_commit(&bars[kBarEmpty0 + s0]);
+                    umma_commit(&bars[kBarEmpty0 + s0 + 1]);
+                    if (db == 3) umma_commit(&bars[kBarCtx]);
+                }
+                o_init = true;
+            }
+        }
+        return;
+    }
+
+    // ================= workers: conversion, softmax, epilogue =================
     const int srow = 32 * (warp & 3) + lane;   // TMEM lane owned in the softmax
     const int hq = warp >> 2;                   // heads 32 hq .. 32 hq + 31
     const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
@@ -367,51 +615,39 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnParams p) {
     bool o_init = false;
     int tile = 0;
 
-    for (int64_t t0 = row0; t0 < row1 && !*sAbort; t0 += kRows, ++tile) {
+    for (; tile < n_tiles; ++tile) {
+        if (worker_any(*sAbort != 0)) break;
+        const int64_t t0 = row0 + (int64_t)tile * kRows;
         const int nt = (int)min((int64_t)kRows, row1 - t0);
-        if (tid < kRows) {
-            float2 s2 = make_float2(0.0f, 0.0f);
-            if (tid < nt) {
-                const int64_t r = t0 + tid;
-                s2 = p.n_blocks == 2 ? make_float2(p.scales[r * 2], p.scales[r * 2 + 1])
-                                     : make_float2(p.scales[r], p.scales[r]);
-            }
-            sScale[tid] = s2;
+        const bool valid = (tid >> 1) < nt;
+        if (tid == 0 && t0 + kRows < row1) {
+            const int64_t n = min((int64_t)kRows, row1 - (t0 + kRows));
+            const int row_bytes = FMT == KVQ_KV8 ? kMlaD : kMlaD / 2;
+            prefetch_l2(p.codes + (t0 + kRows) * row_bytes, (uint32_t)(n * row_bytes));
         }
-        // ---- scores: 9 chunks of 64 dims (8 latent, 1 rope) ----
+        // this thread's softmax row scales (used after the score chunks)
+        float my_sl = 0.0f, my_sr = 0.0f;
+        if (srow < nt) {
+            const int64_t r = t0 + srow;
+            my_sl = p.scales[r * p.n_blocks];
+            my_sr = p.scales[r * p.n_blocks + (p.n_blocks - 1)];
+        }
+        // ---- score chunks: 9 chunks of 64 dims (8 latent, 1 rope) ----
         for (int kc = 0; kc < 9; ++kc) {
-            // KV8: one slot per chunk (codes are exact in f16).  TQ4: a slot pair,
-            // the f16 levels and their rounding residuals, both multiplied by the
-            // query into the same accumulator so the score sees the f32 levels.
             const int s = FMT == KVQ_KV8 ? (kc & 3) : (kc & 1) * 2;
-            if (uses[s] > 0) mbar_wait(&bars[kBarSlot0 + s], (uses[s] - 1) & 1, sAbort);
-            if (FMT == KVQ_TQ4 && uses[s + 1] > 0) mbar_wait(&bars[kBarSlot0 + s + 1], (uses[s + 1] - 1) & 1, sAbort);
-            decode_chunk<FMT>(p.codes, t0, nt, kc, sSlot + s * kSlotBytes, sLut, tid);
-            if (FMT == KVQ_TQ4) decode_delta_chunk(p.codes, t0, nt, kc, sSlot + (s + 1) * kSlotBytes, sDelta, tid);
+            if (uses[s] > 0) mbar_wait(&bars[kBarEmpty0 + s], (uses[s] - 1) & 1, sAbort);
+            if (FMT == KVQ_TQ4 && uses[s + 1] > 0) mbar_wait(&bars[kBarEmpty0 + s + 1], (uses[s + 1] - 1) & 1, sAbort);
+            RawChunk rc;
+            KVQ_NEXT_CHUNK(rc);
+            store_chunk<FMT>(rc, valid, sSlot + s * kSlotBytes, sLut, tid);
+            if (FMT == KVQ_TQ4) store_delta_chunk(rc, valid, sSlot + (s + 1) * kSlotBytes, sDelta, tid);
             fence_async_smem();
-            tc_before();
-            __syncthreads();
-            if (tid == 0) {
-                tc_after();
-                const uint32_t d = tmem + (kc < 8 ? kColSL : kColSR);
-                const uint32_t a0 = smem_u32(sSlot + s * kSlotBytes), b0 = smem_u32(sQ + kc * kQChunkBytes);
-#pragma unroll
-                for (int ks = 0; ks < 4; ++ks)
-                    umma_f16(d, umma_desc(a0 + ks * 32, 16, 1024), umma_desc(b0 + ks * 32, 16, 1024),
-                             has_lo ? kIdescScore2 : kIdescScore, (kc == 0 || kc == 8) ? (ks > 0 ? 1u : 0u) : 1u);
-                if (FMT == KVQ_TQ4) {
-                    const uint32_t a1 = smem_u32(sSlot + (s + 1) * kSlotBytes);
-#pragma unroll
-                    for (int ks = 0; ks < 4; ++ks)
-                        umma_f16(d, umma_desc(a1 + ks * 32, 16, 1024), umma_desc(b0 + ks * 32, 16, 1024), kIdescScore,
-                                 1u);
-                }
-                umma_commit(&bars[kBarSlot0 + s]);
-                if (FMT == KVQ_TQ4) umma_commit(&bars[kBarSlot0 + s + 1]);
-                if (kc == 8) umma_commit(&bars[kBarScore]);
-            }
+            mbar_arrive(&bars[kBarFull0 + s]);
             ++uses[s];
-            if (FMT == KVQ_TQ4) ++uses[s + 1];
+            if (FMT == KVQ_TQ4) {
+                mbar_arrive(&bars[kBarFull0 + s + 1]);
+                ++uses[s + 1];
+            }
         }
         // ---- softmax of the tile (thread = row, 32 heads) ----
         mbar_wait(&bars[kBarScore], tile & 1, sAbort);
@@ -439,29 +675,36 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnParams p) {
                     fr[j] += __uint_as_float(sr[j]);
                 }
             }
-            const float2 sc = sScale[srow];
-            const float a = sc.x * cz, bb = sc.y * cz;
-            const bool valid = srow < nt;
+            const float a = my_sl * cz, bb = my_sr * cz;
+            const bool row_ok = srow < nt;
 #pragma unroll
-            for (int j = 0; j < 32; ++j) z[j] = valid ? fmaf(fl[j], a, fr[j] * bb) : -INFINITY;
+            for (int j = 0; j < 32; ++j) z[j] = row_ok ? fmaf(fl[j], a, fr[j] * bb) : -INFINITY;
         }
         bool flag = false;
 #pragma unroll
         for (int j = 0; j < 32; ++j) flag |= z[j] > sM[32 * hq + j] + 8.0f;
-        if (__syncthreads_or(flag)) {
+        if (worker_any(flag)) {
             // exact column max of the tile, new running max, rescale factors
             float* zbuf = reinterpret_cast<float*>(sSlot);   // 128 x 64 f32 over slots 0-1 (idle now)
 #pragma unroll
             for (int j = 0; j < 32; ++j) zbuf[srow * kHC + 32 * hq + j] = z[j];
-            __syncthreads();
-            if (tid < kHC) {
+            worker_sync();
+            {
+                const int col = tid & (kHC - 1), quarter = tid >> 6;
                 float cm = -INFINITY;
-                for (int r = 0; r < kRows; ++r) cm = fmaxf(cm, zbuf[r * kHC + tid]);
-                const float mo = sM[tid], mn = fmaxf(mo, cm);
-                sAlpha[tid] = mo == -INFINITY ? 0.0f : exp2f(mo - mn);
-                sM[tid] = mn;
+#pragma unroll 8
+                for (int r = 32 * quarter; r < 32 * quarter + 32; ++r) cm = fmaxf(cm, zbuf[r * kHC + col]);
+                float* part = reinterpret_cast<float*>(sP);   // P^T is rewritten after this
+                part[quarter * kHC + col] = cm;
+                worker_sync();
+                if (tid < kHC) {
+                    const float c4 = fmaxf(fmaxf(part[tid], part[kHC + tid]), fmaxf(part[2 * kHC + tid], part[3 * kHC + tid]));
+                    const float mo = sM[tid], mn = fmaxf(mo, c4);
+                    sAlpha[tid] = mo == -INFINITY ? 0.0f : exp2f(mo - mn);
+                    sM[tid] = mn;
+                }
             }
-            __syncthreads();
+            worker_sync();
             if (o_init) {
 #pragma unroll
                 for (int bi = 0; bi < 2; ++bi)
@@ -479,12 +722,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnParams p) {
             }
 #pragma unroll
             for (int j = 0; j < 32; ++j) lsum[j] *= sAlpha[32 * hq + j];
-            tc_before();
-            __syncthreads();
-            tc_after();
         }
         {
-            const float wrow = sScale[srow].x * inv_s_ref;
+            const float wrow = my_sl * inv_s_ref;
             uint32_t pk[16];
 #pragma unroll
             for (int j = 0; j < 32; j += 2) {
@@ -495,55 +735,58 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnParams p) {
                 const __half2 h2 = __floats2half2_rn(p0 * wrow, p1 * wrow);
                 pk[j / 2] = *reinterpret_cast<const uint32_t*>(&h2);
             }
+            // slow path: every column max must be read before P^T overwrites the partials
+            worker_sync();
 #pragma unroll
             for (int i = 0; i < 4; ++i)
                 *reinterpret_cast<uint4*>(sP + sw128(srow, 64 * hq + 16 * i)) =
                     make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
         }
-        // ---- context: 4 blocks of 128 dims, K = the tile's 128 rows ----
+        fence_async_smem();
+        tc_before();
+        mbar_arrive(&bars[kBarP]);
+        // ---- context chunks: 4 blocks of 128 dims (2 chunks each) ----
         for (int db = 0; db < 4; ++db) {
             const int s0 = (db & 1) * 2;
-            if (uses[s0] > 0) mbar_wait(&bars[kBarSlot0 + s0], (uses[s0] - 1) & 1, sAbort);
-            if (uses[s0 + 1] > 0) mbar_wait(&bars[kBarSlot0 + s0 + 1], (uses[s0 + 1] - 1) & 1, sAbort);
-            decode_chunk<FMT>(p.codes, t0, nt, 2 * db, sSlot + s0 * kSlotBytes, sLut, tid);
-            decode_chunk<FMT>(p.codes, t0, nt, 2 * db + 1, sSlot + (s0 + 1) * kSlotBytes, sLut, tid);
+            if (uses[s0] > 0) mbar_wait(&bars[kBarEmpty0 + s0], (uses[s0] - 1) & 1, sAbort);
+            if (uses[s0 + 1] > 0) mbar_wait(&bars[kBarEmpty0 + s0 + 1], (uses[s0 + 1] - 1) & 1, sAbort);
+            RawChunk r0c, r1c;
+            KVQ_NEXT_CHUNK(r0c);
+            KVQ_NEXT_CHUNK(r1c);
+            store_chunk<FMT>(r0c, valid, sSlot + s0 * kSlotBytes, sLut, tid);
+            store_chunk<FMT>(r1c, valid, sSlot + (s0 + 1) * kSlotBytes, sLut, tid);
             fence_async_smem();
-            tc_before();
-            __syncthreads();
-            if (tid == 0) {
-                tc_after();
-                const uint32_t d = tmem + kColO + 64 * db;
-                const uint32_t a0 = smem_u32(sSlot + s0 * kSlotBytes), b0 = smem_u32(sP);
-#pragma unroll
-                for (int ks = 0; ks < 8; ++ks)
-                    umma_f16(d, umma_desc(a0 + ks * 2048, kSlotBytes, 1024), umma_desc(b0 + ks * 2048, kSlotBytes, 1024),
-                             kIdescCtx, (o_init || ks > 0) ? 1u : 0u);
-                umma_commit(&bars[kBarSlot0 + s0]);
-                umma_commit(&bars[kBarSlot0 + s0 + 1]);
-                if (db == 3) umma_commit(&bars[kBarCtx]);
-            }
+            mbar_arrive(&bars[kBarFull0 + s0]);
+            mbar_arrive(&bars[kBarFull0 + s0 + 1]);
             ++uses[s0];
             ++uses[s0 + 1];
         }
         o_init = true;
     }
+#undef KVQ_NEXT_CHUNK
+    if (!LOQ) cp_async_wait<0>();
 
     // ---- epilogue: row sums, O^T -> partial state ----
     if (tile > 0) mbar_wait(&bars[kBarCtx], (tile - 1) & 1, sAbort);
     tc_after();
     {
         float* lbuf = reinterpret_cast<float*>(sSlot);
+        worker_sync();   // every worker is past its last slot use
 #pragma unroll
         for (int j = 0; j < 32; ++j) lbuf[srow * kHC + 32 * hq + j] = lsum[j];
-        __syncthreads();
-        if (tid < kHC) {
-            float l = 0.0f;
-            for (int r = 0; r < kRows; ++r) l += lbuf[r * kHC + tid];
-            sAlpha[tid] = l;
-        }
-        __syncthreads();
+        worker_sync();
+        const int col = tid & (kHC - 1), quarter = tid >> 6;
+        float l = 0.0f;
+#pragma unroll 8
+        for (int r = 32 * quarter; r < 32 * quarter + 32; ++r) l += lbuf[r * kHC + col];
+        float* part = reinterpret_cast<float*>(sP);
+        part[quarter * kHC + col] = l;
+        worker_sync();
+        if (tid < kHC) sAlpha[tid] = (part[tid] + part[kHC + tid]) + (part[2 * kHC + tid] + part[3 * kHC + tid]);
+        worker_sync();
     }
-    if (*sAbort) {
+    const bool aborted = *sAbort != 0 || tile < n_tiles;
+    if (aborted) {
         if (tid == 0) set_err(p.err, KVQ_ERR_DEVICE);
     } else {
 #pragma unroll
@@ -569,17 +812,18 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnParams p) {
         }
     }
     tc_before();
-    __syncthreads();
+    worker_sync();
     tc_after();
     if (warp == 1) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols));
 }
 
 template <int FMT, bool QBF16>
 cudaError_t launch_tc(const AttnParams& p, int64_t grid_x, int groups, cudaStream_t stream) {
-    cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<FMT, QBF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    constexpr bool kLoq = !(FMT == KVQ_KV8 && QBF16);
+    cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<FMT, QBF16, kLoq>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)kSmemAlloc);
     if (e != cudaSuccess) return e;
-    attn_tc_kernel<FMT, QBF16><<<dim3((unsigned)grid_x, (unsigned)groups), kThreads, kSmemAlloc, stream>>>(p);
+    attn_tc_kernel<FMT, QBF16, kLoq><<<dim3((unsigned)grid_x, (unsigned)groups), kThreads, kSmemAlloc, stream>>>(p);
     return cudaGetLastError();
 }
 
