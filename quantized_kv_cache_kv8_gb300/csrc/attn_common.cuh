@@ -120,6 +120,10 @@ AttnParams make_attn_params(kvq_format fmt, const kvq_mla_layout& L, const void*
                             const uint8_t* codes, const float* scales, const int64_t* cu_seqlens,
                             int64_t prefill_past, const AttnPlan& plan, float sm_scale, void* workspace);
 
+// Tensor-core partial kernel for KV8 rows with bf16 queries (every chunk of a
+// tile decoded once); grid = work items x head groups of 64.
+cudaError_t launch_attn_tc_kv8_bf16(const AttnParams& p, int64_t grid_x, int groups, cudaStream_t stream);
+
 // LSE merge of the chunk partials into out[n_seq][n_heads][512] (TQ4: unrotated).
 cudaError_t launch_attn_merge(kvq_format fmt, const AttnParams& p, float* out, cudaStream_t stream);
 

@@ -27,6 +27,7 @@ namespace {
 constexpr int kD = kMlaD, kDL = kMlaDL, kDV = kMlaDV;
 constexpr int kHG = 16;   // heads per CTA
 constexpr int kTR = 16;   // rows per tile
+constexpr int kFlushTiles = 64;   // tiles per block sum (1024 rows)
 constexpr int kNT = 256;  // threads per CTA
 constexpr int kXS = 580;  // shared-memory row stride in floats (bank spread)
 constexpr int kSmSMs = 152;
@@ -98,14 +99,19 @@ __global__ void __launch_bounds__(kNT, 2) attn_partial_kernel(AttnParams p) {
 
     const int sh = tid >> 4;   // score: head of this thread
     const int st = tid & 15;   // score: row of this thread
-    float m_run = -INFINITY, l_run = 0.0f;
+    // Two-level sums: the block sums (o, l_blk) take at most kFlushTiles tiles
+    // and are then added into the totals (o_tot, l_run), so that f32 rounding
+    // grows with sqrt(rows / 1024) + sqrt(1024) rather than sqrt(rows) over
+    // chunks of 10^5 rows.
+    float m_run = -INFINITY, l_run = 0.0f, l_blk = 0.0f;
     const int cq = tid >> 6;   // context: head quad
     const int cc = tid & 63;   // context: dims 4cc..4cc+3 and 256+4cc..+3
-    float o[4][8];
+    float o[4][8], o_tot[4][8];
 #pragma unroll
     for (int i = 0; i < 4; ++i)
 #pragma unroll
-        for (int j = 0; j < 8; ++j) o[i][j] = 0.0f;
+        for (int j = 0; j < 8; ++j) o[i][j] = o_tot[i][j] = 0.0f;
+    int blk_tiles = 0;
 
     for (int64_t t0 = row0; t0 < row1; t0 += kTR) {
         const int nt = (int)min((int64_t)kTR, row1 - t0);
@@ -192,7 +198,8 @@ __global__ void __launch_bounds__(kNT, 2) attn_partial_kernel(AttnParams p) {
             float psum = pz;
 #pragma unroll
             for (int off = 8; off >= 1; off >>= 1) psum += __shfl_xor_sync(kFull, psum, off);
-            l_run = l_run * a + psum;
+            l_blk = l_blk * a + psum;
+            l_run = l_run * a;
             m_run = m_new;
             P[st * kHG + sh] = pz * sc[st * 2];
             if (st == 0) alpha[sh] = a;
@@ -207,7 +214,10 @@ __global__ void __launch_bounds__(kNT, 2) attn_partial_kernel(AttnParams p) {
 #pragma unroll
             for (int i = 0; i < 4; ++i)
 #pragma unroll
-                for (int j = 0; j < 8; ++j) o[i][j] *= al[i];
+                for (int j = 0; j < 8; ++j) {
+                    o[i][j] *= al[i];
+                    o_tot[i][j] *= al[i];
+                }
             for (int t = 0; t < nt; ++t) {
                 const float4 xa = *reinterpret_cast<const float4*>(xs + t * kXS + 4 * cc);
                 const float4 xb = *reinterpret_cast<const float4*>(xs + t * kXS + 256 + 4 * cc);
@@ -226,8 +236,25 @@ __global__ void __launch_bounds__(kNT, 2) attn_partial_kernel(AttnParams p) {
                 }
             }
         }
+        if (++blk_tiles == kFlushTiles) {
+            blk_tiles = 0;
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    o_tot[i][j] += o[i][j];
+                    o[i][j] = 0.0f;
+                }
+            l_run += l_blk;
+            l_blk = 0.0f;
+        }
         __syncthreads();
     }
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) o[i][j] += o_tot[i][j];
+    l_run += l_blk;
 
     // partial state of this chunk
 #pragma unroll

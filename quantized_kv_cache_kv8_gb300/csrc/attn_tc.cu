@@ -27,7 +27,7 @@
 // more than 2^8.  Row sums are accumulated per thread and reduced across the
 // 128 rows once per chunk.  The partial state written for the merge is the
 // same as the SIMT path's, in natural-log units.
-#include "attn_common.cuh"
+#include "tc_common.cuh"
 
 #include <algorithm>
 #include <math.h>
@@ -59,128 +59,15 @@ static_assert(kSmemAlloc <= 232448, "shared memory budget");
 // TMEM columns: O^T blocks 0..255; S_L^T 256..383 and S_R^T 384..511, each as
 // 64 columns for the f16 query and 64 for its residual
 constexpr uint32_t kColO = 0, kColSL = 256, kColSR = 384, kTmemCols = 512;
-constexpr float kLog2e = 1.4426950408889634f;
-constexpr float kLn2 = 0.6931471805599453f;
-constexpr long long kWaitLimit = 1ll << 22;
 
 // mbarriers: slot full (256 worker arrivals), slot empty (MMA commit), score
 // done, context done (MMA commits), P^T ready (256 worker arrivals)
 enum { kBarFull0 = 0, kBarEmpty0 = 4, kBarScore = 8, kBarCtx = 9, kBarP = 10, kNumBars = 11 };
 
-__host__ __device__ constexpr uint32_t idesc_f16(int M, int N, bool a_mn, bool b_mn) {
-    // D f32 (bit 4), A and B f16 (format 0), operand majors, N>>3 at 17, M>>4 at 24
-    return (1u << 4) | ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) |
-           ((uint32_t)(M >> 4) << 24);
-}
+using namespace tc;
 constexpr uint32_t kIdescScore = idesc_f16(128, kHC, false, false);
 constexpr uint32_t kIdescScore2 = idesc_f16(128, 2 * kHC, false, false);
 constexpr uint32_t kIdescCtx = idesc_f16(128, kHC, true, true);
-
-__device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
-
-// Byte offset of (row r, byte b) in a region of 128-byte rows laid out in the
-// 128-byte swizzle (16-byte chunk index XOR row index within 8-row atoms).
-__device__ __forceinline__ uint32_t sw128(int r, int b) {
-    return (uint32_t)((r >> 3) * 1024 + (r & 7) * 128 + ((((b >> 4) ^ r) & 7) << 4) + (b & 15));
-}
-
-// Shared-memory matrix descriptor: start, leading and stride byte offsets,
-// descriptor version 1, 128-byte swizzle.
-__device__ __forceinline__ uint64_t umma_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
-    return (uint64_t)((saddr >> 4) & 0x3FFF) | ((uint64_t)((lbo >> 4) & 0x3FFF) << 16) |
-           ((uint64_t)((sbo >> 4) & 0x3FFF) << 32) | (1ull << 46) | (2ull << 61);
-}
-
-__device__ __forceinline__ void umma_f16(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
-    asm volatile(
-        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d),
-        "l"(a), "l"(b), "r"(idesc), "r"(acc));
-}
-
-__device__ __forceinline__ void umma_commit(uint64_t* bar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
-                 : "memory");
-}
-
-__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
-__device__ __forceinline__ void tc_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-
-// Bounded wait on an mbarrier phase.  Returns false (and raises the CTA's
-// abort flag) when the limit is reached; later waits then return at once.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
-    if (*abort_flag) return false;
-    const uint32_t a = smem_u32(bar);
-    for (long long i = 0; i < kWaitLimit; ++i) {
-        uint32_t ok;
-        asm volatile(
-            "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
-            : "=r"(ok)
-            : "r"(a), "r"(parity)
-            : "memory");
-        if (ok) return true;
-    }
-    *abort_flag = 1;
-    return false;
-}
-
-// Barrier 1 among the 256 worker threads only (the MMA warp never joins it).
-__device__ __forceinline__ void worker_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
-__device__ __forceinline__ bool worker_any(bool v) {
-    uint32_t r;
-    asm volatile(
-        "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.or.pred q, 1, 256, p;\n selp.u32 %0, 1, 0, q;\n}\n"
-        : "=r"(r)
-        : "r"((uint32_t)v)
-        : "memory");
-    return r != 0;
-}
-__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gmem_src) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem_dst)), "l"(gmem_src) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
-__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-
-#define KVQ_R32(v) \
-    "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]), "=r"(v[8]), \
-        "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]), "=r"(v[16]),   \
-        "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]), \
-        "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
-#define KVQ_W32(v)                                                                                                \
-    "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]), \
-        "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]), "r"(v[17]),          \
-        "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]),           \
-        "r"(v[26]), "r"(v[27]), "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
-
-// 32 consecutive TMEM columns of this thread's lane.
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-        : KVQ_R32(v)
-        : "r"(taddr));
-}
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32]) {
-    asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
-        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
-        KVQ_W32(v));
-}
-__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
-__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
-
-__device__ __forceinline__ uint32_t e4m3x2_to_half2_bits(uint32_t two) {
-    __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)two, __NV_E4M3);
-    return (uint32_t)h.x | ((uint32_t)h.y << 16);
-}
 
 // The raw bytes one thread converts for one chunk: dims [64 kc, 64 kc + 64) of
 // row (tid / 2), half (tid % 2) of them.  KV8: 32 bytes (a, b); TQ4: 16 (a).
@@ -856,7 +743,7 @@ cudaError_t launch_attn_tc(kvq_format fmt, const kvq_mla_layout& L, const void* 
     const int groups = n_heads / kHC;
     cudaError_t e;
     if (fmt == KVQ_KV8)
-        e = qdt == KVQ_BF16 ? launch_tc<KVQ_KV8, true>(p, plan.max_items, groups, stream)
+        e = qdt == KVQ_BF16 ? launch_attn_tc_kv8_bf16(p, plan.max_items, groups, stream)
                             : launch_tc<KVQ_KV8, false>(p, plan.max_items, groups, stream);
     else
         e = qdt == KVQ_BF16 ? launch_tc<KVQ_TQ4, true>(p, plan.max_items, groups, stream)

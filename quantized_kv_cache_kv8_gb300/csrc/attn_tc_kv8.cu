@@ -1,0 +1,477 @@
+// attn_tc_kv8.cu -- tensor-core attention over KV8 rows for bf16 queries, with
+// every quantized chunk decoded once per tile.
+//
+// Same transposed formulation as the general tensor-core kernel (one chunk of
+// rows x 64 heads per CTA; S^T = C Q^T with M = 128 rows, N = 64 heads;
+// O^T += C^T P^T with M = 128 dims, K = rows), specialised for the case the
+// decode benchmark runs: e4m3 codes and a bf16 query.
+//
+// A bf16 query times a power of two is exact in f16 (over the range that can
+// matter), so each 64-dim query chunk needs only its 64 head rows: the query
+// takes 72 KB of shared memory.  That leaves room for all 9 f16 chunks of a
+// 128-row tile (144 KB).  Each chunk is decoded once and read twice by the
+// tensor cores: as the K-major A operand of the score and, for the 8 latent
+// chunks, as the MN-major A operand of the context.  P^T takes the rope
+// chunk's slot once the score of the tile has completed.
+//
+// Pipeline per tile t (8 worker warps, 1 MMA warp):
+//   workers: decode chunk kc of tile t into slot kc as soon as the context of
+//            tile t-1 has released it (slot pair kc/2; the rope slot with the
+//            last pair), then issue the loads of tile t+1 into registers, then
+//            the softmax of tile t (thread = row, 32 heads), then P^T.
+//   MMA:     score of tile t chunk by chunk, commit; once P^T(t) is written,
+//            the 4 context blocks, each committed to its slot pair's barrier.
+// The decode of tile t+1 thus overlaps the context MMAs of tile t, and the
+// score MMAs of tile t+1 follow the decode chunk by chunk.
+//
+// Reductions over the 128 rows of a tile (column max in the softmax's exact
+// path, the row sums at the end) run as a 31-shuffle transpose-reduce within
+// each warp plus one 4-way combine in shared memory.
+//
+// The row scales factor out of both sums ([P2] "What's in it"; [P1] "Ready for
+// review" comment, finding 2): z = sm * (s_L * S_L + s_R * S_R), and the
+// context weight is p * s_L (divided by a power of two S_ref that keeps it in
+// f16 range and multiplied back in the epilogue).
+#include "tc_common.cuh"
+
+#include <math.h>
+
+namespace kvq {
+namespace {
+using namespace tc;
+
+constexpr int kRows = 128;      // rows per tile
+constexpr int kHC = 64;         // heads per CTA
+constexpr int kWorkers = 256;
+constexpr int kThreads = kWorkers + 32;
+constexpr int kChunks = 9;      // 64-dim chunks of a row: 8 latent + 1 rope
+constexpr int kRope = 8;        // the rope chunk's slot, reused for P^T
+constexpr uint32_t kSlotBytes = kRows * 128;       // 128 rows x 64 f16
+constexpr uint32_t kQChunkBytes = kHC * 128;       // 64 heads x 64 f16
+constexpr uint32_t kOffQ = 0;
+constexpr uint32_t kOffSlot = kOffQ + kChunks * kQChunkBytes;
+constexpr uint32_t kOffM = kOffSlot + kChunks * kSlotBytes;
+constexpr uint32_t kOffAlpha = kOffM + kHC * 4;
+constexpr uint32_t kOffRed = kOffAlpha + kHC * 4;   // 4 quadrants x 64 heads of f32
+constexpr uint32_t kOffBar = kOffRed + 4 * kHC * 4;
+constexpr uint32_t kOffMisc = kOffBar + 16 * 8;      // abort flag, TMEM base, item info
+constexpr uint32_t kSmemUsed = kOffMisc + 32;
+static_assert(kOffSlot % 1024 == 0, "swizzled operands need 1024-byte alignment");
+static_assert(kSmemUsed <= 232448, "shared memory budget");
+
+// TMEM columns: O^T blocks 0..255, S_L^T 256..319, S_R^T 320..383
+constexpr uint32_t kColO = 0, kColSL = 256, kColSR = 320, kTmemCols = 512;
+
+// mbarriers: chunk kc stored (256 arrivals), slot pair db released by the
+// context (MMA commit; the last pair also releases the rope/P^T slot), score
+// complete (MMA commit), P^T written (256 arrivals), every MMA of the CTA
+// complete (the MMA warp's last commit, also after an abort)
+enum { kBarFull0 = 0, kBarFree0 = 9, kBarScore = 13, kBarP = 14, kBarDone = 15, kNumBars = 16 };
+
+constexpr uint32_t kIdescScore = idesc_f16(128, kHC, false, false);
+constexpr uint32_t kIdescCtx = idesc_f16(128, kHC, true, true);
+
+// One worker's raw share of chunks [K0, K0 + N) of a tile: row (tid / 2); for
+// each chunk kc, the 16 bytes at dims 64 kc + 16 h and the 16 at
+// 64 kc + 32 + 16 h (h = tid % 2), so that each load instruction of a warp
+// reads whole 32-byte sectors.  A tile's 9 chunks are held as a part of 5 and
+// a part of 4, loaded at different points of the previous tile.
+template <int K0, int N>
+struct RawPart {
+    uint4 v[N][2];
+};
+constexpr int kPartA = 5;   // chunks 0..4: loaded before the softmax of the previous tile
+using RawA = RawPart<0, kPartA>;
+using RawB = RawPart<kPartA, kChunks - kPartA>;
+
+template <int K0, int N>
+__device__ __forceinline__ void load_part(RawPart<K0, N>& r, const uint8_t* __restrict__ codes, int64_t t0, int nt,
+                                          int row, int h) {
+    if (row < nt) {
+        const uint8_t* src = codes + (t0 + row) * kMlaD + 16 * h + 64 * K0;
+#pragma unroll
+        for (int k = 0; k < N; ++k) {
+            r.v[k][0] = __ldg(reinterpret_cast<const uint4*>(src + 64 * k));
+            r.v[k][1] = __ldg(reinterpret_cast<const uint4*>(src + 64 * k + 32));
+        }
+    } else {
+#pragma unroll
+        for (int k = 0; k < N; ++k) r.v[k][0] = r.v[k][1] = make_uint4(0u, 0u, 0u, 0u);
+    }
+}
+
+// 16 e4m3 codes -> 16 f16 values (exact) at byte offset `b` of swizzled row `row`.
+__device__ __forceinline__ void store16(unsigned char* slot, const uint4& c, int row, int b) {
+    const uint32_t in[4] = {c.x, c.y, c.z, c.w};
+    uint32_t w[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        w[2 * i] = e4m3x2_to_half2_bits(in[i] & 0xffffu);
+        w[2 * i + 1] = e4m3x2_to_half2_bits(in[i] >> 16);
+    }
+    *reinterpret_cast<uint4*>(slot + sw128(row, b)) = make_uint4(w[0], w[1], w[2], w[3]);
+    *reinterpret_cast<uint4*>(slot + sw128(row, b + 16)) = make_uint4(w[4], w[5], w[6], w[7]);
+}
+
+// In-warp transpose-reduce: on entry each lane holds 32 values (columns
+// 0..31 of its row); on return lane j's v[0] is the reduction of column j over
+// the 32 lanes.  31 shuffles.
+template <bool MAX>
+__device__ __forceinline__ float warp_columns(float (&v)[32], int lane) {
+#pragma unroll
+    for (int s = 16; s >= 1; s >>= 1) {
+        const bool upper = (lane & s) != 0;
+#pragma unroll
+        for (int i = 0; i < s; ++i) {
+            const float send = upper ? v[i] : v[i + s];
+            const float keep = upper ? v[i + s] : v[i];
+            const float got = __shfl_xor_sync(kFull, send, s);
+            v[i] = MAX ? fmaxf(keep, got) : keep + got;
+        }
+    }
+    return v[0];
+}
+
+__global__ void __launch_bounds__(kThreads, 1) attn_tc_kv8_kernel(AttnParams p) {
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    unsigned char* sm = smem_raw;
+    unsigned char* sQ = sm + kOffQ;
+    unsigned char* sSlot = sm + kOffSlot;
+    unsigned char* sP = sSlot + kRope * kSlotBytes;
+    float* sM = reinterpret_cast<float*>(sm + kOffM);
+    float* sAlpha = reinterpret_cast<float*>(sm + kOffAlpha);
+    float* sRed = reinterpret_cast<float*>(sm + kOffRed);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kOffBar);
+    volatile int* sAbort = reinterpret_cast<volatile int*>(sm + kOffMisc);
+    uint32_t* sTmem = reinterpret_cast<uint32_t*>(sm + kOffMisc + 4);
+    int64_t* sInfo = reinterpret_cast<int64_t*>(sm + kOffMisc + 8);
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int64_t item = blockIdx.x;
+    const int hbase = blockIdx.y * kHC;
+
+    if (warp == 0) {
+        int64_t r0 = 0, r1 = 0;
+        int b = locate_item(p, item, lane, &r0, &r1);
+        if (smem_u32(smem_raw) & 1023u) {
+            if (lane == 0) set_err(p.err, KVQ_ERR_DEVICE);
+            b = -1;
+        }
+        if (lane == 0) {
+            sInfo[0] = b;
+            sInfo[1] = r0;
+            sInfo[2] = r1;
+        }
+    }
+    __syncthreads();
+    const int b = (int)sInfo[0];
+    if (b < 0) return;
+    const int64_t row0 = sInfo[1], row1 = sInfo[2];
+    const int n_tiles = (int)((row1 - row0 + kRows - 1) / kRows);
+
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(sTmem)),
+                     "r"(kTmemCols));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
+    if (tid == 64) {
+        for (int i = 0; i < kNumBars; ++i) {
+            const uint32_t count = (i < kBarFree0 || i == kBarP) ? (uint32_t)kWorkers : 1u;
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(&bars[i])), "r"(count));
+        }
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        *sAbort = 0;
+    }
+    if (tid < kHC) sM[tid] = -INFINITY;
+    if (tid == 0) {
+        const int64_t n = min((int64_t)kRows, row1 - row0);
+        prefetch_l2(p.codes + row0 * kMlaD, (uint32_t)(n * kMlaD));
+    }
+
+    // ---- query: 64 heads x 576 bf16, 18 16-byte loads per worker held in
+    // registers; largest |q| and largest latent scale of the chunk ----
+    const int64_t qbase = ((int64_t)b * p.n_heads + hbase) * kMlaD;
+    constexpr int kQPer = kHC * kMlaD / 8 / kWorkers;   // 18
+    static_assert(kHC * kMlaD / 8 == kQPer * kWorkers, "query loads per worker");
+    uint4 qraw[kQPer];
+    if (tid < kWorkers) {
+        const uint4* qv = reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(p.q) + qbase);
+        float qmax = 0.0f, smax = 0.0f;
+#pragma unroll
+        for (int i = 0; i < kQPer; ++i) qraw[i] = __ldg(qv + tid + i * kWorkers);
+        for (int64_t r = row0 + tid; r < row1; r += kWorkers) smax = fmaxf(smax, p.scales[r * p.n_blocks]);
+#pragma unroll
+        for (int i = 0; i < kQPer; ++i) {
+            const uint32_t in[4] = {qraw[i].x, qraw[i].y, qraw[i].z, qraw[i].w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                qmax = fmaxf(qmax, fabsf(__uint_as_float(in[k] << 16)));
+                qmax = fmaxf(qmax, fabsf(__uint_as_float(in[k] & 0xffff0000u)));
+            }
+        }
+        qmax = warp_max(qmax);
+        smax = warp_max(smax);
+        if (lane == 0) {
+            sRed[warp] = qmax;
+            sRed[8 + warp] = smax;
+        }
+    }
+    __syncthreads();
+    float q_max = 0.0f, s_max = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        q_max = fmaxf(q_max, sRed[i]);
+        s_max = fmaxf(s_max, sRed[8 + i]);
+    }
+    int e_s = 0, e_q = 0;
+    if (s_max > 0.0f) frexpf(s_max, &e_s);
+    if (q_max > 0.0f) frexpf(q_max, &e_q);
+    // |q| * q_scale < 2^14: every product with a code (|c| <= 448) and every
+    // 576-term sum stays finite in f32, and a bf16 value scaled by a power of
+    // two is exact in f16 unless it is below 2^-17 of the scaled maximum range
+    // (its residual, under 2^-24 after scaling, is dropped)
+    const float s_ref = s_max > 0.0f ? ldexpf(1.0f, e_s) : 1.0f;
+    const float inv_s_ref = s_max > 0.0f ? ldexpf(1.0f, -e_s) : 1.0f;
+    const float q_scale = q_max > 0.0f ? ldexpf(1.0f, 14 - e_q) : 1.0f;
+    const float cz = p.sm_scale * kLog2e * (q_max > 0.0f ? ldexpf(1.0f, e_q - 14) : 1.0f);
+
+    if (tid < kWorkers) {
+#pragma unroll
+        for (int i = 0; i < kQPer; ++i) {
+            const int u = tid + i * kWorkers;
+            const int e = u * 8, h = e / kMlaD, d = e - h * kMlaD;
+            const uint32_t in[4] = {qraw[i].x, qraw[i].y, qraw[i].z, qraw[i].w};
+            uint32_t hw[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const __half2 h2 = __floats2half2_rn(__uint_as_float(in[k] << 16) * q_scale,
+                                                     __uint_as_float(in[k] & 0xffff0000u) * q_scale);
+                hw[k] = *reinterpret_cast<const uint32_t*>(&h2);
+            }
+            *reinterpret_cast<uint4*>(sQ + (d >> 6) * kQChunkBytes + sw128(h, (d & 63) * 2)) =
+                make_uint4(hw[0], hw[1], hw[2], hw[3]);
+        }
+    }
+    fence_async_smem();
+    tc_before();
+    __syncthreads();
+    tc_after();
+    const uint32_t tmem = *sTmem;
+
+    if (warp == kWorkers / 32) {
+        // ================= MMA warp: lane 0 issues =================
+        if (lane == 0) {
+            const uint64_t dq0 = umma_desc(smem_u32(sQ), 16, 1024);
+            const uint64_t dslot0 = umma_desc(smem_u32(sSlot), 16, 1024);
+            const uint64_t dpair0 = umma_desc(smem_u32(sSlot), kSlotBytes, 1024);
+            const uint64_t dp = umma_desc(smem_u32(sP), kSlotBytes, 1024);
+            constexpr uint64_t kQStep = kQChunkBytes >> 4, kSlotStep = kSlotBytes >> 4;
+            bool ok = true;
+            for (int t = 0; t < n_tiles && ok; ++t) {
+                const uint32_t par = (uint32_t)t & 1u;
+#pragma unroll 1
+                for (int kc = 0; kc < kChunks && ok; ++kc) {
+                    ok = mbar_wait(&bars[kBarFull0 + kc], par, sAbort);
+                    tc_after();
+                    const uint32_t d = tmem + (kc < kRope ? kColSL : kColSR);
+                    const uint64_t a = dslot0 + kc * kSlotStep, bq = dq0 + kc * kQStep;
+                    const bool first = kc == 0 || kc == kRope;
+#pragma unroll
+                    for (int ks = 0; ks < 4; ++ks)
+                        umma_f16(d, a + 2 * ks, bq + 2 * ks, kIdescScore, (first && ks == 0) ? 0u : 1u);
+                }
+                umma_commit(&bars[kBarScore]);
+                ok = ok && mbar_wait(&bars[kBarP], par, sAbort);
+                tc_after();
+#pragma unroll 1
+                for (int db = 0; db < 4 && ok; ++db) {
+                    const uint32_t d = tmem + kColO + 64 * db;
+                    const uint64_t a = dpair0 + 2 * db * kSlotStep;
+#pragma unroll
+                    for (int ks = 0; ks < 8; ++ks)
+                        umma_f16(d, a + 128 * ks, dp + 128 * ks, kIdescCtx, (t > 0 || ks > 0) ? 1u : 0u);
+                    umma_commit(&bars[kBarFree0 + db]);
+                }
+            }
+            umma_commit(&bars[kBarDone]);
+        }
+        return;
+    }
+
+    // ================= workers =================
+    const int crow = tid >> 1, ch = tid & 1;            // decode: row and half
+    const int srow = 32 * (warp & 3) + lane;            // softmax: TMEM lane / row
+    const int hq = warp >> 2;                            // softmax: heads 32 hq .. 32 hq + 31
+    const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
+    // running row sum of head 32 hq + lane over the rows of quadrant (warp & 3)
+    float lcol = 0.0f;
+
+    RawA rawA;
+    RawB rawB;
+    load_part(rawA, p.codes, row0, (int)min((int64_t)kRows, row1 - row0), crow, ch);
+    load_part(rawB, p.codes, row0, (int)min((int64_t)kRows, row1 - row0), crow, ch);
+    int t = 0;
+    for (; t < n_tiles; ++t) {
+        const int64_t t0 = row0 + (int64_t)t * kRows;
+        const int nt = (int)min((int64_t)kRows, row1 - t0);
+        if (tid == 0 && t0 + kRows < row1) {
+            const int64_t n = min((int64_t)kRows, row1 - (t0 + kRows));
+            prefetch_l2(p.codes + (t0 + kRows) * kMlaD, (uint32_t)(n * kMlaD));
+        }
+        float my_sl = 0.0f, my_sr = 0.0f;
+        if (srow < nt) {
+            const int64_t r = t0 + srow;
+            my_sl = p.scales[r * p.n_blocks];
+            my_sr = p.scales[r * p.n_blocks + (p.n_blocks - 1)];
+        }
+        // ---- decode the 9 chunks of this tile ----
+        const uint32_t prev = (uint32_t)(t - 1) & 1u;
+#pragma unroll
+        for (int kc = 0; kc < kChunks; ++kc) {
+            if (t > 0 && (kc & 1) == 0) mbar_wait(&bars[kBarFree0 + (kc < kRope ? kc >> 1 : 3)], prev, sAbort);
+            unsigned char* slot = sSlot + kc * kSlotBytes;
+            const uint4& c0 = kc < kPartA ? rawA.v[kc][0] : rawB.v[kc - kPartA][0];
+            const uint4& c1 = kc < kPartA ? rawA.v[kc][1] : rawB.v[kc - kPartA][1];
+            store16(slot, c0, crow, 32 * ch);
+            store16(slot, c1, crow, 64 + 32 * ch);
+            fence_async_smem();
+            mbar_arrive(&bars[kBarFull0 + kc]);
+        }
+        const int64_t t1 = t0 + kRows;
+        const int nt1 = (int)min((int64_t)kRows, row1 - t1);
+        if (t + 1 < n_tiles) load_part(rawA, p.codes, t1, nt1, crow, ch);
+
+        // ---- softmax of the tile: thread = row srow, 32 heads ----
+        mbar_wait(&bars[kBarScore], (uint32_t)t & 1u, sAbort);
+        tc_after();
+        // z = sm log2(e) (s_L S_L + s_R S_R) for this row's 32 heads, read from TMEM
+        float z[32];
+        const float za = my_sl * cz, zb = my_sr * cz;
+        const bool row_ok = srow < nt;
+        auto load_z = [&]() {
+            uint32_t s32[32];
+            tmem_ld32(tmem + lane_base + kColSR + 32 * hq, s32);
+            tmem_wait_ld();
+#pragma unroll
+            for (int j = 0; j < 32; ++j) z[j] = __uint_as_float(s32[j]) * zb;
+            tmem_ld32(tmem + lane_base + kColSL + 32 * hq, s32);
+            tmem_wait_ld();
+#pragma unroll
+            for (int j = 0; j < 32; ++j) z[j] = row_ok ? fmaf(__uint_as_float(s32[j]), za, z[j]) : -INFINITY;
+        };
+        load_z();
+        bool flag = *sAbort != 0;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) flag |= z[j] > sM[32 * hq + j] + 8.0f;
+        if (worker_any(flag)) {
+            if (worker_any(*sAbort != 0)) break;
+            // exact column max of the tile, new running max, rescale factors
+            sRed[(warp & 3) * kHC + 32 * hq + lane] = warp_columns<true>(z, lane);
+            worker_sync();
+            if (tid < kHC) {
+                const float c4 = fmaxf(fmaxf(sRed[tid], sRed[kHC + tid]), fmaxf(sRed[2 * kHC + tid], sRed[3 * kHC + tid]));
+                const float mo = sM[tid], mn = fmaxf(mo, c4);
+                sAlpha[tid] = mo == -INFINITY ? 0.0f : ex2(mo - mn);
+                sM[tid] = mn;
+            }
+            worker_sync();
+            if (t > 0) {
+                // O^T is stable: the score commit of this tile follows every
+                // context MMA of the previous one
+#pragma unroll 1
+                for (int bi = 0; bi < 2; ++bi)
+#pragma unroll 1
+                    for (int c = 0; c < 2; ++c) {
+                        const uint32_t ta = tmem + lane_base + kColO + 64 * (2 * hq + bi) + 32 * c;
+                        uint32_t o[32];
+                        tmem_ld32(ta, o);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * sAlpha[32 * c + j]);
+                        tmem_st32(ta, o);
+                    }
+                tmem_wait_st();
+            }
+            lcol *= sAlpha[32 * hq + lane];
+            load_z();   // the reduction consumed z
+        }
+        {
+            const float wrow = my_sl * inv_s_ref;
+            uint32_t pk[16];
+#pragma unroll
+            for (int j = 0; j < 32; j += 2) {
+                z[j] = ex2(z[j] - sM[32 * hq + j]);
+                z[j + 1] = ex2(z[j + 1] - sM[32 * hq + j + 1]);
+                const __half2 h2 = __floats2half2_rn(z[j] * wrow, z[j + 1] * wrow);
+                pk[j / 2] = *reinterpret_cast<const uint32_t*>(&h2);
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                *reinterpret_cast<uint4*>(sP + sw128(srow, 64 * hq + 16 * i)) =
+                    make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+        }
+        fence_async_smem();
+        tc_before();
+        mbar_arrive(&bars[kBarP]);
+        lcol += warp_columns<false>(z, lane);
+        if (t + 1 < n_tiles) load_part(rawB, p.codes, t1, nt1, crow, ch);
+    }
+
+    // ---- epilogue: wait for every MMA, row sums, O^T -> partial state ----
+    {
+        // bounded, and not cut short by the abort flag: TMEM is released only
+        // after the MMAs in flight have completed
+        volatile int never = 0;
+        if (!mbar_wait(&bars[kBarDone], 0u, &never)) *sAbort = 1;
+    }
+    tc_after();
+    const bool aborted = worker_any(*sAbort != 0 || t < n_tiles);
+    {
+        worker_sync();   // sRed may still be read by the last exact-max pass
+        sRed[(warp & 3) * kHC + 32 * hq + lane] = lcol;
+        worker_sync();
+        if (tid < kHC) sAlpha[tid] = (sRed[tid] + sRed[kHC + tid]) + (sRed[2 * kHC + tid] + sRed[3 * kHC + tid]);
+        worker_sync();
+    }
+    if (aborted) {
+        if (tid == 0) set_err(p.err, KVQ_ERR_DEVICE);
+    } else {
+#pragma unroll
+        for (int bi = 0; bi < 2; ++bi) {
+            const int db = 2 * hq + bi;
+            const int dim = 128 * db + 32 * (warp & 3) + lane;
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                uint32_t v[32];
+                tmem_ld32(tmem + lane_base + kColO + 64 * db + 32 * c, v);
+                tmem_wait_ld();
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    const int h = hbase + 32 * c + j;
+                    p.ws_o[(item * p.n_heads + h) * kMlaDV + dim] = n_tiles > 0 ? __uint_as_float(v[j]) * s_ref : 0.0f;
+                }
+            }
+        }
+        if (tid < kHC) {
+            float* ml = p.ws_ml + (item * p.n_heads + hbase + tid) * 2;
+            ml[0] = sM[tid] * kLn2;
+            ml[1] = sAlpha[tid];
+        }
+    }
+    tc_before();
+    worker_sync();
+    tc_after();
+    if (warp == 1) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols));
+}
+
+}  // namespace
+
+cudaError_t launch_attn_tc_kv8_bf16(const AttnParams& p, int64_t grid_x, int groups, cudaStream_t stream) {
+    cudaError_t e =
+        cudaFuncSetAttribute(attn_tc_kv8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemUsed);
+    if (e != cudaSuccess) return e;
+    attn_tc_kv8_kernel<<<dim3((unsigned)grid_x, (unsigned)groups), kThreads, kSmemUsed, stream>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace kvq
