@@ -44,13 +44,21 @@ __device__ __forceinline__ int64_t n_chunks_of(const int64_t* cu, int b, int64_t
 }
 
 // Warp-cooperative search for the sequence owning work item `item`.
-// Returns b (or -1) and the chunk index within b.
+// Returns b (or -1), the chunk index within b and, from the bounds the search
+// has already read, the chunk's row range [row0, row1).
 __device__ __forceinline__ int find_item(const int64_t* cu, int n_seq, int64_t chunk, int64_t item, int lane,
-                                         int64_t* ch_out, int32_t* err) {
+                                         int64_t* ch_out, int32_t* err, int64_t* row0 = nullptr,
+                                         int64_t* row1 = nullptr) {
     int64_t base = 0;
     for (int b0 = 0; b0 < n_seq; b0 += 32) {
         const int b = b0 + lane;
-        const int64_t n = b < n_seq ? n_chunks_of(cu, b, chunk, err) : 0;
+        int64_t s = 0, e = 0, n = 0;
+        if (b < n_seq) {
+            s = cu[b];
+            e = cu[b + 1];
+            if (e < s) set_err(err, KVQ_ERR_ARG);
+            else n = (e - s + chunk - 1) / chunk;
+        }
         int64_t incl = n;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -63,7 +71,13 @@ __device__ __forceinline__ int find_item(const int64_t* cu, int n_seq, int64_t c
             const bool mine = b < n_seq && item >= base + excl && item < base + incl;
             const unsigned mask = __ballot_sync(kFull, mine);
             const int src = __ffs(mask) - 1;
-            *ch_out = item - base - __shfl_sync(kFull, excl, src);
+            const int64_t ch = item - base - __shfl_sync(kFull, excl, src);
+            const int64_t ss = __shfl_sync(kFull, s, src), ee = __shfl_sync(kFull, e, src);
+            *ch_out = ch;
+            if (row0) {
+                *row0 = ss + ch * chunk;
+                *row1 = min(*row0 + chunk, ee);
+            }
             return b0 + src;
         }
         base += total;
@@ -93,19 +107,13 @@ __device__ __forceinline__ int locate_item(const AttnParams& p, int64_t item, in
     int b = -1;
     int64_t ch = 0;
     if (p.prefill_past >= 0) {
-        if (item < p.n_seq) b = (int)item;
-    } else {
-        b = find_item(p.cu, p.n_seq, p.chunk, item, lane, &ch, p.err);
-    }
-    if (b >= 0) {
-        if (p.prefill_past >= 0) {
+        if (item < p.n_seq) {
+            b = (int)item;
             *row0 = 0;
             *row1 = p.prefill_past + b + 1;
-        } else {
-            const int64_t s = p.cu[b], e = p.cu[b + 1];
-            *row0 = s + ch * p.chunk;
-            *row1 = min(*row0 + p.chunk, e);
         }
+    } else {
+        b = find_item(p.cu, p.n_seq, p.chunk, item, lane, &ch, p.err, row0, row1);
     }
     return b;
 }

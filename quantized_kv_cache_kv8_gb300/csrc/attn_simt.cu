@@ -295,19 +295,44 @@ __global__ void __launch_bounds__(128) attn_merge_kernel(AttnParams p, float* __
         if (tid == 0) set_err(p.err, KVQ_ERR_DEVICE);
         count = 0;
     }
-    float M = -INFINITY;
-    for (int64_t c = 0; c < count; ++c) M = fmaxf(M, p.ws_ml[((first + c) * p.n_heads + h) * 2]);
-    float L = 0.0f;
+    // one pass over the chunks, 8 at a time: their loads go out together, then
+    // an online log-sum-exp combine (running max M, sum L, weighted context)
+    float M = -INFINITY, L = 0.0f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int64_t c = 0; c < count; ++c) {
-        const float* ml = p.ws_ml + ((first + c) * p.n_heads + h) * 2;
-        const float w = (M == -INFINITY) ? 0.0f : expf(ml[0] - M);
-        L += w * ml[1];
-        const float4 v = *reinterpret_cast<const float4*>(p.ws_o + ((first + c) * p.n_heads + h) * kDV + 4 * tid);
-        acc.x = fmaf(w, v.x, acc.x);
-        acc.y = fmaf(w, v.y, acc.y);
-        acc.z = fmaf(w, v.z, acc.z);
-        acc.w = fmaf(w, v.w, acc.w);
+    constexpr int kBatch = 8;
+    for (int64_t c0 = 0; c0 < count; c0 += kBatch) {
+        float mv[kBatch], lw[kBatch];
+        float4 ov[kBatch];
+#pragma unroll
+        for (int k = 0; k < kBatch; ++k) {
+            mv[k] = -INFINITY;
+            lw[k] = 0.0f;
+            ov[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (c0 + k < count) {
+                const int64_t row = (first + c0 + k) * p.n_heads + h;
+                const float2 ml = *reinterpret_cast<const float2*>(p.ws_ml + row * 2);
+                mv[k] = ml.x;
+                lw[k] = ml.y;
+                ov[k] = *reinterpret_cast<const float4*>(p.ws_o + row * kDV + 4 * tid);
+            }
+        }
+        float mb = M;
+#pragma unroll
+        for (int k = 0; k < kBatch; ++k) mb = fmaxf(mb, mv[k]);
+        if (mb == -INFINITY) continue;   // nothing but empty partials so far
+        const float keep = M == -INFINITY ? 0.0f : expf(M - mb);
+        L *= keep;
+        acc = make_float4(acc.x * keep, acc.y * keep, acc.z * keep, acc.w * keep);
+#pragma unroll
+        for (int k = 0; k < kBatch; ++k) {
+            const float w = mv[k] == -INFINITY ? 0.0f : expf(mv[k] - mb);
+            L = fmaf(w, lw[k], L);
+            acc.x = fmaf(w, ov[k].x, acc.x);
+            acc.y = fmaf(w, ov[k].y, acc.y);
+            acc.z = fmaf(w, ov[k].z, acc.z);
+            acc.w = fmaf(w, ov[k].w, acc.w);
+        }
+        M = mb;
     }
     const float inv = L > 0.0f ? 1.0f / L : 0.0f;
     acc = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);

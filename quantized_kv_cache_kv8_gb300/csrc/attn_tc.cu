@@ -24,8 +24,9 @@
 // The running max per head is lagged: rows are exponentiated against the max
 // of the previous tiles and a tile takes an exact slow path (column max over
 // the tile, rescale of O^T in TMEM) only when some score exceeds that max by
-// more than 2^8.  Row sums are accumulated per thread and reduced across the
-// 128 rows once per chunk.  The partial state written for the merge is the
+// more than 2^14 (weights and their f16 copies then stay below 2^14).  Row
+// sums are accumulated per thread and reduced across the 128 rows once per
+// chunk.  The partial state written for the merge is the
 // same as the SIMT path's, in natural-log units.
 #include "tc_common.cuh"
 
@@ -569,7 +570,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnParams p) {
         }
         bool flag = false;
 #pragma unroll
-        for (int j = 0; j < 32; ++j) flag |= z[j] > sM[32 * hq + j] + 8.0f;
+        for (int j = 0; j < 32; ++j) flag |= z[j] > sM[32 * hq + j] + 14.0f;
         if (worker_any(flag)) {
             // exact column max of the tile, new running max, rescale factors
             float* zbuf = reinterpret_cast<float*>(sSlot);   // 128 x 64 f32 over slots 0-1 (idle now)

@@ -15,14 +15,20 @@
 // chunk's slot once the score of the tile has completed.
 //
 // Pipeline per tile t (8 worker warps, 1 MMA warp):
-//   workers: decode chunk kc of tile t into slot kc as soon as the context of
-//            tile t-1 has released it (slot pair kc/2; the rope slot with the
-//            last pair), then issue the loads of tile t+1 into registers, then
-//            the softmax of tile t (thread = row, 32 heads), then P^T.
-//   MMA:     score of tile t chunk by chunk, commit; once P^T(t) is written,
+//   workers: decode the tile in three groups -- chunks 0-3 (row bytes
+//            0..255), chunks 4-7 (256..511), the rope chunk 8 (512..575) --
+//            each as soon as the context of tile t-1 has released its slots,
+//            then the softmax of tile t (thread = row, 32 heads), then P^T.
+//            The raw bytes of tile t+1 are loaded into registers during tile t
+//            (group A before the softmax, groups B and C after P^T).
+//   MMA:     score of tile t group by group, commit; once P^T(t) is written,
 //            the 4 context blocks, each committed to its slot pair's barrier.
 // The decode of tile t+1 thus overlaps the context MMAs of tile t, and the
-// score MMAs of tile t+1 follow the decode chunk by chunk.
+// score MMAs of tile t+1 follow the decode group by group.
+//
+// Loads are laid out so that each warp instruction reads whole rows: in groups
+// A and B a half-warp reads the 256 contiguous bytes of one row (2 rows per
+// instruction, 4 cache lines), in group C 8 rows of 64 bytes.
 //
 // Reductions over the 128 rows of a tile (column max in the softmax's exact
 // path, the row sums at the end) run as a 31-shuffle transpose-reduce within
@@ -62,41 +68,47 @@ static_assert(kSmemUsed <= 232448, "shared memory budget");
 // TMEM columns: O^T blocks 0..255, S_L^T 256..319, S_R^T 320..383
 constexpr uint32_t kColO = 0, kColSL = 256, kColSR = 320, kTmemCols = 512;
 
-// mbarriers: chunk kc stored (256 arrivals), slot pair db released by the
-// context (MMA commit; the last pair also releases the rope/P^T slot), score
-// complete (MMA commit), P^T written (256 arrivals), every MMA of the CTA
-// complete (the MMA warp's last commit, also after an abort)
-enum { kBarFull0 = 0, kBarFree0 = 9, kBarScore = 13, kBarP = 14, kBarDone = 15, kNumBars = 16 };
+// mbarriers: decode group g stored (256 arrivals; A = chunks 0-3, B = 4-7,
+// C = the rope chunk), slot pair db released by the context (MMA commit; the
+// last pair also releases the rope/P^T slot), score complete (MMA commit), P^T
+// written (256 arrivals), every MMA of the CTA complete (the MMA warp's last
+// commit, also after an abort)
+enum { kBarFull0 = 0, kBarFree0 = 3, kBarScore = 7, kBarP = 8, kBarDone = 9, kNumBars = 10 };
+
+// The running max may lag the true one by up to 2^14: softmax weights stay
+// below 2^14 and their f16 copies (times s_L / S_ref <= 1) below 65504.
+constexpr float kLagLog2 = 14.0f;
 
 constexpr uint32_t kIdescScore = idesc_f16(128, kHC, false, false);
 constexpr uint32_t kIdescCtx = idesc_f16(128, kHC, true, true);
 
-// One worker's raw share of chunks [K0, K0 + N) of a tile: row (tid / 2); for
-// each chunk kc, the 16 bytes at dims 64 kc + 16 h and the 16 at
-// 64 kc + 32 + 16 h (h = tid % 2), so that each load instruction of a warp
-// reads whole 32-byte sectors.  A tile's 9 chunks are held as a part of 5 and
-// a part of 4, loaded at different points of the previous tile.
-template <int K0, int N>
-struct RawPart {
-    uint4 v[N][2];
+// A worker's raw share of a tile.  Groups A and B: 8 pieces of 16 bytes, piece
+// i at row 2 (warp + 8 i) + lane / 16, bytes 16 (lane % 16) of the group's 256
+// (so the thread always serves chunk 4 g + (lane % 16) / 4, 16 dims at
+// 16 (lane % 4)).  Group C: 2 pieces, piece i at row (tid + 256 i) / 4, bytes
+// 16 (tid % 4) of the rope chunk.
+struct RawGroup {
+    uint4 v[8];
 };
-constexpr int kPartA = 5;   // chunks 0..4: loaded before the softmax of the previous tile
-using RawA = RawPart<0, kPartA>;
-using RawB = RawPart<kPartA, kChunks - kPartA>;
+struct RawRope {
+    uint4 v[2];
+};
 
-template <int K0, int N>
-__device__ __forceinline__ void load_part(RawPart<K0, N>& r, const uint8_t* __restrict__ codes, int64_t t0, int nt,
-                                          int row, int h) {
-    if (row < nt) {
-        const uint8_t* src = codes + (t0 + row) * kMlaD + 16 * h + 64 * K0;
+__device__ __forceinline__ void load_group(RawGroup& r, const uint8_t* __restrict__ codes, int64_t t0, int nt, int g,
+                                           int warp, int lane) {
 #pragma unroll
-        for (int k = 0; k < N; ++k) {
-            r.v[k][0] = __ldg(reinterpret_cast<const uint4*>(src + 64 * k));
-            r.v[k][1] = __ldg(reinterpret_cast<const uint4*>(src + 64 * k + 32));
-        }
-    } else {
+    for (int i = 0; i < 8; ++i) {
+        const int row = 2 * (warp + 8 * i) + (lane >> 4);
+        r.v[i] = row < nt ? __ldg(reinterpret_cast<const uint4*>(codes + (t0 + row) * kMlaD + 256 * g + 16 * (lane & 15)))
+                          : make_uint4(0u, 0u, 0u, 0u);
+    }
+}
+__device__ __forceinline__ void load_rope(RawRope& r, const uint8_t* __restrict__ codes, int64_t t0, int nt, int tid) {
 #pragma unroll
-        for (int k = 0; k < N; ++k) r.v[k][0] = r.v[k][1] = make_uint4(0u, 0u, 0u, 0u);
+    for (int i = 0; i < 2; ++i) {
+        const int u = tid + kWorkers * i, row = u >> 2;
+        r.v[i] = row < nt ? __ldg(reinterpret_cast<const uint4*>(codes + (t0 + row) * kMlaD + 512 + 16 * (u & 3)))
+                          : make_uint4(0u, 0u, 0u, 0u);
     }
 }
 
@@ -271,8 +283,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kv8_kernel(AttnParams p) 
                 const uint32_t par = (uint32_t)t & 1u;
 #pragma unroll 1
                 for (int kc = 0; kc < kChunks && ok; ++kc) {
-                    ok = mbar_wait(&bars[kBarFull0 + kc], par, sAbort);
-                    tc_after();
+                    if ((kc & 3) == 0) {
+                        ok = mbar_wait(&bars[kBarFull0 + (kc >> 2)], par, sAbort);
+                        tc_after();
+                    }
                     const uint32_t d = tmem + (kc < kRope ? kColSL : kColSR);
                     const uint64_t a = dslot0 + kc * kSlotStep, bq = dq0 + kc * kQStep;
                     const bool first = kc == 0 || kc == kRope;
@@ -299,17 +313,31 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kv8_kernel(AttnParams p) 
     }
 
     // ================= workers =================
-    const int crow = tid >> 1, ch = tid & 1;            // decode: row and half
     const int srow = 32 * (warp & 3) + lane;            // softmax: TMEM lane / row
     const int hq = warp >> 2;                            // softmax: heads 32 hq .. 32 hq + 31
     const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
     // running row sum of head 32 hq + lane over the rows of quadrant (warp & 3)
     float lcol = 0.0f;
 
-    RawA rawA;
-    RawB rawB;
-    load_part(rawA, p.codes, row0, (int)min((int64_t)kRows, row1 - row0), crow, ch);
-    load_part(rawB, p.codes, row0, (int)min((int64_t)kRows, row1 - row0), crow, ch);
+    // this thread's softmax row scales, one tile ahead
+    float sl_next = 0.0f, sr_next = 0.0f;
+    auto load_scales = [&](int64_t t0n, int ntn) {
+        sl_next = sr_next = 0.0f;
+        if (srow < ntn) {
+            const int64_t r = t0n + srow;
+            sl_next = p.scales[r * p.n_blocks];
+            sr_next = p.scales[r * p.n_blocks + (p.n_blocks - 1)];
+        }
+    };
+    RawGroup rawA, rawB;
+    RawRope rawC;
+    {
+        const int nt0 = (int)min((int64_t)kRows, row1 - row0);
+        load_group(rawA, p.codes, row0, nt0, 0, warp, lane);
+        load_group(rawB, p.codes, row0, nt0, 1, warp, lane);
+        load_rope(rawC, p.codes, row0, nt0, tid);
+        load_scales(row0, nt0);
+    }
     int t = 0;
     for (; t < n_tiles; ++t) {
         const int64_t t0 = row0 + (int64_t)t * kRows;
@@ -318,28 +346,35 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kv8_kernel(AttnParams p) 
             const int64_t n = min((int64_t)kRows, row1 - (t0 + kRows));
             prefetch_l2(p.codes + (t0 + kRows) * kMlaD, (uint32_t)(n * kMlaD));
         }
-        float my_sl = 0.0f, my_sr = 0.0f;
-        if (srow < nt) {
-            const int64_t r = t0 + srow;
-            my_sl = p.scales[r * p.n_blocks];
-            my_sr = p.scales[r * p.n_blocks + (p.n_blocks - 1)];
-        }
-        // ---- decode the 9 chunks of this tile ----
+        const float my_sl = sl_next, my_sr = sr_next;
+        // ---- decode the tile: groups A (chunks 0-3), B (4-7), C (rope) ----
         const uint32_t prev = (uint32_t)(t - 1) & 1u;
+        {
+            const int q4 = lane & 3, cg = (lane & 15) >> 2;
 #pragma unroll
-        for (int kc = 0; kc < kChunks; ++kc) {
-            if (t > 0 && (kc & 1) == 0) mbar_wait(&bars[kBarFree0 + (kc < kRope ? kc >> 1 : 3)], prev, sAbort);
-            unsigned char* slot = sSlot + kc * kSlotBytes;
-            const uint4& c0 = kc < kPartA ? rawA.v[kc][0] : rawB.v[kc - kPartA][0];
-            const uint4& c1 = kc < kPartA ? rawA.v[kc][1] : rawB.v[kc - kPartA][1];
-            store16(slot, c0, crow, 32 * ch);
-            store16(slot, c1, crow, 64 + 32 * ch);
+            for (int g = 0; g < 2; ++g) {
+                if (t > 0) {
+                    mbar_wait(&bars[kBarFree0 + 2 * g], prev, sAbort);
+                    mbar_wait(&bars[kBarFree0 + 2 * g + 1], prev, sAbort);
+                }
+                unsigned char* slot = sSlot + (4 * g + cg) * kSlotBytes;
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    store16(slot, g == 0 ? rawA.v[i] : rawB.v[i], 2 * (warp + 8 * i) + (lane >> 4), 32 * q4);
+                fence_async_smem();
+                mbar_arrive(&bars[kBarFull0 + g]);
+            }
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                const int u = tid + kWorkers * i;
+                store16(sSlot + kRope * kSlotBytes, rawC.v[i], u >> 2, 32 * (u & 3));
+            }
             fence_async_smem();
-            mbar_arrive(&bars[kBarFull0 + kc]);
+            mbar_arrive(&bars[kBarFull0 + 2]);
         }
         const int64_t t1 = t0 + kRows;
         const int nt1 = (int)min((int64_t)kRows, row1 - t1);
-        if (t + 1 < n_tiles) load_part(rawA, p.codes, t1, nt1, crow, ch);
+        if (t + 1 < n_tiles) load_group(rawA, p.codes, t1, nt1, 0, warp, lane);
 
         // ---- softmax of the tile: thread = row srow, 32 heads ----
         mbar_wait(&bars[kBarScore], (uint32_t)t & 1u, sAbort);
@@ -360,9 +395,16 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kv8_kernel(AttnParams p) 
             for (int j = 0; j < 32; ++j) z[j] = row_ok ? fmaf(__uint_as_float(s32[j]), za, z[j]) : -INFINITY;
         };
         load_z();
+        // the rest of tile t+1 is requested while the tensor cores are idle
+        // (their operand reads compete with these loads for the SM's memory pipe)
+        if (t + 1 < n_tiles) {
+            load_group(rawB, p.codes, t1, nt1, 1, warp, lane);
+            load_rope(rawC, p.codes, t1, nt1, tid);
+            load_scales(t1, nt1);
+        }
         bool flag = *sAbort != 0;
 #pragma unroll
-        for (int j = 0; j < 32; ++j) flag |= z[j] > sM[32 * hq + j] + 8.0f;
+        for (int j = 0; j < 32; ++j) flag |= z[j] > sM[32 * hq + j] + kLagLog2;
         if (worker_any(flag)) {
             if (worker_any(*sAbort != 0)) break;
             // exact column max of the tile, new running max, rescale factors
@@ -414,7 +456,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kv8_kernel(AttnParams p) 
         tc_before();
         mbar_arrive(&bars[kBarP]);
         lcol += warp_columns<false>(z, lane);
-        if (t + 1 < n_tiles) load_part(rawB, p.codes, t1, nt1, crow, ch);
     }
 
     // ---- epilogue: wait for every MMA, row sums, O^T -> partial state ----
