@@ -146,7 +146,7 @@ def run_ours(args, rank, world):
     q = inp["q_host"].to(dev)
     out = torch.empty((B, H, DV), dtype=torch.float32, device=dev)
     out_host = torch.empty((B, H, DV), dtype=torch.float32).pin_memory()
-    ws = torch.empty(kvq.kv_attn_workspace_size(kvq.KVQ_KV8, B, H, B * T, path=path), dtype=torch.uint8, device=dev)
+    ws = torch.zeros(kvq.kv_attn_workspace_size(kvq.KVQ_KV8, B, H, B * T, path=path), dtype=torch.uint8, device=dev)
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
 
     def step(xn, qq):

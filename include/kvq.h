@@ -22,8 +22,11 @@
  *     reported as a kvq_status; nothing is thrown across the ABI.  A launch
  *     failure returns KVQ_ERR_CUDA.  Conditions only the device can see (a
  *     ragged batch larger than the bound it was sized for, a non-monotone
- *     cu_seqlens) set an error word in the workspace, read with
- *     kvq_read_device_error; the kernels never trap.
+ *     cu_seqlens) set an error word in the workspace (its first 4 bytes),
+ *     read with kvq_read_device_error; the kernels never trap.  The word is
+ *     sticky: it keeps the first error of any call until read with `clear`,
+ *     and a decode/prefill workspace must start with it zero (allocate the
+ *     workspace zeroed, or clear it once with kvq_read_device_error).
  *   - The library keeps no global state; calls on different streams with
  *     different workspaces are independent.
  *   - Encoders are bit-exact by construction: IEEE f32 arithmetic in a fixed
@@ -214,8 +217,9 @@ kvq_status kv_attn_prefill(kvq_format fmt, const kvq_mla_layout* layout,
                            void* workspace, size_t workspace_bytes, kvq_path path, void* stream);
 
 /* Reads the device error word of a decode/prefill workspace (synchronizes
- * `stream`).  Returns 0 when clear, else a kvq_status value; clears it when
- * `clear` is non-zero. */
+ * `stream`).  Returns 0 when clear, else the kvq_status value of the first
+ * error recorded since it was last cleared; clears it when `clear` is
+ * non-zero. */
 int32_t kvq_read_device_error(void* workspace, int32_t clear, void* stream);
 
 /* ------------------------------------------------------------------------ */

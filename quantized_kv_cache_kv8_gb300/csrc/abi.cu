@@ -186,8 +186,6 @@ kvq_status kv_attn_decode(kvq_format fmt, const kvq_mla_layout* layout, const vo
     const size_t need = kv_attn_workspace_size(fmt, layout, batch, n_heads, max_total_rows, path);
     if (!workspace || workspace_bytes < need) return KVQ_ERR_WORKSPACE;
     cudaStream_t st = (cudaStream_t)stream;
-    cudaError_t e = cudaMemsetAsync(workspace, 0, sizeof(int32_t), st);
-    if (e != cudaSuccess) return KVQ_ERR_CUDA;
     const AttnPlan pl = plan_decode(rp, batch, n_heads, max_total_rows);
     if (rp == KVQ_PATH_TENSOR)
         return cuda_status(launch_attn_tc(fmt, *layout, q, q_dtype, batch, n_heads, codes, scales, cu_seqlens, -1, pl,
@@ -239,7 +237,6 @@ kvq_status kv_attn_prefill(kvq_format fmt, const kvq_mla_layout* layout, const f
         e = launch_tq4_encode(x_new, n_new, *layout, nullptr, codes + n_past * row_bytes,
                               scales + n_past * layout->n_blocks, st);
     if (e != cudaSuccess) return KVQ_ERR_CUDA;
-    if ((e = cudaMemsetAsync(workspace, 0, sizeof(int32_t), st)) != cudaSuccess) return KVQ_ERR_CUDA;
     const AttnPlan pl = plan_prefill(n_past, n_new);
     if (rp == KVQ_PATH_TENSOR)
         return cuda_status(launch_attn_tc(fmt, *layout, q, q_dtype, (int32_t)n_new, n_heads, codes, scales, nullptr,

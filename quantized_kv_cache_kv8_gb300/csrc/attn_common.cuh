@@ -33,6 +33,13 @@ struct AttnParams {
 
 __device__ __forceinline__ void set_err(int32_t* err, int32_t code) { atomicCAS(err, 0, code); }
 
+// Programmatic dependent launch: a partial kernel lets the dependent merge grid
+// be scheduled early; the merge waits for the partial grid's completion (and
+// the visibility of its writes) before it reads the partial state.  Both are
+// no-ops when the launch carries no programmatic dependency.
+__device__ __forceinline__ void launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // Number of chunks of sequence b (0 for an empty or malformed range).
 __device__ __forceinline__ int64_t n_chunks_of(const int64_t* cu, int b, int64_t chunk, int32_t* err) {
     const int64_t len = cu[b + 1] - cu[b];

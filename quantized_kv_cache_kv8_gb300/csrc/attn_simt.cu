@@ -36,6 +36,7 @@ constexpr size_t kSmemFloats = (size_t)kHG * kXS + (size_t)kTR * kXS + kTR * 2 +
 
 template <int FMT, bool QBF16>
 __global__ void __launch_bounds__(kNT, 2) attn_partial_kernel(AttnParams p) {
+    launch_dependents();
     extern __shared__ float4 smem4[];
     float* qs = reinterpret_cast<float*>(smem4);
     float* xs = qs + kHG * kXS;
@@ -289,6 +290,7 @@ __global__ void __launch_bounds__(128) attn_merge_kernel(AttnParams p, float* __
         }
     }
     __syncthreads();
+    grid_dependency_wait();   // the partial state is complete and visible past this point
     const int64_t first = info[0];
     int64_t count = info[1];
     if (first + count > p.max_items) {
@@ -434,12 +436,22 @@ cudaError_t launch_attn_simt(kvq_format fmt, const kvq_mla_layout& L, const void
     return launch_attn_merge(fmt, p, out, stream);
 }
 
+// The merge is launched as a programmatic dependent of the partial kernel: its
+// CTAs may start (and find their chunks) while the partial kernel drains, and
+// wait for its completion before reading the partial state.
 cudaError_t launch_attn_merge(kvq_format fmt, const AttnParams& p, float* out, cudaStream_t stream) {
-    if (fmt == KVQ_KV8)
-        attn_merge_kernel<KVQ_KV8><<<dim3(p.n_heads, p.n_seq), 128, 0, stream>>>(p, out);
-    else
-        attn_merge_kernel<KVQ_TQ4><<<dim3(p.n_heads, p.n_seq), 128, 0, stream>>>(p, out);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)p.n_heads, (unsigned)p.n_seq);
+    cfg.blockDim = dim3(128);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (fmt == KVQ_KV8) return cudaLaunchKernelEx(&cfg, attn_merge_kernel<KVQ_KV8>, p, out);
+    return cudaLaunchKernelEx(&cfg, attn_merge_kernel<KVQ_TQ4>, p, out);
 }
 
 }  // namespace kvq

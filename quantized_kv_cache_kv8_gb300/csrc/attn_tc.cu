@@ -169,6 +169,7 @@ __device__ __forceinline__ void store_delta_chunk(const RawChunk& c, bool valid,
 constexpr int kRing = 5;      // stages; chunk k + 4 is copied while chunk k is converted
 template <int FMT, bool QBF16, bool LOQ>
 __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnParams p) {
+    launch_dependents();
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char* sm = smem_raw;
     unsigned char* sQ = sm + kOffQ;

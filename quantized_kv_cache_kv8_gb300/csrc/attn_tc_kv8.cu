@@ -145,6 +145,7 @@ __device__ __forceinline__ float warp_columns(float (&v)[32], int lane) {
 }
 
 __global__ void __launch_bounds__(kThreads, 1) attn_tc_kv8_kernel(AttnParams p) {
+    launch_dependents();
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char* sm = smem_raw;
     unsigned char* sQ = sm + kOffQ;

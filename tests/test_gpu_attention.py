@@ -27,7 +27,7 @@ def run_decode(kvq, fmt, lens, H, bf16, seed, path, layout=None, max_rows=None):
     qd, qv = queries(seed + 1, (len(lens), H, 576), bf16)
     out = torch.full((len(lens), H, 512), float("nan"), device="cuda")
     max_rows = int(cu[-1]) if max_rows is None else max_rows
-    ws = torch.empty(kvq.kv_attn_workspace_size(fmt, len(lens), H, max_rows, layout, path), dtype=torch.uint8,
+    ws = torch.zeros(kvq.kv_attn_workspace_size(fmt, len(lens), H, max_rows, layout, path), dtype=torch.uint8,
                      device="cuda")
     kvq.kv_attn_decode(fmt, qd, codes, scales, to_dev(cu), out, ws, max_rows, SM, layout, path)
     torch.cuda.synchronize()
@@ -137,7 +137,7 @@ def test_prefill_small(kvq, oracle, fmt, H, path):
     scales[:n_past] = ps
     qd, qv = queries(32, (n_new, H, 576), False)
     out = torch.empty((n_new, H, 512), device="cuda")
-    ws = torch.empty(kvq.kv_attn_prefill_workspace_size(fmt, H, n_past, n_new, layout, pth), dtype=torch.uint8,
+    ws = torch.zeros(kvq.kv_attn_prefill_workspace_size(fmt, H, n_past, n_new, layout, pth), dtype=torch.uint8,
                      device="cuda")
     kvq.kv_attn_prefill(fmt, to_dev(x_all[n_past:]), qd, codes, scales, n_past, out, ws, SM, layout, pth)
     torch.cuda.synchronize()

@@ -66,7 +66,7 @@ def test_config4_ragged_decode(kvq, oracle, ragged_inputs, fmt, path):
     del idx_t
     total = int(cu[-1])
     out = torch.full((B, H, 512), float("nan"), device="cuda")
-    ws = torch.empty(kvq.kv_attn_workspace_size(fmt, B, H, total, layout, pth), dtype=torch.uint8, device="cuda")
+    ws = torch.zeros(kvq.kv_attn_workspace_size(fmt, B, H, total, layout, pth), dtype=torch.uint8, device="cuda")
     kvq.kv_attn_decode(fmt, _bf16_dev(d["q_bits"]), codes, scales, to_dev(cu), out, ws, total, SM, layout, pth)
     torch.cuda.synchronize()
     assert kvq.read_device_error(ws) == 0
@@ -113,7 +113,7 @@ def test_config4_prefill(kvq, oracle, prefill_inputs, fmt, path):
     scales[:n_past] = ps
     del pc, ps
     out = torch.full((n_new, H, 512), float("nan"), device="cuda")
-    ws = torch.empty(kvq.kv_attn_prefill_workspace_size(fmt, H, n_past, n_new, layout, pth), dtype=torch.uint8,
+    ws = torch.zeros(kvq.kv_attn_prefill_workspace_size(fmt, H, n_past, n_new, layout, pth), dtype=torch.uint8,
                      device="cuda")
     kvq.kv_attn_prefill(fmt, to_dev(x[n_past:]), _bf16_dev(d["q_bits"]), codes, scales, n_past, out, ws, SM,
                         layout, pth)

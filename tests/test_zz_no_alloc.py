@@ -29,7 +29,7 @@ def _case(kvq, fmt, lens, H, bf16, seed):
     qd, _ = queries(seed + 1, (len(lens), H, 576), bf16)
     cu_d = to_dev(cu)
     ref = torch.empty((len(lens), H, 512), device="cuda")
-    ws = torch.empty(kvq.kv_attn_workspace_size(fmt, len(lens), H, total, layout), dtype=torch.uint8, device="cuda")
+    ws = torch.zeros(kvq.kv_attn_workspace_size(fmt, len(lens), H, total, layout), dtype=torch.uint8, device="cuda")
     kvq.kv_attn_decode(fmt, qd, codes, scales, cu_d, ref, ws, total, SM, layout)
     got = torch.full((len(lens), H, 512), float("nan"), device="cuda")
     kvq.kv_attn_decode_noalloc(fmt, qd, codes, scales, cu_d, got, total, SM, layout)
