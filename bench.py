@@ -7,10 +7,14 @@ query token per sequence and head.  Inputs are synthetic and seeded
 (quantized_kv_cache_kv8_gb300.synth): latent rows N(0,1) x per-channel
 log-normal gains.
 
-One step = the whole hot path for one decode token of every sequence:
-  1. kv8_encode of the 8 new rows (one per sequence, appended at the end of its
-     range of the resident pool),
-  2. kv_attn_decode over all 8 x 4096 rows (split-T partials + merge).
+One step = the whole hot path for one decode token of every sequence, one
+call of kv_attn_decode_append:
+  1. the 8 new rows (one per sequence, the last row of its range of the
+     resident pool) are encoded to KV8 and stored,
+  2. attention over all 8 x 4096 rows, the new ones included (split-T
+     partials + merge).
+On the tensor-core path both run in one launch (plus the merge); on the fp32
+path (--path simt) the encoder is its own launch.
 The cache (19 MB) fits in L2, so a 256 MB buffer is written between timed
 steps (outside the timed events) to flush it.
 
@@ -150,8 +154,8 @@ def run_ours(args, rank, world):
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
 
     def step(xn, qq):
-        kvq.kv8_encode(xn, inp["codes"], inp["scales"], dst_rows=inp["dst"])
-        kvq.kv_attn_decode(kvq.KVQ_KV8, qq, inp["codes"], inp["scales"], inp["cu"], out, ws, B * T, path=path)
+        kvq.kv_attn_decode_append(kvq.KVQ_KV8, xn, inp["dst"], qq, inp["codes"], inp["scales"], inp["cu"], out, ws,
+                                  B * T, path=path)
 
     for _ in range(max(args.warmup, 3)):
         step(x_new, q)
@@ -164,24 +168,20 @@ def run_ours(args, rank, world):
     sampler.start()
     time.sleep(0.3)
     K = args.steps
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
-           torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
     sampler.mark(True)
     for i in range(K):
-        e0, e1, e2 = ev[i]
+        e0, e2 = ev[i]
         e0.record(stream)
-        kvq.kv8_encode(x_new, inp["codes"], inp["scales"], dst_rows=inp["dst"])
-        e1.record(stream)
-        kvq.kv_attn_decode(kvq.KVQ_KV8, q, inp["codes"], inp["scales"], inp["cu"], out, ws, B * T, path=path)
+        step(x_new, q)
         e2.record(stream)
         flush.zero_()
     torch.cuda.synchronize()
     sampler.mark(False)
-    step_ms = sum(e0.elapsed_time(e2) for e0, _, e2 in ev) / K
-    decode_ms = sum(e1.elapsed_time(e2) for _, e1, e2 in ev) / K
+    step_ms = sum(e0.elapsed_time(e2) for e0, e2 in ev) / K
 
     # end to end through the public API: pinned host inputs in, result out, every step
     e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
@@ -201,11 +201,11 @@ def run_ours(args, rank, world):
     if err != 0:
         raise RuntimeError(f"device error word {err} after the timed region")
 
-    t = torch.tensor([step_ms, decode_ms, e2e_ms], dtype=torch.float64, device=dev)
+    t = torch.tensor([step_ms, e2e_ms], dtype=torch.float64, device=dev)
     if dist:
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         dist.barrier()
-    step_ms, decode_ms, e2e_ms = t.tolist()
+    step_ms, e2e_ms = t.tolist()
     if rank != 0:
         return None
 
@@ -218,19 +218,19 @@ def run_ours(args, rank, world):
     # path by the fp32 FMA pipe (152 SMs x 128 lanes x 2 flop x max SM clock)
     used_path = "tensor" if (path == kvq.PATH_TENSOR or (path == kvq.PATH_AUTO and H % 64 == 0)) else "simt"
     flops = B * T * FLOPS_PER_ROW
-    achieved_tf = flops / (decode_ms * 1e-3) / 1e12
+    achieved_tf = flops / (step_ms * 1e-3) / 1e12
     if used_path == "simt":
         peak = 152 * 128 * 2 * peaks.get("sm_max_mhz", 2070.0) * 1e6 / 1e12
         roof = {"bound": "alu", "achieved": round(achieved_tf, 3), "peak": round(peak, 2), "unit": "TFLOP/s",
                 "frac": round(achieved_tf / peak, 4), "traffic": None,
                 "peak_source": "derived: 152 SMs x 128 fp32 lanes x 2 x max SM clock (MEASURED_PEAKS sm_max_mhz)",
-                "kernel": "kv_attn_decode (split-T partial + merge)"}
+                "kernel": "kv_attn_decode_append, fp32 path (encoder + split-T partials + merge, timed together)"}
     else:
         peak = peaks["bf16_tflops"]
         roof = {"bound": "tensor", "achieved": round(achieved_tf, 2), "peak": peak, "unit": "TFLOP/s",
                 "frac": round(achieved_tf / peak, 4), "traffic": None,
                 "peak_source": f"bf16_tflops ({src}); f16 operands run at the bf16 dense rate",
-                "kernel": "kv_attn_decode (tcgen05 partial + merge)"}
+                "kernel": "kv_attn_decode_append, tensor path (tcgen05 partials with the row append + merge, timed together)"}
     line = {
         "metric": METRIC, "value": round(gbs, 3), "unit": "GB/s", "n_gpus": world, "steps": K,
         "warmup": max(args.warmup, 3), "ms_per_step": round(step_ms, 5), "higher_is_better": True,
@@ -243,10 +243,10 @@ def run_ours(args, rank, world):
         "rows_per_s": round(rows / (step_ms * 1e-3), 1),
         "hbm_roof_frac": round(gbs / peaks["hbm_gbs"], 5),
         "hbm_peak_gbs": peaks["hbm_gbs"], "peak_source": src,
-        "decode_ms": round(decode_ms, 5),
         "e2e": {"value": round(e2e_gbs, 3), "unit": "GB/s", "ms_per_step": round(e2e_ms, 5),
                 "h2d_bytes_per_step": int(B * D * 4 + B * H * D * 2), "d2h_bytes_per_step": int(B * H * DV * 4)},
-        "gpu_launches": 3 * K,
+        # tensor path: the fused partial kernel + the merge; fp32 path: encoder, partials, merge
+        "gpu_launches": (2 if used_path == "tensor" else 3) * K,
         "roofline": roof,
         "clocks": clocks,
     }

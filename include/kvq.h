@@ -167,6 +167,30 @@ kvq_status kv_attn_decode(kvq_format fmt, const kvq_mla_layout* layout,
                           int64_t max_total_rows, float sm_scale, float* out,
                           void* workspace, size_t workspace_bytes, kvq_path path, void* stream);
 
+/* One decode step together with the step's new rows: encodes x_new[b] into
+ * pool row dst_rows[b] exactly as kv8_encode / tq4_encode with dst_rows would,
+ * then runs kv_attn_decode over the pool with those rows included.  The
+ * producer writes each new row before the consumer attends over it ([P2]
+ * rebase comment, point 1, the KV producer loop; [P3] "Attention error under
+ * the engine's append patterns": decode appends to the cache at every step).
+ * For KV8 with a bf16 query on the tensor-core path both run in one launch:
+ * the CTAs whose chunk holds row dst_rows[b] encode it themselves, use it in
+ * place and (one of them) store it; other formats and paths launch the
+ * encoder and then the decode.
+ *   x_new     [batch][D] f32
+ *   dst_rows  [batch] int64, device; dst_rows[b] must lie in [cu[b], cu[b+1])
+ *             (the one-launch path sets KVQ_ERR_ARG in the device error word
+ *             and skips a row outside it; elsewhere the result is undefined)
+ *   codes, scales  the pool: rows dst_rows[b] written, rows of cu_seqlens read
+ * Other arguments, the workspace (kv_attn_workspace_size) and the results are
+ * those of kv_attn_decode; max_total_rows must be at least batch. */
+kvq_status kv_attn_decode_append(kvq_format fmt, const kvq_mla_layout* layout,
+                                 const float* x_new, const int64_t* dst_rows,
+                                 const void* q, kvq_dtype q_dtype, int32_t batch, int32_t n_heads,
+                                 uint8_t* codes, float* scales, const int64_t* cu_seqlens,
+                                 int64_t max_total_rows, float sm_scale, float* out,
+                                 void* workspace, size_t workspace_bytes, kvq_path path, void* stream);
+
 /* kv_attn_decode for callers that cannot allocate device memory.  The pages
  * have no counterpart: this is a convenience of this library.
  *

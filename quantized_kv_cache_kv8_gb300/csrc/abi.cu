@@ -194,6 +194,39 @@ kvq_status kv_attn_decode(kvq_format fmt, const kvq_mla_layout* layout, const vo
                                         sm_scale, out, workspace, st));
 }
 
+kvq_status kv_attn_decode_append(kvq_format fmt, const kvq_mla_layout* layout, const float* x_new,
+                                 const int64_t* dst_rows, const void* q, kvq_dtype q_dtype, int32_t batch,
+                                 int32_t n_heads, uint8_t* codes, float* scales, const int64_t* cu_seqlens,
+                                 int64_t max_total_rows, float sm_scale, float* out, void* workspace,
+                                 size_t workspace_bytes, kvq_path path, void* stream) {
+    kvq_status s = check_attn_layout(fmt, layout);
+    if (s != KVQ_OK) return s;
+    if ((s = check_path(path)) != KVQ_OK) return s;
+    if (batch < 0 || n_heads < 0 || max_total_rows < 0 || (q_dtype != KVQ_F32 && q_dtype != KVQ_BF16))
+        return KVQ_ERR_ARG;
+    if (batch > 65535 || n_heads > 65535) return KVQ_ERR_UNSUPPORTED;
+    if (batch == 0 || n_heads == 0) return KVQ_OK;
+    kvq_path rp;
+    if ((s = resolve_path(path, layout, n_heads, &rp)) != KVQ_OK) return s;
+    if (!x_new || !dst_rows || !q || !cu_seqlens || !out || !codes || !scales) return KVQ_ERR_ARG;
+    if (max_total_rows < batch) return KVQ_ERR_ARG;   // every sequence holds at least its new row
+    if (!isfinite(sm_scale)) return KVQ_ERR_ARG;
+    const size_t need = kv_attn_workspace_size(fmt, layout, batch, n_heads, max_total_rows, path);
+    if (!workspace || workspace_bytes < need) return KVQ_ERR_WORKSPACE;
+    cudaStream_t st = (cudaStream_t)stream;
+    if (rp == KVQ_PATH_TENSOR && fmt == KVQ_KV8 && q_dtype == KVQ_BF16) {
+        const AttnPlan pl = plan_decode(rp, batch, n_heads, max_total_rows);
+        return cuda_status(launch_attn_tc_kv8_append(*layout, x_new, dst_rows, q, batch, n_heads, codes, scales,
+                                                     cu_seqlens, pl, sm_scale, out, workspace, st));
+    }
+    // other formats and paths: the encoder launch, then the decode
+    const cudaError_t e = fmt == KVQ_KV8 ? launch_kv8_encode(x_new, batch, *layout, dst_rows, codes, scales, st)
+                                         : launch_tq4_encode(x_new, batch, *layout, dst_rows, codes, scales, st);
+    if (e != cudaSuccess) return KVQ_ERR_CUDA;
+    return kv_attn_decode(fmt, layout, q, q_dtype, batch, n_heads, codes, scales, cu_seqlens, max_total_rows,
+                          sm_scale, out, workspace, workspace_bytes, path, stream);
+}
+
 static AttnPlan plan_prefill(int64_t n_past, int64_t n_new) {
     AttnPlan pl{};
     pl.chunk = std::max<int64_t>(1, n_past + n_new);

@@ -29,6 +29,13 @@ struct AttnParams {
     SignWords signs;
     float kn[2];
     float lv[16];
+    // decode with rows appended in the same launch (tensor-core KV8 kernel):
+    // x_new[b] is encoded into pool row dst_rows[b], inside [cu[b], cu[b+1])
+    const float* x_new;
+    const int64_t* dst_rows;
+    uint8_t* codes_out;
+    float* scales_out;
+    int32_t bd0, bd1;
 };
 
 __device__ __forceinline__ void set_err(int32_t* err, int32_t code) { atomicCAS(err, 0, code); }
@@ -138,6 +145,9 @@ AttnParams make_attn_params(kvq_format fmt, const kvq_mla_layout& L, const void*
 // Tensor-core partial kernel for KV8 rows with bf16 queries (every chunk of a
 // tile decoded once); grid = work items x head groups of 64.
 cudaError_t launch_attn_tc_kv8_bf16(const AttnParams& p, int64_t grid_x, int groups, cudaStream_t stream);
+// The same kernel with the per-sequence new rows (p.x_new, p.dst_rows) encoded
+// into the pool and substituted into the tiles that hold them.
+cudaError_t launch_attn_tc_kv8_bf16_append(const AttnParams& p, int64_t grid_x, int groups, cudaStream_t stream);
 
 // LSE merge of the chunk partials into out[n_seq][n_heads][512] (TQ4: unrotated).
 cudaError_t launch_attn_merge(kvq_format fmt, const AttnParams& p, float* out, cudaStream_t stream);

@@ -754,4 +754,22 @@ cudaError_t launch_attn_tc(kvq_format fmt, const kvq_mla_layout& L, const void* 
     return launch_attn_merge(fmt, p, out, stream);
 }
 
+cudaError_t launch_attn_tc_kv8_append(const kvq_mla_layout& L, const float* x_new, const int64_t* dst_rows,
+                                      const void* q, int32_t n_seq, int32_t n_heads, uint8_t* codes, float* scales,
+                                      const int64_t* cu_seqlens, const AttnPlan& plan, float sm_scale, float* out,
+                                      void* workspace, cudaStream_t stream) {
+    if (n_seq == 0 || n_heads == 0) return cudaSuccess;
+    AttnParams p = make_attn_params(KVQ_KV8, L, q, n_seq, n_heads, codes, scales, cu_seqlens, -1, plan, sm_scale,
+                                    workspace);
+    p.x_new = x_new;
+    p.dst_rows = dst_rows;
+    p.codes_out = codes;
+    p.scales_out = scales;
+    p.bd0 = L.block_dim[0];
+    p.bd1 = L.n_blocks > 1 ? L.block_dim[1] : 0;
+    const cudaError_t e = launch_attn_tc_kv8_bf16_append(p, plan.max_items, n_heads / kHC, stream);
+    if (e != cudaSuccess) return e;
+    return launch_attn_merge(KVQ_KV8, p, out, stream);
+}
+
 }  // namespace kvq

@@ -61,7 +61,8 @@ constexpr uint32_t kOffAlpha = kOffM + kHC * 4;
 constexpr uint32_t kOffRed = kOffAlpha + kHC * 4;   // 4 quadrants x 64 heads of f32
 constexpr uint32_t kOffBar = kOffRed + 4 * kHC * 4;
 constexpr uint32_t kOffMisc = kOffBar + 16 * 8;      // abort flag, TMEM base, item info
-constexpr uint32_t kSmemUsed = kOffMisc + 32;
+constexpr uint32_t kOffNew = kOffMisc + 32;          // appended row: 576 codes, 2 scales, row index
+constexpr uint32_t kSmemUsed = kOffNew + 576 + 16;
 static_assert(kOffSlot % 1024 == 0, "swizzled operands need 1024-byte alignment");
 static_assert(kSmemUsed <= 232448, "shared memory budget");
 
@@ -94,21 +95,30 @@ struct RawRope {
     uint4 v[2];
 };
 
+// Pool row `rn` (an appended row, or -1) is read from its shared-memory copy
+// `snew` instead of global memory.
+template <bool APPEND>
+__device__ __forceinline__ uint4 load16(const uint8_t* __restrict__ codes, int64_t row, int byte, int64_t rn,
+                                        const unsigned char* snew) {
+    if (APPEND && row == rn) return *reinterpret_cast<const uint4*>(snew + byte);
+    return __ldg(reinterpret_cast<const uint4*>(codes + row * kMlaD + byte));
+}
+template <bool APPEND>
 __device__ __forceinline__ void load_group(RawGroup& r, const uint8_t* __restrict__ codes, int64_t t0, int nt, int g,
-                                           int warp, int lane) {
+                                           int warp, int lane, int64_t rn, const unsigned char* snew) {
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
         const int row = 2 * (warp + 8 * i) + (lane >> 4);
-        r.v[i] = row < nt ? __ldg(reinterpret_cast<const uint4*>(codes + (t0 + row) * kMlaD + 256 * g + 16 * (lane & 15)))
-                          : make_uint4(0u, 0u, 0u, 0u);
+        r.v[i] = row < nt ? load16<APPEND>(codes, t0 + row, 256 * g + 16 * (lane & 15), rn, snew) : make_uint4(0u, 0u, 0u, 0u);
     }
 }
-__device__ __forceinline__ void load_rope(RawRope& r, const uint8_t* __restrict__ codes, int64_t t0, int nt, int tid) {
+template <bool APPEND>
+__device__ __forceinline__ void load_rope(RawRope& r, const uint8_t* __restrict__ codes, int64_t t0, int nt, int tid,
+                                          int64_t rn, const unsigned char* snew) {
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
         const int u = tid + kWorkers * i, row = u >> 2;
-        r.v[i] = row < nt ? __ldg(reinterpret_cast<const uint4*>(codes + (t0 + row) * kMlaD + 512 + 16 * (u & 3)))
-                          : make_uint4(0u, 0u, 0u, 0u);
+        r.v[i] = row < nt ? load16<APPEND>(codes, t0 + row, 512 + 16 * (u & 3), rn, snew) : make_uint4(0u, 0u, 0u, 0u);
     }
 }
 
@@ -144,6 +154,7 @@ __device__ __forceinline__ float warp_columns(float (&v)[32], int lane) {
     return v[0];
 }
 
+template <bool APPEND>
 __global__ void __launch_bounds__(kThreads, 1) attn_tc_kv8_kernel(AttnParams p) {
     launch_dependents();
     extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -158,6 +169,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kv8_kernel(AttnParams p) 
     volatile int* sAbort = reinterpret_cast<volatile int*>(sm + kOffMisc);
     uint32_t* sTmem = reinterpret_cast<uint32_t*>(sm + kOffMisc + 4);
     int64_t* sInfo = reinterpret_cast<int64_t*>(sm + kOffMisc + 8);
+    unsigned char* sNew = sm + kOffNew;                       // appended row's codes
+    float* sNewScale = reinterpret_cast<float*>(sm + kOffNew + 576);
+    int64_t* sNewRow = reinterpret_cast<int64_t*>(sm + kOffNew + 584);
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int64_t item = blockIdx.x;
@@ -201,6 +215,31 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kv8_kernel(AttnParams p) 
         prefetch_l2(p.codes + row0 * kMlaD, (uint32_t)(n * kMlaD));
     }
 
+    // ---- appended row: the MMA warp (idle until the first score) encodes it
+    // into shared memory; the group-0 CTA of the chunk also writes it to the
+    // pool.  Workers learn its index from dst_rows directly. ----
+    int64_t rn = -1;
+    if (APPEND) {
+        const int64_t d = p.dst_rows[b];
+        rn = (d >= row0 && d < row1) ? d : -1;
+        if (warp == kWorkers / 32) {
+            if (lane == 0) {
+                *sNewRow = rn;
+                const int64_t s0 = p.cu[b], s1 = p.cu[b + 1];
+                if ((d < s0 || d >= s1) && row0 == s0 && blockIdx.y == 0) set_err(p.err, KVQ_ERR_ARG);
+            }
+            if (rn >= 0) {
+                kv8_encode_row_warp(p.x_new + (int64_t)b * kMlaD, p.n_blocks, p.bd0, p.bd1, sNew, sNewScale, lane);
+                __syncwarp();
+                if (blockIdx.y == 0) {
+                    for (int i = lane; i < kMlaD / 16; i += 32)
+                        reinterpret_cast<uint4*>(p.codes_out + rn * kMlaD)[i] = reinterpret_cast<const uint4*>(sNew)[i];
+                    if (lane < p.n_blocks) p.scales_out[rn * p.n_blocks + lane] = sNewScale[lane];
+                }
+            }
+        }
+    }
+
     // ---- query: 64 heads x 576 bf16, 18 16-byte loads per worker held in
     // registers; largest |q| and largest latent scale of the chunk ----
     const int64_t qbase = ((int64_t)b * p.n_heads + hbase) * kMlaD;
@@ -212,7 +251,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kv8_kernel(AttnParams p) 
         float qmax = 0.0f, smax = 0.0f;
 #pragma unroll
         for (int i = 0; i < kQPer; ++i) qraw[i] = __ldg(qv + tid + i * kWorkers);
-        for (int64_t r = row0 + tid; r < row1; r += kWorkers) smax = fmaxf(smax, p.scales[r * p.n_blocks]);
+        for (int64_t r = row0 + tid; r < row1; r += kWorkers)
+            if (!APPEND || r != rn) smax = fmaxf(smax, p.scales[r * p.n_blocks]);
 #pragma unroll
         for (int i = 0; i < kQPer; ++i) {
             const uint32_t in[4] = {qraw[i].x, qraw[i].y, qraw[i].z, qraw[i].w};
@@ -236,6 +276,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kv8_kernel(AttnParams p) 
         q_max = fmaxf(q_max, sRed[i]);
         s_max = fmaxf(s_max, sRed[8 + i]);
     }
+    if (APPEND && rn >= 0) s_max = fmaxf(s_max, sNewScale[0]);
     int e_s = 0, e_q = 0;
     if (s_max > 0.0f) frexpf(s_max, &e_s);
     if (q_max > 0.0f) frexpf(q_max, &e_q);
@@ -326,17 +367,22 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kv8_kernel(AttnParams p) 
         sl_next = sr_next = 0.0f;
         if (srow < ntn) {
             const int64_t r = t0n + srow;
-            sl_next = p.scales[r * p.n_blocks];
-            sr_next = p.scales[r * p.n_blocks + (p.n_blocks - 1)];
+            if (APPEND && r == rn) {
+                sl_next = sNewScale[0];
+                sr_next = sNewScale[p.n_blocks - 1];
+            } else {
+                sl_next = p.scales[r * p.n_blocks];
+                sr_next = p.scales[r * p.n_blocks + (p.n_blocks - 1)];
+            }
         }
     };
     RawGroup rawA, rawB;
     RawRope rawC;
     {
         const int nt0 = (int)min((int64_t)kRows, row1 - row0);
-        load_group(rawA, p.codes, row0, nt0, 0, warp, lane);
-        load_group(rawB, p.codes, row0, nt0, 1, warp, lane);
-        load_rope(rawC, p.codes, row0, nt0, tid);
+        load_group<APPEND>(rawA, p.codes, row0, nt0, 0, warp, lane, rn, sNew);
+        load_group<APPEND>(rawB, p.codes, row0, nt0, 1, warp, lane, rn, sNew);
+        load_rope<APPEND>(rawC, p.codes, row0, nt0, tid, rn, sNew);
         load_scales(row0, nt0);
     }
     int t = 0;
@@ -375,7 +421,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kv8_kernel(AttnParams p) 
         }
         const int64_t t1 = t0 + kRows;
         const int nt1 = (int)min((int64_t)kRows, row1 - t1);
-        if (t + 1 < n_tiles) load_group(rawA, p.codes, t1, nt1, 0, warp, lane);
+        if (t + 1 < n_tiles) load_group<APPEND>(rawA, p.codes, t1, nt1, 0, warp, lane, rn, sNew);
 
         // ---- softmax of the tile: thread = row srow, 32 heads ----
         mbar_wait(&bars[kBarScore], (uint32_t)t & 1u, sAbort);
@@ -399,8 +445,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kv8_kernel(AttnParams p) 
         // the rest of tile t+1 is requested while the tensor cores are idle
         // (their operand reads compete with these loads for the SM's memory pipe)
         if (t + 1 < n_tiles) {
-            load_group(rawB, p.codes, t1, nt1, 1, warp, lane);
-            load_rope(rawC, p.codes, t1, nt1, tid);
+            load_group<APPEND>(rawB, p.codes, t1, nt1, 1, warp, lane, rn, sNew);
+            load_rope<APPEND>(rawC, p.codes, t1, nt1, tid, rn, sNew);
             load_scales(t1, nt1);
         }
         bool flag = *sAbort != 0;
@@ -508,12 +554,23 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kv8_kernel(AttnParams p) 
 
 }  // namespace
 
-cudaError_t launch_attn_tc_kv8_bf16(const AttnParams& p, int64_t grid_x, int groups, cudaStream_t stream) {
-    cudaError_t e =
-        cudaFuncSetAttribute(attn_tc_kv8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemUsed);
+namespace {
+template <bool APPEND>
+cudaError_t launch_kv8(const AttnParams& p, int64_t grid_x, int groups, cudaStream_t stream) {
+    cudaError_t e = cudaFuncSetAttribute(attn_tc_kv8_kernel<APPEND>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)kSmemUsed);
     if (e != cudaSuccess) return e;
-    attn_tc_kv8_kernel<<<dim3((unsigned)grid_x, (unsigned)groups), kThreads, kSmemUsed, stream>>>(p);
+    attn_tc_kv8_kernel<APPEND><<<dim3((unsigned)grid_x, (unsigned)groups), kThreads, kSmemUsed, stream>>>(p);
     return cudaGetLastError();
+}
+}  // namespace
+
+cudaError_t launch_attn_tc_kv8_bf16(const AttnParams& p, int64_t grid_x, int groups, cudaStream_t stream) {
+    return launch_kv8<false>(p, grid_x, groups, stream);
+}
+
+cudaError_t launch_attn_tc_kv8_bf16_append(const AttnParams& p, int64_t grid_x, int groups, cudaStream_t stream) {
+    return launch_kv8<true>(p, grid_x, groups, stream);
 }
 
 }  // namespace kvq

@@ -61,24 +61,8 @@ __global__ void __launch_bounds__(256) kv8_encode_kernel(const float* __restrict
     const int64_t src = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     if (src >= n_rows) return;
     const int64_t row = dst_rows ? dst_rows[src] : src;
-    const float* xr = x + src * p.D;
-    uint8_t* cr = codes + row * p.D;
-    int off = 0;
-    for (int b = 0; b < p.n_blocks; ++b) {
-        const int n = p.bd[b];
-        float amax = 0.0f;
-        for (int i = lane; i < n; i += 32) amax = fmaxf(amax, fabsf(__ldg(xr + off + i)));
-        amax = warp_max(amax);
-        const float s = __fdiv_rn(amax, 448.0f);
-        if (lane == 0) scales[row * p.n_blocks + b] = s;
-        for (int i = lane; i < n; i += 32) {
-            uint8_t c = 0;
-            if (s != 0.0f)
-                c = (uint8_t)__nv_cvt_float_to_fp8(__fdiv_rn(__ldg(xr + off + i), s), __NV_SATFINITE, __NV_E4M3);
-            cr[off + i] = c;
-        }
-        off += n;
-    }
+    kv8_encode_row_warp(x + src * p.D, p.n_blocks, p.bd[0], p.bd[1], codes + row * p.D, scales + row * p.n_blocks,
+                        lane);
 }
 
 cudaError_t launch_kv8_encode(const float* x, int64_t n_rows, const kvq_mla_layout& L, const int64_t* dst_rows,

@@ -68,6 +68,31 @@ __device__ __forceinline__ float warp_max(float v) {
     for (int o = 16; o >= 1; o >>= 1) v = fmaxf(v, __shfl_xor_sync(kFull, v, o));
     return v;
 }
+
+// KV8 encoding of one row by one warp ([P1] Commits item 1): per scale block,
+// s = amax / 448 (f32 division, round to nearest) and code =
+// e4m3_rn_satfinite(x / s); a block with s == 0 stores s = 0 and codes 0.
+// Lane 0 writes the block scales to sr[0 .. n_blocks).  The encoder kernel and
+// the decode kernel that appends rows both call this, so their bytes agree.
+__device__ __forceinline__ void kv8_encode_row_warp(const float* __restrict__ xr, int n_blocks, int bd0, int bd1,
+                                                    uint8_t* cr, float* sr, int lane) {
+    int off = 0;
+    for (int b = 0; b < n_blocks; ++b) {
+        const int n = b == 0 ? bd0 : bd1;
+        float amax = 0.0f;
+        for (int i = lane; i < n; i += 32) amax = fmaxf(amax, fabsf(__ldg(xr + off + i)));
+        amax = warp_max(amax);
+        const float s = __fdiv_rn(amax, 448.0f);
+        if (lane == 0) sr[b] = s;
+        for (int i = lane; i < n; i += 32) {
+            uint8_t c = 0;
+            if (s != 0.0f)
+                c = (uint8_t)__nv_cvt_float_to_fp8(__fdiv_rn(__ldg(xr + off + i), s), __NV_SATFINITE, __NV_E4M3);
+            cr[off + i] = c;
+        }
+        off += n;
+    }
+}
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
     for (int o = 16; o >= 1; o >>= 1) v = __fadd_rn(v, __shfl_xor_sync(kFull, v, o));
@@ -153,6 +178,12 @@ cudaError_t launch_attn_simt(kvq_format fmt, const kvq_mla_layout& L, const void
 // Tensor-core attention (tcgen05, 64 heads per CTA).
 bool tc_supported(const kvq_mla_layout& L, int32_t n_heads);
 AttnPlan plan_decode_tc(int32_t batch, int32_t n_heads, int64_t max_total_rows);
+// KV8 decode with bf16 queries on the tensor cores, the step's new rows
+// encoded in the same launch (row x_new[b] -> pool row dst_rows[b]).
+cudaError_t launch_attn_tc_kv8_append(const kvq_mla_layout& L, const float* x_new, const int64_t* dst_rows,
+                                      const void* q, int32_t n_seq, int32_t n_heads, uint8_t* codes, float* scales,
+                                      const int64_t* cu_seqlens, const AttnPlan& plan, float sm_scale, float* out,
+                                      void* workspace, cudaStream_t stream);
 cudaError_t launch_attn_tc(kvq_format fmt, const kvq_mla_layout& L, const void* q, kvq_dtype qdt, int32_t n_seq,
                            int32_t n_heads, const uint8_t* codes, const float* scales, const int64_t* cu_seqlens,
                            int64_t prefill_past, const AttnPlan& plan, float sm_scale, float* out, void* workspace,

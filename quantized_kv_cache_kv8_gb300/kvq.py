@@ -79,6 +79,9 @@ def _declare(L):
     L.kv_attn_workspace_size.argtypes = [C.c_int, pl, I32, I32, I64, C.c_int]
     L.kv_attn_decode.restype = C.c_int
     L.kv_attn_decode.argtypes = [C.c_int, pl, P, C.c_int, I32, I32, P, P, P, I64, C.c_float, P, P, S, C.c_int, P]
+    L.kv_attn_decode_append.restype = C.c_int
+    L.kv_attn_decode_append.argtypes = [C.c_int, pl, P, P, P, C.c_int, I32, I32, P, P, P, I64, C.c_float, P, P, S,
+                                        C.c_int, P]
     L.kv_attn_decode_noalloc.restype = C.c_int
     L.kv_attn_decode_noalloc.argtypes = [C.c_int, pl, P, C.c_int, I32, I32, P, P, P, I64, C.c_float, P, C.c_int, P]
     L.kv_attn_prefill_workspace_size.restype = S
@@ -190,6 +193,22 @@ def kv_attn_decode(fmt: int, q, codes, scales, cu_seqlens, out, workspace, max_t
                              _ptr(cu_seqlens, torch.int64, "cu_seqlens"), int(max_total_rows), float(sm_scale),
                              _ptr(out, torch.float32, "out"), _ptr(workspace, torch.uint8, "workspace"),
                              workspace.numel(), path, _stream(stream)), "kv_attn_decode")
+
+
+def kv_attn_decode_append(fmt: int, x_new, dst_rows, q, codes, scales, cu_seqlens, out, workspace,
+                          max_total_rows: int, sm_scale: float = SM_SCALE_MLA, layout: MLALayout | None = None,
+                          path: int = PATH_AUTO, stream=None):
+    """One decode step with its new rows: x_new[b] is encoded into pool row
+    dst_rows[b] (inside sequence b), then attention runs over the pool."""
+    layout = layout or mla_layout()
+    B, H = q.shape[0], q.shape[1]
+    _ok(lib().kv_attn_decode_append(fmt, C.byref(layout), _ptr(x_new, torch.float32, "x_new"),
+                                    _ptr(dst_rows, torch.int64, "dst_rows"), _ptr(q, None, "q"), _qdtype(q), B, H,
+                                    _ptr(codes, torch.uint8, "codes"), _ptr(scales, torch.float32, "scales"),
+                                    _ptr(cu_seqlens, torch.int64, "cu_seqlens"), int(max_total_rows),
+                                    float(sm_scale), _ptr(out, torch.float32, "out"),
+                                    _ptr(workspace, torch.uint8, "workspace"), workspace.numel(), path,
+                                    _stream(stream)), "kv_attn_decode_append")
 
 
 def kv_attn_decode_noalloc(fmt: int, q, codes, scales, cu_seqlens, out, max_total_rows: int,

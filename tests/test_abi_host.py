@@ -89,3 +89,22 @@ def test_workspace_sizes_grow_with_work(kvq):
     assert p >= 2048 * 128 * 514 * 4
     k = kvq.kv_attn_decode_k2v4_workspace_size(kvq.k2v4_layout(), 4, 16, 32768)
     assert k > 0
+
+
+def test_decode_append_validates_before_launch(kvq):
+    L = kvq.lib()
+    lay = kvq.mla_layout()
+    # null x_new / dst_rows, fewer rows than sequences, no workspace: refused on the host
+    assert L.kv_attn_decode_append(1, C.byref(lay), None, None, None, 1, 2, 64, None, None, None, 10, 0.1, None,
+                                   None, 0, 0, None) == 1
+    dummy = C.c_void_p(16)
+    assert L.kv_attn_decode_append(1, C.byref(lay), dummy, dummy, dummy, 1, 4, 64, dummy, dummy, dummy, 3, 0.1,
+                                   dummy, dummy, 1 << 30, 0, None) == 1
+    assert L.kv_attn_decode_append(1, C.byref(lay), dummy, dummy, dummy, 1, 2, 64, dummy, dummy, dummy, 10, 0.1,
+                                   dummy, None, 0, 0, None) == 3
+    bad = kvq.mla_layout((500, 76))
+    assert L.kv_attn_decode_append(2, C.byref(bad), dummy, dummy, dummy, 1, 2, 64, dummy, dummy, dummy, 10, 0.1,
+                                   dummy, dummy, 1 << 30, 0, None) == 2
+    # empty batch: nothing to do
+    assert L.kv_attn_decode_append(1, C.byref(lay), None, None, None, 1, 0, 64, None, None, None, 0, 0.1, None,
+                                   None, 0, 0, None) == 0
