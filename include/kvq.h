@@ -15,7 +15,12 @@
  *     allocates nothing on the device and frees nothing; scratch space is the
  *     caller's `workspace`, sized by the matching *_workspace_size call.
  *   - Pointers are device pointers (any memory the GPU can address), except the
- *     layout structs, which are read on the host during the call.
+ *     layout structs, which are read on the host during the call.  The
+ *     attention entry points read and write with vector instructions and
+ *     return KVQ_ERR_ARG for a misaligned pointer: the code pool must be
+ *     32-byte aligned (then every row is, as rows are 576 or 288 bytes),
+ *     queries, outputs and new rows 16-byte aligned, scales, cu_seqlens and
+ *     dst_rows 8-byte aligned.  Allocations from cudaMalloc (and PyTorch) are.
  *   - Execution is asynchronous on `stream` (a cudaStream_t; NULL is the legacy
  *     default stream).  Nothing is synchronized unless stated.
  *   - Errors: arguments are validated on the host before any launch and

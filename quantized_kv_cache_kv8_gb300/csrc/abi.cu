@@ -40,6 +40,16 @@ kvq_status check_tq4_layout(const kvq_mla_layout* L) {
 }
 
 // The attention kernels are written for the 576-dim MLA latent row.
+// Vector widths the attention kernels read and write with: the code pool in
+// 32-byte pieces (every row of a 32-byte aligned pool is, as 576 and 288 are
+// multiples of 32), queries, outputs and new rows in 16 bytes, scales and the
+// int64 arrays in 8.
+static bool aligned(const void* p, uintptr_t n) { return ((uintptr_t)p & (n - 1)) == 0; }
+static bool attn_pointers_aligned(const void* q, const uint8_t* codes, const float* scales, const int64_t* cu,
+                                  const float* out) {
+    return aligned(q, 16) && aligned(codes, 32) && aligned(scales, 8) && aligned(cu, 8) && aligned(out, 16);
+}
+
 kvq_status check_attn_layout(kvq_format fmt, const kvq_mla_layout* L) {
     kvq_status s = fmt == KVQ_TQ4 ? check_tq4_layout(L) : (fmt == KVQ_KV8 ? check_layout(L) : KVQ_ERR_ARG);
     if (s != KVQ_OK) return s;
@@ -182,6 +192,7 @@ kvq_status kv_attn_decode(kvq_format fmt, const kvq_mla_layout* layout, const vo
     if ((s = resolve_path(path, layout, n_heads, &rp)) != KVQ_OK) return s;
     if (!q || !cu_seqlens || !out) return KVQ_ERR_ARG;
     if (max_total_rows > 0 && (!codes || !scales)) return KVQ_ERR_ARG;
+    if (!attn_pointers_aligned(q, codes, scales, cu_seqlens, out)) return KVQ_ERR_ARG;
     if (!isfinite(sm_scale)) return KVQ_ERR_ARG;
     const size_t need = kv_attn_workspace_size(fmt, layout, batch, n_heads, max_total_rows, path);
     if (!workspace || workspace_bytes < need) return KVQ_ERR_WORKSPACE;
@@ -209,6 +220,8 @@ kvq_status kv_attn_decode_append(kvq_format fmt, const kvq_mla_layout* layout, c
     kvq_path rp;
     if ((s = resolve_path(path, layout, n_heads, &rp)) != KVQ_OK) return s;
     if (!x_new || !dst_rows || !q || !cu_seqlens || !out || !codes || !scales) return KVQ_ERR_ARG;
+    if (!attn_pointers_aligned(q, codes, scales, cu_seqlens, out) || !aligned(x_new, 16) || !aligned(dst_rows, 8))
+        return KVQ_ERR_ARG;
     if (max_total_rows < batch) return KVQ_ERR_ARG;   // every sequence holds at least its new row
     if (!isfinite(sm_scale)) return KVQ_ERR_ARG;
     const size_t need = kv_attn_workspace_size(fmt, layout, batch, n_heads, max_total_rows, path);
@@ -256,6 +269,7 @@ kvq_status kv_attn_prefill(kvq_format fmt, const kvq_mla_layout* layout, const f
     kvq_path rp;
     if ((s = resolve_path(path, layout, n_heads, &rp)) != KVQ_OK) return s;
     if (!x_new || !q || !codes || !scales || !out) return KVQ_ERR_ARG;
+    if (!attn_pointers_aligned(q, codes, scales, nullptr, out) || !aligned(x_new, 16)) return KVQ_ERR_ARG;
     if (!isfinite(sm_scale)) return KVQ_ERR_ARG;
     const size_t need = kv_attn_prefill_workspace_size(fmt, layout, n_heads, n_past, n_new, path);
     if (!workspace || workspace_bytes < need) return KVQ_ERR_WORKSPACE;

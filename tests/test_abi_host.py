@@ -71,8 +71,8 @@ def test_argument_validation(kvq):
     # workspace too small is reported before any launch
     need = kvq.kv_attn_workspace_size(1, 8, 128, 32768)
     assert need > 0
-    assert L.kv_attn_decode(1, C.byref(lay), C.c_void_p(16), 1, 8, 128, C.c_void_p(16), C.c_void_p(16),
-                            C.c_void_p(16), 32768, 0.07, C.c_void_p(16), C.c_void_p(16), need - 1, 0, None) == 3
+    d = C.c_void_p(256)     # a dummy device address, aligned for every operand (never dereferenced)
+    assert L.kv_attn_decode(1, C.byref(lay), d, 1, 8, 128, d, d, d, 32768, 0.07, d, d, need - 1, 0, None) == 3
     # unsupported attention layouts
     odd = kvq.mla_layout((256, 64), v_dim=256)
     assert kvq.kv_attn_workspace_size(1, 1, 16, 100, layout=odd) == 0
@@ -97,7 +97,7 @@ def test_decode_append_validates_before_launch(kvq):
     # null x_new / dst_rows, fewer rows than sequences, no workspace: refused on the host
     assert L.kv_attn_decode_append(1, C.byref(lay), None, None, None, 1, 2, 64, None, None, None, 10, 0.1, None,
                                    None, 0, 0, None) == 1
-    dummy = C.c_void_p(16)
+    dummy = C.c_void_p(256)
     assert L.kv_attn_decode_append(1, C.byref(lay), dummy, dummy, dummy, 1, 4, 64, dummy, dummy, dummy, 3, 0.1,
                                    dummy, dummy, 1 << 30, 0, None) == 1
     assert L.kv_attn_decode_append(1, C.byref(lay), dummy, dummy, dummy, 1, 2, 64, dummy, dummy, dummy, 10, 0.1,
@@ -108,3 +108,18 @@ def test_decode_append_validates_before_launch(kvq):
     # empty batch: nothing to do
     assert L.kv_attn_decode_append(1, C.byref(lay), None, None, None, 1, 0, 64, None, None, None, 0, 0.1, None,
                                    None, 0, 0, None) == 0
+
+
+def test_attention_refuses_misaligned_pointers(kvq):
+    """Checked on the host before any launch (no GPU needed)."""
+    L = kvq.lib()
+    lay = kvq.mla_layout()
+    ok, odd = C.c_void_p(1 << 20), C.c_void_p((1 << 20) + 16)     # 16-byte but not 32-byte aligned
+    ws = C.c_void_p(1 << 21)
+    # codes pointer off a 32-byte boundary
+    assert L.kv_attn_decode(1, C.byref(lay), ok, 1, 2, 64, odd, ok, ok, 10, 0.1, ok, ws, 1 << 30, 0, None) == 1
+    # query off a 16-byte boundary
+    assert L.kv_attn_decode(1, C.byref(lay), C.c_void_p((1 << 20) + 8), 1, 2, 64, ok, ok, ok, 10, 0.1, ok, ws,
+                            1 << 30, 0, None) == 1
+    assert L.kv_attn_decode_append(1, C.byref(lay), C.c_void_p((1 << 20) + 4), ok, ok, 1, 2, 64, ok, ok, ok, 10,
+                                   0.1, ok, ws, 1 << 30, 0, None) == 1
