@@ -66,6 +66,12 @@ constexpr uint32_t kColO = 0, kColSL = 256, kColSR = 384, kTmemCols = 512;
 enum { kBarFull0 = 0, kBarEmpty0 = 4, kBarScore = 8, kBarCtx = 9, kBarP = 10, kNumBars = 11 };
 
 using namespace tc;
+// TQ4 levels in f16: the 16 Lloyd-Max levels times kTq4Gamma round to f16 with
+// a relative error of at most 9.3e-5 (2^-13.4), against 3.2e-4 unscaled; the
+// value comes from a search over scales in [1, 2) (csrc/gen_codebook.py
+// --level-scale).  Scores and context are divided by it in f32.
+constexpr float kTq4Gamma = 1.3338516f;
+constexpr float kTq4InvGamma = 1.0f / 1.3338516f;
 constexpr uint32_t kIdescScore = idesc_f16(128, kHC, false, false);
 constexpr uint32_t kIdescScore2 = idesc_f16(128, 2 * kHC, false, false);
 constexpr uint32_t kIdescCtx = idesc_f16(128, kHC, true, true);
@@ -137,32 +143,6 @@ __device__ __forceinline__ void store_chunk(const RawChunk& c, bool valid, unsig
             make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
 }
 
-// TQ4: the f16 rounding residual of each code's level (level - f16(level)),
-// same layout as store_chunk.  Residuals are below 4e-4 of the level.
-__device__ __forceinline__ void store_delta_chunk(const RawChunk& c, bool valid, unsigned char* slot,
-                                                  const __half* delta, int tid) {
-    const int r = tid >> 1, half = tid & 1;
-    uint32_t w[16];
-    if (valid) {
-        const uint32_t in[4] = {c.a.x, c.a.y, c.a.z, c.a.w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const uint32_t byte = (in[i] >> (8 * j)) & 0xffu;
-                w[4 * i + j] = (uint32_t)__half_as_ushort(delta[byte & 15u]) |
-                               ((uint32_t)__half_as_ushort(delta[byte >> 4]) << 16);
-            }
-    } else {
-#pragma unroll
-        for (int i = 0; i < 16; ++i) w[i] = 0u;
-    }
-#pragma unroll
-    for (int j = 0; j < 4; ++j)
-        *reinterpret_cast<uint4*>(slot + sw128(r, half * 64 + 16 * j)) =
-            make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
-}
-
 // LOQ: the query needs its f16 residual rows (f32 queries, or TQ4's rotated
 // queries).  Without them (KV8 with a bf16 query, exact in f16) the residual
 // half of the query area holds a 5-stage cp.async ring of raw code chunks.
@@ -184,7 +164,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnParams p) {
     int* sHasLo = reinterpret_cast<int*>(sm + kOffMisc + 8);
     int64_t* sInfo = reinterpret_cast<int64_t*>(sm + kOffMisc + 16);
     float* sRed = reinterpret_cast<float*>(sm + kOffMisc + 48);       // 16 floats
-    __half* sDelta = reinterpret_cast<__half*>(sm + kOffMisc + 112);  // TQ4: level - f16(level)
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int64_t item = blockIdx.x;
@@ -226,9 +205,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnParams p) {
     if (tid < kHC) sM[tid] = -INFINITY;
     if (FMT == KVQ_TQ4 && tid < 256) {
         const int lo = tid & 15, hi = tid >> 4;
-        const __half2 h2 = __halves2half2(__float2half_rn(p.lv[lo]), __float2half_rn(p.lv[hi]));
+        const __half2 h2 = __halves2half2(__float2half_rn(__fmul_rn(p.lv[lo], kTq4Gamma)),
+                                          __float2half_rn(__fmul_rn(p.lv[hi], kTq4Gamma)));
         sLut[tid] = *reinterpret_cast<const uint32_t*>(&h2);
-        if (tid < 16) sDelta[tid] = __float2half_rn(p.lv[tid] - __half2float(__float2half_rn(p.lv[tid])));
     }
 
     // workers: the first chunk copies go out now and overlap the query prologue
@@ -332,7 +311,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnParams p) {
     const float s_ref = s_max > 0.0f ? ldexpf(1.0f, e_s) : 1.0f;
     const float inv_s_ref = s_max > 0.0f ? ldexpf(1.0f, -e_s) : 1.0f;
     const float q_scale = q_bound > 0.0f ? ldexpf(1.0f, 14 - e_q) : 1.0f;
-    const float cz = p.sm_scale * kLog2e * (q_bound > 0.0f ? ldexpf(1.0f, e_q - 14) : 1.0f);
+    // TQ4 levels enter the products scaled by kTq4Gamma; it is divided out of
+    // the scores here and out of the context in the epilogue
+    const float lv_unscale = FMT == KVQ_TQ4 ? kTq4InvGamma : 1.0f;
+    const float cz = p.sm_scale * kLog2e * (q_bound > 0.0f ? ldexpf(1.0f, e_q - 14) : 1.0f) * lv_unscale;
     const uint32_t tmem = *sTmem;
 
     // queries -> f16 pair (value, residual) in the score's B layout (K-major,
@@ -448,25 +430,16 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnParams p) {
             bool o_init = false, ok = true;
             for (int tile = 0; tile < n_tiles && ok; ++tile) {
                 for (int kc = 0; kc < 9 && ok; ++kc) {
-                    const int s = FMT == KVQ_KV8 ? (kc & 3) : (kc & 1) * 2;
+                    const int s = kc & 3;
                     ok = mbar_wait(&bars[kBarFull0 + s], fills[s] & 1, sAbort);
                     ++fills[s];
-                    if (FMT == KVQ_TQ4) {
-                        ok = ok && mbar_wait(&bars[kBarFull0 + s + 1], fills[s + 1] & 1, sAbort);
-                        ++fills[s + 1];
-                    }
                     tc_after();
                     const uint32_t d = tmem + (kc < 8 ? kColSL : kColSR);
                     const uint64_t a = dslot0 + s * kSlotStep, bq = dq0 + kc * kQStep;
 #pragma unroll
                     for (int ks = 0; ks < 4; ++ks)
                         umma_f16(d, a + 2 * ks, bq + 2 * ks, id_score, (kc == 0 || kc == 8) ? (ks > 0 ? 1u : 0u) : 1u);
-                    if (FMT == KVQ_TQ4) {
-#pragma unroll
-                        for (int ks = 0; ks < 4; ++ks) umma_f16(d, a + kSlotStep + 2 * ks, bq + 2 * ks, kIdescScore, 1u);
-                    }
                     umma_commit(&bars[kBarEmpty0 + s]);
-                    if (FMT == KVQ_TQ4) umma_commit(&bars[kBarEmpty0 + s + 1]);
                     if (kc == 8) umma_commit(&bars[kBarScore]);
                 }
                 ok = ok && mbar_wait(&bars[kBarP], tile & 1, sAbort);
@@ -523,20 +496,14 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnParams p) {
         }
         // ---- score chunks: 9 chunks of 64 dims (8 latent, 1 rope) ----
         for (int kc = 0; kc < 9; ++kc) {
-            const int s = FMT == KVQ_KV8 ? (kc & 3) : (kc & 1) * 2;
+            const int s = kc & 3;
             if (uses[s] > 0) mbar_wait(&bars[kBarEmpty0 + s], (uses[s] - 1) & 1, sAbort);
-            if (FMT == KVQ_TQ4 && uses[s + 1] > 0) mbar_wait(&bars[kBarEmpty0 + s + 1], (uses[s + 1] - 1) & 1, sAbort);
             RawChunk rc;
             KVQ_NEXT_CHUNK(rc);
             store_chunk<FMT>(rc, valid, sSlot + s * kSlotBytes, sLut, tid);
-            if (FMT == KVQ_TQ4) store_delta_chunk(rc, valid, sSlot + (s + 1) * kSlotBytes, sDelta, tid);
             fence_async_smem();
             mbar_arrive(&bars[kBarFull0 + s]);
             ++uses[s];
-            if (FMT == KVQ_TQ4) {
-                mbar_arrive(&bars[kBarFull0 + s + 1]);
-                ++uses[s + 1];
-            }
         }
         // ---- softmax of the tile (thread = row, 32 heads) ----
         mbar_wait(&bars[kBarScore], tile & 1, sAbort);
@@ -690,7 +657,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnParams p) {
 #pragma unroll
                 for (int j = 0; j < 32; ++j) {
                     const int h = hbase + 32 * c + j;
-                    p.ws_o[(item * p.n_heads + h) * kMlaDV + dim] = o_init ? __uint_as_float(v[j]) * s_ref : 0.0f;
+                    p.ws_o[(item * p.n_heads + h) * kMlaDV + dim] =
+                        o_init ? __uint_as_float(v[j]) * (s_ref * lv_unscale) : 0.0f;
                 }
             }
         }

@@ -11,8 +11,17 @@ is odd-symmetric, so for an even level count the middle threshold is 0):
 
 Levels and thresholds are rounded once from float64 to float32.
 
+The tensor-core TQ4 kernel multiplies the 16 levels by one scale before
+rounding them to f16 (the MMA operand type), chosen so that all of them land
+close to f16 values; --level-scale repeats that search: random scales in
+[1, 2), then a fine grid around the best, minimising the largest relative
+rounding error over the levels.
+
 Run:  python gen_codebook.py   (prints the C initialisers)
+      python gen_codebook.py --level-scale
 """
+import sys
+
 import numpy as np
 from scipy import optimize, stats
 
@@ -43,6 +52,35 @@ def emit(name: str, c: np.ndarray) -> None:
     print(f"{name}_THRESH_BITS = {{ {hx(th)} }};")
 
 
+def level_scale_error(g: np.ndarray, levels_f32: np.ndarray) -> np.ndarray:
+    x = g[:, None] * np.abs(levels_f32.astype(np.float64))[None, :]
+    return np.max(np.abs(x.astype(np.float16).astype(np.float64) - x) / x, axis=1)
+
+
+def level_scale(levels: np.ndarray, seed: int = 1) -> tuple[float, float]:
+    lv = levels.astype(np.float32)
+    rng = np.random.default_rng(seed)
+    cand = []
+    for _ in range(20):
+        g = 1.0 + rng.random(2_000_000)
+        e = level_scale_error(g, lv)
+        i = np.argsort(e)[:20]
+        cand += list(zip(e[i], g[i]))
+    cand.sort()
+    best = cand[0]
+    for _, g0 in cand[:50]:
+        g = g0 + np.linspace(-2e-5, 2e-5, 400001)
+        e = level_scale_error(g, lv)
+        i = int(np.argmin(e))
+        if e[i] < best[0]:
+            best = (e[i], g[i])
+    return float(np.float32(best[1])), float(best[0])
+
+
 if __name__ == "__main__":
-    emit("TQ4", solve(16))
-    emit("K2", solve(4))
+    if "--level-scale" in sys.argv:
+        g, err = level_scale(solve(16))
+        print(f"TQ4 level scale {g!r} (f32), largest relative f16 rounding error {err:.3e}")
+    else:
+        emit("TQ4", solve(16))
+        emit("K2", solve(4))

@@ -123,3 +123,18 @@ def test_attention_refuses_misaligned_pointers(kvq):
                             1 << 30, 0, None) == 1
     assert L.kv_attn_decode_append(1, C.byref(lay), C.c_void_p((1 << 20) + 4), ok, ok, 1, 2, 64, ok, ok, ok, 10,
                                    0.1, ok, ws, 1 << 30, 0, None) == 1
+
+
+def test_tq4_tensor_level_scale_keeps_levels_near_f16(oracle):
+    """The tensor-core TQ4 kernel feeds f16(f32(level * scale)) to the MMA; the
+    scale in its source keeps every level within 1e-4 relative of its f16 copy
+    (unscaled levels are off by up to 3.2e-4)."""
+    src = open(os.path.join(ROOT, "quantized_kv_cache_kv8_gb300", "csrc", "attn_tc.cu")).read()
+    g = np.float32(float(re.search(r"constexpr float kTq4Gamma = ([0-9.]+)f;", src).group(1)))
+    lv, _ = oracle.tq4_codebook()
+    scaled = (lv.astype(np.float32) * g).astype(np.float32)
+    rel = np.abs(scaled.astype(np.float16).astype(np.float64) - lv.astype(np.float64) * float(g)) / \
+        np.abs(lv.astype(np.float64) * float(g))
+    assert rel.max() <= 1e-4, rel.max()
+    plain = np.abs(lv.astype(np.float16).astype(np.float64) - lv) / np.abs(lv)
+    assert plain.max() > 3e-4
