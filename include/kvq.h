@@ -196,6 +196,36 @@ kvq_status kv_attn_decode_append(kvq_format fmt, const kvq_mla_layout* layout,
                                  int64_t max_total_rows, float sm_scale, float* out,
                                  void* workspace, size_t workspace_bytes, kvq_path path, void* stream);
 
+/* Bytes of workspace kv_attn_decode_gather needs for at most
+ * max_total_selected selected rows across `batch` sequences (the path choice,
+ * and so the split, depends on q_dtype here).  Returns 0 for invalid or
+ * unsupported arguments. */
+size_t kv_attn_gather_workspace_size(kvq_format fmt, const kvq_mla_layout* layout, kvq_dtype q_dtype,
+                                     int32_t batch, int32_t n_heads, int64_t max_total_selected, kvq_path path);
+
+/* Decode attention over selected rows only: the top-k rows a sparse-attention
+ * indexer picked for each sequence, read in place by absolute index ([P1]
+ * Commits item 2 and the rebase comment's point 1: the KV8 shadow's
+ * absolute-index gather for DSA selection).  For sequence b the rows are the
+ * pool rows sel_rows[cu_sel[b]] .. sel_rows[cu_sel[b+1] - 1]; otherwise as
+ * kv_attn_decode (same formulas, same output).
+ *   pool_rows   number of rows in the pool; an index outside [0, pool_rows)
+ *               sets KVQ_ERR_ARG in the device error word and is clamped
+ *               (never read out of bounds)
+ *   sel_rows    [cu_sel[batch]] int64, device, absolute pool rows (any order,
+ *               repeats allowed)
+ *   cu_sel      [batch+1] int64, device, non-decreasing, cu_sel[0] = 0
+ *   max_total_selected  host-side bound on cu_sel[batch]
+ * Paths: the tensor-core kernel for KV8 with bf16 queries, the fp32 kernels
+ * otherwise (KVQ_PATH_TENSOR with another format or query type returns
+ * KVQ_ERR_UNSUPPORTED). */
+kvq_status kv_attn_decode_gather(kvq_format fmt, const kvq_mla_layout* layout,
+                                 const void* q, kvq_dtype q_dtype, int32_t batch, int32_t n_heads,
+                                 const uint8_t* codes, const float* scales, int64_t pool_rows,
+                                 const int64_t* sel_rows, const int64_t* cu_sel, int64_t max_total_selected,
+                                 float sm_scale, float* out, void* workspace, size_t workspace_bytes,
+                                 kvq_path path, void* stream);
+
 /* kv_attn_decode for callers that cannot allocate device memory.  The pages
  * have no counterpart: this is a convenience of this library.
  *

@@ -240,6 +240,56 @@ kvq_status kv_attn_decode_append(kvq_format fmt, const kvq_mla_layout* layout, c
                           sm_scale, out, workspace, workspace_bytes, path, stream);
 }
 
+// Gather decode: the tensor-core kernel reads rows through an index table for
+// KV8 with bf16 queries; every other combination runs on the fp32 kernels.
+static kvq_status resolve_gather_path(kvq_format fmt, kvq_dtype qdt, kvq_path path, const kvq_mla_layout* L,
+                                      int32_t n_heads, kvq_path* out) {
+    const bool tc_ok = fmt == KVQ_KV8 && qdt == KVQ_BF16 && tc_supported(*L, n_heads);
+    if (path == KVQ_PATH_TENSOR && !tc_ok) return KVQ_ERR_UNSUPPORTED;
+    *out = path == KVQ_PATH_SIMT ? KVQ_PATH_SIMT : (tc_ok ? KVQ_PATH_TENSOR : KVQ_PATH_SIMT);
+    return KVQ_OK;
+}
+
+size_t kv_attn_gather_workspace_size(kvq_format fmt, const kvq_mla_layout* layout, kvq_dtype q_dtype, int32_t batch,
+                                     int32_t n_heads, int64_t max_total_selected, kvq_path path) {
+    if (check_attn_layout(fmt, layout) != KVQ_OK || check_path(path) != KVQ_OK) return 0;
+    if (batch < 0 || n_heads < 0 || max_total_selected < 0 || (q_dtype != KVQ_F32 && q_dtype != KVQ_BF16)) return 0;
+    kvq_path rp;
+    if (resolve_gather_path(fmt, q_dtype, path, layout, n_heads, &rp) != KVQ_OK) return 0;
+    const AttnPlan pl = plan_decode(rp, batch, n_heads, max_total_selected);
+    return kWsHeader + partial_bytes(pl.max_items, n_heads, layout->v_dim);
+}
+
+kvq_status kv_attn_decode_gather(kvq_format fmt, const kvq_mla_layout* layout, const void* q, kvq_dtype q_dtype,
+                                 int32_t batch, int32_t n_heads, const uint8_t* codes, const float* scales,
+                                 int64_t pool_rows, const int64_t* sel_rows, const int64_t* cu_sel,
+                                 int64_t max_total_selected, float sm_scale, float* out, void* workspace,
+                                 size_t workspace_bytes, kvq_path path, void* stream) {
+    kvq_status s = check_attn_layout(fmt, layout);
+    if (s != KVQ_OK) return s;
+    if ((s = check_path(path)) != KVQ_OK) return s;
+    if (batch < 0 || n_heads < 0 || max_total_selected < 0 || pool_rows < 0 ||
+        (q_dtype != KVQ_F32 && q_dtype != KVQ_BF16))
+        return KVQ_ERR_ARG;
+    if (batch > 65535 || n_heads > 65535) return KVQ_ERR_UNSUPPORTED;
+    if (batch == 0 || n_heads == 0) return KVQ_OK;
+    kvq_path rp;
+    if ((s = resolve_gather_path(fmt, q_dtype, path, layout, n_heads, &rp)) != KVQ_OK) return s;
+    if (!q || !cu_sel || !out) return KVQ_ERR_ARG;
+    if (max_total_selected > 0 && (!codes || !scales || !sel_rows || pool_rows == 0)) return KVQ_ERR_ARG;
+    if (!attn_pointers_aligned(q, codes, scales, cu_sel, out) || !aligned(sel_rows, 8)) return KVQ_ERR_ARG;
+    if (!isfinite(sm_scale)) return KVQ_ERR_ARG;
+    const size_t need = kv_attn_gather_workspace_size(fmt, layout, q_dtype, batch, n_heads, max_total_selected, path);
+    if (!workspace || workspace_bytes < need) return KVQ_ERR_WORKSPACE;
+    cudaStream_t st = (cudaStream_t)stream;
+    const AttnPlan pl = plan_decode(rp, batch, n_heads, max_total_selected);
+    if (rp == KVQ_PATH_TENSOR)
+        return cuda_status(launch_attn_tc(fmt, *layout, q, q_dtype, batch, n_heads, codes, scales, cu_sel, -1, pl,
+                                          sm_scale, out, workspace, st, sel_rows, pool_rows));
+    return cuda_status(launch_attn_simt(fmt, *layout, q, q_dtype, batch, n_heads, codes, scales, cu_sel, -1, pl,
+                                        sm_scale, out, workspace, st, sel_rows, pool_rows));
+}
+
 static AttnPlan plan_prefill(int64_t n_past, int64_t n_new) {
     AttnPlan pl{};
     pl.chunk = std::max<int64_t>(1, n_past + n_new);

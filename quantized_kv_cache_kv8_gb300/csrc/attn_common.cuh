@@ -36,7 +36,22 @@ struct AttnParams {
     uint8_t* codes_out;
     float* scales_out;
     int32_t bd0, bd1;
+    // decode over selected rows: the rows of sequence b are the pool rows
+    // sel[cu[b]] .. sel[cu[b+1] - 1] (absolute indices, each < pool_rows)
+    const int64_t* sel;
+    int64_t pool_rows;
 };
+
+// Pool row of logical row r of a gather decode; an index outside the pool sets
+// the error word and is clamped so that nothing outside the pool is read.
+__device__ __forceinline__ int64_t gather_row(const AttnParams& p, int64_t r) {
+    int64_t pr = p.sel[r];
+    if (pr < 0 || pr >= p.pool_rows) {
+        atomicCAS(p.err, 0, KVQ_ERR_ARG);
+        pr = pr < 0 ? 0 : p.pool_rows - 1;
+    }
+    return pr;
+}
 
 __device__ __forceinline__ void set_err(int32_t* err, int32_t code) { atomicCAS(err, 0, code); }
 

@@ -32,9 +32,11 @@ constexpr int kNT = 256;  // threads per CTA
 constexpr int kXS = 580;  // shared-memory row stride in floats (bank spread)
 constexpr int kSmSMs = 152;
 
-constexpr size_t kSmemFloats = (size_t)kHG * kXS + (size_t)kTR * kXS + kTR * 2 + kTR * kHG + kHG + 16 + 6;
+// shared floats: queries, tile, row scales, weights, rescale factors, TQ4 levels (16),
+// item info (4 int64), the pool rows of a gather tile (kTR int64)
+constexpr size_t kSmemFloats = (size_t)kHG * kXS + (size_t)kTR * kXS + kTR * 2 + kTR * kHG + kHG + 16 + 8 + 2 * kTR;
 
-template <int FMT, bool QBF16>
+template <int FMT, bool QBF16, bool GATHER>
 __global__ void __launch_bounds__(kNT, 2) attn_partial_kernel(AttnParams p) {
     launch_dependents();
     extern __shared__ float4 smem4[];
@@ -45,6 +47,7 @@ __global__ void __launch_bounds__(kNT, 2) attn_partial_kernel(AttnParams p) {
     float* alpha = P + kTR * kHG;
     float* lvs = alpha + kHG;
     int64_t* info = reinterpret_cast<int64_t*>(lvs + 16);
+    int64_t* prow = info + 4;   // gather: the pool rows of the tile
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int64_t item = blockIdx.x;
@@ -116,6 +119,10 @@ __global__ void __launch_bounds__(kNT, 2) attn_partial_kernel(AttnParams p) {
 
     for (int64_t t0 = row0; t0 < row1; t0 += kTR) {
         const int nt = (int)min((int64_t)kTR, row1 - t0);
+        if (GATHER) {
+            if (tid < kTR) prow[tid] = tid < nt ? gather_row(p, t0 + tid) : 0;
+            __syncthreads();
+        }
         // decode the tile to code values (no scale applied)
         if (FMT == KVQ_KV8) {
             const uint32_t* src = reinterpret_cast<const uint32_t*>(p.codes + t0 * kD);
@@ -123,7 +130,8 @@ __global__ void __launch_bounds__(kNT, 2) attn_partial_kernel(AttnParams p) {
                 const int r = w / (kD / 4), c4 = (w - r * (kD / 4)) * 4;
                 float4 f = make_float4(0.f, 0.f, 0.f, 0.f);
                 if (r < nt) {
-                    const uint32_t u = __ldg(src + w);
+                    const uint32_t u = GATHER ? __ldg(reinterpret_cast<const uint32_t*>(p.codes + prow[r] * kD) + c4 / 4)
+                                              : __ldg(src + w);
                     const float2 a = e4m3x2_to_float2((uint16_t)(u & 0xffffu));
                     const float2 c = e4m3x2_to_float2((uint16_t)(u >> 16));
                     f = make_float4(a.x, a.y, c.x, c.y);
@@ -136,7 +144,8 @@ __global__ void __launch_bounds__(kNT, 2) attn_partial_kernel(AttnParams p) {
                 const int r = w / (kD / 8), c8 = (w - r * (kD / 8)) * 8;
                 float f[8];
                 if (r < nt) {
-                    const uint32_t u = __ldg(src + w);
+                    const uint32_t u = GATHER ? __ldg(reinterpret_cast<const uint32_t*>(p.codes + prow[r] * (kD / 2)) + c8 / 8)
+                                              : __ldg(src + w);
 #pragma unroll
                     for (int j = 0; j < 8; ++j) f[j] = lvs[(u >> (4 * j)) & 15u];
                 } else {
@@ -150,7 +159,7 @@ __global__ void __launch_bounds__(kNT, 2) attn_partial_kernel(AttnParams p) {
         if (tid < kTR) {
             float sL = 0.0f, sR = 0.0f;
             if (tid < nt) {
-                const int64_t row = t0 + tid;
+                const int64_t row = GATHER ? prow[tid] : t0 + tid;
                 if (p.n_blocks == 2) {
                     sL = p.scales[row * 2];
                     sR = p.scales[row * 2 + 1];
@@ -363,10 +372,10 @@ __global__ void __launch_bounds__(128) attn_merge_kernel(AttnParams p, float* __
 template <int FMT, bool QBF16>
 cudaError_t launch_partial(const AttnParams& p, int64_t grid_x, int groups, cudaStream_t stream) {
     const size_t smem = kSmemFloats * sizeof(float);
-    cudaError_t e = cudaFuncSetAttribute(attn_partial_kernel<FMT, QBF16>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    auto kernel = p.sel ? attn_partial_kernel<FMT, QBF16, true> : attn_partial_kernel<FMT, QBF16, false>;
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    attn_partial_kernel<FMT, QBF16><<<dim3((unsigned)grid_x, (unsigned)groups), kNT, smem, stream>>>(p);
+    kernel<<<dim3((unsigned)grid_x, (unsigned)groups), kNT, smem, stream>>>(p);
     return cudaGetLastError();
 }
 
@@ -420,10 +429,12 @@ size_t partial_bytes(int64_t max_items, int32_t n_heads, int32_t v_dim) {
 cudaError_t launch_attn_simt(kvq_format fmt, const kvq_mla_layout& L, const void* q, kvq_dtype qdt, int32_t n_seq,
                              int32_t n_heads, const uint8_t* codes, const float* scales, const int64_t* cu_seqlens,
                              int64_t prefill_past, const AttnPlan& plan, float sm_scale, float* out,
-                             void* workspace, cudaStream_t stream) {
+                             void* workspace, cudaStream_t stream, const int64_t* sel, int64_t pool_rows) {
     if (n_seq == 0 || n_heads == 0) return cudaSuccess;
-    const AttnParams p = make_attn_params(fmt, L, q, n_seq, n_heads, codes, scales, cu_seqlens, prefill_past, plan,
-                                          sm_scale, workspace);
+    AttnParams p = make_attn_params(fmt, L, q, n_seq, n_heads, codes, scales, cu_seqlens, prefill_past, plan,
+                                    sm_scale, workspace);
+    p.sel = sel;
+    p.pool_rows = pool_rows;
     const int groups = (n_heads + kHG - 1) / kHG;
     cudaError_t e;
     if (fmt == KVQ_KV8)

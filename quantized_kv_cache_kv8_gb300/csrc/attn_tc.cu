@@ -706,10 +706,14 @@ AttnPlan plan_decode_tc(int32_t batch, int32_t n_heads, int64_t max_total_rows) 
 cudaError_t launch_attn_tc(kvq_format fmt, const kvq_mla_layout& L, const void* q, kvq_dtype qdt, int32_t n_seq,
                            int32_t n_heads, const uint8_t* codes, const float* scales, const int64_t* cu_seqlens,
                            int64_t prefill_past, const AttnPlan& plan, float sm_scale, float* out, void* workspace,
-                           cudaStream_t stream) {
+                           cudaStream_t stream, const int64_t* sel, int64_t pool_rows) {
     if (n_seq == 0 || n_heads == 0) return cudaSuccess;
-    const AttnParams p = make_attn_params(fmt, L, q, n_seq, n_heads, codes, scales, cu_seqlens, prefill_past, plan,
-                                          sm_scale, workspace);
+    AttnParams p = make_attn_params(fmt, L, q, n_seq, n_heads, codes, scales, cu_seqlens, prefill_past, plan,
+                                    sm_scale, workspace);
+    p.sel = sel;
+    p.pool_rows = pool_rows;
+    // only the KV8 / bf16-query kernel reads rows through an index table
+    if (sel && !(fmt == KVQ_KV8 && qdt == KVQ_BF16)) return cudaErrorNotSupported;
     const int groups = n_heads / kHC;
     cudaError_t e;
     if (fmt == KVQ_KV8)

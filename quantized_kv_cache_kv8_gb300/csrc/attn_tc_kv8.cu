@@ -62,7 +62,8 @@ constexpr uint32_t kOffRed = kOffAlpha + kHC * 4;   // 4 quadrants x 64 heads of
 constexpr uint32_t kOffBar = kOffRed + 4 * kHC * 4;
 constexpr uint32_t kOffMisc = kOffBar + 16 * 8;      // abort flag, TMEM base, item info
 constexpr uint32_t kOffNew = kOffMisc + 32;          // appended row: 576 codes, 2 scales, row index
-constexpr uint32_t kSmemUsed = kOffNew + 576 + 16;
+constexpr uint32_t kOffRowIdx = kOffNew + 576 + 16;   // gather: pool rows of 2 tiles (int64)
+constexpr uint32_t kSmemUsed = kOffRowIdx + 2 * kRows * 8;
 static_assert(kOffSlot % 1024 == 0, "swizzled operands need 1024-byte alignment");
 static_assert(kSmemUsed <= 232448, "shared memory budget");
 
@@ -103,22 +104,30 @@ __device__ __forceinline__ uint4 load16(const uint8_t* __restrict__ codes, int64
     if (APPEND && row == rn) return *reinterpret_cast<const uint4*>(snew + byte);
     return __ldg(reinterpret_cast<const uint4*>(codes + row * kMlaD + byte));
 }
-template <bool APPEND>
+// Pool row of tile row `row`: contiguous rows, or (gather) the tile's index table.
+template <bool GATHER>
+__device__ __forceinline__ int64_t pool_row(int64_t t0, int row, const int64_t* prow) {
+    return GATHER ? prow[row] : t0 + row;
+}
+template <bool APPEND, bool GATHER>
 __device__ __forceinline__ void load_group(RawGroup& r, const uint8_t* __restrict__ codes, int64_t t0, int nt, int g,
-                                           int warp, int lane, int64_t rn, const unsigned char* snew) {
+                                           int warp, int lane, int64_t rn, const unsigned char* snew,
+                                           const int64_t* prow) {
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
         const int row = 2 * (warp + 8 * i) + (lane >> 4);
-        r.v[i] = row < nt ? load16<APPEND>(codes, t0 + row, 256 * g + 16 * (lane & 15), rn, snew) : make_uint4(0u, 0u, 0u, 0u);
+        r.v[i] = row < nt ? load16<APPEND>(codes, pool_row<GATHER>(t0, row, prow), 256 * g + 16 * (lane & 15), rn, snew)
+                          : make_uint4(0u, 0u, 0u, 0u);
     }
 }
-template <bool APPEND>
+template <bool APPEND, bool GATHER>
 __device__ __forceinline__ void load_rope(RawRope& r, const uint8_t* __restrict__ codes, int64_t t0, int nt, int tid,
-                                          int64_t rn, const unsigned char* snew) {
+                                          int64_t rn, const unsigned char* snew, const int64_t* prow) {
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
         const int u = tid + kWorkers * i, row = u >> 2;
-        r.v[i] = row < nt ? load16<APPEND>(codes, t0 + row, 512 + 16 * (u & 3), rn, snew) : make_uint4(0u, 0u, 0u, 0u);
+        r.v[i] = row < nt ? load16<APPEND>(codes, pool_row<GATHER>(t0, row, prow), 512 + 16 * (u & 3), rn, snew)
+                          : make_uint4(0u, 0u, 0u, 0u);
     }
 }
 
@@ -154,7 +163,7 @@ __device__ __forceinline__ float warp_columns(float (&v)[32], int lane) {
     return v[0];
 }
 
-template <bool APPEND>
+template <bool APPEND, bool GATHER>
 __global__ void __launch_bounds__(kThreads, 1) attn_tc_kv8_kernel(AttnParams p) {
     launch_dependents();
     extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -172,6 +181,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kv8_kernel(AttnParams p) 
     unsigned char* sNew = sm + kOffNew;                       // appended row's codes
     float* sNewScale = reinterpret_cast<float*>(sm + kOffNew + 576);
     int64_t* sNewRow = reinterpret_cast<int64_t*>(sm + kOffNew + 584);
+    int64_t* sRowIdx = reinterpret_cast<int64_t*>(sm + kOffRowIdx);   // gather: [2][kRows]
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int64_t item = blockIdx.x;
@@ -210,10 +220,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kv8_kernel(AttnParams p) 
         *sAbort = 0;
     }
     if (tid < kHC) sM[tid] = -INFINITY;
-    if (tid == 0) {
+    if (!GATHER && tid == 0) {
         const int64_t n = min((int64_t)kRows, row1 - row0);
         prefetch_l2(p.codes + row0 * kMlaD, (uint32_t)(n * kMlaD));
     }
+    if (GATHER && tid < kRows) sRowIdx[tid] = row0 + tid < row1 ? gather_row(p, row0 + tid) : 0;
 
     // ---- appended row: the MMA warp (idle until the first score) encodes it
     // into shared memory; the group-0 CTA of the chunk also writes it to the
@@ -252,7 +263,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kv8_kernel(AttnParams p) 
 #pragma unroll
         for (int i = 0; i < kQPer; ++i) qraw[i] = __ldg(qv + tid + i * kWorkers);
         for (int64_t r = row0 + tid; r < row1; r += kWorkers)
-            if (!APPEND || r != rn) smax = fmaxf(smax, p.scales[r * p.n_blocks]);
+            if (!APPEND || r != rn) smax = fmaxf(smax, p.scales[(GATHER ? gather_row(p, r) : r) * p.n_blocks]);
 #pragma unroll
         for (int i = 0; i < kQPer; ++i) {
             const uint32_t in[4] = {qraw[i].x, qraw[i].y, qraw[i].z, qraw[i].w};
@@ -366,7 +377,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kv8_kernel(AttnParams p) 
     auto load_scales = [&](int64_t t0n, int ntn) {
         sl_next = sr_next = 0.0f;
         if (srow < ntn) {
-            const int64_t r = t0n + srow;
+            const int64_t r = GATHER ? sRowIdx[(((t0n - row0) / kRows) & 1) * kRows + srow] : t0n + srow;
             if (APPEND && r == rn) {
                 sl_next = sNewScale[0];
                 sr_next = sNewScale[p.n_blocks - 1];
@@ -380,19 +391,22 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kv8_kernel(AttnParams p) 
     RawRope rawC;
     {
         const int nt0 = (int)min((int64_t)kRows, row1 - row0);
-        load_group<APPEND>(rawA, p.codes, row0, nt0, 0, warp, lane, rn, sNew);
-        load_group<APPEND>(rawB, p.codes, row0, nt0, 1, warp, lane, rn, sNew);
-        load_rope<APPEND>(rawC, p.codes, row0, nt0, tid, rn, sNew);
+        load_group<APPEND, GATHER>(rawA, p.codes, row0, nt0, 0, warp, lane, rn, sNew, sRowIdx);
+        load_group<APPEND, GATHER>(rawB, p.codes, row0, nt0, 1, warp, lane, rn, sNew, sRowIdx);
+        load_rope<APPEND, GATHER>(rawC, p.codes, row0, nt0, tid, rn, sNew, sRowIdx);
         load_scales(row0, nt0);
     }
     int t = 0;
     for (; t < n_tiles; ++t) {
         const int64_t t0 = row0 + (int64_t)t * kRows;
         const int nt = (int)min((int64_t)kRows, row1 - t0);
-        if (tid == 0 && t0 + kRows < row1) {
+        if (!GATHER && tid == 0 && t0 + kRows < row1) {
             const int64_t n = min((int64_t)kRows, row1 - (t0 + kRows));
             prefetch_l2(p.codes + (t0 + kRows) * kMlaD, (uint32_t)(n * kMlaD));
         }
+        // gather: the next tile's pool rows, read after the softmax's first barrier
+        if (GATHER && tid < kRows && t0 + kRows < row1)
+            sRowIdx[((t + 1) & 1) * kRows + tid] = t0 + kRows + tid < row1 ? gather_row(p, t0 + kRows + tid) : 0;
         const float my_sl = sl_next, my_sr = sr_next;
         // ---- decode the tile: groups A (chunks 0-3), B (4-7), C (rope) ----
         const uint32_t prev = (uint32_t)(t - 1) & 1u;
@@ -421,7 +435,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kv8_kernel(AttnParams p) 
         }
         const int64_t t1 = t0 + kRows;
         const int nt1 = (int)min((int64_t)kRows, row1 - t1);
-        if (t + 1 < n_tiles) load_group<APPEND>(rawA, p.codes, t1, nt1, 0, warp, lane, rn, sNew);
+        if (!GATHER && t + 1 < n_tiles) load_group<APPEND, GATHER>(rawA, p.codes, t1, nt1, 0, warp, lane, rn, sNew, nullptr);
 
         // ---- softmax of the tile: thread = row srow, 32 heads ----
         mbar_wait(&bars[kBarScore], (uint32_t)t & 1u, sAbort);
@@ -444,15 +458,24 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kv8_kernel(AttnParams p) 
         load_z();
         // the rest of tile t+1 is requested while the tensor cores are idle
         // (their operand reads compete with these loads for the SM's memory pipe)
-        if (t + 1 < n_tiles) {
-            load_group<APPEND>(rawB, p.codes, t1, nt1, 1, warp, lane, rn, sNew);
-            load_rope<APPEND>(rawC, p.codes, t1, nt1, tid, rn, sNew);
+        if (!GATHER && t + 1 < n_tiles) {
+            load_group<APPEND, GATHER>(rawB, p.codes, t1, nt1, 1, warp, lane, rn, sNew, nullptr);
+            load_rope<APPEND, GATHER>(rawC, p.codes, t1, nt1, tid, rn, sNew, nullptr);
             load_scales(t1, nt1);
         }
         bool flag = *sAbort != 0;
 #pragma unroll
         for (int j = 0; j < 32; ++j) flag |= z[j] > sM[32 * hq + j] + kLagLog2;
-        if (worker_any(flag)) {
+        const bool any_flag = worker_any(flag);
+        if (GATHER && t + 1 < n_tiles) {
+            // the barrier above made the next tile's index table visible
+            const int64_t* prow = sRowIdx + ((t + 1) & 1) * kRows;
+            load_group<APPEND, GATHER>(rawA, p.codes, t1, nt1, 0, warp, lane, rn, sNew, prow);
+            load_group<APPEND, GATHER>(rawB, p.codes, t1, nt1, 1, warp, lane, rn, sNew, prow);
+            load_rope<APPEND, GATHER>(rawC, p.codes, t1, nt1, tid, rn, sNew, prow);
+            load_scales(t1, nt1);
+        }
+        if (any_flag) {
             if (worker_any(*sAbort != 0)) break;
             // exact column max of the tile, new running max, rescale factors
             sRed[(warp & 3) * kHC + 32 * hq + lane] = warp_columns<true>(z, lane);
@@ -555,22 +578,22 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kv8_kernel(AttnParams p) 
 }  // namespace
 
 namespace {
-template <bool APPEND>
+template <bool APPEND, bool GATHER>
 cudaError_t launch_kv8(const AttnParams& p, int64_t grid_x, int groups, cudaStream_t stream) {
-    cudaError_t e = cudaFuncSetAttribute(attn_tc_kv8_kernel<APPEND>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)kSmemUsed);
+    cudaError_t e = cudaFuncSetAttribute(attn_tc_kv8_kernel<APPEND, GATHER>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemUsed);
     if (e != cudaSuccess) return e;
-    attn_tc_kv8_kernel<APPEND><<<dim3((unsigned)grid_x, (unsigned)groups), kThreads, kSmemUsed, stream>>>(p);
+    attn_tc_kv8_kernel<APPEND, GATHER><<<dim3((unsigned)grid_x, (unsigned)groups), kThreads, kSmemUsed, stream>>>(p);
     return cudaGetLastError();
 }
 }  // namespace
 
 cudaError_t launch_attn_tc_kv8_bf16(const AttnParams& p, int64_t grid_x, int groups, cudaStream_t stream) {
-    return launch_kv8<false>(p, grid_x, groups, stream);
+    return p.sel ? launch_kv8<false, true>(p, grid_x, groups, stream) : launch_kv8<false, false>(p, grid_x, groups, stream);
 }
 
 cudaError_t launch_attn_tc_kv8_bf16_append(const AttnParams& p, int64_t grid_x, int groups, cudaStream_t stream) {
-    return launch_kv8<true>(p, grid_x, groups, stream);
+    return launch_kv8<true, false>(p, grid_x, groups, stream);
 }
 
 }  // namespace kvq

@@ -173,7 +173,8 @@ constexpr size_t kWsHeader = 256;   // error word + padding
 cudaError_t launch_attn_simt(kvq_format fmt, const kvq_mla_layout& L, const void* q, kvq_dtype qdt, int32_t n_seq,
                              int32_t n_heads, const uint8_t* codes, const float* scales, const int64_t* cu_seqlens,
                              int64_t prefill_past, const AttnPlan& plan, float sm_scale, float* out,
-                             void* workspace, cudaStream_t stream);
+                             void* workspace, cudaStream_t stream, const int64_t* sel = nullptr,
+                             int64_t pool_rows = 0);
 
 // Tensor-core attention (tcgen05, 64 heads per CTA).
 bool tc_supported(const kvq_mla_layout& L, int32_t n_heads);
@@ -187,7 +188,7 @@ cudaError_t launch_attn_tc_kv8_append(const kvq_mla_layout& L, const float* x_ne
 cudaError_t launch_attn_tc(kvq_format fmt, const kvq_mla_layout& L, const void* q, kvq_dtype qdt, int32_t n_seq,
                            int32_t n_heads, const uint8_t* codes, const float* scales, const int64_t* cu_seqlens,
                            int64_t prefill_past, const AttnPlan& plan, float sm_scale, float* out, void* workspace,
-                           cudaStream_t stream);
+                           cudaStream_t stream, const int64_t* sel = nullptr, int64_t pool_rows = 0);
 
 // K2/V4
 cudaError_t launch_k2v4_encode(const kvq_k2v4_layout& L, const float* k, const float* v, int32_t batch,

@@ -79,6 +79,11 @@ def _declare(L):
     L.kv_attn_workspace_size.argtypes = [C.c_int, pl, I32, I32, I64, C.c_int]
     L.kv_attn_decode.restype = C.c_int
     L.kv_attn_decode.argtypes = [C.c_int, pl, P, C.c_int, I32, I32, P, P, P, I64, C.c_float, P, P, S, C.c_int, P]
+    L.kv_attn_gather_workspace_size.restype = S
+    L.kv_attn_gather_workspace_size.argtypes = [C.c_int, pl, C.c_int, I32, I32, I64, C.c_int]
+    L.kv_attn_decode_gather.restype = C.c_int
+    L.kv_attn_decode_gather.argtypes = [C.c_int, pl, P, C.c_int, I32, I32, P, P, I64, P, P, I64, C.c_float, P, P, S,
+                                        C.c_int, P]
     L.kv_attn_decode_append.restype = C.c_int
     L.kv_attn_decode_append.argtypes = [C.c_int, pl, P, P, P, C.c_int, I32, I32, P, P, P, I64, C.c_float, P, P, S,
                                         C.c_int, P]
@@ -209,6 +214,28 @@ def kv_attn_decode_append(fmt: int, x_new, dst_rows, q, codes, scales, cu_seqlen
                                     float(sm_scale), _ptr(out, torch.float32, "out"),
                                     _ptr(workspace, torch.uint8, "workspace"), workspace.numel(), path,
                                     _stream(stream)), "kv_attn_decode_append")
+
+
+def kv_attn_gather_workspace_size(fmt: int, batch: int, n_heads: int, max_total_selected: int, bf16: bool = True,
+                                  layout: MLALayout | None = None, path: int = PATH_AUTO) -> int:
+    layout = layout or mla_layout()
+    return lib().kv_attn_gather_workspace_size(fmt, C.byref(layout), KVQ_BF16 if bf16 else KVQ_F32, batch, n_heads,
+                                               max_total_selected, path)
+
+
+def kv_attn_decode_gather(fmt: int, q, codes, scales, sel_rows, cu_sel, out, workspace, max_total_selected: int,
+                          sm_scale: float = SM_SCALE_MLA, layout: MLALayout | None = None, path: int = PATH_AUTO,
+                          stream=None):
+    """Decode over selected rows: sequence b attends the pool rows
+    sel_rows[cu_sel[b]:cu_sel[b+1]] (absolute indices)."""
+    layout = layout or mla_layout()
+    B, H = q.shape[0], q.shape[1]
+    _ok(lib().kv_attn_decode_gather(fmt, C.byref(layout), _ptr(q, None, "q"), _qdtype(q), B, H,
+                                    _ptr(codes, torch.uint8, "codes"), _ptr(scales, torch.float32, "scales"),
+                                    int(codes.shape[0]), _ptr(sel_rows, torch.int64, "sel_rows"),
+                                    _ptr(cu_sel, torch.int64, "cu_sel"), int(max_total_selected), float(sm_scale),
+                                    _ptr(out, torch.float32, "out"), _ptr(workspace, torch.uint8, "workspace"),
+                                    workspace.numel(), path, _stream(stream)), "kv_attn_decode_gather")
 
 
 def kv_attn_decode_noalloc(fmt: int, q, codes, scales, cu_seqlens, out, max_total_rows: int,
