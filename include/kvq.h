@@ -55,7 +55,9 @@ typedef enum kvq_status {
     KVQ_ERR_WORKSPACE = 3,    /* workspace missing or smaller than required */
     KVQ_ERR_CUDA = 4,         /* a CUDA launch or runtime call failed */
     KVQ_ERR_UNSUPPORTED = 5,  /* valid arguments this build has no kernel for */
-    KVQ_ERR_DEVICE = 6        /* the device error word was set (see kvq_read_device_error) */
+    KVQ_ERR_DEVICE = 6,       /* the device error word was set (see kvq_read_device_error) */
+    KVQ_ERR_MISMATCH = 7,     /* cache file of another tier, codec, bit width or layout: refused */
+    KVQ_ERR_IO = 8            /* cache file missing, unreadable, corrupt or of the wrong size */
 } kvq_status;
 
 typedef enum kvq_format { KVQ_KV8 = 1, KVQ_TQ4 = 2 } kvq_format;
@@ -327,6 +329,53 @@ kvq_status kv_attn_decode_k2v4(const kvq_k2v4_layout* layout, const float* q, in
                                const uint8_t* k_codes, const uint16_t* k_scales, const uint8_t* v_blocks,
                                const uint16_t* k_win, const uint16_t* v_win, float sm_scale, float* out,
                                void* workspace, size_t workspace_bytes, kvq_path path, void* stream);
+
+
+/* ------------------------------------------------------------------------ */
+/* Persistence of quantized row pools ([P1] "KV persistence across mode      */
+/* changes"; [P2] "What's in it", the .coli_kv bullet)                       */
+/* ------------------------------------------------------------------------ */
+
+/* Files are versioned by their magic, which names the tier: "COLIKV" (v1,
+ * f32 rows), "COLIKV2" (v2, KV8 codes), "COLIKV3" (v3, TQ4 codes); eight int64
+ * header words follow: rows, row dimension, scale blocks, the two block dims,
+ * v_dim, the TQ sign seed and, in h[7], codec << 8 | bits (TQ4: codec 1, 4
+ * bits).  Then one record per row: its codes, then its f32 scales (v1: its f32
+ * values).  All pointers here are HOST pointers; copy device pools to the host
+ * first.  Files are written to "<path>.tmp" and renamed over `path`.
+ * `msg` (optional, msg_len bytes) receives the reason of a refusal. */
+
+/* Writes a KV8 or TQ4 pool of n_rows rows (codes [n][row_bytes], scales
+ * [n][n_blocks]). */
+kvq_status kvq_cache_save(const char* path, kvq_format fmt, const kvq_mla_layout* layout, int64_t n_rows,
+                          const uint8_t* codes, const float* scales);
+
+/* Writes f32 rows [n][D] as a v1 file (the unquantized tier). */
+kvq_status kvq_cache_save_f32(const char* path, const kvq_mla_layout* layout, int64_t n_rows, const float* rows);
+
+/* Reads a file's tier (1, 2, 3), row count and the 8 header words. */
+kvq_status kvq_cache_info(const char* path, int32_t* version, int64_t* n_rows, int64_t* header_words, char* msg,
+                          size_t msg_len);
+
+/* Reads a KV8 / TQ4 pool into codes / scales (room for `capacity` rows).  A
+ * file of another tier, TQ codec, bit width, rotation seed or layout returns
+ * KVQ_ERR_MISMATCH (e.g. "file is fp8 (KV8), current mode is KV_TQ: refused")
+ * and reads nothing; a size that disagrees with the header returns KVQ_ERR_IO;
+ * more rows than `capacity` returns KVQ_ERR_WORKSPACE. */
+kvq_status kvq_cache_load(const char* path, kvq_format fmt, const kvq_mla_layout* layout, int64_t capacity,
+                          uint8_t* codes, float* scales, int64_t* n_rows, char* msg, size_t msg_len);
+
+/* Reads a v1 (f32) file: a quantized mode loads it by encoding these rows
+ * (kv8_encode / tq4_encode) and keeps the file unchanged until it saves. */
+kvq_status kvq_cache_load_f32(const char* path, const kvq_mla_layout* layout, int64_t capacity, float* rows,
+                              int64_t* n_rows, char* msg, size_t msg_len);
+
+/* Appends n_new rows to a KV8 / TQ4 file in place: the records are written,
+ * flushed, and only then counted in the header.  Bytes past the header's
+ * count -- an append interrupted before its header update -- are dropped
+ * first (and `msg` says so).  Mode checks as kvq_cache_load. */
+kvq_status kvq_cache_append(const char* path, kvq_format fmt, const kvq_mla_layout* layout, int64_t n_new,
+                            const uint8_t* codes, const float* scales, int64_t* n_rows, char* msg, size_t msg_len);
 
 #ifdef __cplusplus
 }

@@ -114,6 +114,8 @@ const char* kvq_status_string(kvq_status s) {
         case KVQ_ERR_CUDA: return "CUDA launch or runtime error";
         case KVQ_ERR_UNSUPPORTED: return "arguments valid but not supported by this build";
         case KVQ_ERR_DEVICE: return "device error word set";
+        case KVQ_ERR_MISMATCH: return "cache file of another tier, codec, bit width or layout: refused";
+        case KVQ_ERR_IO: return "cache file missing, unreadable, corrupt or of the wrong size";
     }
     return "unknown status";
 }

@@ -79,6 +79,15 @@ def _declare(L):
     L.kv_attn_workspace_size.argtypes = [C.c_int, pl, I32, I32, I64, C.c_int]
     L.kv_attn_decode.restype = C.c_int
     L.kv_attn_decode.argtypes = [C.c_int, pl, P, C.c_int, I32, I32, P, P, P, I64, C.c_float, P, P, S, C.c_int, P]
+    for name in ("kvq_cache_save", "kvq_cache_save_f32", "kvq_cache_info", "kvq_cache_load", "kvq_cache_load_f32",
+                 "kvq_cache_append"):
+        getattr(L, name).restype = C.c_int
+    L.kvq_cache_save.argtypes = [C.c_char_p, C.c_int, pl, I64, P, P]
+    L.kvq_cache_save_f32.argtypes = [C.c_char_p, pl, I64, P]
+    L.kvq_cache_info.argtypes = [C.c_char_p, P, P, P, C.c_char_p, S]
+    L.kvq_cache_load.argtypes = [C.c_char_p, C.c_int, pl, I64, P, P, P, C.c_char_p, S]
+    L.kvq_cache_load_f32.argtypes = [C.c_char_p, pl, I64, P, P, C.c_char_p, S]
+    L.kvq_cache_append.argtypes = [C.c_char_p, C.c_int, pl, I64, P, P, P, C.c_char_p, S]
     L.kv_attn_gather_workspace_size.restype = S
     L.kv_attn_gather_workspace_size.argtypes = [C.c_int, pl, C.c_int, I32, I32, I64, C.c_int]
     L.kv_attn_decode_gather.restype = C.c_int
@@ -301,3 +310,96 @@ def kv_attn_decode_k2v4(layout: K2V4Layout, q, n_cells: int, k_codes, k_scales, 
                                   _ptr(v_win, torch.int16, "v_win"), float(sm_scale), _ptr(out, torch.float32, "out"),
                                   _ptr(workspace, torch.uint8, "workspace"), workspace.numel(), path,
                                   _stream(stream)), "kv_attn_decode_k2v4")
+
+
+# -- persistence of quantized pools (host arrays) ------------------------------
+
+class CacheFileError(KvqError):
+    """A cache file was refused (another tier/codec/layout) or unreadable; .msg says why."""
+
+    def __init__(self, status: int, what: str, msg: str):
+        super().__init__(status, what)
+        self.msg = msg
+
+    def __str__(self):
+        return f"{super().__str__()}: {self.msg}"
+
+
+def _np_ptr(a):
+    return None if a is None else C.c_void_p(a.ctypes.data)
+
+
+def _row_bytes(fmt: int, layout: MLALayout) -> int:
+    D = sum(layout.block_dim[b] for b in range(layout.n_blocks))
+    return D if fmt == KVQ_KV8 else D // 2
+
+
+def cache_save(path: str, fmt: int, codes, scales, layout: MLALayout | None = None):
+    import numpy as np
+    layout = layout or mla_layout()
+    codes = np.ascontiguousarray(codes, np.uint8)
+    scales = np.ascontiguousarray(scales, np.float32)
+    _ok(lib().kvq_cache_save(path.encode(), fmt, C.byref(layout), codes.shape[0], _np_ptr(codes), _np_ptr(scales)),
+        "kvq_cache_save")
+
+
+def cache_save_f32(path: str, rows, layout: MLALayout | None = None):
+    import numpy as np
+    layout = layout or mla_layout()
+    rows = np.ascontiguousarray(rows, np.float32)
+    _ok(lib().kvq_cache_save_f32(path.encode(), C.byref(layout), rows.shape[0], _np_ptr(rows)), "kvq_cache_save_f32")
+
+
+def cache_info(path: str):
+    """(version, rows, header words)."""
+    import numpy as np
+    v, n, h = C.c_int32(), C.c_int64(), np.zeros(8, np.int64)
+    msg = C.create_string_buffer(256)
+    st = lib().kvq_cache_info(path.encode(), C.byref(v), C.byref(n), _np_ptr(h), msg, 256)
+    if st != 0:
+        raise CacheFileError(st, "kvq_cache_info", msg.value.decode())
+    return v.value, n.value, h
+
+
+def cache_load(path: str, fmt: int, capacity: int, layout: MLALayout | None = None):
+    """(codes [n][row_bytes] u8, scales [n][n_blocks] f32); raises CacheFileError on refusal."""
+    import numpy as np
+    layout = layout or mla_layout()
+    codes = np.zeros((capacity, _row_bytes(fmt, layout)), np.uint8)
+    scales = np.zeros((capacity, layout.n_blocks), np.float32)
+    n = C.c_int64()
+    msg = C.create_string_buffer(256)
+    st = lib().kvq_cache_load(path.encode(), fmt, C.byref(layout), capacity, _np_ptr(codes), _np_ptr(scales),
+                              C.byref(n), msg, 256)
+    if st != 0:
+        raise CacheFileError(st, "kvq_cache_load", msg.value.decode())
+    return codes[:n.value], scales[:n.value]
+
+
+def cache_load_f32(path: str, capacity: int, layout: MLALayout | None = None):
+    import numpy as np
+    layout = layout or mla_layout()
+    D = sum(layout.block_dim[b] for b in range(layout.n_blocks))
+    rows = np.zeros((capacity, D), np.float32)
+    n = C.c_int64()
+    msg = C.create_string_buffer(256)
+    st = lib().kvq_cache_load_f32(path.encode(), C.byref(layout), capacity, _np_ptr(rows), C.byref(n), msg, 256)
+    if st != 0:
+        raise CacheFileError(st, "kvq_cache_load_f32", msg.value.decode())
+    return rows[:n.value]
+
+
+def cache_append(path: str, fmt: int, codes, scales, layout: MLALayout | None = None):
+    """Appends rows in place; returns (total rows, message)."""
+    import numpy as np
+    layout = layout or mla_layout()
+    codes = np.ascontiguousarray(codes, np.uint8)
+    scales = np.ascontiguousarray(scales, np.float32)
+    n = C.c_int64()
+    msg = C.create_string_buffer(256)
+    st = lib().kvq_cache_append(path.encode(), fmt, C.byref(layout), codes.shape[0], _np_ptr(codes), _np_ptr(scales),
+                                C.byref(n), msg, 256)
+    if st != 0:
+        raise CacheFileError(st, "kvq_cache_append", msg.value.decode())
+    return n.value, msg.value.decode()
+

@@ -35,7 +35,7 @@ def test_every_declared_symbol_is_exported(kvq):
 
 def test_status_strings_and_version(kvq):
     assert kvq.version() == "0.1.0"
-    for s in range(7):
+    for s in range(9):
         assert kvq.status_string(s)
 
 
