@@ -80,10 +80,14 @@ kvq_status resolve_path(kvq_path path, const kvq_mla_layout* L, int32_t n_heads,
     return KVQ_OK;
 }
 
-kvq_status check_k2v4_path(kvq_path path) {
-    kvq_status s = check_path(path);
-    if (s != KVQ_OK) return s;
-    return path == KVQ_PATH_TENSOR ? KVQ_ERR_UNSUPPORTED : KVQ_OK;
+// K2/V4 paths: the tensor-core kernel serves head_dim 128 and 256 (AUTO takes
+// it there), the fp32 kernel every supported layout.
+kvq_status check_k2v4_path(kvq_path path) { return check_path(path); }
+static kvq_status resolve_k2v4_path(kvq_path path, const kvq_k2v4_layout* L, bool* tensor) {
+    const bool tc = k2v4_tc_supported(*L);
+    if (path == KVQ_PATH_TENSOR && !tc) return KVQ_ERR_UNSUPPORTED;
+    *tensor = path == KVQ_PATH_SIMT ? false : tc;
+    return KVQ_OK;
 }
 
 AttnPlan plan_decode(kvq_path resolved, int32_t batch, int32_t n_heads, int64_t max_total_rows) {
@@ -375,7 +379,9 @@ size_t kv_attn_decode_k2v4_workspace_size(const kvq_k2v4_layout* layout, int32_t
                                           int64_t n_cells, kvq_path path) {
     if (check_k2v4(layout) != KVQ_OK || check_k2v4_path(path) != KVQ_OK) return 0;
     if (batch < 0 || n_q_heads < 0 || n_cells < 0) return 0;
-    const K2V4Plan pl = plan_k2v4(*layout, batch, n_q_heads, n_cells);
+    bool tensor;
+    if (resolve_k2v4_path(path, layout, &tensor) != KVQ_OK) return 0;
+    const K2V4Plan pl = plan_k2v4(*layout, batch, n_q_heads, n_cells, tensor);
     return kWsHeader + k2v4_partial_bytes(*layout, batch, n_q_heads, pl);
 }
 
@@ -399,7 +405,9 @@ kvq_status kv_attn_decode_k2v4(const kvq_k2v4_layout* layout, const float* q, in
     if (!isfinite(sm_scale)) return KVQ_ERR_ARG;
     const size_t need = kv_attn_decode_k2v4_workspace_size(layout, batch, n_q_heads, n_cells, path);
     if (!workspace || workspace_bytes < need) return KVQ_ERR_WORKSPACE;
-    const K2V4Plan pl = plan_k2v4(*layout, batch, n_q_heads, n_cells);
+    bool tensor;
+    if ((s = resolve_k2v4_path(path, layout, &tensor)) != KVQ_OK) return s;
+    const K2V4Plan pl = plan_k2v4(*layout, batch, n_q_heads, n_cells, tensor);
     return cuda_status(launch_k2v4_decode(*layout, q, batch, n_q_heads, n_cells, capacity, k_codes, k_scales,
                                           v_blocks, k_win, v_win, sm_scale, out, workspace, pl,
                                           (cudaStream_t)stream));

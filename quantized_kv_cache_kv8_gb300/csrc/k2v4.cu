@@ -7,12 +7,17 @@
 // V per cell and 32-dim block (q4_0) -- one warp per block.  Cells inside the
 // sink/window overlay also get exact fp16 copies.
 //
-// Decode (fp32 CUDA cores): one CTA per (sequence, kv head, chunk of cells)
-// serves the kv head's 8 query heads; tiles of 32 cells are dequantized to f32
-// in shared memory (overlay cells take their fp16 copy), then scores, online
-// softmax and the context follow as in the MLA path; a merge kernel combines
-// the chunks by log-sum-exp.
-#include "kvq_internal.cuh"
+// Decode, fp32 CUDA cores: one CTA per (sequence, kv head, chunk of cells)
+// serves the kv head's query heads; tiles of 32 cells are staged, dequantized
+// to f32 in shared memory (overlay cells take their fp16 copy), then scores,
+// online softmax and the context follow as in the MLA path.
+// Decode, tensor cores (head_dim 128 or 256): tiles of 128 cells are
+// dequantized to f16 in shared memory and both products run as tcgen05 MMAs
+// with the cells on M: S^T = K Q^T (N = 16: the query heads as f16 and as
+// their f16 residuals) and O^T += V^T P^T (N = 16, heads past the group are
+// zero).  Both paths write the same chunk partials; a merge kernel combines
+// them by log-sum-exp.
+#include "tc_common.cuh"
 
 #include <algorithm>
 #include <math.h>
@@ -138,19 +143,36 @@ struct K2V4DecodeParams {
     const uint16_t* v_win;
     float* ws_o;   // [batch][Hq][n_chunks][D]
     float* ws_ml;  // [batch][Hq][n_chunks][2]
+    int32_t* err;  // the workspace's error word
 };
 
 constexpr int kHQ = 8;   // query heads per CTA (one kv group)
 
+// Raw bytes of one 32-cell tile of one kv head, staged in shared memory with
+// 16-byte loads: K codes (32 x D/4), the group's K scales (D fp16), V blocks
+// (32 x D/32 x 18).  Each piece is contiguous in the cache, and as tiles start
+// on a multiple of 32 cells (and cell counts and capacities are multiples of
+// 32), each starts 16-byte aligned and lies inside the allocation.
+template <int D>
+struct RawTileBytes {
+    static constexpr int kKc = kTC * D / 4, kKs = 2 * D, kVb = kTC * (D / 32) * 18;
+    static constexpr int kTotal = kKc + kKs + kVb;
+};
+
 template <int D>
 __global__ void __launch_bounds__(kNT) k2v4_partial_kernel(K2V4DecodeParams p) {
     constexpr int XS = D + 4;
+    using RB = RawTileBytes<D>;
     extern __shared__ float4 smem4[];
     float* qs = reinterpret_cast<float*>(smem4);   // [8][XS]
     float* ks = qs + kHQ * XS;                      // [32][XS]
     float* vs = ks + kTC * XS;                      // [32][XS]
     float* P = vs + kTC * XS;                       // [32][8]
     float* alpha = P + kTC * kHQ;                   // [8]
+    unsigned char* raw = reinterpret_cast<unsigned char*>(alpha + 8);   // RB::kTotal bytes
+    const unsigned char* raw_kc = raw;
+    const uint16_t* raw_ks = reinterpret_cast<const uint16_t*>(raw + RB::kKc);
+    const unsigned char* raw_vb = raw + RB::kKc + RB::kKs;
     const int tid = threadIdx.x;
     const int chunk_id = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
     const int64_t seq = (int64_t)b * p.c.H + g;
@@ -171,8 +193,25 @@ __global__ void __launch_bounds__(kNT) k2v4_partial_kernel(K2V4DecodeParams p) {
 
     for (int64_t t0 = c0; t0 < c1; t0 += kTC) {
         const int nt = (int)min((int64_t)kTC, c1 - t0);
-        // dequantize K and V of the tile (overlay cells read their fp16 copy)
+        // stage the tile's raw bytes (a whole 32-cell group)
         const int64_t grp_idx = t0 / kG;
+        {
+            const uint4* kc_src = reinterpret_cast<const uint4*>(p.k_codes + (seq * p.c.cap + t0) * (D / 4));
+            const uint4* ks_src = reinterpret_cast<const uint4*>(p.k_scales + (seq * (p.c.cap / kG) + grp_idx) * D);
+            const uint4* vb_src = reinterpret_cast<const uint4*>(p.v_blocks + (seq * p.c.cap + t0) * (D / 32) * 18);
+            for (int i = tid; i < RB::kTotal / 16; i += kNT) {
+                uint4 w;
+                if (i < RB::kKc / 16)
+                    w = __ldg(kc_src + i);
+                else if (i < (RB::kKc + RB::kKs) / 16)
+                    w = __ldg(ks_src + (i - RB::kKc / 16));
+                else
+                    w = __ldg(vb_src + (i - (RB::kKc + RB::kKs) / 16));
+                reinterpret_cast<uint4*>(raw)[i] = w;
+            }
+        }
+        __syncthreads();
+        // dequantize K and V of the tile (overlay cells read their fp16 copy)
         for (int i = tid; i < kTC * D; i += kNT) {
             const int r = i / D, d = i - r * D;
             float kv = 0.0f, vv = 0.0f;
@@ -184,10 +223,10 @@ __global__ void __launch_bounds__(kNT) k2v4_partial_kernel(K2V4DecodeParams p) {
                     kv = __half2float(__ushort_as_half(p.k_win[o2]));
                     vv = __half2float(__ushort_as_half(p.v_win[o2]));
                 } else {
-                    const uint8_t kb = p.k_codes[(seq * p.c.cap + cell) * (D / 4) + d / 4];
-                    const float ksc = __half2float(__ushort_as_half(p.k_scales[(seq * (p.c.cap / kG) + grp_idx) * D + d]));
+                    const uint8_t kb = raw_kc[r * (D / 4) + d / 4];
+                    const float ksc = __half2float(__ushort_as_half(raw_ks[d]));
                     kv = p.c.lv[(kb >> (2 * (d & 3))) & 3] * ksc;
-                    const uint8_t* blk = p.v_blocks + ((seq * p.c.cap + cell) * (D / 32) + d / 32) * 18;
+                    const unsigned char* blk = raw_vb + (r * (D / 32) + d / 32) * 18;
                     const float dd = __half2float(__ushort_as_half((uint16_t)(blk[0] | (blk[1] << 8))));
                     const int j = d & 31;
                     const int code = j < 16 ? (blk[2 + j] & 15) : (blk[2 + j - 16] >> 4);
@@ -276,6 +315,311 @@ __global__ void k2v4_merge_kernel(K2V4DecodeParams p, float* __restrict__ out) {
     }
 }
 
+// ---------------------------------------------------------------------------
+// Tensor-core decode
+// ---------------------------------------------------------------------------
+using namespace tc;
+constexpr int kRowsT = 128;     // cells per tile: the MMA M
+constexpr int kNq = 16;         // MMA N: 8 heads as f16 + their residuals (score), heads (context)
+constexpr int kThreadsT = 256;
+constexpr uint32_t kChunkT = kRowsT * 128;   // 128 cells x 64 dims f16, 128-byte swizzle
+
+template <int D>
+struct SmemT {
+    static constexpr int kChunks = D / 64;
+    static constexpr uint32_t kOffK = 0;
+    static constexpr uint32_t kOffV = kOffK + kChunks * kChunkT;
+    static constexpr uint32_t kOffQ = kOffV + kChunks * kChunkT;     // kChunks x (16 rows x 128 B)
+    static constexpr uint32_t kOffP = kOffQ + kChunks * kNq * 128;    // 2 x (16 rows x 128 B): P^T by 64 cells
+    static constexpr uint32_t kOffRed = kOffP + 2 * kNq * 128;        // [4 warps][8] max, [4][8] sums
+    static constexpr uint32_t kOffState = kOffRed + 2 * 4 * 8 * 4;    // running max, sum, qmax (8 each), levels (4)
+    static constexpr uint32_t kOffBar = kOffState + 3 * 8 * 4 + 16;
+    static constexpr uint32_t kOffMisc = kOffBar + 4 * 8;             // abort flag, TMEM base
+    static constexpr uint32_t kBytes = kOffMisc + 16;
+};
+
+constexpr uint32_t kColS = 0, kColO = 32, kTmemColsT = 64;
+constexpr uint32_t kIdescK2Score = idesc_f16(128, kNq, false, false);
+constexpr uint32_t kIdescK2Ctx = idesc_f16(128, kNq, true, false);
+
+__device__ __forceinline__ uint32_t pack_half2(float a, float b) {
+    const __half2 h = __floats2half2_rn(a, b);
+    return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreadsT, 1) k2v4_tc_kernel(K2V4DecodeParams p) {
+    using SM = SmemT<D>;
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    unsigned char* sK = smem_raw + SM::kOffK;
+    unsigned char* sV = smem_raw + SM::kOffV;
+    unsigned char* sQ = smem_raw + SM::kOffQ;
+    unsigned char* sP = smem_raw + SM::kOffP;
+    float* sRedM = reinterpret_cast<float*>(smem_raw + SM::kOffRed);
+    float* sRedL = sRedM + 32;
+    float* sM = reinterpret_cast<float*>(smem_raw + SM::kOffState);
+    float* sL = sM + 8;
+    float* sQmax = sL + 8;
+    float* sLv = sQmax + 8;   // the 4 K levels
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem_raw + SM::kOffBar);   // 0 score, 1 context
+    volatile int* sAbort = reinterpret_cast<volatile int*>(smem_raw + SM::kOffMisc);
+    uint32_t* sTmem = reinterpret_cast<uint32_t*>(smem_raw + SM::kOffMisc + 4);
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int chunk_id = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+    const int64_t seq = (int64_t)b * p.c.H + g;
+    const int64_t c0 = (int64_t)chunk_id * p.chunk;
+    const int64_t c1 = min(c0 + p.chunk, p.c.T);
+    const int n_tiles = (int)((c1 - c0 + kRowsT - 1) / kRowsT);
+    const int grp = p.grp;
+
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(sTmem)),
+                     "r"(kTmemColsT));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
+    if (tid == 32) {
+        for (int i = 0; i < 2; ++i)
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(&bars[i])), "r"(1u));
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        *sAbort = smem_u32(smem_raw) & 1023u ? 1 : 0;   // the swizzled operands need a 1024-byte base
+    }
+    if (tid < 8) {
+        sM[tid] = -INFINITY;
+        sL[tid] = 0.0f;
+    }
+    if (tid < 4) sLv[tid] = p.c.lv[tid];
+    // P^T rows 8..15 (no head) stay zero; rows of heads past the group too
+    for (int i = tid; i < 2 * kNq * 128 / 16; i += kThreadsT) reinterpret_cast<uint4*>(sP)[i] = make_uint4(0, 0, 0, 0);
+
+    // ---- query: the group's heads as an f16 pair (value, residual), scaled
+    // by a power of two so that every element stays below 2^14 ----
+    const float* qg = p.q + ((int64_t)b * p.Hq + (int64_t)g * grp) * D;
+    float qmax = 0.0f;
+    for (int i = tid; i < grp * D; i += kThreadsT) qmax = fmaxf(qmax, fabsf(qg[i]));
+    qmax = warp_max(qmax);
+    if (lane == 0) sQmax[warp] = qmax;
+    __syncthreads();
+    float q_max = 0.0f;
+    for (int i = 0; i < 8; ++i) q_max = fmaxf(q_max, sQmax[i]);
+    int e_q = 0;
+    if (q_max > 0.0f) frexpf(q_max, &e_q);
+    const float q_scale = q_max > 0.0f ? ldexpf(1.0f, 14 - e_q) : 1.0f;
+    const float cz = p.sm_scale * kLog2e * (q_max > 0.0f ? ldexpf(1.0f, e_q - 14) : 1.0f);
+    for (int i = tid; i < 8 * D; i += kThreadsT) {
+        const int h = i / D, d = i - h * D;
+        const float x = h < grp ? qg[h * D + d] * q_scale : 0.0f;
+        const __half hi = __float2half_rn(x);
+        const __half lo = __float2half_rn(x - __half2float(hi));
+        unsigned char* chunk = sQ + (d >> 6) * (kNq * 128);
+        *reinterpret_cast<__half*>(chunk + sw128(h, (d & 63) * 2)) = hi;
+        *reinterpret_cast<__half*>(chunk + sw128(8 + h, (d & 63) * 2)) = lo;
+    }
+    tc_before();
+    __syncthreads();
+    tc_after();
+    const uint32_t tmem = *sTmem;
+
+    const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
+    for (int t = 0; t < n_tiles; ++t) {
+        const int64_t t0 = c0 + (int64_t)t * kRowsT;
+        const int nt = (int)min((int64_t)kRowsT, c1 - t0);
+        // the previous tile's context MMAs still read sV and P^T
+        if (t > 0) mbar_wait(&bars[1], (uint32_t)(t - 1) & 1u, sAbort);
+        tc_after();
+        // ---- dequantize the tile to f16 (cells on rows, 64 dims per chunk) ----
+        for (int it = tid; it < kRowsT * (D / 32); it += kThreadsT) {
+            const int r = it / (D / 32), j = it - r * (D / 32);   // cell, 32-dim slice
+            uint32_t kw[16], vw[16];
+            if (r < nt) {
+                const int64_t cell = t0 + r;
+                const int64_t slot = overlay_slot(cell, p.c);
+                if (slot >= 0) {
+                    // exact fp16 copies
+                    const uint4* kwin = reinterpret_cast<const uint4*>(p.k_win + (seq * p.c.slots + slot) * D + 32 * j);
+                    const uint4* vwin = reinterpret_cast<const uint4*>(p.v_win + (seq * p.c.slots + slot) * D + 32 * j);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const uint4 a = __ldg(kwin + i), c = __ldg(vwin + i);
+                        kw[4 * i] = a.x; kw[4 * i + 1] = a.y; kw[4 * i + 2] = a.z; kw[4 * i + 3] = a.w;
+                        vw[4 * i] = c.x; vw[4 * i + 1] = c.y; vw[4 * i + 2] = c.z; vw[4 * i + 3] = c.w;
+                    }
+                } else {
+                    // K: 2-bit codes (32 dims = 8 bytes) times the group's per-dim fp16 scales
+                    const uint2 kc = __ldg(reinterpret_cast<const uint2*>(p.k_codes + (seq * p.c.cap + cell) * (D / 4) + 8 * j));
+                    const uint4* ksc = reinterpret_cast<const uint4*>(p.k_scales + (seq * (p.c.cap / kG) + cell / kG) * D + 32 * j);
+                    const uint32_t kcw[2] = {kc.x, kc.y};
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const uint4 sc = __ldg(ksc + i);
+                        const uint32_t scw[4] = {sc.x, sc.y, sc.z, sc.w};
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            const int d0 = 8 * i + 2 * k;   // dims d0, d0 + 1 of the slice
+                            const uint32_t c_a = (kcw[d0 >> 4] >> (2 * (d0 & 15))) & 3u;
+                            const uint32_t c_b = (kcw[(d0 + 1) >> 4] >> (2 * ((d0 + 1) & 15))) & 3u;
+                            const float s_a = __half2float(__ushort_as_half((uint16_t)(scw[k] & 0xffffu)));
+                            const float s_b = __half2float(__ushort_as_half((uint16_t)(scw[k] >> 16)));
+                            kw[4 * i + k] = pack_half2(sLv[c_a] * s_a, sLv[c_b] * s_b);
+                        }
+                    }
+                    // V: q4_0 block (d, then 16 bytes: element e in the low nibble of byte e, e + 16 in the high)
+                    const uint16_t* blk =
+                        reinterpret_cast<const uint16_t*>(p.v_blocks + ((seq * p.c.cap + cell) * (D / 32) + j) * 18);
+                    const float dd = __half2float(__ushort_as_half(__ldg(blk)));
+                    uint32_t cb[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) cb[i] = __ldg(blk + 1 + i);   // code bytes 2i, 2i + 1
+#pragma unroll
+                    for (int e = 0; e < 32; e += 2) {
+                        const int e0 = e & 15;   // byte index of elements e, e + 1 (same nibble half)
+                        const uint32_t b0 = (cb[e0 >> 1] >> (8 * (e0 & 1))) & 0xffu;
+                        const uint32_t b1 = (cb[(e0 + 1) >> 1] >> (8 * ((e0 + 1) & 1))) & 0xffu;
+                        const int q0 = e < 16 ? (int)(b0 & 15u) : (int)(b0 >> 4);
+                        const int q1 = e < 16 ? (int)(b1 & 15u) : (int)(b1 >> 4);
+                        vw[e / 2] = pack_half2((float)(q0 - 8) * dd, (float)(q1 - 8) * dd);
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int i = 0; i < 16; ++i) kw[i] = vw[i] = 0u;
+            }
+            unsigned char* kdst = sK + (j >> 1) * kChunkT;
+            unsigned char* vdst = sV + (j >> 1) * kChunkT;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int byte = (j & 1) * 64 + 16 * i;
+                *reinterpret_cast<uint4*>(kdst + sw128(r, byte)) = make_uint4(kw[4 * i], kw[4 * i + 1], kw[4 * i + 2], kw[4 * i + 3]);
+                *reinterpret_cast<uint4*>(vdst + sw128(r, byte)) = make_uint4(vw[4 * i], vw[4 * i + 1], vw[4 * i + 2], vw[4 * i + 3]);
+            }
+        }
+        fence_async_smem();
+        tc_before();
+        __syncthreads();
+        tc_after();
+        // ---- score MMAs ----
+        if (tid == 0 && !*sAbort) {
+            const uint64_t dk = umma_desc(smem_u32(sK), 16, 1024), dq = umma_desc(smem_u32(sQ), 16, 1024);
+#pragma unroll
+            for (int c = 0; c < D / 64; ++c)
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks)
+                    umma_f16(tmem + kColS, dk + c * (kChunkT >> 4) + 2 * ks, dq + c * (kNq * 128 >> 4) + 2 * ks,
+                             kIdescK2Score, (c | ks) ? 1u : 0u);
+            umma_commit(&bars[0]);
+        }
+        // ---- softmax: warps 0-3, thread = cell (TMEM lane), the group's heads ----
+        if (warp < 4) {
+            mbar_wait(&bars[0], (uint32_t)t & 1u, sAbort);
+            tc_after();
+            uint32_t sv[16];
+            tmem_ld16(tmem + lane_base + kColS, sv);
+            tmem_wait_ld();
+            const int r = 32 * warp + lane;
+            float z[8];
+#pragma unroll
+            for (int h = 0; h < 8; ++h)
+                z[h] = (r < nt && h < grp) ? (__uint_as_float(sv[h]) + __uint_as_float(sv[8 + h])) * cz : -INFINITY;
+#pragma unroll
+            for (int h = 0; h < 8; ++h) {
+                const float m = warp_max(z[h]);
+                if (lane == 0) sRedM[warp * 8 + h] = m;
+            }
+            asm volatile("bar.sync 2, 128;" ::: "memory");
+            float mnew[8], alpha[8], pv[8];
+#pragma unroll
+            for (int h = 0; h < 8; ++h) {
+                const float mt = fmaxf(fmaxf(sRedM[h], sRedM[8 + h]), fmaxf(sRedM[16 + h], sRedM[24 + h]));
+                mnew[h] = fmaxf(sM[h], mt);
+                alpha[h] = (sM[h] == -INFINITY) ? 0.0f : ex2(sM[h] - mnew[h]);
+                pv[h] = mnew[h] == -INFINITY ? 0.0f : ex2(z[h] - mnew[h]);
+            }
+            unsigned char* pc = sP + (r >> 6) * (kNq * 128);
+#pragma unroll
+            for (int h = 0; h < 8; ++h) *reinterpret_cast<__half*>(pc + sw128(h, (r & 63) * 2)) = __float2half_rn(pv[h]);
+#pragma unroll
+            for (int h = 0; h < 8; ++h) {
+                float l = pv[h];
+#pragma unroll
+                for (int o = 16; o >= 1; o >>= 1) l += __shfl_xor_sync(kFull, l, o);
+                if (lane == 0) sRedL[warp * 8 + h] = l;
+            }
+            if (t > 0) {
+                // rescale O^T (its lanes are dims, its first 8 columns heads)
+#pragma unroll
+                for (int m = 0; m < D / 128; ++m) {
+                    uint32_t ov[16];
+                    tmem_ld16(tmem + lane_base + kColO + 16 * m, ov);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int h = 0; h < 8; ++h) ov[h] = __float_as_uint(__uint_as_float(ov[h]) * alpha[h]);
+                    tmem_st16(tmem + lane_base + kColO + 16 * m, ov);
+                }
+                tmem_wait_st();
+            }
+            asm volatile("bar.sync 2, 128;" ::: "memory");
+            if (tid < 8) {
+                float a = 0.0f, mn = 0.0f;
+#pragma unroll
+                for (int h = 0; h < 8; ++h)
+                    if (h == tid) {
+                        a = alpha[h];
+                        mn = mnew[h];
+                    }
+                sL[tid] = sL[tid] * a + ((sRedL[tid] + sRedL[8 + tid]) + (sRedL[16 + tid] + sRedL[24 + tid]));
+                sM[tid] = mn;
+            }
+        }
+        fence_async_smem();
+        tc_before();
+        __syncthreads();
+        tc_after();
+        // ---- context MMAs ----
+        if (tid == 0 && !*sAbort) {
+            const uint64_t dv = umma_desc(smem_u32(sV), kChunkT, 1024), dp = umma_desc(smem_u32(sP), 16, 1024);
+#pragma unroll
+            for (int m = 0; m < D / 128; ++m)
+#pragma unroll
+                for (int ks = 0; ks < kRowsT / 16; ++ks)
+                    umma_f16(tmem + kColO + 16 * m, dv + 2 * m * (kChunkT >> 4) + 128 * ks,
+                             dp + (ks >> 2) * (kNq * 128 >> 4) + 2 * (ks & 3), kIdescK2Ctx, (t > 0 || ks > 0) ? 1u : 0u);
+            umma_commit(&bars[1]);
+        }
+    }
+    // ---- epilogue: O^T -> chunk partials (natural-log max, sum) ----
+    if (n_tiles > 0) {
+        volatile int never = 0;
+        if (!mbar_wait(&bars[1], (uint32_t)(n_tiles - 1) & 1u, &never)) *sAbort = 1;
+    }
+    tc_after();
+    if (*sAbort) {
+        if (tid == 0) atomicCAS(p.err, 0, KVQ_ERR_DEVICE);
+    } else if (warp < 4) {
+#pragma unroll
+        for (int m = 0; m < D / 128; ++m) {
+            uint32_t ov[16];
+            tmem_ld16(tmem + lane_base + kColO + 16 * m, ov);
+            tmem_wait_ld();
+            const int d = 128 * m + 32 * warp + lane;
+#pragma unroll
+            for (int h = 0; h < 8; ++h)
+                if (h < grp) {
+                    const int64_t slot = ((int64_t)b * p.Hq + (int64_t)g * grp + h) * p.n_chunks + chunk_id;
+                    p.ws_o[slot * D + d] = n_tiles > 0 ? __uint_as_float(ov[h]) : 0.0f;
+                }
+        }
+        if (tid < grp) {
+            const int64_t slot = ((int64_t)b * p.Hq + (int64_t)g * grp + tid) * p.n_chunks + chunk_id;
+            p.ws_ml[slot * 2] = sM[tid] * kLn2;
+            p.ws_ml[slot * 2 + 1] = sL[tid];
+        }
+    }
+    tc_before();
+    __syncthreads();
+    tc_after();
+    if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemColsT));
+}
+
 K2V4Params make_params(const kvq_k2v4_layout& L, int64_t T, int64_t cap) {
     K2V4Params p{};
     p.H = L.n_kv_heads;
@@ -309,8 +653,21 @@ cudaError_t launch_k2v4_encode(const kvq_k2v4_layout& L, const float* k, const f
     return cudaGetLastError();
 }
 
-K2V4Plan plan_k2v4(const kvq_k2v4_layout& L, int32_t batch, int32_t, int64_t n_cells) {
+bool k2v4_tc_supported(const kvq_k2v4_layout& L) { return L.head_dim == 128 || L.head_dim == 256; }
+
+K2V4Plan plan_k2v4(const kvq_k2v4_layout& L, int32_t batch, int32_t, int64_t n_cells, bool tensor) {
     K2V4Plan pl{};
+    pl.tensor = tensor;
+    if (tensor) {
+        // about one CTA per SM, chunks of whole 128-cell tiles
+        const int64_t per = std::max<int64_t>(1, (int64_t)batch * L.n_kv_heads);
+        const int64_t target = std::max<int64_t>(1, (int64_t)kSmSMs / per);
+        int64_t chunk = (std::max<int64_t>(n_cells, 1) + target - 1) / target;
+        chunk = std::max<int64_t>(kRowsT, (chunk + kRowsT - 1) / kRowsT * kRowsT);
+        pl.chunk = chunk;
+        pl.n_chunks = (int32_t)((n_cells + chunk - 1) / chunk);
+        return pl;
+    }
     const int64_t per = std::max<int64_t>(1, (int64_t)batch * L.n_kv_heads);
     const int64_t target = std::max<int64_t>(1, (int64_t)kSmSMs * 4 / per);
     int64_t chunk = (std::max<int64_t>(n_cells, 1) + target - 1) / target;
@@ -344,15 +701,37 @@ cudaError_t launch_k2v4_decode(const kvq_k2v4_layout& L, const float* q, int32_t
     p.v_blocks = v_blocks;
     p.k_win = k_win;
     p.v_win = v_win;
+    p.err = static_cast<int32_t*>(workspace);
     char* ws = static_cast<char*>(workspace) + kWsHeader;
     p.ws_o = reinterpret_cast<float*>(ws);
     p.ws_ml = p.ws_o + (size_t)batch * n_q_heads * plan.n_chunks * L.head_dim;
     const dim3 grid(plan.n_chunks, L.n_kv_heads, batch);
     cudaError_t e = cudaSuccess;
+    if (plan.tensor) {
+        switch (L.head_dim) {
+#define KVQ_TC_CASE(DD)                                                                                 \
+    case DD: {                                                                                          \
+        e = cudaFuncSetAttribute(k2v4_tc_kernel<DD>, cudaFuncAttributeMaxDynamicSharedMemorySize,      \
+                                 (int)SmemT<DD>::kBytes);                                              \
+        if (e != cudaSuccess) return e;                                                                 \
+        k2v4_tc_kernel<DD><<<grid, kThreadsT, SmemT<DD>::kBytes, stream>>>(p);                         \
+        break;                                                                                          \
+    }
+            KVQ_TC_CASE(128)
+            KVQ_TC_CASE(256)
+#undef KVQ_TC_CASE
+            default: return cudaErrorInvalidValue;
+        }
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+        k2v4_merge_kernel<<<dim3(n_q_heads, batch), 256, 0, stream>>>(p, out);
+        return cudaGetLastError();
+    }
     switch (L.head_dim) {
 #define KVQ_D_CASE(DD)                                                                                  \
     case DD: {                                                                                          \
-        const size_t smem = ((size_t)(kHQ + 2 * kTC) * (DD + 4) + kTC * kHQ + kHQ) * sizeof(float);    \
+        const size_t smem = ((size_t)(kHQ + 2 * kTC) * (DD + 4) + kTC * kHQ + 8) * sizeof(float) +     \
+                            RawTileBytes<DD>::kTotal;                                                  \
         e = cudaFuncSetAttribute(k2v4_partial_kernel<DD>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
                                  (int)smem);                                                            \
         if (e != cudaSuccess) return e;                                                                 \

@@ -197,8 +197,10 @@ cudaError_t launch_k2v4_encode(const kvq_k2v4_layout& L, const float* k, const f
 struct K2V4Plan {
     int64_t chunk;
     int32_t n_chunks;
+    bool tensor;   // tensor-core kernel (head_dim 128 or 256), else fp32
 };
-K2V4Plan plan_k2v4(const kvq_k2v4_layout& L, int32_t batch, int32_t n_q_heads, int64_t n_cells);
+bool k2v4_tc_supported(const kvq_k2v4_layout& L);
+K2V4Plan plan_k2v4(const kvq_k2v4_layout& L, int32_t batch, int32_t n_q_heads, int64_t n_cells, bool tensor);
 size_t k2v4_partial_bytes(const kvq_k2v4_layout& L, int32_t batch, int32_t n_q_heads, const K2V4Plan& p);
 cudaError_t launch_k2v4_decode(const kvq_k2v4_layout& L, const float* q, int32_t batch, int32_t n_q_heads,
                                int64_t n_cells, int64_t cap, const uint8_t* k_codes, const uint16_t* k_scales,
