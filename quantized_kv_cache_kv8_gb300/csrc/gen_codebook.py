@@ -17,8 +17,13 @@ close to f16 values; --level-scale repeats that search: random scales in
 [1, 2), then a fine grid around the best, minimising the largest relative
 rounding error over the levels.
 
+The tensor-core K2/V4 kernel does the same for the 4 K levels (searched over
+the 1024 f16 values in [1, 2), so that the scale itself is exact in f16):
+--k2-level-scale.
+
 Run:  python gen_codebook.py   (prints the C initialisers)
       python gen_codebook.py --level-scale
+      python gen_codebook.py --k2-level-scale
 """
 import sys
 
@@ -78,7 +83,18 @@ def level_scale(levels: np.ndarray, seed: int = 1) -> tuple[float, float]:
 
 
 if __name__ == "__main__":
-    if "--level-scale" in sys.argv:
+    if "--k2-level-scale" in sys.argv:
+        lv = solve(4).astype(np.float32)
+        cand = np.array([1.0 + k / 1024 for k in range(1024)], np.float64)
+        best = None
+        for g in cand:
+            x = np.abs(lv[2:]).astype(np.float64) * g
+            h = (np.abs(lv[2:]) * np.float32(g)).astype(np.float32).astype(np.float16).astype(np.float64)
+            e = float(np.max(np.abs(h - x) / x))
+            if best is None or e < best[0]:
+                best = (e, g)
+        print(f"K2 level scale {float(best[1])!r} (exact in f16), largest relative f16 rounding error {best[0]:.3e}")
+    elif "--level-scale" in sys.argv:
         g, err = level_scale(solve(16))
         print(f"TQ4 level scale {g!r} (f32), largest relative f16 rounding error {err:.3e}")
     else:

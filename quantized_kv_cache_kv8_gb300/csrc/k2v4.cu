@@ -161,6 +161,7 @@ struct RawTileBytes {
 
 template <int D>
 __global__ void __launch_bounds__(kNT) k2v4_partial_kernel(K2V4DecodeParams p) {
+    launch_dependents();
     constexpr int XS = D + 4;
     using RB = RawTileBytes<D>;
     extern __shared__ float4 smem4[];
@@ -298,21 +299,60 @@ __global__ void __launch_bounds__(kNT) k2v4_partial_kernel(K2V4DecodeParams p) {
     }
 }
 
-__global__ void k2v4_merge_kernel(K2V4DecodeParams p, float* __restrict__ out) {
+// One pass over the chunk partials of (sequence, query head), 8 chunks at a
+// time with their loads in flight together, combined by an online
+// log-sum-exp; launched as a programmatic dependent of the partial kernel.
+__global__ void __launch_bounds__(256) k2v4_merge_kernel(K2V4DecodeParams p, float* __restrict__ out) {
+    grid_dependency_wait();
     const int hq = blockIdx.x, b = blockIdx.y;
     const int D = p.c.D;
     const int64_t base = ((int64_t)b * p.Hq + hq) * p.n_chunks;
-    float M = -INFINITY;
-    for (int c = 0; c < p.n_chunks; ++c) M = fmaxf(M, p.ws_ml[(base + c) * 2]);
+    constexpr int kBatch = 8;
     for (int d = threadIdx.x; d < D; d += blockDim.x) {
-        float L = 0.0f, acc = 0.0f;
-        for (int c = 0; c < p.n_chunks; ++c) {
-            const float w = M == -INFINITY ? 0.0f : expf(p.ws_ml[(base + c) * 2] - M);
-            L += w * p.ws_ml[(base + c) * 2 + 1];
-            acc = fmaf(w, p.ws_o[(base + c) * D + d], acc);
+        float M = -INFINITY, L = 0.0f, acc = 0.0f;
+        for (int c0 = 0; c0 < p.n_chunks; c0 += kBatch) {
+            float mv[kBatch], lw[kBatch], ov[kBatch];
+#pragma unroll
+            for (int k = 0; k < kBatch; ++k) {
+                mv[k] = -INFINITY;
+                lw[k] = ov[k] = 0.0f;
+                if (c0 + k < p.n_chunks) {
+                    const float2 ml = *reinterpret_cast<const float2*>(p.ws_ml + (base + c0 + k) * 2);
+                    mv[k] = ml.x;
+                    lw[k] = ml.y;
+                    ov[k] = p.ws_o[(base + c0 + k) * D + d];
+                }
+            }
+            float mb = M;
+#pragma unroll
+            for (int k = 0; k < kBatch; ++k) mb = fmaxf(mb, mv[k]);
+            if (mb == -INFINITY) continue;
+            const float keep = M == -INFINITY ? 0.0f : expf(M - mb);
+            L *= keep;
+            acc *= keep;
+#pragma unroll
+            for (int k = 0; k < kBatch; ++k) {
+                const float w = mv[k] == -INFINITY ? 0.0f : expf(mv[k] - mb);
+                L = fmaf(w, lw[k], L);
+                acc = fmaf(w, ov[k], acc);
+            }
+            M = mb;
         }
         out[((int64_t)b * p.Hq + hq) * D + d] = L > 0.0f ? acc / L : 0.0f;
     }
+}
+
+cudaError_t launch_k2v4_merge(const K2V4DecodeParams& p, float* out, cudaStream_t stream) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)p.Hq, (unsigned)p.batch);
+    cfg.blockDim = dim3(256);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, k2v4_merge_kernel, p, out);
 }
 
 // ---------------------------------------------------------------------------
@@ -335,20 +375,72 @@ struct SmemT {
     static constexpr uint32_t kOffState = kOffRed + 2 * 4 * 8 * 4;    // running max, sum, qmax (8 each), levels (4)
     static constexpr uint32_t kOffBar = kOffState + 3 * 8 * 4 + 16;
     static constexpr uint32_t kOffMisc = kOffBar + 4 * 8;             // abort flag, TMEM base
-    static constexpr uint32_t kBytes = kOffMisc + 16;
+    // raw bytes of a tile, double-buffered: K codes (128 x D/4), the 4 groups'
+    // K scales (4 x D fp16), V blocks (128 x D/32 x 18)
+    static constexpr uint32_t kRawKc = kRowsT * D / 4, kRawKs = 4 * 2 * D, kRawVb = kRowsT * (D / 32) * 18;
+    static constexpr uint32_t kRawBytes = kRawKc + kRawKs + kRawVb;
+    static constexpr uint32_t kOffRaw = (kOffMisc + 16 + 127) / 128 * 128;
+    static constexpr uint32_t kBytes = kOffRaw + 2 * kRawBytes;
 };
 
 constexpr uint32_t kColS = 0, kColO = 32, kTmemColsT = 64;
 constexpr uint32_t kIdescK2Score = idesc_f16(128, kNq, false, false);
 constexpr uint32_t kIdescK2Ctx = idesc_f16(128, kNq, true, false);
 
-__device__ __forceinline__ uint32_t pack_half2(float a, float b) {
-    const __half2 h = __floats2half2_rn(a, b);
-    return *reinterpret_cast<const uint32_t*>(&h);
+// Bulk K values enter the f16 operand scaled by kK2Gamma: the two level
+// magnitudes times it round to f16 within 1.6e-5 relative (2.4e-4 unscaled;
+// gen_codebook.py --k2-level-scale), so a K value is one correctly rounded f16
+// product of (level, scale).  Overlay rows keep their exact fp16 K; the
+// softmax divides the scores of bulk rows by the scale.
+constexpr float kK2Gamma = 1.126953125f;
+
+__device__ __forceinline__ uint32_t hmul2_bits(uint32_t a, uint32_t b) {
+    const __half2 z = __hmul2(*reinterpret_cast<const __half2*>(&a), *reinterpret_cast<const __half2*>(&b));
+    return *reinterpret_cast<const uint32_t*>(&z);
+}
+__device__ __forceinline__ uint32_t hsub2_bits(uint32_t a, uint32_t b) {
+    const __half2 z = __hsub2(*reinterpret_cast<const __half2*>(&a), *reinterpret_cast<const __half2*>(&b));
+    return *reinterpret_cast<const uint32_t*>(&z);
+}
+// Two q4_0 codes (each 0..15 in the low 4 bits of a 16-bit half) -> half2
+// (code - 8) * d, one correctly rounded f16 multiply: 0x6400 | c is 1024 + c
+// in f16 and 0x6408 is 1032, so the subtraction is exact.
+__device__ __forceinline__ uint32_t q4_pair(uint32_t codes2, uint32_t d2) {
+    return hmul2_bits(hsub2_bits(codes2 | 0x64006400u, 0x64086408u), d2);
+}
+
+// Copies the raw bytes of the tile at cells [t0, t0 + nt) into `dst` with
+// 16-byte cp.async (nt a multiple of 32; each piece is contiguous and 16-byte
+// aligned in the cache).  One commit group per call.
+template <int D>
+__device__ __forceinline__ void stage_tile(const K2V4DecodeParams& p, int64_t seq, int64_t t0, int nt,
+                                           unsigned char* dst, int tid) {
+    using SM = SmemT<D>;
+    const int n_kc = nt * (D / 4) / 16, n_ks = (nt / kG) * 2 * D / 16, n_vb = nt * (D / 32) * 18 / 16;
+    const unsigned char* kc = p.k_codes + (seq * p.c.cap + t0) * (D / 4);
+    const unsigned char* ks = reinterpret_cast<const unsigned char*>(p.k_scales + (seq * (p.c.cap / kG) + t0 / kG) * D);
+    const unsigned char* vb = p.v_blocks + (seq * p.c.cap + t0) * (D / 32) * 18;
+    for (int i = tid; i < n_kc + n_ks + n_vb; i += kThreadsT) {
+        const unsigned char* src;
+        unsigned char* d;
+        if (i < n_kc) {
+            src = kc + 16 * i;
+            d = dst + 16 * i;
+        } else if (i < n_kc + n_ks) {
+            src = ks + 16 * (i - n_kc);
+            d = dst + SM::kRawKc + 16 * (i - n_kc);
+        } else {
+            src = vb + 16 * (i - n_kc - n_ks);
+            d = dst + SM::kRawKc + SM::kRawKs + 16 * (i - n_kc - n_ks);
+        }
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(d)), "l"(src) : "memory");
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
 }
 
 template <int D>
 __global__ void __launch_bounds__(kThreadsT, 1) k2v4_tc_kernel(K2V4DecodeParams p) {
+    launch_dependents();
     using SM = SmemT<D>;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char* sK = smem_raw + SM::kOffK;
@@ -364,6 +456,7 @@ __global__ void __launch_bounds__(kThreadsT, 1) k2v4_tc_kernel(K2V4DecodeParams 
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem_raw + SM::kOffBar);   // 0 score, 1 context
     volatile int* sAbort = reinterpret_cast<volatile int*>(smem_raw + SM::kOffMisc);
     uint32_t* sTmem = reinterpret_cast<uint32_t*>(smem_raw + SM::kOffMisc + 4);
+    unsigned char* sRaw = smem_raw + SM::kOffRaw;   // [2][kRawBytes]
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int chunk_id = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
@@ -372,6 +465,7 @@ __global__ void __launch_bounds__(kThreadsT, 1) k2v4_tc_kernel(K2V4DecodeParams 
     const int64_t c1 = min(c0 + p.chunk, p.c.T);
     const int n_tiles = (int)((c1 - c0 + kRowsT - 1) / kRowsT);
     const int grp = p.grp;
+    if (n_tiles > 0) stage_tile<D>(p, seq, c0, (int)min((int64_t)kRowsT, c1 - c0), sRaw, tid);
 
     if (warp == 0) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(sTmem)),
@@ -406,6 +500,15 @@ __global__ void __launch_bounds__(kThreadsT, 1) k2v4_tc_kernel(K2V4DecodeParams 
     if (q_max > 0.0f) frexpf(q_max, &e_q);
     const float q_scale = q_max > 0.0f ? ldexpf(1.0f, 14 - e_q) : 1.0f;
     const float cz = p.sm_scale * kLog2e * (q_max > 0.0f ? ldexpf(1.0f, e_q - 14) : 1.0f);
+    // the 4 scaled K levels as f16, bytes 0..7 of (lv01, lv23) for byte_perm lookups
+    uint32_t lv01, lv23;
+    {
+        const __half2 a = __floats2half2_rn(sLv[0] * kK2Gamma, sLv[1] * kK2Gamma);
+        const __half2 c = __floats2half2_rn(sLv[2] * kK2Gamma, sLv[3] * kK2Gamma);
+        lv01 = *reinterpret_cast<const uint32_t*>(&a);
+        lv23 = *reinterpret_cast<const uint32_t*>(&c);
+    }
+
     for (int i = tid; i < 8 * D; i += kThreadsT) {
         const int h = i / D, d = i - h * D;
         const float x = h < grp ? qg[h * D + d] * q_scale : 0.0f;
@@ -427,6 +530,19 @@ __global__ void __launch_bounds__(kThreadsT, 1) k2v4_tc_kernel(K2V4DecodeParams 
         // the previous tile's context MMAs still read sV and P^T
         if (t > 0) mbar_wait(&bars[1], (uint32_t)(t - 1) & 1u, sAbort);
         tc_after();
+        // the next tile's bytes stream in while this one is processed
+        if (t + 1 < n_tiles) {
+            stage_tile<D>(p, seq, t0 + kRowsT, (int)min((int64_t)kRowsT, c1 - t0 - kRowsT),
+                          sRaw + ((t + 1) & 1) * SM::kRawBytes, tid);
+            asm volatile("cp.async.wait_group 1;" ::: "memory");
+        } else {
+            asm volatile("cp.async.wait_group 0;" ::: "memory");
+        }
+        __syncthreads();
+        const unsigned char* raw = sRaw + (t & 1) * SM::kRawBytes;
+        const unsigned char* raw_kc = raw;
+        const uint16_t* raw_ks = reinterpret_cast<const uint16_t*>(raw + SM::kRawKc);
+        const unsigned char* raw_vb = raw + SM::kRawKc + SM::kRawKs;
         // ---- dequantize the tile to f16 (cells on rows, 64 dims per chunk) ----
         for (int it = tid; it < kRowsT * (D / 32); it += kThreadsT) {
             const int r = it / (D / 32), j = it - r * (D / 32);   // cell, 32-dim slice
@@ -444,40 +560,30 @@ __global__ void __launch_bounds__(kThreadsT, 1) k2v4_tc_kernel(K2V4DecodeParams 
                         kw[4 * i] = a.x; kw[4 * i + 1] = a.y; kw[4 * i + 2] = a.z; kw[4 * i + 3] = a.w;
                         vw[4 * i] = c.x; vw[4 * i + 1] = c.y; vw[4 * i + 2] = c.z; vw[4 * i + 3] = c.w;
                     }
+
                 } else {
-                    // K: 2-bit codes (32 dims = 8 bytes) times the group's per-dim fp16 scales
-                    const uint2 kc = __ldg(reinterpret_cast<const uint2*>(p.k_codes + (seq * p.c.cap + cell) * (D / 4) + 8 * j));
-                    const uint4* ksc = reinterpret_cast<const uint4*>(p.k_scales + (seq * (p.c.cap / kG) + cell / kG) * D + 32 * j);
-                    const uint32_t kcw[2] = {kc.x, kc.y};
+                    // K: 2-bit codes (32 dims = 8 bytes; dims 2m, 2m+1 in bits 4m..4m+3)
+                    // times the group's per-dim fp16 scales, pairwise in f16
+                    const uint2 kc = *reinterpret_cast<const uint2*>(raw_kc + r * (D / 4) + 8 * j);
+                    const uint32_t* scw = reinterpret_cast<const uint32_t*>(raw_ks + (r / kG) * D + 32 * j);
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const uint4 sc = __ldg(ksc + i);
-                        const uint32_t scw[4] = {sc.x, sc.y, sc.z, sc.w};
-#pragma unroll
-                        for (int k = 0; k < 4; ++k) {
-                            const int d0 = 8 * i + 2 * k;   // dims d0, d0 + 1 of the slice
-                            const uint32_t c_a = (kcw[d0 >> 4] >> (2 * (d0 & 15))) & 3u;
-                            const uint32_t c_b = (kcw[(d0 + 1) >> 4] >> (2 * ((d0 + 1) & 15))) & 3u;
-                            const float s_a = __half2float(__ushort_as_half((uint16_t)(scw[k] & 0xffffu)));
-                            const float s_b = __half2float(__ushort_as_half((uint16_t)(scw[k] >> 16)));
-                            kw[4 * i + k] = pack_half2(sLv[c_a] * s_a, sLv[c_b] * s_b);
-                        }
+                    for (int m = 0; m < 16; ++m) {
+                        const uint32_t nib = ((m < 8 ? kc.x : kc.y) >> (4 * (m & 7))) & 15u;
+                        const uint32_t sel = ((nib & 3u) | ((nib & 12u) << 6)) * 0x22u + 0x1010u;
+                        kw[m] = hmul2_bits(__byte_perm(lv01, lv23, sel), scw[m]);
                     }
-                    // V: q4_0 block (d, then 16 bytes: element e in the low nibble of byte e, e + 16 in the high)
-                    const uint16_t* blk =
-                        reinterpret_cast<const uint16_t*>(p.v_blocks + ((seq * p.c.cap + cell) * (D / 32) + j) * 18);
-                    const float dd = __half2float(__ushort_as_half(__ldg(blk)));
-                    uint32_t cb[8];
+                    // V: q4_0 block (d, then 16 bytes: element e in the low nibble of
+                    // byte e, e + 16 in the high nibble)
+                    const uint16_t* blk = reinterpret_cast<const uint16_t*>(raw_vb + (r * (D / 32) + j) * 18);
+                    const uint32_t d2 = (uint32_t)blk[0] * 0x10001u;
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) cb[i] = __ldg(blk + 1 + i);   // code bytes 2i, 2i + 1
-#pragma unroll
-                    for (int e = 0; e < 32; e += 2) {
-                        const int e0 = e & 15;   // byte index of elements e, e + 1 (same nibble half)
-                        const uint32_t b0 = (cb[e0 >> 1] >> (8 * (e0 & 1))) & 0xffu;
-                        const uint32_t b1 = (cb[(e0 + 1) >> 1] >> (8 * ((e0 + 1) & 1))) & 0xffu;
-                        const int q0 = e < 16 ? (int)(b0 & 15u) : (int)(b0 >> 4);
-                        const int q1 = e < 16 ? (int)(b1 & 15u) : (int)(b1 >> 4);
-                        vw[e / 2] = pack_half2((float)(q0 - 8) * dd, (float)(q1 - 8) * dd);
+                    for (int m = 0; m < 4; ++m) {
+                        const uint32_t w = (uint32_t)blk[1 + 2 * m] | ((uint32_t)blk[2 + 2 * m] << 16);
+                        const uint32_t p01 = __byte_perm(w, 0u, 0x4140u), p23 = __byte_perm(w, 0u, 0x4342u);
+                        vw[2 * m] = q4_pair(p01 & 0x000F000Fu, d2);
+                        vw[2 * m + 1] = q4_pair(p23 & 0x000F000Fu, d2);
+                        vw[8 + 2 * m] = q4_pair((p01 >> 4) & 0x000F000Fu, d2);
+                        vw[9 + 2 * m] = q4_pair((p23 >> 4) & 0x000F000Fu, d2);
                     }
                 }
             } else {
@@ -516,10 +622,12 @@ __global__ void __launch_bounds__(kThreadsT, 1) k2v4_tc_kernel(K2V4DecodeParams 
             tmem_ld16(tmem + lane_base + kColS, sv);
             tmem_wait_ld();
             const int r = 32 * warp + lane;
+            // bulk rows carry K scaled by kK2Gamma, overlay rows do not
+            const float rz = overlay_slot(t0 + r, p.c) >= 0 ? cz : cz * (1.0f / kK2Gamma);
             float z[8];
 #pragma unroll
             for (int h = 0; h < 8; ++h)
-                z[h] = (r < nt && h < grp) ? (__uint_as_float(sv[h]) + __uint_as_float(sv[8 + h])) * cz : -INFINITY;
+                z[h] = (r < nt && h < grp) ? (__uint_as_float(sv[h]) + __uint_as_float(sv[8 + h])) * rz : -INFINITY;
 #pragma unroll
             for (int h = 0; h < 8; ++h) {
                 const float m = warp_max(z[h]);
@@ -724,8 +832,7 @@ cudaError_t launch_k2v4_decode(const kvq_k2v4_layout& L, const float* q, int32_t
         }
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
-        k2v4_merge_kernel<<<dim3(n_q_heads, batch), 256, 0, stream>>>(p, out);
-        return cudaGetLastError();
+        return launch_k2v4_merge(p, out, stream);
     }
     switch (L.head_dim) {
 #define KVQ_D_CASE(DD)                                                                                  \
@@ -746,8 +853,7 @@ cudaError_t launch_k2v4_decode(const kvq_k2v4_layout& L, const float* q, int32_t
     }
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    k2v4_merge_kernel<<<dim3(n_q_heads, batch), 256, 0, stream>>>(p, out);
-    return cudaGetLastError();
+    return launch_k2v4_merge(p, out, stream);
 }
 
 }  // namespace kvq

@@ -138,3 +138,15 @@ def test_tq4_tensor_level_scale_keeps_levels_near_f16(oracle):
     assert rel.max() <= 1e-4, rel.max()
     plain = np.abs(lv.astype(np.float16).astype(np.float64) - lv) / np.abs(lv)
     assert plain.max() > 3e-4
+
+
+def test_k2_tensor_level_scale_is_f16_exact_and_tight(oracle):
+    """The tensor-core K2/V4 kernel scales bulk K levels by a constant (an f16
+    value) that keeps both level magnitudes within 2e-5 of their f16 copies."""
+    src = open(os.path.join(ROOT, "quantized_kv_cache_kv8_gb300", "csrc", "k2v4.cu")).read()
+    g = float(re.search(r"constexpr float kK2Gamma = ([0-9.]+)f;", src).group(1))
+    assert float(np.float16(g)) == g
+    lv, _ = oracle.k2_codebook()
+    prod = (np.abs(lv).astype(np.float32) * np.float32(g)).astype(np.float32)
+    rel = np.abs(prod.astype(np.float16).astype(np.float64) - np.abs(lv) * g) / (np.abs(lv) * g)
+    assert rel.max() <= 2e-5, rel.max()
