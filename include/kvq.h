@@ -243,7 +243,7 @@ kvq_status kv_attn_decode_gather(kvq_format fmt, const kvq_mla_layout* layout,
  * request whose kv_attn_workspace_size exceeds 32 MiB returns
  * KVQ_ERR_WORKSPACE and launches nothing (the scratch grows with the number
  * of sequences, not their length: 32 MiB covers 128 heads for batches of up
- * to 51 sequences of any length).  The first call on each device
+ * to 76 sequences (KV8) or 114 (TQ4) of any length on the tensor-core path).  The first call on each device
  * looks up the array's device address (cudaGetSymbolAddress, which may load
  * the library's device code); make that first call before any stream
  * capture.  All calls share the one array, which keeps the last call's

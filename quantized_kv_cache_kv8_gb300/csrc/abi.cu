@@ -90,8 +90,9 @@ static kvq_status resolve_k2v4_path(kvq_path path, const kvq_k2v4_layout* L, boo
     return KVQ_OK;
 }
 
-AttnPlan plan_decode(kvq_path resolved, int32_t batch, int32_t n_heads, int64_t max_total_rows) {
-    return resolved == KVQ_PATH_TENSOR ? plan_decode_tc(batch, n_heads, max_total_rows)
+AttnPlan plan_decode(kvq_format fmt, kvq_path resolved, int32_t batch, int32_t n_heads, int64_t max_total_rows,
+                     int waves = kDecodeWaves) {
+    return resolved == KVQ_PATH_TENSOR ? plan_decode_tc(fmt, batch, n_heads, max_total_rows, waves)
                                        : plan_decode_simt(batch, n_heads, max_total_rows);
 }
 
@@ -173,20 +174,24 @@ kvq_status tq4_rotate(const void* in, kvq_dtype in_dtype, int64_t n_vecs, const 
     return cuda_status(launch_tq4_rotate(in, in_dtype, n_vecs, *layout, inverse, out, (cudaStream_t)stream));
 }
 
-size_t kv_attn_workspace_size(kvq_format fmt, const kvq_mla_layout* layout, int32_t batch, int32_t n_heads,
-                              int64_t max_total_rows, kvq_path path) {
+}  // extern "C"
+
+namespace kvq {
+
+size_t attn_workspace_size_waves(kvq_format fmt, const kvq_mla_layout* layout, int32_t batch, int32_t n_heads,
+                                 int64_t max_total_rows, kvq_path path, int waves) {
     if (check_attn_layout(fmt, layout) != KVQ_OK || check_path(path) != KVQ_OK) return 0;
     if (batch < 0 || n_heads < 0 || max_total_rows < 0) return 0;
     kvq_path rp;
     if (resolve_path(path, layout, n_heads, &rp) != KVQ_OK) return 0;
-    const AttnPlan pl = plan_decode(rp, batch, n_heads, max_total_rows);
+    const AttnPlan pl = plan_decode(fmt, rp, batch, n_heads, max_total_rows, waves);
     return kWsHeader + partial_bytes(pl.max_items, n_heads, layout->v_dim);
 }
 
-kvq_status kv_attn_decode(kvq_format fmt, const kvq_mla_layout* layout, const void* q, kvq_dtype q_dtype,
-                          int32_t batch, int32_t n_heads, const uint8_t* codes, const float* scales,
-                          const int64_t* cu_seqlens, int64_t max_total_rows, float sm_scale, float* out,
-                          void* workspace, size_t workspace_bytes, kvq_path path, void* stream) {
+kvq_status attn_decode_waves(kvq_format fmt, const kvq_mla_layout* layout, const void* q, kvq_dtype q_dtype,
+                             int32_t batch, int32_t n_heads, const uint8_t* codes, const float* scales,
+                             const int64_t* cu_seqlens, int64_t max_total_rows, float sm_scale, float* out,
+                             void* workspace, size_t workspace_bytes, kvq_path path, void* stream, int waves) {
     kvq_status s = check_attn_layout(fmt, layout);
     if (s != KVQ_OK) return s;
     if ((s = check_path(path)) != KVQ_OK) return s;
@@ -200,15 +205,32 @@ kvq_status kv_attn_decode(kvq_format fmt, const kvq_mla_layout* layout, const vo
     if (max_total_rows > 0 && (!codes || !scales)) return KVQ_ERR_ARG;
     if (!attn_pointers_aligned(q, codes, scales, cu_seqlens, out)) return KVQ_ERR_ARG;
     if (!isfinite(sm_scale)) return KVQ_ERR_ARG;
-    const size_t need = kv_attn_workspace_size(fmt, layout, batch, n_heads, max_total_rows, path);
+    const size_t need = attn_workspace_size_waves(fmt, layout, batch, n_heads, max_total_rows, path, waves);
     if (!workspace || workspace_bytes < need) return KVQ_ERR_WORKSPACE;
     cudaStream_t st = (cudaStream_t)stream;
-    const AttnPlan pl = plan_decode(rp, batch, n_heads, max_total_rows);
+    const AttnPlan pl = plan_decode(fmt, rp, batch, n_heads, max_total_rows, waves);
     if (rp == KVQ_PATH_TENSOR)
         return cuda_status(launch_attn_tc(fmt, *layout, q, q_dtype, batch, n_heads, codes, scales, cu_seqlens, -1, pl,
                                           sm_scale, out, workspace, st));
     return cuda_status(launch_attn_simt(fmt, *layout, q, q_dtype, batch, n_heads, codes, scales, cu_seqlens, -1, pl,
                                         sm_scale, out, workspace, st));
+}
+
+}  // namespace kvq
+
+extern "C" {
+
+size_t kv_attn_workspace_size(kvq_format fmt, const kvq_mla_layout* layout, int32_t batch, int32_t n_heads,
+                              int64_t max_total_rows, kvq_path path) {
+    return attn_workspace_size_waves(fmt, layout, batch, n_heads, max_total_rows, path, kDecodeWaves);
+}
+
+kvq_status kv_attn_decode(kvq_format fmt, const kvq_mla_layout* layout, const void* q, kvq_dtype q_dtype,
+                          int32_t batch, int32_t n_heads, const uint8_t* codes, const float* scales,
+                          const int64_t* cu_seqlens, int64_t max_total_rows, float sm_scale, float* out,
+                          void* workspace, size_t workspace_bytes, kvq_path path, void* stream) {
+    return attn_decode_waves(fmt, layout, q, q_dtype, batch, n_heads, codes, scales, cu_seqlens, max_total_rows,
+                             sm_scale, out, workspace, workspace_bytes, path, stream, kDecodeWaves);
 }
 
 kvq_status kv_attn_decode_append(kvq_format fmt, const kvq_mla_layout* layout, const float* x_new,
@@ -234,7 +256,7 @@ kvq_status kv_attn_decode_append(kvq_format fmt, const kvq_mla_layout* layout, c
     if (!workspace || workspace_bytes < need) return KVQ_ERR_WORKSPACE;
     cudaStream_t st = (cudaStream_t)stream;
     if (rp == KVQ_PATH_TENSOR && fmt == KVQ_KV8 && q_dtype == KVQ_BF16) {
-        const AttnPlan pl = plan_decode(rp, batch, n_heads, max_total_rows);
+        const AttnPlan pl = plan_decode(fmt, rp, batch, n_heads, max_total_rows);
         return cuda_status(launch_attn_tc_kv8_append(*layout, x_new, dst_rows, q, batch, n_heads, codes, scales,
                                                      cu_seqlens, pl, sm_scale, out, workspace, st));
     }
@@ -262,7 +284,7 @@ size_t kv_attn_gather_workspace_size(kvq_format fmt, const kvq_mla_layout* layou
     if (batch < 0 || n_heads < 0 || max_total_selected < 0 || (q_dtype != KVQ_F32 && q_dtype != KVQ_BF16)) return 0;
     kvq_path rp;
     if (resolve_gather_path(fmt, q_dtype, path, layout, n_heads, &rp) != KVQ_OK) return 0;
-    const AttnPlan pl = plan_decode(rp, batch, n_heads, max_total_selected);
+    const AttnPlan pl = plan_decode(fmt, rp, batch, n_heads, max_total_selected);
     return kWsHeader + partial_bytes(pl.max_items, n_heads, layout->v_dim);
 }
 
@@ -288,7 +310,7 @@ kvq_status kv_attn_decode_gather(kvq_format fmt, const kvq_mla_layout* layout, c
     const size_t need = kv_attn_gather_workspace_size(fmt, layout, q_dtype, batch, n_heads, max_total_selected, path);
     if (!workspace || workspace_bytes < need) return KVQ_ERR_WORKSPACE;
     cudaStream_t st = (cudaStream_t)stream;
-    const AttnPlan pl = plan_decode(rp, batch, n_heads, max_total_selected);
+    const AttnPlan pl = plan_decode(fmt, rp, batch, n_heads, max_total_selected);
     if (rp == KVQ_PATH_TENSOR)
         return cuda_status(launch_attn_tc(fmt, *layout, q, q_dtype, batch, n_heads, codes, scales, cu_sel, -1, pl,
                                           sm_scale, out, workspace, st, sel_rows, pool_rows));

@@ -290,16 +290,19 @@ __global__ void __launch_bounds__(128) attn_merge_kernel(AttnParams p, float* __
     const int h = blockIdx.x, b = blockIdx.y;
     const int tid = threadIdx.x, lane = tid & 31;
     const bool prefill = p.prefill_past >= 0;
+    // a chunk the partial kernel chose on the device is read after the wait
+    const bool dev_chunk = !prefill && p.wave_items > 0;
+    if (dev_chunk) grid_dependency_wait();
     if (tid < 32) {
         int64_t first = b, count = 1;
-        if (!prefill) seq_items(p.cu, b, p.chunk, lane, &first, &count, p.err);
+        if (!prefill) seq_items(p.cu, b, dev_chunk ? *p.ws_chunk : p.chunk, lane, &first, &count, p.err);
         if (lane == 0) {
             info[0] = first;
             info[1] = count;
         }
     }
     __syncthreads();
-    grid_dependency_wait();   // the partial state is complete and visible past this point
+    if (!dev_chunk) grid_dependency_wait();   // the partial state is complete and visible past this point
     const int64_t first = info[0];
     int64_t count = info[1];
     if (first + count > p.max_items) {
@@ -407,9 +410,13 @@ AttnParams make_attn_params(kvq_format fmt, const kvq_mla_layout& L, const void*
     p.prefill_past = prefill_past;
     p.chunk = plan.chunk;
     p.max_items = plan.max_items;
+    p.wave_items = plan.wave_items;
+    p.max_waves = plan.max_waves;
+    p.max_rows = plan.max_rows;
     p.sm_scale = sm_scale;
     char* ws = static_cast<char*>(workspace);
     p.err = reinterpret_cast<int32_t*>(ws);
+    p.ws_chunk = reinterpret_cast<int64_t*>(ws + 8);
     p.ws_o = reinterpret_cast<float*>(ws + kWsHeader);
     p.ws_ml = p.ws_o + (size_t)plan.max_items * n_heads * kMlaDV;
     if (fmt == KVQ_TQ4) {

@@ -150,6 +150,7 @@ constexpr int kRing = 5;      // stages; chunk k + 4 is copied while chunk k is 
 template <int FMT, bool QBF16, bool LOQ>
 __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnParams p) {
     launch_dependents();
+    const int64_t w = blockIdx.x;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char* sm = smem_raw;
     unsigned char* sQ = sm + kOffQ;
@@ -166,8 +167,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnParams p) {
     float* sRed = reinterpret_cast<float*>(sm + kOffMisc + 48);       // 16 floats
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int64_t item = blockIdx.x;
-    const int hbase = blockIdx.y * kHC;
+    // item-major linear grid: the CTAs of the first items (the ones with work)
+    // are dispatched first; item and head group are re-derived where the
+    // epilogue needs them, so that they hold no register over the tile loop
+    const int64_t item = w / (p.n_heads / kHC);
+    const int group = (int)(w % (p.n_heads / kHC));
+    const int hbase = group * kHC;
 
     if (warp == 0) {
         int64_t r0 = 0, r1 = 0;
@@ -184,7 +189,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnParams p) {
     }
     __syncthreads();
     const int b = (int)sInfo[0];
-    if (b < 0) return;   // past the last work item: nothing allocated yet
+    if (b < 0) return;   // past the last work item
     const int64_t row0 = sInfo[1], row1 = sInfo[2];
     const int n_tiles = (int)((row1 - row0 + kRows - 1) / kRows);
 
@@ -645,6 +650,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnParams p) {
     if (aborted) {
         if (tid == 0) set_err(p.err, KVQ_ERR_DEVICE);
     } else {
+        const int64_t unit = blockIdx.x;
+        const int64_t item = unit / (p.n_heads / kHC);
+        const int hbase = (int)(unit % (p.n_heads / kHC)) * kHC;
 #pragma unroll
         for (int bi = 0; bi < 2; ++bi) {
             const int db = 2 * hq + bi;
@@ -680,7 +688,7 @@ cudaError_t launch_tc(const AttnParams& p, int64_t grid_x, int groups, cudaStrea
     cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<FMT, QBF16, kLoq>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)kSmemAlloc);
     if (e != cudaSuccess) return e;
-    attn_tc_kernel<FMT, QBF16, kLoq><<<dim3((unsigned)grid_x, (unsigned)groups), kThreads, kSmemAlloc, stream>>>(p);
+    attn_tc_kernel<FMT, QBF16, kLoq><<<dim3((unsigned)(grid_x * groups)), kThreads, kSmemAlloc, stream>>>(p);
     return cudaGetLastError();
 }
 
@@ -691,15 +699,41 @@ bool tc_supported(const kvq_mla_layout& L, int32_t n_heads) {
     return n_heads > 0 && n_heads % kHC == 0;
 }
 
-AttnPlan plan_decode_tc(int32_t batch, int32_t n_heads, int64_t max_total_rows) {
+AttnPlan plan_decode_tc(kvq_format fmt, int32_t batch, int32_t n_heads, int64_t max_total_rows, int waves) {
     AttnPlan pl{};
-    pl.heads_per_cta = kHC;
-    const int64_t groups = std::max<int64_t>(1, n_heads / kHC);
+    pl.heads_per_cta = fmt == KVQ_TQ4 ? kHC / 2 : kHC;
+    const int64_t groups = std::max<int64_t>(1, n_heads / pl.heads_per_cta);
     const int64_t target_items = std::max<int64_t>(1, 152 / groups);
     int64_t chunk = (std::max<int64_t>(max_total_rows, 1) + target_items - 1) / target_items;
     chunk = std::max<int64_t>(kRows, (chunk + kRows - 1) / kRows * kRows);
-    pl.chunk = chunk;
-    pl.max_items = (max_total_rows + chunk - 1) / chunk + batch;
+    pl.chunk = chunk;   // used as is for more than kBalanceSeqs sequences
+    pl.max_rows = max_total_rows;
+    // A chunk fixed here is enough when it guarantees one wave whatever the
+    // split of the rows into `batch` sequences (at most R / C + batch items)
+    // at little more than the ideal R / S rows per item: the CTAs then skip
+    // the device-side search (8 x 4096 KV8 rows: 512 either way).
+    if (target_items > batch) {
+        int64_t c1 = (std::max<int64_t>(max_total_rows, 1) + (target_items - batch) - 1) / (target_items - batch);
+        c1 = std::max<int64_t>(kRows, (c1 + kRows - 1) / kRows * kRows);
+        if (c1 <= chunk + chunk / 4) {
+            pl.chunk = c1;
+            pl.wave_items = 0;
+            pl.max_waves = 1;
+            pl.max_items = (max_total_rows + c1 - 1) / c1 + batch;
+            return pl;
+        }
+    }
+    pl.wave_items = target_items;
+    pl.max_waves = std::max(1, waves);
+    if (batch <= kBalanceSeqs) {
+        // the balanced chunk yields at most max_waves * target * ceil(n / target)
+        // items, and at most one per tile plus one per sequence
+        const int64_t per_wave = target_items * std::max<int64_t>(1, (batch + target_items - 1) / target_items);
+        pl.max_items = std::min<int64_t>(pl.max_waves * per_wave,
+                                         (max_total_rows + kBalanceGranule - 1) / kBalanceGranule + batch);
+    } else {
+        pl.max_items = (max_total_rows + chunk - 1) / chunk + batch;
+    }
     return pl;
 }
 
@@ -720,8 +754,7 @@ cudaError_t launch_attn_tc(kvq_format fmt, const kvq_mla_layout& L, const void* 
         e = qdt == KVQ_BF16 ? launch_attn_tc_kv8_bf16(p, plan.max_items, groups, stream)
                             : launch_tc<KVQ_KV8, false>(p, plan.max_items, groups, stream);
     else
-        e = qdt == KVQ_BF16 ? launch_tc<KVQ_TQ4, true>(p, plan.max_items, groups, stream)
-                            : launch_tc<KVQ_TQ4, false>(p, plan.max_items, groups, stream);
+        e = launch_attn_tc_tq4(p, qdt == KVQ_BF16, plan.max_items, n_heads, stream);
     if (e != cudaSuccess) return e;
     return launch_attn_merge(fmt, p, out, stream);
 }

@@ -166,6 +166,7 @@ __device__ __forceinline__ float warp_columns(float (&v)[32], int lane) {
 template <bool APPEND, bool GATHER>
 __global__ void __launch_bounds__(kThreads, 1) attn_tc_kv8_kernel(AttnParams p) {
     launch_dependents();
+    const int64_t w = blockIdx.x;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char* sm = smem_raw;
     unsigned char* sQ = sm + kOffQ;
@@ -184,8 +185,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kv8_kernel(AttnParams p) 
     int64_t* sRowIdx = reinterpret_cast<int64_t*>(sm + kOffRowIdx);   // gather: [2][kRows]
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int64_t item = blockIdx.x;
-    const int hbase = blockIdx.y * kHC;
+    // item-major linear grid: the CTAs of the first items (the ones with work)
+    // are dispatched first; item and head group are re-derived where the
+    // epilogue needs them, so that they hold no register over the tile loop
+    const int64_t item = w / (p.n_heads / kHC);
+    const int group = (int)(w % (p.n_heads / kHC));
+    const int hbase = group * kHC;
 
     if (warp == 0) {
         int64_t r0 = 0, r1 = 0;
@@ -237,12 +242,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kv8_kernel(AttnParams p) 
             if (lane == 0) {
                 *sNewRow = rn;
                 const int64_t s0 = p.cu[b], s1 = p.cu[b + 1];
-                if ((d < s0 || d >= s1) && row0 == s0 && blockIdx.y == 0) set_err(p.err, KVQ_ERR_ARG);
+                if ((d < s0 || d >= s1) && row0 == s0 && group == 0) set_err(p.err, KVQ_ERR_ARG);
             }
             if (rn >= 0) {
                 kv8_encode_row_warp(p.x_new + (int64_t)b * kMlaD, p.n_blocks, p.bd0, p.bd1, sNew, sNewScale, lane);
                 __syncwarp();
-                if (blockIdx.y == 0) {
+                if (group == 0) {
                     for (int i = lane; i < kMlaD / 16; i += 32)
                         reinterpret_cast<uint4*>(p.codes_out + rn * kMlaD)[i] = reinterpret_cast<const uint4*>(sNew)[i];
                     if (lane < p.n_blocks) p.scales_out[rn * p.n_blocks + lane] = sNewScale[lane];
@@ -547,6 +552,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kv8_kernel(AttnParams p) 
     if (aborted) {
         if (tid == 0) set_err(p.err, KVQ_ERR_DEVICE);
     } else {
+        const int64_t unit = blockIdx.x;
+        const int64_t item = unit / (p.n_heads / kHC);
+        const int hbase = (int)(unit % (p.n_heads / kHC)) * kHC;
 #pragma unroll
         for (int bi = 0; bi < 2; ++bi) {
             const int db = 2 * hq + bi;
@@ -583,7 +591,7 @@ cudaError_t launch_kv8(const AttnParams& p, int64_t grid_x, int groups, cudaStre
     cudaError_t e = cudaFuncSetAttribute(attn_tc_kv8_kernel<APPEND, GATHER>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemUsed);
     if (e != cudaSuccess) return e;
-    attn_tc_kv8_kernel<APPEND, GATHER><<<dim3((unsigned)grid_x, (unsigned)groups), kThreads, kSmemUsed, stream>>>(p);
+    attn_tc_kv8_kernel<APPEND, GATHER><<<dim3((unsigned)(grid_x * groups)), kThreads, kSmemUsed, stream>>>(p);
     return cudaGetLastError();
 }
 }  // namespace

@@ -1,0 +1,508 @@
+// attn_tc_tq4.cu -- tensor-core attention over TQ4 rows with every chunk of a
+// tile decoded once.
+//
+// The structure of the KV8 kernel (attn_tc_kv8.cu): one chunk of rows per CTA,
+// 128-row tiles whose 9 f16 chunks stay resident for both products, decode in
+// three groups overlapping the previous tile's context MMAs, a single MMA
+// issuer, a lagged running max.  What differs for TQ4 ([P1] "Ready for review"
+// comment, finding 2: rotate the query once per head, dot it with the
+// codebook levels, unrotate the context once):
+//   - the rotated query is not exact in f16, so each query chunk holds the f16
+//     value and the f16 residual of every head; to leave room for the retained
+//     chunks a CTA serves 32 heads: the score runs with N = 64 (32 values + 32
+//     residuals), the context with N = 32;
+//   - codes are nibbles: a 256-entry table maps a code byte to the f16 pair of
+//     its two levels, the levels scaled by kTq4Gamma (within 9.3e-5 of f16;
+//     divided out of scores and context);
+//   - P is stored K-major (heads on rows) so that N = 32 needs no padding.
+// The context accumulates in the rotated domain; the merge unrotates it.
+#include "tc_common.cuh"
+
+#include <math.h>
+
+namespace kvq {
+namespace {
+using namespace tc;
+
+constexpr int kRows = 128;      // rows per tile
+constexpr int kHC = 32;         // heads per CTA
+constexpr int kWorkers = 256;
+constexpr int kThreads = kWorkers + 32;
+constexpr int kChunks = 9;      // 64-dim chunks: 8 latent + 1 rope
+constexpr int kRope = 8;
+constexpr int kRowBytes = kMlaD / 2;                // 288 code bytes per row
+constexpr uint32_t kSlotBytes = kRows * 128;       // 128 rows x 64 f16
+constexpr uint32_t kQChunkBytes = 2 * kHC * 128;   // 32 heads (f16) + 32 residual rows
+constexpr uint32_t kPChunkBytes = kHC * 128;       // P: 32 head rows x 64 cells
+constexpr uint32_t kOffQ = 0;
+constexpr uint32_t kOffSlot = kOffQ + kChunks * kQChunkBytes;
+constexpr uint32_t kOffLut = kOffSlot + kChunks * kSlotBytes;
+constexpr uint32_t kOffM = kOffLut + 256 * 4;
+constexpr uint32_t kOffAlpha = kOffM + kHC * 4;
+constexpr uint32_t kOffRed = kOffAlpha + kHC * 4;   // 4 quadrants x 32 heads
+constexpr uint32_t kOffBar = kOffRed + 4 * kHC * 4;
+constexpr uint32_t kOffMisc = kOffBar + 16 * 8;
+constexpr uint32_t kSmemUsed = kOffMisc + 32;
+static_assert(kOffSlot % 1024 == 0, "swizzled operands need 1024-byte alignment");
+static_assert(kSmemUsed <= 232448, "shared memory budget");
+
+// TMEM: O^T 4 blocks x 32 columns, S_L^T and S_R^T 64 columns each (values, residuals)
+constexpr uint32_t kColO = 0, kColSL = 128, kColSR = 192, kTmemCols = 256;
+
+enum { kBarFull0 = 0, kBarFree0 = 3, kBarScore = 7, kBarP = 8, kBarDone = 9, kNumBars = 10 };
+
+constexpr float kLagLog2 = 14.0f;
+constexpr float kTq4Gamma = 1.3338516f;             // see the general kernel (attn_tc.cu)
+constexpr float kTq4InvGamma = 1.0f / 1.3338516f;
+constexpr uint32_t kIdescScore = idesc_f16(128, 2 * kHC, false, false);
+constexpr uint32_t kIdescCtx = idesc_f16(128, kHC, true, false);
+
+// A worker's raw share of a tile.  Groups A and B (code bytes 128 g .. + 127):
+// 4 pieces, piece i at row 4 (warp + 8 i) + lane / 8, bytes 16 (lane % 8) of
+// the group -- chunk 4 g + (lane % 8) / 2, dims 32 (lane % 2) of it.  Group C
+// (the rope chunk, bytes 256..287): 1 piece at row 16 warp + lane / 2, bytes
+// 16 (lane % 2).
+struct RawGroup {
+    uint4 v[4];
+};
+
+__device__ __forceinline__ void load_group(RawGroup& r, const uint8_t* __restrict__ codes, int64_t t0, int nt, int g,
+                                           int warp, int lane) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int row = 4 * (warp + 8 * i) + (lane >> 3);
+        r.v[i] = row < nt ? __ldg(reinterpret_cast<const uint4*>(codes + (t0 + row) * kRowBytes + 128 * g + 16 * (lane & 7)))
+                          : make_uint4(0u, 0u, 0u, 0u);
+    }
+}
+__device__ __forceinline__ uint4 load_rope(const uint8_t* __restrict__ codes, int64_t t0, int nt, int warp, int lane) {
+    const int row = 16 * warp + (lane >> 1);
+    return row < nt ? __ldg(reinterpret_cast<const uint4*>(codes + (t0 + row) * kRowBytes + 256 + 16 * (lane & 1)))
+                    : make_uint4(0u, 0u, 0u, 0u);
+}
+
+// 16 code bytes (32 codes) -> 32 f16 levels at byte offset `b` (64 bytes) of
+// swizzled row `row`.
+__device__ __forceinline__ void store32(unsigned char* slot, const uint4& c, int row, int b, const uint32_t* lut) {
+    const uint32_t in[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t w0 = lut[in[i] & 0xffu], w1 = lut[(in[i] >> 8) & 0xffu];
+        const uint32_t w2 = lut[(in[i] >> 16) & 0xffu], w3 = lut[in[i] >> 24];
+        *reinterpret_cast<uint4*>(slot + sw128(row, b + 16 * i)) = make_uint4(w0, w1, w2, w3);
+    }
+}
+
+// In-warp transpose-reduce of 16 columns over 32 lanes: lane j's result is
+// column j % 16 reduced over all lanes.  31 shuffles.
+template <bool MAX>
+__device__ __forceinline__ float warp_columns16(float (&v)[16], int lane) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        const float got = __shfl_xor_sync(kFull, v[i], 16);
+        v[i] = MAX ? fmaxf(v[i], got) : v[i] + got;
+    }
+#pragma unroll
+    for (int s = 8; s >= 1; s >>= 1) {
+        const bool upper = (lane & s) != 0;
+#pragma unroll
+        for (int i = 0; i < s; ++i) {
+            const float send = upper ? v[i] : v[i + s];
+            const float keep = upper ? v[i + s] : v[i];
+            const float got = __shfl_xor_sync(kFull, send, s);
+            v[i] = MAX ? fmaxf(keep, got) : keep + got;
+        }
+    }
+    return v[0];
+}
+
+template <bool QBF16>
+__global__ void __launch_bounds__(kThreads, 1) attn_tc_tq4_kernel(AttnParams p) {
+    launch_dependents();
+    const int64_t w = blockIdx.x;
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    unsigned char* sm = smem_raw;
+    unsigned char* sQ = sm + kOffQ;
+    unsigned char* sSlot = sm + kOffSlot;
+    unsigned char* sP = sSlot + kRope * kSlotBytes;
+    uint32_t* sLut = reinterpret_cast<uint32_t*>(sm + kOffLut);
+    float* sM = reinterpret_cast<float*>(sm + kOffM);
+    float* sAlpha = reinterpret_cast<float*>(sm + kOffAlpha);
+    float* sRed = reinterpret_cast<float*>(sm + kOffRed);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kOffBar);
+    volatile int* sAbort = reinterpret_cast<volatile int*>(sm + kOffMisc);
+    uint32_t* sTmem = reinterpret_cast<uint32_t*>(sm + kOffMisc + 4);
+    int64_t* sInfo = reinterpret_cast<int64_t*>(sm + kOffMisc + 8);
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    // item-major linear grid: the CTAs of the first items (the ones with work)
+    // are dispatched first; item and head group are re-derived where the
+    // epilogue needs them, so that they hold no register over the tile loop
+    const int64_t item = w / (p.n_heads / kHC);
+    const int group = (int)(w % (p.n_heads / kHC));
+    const int hbase = group * kHC;
+
+    if (warp == 0) {
+        int64_t r0 = 0, r1 = 0;
+        int b = locate_item(p, item, lane, &r0, &r1);
+        if (smem_u32(smem_raw) & 1023u) {
+            if (lane == 0) set_err(p.err, KVQ_ERR_DEVICE);
+            b = -1;
+        }
+        if (lane == 0) {
+            sInfo[0] = b;
+            sInfo[1] = r0;
+            sInfo[2] = r1;
+        }
+    }
+    __syncthreads();
+    const int b = (int)sInfo[0];
+    if (b < 0) return;
+    const int64_t row0 = sInfo[1], row1 = sInfo[2];
+    const int n_tiles = (int)((row1 - row0 + kRows - 1) / kRows);
+
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(sTmem)),
+                     "r"(kTmemCols));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
+    if (tid == 64) {
+        for (int i = 0; i < kNumBars; ++i) {
+            const uint32_t count = (i < kBarFree0 || i == kBarP) ? (uint32_t)kWorkers : 1u;
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(&bars[i])), "r"(count));
+        }
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        *sAbort = 0;
+    }
+    if (tid < kHC) sM[tid] = -INFINITY;
+    if (tid < 256) {
+        const int lo = tid & 15, hi = tid >> 4;
+        const __half2 h2 = __halves2half2(__float2half_rn(__fmul_rn(p.lv[lo], kTq4Gamma)),
+                                          __float2half_rn(__fmul_rn(p.lv[hi], kTq4Gamma)));
+        sLut[tid] = *reinterpret_cast<const uint32_t*>(&h2);
+    }
+    if (tid == 0) {
+        const int64_t n = min((int64_t)kRows, row1 - row0);
+        prefetch_l2(p.codes + row0 * kRowBytes, (uint32_t)(n * kRowBytes));
+    }
+
+    // ---- query: 32 heads, 4 per worker warp, rotated once (sign flip, FWHT of
+    // the 512 and 64 blocks, 1/sqrt(n)), then stored as an f16 pair scaled by a
+    // power of two that keeps every element below 2^14 ----
+    const int64_t qbase = ((int64_t)b * p.n_heads + hbase) * kMlaD;
+    float qv[4][18];
+    float smax = 0.0f;
+    if (tid < kWorkers) {
+        float qmax = 0.0f;
+#pragma unroll
+        for (int hh = 0; hh < 4; ++hh) {
+            const int64_t base = qbase + (int64_t)(4 * warp + hh) * kMlaD;
+#pragma unroll
+            for (int k = 0; k < 18; ++k) {
+                const int64_t idx = base + lane + 32 * k;
+                qv[hh][k] = QBF16 ? __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(p.q)[idx])
+                                  : reinterpret_cast<const float*>(p.q)[idx];
+                qmax = fmaxf(qmax, fabsf(qv[hh][k]));
+            }
+        }
+        for (int64_t r = row0 + tid; r < row1; r += kWorkers) smax = fmaxf(smax, p.scales[r * p.n_blocks]);
+        qmax = warp_max(qmax);
+        smax = warp_max(smax);
+        if (lane == 0) {
+            sRed[warp] = qmax;
+            sRed[8 + warp] = smax;
+        }
+    }
+    __syncthreads();
+    float q_max = 0.0f, s_max = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        q_max = fmaxf(q_max, sRed[i]);
+        s_max = fmaxf(s_max, sRed[8 + i]);
+    }
+    // |q'_i| <= ||q|| <= 24 max|q| for the rotated query
+    const float q_bound = 24.0f * q_max;
+    int e_s = 0, e_q = 0;
+    if (s_max > 0.0f) frexpf(s_max, &e_s);
+    if (q_bound > 0.0f) frexpf(q_bound, &e_q);
+    const float s_ref = s_max > 0.0f ? ldexpf(1.0f, e_s) : 1.0f;
+    const float inv_s_ref = s_max > 0.0f ? ldexpf(1.0f, -e_s) : 1.0f;
+    const float q_scale = q_bound > 0.0f ? ldexpf(1.0f, 14 - e_q) : 1.0f;
+    const float cz = p.sm_scale * kLog2e * (q_bound > 0.0f ? ldexpf(1.0f, e_q - 14) : 1.0f) * kTq4InvGamma;
+    if (tid < kWorkers) {
+#pragma unroll
+        for (int hh = 0; hh < 4; ++hh) {
+            float (&v)[18] = qv[hh];
+#pragma unroll
+            for (int k = 0; k < 16; ++k)
+                if (sign_neg(p.signs, 0, lane + 32 * k)) v[k] = -v[k];
+            warp_fwht<512>(v, lane);
+#pragma unroll
+            for (int k = 0; k < 16; ++k) v[k] = __fmul_rn(v[k], p.kn[0]);
+#pragma unroll
+            for (int k = 16; k < 18; ++k)
+                if (sign_neg(p.signs, 1, lane + 32 * (k - 16))) v[k] = -v[k];
+            warp_fwht<64>(v + 16, lane);
+#pragma unroll
+            for (int k = 16; k < 18; ++k) v[k] = __fmul_rn(v[k], p.kn[1]);
+            const int h = 4 * warp + hh;
+#pragma unroll
+            for (int k = 0; k < 18; ++k) {
+                const int d = lane + 32 * k;
+                const float x = v[k] * q_scale;
+                const __half hi = __float2half_rn(x);
+                const __half lo = __float2half_rn(x - __half2float(hi));
+                unsigned char* chunk = sQ + (d >> 6) * kQChunkBytes;
+                *reinterpret_cast<__half*>(chunk + sw128(h, (d & 63) * 2)) = hi;
+                *reinterpret_cast<__half*>(chunk + sw128(kHC + h, (d & 63) * 2)) = lo;
+            }
+        }
+    }
+    fence_async_smem();
+    tc_before();
+    __syncthreads();
+    tc_after();
+    const uint32_t tmem = *sTmem;
+
+    if (warp == kWorkers / 32) {
+        // ================= MMA warp: lane 0 issues =================
+        if (lane == 0) {
+            const uint64_t dq0 = umma_desc(smem_u32(sQ), 16, 1024);
+            const uint64_t dslot0 = umma_desc(smem_u32(sSlot), 16, 1024);
+            const uint64_t dpair0 = umma_desc(smem_u32(sSlot), kSlotBytes, 1024);
+            const uint64_t dp = umma_desc(smem_u32(sP), 16, 1024);
+            constexpr uint64_t kQStep = kQChunkBytes >> 4, kSlotStep = kSlotBytes >> 4, kPStep = kPChunkBytes >> 4;
+            bool ok = true;
+            for (int t = 0; t < n_tiles && ok; ++t) {
+                const uint32_t par = (uint32_t)t & 1u;
+#pragma unroll 1
+                for (int kc = 0; kc < kChunks && ok; ++kc) {
+                    if ((kc & 3) == 0) {
+                        ok = mbar_wait(&bars[kBarFull0 + (kc >> 2)], par, sAbort);
+                        tc_after();
+                    }
+                    const uint32_t d = tmem + (kc < kRope ? kColSL : kColSR);
+                    const uint64_t a = dslot0 + kc * kSlotStep, bq = dq0 + kc * kQStep;
+                    const bool first = kc == 0 || kc == kRope;
+#pragma unroll
+                    for (int ks = 0; ks < 4; ++ks)
+                        umma_f16(d, a + 2 * ks, bq + 2 * ks, kIdescScore, (first && ks == 0) ? 0u : 1u);
+                }
+                umma_commit(&bars[kBarScore]);
+                ok = ok && mbar_wait(&bars[kBarP], par, sAbort);
+                tc_after();
+#pragma unroll 1
+                for (int db = 0; db < 4 && ok; ++db) {
+                    const uint32_t d = tmem + kColO + kHC * db;
+                    const uint64_t a = dpair0 + 2 * db * kSlotStep;
+#pragma unroll
+                    for (int ks = 0; ks < 8; ++ks)
+                        umma_f16(d, a + 128 * ks, dp + (ks >> 2) * kPStep + 2 * (ks & 3), kIdescCtx,
+                                 (t > 0 || ks > 0) ? 1u : 0u);
+                    umma_commit(&bars[kBarFree0 + db]);
+                }
+            }
+            umma_commit(&bars[kBarDone]);
+        }
+        return;
+    }
+
+    // ================= workers =================
+    const int srow = 32 * (warp & 3) + lane;            // softmax: TMEM lane / row
+    const int hq = warp >> 2;                            // softmax: heads 16 hq .. 16 hq + 15
+    const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
+    float lcol = 0.0f;   // row sum of head 16 hq + lane % 16 over this quadrant (lanes 0-15)
+
+    float sl_next = 0.0f, sr_next = 0.0f;
+    auto load_scales = [&](int64_t t0n, int ntn) {
+        sl_next = sr_next = 0.0f;
+        if (srow < ntn) {
+            const int64_t r = t0n + srow;
+            sl_next = p.scales[r * p.n_blocks];
+            sr_next = p.scales[r * p.n_blocks + (p.n_blocks - 1)];
+        }
+    };
+    RawGroup rawA, rawB;
+    uint4 rawC;
+    {
+        const int nt0 = (int)min((int64_t)kRows, row1 - row0);
+        load_group(rawA, p.codes, row0, nt0, 0, warp, lane);
+        load_group(rawB, p.codes, row0, nt0, 1, warp, lane);
+        rawC = load_rope(p.codes, row0, nt0, warp, lane);
+        load_scales(row0, nt0);
+    }
+    int t = 0;
+    for (; t < n_tiles; ++t) {
+        const int64_t t0 = row0 + (int64_t)t * kRows;
+        const int nt = (int)min((int64_t)kRows, row1 - t0);
+        if (tid == 0 && t0 + kRows < row1) {
+            const int64_t n = min((int64_t)kRows, row1 - (t0 + kRows));
+            prefetch_l2(p.codes + (t0 + kRows) * kRowBytes, (uint32_t)(n * kRowBytes));
+        }
+        const float my_sl = sl_next, my_sr = sr_next;
+        // ---- decode the tile: groups A (chunks 0-3), B (4-7), C (rope) ----
+        const uint32_t prev = (uint32_t)(t - 1) & 1u;
+        {
+            const int half = lane & 1, cg = (lane & 7) >> 1;
+#pragma unroll
+            for (int g = 0; g < 2; ++g) {
+                if (t > 0) {
+                    mbar_wait(&bars[kBarFree0 + 2 * g], prev, sAbort);
+                    mbar_wait(&bars[kBarFree0 + 2 * g + 1], prev, sAbort);
+                }
+                unsigned char* slot = sSlot + (4 * g + cg) * kSlotBytes;
+                const RawGroup& rg = g == 0 ? rawA : rawB;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) store32(slot, rg.v[i], 4 * (warp + 8 * i) + (lane >> 3), 64 * half, sLut);
+                fence_async_smem();
+                mbar_arrive(&bars[kBarFull0 + g]);
+            }
+            store32(sSlot + kRope * kSlotBytes, rawC, 16 * warp + (lane >> 1), 64 * half, sLut);
+            fence_async_smem();
+            mbar_arrive(&bars[kBarFull0 + 2]);
+        }
+        const int64_t t1 = t0 + kRows;
+        const int nt1 = (int)min((int64_t)kRows, row1 - t1);
+        if (t + 1 < n_tiles) load_group(rawA, p.codes, t1, nt1, 0, warp, lane);
+
+        // ---- softmax of the tile: thread = row srow, 16 heads ----
+        mbar_wait(&bars[kBarScore], (uint32_t)t & 1u, sAbort);
+        tc_after();
+        float z[16];
+        const float za = my_sl * cz, zb = my_sr * cz;
+        const bool row_ok = srow < nt;
+        auto load_z = [&]() {
+            uint32_t a[16], c[16];
+            tmem_ld16(tmem + lane_base + kColSR + 16 * hq, a);            // rope, values
+            tmem_ld16(tmem + lane_base + kColSR + kHC + 16 * hq, c);      // rope, residuals
+            tmem_wait_ld();
+#pragma unroll
+            for (int j = 0; j < 16; ++j) z[j] = (__uint_as_float(a[j]) + __uint_as_float(c[j])) * zb;
+            tmem_ld16(tmem + lane_base + kColSL + 16 * hq, a);
+            tmem_ld16(tmem + lane_base + kColSL + kHC + 16 * hq, c);
+            tmem_wait_ld();
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+                z[j] = row_ok ? fmaf(__uint_as_float(a[j]) + __uint_as_float(c[j]), za, z[j]) : -INFINITY;
+        };
+        load_z();
+        if (t + 1 < n_tiles) {
+            load_group(rawB, p.codes, t1, nt1, 1, warp, lane);
+            rawC = load_rope(p.codes, t1, nt1, warp, lane);
+            load_scales(t1, nt1);
+        }
+        bool flag = *sAbort != 0;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) flag |= z[j] > sM[16 * hq + j] + kLagLog2;
+        if (worker_any(flag)) {
+            if (worker_any(*sAbort != 0)) break;
+            const float cm = warp_columns16<true>(z, lane);
+            if (lane < 16) sRed[(warp & 3) * kHC + 16 * hq + lane] = cm;
+            worker_sync();
+            if (tid < kHC) {
+                const float c4 = fmaxf(fmaxf(sRed[tid], sRed[kHC + tid]), fmaxf(sRed[2 * kHC + tid], sRed[3 * kHC + tid]));
+                const float mo = sM[tid], mn = fmaxf(mo, c4);
+                sAlpha[tid] = mo == -INFINITY ? 0.0f : ex2(mo - mn);
+                sM[tid] = mn;
+            }
+            worker_sync();
+            if (t > 0) {
+                // O^T (lanes = dims, columns = heads) is stable: the score commit
+                // of this tile follows every context MMA of the previous one
+                const uint32_t ta = tmem + lane_base + kColO + kHC * (2 * hq);
+#pragma unroll 1
+                for (int bi = 0; bi < 2; ++bi) {
+                    uint32_t o[32];
+                    tmem_ld32(ta + kHC * bi, o);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * sAlpha[j]);
+                    tmem_st32(ta + kHC * bi, o);
+                }
+                tmem_wait_st();
+            }
+            if (lane < 16) lcol *= sAlpha[16 * hq + lane];
+            load_z();
+        }
+        {
+            const float wrow = my_sl * inv_s_ref;
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                z[j] = ex2(z[j] - sM[16 * hq + j]);
+                const int h = 16 * hq + j;
+                *reinterpret_cast<__half*>(sP + (srow >> 6) * kPChunkBytes + sw128(h, (srow & 63) * 2)) =
+                    __float2half_rn(z[j] * wrow);
+            }
+        }
+        fence_async_smem();
+        tc_before();
+        mbar_arrive(&bars[kBarP]);
+        {
+            const float l = warp_columns16<false>(z, lane);
+            if (lane < 16) lcol += l;
+        }
+    }
+
+    // ---- epilogue: wait for every MMA, row sums, O^T -> partial state ----
+    {
+        volatile int never = 0;
+        if (!mbar_wait(&bars[kBarDone], 0u, &never)) *sAbort = 1;
+    }
+    tc_after();
+    const bool aborted = worker_any(*sAbort != 0 || t < n_tiles);
+    {
+        worker_sync();
+        if (lane < 16) sRed[(warp & 3) * kHC + 16 * hq + lane] = lcol;
+        worker_sync();
+        if (tid < kHC) sAlpha[tid] = (sRed[tid] + sRed[kHC + tid]) + (sRed[2 * kHC + tid] + sRed[3 * kHC + tid]);
+        worker_sync();
+    }
+    if (aborted) {
+        if (tid == 0) set_err(p.err, KVQ_ERR_DEVICE);
+    } else {
+        const int64_t unit = blockIdx.x;
+        const int64_t item = unit / (p.n_heads / kHC);
+        const int hbase = (int)(unit % (p.n_heads / kHC)) * kHC;
+        const float o_scale = s_ref * kTq4InvGamma;
+#pragma unroll
+        for (int bi = 0; bi < 2; ++bi) {
+            const int db = 2 * hq + bi;
+            const int dim = 128 * db + 32 * (warp & 3) + lane;
+            uint32_t v[32];
+            tmem_ld32(tmem + lane_base + kColO + kHC * db, v);
+            tmem_wait_ld();
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                const int h = hbase + j;
+                p.ws_o[(item * p.n_heads + h) * kMlaDV + dim] = n_tiles > 0 ? __uint_as_float(v[j]) * o_scale : 0.0f;
+            }
+        }
+        if (tid < kHC) {
+            float* ml = p.ws_ml + (item * p.n_heads + hbase + tid) * 2;
+            ml[0] = sM[tid] * kLn2;
+            ml[1] = sAlpha[tid];
+        }
+    }
+    tc_before();
+    worker_sync();
+    tc_after();
+    if (warp == 1) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols));
+}
+
+template <bool QBF16>
+cudaError_t launch_tq4(const AttnParams& p, int64_t grid_x, int groups, cudaStream_t stream) {
+    cudaError_t e = cudaFuncSetAttribute(attn_tc_tq4_kernel<QBF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)kSmemUsed);
+    if (e != cudaSuccess) return e;
+    attn_tc_tq4_kernel<QBF16><<<dim3((unsigned)(grid_x * groups)), kThreads, kSmemUsed, stream>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_attn_tc_tq4(const AttnParams& p, bool q_bf16, int64_t grid_x, int n_heads, cudaStream_t stream) {
+    return q_bf16 ? launch_tq4<true>(p, grid_x, n_heads / kHC, stream)
+                  : launch_tq4<false>(p, grid_x, n_heads / kHC, stream);
+}
+
+}  // namespace kvq

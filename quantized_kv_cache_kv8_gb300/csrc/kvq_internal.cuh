@@ -165,10 +165,13 @@ struct AttnPlan {
     int64_t chunk;        // rows per work item
     int64_t max_items;    // grid bound
     int32_t heads_per_cta;
+    int64_t wave_items;   // > 0: the chunk is balanced on the device (items per wave of CTAs)
+    int32_t max_waves;    // waves of items the workspace holds
+    int64_t max_rows;     // host bound on the total rows
 };
 AttnPlan plan_decode_simt(int32_t batch, int32_t n_heads, int64_t max_total_rows);
 size_t partial_bytes(int64_t max_items, int32_t n_heads, int32_t v_dim);
-constexpr size_t kWsHeader = 256;   // error word + padding
+constexpr size_t kWsHeader = 256;   // error word, device-chosen chunk, padding
 
 cudaError_t launch_attn_simt(kvq_format fmt, const kvq_mla_layout& L, const void* q, kvq_dtype qdt, int32_t n_seq,
                              int32_t n_heads, const uint8_t* codes, const float* scales, const int64_t* cu_seqlens,
@@ -176,9 +179,20 @@ cudaError_t launch_attn_simt(kvq_format fmt, const kvq_mla_layout& L, const void
                              void* workspace, cudaStream_t stream, const int64_t* sel = nullptr,
                              int64_t pool_rows = 0);
 
-// Tensor-core attention (tcgen05, 64 heads per CTA).
+// Tensor-core attention (tcgen05; 64 heads per CTA for KV8, 32 for TQ4).
 bool tc_supported(const kvq_mla_layout& L, int32_t n_heads);
-AttnPlan plan_decode_tc(int32_t batch, int32_t n_heads, int64_t max_total_rows);
+// Waves of work items a decode workspace is sized for (the device picks
+// 1 .. waves from the actual lengths).
+constexpr int kDecodeWaves = 4;
+AttnPlan plan_decode_tc(kvq_format fmt, int32_t batch, int32_t n_heads, int64_t max_total_rows, int waves);
+// kv_attn_workspace_size / kv_attn_decode with a given wave budget (the
+// no-allocation entry takes fewer waves to fit its fixed scratch).
+size_t attn_workspace_size_waves(kvq_format fmt, const kvq_mla_layout* layout, int32_t batch, int32_t n_heads,
+                                 int64_t max_total_rows, kvq_path path, int waves);
+kvq_status attn_decode_waves(kvq_format fmt, const kvq_mla_layout* layout, const void* q, kvq_dtype q_dtype,
+                             int32_t batch, int32_t n_heads, const uint8_t* codes, const float* scales,
+                             const int64_t* cu_seqlens, int64_t max_total_rows, float sm_scale, float* out,
+                             void* workspace, size_t workspace_bytes, kvq_path path, void* stream, int waves);
 // KV8 decode with bf16 queries on the tensor cores, the step's new rows
 // encoded in the same launch (row x_new[b] -> pool row dst_rows[b]).
 cudaError_t launch_attn_tc_kv8_append(const kvq_mla_layout& L, const float* x_new, const int64_t* dst_rows,

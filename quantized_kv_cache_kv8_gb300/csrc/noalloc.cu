@@ -18,9 +18,11 @@
 
 #include <mutex>
 
-// 32 MiB.  The decode plan cuts a batch into about 76 + batch work items and
-// each item keeps heads x 514 floats, so at 128 heads this covers batches of
-// up to 51 sequences whatever their lengths.
+// 32 MiB.  The tensor-core decode balances a batch over whole waves of CTAs,
+// each wave 76 * ceil(batch / 76) work items for KV8 (38 * ceil(batch / 38)
+// for TQ4), each item keeping heads x 514 floats; this entry takes as many
+// waves (up to the regular entry's 4) as fit, so at 128 heads it covers
+// batches of up to 76 sequences (KV8) or 114 (TQ4) whatever their lengths.
 static constexpr size_t kNoAllocScratchBytes = size_t(32) << 20;
 
 static __device__ __align__(256) unsigned char g_decode_scratch[kNoAllocScratchBytes];
@@ -54,7 +56,11 @@ extern "C" kvq_status kv_attn_decode_noalloc(kvq_format fmt, const kvq_mla_layou
                                              float sm_scale, float* out, kvq_path path, void* stream) {
     if (batch < 0 || n_heads < 0 || max_total_rows < 0) return KVQ_ERR_ARG;
     if (batch == 0 || n_heads == 0) return KVQ_OK;
-    const size_t need = kv_attn_workspace_size(fmt, layout, batch, n_heads, max_total_rows, path);
+    // the largest wave budget whose workspace fits the scratch
+    int waves = kvq::kDecodeWaves;
+    size_t need = kvq::attn_workspace_size_waves(fmt, layout, batch, n_heads, max_total_rows, path, waves);
+    while (need > kNoAllocScratchBytes && waves > 1)
+        need = kvq::attn_workspace_size_waves(fmt, layout, batch, n_heads, max_total_rows, path, --waves);
     if (need == 0) {
         // invalid or unsupported arguments: let the regular entry point name the
         // reason without touching any memory (its checks run before the workspace check)
@@ -65,6 +71,6 @@ extern "C" kvq_status kv_attn_decode_noalloc(kvq_format fmt, const kvq_mla_layou
     void* scratch = nullptr;
     const kvq_status s = scratch_on_current_device(&scratch);
     if (s != KVQ_OK) return s;
-    return kv_attn_decode(fmt, layout, q, q_dtype, batch, n_heads, codes, scales, cu_seqlens, max_total_rows,
-                          sm_scale, out, scratch, kNoAllocScratchBytes, path, stream);
+    return kvq::attn_decode_waves(fmt, layout, q, q_dtype, batch, n_heads, codes, scales, cu_seqlens, max_total_rows,
+                                  sm_scale, out, scratch, kNoAllocScratchBytes, path, stream, waves);
 }

@@ -82,9 +82,24 @@ def test_argument_validation(kvq):
 
 
 def test_workspace_sizes_grow_with_work(kvq):
+    item = 128 * 514 * 4                      # one work item's partial state, 128 heads
     a = kvq.kv_attn_workspace_size(1, 8, 128, 32768)
     b = kvq.kv_attn_workspace_size(1, 32, 128, 2_100_000)
-    assert 0 < a < b
+    assert 0 < a
+    # tensor-core split: a host chunk when it guarantees one wave (76 items of
+    # 64 heads per wave for KV8) near the ideal size: 8 x 4096 rows -> 512-row
+    # chunks, 64 + 8 items; otherwise the device balances items over at most
+    # 4 waves (38 items of 32 heads per wave for TQ4; whole waves per 76 / 38
+    # sequences), never more than one per 128-row tile plus one per sequence
+    assert a == 256 + (64 + 8) * item
+    assert b == 256 + 4 * 76 * item
+    assert kvq.kv_attn_workspace_size(2, 8, 128, 32768) == 256 + 4 * 38 * item
+    assert kvq.kv_attn_workspace_size(1, 8, 128, 1000) == 256 + (8 + 8) * item
+    assert kvq.kv_attn_workspace_size(1, 100, 128, 10**6) == 256 + 4 * 152 * item
+    # the SIMT split grows with the rows
+    s1 = kvq.kv_attn_workspace_size(1, 8, 128, 32768, path=kvq.PATH_SIMT)
+    s2 = kvq.kv_attn_workspace_size(1, 32, 128, 2_100_000, path=kvq.PATH_SIMT)
+    assert 0 < s1 < s2
     p = kvq.kv_attn_prefill_workspace_size(2, 128, 126976, 2048)
     assert p >= 2048 * 128 * 514 * 4
     k = kvq.kv_attn_decode_k2v4_workspace_size(kvq.k2v4_layout(), 4, 16, 32768)

@@ -101,6 +101,34 @@ def test_tensor_ragged_with_edges(kvq, oracle, fmt, bf16):
     assert kvq.read_device_error(ws) == 0
 
 
+@pytest.mark.parametrize("fmt", [1, 2])
+def test_tensor_many_sequences(kvq, oracle, fmt):
+    """More sequences than the device-side chunk balancing handles (1024): the
+    tensor path falls back to the host's chunk; lengths 0..300."""
+    rng = np.random.default_rng(23)
+    lens = [int(v) for v in rng.integers(0, 301, size=1100)]
+    x, cu, qv, got, ws = run_decode(kvq, fmt, lens, 64, True, 23, kvq.PATH_TENSOR)
+    pairs = [(b, h) for b in (0, 1, 517, 1023, 1024, 1099) for h in (0, 31, 32, 63)]
+    pairs += [(b, 5) for b in range(0, 1100, 97)]
+    check_decode(oracle, fmt, x, cu, qv, got, pairs=pairs, seed=23, tol=TENSOR_TOL)
+    for b, T in enumerate(lens):
+        if T == 0:
+            assert np.all(got[b] == 0.0)
+    assert kvq.read_device_error(ws) == 0
+
+
+@pytest.mark.parametrize("fmt", [1, 2])
+def test_tensor_balanced_chunks_skewed(kvq, oracle, fmt):
+    """One long sequence among short ones: the device-chosen chunk splits the
+    long one across many CTAs (several items per sequence, one wave)."""
+    lens = [20000, 5, 300, 0, 129, 1]
+    x, cu, qv, got, ws = run_decode(kvq, fmt, lens, 128, True, 29, kvq.PATH_TENSOR)
+    pairs = [(b, h) for b in range(len(lens)) for h in (0, 33, 64, 127)]
+    check_decode(oracle, fmt, x, cu, qv, got, pairs=pairs, seed=29, tol=TENSOR_TOL)
+    assert np.all(got[3] == 0.0)
+    assert kvq.read_device_error(ws) == 0
+
+
 def test_tensor_matches_simt_closely(kvq):
     """The two kernel families on the same inputs agree to the tensor path's tolerance."""
     lens = [777, 2048, 5]
@@ -113,11 +141,13 @@ def test_tensor_matches_simt_closely(kvq):
             assert rel_err(outs[1][b, h], outs[0][b, h]) <= TENSOR_TOL
 
 
-def test_device_error_when_rows_exceed_bound(kvq):
+@pytest.mark.parametrize("H,path", [(16, "simt"), (64, "tensor")])
+def test_device_error_when_rows_exceed_bound(kvq, H, path):
     """A ragged batch larger than the bound the call was sized for sets the
     device error word instead of reading or writing out of bounds."""
     lens = [600, 600]
-    x, cu, qv, got, ws = run_decode(kvq, 1, lens, 16, False, 5, kvq.PATH_SIMT, max_rows=100)
+    pth = kvq.PATH_SIMT if path == "simt" else kvq.PATH_TENSOR
+    x, cu, qv, got, ws = run_decode(kvq, 1, lens, H, False, 5, pth, max_rows=100)
     assert kvq.read_device_error(ws) == 6
     assert kvq.read_device_error(ws) == 0             # cleared by the first read
 

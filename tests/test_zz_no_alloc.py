@@ -50,9 +50,10 @@ def test_noalloc_matches_regular_entry_on_two_calls():
 
 def test_noalloc_refuses_requests_beyond_its_scratch():
     kvq = kvq_module()
-    q = torch.zeros((64, 128, 576), dtype=torch.bfloat16, device="cuda")
-    out = torch.zeros((64, 128, 512), device="cuda")
-    cu = torch.zeros(65, dtype=torch.int64, device="cuda")
+    # 100 sequences take two waves of 76 work items: 152 x 128 x 514 floats > 32 MiB
+    q = torch.zeros((100, 128, 576), dtype=torch.bfloat16, device="cuda")
+    out = torch.zeros((100, 128, 512), device="cuda")
+    cu = torch.zeros(101, dtype=torch.int64, device="cuda")
     codes = torch.zeros((16, 576), dtype=torch.uint8, device="cuda")
     scales = torch.zeros((16, 2), device="cuda")
     with pytest.raises(kvq.KvqError) as e:
