@@ -11,9 +11,9 @@
 //     value and the f16 residual of every head; to leave room for the retained
 //     chunks a CTA serves 32 heads: the score runs with N = 64 (32 values + 32
 //     residuals), the context with N = 32;
-//   - codes are nibbles: a 256-entry table maps a code byte to the f16 pair of
-//     its two levels, the levels scaled by kTq4Gamma (within 9.3e-5 of f16;
-//     divided out of scores and context);
+//   - codes are nibbles: byte permutes over the 16 f16 levels (levels4) turn
+//     them into f16 operands, the levels scaled by kTq4Gamma (within 9.3e-5
+//     of f16; divided out of scores and context);
 //   - P is stored K-major (heads on rows) so that N = 32 needs no padding.
 // The context accumulates in the rotated domain; the merge unrotates it.
 #include "tc_common.cuh"
@@ -36,8 +36,8 @@ constexpr uint32_t kQChunkBytes = 2 * kHC * 128;   // 32 heads (f16) + 32 residu
 constexpr uint32_t kPChunkBytes = kHC * 128;       // P: 32 head rows x 64 cells
 constexpr uint32_t kOffQ = 0;
 constexpr uint32_t kOffSlot = kOffQ + kChunks * kQChunkBytes;
-constexpr uint32_t kOffLut = kOffSlot + kChunks * kSlotBytes;
-constexpr uint32_t kOffM = kOffLut + 256 * 4;
+constexpr uint32_t kOffLevels = kOffSlot + kChunks * kSlotBytes;   // LevelBytes: 32 bytes
+constexpr uint32_t kOffM = kOffLevels + 32;
 constexpr uint32_t kOffAlpha = kOffM + kHC * 4;
 constexpr uint32_t kOffRed = kOffAlpha + kHC * 4;   // 4 quadrants x 32 heads
 constexpr uint32_t kOffBar = kOffRed + 4 * kHC * 4;
@@ -81,14 +81,36 @@ __device__ __forceinline__ uint4 load_rope(const uint8_t* __restrict__ codes, in
                     : make_uint4(0u, 0u, 0u, 0u);
 }
 
+// The 16 f16 levels (x kTq4Gamma) as byte planes, four levels per word:
+// lo[k] holds the low bytes of levels 4k .. 4k+3, hi[k] their high bytes.
+struct LevelBytes {
+    uint32_t lo[4], hi[4];
+};
+
+// The 4 codes in the low 16 bits of s (one per nibble, dims in order) -> their
+// f16 levels as two f16x2 words, by byte permutes: the low 3 bits of each
+// code pick a byte from levels 0-7 and from levels 8-15, bit 3 picks between
+// the two, then the low and high byte planes are interleaved.  No shared
+// memory access (a 256-entry table in shared memory took ~4k bank-conflicted
+// wavefronts per tile on the port the MMAs read their operands through).
+__device__ __forceinline__ void levels4(const LevelBytes& t, uint32_t s, uint32_t& w0, uint32_t& w1) {
+    const uint32_t sel = s & 0x7777u;
+    const uint32_t pick = ((s >> 1) & 0x4444u) | 0x3210u;
+    const uint32_t l = __byte_perm(__byte_perm(t.lo[0], t.lo[1], sel), __byte_perm(t.lo[2], t.lo[3], sel), pick);
+    const uint32_t h = __byte_perm(__byte_perm(t.hi[0], t.hi[1], sel), __byte_perm(t.hi[2], t.hi[3], sel), pick);
+    w0 = __byte_perm(l, h, 0x5140u);
+    w1 = __byte_perm(l, h, 0x7362u);
+}
+
 // 16 code bytes (32 codes) -> 32 f16 levels at byte offset `b` (64 bytes) of
 // swizzled row `row`.
-__device__ __forceinline__ void store32(unsigned char* slot, const uint4& c, int row, int b, const uint32_t* lut) {
+__device__ __forceinline__ void store32(unsigned char* slot, const uint4& c, int row, int b, const LevelBytes& t) {
     const uint32_t in[4] = {c.x, c.y, c.z, c.w};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-        const uint32_t w0 = lut[in[i] & 0xffu], w1 = lut[(in[i] >> 8) & 0xffu];
-        const uint32_t w2 = lut[(in[i] >> 16) & 0xffu], w3 = lut[in[i] >> 24];
+        uint32_t w0, w1, w2, w3;
+        levels4(t, in[i], w0, w1);
+        levels4(t, in[i] >> 16, w2, w3);
         *reinterpret_cast<uint4*>(slot + sw128(row, b + 16 * i)) = make_uint4(w0, w1, w2, w3);
     }
 }
@@ -125,7 +147,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_tq4_kernel(AttnParams p) 
     unsigned char* sQ = sm + kOffQ;
     unsigned char* sSlot = sm + kOffSlot;
     unsigned char* sP = sSlot + kRope * kSlotBytes;
-    uint32_t* sLut = reinterpret_cast<uint32_t*>(sm + kOffLut);
+    unsigned char* sLevels = sm + kOffLevels;
     float* sM = reinterpret_cast<float*>(sm + kOffM);
     float* sAlpha = reinterpret_cast<float*>(sm + kOffAlpha);
     float* sRed = reinterpret_cast<float*>(sm + kOffRed);
@@ -175,11 +197,20 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_tq4_kernel(AttnParams p) 
         *sAbort = 0;
     }
     if (tid < kHC) sM[tid] = -INFINITY;
-    if (tid < 256) {
-        const int lo = tid & 15, hi = tid >> 4;
-        const __half2 h2 = __halves2half2(__float2half_rn(__fmul_rn(p.lv[lo], kTq4Gamma)),
-                                          __float2half_rn(__fmul_rn(p.lv[hi], kTq4Gamma)));
-        sLut[tid] = *reinterpret_cast<const uint32_t*>(&h2);
+    if (tid == 0) {
+        // one thread, constant level indices: written by 16 threads with a
+        // per-thread index into the parameter block, these planes read back
+        // wrong on the device (found by comparing them with planes built in
+        // registers), while this form matches
+        uint32_t lo[4] = {0u, 0u, 0u, 0u}, hi[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+            const uint32_t h = __half_as_ushort(__float2half_rn(__fmul_rn(p.lv[k], kTq4Gamma)));
+            lo[k >> 2] |= (h & 0xffu) << (8 * (k & 3));
+            hi[k >> 2] |= (h >> 8) << (8 * (k & 3));
+        }
+        *reinterpret_cast<uint4*>(sLevels) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        *reinterpret_cast<uint4*>(sLevels + 16) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
     }
     if (tid == 0) {
         const int64_t n = min((int64_t)kRows, row1 - row0);
@@ -343,6 +374,17 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_tq4_kernel(AttnParams p) 
         // ---- decode the tile: groups A (chunks 0-3), B (4-7), C (rope) ----
         const uint32_t prev = (uint32_t)(t - 1) & 1u;
         {
+            // the level byte planes, re-read per tile (asm volatile: not kept
+            // in registers across the softmax)
+            LevelBytes lvb;
+            asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                         : "=r"(lvb.lo[0]), "=r"(lvb.lo[1]), "=r"(lvb.lo[2]), "=r"(lvb.lo[3])
+                         : "r"(smem_u32(sLevels))
+                         : "memory");
+            asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                         : "=r"(lvb.hi[0]), "=r"(lvb.hi[1]), "=r"(lvb.hi[2]), "=r"(lvb.hi[3])
+                         : "r"(smem_u32(sLevels + 16))
+                         : "memory");
             const int half = lane & 1, cg = (lane & 7) >> 1;
 #pragma unroll
             for (int g = 0; g < 2; ++g) {
@@ -353,11 +395,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_tq4_kernel(AttnParams p) 
                 unsigned char* slot = sSlot + (4 * g + cg) * kSlotBytes;
                 const RawGroup& rg = g == 0 ? rawA : rawB;
 #pragma unroll
-                for (int i = 0; i < 4; ++i) store32(slot, rg.v[i], 4 * (warp + 8 * i) + (lane >> 3), 64 * half, sLut);
+                for (int i = 0; i < 4; ++i) store32(slot, rg.v[i], 4 * (warp + 8 * i) + (lane >> 3), 64 * half, lvb);
                 fence_async_smem();
                 mbar_arrive(&bars[kBarFull0 + g]);
             }
-            store32(sSlot + kRope * kSlotBytes, rawC, 16 * warp + (lane >> 1), 64 * half, sLut);
+            store32(sSlot + kRope * kSlotBytes, rawC, 16 * warp + (lane >> 1), 64 * half, lvb);
             fence_async_smem();
             mbar_arrive(&bars[kBarFull0 + 2]);
         }
