@@ -40,6 +40,10 @@
  *                              orthogonality identities of [P1]/[P2])
  *   K2/V4 codec + overlay ... pinned (byte counts and overlay footprint from
  *                              [P3], q4_0 nibble order fixture, gain property)
+ *   K2/V4 append ............ pinned (whole groups = the encoder, constant-
+ *                              magnitude closed forms of the partial-group
+ *                              rule, one call = two calls split at a group
+ *                              boundary)
  */
 #include <math.h>
 #include <stdint.h>
@@ -626,6 +630,28 @@ int64_t kvqo_k2v4_slot(int64_t cell, int64_t T, const kvqo_k2v4_layout* L)
     return -1;
 }
 
+/* One q4_0 block of 32 values -> 18 bytes (fp16 d, then 16 bytes of nibbles). */
+static void v4_encode_block(const float* xb, uint8_t* out)
+{
+    float m = 0.0f;
+    for (int j = 0; j < 32; ++j)
+        if (fabsf(xb[j]) > fabsf(m)) m = xb[j];
+    float d = m / -8.0f;
+    unsigned dh = kvqo_f16_encode(d);
+    out[0] = (uint8_t)(dh & 255u);
+    out[1] = (uint8_t)(dh >> 8);
+    for (int j = 0; j < 16; ++j) out[2 + j] = 0;
+    for (int j = 0; j < 32; ++j) {
+        unsigned code = 8;
+        if (d != 0.0f) {
+            int c = (int)(xb[j] / d + 8.5f);
+            code = (unsigned)(c > 15 ? 15 : c);
+        }
+        if (j < 16) out[2 + j] = (uint8_t)(out[2 + j] | code);
+        else        out[2 + j - 16] = (uint8_t)(out[2 + j - 16] | (code << 4));
+    }
+}
+
 int kvqo_k2v4_encode(const float* k, const float* v, int64_t T, int64_t cap, const kvqo_k2v4_layout* L,
                      uint8_t* k_codes, uint16_t* k_scales, uint8_t* v_blocks, uint16_t* k_win, uint16_t* v_win)
 {
@@ -657,31 +683,101 @@ int kvqo_k2v4_encode(const float* k, const float* v, int64_t T, int64_t cap, con
         }
         for (int64_t cell = 0; cell < T; ++cell) {
             const float* vr = vh + cell * D;
-            for (int blk = 0; blk < D / 32; ++blk) {
-                const float* xb = vr + blk * 32;
-                uint8_t* out = v_blocks + (((int64_t)h * cap + cell) * (D / 32) + blk) * 18;
-                float m = 0.0f;
-                for (int j = 0; j < 32; ++j)
-                    if (fabsf(xb[j]) > fabsf(m)) m = xb[j];
-                float d = m / -8.0f;
-                unsigned dh = kvqo_f16_encode(d);
-                out[0] = (uint8_t)(dh & 255u);
-                out[1] = (uint8_t)(dh >> 8);
-                for (int j = 0; j < 16; ++j) out[2 + j] = 0;
-                for (int j = 0; j < 32; ++j) {
-                    unsigned code = 8;
-                    if (d != 0.0f) {
-                        int c = (int)(xb[j] / d + 8.5f);
-                        code = (unsigned)(c > 15 ? 15 : c);
-                    }
-                    if (j < 16) out[2 + j] = (uint8_t)(out[2 + j] | code);
-                    else        out[2 + j - 16] = (uint8_t)(out[2 + j - 16] | (code << 4));
-                }
-            }
+            for (int blk = 0; blk < D / 32; ++blk)
+                v4_encode_block(vr + blk * 32, v_blocks + (((int64_t)h * cap + cell) * (D / 32) + blk) * 18);
             int64_t slot = kvqo_k2v4_slot(cell, T, L);
             if (slot >= 0) {
                 for (int d = 0; d < D; ++d) {
                     k_win[((int64_t)h * slots + slot) * D + d] = (uint16_t)kvqo_f16_encode(kh[cell * D + d]);
+                    v_win[((int64_t)h * slots + slot) * D + d] = (uint16_t)kvqo_f16_encode(vr[d]);
+                }
+            }
+        }
+    }
+    return KVQO_OK;
+}
+
+/* Append of n_new cells at positions T_old .. T_old + n_new - 1 of one
+ * sequence (k_new, v_new are [Hkv][n_new][D]); the engine's append patterns of
+ * [P3] ("Attention error under the engine's append patterns": decode appends,
+ * speculative-verify windows, prefill chunks that fall mid-group) and its
+ * "Review fixes" item "Fresh partial-group scale".  The K scale of a group:
+ *   - first written by this append (fresh) with all 32 cells present: the
+ *     encoder's rule, sqrt(ss / 32);
+ *   - fresh with n < 32 cells present: sqrt((ss + (32 - n) * prev^2) / 32):
+ *     ss the sum of squares of the n cells (the encoder's fixed order, absent
+ *     cells as zero), prev the previous group's rule scale recovered from its
+ *     stored fp16 value as f16(stored) / k_gain, the same whether that group
+ *     was stored by an earlier call or in this one (reading: the pages have
+ *     prev recomputed in the same launch or read from storage, bit-exact
+ *     either way, and standing in for the previous group's mean square, i.e.
+ *     in the rule's un-gained units); f32 evaluation left to right:
+ *     prev * prev, times (32 - n), plus ss, over 32, square root;
+ *   - fresh with n < 32 cells and no previous group (group 0): sqrt(ss / n),
+ *     the RMS of the cells present (reading: the /n rule the pages state
+ *     before the shrink toward prev);
+ *   - a group that already holds cells from an earlier call: its stored scale
+ *     is kept, the new cells are coded against f16(stored) / k_gain (reading:
+ *     the pages define the rule for a group first written by a partial batch).
+ * V blocks and the fp16 overlay of each new cell as in the encoder, with the
+ * window taken at T = T_old + n_new. */
+int kvqo_k2v4_append(const float* k_new, const float* v_new, int64_t T_old, int64_t n_new, int64_t cap,
+                     const kvqo_k2v4_layout* L, uint8_t* k_codes, uint16_t* k_scales, uint8_t* v_blocks,
+                     uint16_t* k_win, uint16_t* v_win)
+{
+    const int H = L->n_kv_heads, D = L->head_dim, G = L->group;
+    if (G != 32 || D % 32 != 0 || cap % G != 0) return KVQO_ERR_SHAPE;
+    if (T_old < 0 || n_new < 0 || T_old + n_new > cap) return KVQO_ERR_ARG;
+    const int64_t T_new = T_old + n_new;
+    float lv[4], th[3];
+    kvqo_k2_codebook(lv, th);
+    const int slots = L->n_sink + L->n_window + L->n_slack;
+    for (int h = 0; h < H; ++h) {
+        const float* kh = k_new + (int64_t)h * n_new * D;
+        const float* vh = v_new + (int64_t)h * n_new * D;
+        for (int64_t g = T_old / G; n_new > 0 && g <= (T_new - 1) / G; ++g) {
+            const int64_t g0 = g * G;
+            const int fresh = g0 >= T_old;
+            const int64_t c0 = g0 > T_old ? g0 : T_old;                /* first new cell of the group */
+            const int64_t c1 = g0 + G < T_new ? g0 + G : T_new;        /* one past the last */
+            for (int d = 0; d < D; ++d) {
+                uint16_t* sc = k_scales + ((int64_t)h * (cap / G) + g) * D + d;
+                float s_rule;
+                if (fresh) {
+                    const int n = (int)(c1 - c0);
+                    const float ss = sumsq_r32(kh + (c0 - T_old) * D + d, n, D);
+                    if (n == G) {
+                        s_rule = sqrtf(ss / 32.0f);
+                    } else if (g == 0) {
+                        s_rule = sqrtf(ss / (float)n);
+                    } else {
+                        const float prev = (float)kvqo_f16_value(sc[-D]) / L->k_gain;
+                        const float prev2 = prev * prev;
+                        const float add = (float)(G - n) * prev2;
+                        const float num = ss + add;
+                        s_rule = sqrtf(num / 32.0f);
+                    }
+                    *sc = (uint16_t)kvqo_f16_encode(L->k_gain * s_rule);
+                } else {
+                    s_rule = (float)kvqo_f16_value(*sc) / L->k_gain;
+                }
+                for (int64_t cell = c0; cell < c1; ++cell) {
+                    unsigned code = 0;
+                    if (s_rule != 0.0f) code = code_of(kh[(cell - T_old) * D + d] / s_rule, th, 3);
+                    uint8_t* byte = k_codes + ((int64_t)h * cap + cell) * (D / 4) + d / 4;
+                    if (d % 4 == 0) *byte = 0;
+                    *byte = (uint8_t)(*byte | (code << (2 * (d % 4))));
+                }
+            }
+        }
+        for (int64_t cell = T_old; cell < T_new; ++cell) {
+            const float* vr = vh + (cell - T_old) * D;
+            for (int blk = 0; blk < D / 32; ++blk)
+                v4_encode_block(vr + blk * 32, v_blocks + (((int64_t)h * cap + cell) * (D / 32) + blk) * 18);
+            int64_t slot = kvqo_k2v4_slot(cell, T_new, L);
+            if (slot >= 0) {
+                for (int d = 0; d < D; ++d) {
+                    k_win[((int64_t)h * slots + slot) * D + d] = (uint16_t)kvqo_f16_encode(kh[(cell - T_old) * D + d]);
                     v_win[((int64_t)h * slots + slot) * D + d] = (uint16_t)kvqo_f16_encode(vr[d]);
                 }
             }

@@ -99,6 +99,8 @@ def _declare(L):
     L.kvqo_k2v4_slot.argtypes = [C.c_int64, C.c_int64, C.POINTER(K2V4Layout)]
     L.kvqo_k2v4_encode.restype = C.c_int
     L.kvqo_k2v4_encode.argtypes = [P, P, C.c_int64, C.c_int64, C.POINTER(K2V4Layout), P, P, P, P, P]
+    L.kvqo_k2v4_append.restype = C.c_int
+    L.kvqo_k2v4_append.argtypes = [P, P, C.c_int64, C.c_int64, C.c_int64, C.POINTER(K2V4Layout), P, P, P, P, P]
     L.kvqo_k2v4_reconstruct.restype = C.c_int
     L.kvqo_k2v4_reconstruct.argtypes = [P, P, P, P, P, C.c_int64, C.c_int64, C.POINTER(K2V4Layout),
                                         C.c_int, P, P]
@@ -329,6 +331,18 @@ def k2v4_encode(k: np.ndarray, v: np.ndarray, L: K2V4Layout, cap: int | None = N
     vw = np.zeros((H, slots, D), np.uint16)
     _check(lib().kvqo_k2v4_encode(_p(k), _p(v), T, cap, C.byref(L), _p(kc), _p(ks), _p(vb), _p(kw), _p(vw)),
            "k2v4_encode")
+    return kc, ks, vb, kw, vw
+
+
+def k2v4_append(kc, ks, vb, kw, vw, k_new: np.ndarray, v_new: np.ndarray, T_old: int, L: K2V4Layout):
+    """Append k_new, v_new ([Hkv, n, D] float32) at cells T_old .. T_old + n - 1 of
+    one sequence's pools; returns updated copies (kc, ks, vb, kw, vw)."""
+    kc, ks, vb, kw, vw = (np.array(a, copy=True) for a in (kc, ks, vb, kw, vw))
+    k_new = np.ascontiguousarray(k_new, np.float32)
+    v_new = np.ascontiguousarray(v_new, np.float32)
+    cap = kc.shape[1]
+    _check(lib().kvqo_k2v4_append(_p(k_new), _p(v_new), int(T_old), k_new.shape[1], cap, C.byref(L), _p(kc),
+                                  _p(ks), _p(vb), _p(kw), _p(vw)), "k2v4_append")
     return kc, ks, vb, kw, vw
 
 

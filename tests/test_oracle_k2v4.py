@@ -131,3 +131,122 @@ def test_overlay_cells_match_fp16_attention(oracle):
     Kf = k[0].astype(np.float16).astype(np.float64)
     Vf = v[0].astype(np.float16).astype(np.float64)
     np.testing.assert_array_equal(got, oracle.k2v4_attn(Kf, Vf, q, 1 / 8))
+
+
+# --- appends and the partial-group scale rule ([P3] "Review fixes", item
+# "Fresh partial-group scale"; "Attention error under the engine's append
+# patterns") ---------------------------------------------------------------
+
+def _empty_pools(H, cap, D, slots):
+    return (np.zeros((H, cap, D // 4), np.uint8), np.zeros((H, cap // 32, D), np.uint16),
+            np.zeros((H, cap, D // 32, 18), np.uint8), np.zeros((H, slots, D), np.uint16),
+            np.zeros((H, slots, D), np.uint16))
+
+
+def _append_all(oracle, L, k, v, cuts, cap):
+    """Append k[:, a:b], v[:, a:b] for consecutive cut points, from an empty pool."""
+    H, _, D = k.shape
+    pools = _empty_pools(H, cap, D, L.n_sink + L.n_window + L.n_slack)
+    for a, b in zip(cuts[:-1], cuts[1:]):
+        pools = oracle.k2v4_append(*pools, k[:, a:b], v[:, a:b], a, L)
+    return pools
+
+
+def _f16(x):
+    return int(np.float16(x).view(np.uint16))
+
+
+def test_append_of_whole_groups_equals_encoder(oracle):
+    """Appends of whole 32-cell groups never run the partial rule: the pools
+    equal the encoder's (bulk bit for bit, the reader's view through the
+    overlay identical)."""
+    H, T, D, cap = 2, 96, 64, 128
+    k, v = synth.gqa_kv(41, 1, H, T, D)
+    L = oracle.k2v4_layout(H, D, 1.10, 4, 16, 16)
+    enc = oracle.k2v4_encode(k[0], v[0], L, cap)
+    for cuts in ([0, 96], [0, 32, 96], [0, 32, 64, 96]):
+        app = _append_all(oracle, L, k[0], v[0], cuts, cap)
+        for a, b in zip(enc[:3], app[:3]):
+            np.testing.assert_array_equal(a, b)
+        ke, ve = oracle.k2v4_reconstruct(*enc, T, L)
+        ka, va = oracle.k2v4_reconstruct(*app, T, L)
+        np.testing.assert_array_equal(ke, ka)
+        np.testing.assert_array_equal(ve, va)
+
+
+def test_partial_group_closed_forms_at_constant_magnitude(oracle):
+    """Every cell of magnitude c: the previous group's mean square equals the
+    present cells', so the shrink rule returns c for any n, and the /n rule of
+    a partial first group returns c too; a later append into a started group
+    keeps its scale."""
+    H, D, cap, c = 1, 32, 160, 0.75
+    rng = np.random.default_rng(3)
+    k = (c * rng.choice([-1.0, 1.0], size=(H, 150, D))).astype(np.float32)
+    v = rng.standard_normal((H, 150, D)).astype(np.float32)
+    L = oracle.k2v4_layout(H, D, 1.0, 0, 0, 0)
+    for cuts in ([0, 5], [0, 40], [0, 40, 43, 93], [0, 1, 2, 3, 35, 150]):
+        kc, ks, vb, kw, vw = _append_all(oracle, L, k, v, cuts, cap)
+        n_groups = (cuts[-1] + 31) // 32
+        assert np.all(ks[0, :n_groups] == _f16(c)), cuts
+        # codes: x / s = +-1 is nearest the outer levels +-1.510 (|1 - 1.510| <
+        # |1 - 0.4528|), read back as +-1.510 c
+        K, _ = oracle.k2v4_reconstruct(kc, ks, vb, kw, vw, cuts[-1], L, use_overlay=False)
+        lv, _ = oracle.k2_codebook()
+        want = np.where(k[0, :cuts[-1]] > 0, lv[3], lv[0]) * c
+        np.testing.assert_allclose(K[0], want, rtol=1e-6)
+
+
+def test_partial_group_shrinks_toward_previous_scale(oracle):
+    """A fresh group of n zero cells after a group of magnitude c: s =
+    c * sqrt((32 - n) / 32) (no present energy, the previous mean square
+    fills the 32 - n missing cells), to one fp16 step after the f32 steps."""
+    H, D, cap, c = 1, 32, 64, 0.75
+    for gain in (1.0, 1.10):
+        L = oracle.k2v4_layout(H, D, gain, 0, 0, 0)
+        for n in (1, 3, 17, 31):
+            k = np.zeros((H, 32 + n, D), np.float32)
+            k[:, :32] = c
+            v = np.zeros_like(k)
+            _, ks, _, _, _ = _append_all(oracle, L, k, v, [0, 32 + n], cap)
+            prev = float(np.float16(gain * c)) / gain
+            want = gain * prev * math.sqrt((32 - n) / 32)
+            got = float(ks[0, 1, 0].view(np.float16))
+            assert abs(got - want) <= 2 ** -10 * want + 1e-12, (gain, n, got, want)
+            assert ks[0, 0, 0] == _f16(gain * c)
+
+
+def test_partial_first_group_is_rms_of_present_cells(oracle):
+    """Group 0 written by a partial batch has no previous group: its scale is
+    the RMS of the n cells present (3, 4, 0, 0 -> sqrt(25 / 4) = 2.5)."""
+    H, D, cap = 1, 32, 64
+    L = oracle.k2v4_layout(H, D, 1.0, 0, 0, 0)
+    k = np.zeros((H, 4, D), np.float32)
+    k[0, 0], k[0, 1] = 3.0, 4.0
+    _, ks, _, _, _ = _append_all(oracle, L, k, np.zeros_like(k), [0, 4], cap)
+    assert np.all(ks[0, 0] == _f16(2.5))
+
+
+def test_one_call_equals_two_calls_split_at_a_group_boundary(oracle):
+    """The previous group's scale enters the partial rule identically whether
+    it was stored by an earlier call or in the same call ([P3]: two-call and
+    one-call appends store the same scale)."""
+    H, D, cap = 2, 64, 192
+    k, v = synth.gqa_kv(43, 1, H, 180, D)
+    L = oracle.k2v4_layout(H, D, 1.10, 4, 16, 16)
+    for total, split in ((70, 64), (101, 96), (180, 128), (40, 32)):
+        one = _append_all(oracle, L, k[0, :, :total], v[0, :, :total], [0, total], cap)
+        two = _append_all(oracle, L, k[0, :, :total], v[0, :, :total], [0, split, total], cap)
+        for a, b in zip(one[:3], two[:3]):
+            np.testing.assert_array_equal(a, b)
+
+
+def test_append_into_started_group_keeps_its_scale(oracle):
+    """Cells appended into a group that already holds cells are coded against
+    the stored scale, which stays as it was."""
+    H, D, cap = 2, 64, 128
+    k, v = synth.gqa_kv(47, 1, H, 100, D)
+    L = oracle.k2v4_layout(H, D, 1.10, 4, 16, 16)
+    first = _append_all(oracle, L, k[0, :, :45], v[0, :, :45], [0, 45], cap)
+    after = oracle.k2v4_append(*first, k[0, :, 45:50], v[0, :, 45:50], 45, L)
+    np.testing.assert_array_equal(first[1][:, :2], after[1][:, :2])
+    np.testing.assert_array_equal(first[0][:, :45], after[0][:, :45])
