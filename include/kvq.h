@@ -318,11 +318,38 @@ kvq_status k2v4_encode(const kvq_k2v4_layout* layout, const float* k, const floa
                        uint8_t* k_codes, uint16_t* k_scales, uint8_t* v_blocks,
                        uint16_t* k_win, uint16_t* v_win, void* stream);
 
+/* Appends n_new cells to every sequence at cells n_past .. n_past + n_new - 1
+ * (the engine's append patterns of [P3] "Attention error under the engine's
+ * append patterns": decode steps, speculative-verify windows, prefill chunks
+ * that start or end inside a 32-cell group).
+ *   k_new, v_new  [batch][n_kv_heads][n_new][head_dim] f32
+ *   pools         as for k2v4_encode; cells < n_past are left as they are
+ * K scale of a group ([P3] "Review fixes", "Fresh partial-group scale"):
+ *   - first written by this call with all 32 cells: the encoder's rule;
+ *   - first written by this call with n < 32 cells:
+ *       s = sqrt((ss + (32 - n) prev^2) / 32), ss the sum of squares of the n
+ *       cells, prev = fp16(stored scale of the previous group) / k_gain, the
+ *       same bits whether that group was stored by an earlier call or in this
+ *       one (two calls split at a group boundary store what one call stores);
+ *     group 0 with n < 32 cells: s = sqrt(ss / n);
+ *   - already holding cells from an earlier call: the stored scale is kept
+ *     and the new cells are coded against fp16(stored) / k_gain.
+ * Stored scale fp16(k_gain * s), codes against s, as in the encoder.  V and
+ * the overlay of the new cells as in the encoder, the window taken at
+ * n_past + n_new.  Requires n_past + n_new <= capacity (a multiple of 32);
+ * returns KVQ_ERR_ARG otherwise. */
+kvq_status k2v4_append(const kvq_k2v4_layout* layout, const float* k_new, const float* v_new,
+                       int32_t batch, int64_t n_past, int64_t n_new, int64_t capacity,
+                       uint8_t* k_codes, uint16_t* k_scales, uint8_t* v_blocks,
+                       uint16_t* k_win, uint16_t* v_win, void* stream);
+
 size_t kv_attn_decode_k2v4_workspace_size(const kvq_k2v4_layout* layout, int32_t batch,
                                           int32_t n_q_heads, int64_t n_cells, kvq_path path);
 
 /* GQA decode over the K2/V4 cache: q head h reads kv head h / (n_q_heads /
  * n_kv_heads); cells in the overlay read fp16 exactly, the rest the bulk.
+ * n_cells may end inside a 32-cell group (after appends); capacity is a
+ * multiple of 32.
  *   q    [batch][n_q_heads][head_dim] f32;  out [batch][n_q_heads][head_dim] f32 */
 kvq_status kv_attn_decode_k2v4(const kvq_k2v4_layout* layout, const float* q, int32_t batch,
                                int32_t n_q_heads, int64_t n_cells, int64_t capacity,

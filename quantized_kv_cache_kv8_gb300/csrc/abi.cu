@@ -397,6 +397,21 @@ kvq_status k2v4_encode(const kvq_k2v4_layout* layout, const float* k, const floa
                                           v_win, (cudaStream_t)stream));
 }
 
+kvq_status k2v4_append(const kvq_k2v4_layout* layout, const float* k_new, const float* v_new, int32_t batch,
+                       int64_t n_past, int64_t n_new, int64_t capacity, uint8_t* k_codes, uint16_t* k_scales,
+                       uint8_t* v_blocks, uint16_t* k_win, uint16_t* v_win, void* stream) {
+    kvq_status s = check_k2v4(layout);
+    if (s != KVQ_OK) return s;
+    if (batch < 0 || n_past < 0 || n_new < 0 || capacity < 0 || n_past > capacity - n_new) return KVQ_ERR_ARG;
+    if (capacity % 32 != 0) return KVQ_ERR_UNSUPPORTED;
+    if (batch > 65535 || layout->n_kv_heads > 65535 || n_new > 0x7fffffff) return KVQ_ERR_UNSUPPORTED;
+    if (batch == 0 || n_new == 0) return KVQ_OK;
+    if (!k_new || !v_new || !k_codes || !k_scales || !v_blocks) return KVQ_ERR_ARG;
+    if ((layout->n_sink + layout->n_window) > 0 && (!k_win || !v_win)) return KVQ_ERR_ARG;
+    return cuda_status(launch_k2v4_append(*layout, k_new, v_new, batch, n_past, n_new, capacity, k_codes, k_scales,
+                                          v_blocks, k_win, v_win, (cudaStream_t)stream));
+}
+
 size_t kv_attn_decode_k2v4_workspace_size(const kvq_k2v4_layout* layout, int32_t batch, int32_t n_q_heads,
                                           int64_t n_cells, kvq_path path) {
     if (check_k2v4(layout) != KVQ_OK || check_k2v4_path(path) != KVQ_OK) return 0;
@@ -417,7 +432,7 @@ kvq_status kv_attn_decode_k2v4(const kvq_k2v4_layout* layout, const float* q, in
     if (batch < 0 || n_q_heads < 0 || n_cells < 0 || capacity < n_cells) return KVQ_ERR_ARG;
     if (n_q_heads % layout->n_kv_heads != 0) return KVQ_ERR_ARG;
     if (n_q_heads / layout->n_kv_heads > 8) return KVQ_ERR_UNSUPPORTED;
-    if (n_cells % 32 != 0 || capacity % 32 != 0) return KVQ_ERR_UNSUPPORTED;
+    if (capacity % 32 != 0) return KVQ_ERR_UNSUPPORTED;   // n_cells may end inside a group
     const int D = layout->head_dim;
     if (D != 128 && D != 256 && D != 512) return KVQ_ERR_UNSUPPORTED;
     if (batch > 65535) return KVQ_ERR_UNSUPPORTED;

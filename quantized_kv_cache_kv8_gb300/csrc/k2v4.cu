@@ -82,15 +82,105 @@ __global__ void __launch_bounds__(kMaxD) k2_encode_kernel(const float* __restric
     }
 }
 
-// grid: (T, H, batch), block: D threads; warp w encodes 32-dim block w of the cell
+// Append of n_new cells at t_old .. t_old + n_new - 1 (k_new is [batch][H]
+// [n_new][D]): one block per (touched group, kv head, sequence), one thread
+// per channel.  A group first written here takes, with all 32 cells present,
+// the encoder's rule; with n < 32 cells, sqrt((ss + (32 - n) prev^2) / 32)
+// ([P3] "Review fixes": the previous group's mean square stands in for the
+// cells not yet written), prev = f16(stored scale of the previous group) /
+// k_gain -- recomputed here from the new cells when that group is written in
+// this launch (it is then whole), read from the pool otherwise, the same bits
+// either way; group 0 with n < 32 cells takes the RMS of the cells present.
+// A group that already holds cells keeps its scale and codes the new cells
+// against f16(stored) / k_gain.
+__global__ void __launch_bounds__(kMaxD) k2_append_kernel(const float* __restrict__ k_new, K2V4Params p,
+                                                          int64_t t_old, int64_t n_new,
+                                                          uint8_t* __restrict__ k_codes,
+                                                          uint16_t* __restrict__ k_scales) {
+    const int d = threadIdx.x, lane = threadIdx.x & 31;
+    const int64_t gi = t_old / kG + blockIdx.x;
+    const int h = blockIdx.y, b = blockIdx.z;
+    const int64_t seq = (int64_t)b * p.H + h;
+    const int64_t g0 = gi * kG;
+    const bool fresh = g0 >= t_old;
+    const int64_t c0 = fresh ? g0 : t_old;
+    const int n = (int)(min(g0 + kG, t_old + n_new) - c0);            // new cells of the group
+    const float* col = k_new + (seq * n_new + (c0 - t_old)) * p.D + d;
+    uint16_t* sc = k_scales + (seq * (p.cap / kG) + gi) * p.D + d;
+    float x[kG];
+#pragma unroll
+    for (int j = 0; j < kG; ++j) x[j] = j < n ? __ldg(col + (int64_t)j * p.D) : 0.0f;
+    float s_rule;
+    if (fresh) {
+        float ps[kG];
+#pragma unroll
+        for (int j = 0; j < kG; ++j) ps[j] = __fmaf_rn(x[j], x[j], 0.0f);
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1)
+#pragma unroll
+            for (int j = 0; j < off; ++j) ps[j] = __fadd_rn(ps[j], ps[j + off]);
+        if (n == kG) {
+            s_rule = __fsqrt_rn(__fdiv_rn(ps[0], 32.0f));
+        } else if (gi == 0) {
+            s_rule = __fsqrt_rn(__fdiv_rn(ps[0], (float)n));
+        } else {
+            uint16_t prev_bits;
+            if ((gi - 1) * kG >= t_old) {
+                // the previous group is written by this launch, whole: its stored
+                // scale is recomputed here in the encoder's order
+                const float* pc = col - (int64_t)kG * p.D;
+                float pp[kG];
+#pragma unroll
+                for (int j = 0; j < kG; ++j) {
+                    const float y = __ldg(pc + (int64_t)j * p.D);
+                    pp[j] = __fmaf_rn(y, y, 0.0f);
+                }
+#pragma unroll
+                for (int off = 16; off >= 1; off >>= 1)
+#pragma unroll
+                    for (int j = 0; j < off; ++j) pp[j] = __fadd_rn(pp[j], pp[j + off]);
+                const float s_prev = __fsqrt_rn(__fdiv_rn(pp[0], 32.0f));
+                prev_bits = __half_as_ushort(__float2half_rn(__fmul_rn(p.k_gain, s_prev)));
+            } else {
+                prev_bits = sc[-p.D];   // stored by an earlier call
+            }
+            const float prev = __fdiv_rn(__half2float(__ushort_as_half(prev_bits)), p.k_gain);
+            const float add = __fmul_rn((float)(kG - n), __fmul_rn(prev, prev));
+            s_rule = __fsqrt_rn(__fdiv_rn(__fadd_rn(ps[0], add), 32.0f));
+        }
+        *sc = __half_as_ushort(__float2half_rn(__fmul_rn(p.k_gain, s_rule)));
+    } else {
+        s_rule = __fdiv_rn(__half2float(__ushort_as_half(*sc)), p.k_gain);
+    }
+#pragma unroll
+    for (int j = 0; j < kG; ++j) {
+        if (j >= n) break;   // n is the same for the whole block
+        int c = 0;
+        if (s_rule != 0.0f) {
+            const float u = __fdiv_rn(x[j], s_rule);
+            c = (u > p.th[0]) + (u > p.th[1]) + (u > p.th[2]);
+        }
+        const int c1 = __shfl_down_sync(kFull, c, 1);
+        const int c2 = __shfl_down_sync(kFull, c, 2);
+        const int c3 = __shfl_down_sync(kFull, c, 3);
+        if ((lane & 3) == 0)
+            k_codes[(seq * p.cap + c0 + j) * (p.D / 4) + d / 4] = (uint8_t)(c | (c1 << 2) | (c2 << 4) | (c3 << 6));
+    }
+}
+
+// grid: (cells written, H, batch), block: D threads; warp w encodes 32-dim
+// block w of cell cell0 + blockIdx.x, read from row blockIdx.x of a source of
+// src_cells rows per sequence (the whole sequence for the encoder, the new
+// cells for an append); the overlay window is taken at p.T
 __global__ void __launch_bounds__(kMaxD) v4_encode_kernel(const float* __restrict__ k, const float* __restrict__ v,
-                                                          K2V4Params p, uint8_t* __restrict__ v_blocks,
+                                                          K2V4Params p, int64_t src_cells, int64_t cell0,
+                                                          uint8_t* __restrict__ v_blocks,
                                                           uint16_t* __restrict__ k_win, uint16_t* __restrict__ v_win) {
     const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
-    const int64_t cell = blockIdx.x;
+    const int64_t cell = cell0 + blockIdx.x;
     const int g = blockIdx.y, b = blockIdx.z;
     const int64_t seq = (int64_t)b * p.H + g;
-    const int64_t src = (seq * p.T + cell) * p.D + tid;
+    const int64_t src = (seq * src_cells + blockIdx.x) * p.D + tid;
     const float x = __ldg(v + src);
     const float ax = fabsf(x);
     const float amax = warp_max(ax);
@@ -416,7 +506,11 @@ template <int D>
 __device__ __forceinline__ void stage_tile(const K2V4DecodeParams& p, int64_t seq, int64_t t0, int nt,
                                            unsigned char* dst, int tid) {
     using SM = SmemT<D>;
-    const int n_kc = nt * (D / 4) / 16, n_ks = (nt / kG) * 2 * D / 16, n_vb = nt * (D / 32) * 18 / 16;
+    // whole 32-cell groups: a sequence may end inside its last group (after
+    // appends); the cells past its end lie inside the pool (capacities are
+    // multiples of 32) and are zeroed and masked by the caller
+    const int ns = (nt + kG - 1) / kG * kG;
+    const int n_kc = ns * (D / 4) / 16, n_ks = (ns / kG) * 2 * D / 16, n_vb = ns * (D / 32) * 18 / 16;
     const unsigned char* kc = p.k_codes + (seq * p.c.cap + t0) * (D / 4);
     const unsigned char* ks = reinterpret_cast<const unsigned char*>(p.k_scales + (seq * (p.c.cap / kG) + t0 / kG) * D);
     const unsigned char* vb = p.v_blocks + (seq * p.c.cap + t0) * (D / 32) * 18;
@@ -757,7 +851,23 @@ cudaError_t launch_k2v4_encode(const kvq_k2v4_layout& L, const float* k, const f
     k2_encode_kernel<<<dim3((unsigned)(n_cells / kG), p.H, batch), p.D, 0, stream>>>(k, p, k_codes, k_scales);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    v4_encode_kernel<<<dim3((unsigned)n_cells, p.H, batch), p.D, 0, stream>>>(k, v, p, v_blocks, k_win, v_win);
+    v4_encode_kernel<<<dim3((unsigned)n_cells, p.H, batch), p.D, 0, stream>>>(k, v, p, n_cells, 0, v_blocks, k_win,
+                                                                              v_win);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_k2v4_append(const kvq_k2v4_layout& L, const float* k_new, const float* v_new, int32_t batch,
+                               int64_t n_past, int64_t n_new, int64_t cap, uint8_t* k_codes, uint16_t* k_scales,
+                               uint8_t* v_blocks, uint16_t* k_win, uint16_t* v_win, cudaStream_t stream) {
+    if (batch == 0 || n_new == 0) return cudaSuccess;
+    const K2V4Params p = make_params(L, n_past + n_new, cap);   // overlay window at the new length
+    const int64_t groups = (n_past + n_new - 1) / kG - n_past / kG + 1;
+    k2_append_kernel<<<dim3((unsigned)groups, p.H, batch), p.D, 0, stream>>>(k_new, p, n_past, n_new, k_codes,
+                                                                            k_scales);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    v4_encode_kernel<<<dim3((unsigned)n_new, p.H, batch), p.D, 0, stream>>>(k_new, v_new, p, n_new, n_past,
+                                                                            v_blocks, k_win, v_win);
     return cudaGetLastError();
 }
 

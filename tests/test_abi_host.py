@@ -165,3 +165,17 @@ def test_k2_tensor_level_scale_is_f16_exact_and_tight(oracle):
     prod = (np.abs(lv).astype(np.float32) * np.float32(g)).astype(np.float32)
     rel = np.abs(prod.astype(np.float16).astype(np.float64) - np.abs(lv) * g) / (np.abs(lv) * g)
     assert rel.max() <= 2e-5, rel.max()
+
+
+def test_k2v4_append_validates_before_launch(kvq):
+    """Refused on the host, nothing launched: a range past the capacity, a
+    negative position, a capacity that is not whole groups, missing pools."""
+    L = kvq.lib()
+    lay = kvq.k2v4_layout()
+    d = C.c_void_p(256)
+    assert L.k2v4_append(C.byref(lay), d, d, 1, 60, 10, 64, d, d, d, d, d, None) == 1      # 70 > 64 cells
+    assert L.k2v4_append(C.byref(lay), d, d, 1, -1, 10, 64, d, d, d, d, d, None) == 1
+    assert L.k2v4_append(C.byref(lay), d, d, 1, 0, 10, 40, d, d, d, d, d, None) == 5       # capacity 40
+    assert L.k2v4_append(C.byref(lay), None, d, 1, 0, 10, 64, d, d, d, d, d, None) == 1
+    assert L.k2v4_append(C.byref(lay), d, d, 1, 0, 10, 64, d, d, d, None, d, None) == 1  # overlay pools
+    assert L.k2v4_append(C.byref(lay), None, None, 1, 5, 0, 64, None, None, None, None, None, None) == 0
