@@ -192,6 +192,17 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kv8_kernel(AttnParams p) 
     const int group = (int)(w % (p.n_heads / kHC));
     const int hbase = group * kHC;
 
+    if (tid == 32 && p.prefill_past < 0) {
+        // a decode batch's queries into L2, a slice per CTA, while warp 0
+        // looks up the item: the query loads after the lookup then hit L2
+        // (not for prefill, whose CTAs each read one token's query, nor for
+        // batches whose queries would crowd the cache)
+        const uint64_t total = (uint64_t)p.n_seq * p.n_heads * kMlaD * 2;   // bf16, a multiple of 16
+        const uint64_t per = (total / gridDim.x + 15) & ~(uint64_t)15;
+        const uint64_t off = per * blockIdx.x;
+        if (total <= (32ull << 20) && off < total)
+            prefetch_l2(reinterpret_cast<const char*>(p.q) + off, (uint32_t)min(per, total - off));
+    }
     if (warp == 0) {
         int64_t r0 = 0, r1 = 0;
         int b = locate_item(p, item, lane, &r0, &r1);
@@ -267,6 +278,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kv8_kernel(AttnParams p) 
         float qmax = 0.0f, smax = 0.0f;
 #pragma unroll
         for (int i = 0; i < kQPer; ++i) qraw[i] = __ldg(qv + tid + i * kWorkers);
+#pragma unroll 4
         for (int64_t r = row0 + tid; r < row1; r += kWorkers)
             if (!APPEND || r != rn) smax = fmaxf(smax, p.scales[(GATHER ? gather_row(p, r) : r) * p.n_blocks]);
 #pragma unroll
