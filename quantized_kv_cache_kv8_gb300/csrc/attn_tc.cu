@@ -1,20 +1,25 @@
-// attn_tc.cu -- tensor-core (tcgen05 / TMEM) attention over quantized MLA rows.
+// attn_tc.cu -- tensor-core (tcgen05 / TMEM) attention over KV8 rows with f32
+// queries, the planning of the tensor-core split and the dispatch to the
+// kernels of each format (attn_tc_kv8.cu: KV8 with bf16 queries; attn_tc_tq4.cu:
+// TQ4).
 //
 // All heads share one latent cache, so per tile of rows the score (heads x
 // rows x 576) and the context (heads x 512 x rows) are dense contractions.
 // They run on the 5th-generation tensor cores with f16 operands decoded from
 // the quantized rows in shared memory; accumulators live in tensor memory.
+// An f32 query is not exact in f16: it enters as an f16 value and an f16
+// residual (rows 64..127 of each query chunk), which leaves room for a 4-slot
+// ring of decoded chunks only, each chunk decoded once for the score and once
+// for the context.
 //
 // Formulation (transposed, per CTA: one chunk of rows x 64 heads):
 //   S_L^T[t][h] = sum_{d<512} c[t][d] q[h][d]     M = 128 rows, N = 64 heads
 //   S_R^T[t][h] = sum_{d>=512} c[t][d] q[h][d]    (the rope block, own scale)
 //   O^T[d][h]  += sum_t c[t][d] * P^T[t][h]        M = 128 dims (x4), K = rows
-// c are the codes' values (e4m3 value, or TQ4 codebook level against the
-// rotated query), exact in f16 for KV8.  The per-row scales stay outside the
-// products and are applied by the thread that owns the row: z = sm*(s_L*S_L +
-// s_R*S_R), and the context weight is p*s_L ([P2] "What's in it": the row
-// scale factors out of both sums; [P1] "Ready for review" comment, finding 2:
-// TQ4 dots the rotated query with codebook levels and unrotates once).
+// c are the codes' e4m3 values, exact in f16.  The per-row scales stay outside
+// the products and are applied by the thread that owns the row: z = sm*(s_L*S_L
+// + s_R*S_R), and the context weight is p*s_L ([P2] "What's in it": the row
+// scale factors out of both sums).
 //
 // TMEM (512 columns x 128 lanes of f32): O^T = 4 blocks x 64 columns, S_L^T and
 // S_R^T 64 columns each.  A full O for 128 heads x 512 dims would fill all of
@@ -50,9 +55,8 @@ constexpr uint32_t kOffSlot = kOffQ + 9 * kQChunkBytes;
 constexpr uint32_t kOffP = kOffSlot + kSlots * kSlotBytes;
 constexpr uint32_t kOffM = kOffP + kRows * 128;
 constexpr uint32_t kOffAlpha = kOffM + kHC * 4;
-constexpr uint32_t kOffLut = kOffAlpha + kHC * 4;
-constexpr uint32_t kOffBar = kOffLut + 256 * 4;
-constexpr uint32_t kOffMisc = kOffBar + 16 * 8;   // abort flag, TMEM base, item info, reductions, TQ4 residuals
+constexpr uint32_t kOffBar = kOffAlpha + kHC * 4;
+constexpr uint32_t kOffMisc = kOffBar + 16 * 8;   // abort flag, TMEM base, residual flag, item info, reductions
 constexpr uint32_t kSmemUsed = kOffMisc + 160;
 constexpr size_t kSmemAlloc = kSmemUsed;          // the base is 1024-aligned (checked at run time)
 static_assert(kSmemAlloc <= 232448, "shared memory budget");
@@ -66,18 +70,12 @@ constexpr uint32_t kColO = 0, kColSL = 256, kColSR = 384, kTmemCols = 512;
 enum { kBarFull0 = 0, kBarEmpty0 = 4, kBarScore = 8, kBarCtx = 9, kBarP = 10, kNumBars = 11 };
 
 using namespace tc;
-// TQ4 levels in f16: the 16 Lloyd-Max levels times kTq4Gamma round to f16 with
-// a relative error of at most 9.3e-5 (2^-13.4), against 3.2e-4 unscaled; the
-// value comes from a search over scales in [1, 2) (csrc/gen_codebook.py
-// --level-scale).  Scores and context are divided by it in f32.
-constexpr float kTq4Gamma = 1.3338516f;
-constexpr float kTq4InvGamma = 1.0f / 1.3338516f;
 constexpr uint32_t kIdescScore = idesc_f16(128, kHC, false, false);
 constexpr uint32_t kIdescScore2 = idesc_f16(128, 2 * kHC, false, false);
 constexpr uint32_t kIdescCtx = idesc_f16(128, kHC, true, true);
 
 // The raw bytes one thread converts for one chunk: dims [64 kc, 64 kc + 64) of
-// row (tid / 2), half (tid % 2) of them.  KV8: 32 bytes (a, b); TQ4: 16 (a).
+// row (tid / 2), half (tid % 2) of them: 32 bytes (a, b).
 struct RawChunk {
     uint4 a, b;
 };
@@ -88,7 +86,6 @@ struct RawChunk {
 // conversion and the MMAs of the steps in between.
 constexpr int kStepsPerTile = 17;
 
-template <int FMT>
 __device__ __forceinline__ RawChunk load_step(const uint8_t* __restrict__ codes, int64_t row0, int64_t row1,
                                               int64_t step, int tid) {
     const int64_t tile = step / kStepsPerTile;
@@ -99,39 +96,25 @@ __device__ __forceinline__ RawChunk load_step(const uint8_t* __restrict__ codes,
     RawChunk c;
     c.a = c.b = make_uint4(0u, 0u, 0u, 0u);
     if (row < row1) {
-        if (FMT == KVQ_KV8) {
-            const uint4* src = reinterpret_cast<const uint4*>(codes + row * kMlaD + kc * 64 + half * 32);
-            c.a = __ldg(src);
-            c.b = __ldg(src + 1);
-        } else {
-            c.a = __ldg(reinterpret_cast<const uint4*>(codes + row * (kMlaD / 2) + kc * 32 + half * 16));
-        }
+        const uint4* src = reinterpret_cast<const uint4*>(codes + row * kMlaD + kc * 64 + half * 32);
+        c.a = __ldg(src);
+        c.b = __ldg(src + 1);
     }
     return c;
 }
 
-// Converts a thread's raw chunk to f16 code values (e4m3 value, or TQ4 level)
-// in a staging slot: row r = one 128-byte swizzled row.  Rows past the tile's
-// end are written as zeros.
-template <int FMT>
-__device__ __forceinline__ void store_chunk(const RawChunk& c, bool valid, unsigned char* slot, const uint32_t* lut,
-                                            int tid) {
+// Converts a thread's raw chunk to f16 code values (e4m3 values) in a staging
+// slot: row r = one 128-byte swizzled row.  Rows past the tile's end are
+// written as zeros.
+__device__ __forceinline__ void store_chunk(const RawChunk& c, bool valid, unsigned char* slot, int tid) {
     const int r = tid >> 1, half = tid & 1;
     uint32_t w[16];
     if (valid) {
-        if (FMT == KVQ_KV8) {
-            const uint32_t in[8] = {c.a.x, c.a.y, c.a.z, c.a.w, c.b.x, c.b.y, c.b.z, c.b.w};
+        const uint32_t in[8] = {c.a.x, c.a.y, c.a.z, c.a.w, c.b.x, c.b.y, c.b.z, c.b.w};
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                w[2 * i] = e4m3x2_to_half2_bits(in[i] & 0xffffu);
-                w[2 * i + 1] = e4m3x2_to_half2_bits(in[i] >> 16);
-            }
-        } else {
-            const uint32_t in[4] = {c.a.x, c.a.y, c.a.z, c.a.w};
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-#pragma unroll
-                for (int j = 0; j < 4; ++j) w[4 * i + j] = lut[(in[i] >> (8 * j)) & 0xffu];
+        for (int i = 0; i < 8; ++i) {
+            w[2 * i] = e4m3x2_to_half2_bits(in[i] & 0xffffu);
+            w[2 * i + 1] = e4m3x2_to_half2_bits(in[i] >> 16);
         }
     } else {
 #pragma unroll
@@ -143,11 +126,6 @@ __device__ __forceinline__ void store_chunk(const RawChunk& c, bool valid, unsig
             make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
 }
 
-// LOQ: the query needs its f16 residual rows (f32 queries, or TQ4's rotated
-// queries).  Without them (KV8 with a bf16 query, exact in f16) the residual
-// half of the query area holds a 5-stage cp.async ring of raw code chunks.
-constexpr int kRing = 5;      // stages; chunk k + 4 is copied while chunk k is converted
-template <int FMT, bool QBF16, bool LOQ>
 __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnParams p) {
     launch_dependents();
     const int64_t w = blockIdx.x;
@@ -158,7 +136,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnParams p) {
     unsigned char* sP = sm + kOffP;
     float* sM = reinterpret_cast<float*>(sm + kOffM);
     float* sAlpha = reinterpret_cast<float*>(sm + kOffAlpha);
-    uint32_t* sLut = reinterpret_cast<uint32_t*>(sm + kOffLut);
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kOffBar);
     volatile int* sAbort = reinterpret_cast<volatile int*>(sm + kOffMisc);
     uint32_t* sTmem = reinterpret_cast<uint32_t*>(sm + kOffMisc + 4);
@@ -208,69 +185,32 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnParams p) {
         *sHasLo = 0;
     }
     if (tid < kHC) sM[tid] = -INFINITY;
-    if (FMT == KVQ_TQ4 && tid < 256) {
-        const int lo = tid & 15, hi = tid >> 4;
-        const __half2 h2 = __halves2half2(__float2half_rn(__fmul_rn(p.lv[lo], kTq4Gamma)),
-                                          __float2half_rn(__fmul_rn(p.lv[hi], kTq4Gamma)));
-        sLut[tid] = *reinterpret_cast<const uint32_t*>(&h2);
-    }
 
-    // workers: the first chunk copies go out now and overlap the query prologue
     const int wt = tid < kWorkers ? tid : 0;
-    const int wrow = wt >> 1, whalf = wt & 1;
     int64_t step = 0;
-    // raw ring stage k: the residual half of query chunk k (free when !LOQ)
-    auto ring_ptr = [&](int64_t k) -> unsigned char* {
-        return sQ + (int)(k % kRing) * kQChunkBytes + kHC * 128 + wrow * 64 + whalf * 32;
-    };
-    auto issue_copy = [&](int64_t k) {
-        const int64_t tl = k / kStepsPerTile;
-        const int j = (int)(k - tl * kStepsPerTile);
-        const int kc = j < 9 ? j : j - 9;
-        const int64_t row = row0 + tl * kRows + wrow;
-        if (row < row1) {
-            const uint8_t* src = p.codes + row * kMlaD + kc * 64 + whalf * 32;
-            unsigned char* dst = ring_ptr(k);
-            cp_async16(dst, src);
-            cp_async16(dst + 16, src + 16);
-        }
-        cp_async_commit();
-    };
-    if (!LOQ && tid < kWorkers) {
-        for (int k = 0; k < kRing - 1; ++k) issue_copy(k);
-    }
     if (tid == 0) {
         // the first tile's bytes (contiguous rows) into L2
         const int64_t n = min((int64_t)kRows, row1 - row0);
-        const int row_bytes = FMT == KVQ_KV8 ? kMlaD : kMlaD / 2;
-        prefetch_l2(p.codes + row0 * row_bytes, (uint32_t)(n * row_bytes));
+        prefetch_l2(p.codes + row0 * kMlaD, (uint32_t)(n * kMlaD));
     }
-    // the raw chunk of step `step`: from the ring (after its copy group lands)
-    // or, with LOQ, straight from global memory (L2-prefetched one tile ahead)
-#define KVQ_NEXT_CHUNK(dst)                                                       \
-    do {                                                                          \
-        if (!LOQ) {                                                               \
-            issue_copy(step + kRing - 1);                                         \
-            cp_async_wait<kRing - 1>();                                           \
-            const uint4* src_ = reinterpret_cast<const uint4*>(ring_ptr(step));   \
-            dst.a = src_[0];                                                      \
-            dst.b = src_[1];                                                      \
-        } else {                                                                  \
-            dst = load_step<FMT>(p.codes, row0, row1, step, wt);                  \
-        }                                                                         \
-        ++step;                                                                   \
+    // the raw chunk of step `step`, straight from global memory (L2-prefetched
+    // one tile ahead)
+#define KVQ_NEXT_CHUNK(dst)                                    \
+    do {                                                       \
+        dst = load_step(p.codes, row0, row1, step, wt);        \
+        ++step;                                                \
     } while (0)
 
     // The 64 heads of this CTA are 64 x 576 contiguous query values.
     const int64_t qbase = ((int64_t)b * p.n_heads + hbase) * kMlaD;
-    constexpr int kQVec = QBF16 ? 8 : 4;                   // values per 16-byte load
+    constexpr int kQVec = 4;                               // f32 values per 16-byte load
     constexpr int kQLoads = kHC * kMlaD / kQVec;           // 16-byte loads covering the 64 heads
-    // largest |q| (bounds every rotated element too: |q'_i| <= ||q|| <= 24 max|q|)
-    // and the largest latent scale of the chunk
+    // largest |q| (with the bound 24 max|q| >= ||q|| that the other kernels
+    // use for rotated queries) and the largest latent scale of the chunk
     float qmax = 0.0f, smax = 0.0f;
     if (tid < kWorkers) {
-        const uint4* qv = reinterpret_cast<const uint4*>(reinterpret_cast<const char*>(p.q) + qbase * (QBF16 ? 2 : 4));
-        constexpr int kPer = kQLoads / kWorkers;           // 18 (bf16) or 36 (f32): all in flight at once
+        const uint4* qv = reinterpret_cast<const uint4*>(reinterpret_cast<const float*>(p.q) + qbase);
+        constexpr int kPer = kQLoads / kWorkers;           // 36: all in flight at once
         static_assert(kQLoads % kWorkers == 0, "query loads per worker");
 #pragma unroll 6
         for (int i0 = 0; i0 < kPer; i0 += 6) {
@@ -281,14 +221,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnParams p) {
             for (int i = 0; i < 6; ++i) {
                 const uint32_t in[4] = {w[i].x, w[i].y, w[i].z, w[i].w};
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    if (QBF16) {
-                        qmax = fmaxf(qmax, fabsf(__uint_as_float(in[k] << 16)));
-                        qmax = fmaxf(qmax, fabsf(__uint_as_float(in[k] & 0xffff0000u)));
-                    } else {
-                        qmax = fmaxf(qmax, fabsf(__uint_as_float(in[k])));
-                    }
-                }
+                for (int k = 0; k < 4; ++k) qmax = fmaxf(qmax, fabsf(__uint_as_float(in[k])));
             }
         }
         for (int64_t r = row0 + tid; r < row1; r += kWorkers) smax = fmaxf(smax, p.scales[r * p.n_blocks]);
@@ -316,110 +249,44 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnParams p) {
     const float s_ref = s_max > 0.0f ? ldexpf(1.0f, e_s) : 1.0f;
     const float inv_s_ref = s_max > 0.0f ? ldexpf(1.0f, -e_s) : 1.0f;
     const float q_scale = q_bound > 0.0f ? ldexpf(1.0f, 14 - e_q) : 1.0f;
-    // TQ4 levels enter the products scaled by kTq4Gamma; it is divided out of
-    // the scores here and out of the context in the epilogue
-    const float lv_unscale = FMT == KVQ_TQ4 ? kTq4InvGamma : 1.0f;
-    const float cz = p.sm_scale * kLog2e * (q_bound > 0.0f ? ldexpf(1.0f, e_q - 14) : 1.0f) * lv_unscale;
+    const float cz = p.sm_scale * kLog2e * (q_bound > 0.0f ? ldexpf(1.0f, e_q - 14) : 1.0f);
     const uint32_t tmem = *sTmem;
 
     // queries -> f16 pair (value, residual) in the score's B layout (K-major,
     // 9 chunks of 64 dims x 128 rows)
     int any_lo = 0;
-    if (FMT == KVQ_KV8) {
-        if (tid < kWorkers) {
-            // 8 consecutive dims of one head per step: one 16-byte store of each half
-            const uint4* qv = reinterpret_cast<const uint4*>(reinterpret_cast<const char*>(p.q) + qbase * (QBF16 ? 2 : 4));
+    if (tid < kWorkers) {
+        // 8 consecutive dims of one head per step: one 16-byte store of each half
+        const uint4* qv = reinterpret_cast<const uint4*>(reinterpret_cast<const float*>(p.q) + qbase);
 #pragma unroll 3
-            for (int u = tid; u < kHC * kMlaD / 8; u += kWorkers) {
-                float x[8];
-                if (QBF16) {
-                    const uint4 w = __ldg(qv + u);
-                    const uint32_t in[4] = {w.x, w.y, w.z, w.w};
+        for (int u = tid; u < kHC * kMlaD / 8; u += kWorkers) {
+            const uint4 w0 = __ldg(qv + 2 * u), w1 = __ldg(qv + 2 * u + 1);
+            const float x[8] = {__uint_as_float(w0.x), __uint_as_float(w0.y), __uint_as_float(w0.z),
+                                __uint_as_float(w0.w), __uint_as_float(w1.x), __uint_as_float(w1.y),
+                                __uint_as_float(w1.z), __uint_as_float(w1.w)};
+            const int e = u * 8, h = e / kMlaD, d = e - h * kMlaD;
+            uint32_t hw[4], lw[4];
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        x[2 * i] = __uint_as_float(in[i] << 16);
-                        x[2 * i + 1] = __uint_as_float(in[i] & 0xffff0000u);
-                    }
-                } else {
-                    const uint4 w0 = __ldg(qv + 2 * u), w1 = __ldg(qv + 2 * u + 1);
-                    const uint32_t in[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) x[i] = __uint_as_float(in[i]);
-                }
-                const int e = u * 8, h = e / kMlaD, d = e - h * kMlaD;
-                uint32_t hw[4], lw[4];
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const float a0 = x[2 * i] * q_scale, a1 = x[2 * i + 1] * q_scale;
-                    const __half h0 = __float2half_rn(a0), h1 = __float2half_rn(a1);
-                    const __half l0 = __float2half_rn(a0 - __half2float(h0));
-                    const __half l1 = __float2half_rn(a1 - __half2float(h1));
-                    any_lo |= (__half_as_ushort(l0) | __half_as_ushort(l1)) & 0x7fff;
-                    hw[i] = (uint32_t)__half_as_ushort(h0) | ((uint32_t)__half_as_ushort(h1) << 16);
-                    lw[i] = (uint32_t)__half_as_ushort(l0) | ((uint32_t)__half_as_ushort(l1) << 16);
-                }
-                unsigned char* chunk = sQ + (d >> 6) * kQChunkBytes;
-                *reinterpret_cast<uint4*>(chunk + sw128(h, (d & 63) * 2)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-                if (LOQ)
-                    *reinterpret_cast<uint4*>(chunk + sw128(kHC + h, (d & 63) * 2)) =
-                        make_uint4(lw[0], lw[1], lw[2], lw[3]);
+            for (int i = 0; i < 4; ++i) {
+                const float a0 = x[2 * i] * q_scale, a1 = x[2 * i + 1] * q_scale;
+                const __half h0 = __float2half_rn(a0), h1 = __float2half_rn(a1);
+                const __half l0 = __float2half_rn(a0 - __half2float(h0));
+                const __half l1 = __float2half_rn(a1 - __half2float(h1));
+                any_lo |= (__half_as_ushort(l0) | __half_as_ushort(l1)) & 0x7fff;
+                hw[i] = (uint32_t)__half_as_ushort(h0) | ((uint32_t)__half_as_ushort(h1) << 16);
+                lw[i] = (uint32_t)__half_as_ushort(l0) | ((uint32_t)__half_as_ushort(l1) << 16);
             }
-        }
-    } else {
-        // TQ4: rotate every head once.  The raw queries of a group of heads are
-        // staged in the (still idle) slot and P^T area, then each warp rotates
-        // its heads with the warp FWHT.
-        constexpr int kGroup = QBF16 ? kHC : kHC / 2;       // 73,728 bytes of raw query per group
-        for (int g0 = 0; g0 < kHC; g0 += kGroup) {
-            if (tid < kWorkers) {
-                const uint4* src = reinterpret_cast<const uint4*>(reinterpret_cast<const char*>(p.q) +
-                                                                   (qbase + (int64_t)g0 * kMlaD) * (QBF16 ? 2 : 4));
-                uint4* dst = reinterpret_cast<uint4*>(sSlot);
-                for (int u = tid; u < kGroup * kMlaD / kQVec; u += kWorkers) dst[u] = __ldg(src + u);
-                worker_sync();
-                for (int hh = warp; hh < kGroup; hh += kWorkers / 32) {
-                    float v[18];
-#pragma unroll
-                    for (int k = 0; k < 18; ++k) {
-                        const int idx = hh * kMlaD + lane + 32 * k;
-                        v[k] = QBF16 ? __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(sSlot)[idx])
-                                     : reinterpret_cast<const float*>(sSlot)[idx];
-                    }
-#pragma unroll
-                    for (int k = 0; k < 16; ++k)
-                        if (sign_neg(p.signs, 0, lane + 32 * k)) v[k] = -v[k];
-                    warp_fwht<512>(v, lane);
-#pragma unroll
-                    for (int k = 0; k < 16; ++k) v[k] = __fmul_rn(v[k], p.kn[0]);
-#pragma unroll
-                    for (int k = 16; k < 18; ++k)
-                        if (sign_neg(p.signs, 1, lane + 32 * (k - 16))) v[k] = -v[k];
-                    warp_fwht<64>(v + 16, lane);
-#pragma unroll
-                    for (int k = 16; k < 18; ++k) v[k] = __fmul_rn(v[k], p.kn[1]);
-                    const int h = g0 + hh;
-#pragma unroll
-                    for (int k = 0; k < 18; ++k) {
-                        const int d = lane + 32 * k;
-                        const float x = v[k] * q_scale;
-                        const __half hi = __float2half_rn(x);
-                        const __half lo = __float2half_rn(x - __half2float(hi));
-                        any_lo |= __half_as_ushort(lo) & 0x7fff;
-                        unsigned char* chunk = sQ + (d >> 6) * kQChunkBytes;
-                        *reinterpret_cast<__half*>(chunk + sw128(h, (d & 63) * 2)) = hi;
-                        *reinterpret_cast<__half*>(chunk + sw128(kHC + h, (d & 63) * 2)) = lo;
-                    }
-                }
-                worker_sync();
-            }
+            unsigned char* chunk = sQ + (d >> 6) * kQChunkBytes;
+            *reinterpret_cast<uint4*>(chunk + sw128(h, (d & 63) * 2)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+            *reinterpret_cast<uint4*>(chunk + sw128(kHC + h, (d & 63) * 2)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
         }
     }
-    if (LOQ && any_lo) atomicOr(sHasLo, 1);
+    if (any_lo) atomicOr(sHasLo, 1);
     fence_async_smem();
     tc_before();
     __syncthreads();
     tc_after();
-    // a query exact in f16 (bf16 input, KV8) needs only the first 64 rows
+    // a query exact in f16 needs only the first 64 rows
     const bool has_lo = *sHasLo != 0;
 
     if (warp == kWorkers / 32) {
@@ -489,8 +356,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnParams p) {
         const bool valid = (tid >> 1) < nt;
         if (tid == 0 && t0 + kRows < row1) {
             const int64_t n = min((int64_t)kRows, row1 - (t0 + kRows));
-            const int row_bytes = FMT == KVQ_KV8 ? kMlaD : kMlaD / 2;
-            prefetch_l2(p.codes + (t0 + kRows) * row_bytes, (uint32_t)(n * row_bytes));
+            prefetch_l2(p.codes + (t0 + kRows) * kMlaD, (uint32_t)(n * kMlaD));
         }
         // this thread's softmax row scales (used after the score chunks)
         float my_sl = 0.0f, my_sr = 0.0f;
@@ -505,7 +371,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnParams p) {
             if (uses[s] > 0) mbar_wait(&bars[kBarEmpty0 + s], (uses[s] - 1) & 1, sAbort);
             RawChunk rc;
             KVQ_NEXT_CHUNK(rc);
-            store_chunk<FMT>(rc, valid, sSlot + s * kSlotBytes, sLut, tid);
+            store_chunk(rc, valid, sSlot + s * kSlotBytes, tid);
             fence_async_smem();
             mbar_arrive(&bars[kBarFull0 + s]);
             ++uses[s];
@@ -614,8 +480,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnParams p) {
             RawChunk r0c, r1c;
             KVQ_NEXT_CHUNK(r0c);
             KVQ_NEXT_CHUNK(r1c);
-            store_chunk<FMT>(r0c, valid, sSlot + s0 * kSlotBytes, sLut, tid);
-            store_chunk<FMT>(r1c, valid, sSlot + (s0 + 1) * kSlotBytes, sLut, tid);
+            store_chunk(r0c, valid, sSlot + s0 * kSlotBytes, tid);
+            store_chunk(r1c, valid, sSlot + (s0 + 1) * kSlotBytes, tid);
             fence_async_smem();
             mbar_arrive(&bars[kBarFull0 + s0]);
             mbar_arrive(&bars[kBarFull0 + s0 + 1]);
@@ -625,7 +491,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnParams p) {
         o_init = true;
     }
 #undef KVQ_NEXT_CHUNK
-    if (!LOQ) cp_async_wait<0>();
 
     // ---- epilogue: row sums, O^T -> partial state ----
     if (tile > 0) mbar_wait(&bars[kBarCtx], (tile - 1) & 1, sAbort);
@@ -666,7 +531,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnParams p) {
                 for (int j = 0; j < 32; ++j) {
                     const int h = hbase + 32 * c + j;
                     p.ws_o[(item * p.n_heads + h) * kMlaDV + dim] =
-                        o_init ? __uint_as_float(v[j]) * (s_ref * lv_unscale) : 0.0f;
+                        o_init ? __uint_as_float(v[j]) * s_ref : 0.0f;
                 }
             }
         }
@@ -682,13 +547,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnParams p) {
     if (warp == 1) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols));
 }
 
-template <int FMT, bool QBF16>
-cudaError_t launch_tc(const AttnParams& p, int64_t grid_x, int groups, cudaStream_t stream) {
-    constexpr bool kLoq = !(FMT == KVQ_KV8 && QBF16);
-    cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<FMT, QBF16, kLoq>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)kSmemAlloc);
+cudaError_t launch_tc_kv8_f32(const AttnParams& p, int64_t grid_x, int groups, cudaStream_t stream) {
+    cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemAlloc);
     if (e != cudaSuccess) return e;
-    attn_tc_kernel<FMT, QBF16, kLoq><<<dim3((unsigned)(grid_x * groups)), kThreads, kSmemAlloc, stream>>>(p);
+    attn_tc_kernel<<<dim3((unsigned)(grid_x * groups)), kThreads, kSmemAlloc, stream>>>(p);
     return cudaGetLastError();
 }
 
@@ -752,7 +614,7 @@ cudaError_t launch_attn_tc(kvq_format fmt, const kvq_mla_layout& L, const void* 
     cudaError_t e;
     if (fmt == KVQ_KV8)
         e = qdt == KVQ_BF16 ? launch_attn_tc_kv8_bf16(p, plan.max_items, groups, stream)
-                            : launch_tc<KVQ_KV8, false>(p, plan.max_items, groups, stream);
+                            : launch_tc_kv8_f32(p, plan.max_items, groups, stream);
     else
         e = launch_attn_tc_tq4(p, qdt == KVQ_BF16, plan.max_items, n_heads, stream);
     if (e != cudaSuccess) return e;

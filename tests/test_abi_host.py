@@ -144,7 +144,7 @@ def test_tq4_tensor_level_scale_keeps_levels_near_f16(oracle):
     """The tensor-core TQ4 kernel feeds f16(f32(level * scale)) to the MMA; the
     scale in its source keeps every level within 1e-4 relative of its f16 copy
     (unscaled levels are off by up to 3.2e-4)."""
-    src = open(os.path.join(ROOT, "quantized_kv_cache_kv8_gb300", "csrc", "attn_tc.cu")).read()
+    src = open(os.path.join(ROOT, "quantized_kv_cache_kv8_gb300", "csrc", "attn_tc_tq4.cu")).read()
     g = np.float32(float(re.search(r"constexpr float kTq4Gamma = ([0-9.]+)f;", src).group(1)))
     lv, _ = oracle.tq4_codebook()
     scaled = (lv.astype(np.float32) * g).astype(np.float32)
