@@ -132,6 +132,21 @@ def make_inputs(torch, kvq):
                 q_host=torch.from_numpy(q_bits.view(np.int16)).view(torch.bfloat16).pin_memory())
 
 
+def max_over_ranks(vals, dist, device):
+    """Each timing's maximum over the ranks: the slowest replica bounds the job."""
+    import torch
+    t = torch.tensor(vals, dtype=torch.float64, device=device)
+    if dist:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        dist.barrier()
+    return t.tolist()
+
+
+def job_rate_gbs(rows_per_rank, world, ms):
+    """Whole-job cache throughput: every replica's rows over the slowest step time."""
+    return rows_per_rank * world * ROW_BYTES / (ms * 1e-3) / 1e9
+
+
 def run_ours(args, rank, world):
     import torch
     from quantized_kv_cache_kv8_gb300 import kvq
@@ -201,18 +216,14 @@ def run_ours(args, rank, world):
     if err != 0:
         raise RuntimeError(f"device error word {err} after the timed region")
 
-    t = torch.tensor([step_ms, e2e_ms], dtype=torch.float64, device=dev)
-    if dist:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        dist.barrier()
-    step_ms, e2e_ms = t.tolist()
+    step_ms, e2e_ms = max_over_ranks([step_ms, e2e_ms], dist, dev)
     if rank != 0:
         return None
 
     rows = B * T * world
     peaks, src = load_peaks()
-    gbs = rows * ROW_BYTES / (step_ms * 1e-3) / 1e9
-    e2e_gbs = rows * ROW_BYTES / (e2e_ms * 1e-3) / 1e9
+    gbs = job_rate_gbs(B * T, world, step_ms)
+    e2e_gbs = job_rate_gbs(B * T, world, e2e_ms)
     clocks = sampler.summary()
     # the decode's tensor-core path is bound by the bf16 tensor pipe; the SIMT
     # path by the fp32 FMA pipe (152 SMs x 128 lanes x 2 flop x max SM clock)
