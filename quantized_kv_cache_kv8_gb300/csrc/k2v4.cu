@@ -499,9 +499,10 @@ __device__ __forceinline__ uint32_t q4_pair(uint32_t codes2, uint32_t d2) {
     return hmul2_bits(hsub2_bits(codes2 | 0x64006400u, 0x64086408u), d2);
 }
 
-// Copies the raw bytes of the tile at cells [t0, t0 + nt) into `dst` with
-// 16-byte cp.async (nt a multiple of 32; each piece is contiguous and 16-byte
-// aligned in the cache).  One commit group per call.
+// Copies the raw bytes of the tile at cells [t0, t0 + nt), rounded up to whole
+// 32-cell groups, into `dst` with 16-byte cp.async (t0 a multiple of 32; each
+// piece is contiguous and 16-byte aligned in the cache).  One commit group per
+// call.
 template <int D>
 __device__ __forceinline__ void stage_tile(const K2V4DecodeParams& p, int64_t seq, int64_t t0, int nt,
                                            unsigned char* dst, int tid) {
@@ -527,9 +528,9 @@ __device__ __forceinline__ void stage_tile(const K2V4DecodeParams& p, int64_t se
             src = vb + 16 * (i - n_kc - n_ks);
             d = dst + SM::kRawKc + SM::kRawKs + 16 * (i - n_kc - n_ks);
         }
-        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(d)), "l"(src) : "memory");
+        cp_async16(d, src);
     }
-    asm volatile("cp.async.commit_group;" ::: "memory");
+    cp_async_commit();
 }
 
 template <int D>
@@ -628,9 +629,9 @@ __global__ void __launch_bounds__(kThreadsT, 1) k2v4_tc_kernel(K2V4DecodeParams 
         if (t + 1 < n_tiles) {
             stage_tile<D>(p, seq, t0 + kRowsT, (int)min((int64_t)kRowsT, c1 - t0 - kRowsT),
                           sRaw + ((t + 1) & 1) * SM::kRawBytes, tid);
-            asm volatile("cp.async.wait_group 1;" ::: "memory");
+            cp_async_wait<1>();
         } else {
-            asm volatile("cp.async.wait_group 0;" ::: "memory");
+            cp_async_wait<0>();
         }
         __syncthreads();
         const unsigned char* raw = sRaw + (t & 1) * SM::kRawBytes;
