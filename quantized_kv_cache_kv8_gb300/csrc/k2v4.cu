@@ -638,51 +638,67 @@ __global__ void __launch_bounds__(kThreadsT, 1) k2v4_tc_kernel(K2V4DecodeParams 
         // ---- K of the tile to f16 (cells on rows, 64 dims per chunk), all
         // warps.  sK is free: the previous tile's softmax waited for its score;
         // the previous context MMAs, which read sV and P^T only, may still run.
-        // unrolled: the iterations' dependent chains interleave (one CTA of 8
-        // warps per SM leaves little else to hide their latency)
+        // A whole tile of bulk cells (no sink or window cell, the usual case)
+        // takes a branch-free loop whose unrolled iterations interleave: with
+        // one CTA of 8 warps per SM little else hides their latency.
+        const bool plain = nt == kRowsT && t0 >= p.c.n_sink && t0 + kRowsT <= p.c.T - p.c.n_window;
+        auto k_bulk = [&](int r, int j, uint32_t (&kw)[16]) {
+            // 2-bit codes (32 dims = 8 bytes; dims 2m, 2m+1 in bits 4m..4m+3)
+            // times the group's per-dim fp16 scales, pairwise in f16
+            const uint2 kc = *reinterpret_cast<const uint2*>(raw_kc + r * (D / 4) + 8 * j);
+            const uint4* scq = reinterpret_cast<const uint4*>(raw_ks + (r / kG) * D + 32 * j);
+            uint32_t scw[16];
 #pragma unroll
-        for (int it = tid; it < kRowsT * (D / 32); it += kThreadsT) {
-            const int r = it / (D / 32), j = it - r * (D / 32);   // cell, 32-dim slice
-            uint32_t kw[16];
-            if (r < nt) {
-                const int64_t slot = overlay_slot(t0 + r, p.c);
-                if (slot >= 0) {
-                    // exact fp16 copy
-                    const uint4* kwin = reinterpret_cast<const uint4*>(p.k_win + (seq * p.c.slots + slot) * D + 32 * j);
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const uint4 a = __ldg(kwin + i);
-                        kw[4 * i] = a.x; kw[4 * i + 1] = a.y; kw[4 * i + 2] = a.z; kw[4 * i + 3] = a.w;
-                    }
-                } else {
-                    // 2-bit codes (32 dims = 8 bytes; dims 2m, 2m+1 in bits 4m..4m+3)
-                    // times the group's per-dim fp16 scales, pairwise in f16
-                    const uint2 kc = *reinterpret_cast<const uint2*>(raw_kc + r * (D / 4) + 8 * j);
-                    // the 32 dims' scales as four 16-byte loads (16 word loads
-                    // from 8 slices per warp conflict 4-way on the banks)
-                    const uint4* scq = reinterpret_cast<const uint4*>(raw_ks + (r / kG) * D + 32 * j);
-                    uint32_t scw[16];
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const uint4 w = scq[i];
-                        scw[4 * i] = w.x; scw[4 * i + 1] = w.y; scw[4 * i + 2] = w.z; scw[4 * i + 3] = w.w;
-                    }
-#pragma unroll
-                    for (int m = 0; m < 16; ++m) {
-                        const uint32_t nib = ((m < 8 ? kc.x : kc.y) >> (4 * (m & 7))) & 15u;
-                        const uint32_t sel = ((nib & 3u) | ((nib & 12u) << 6)) * 0x22u + 0x1010u;
-                        kw[m] = hmul2_bits(__byte_perm(lv01, lv23, sel), scw[m]);
-                    }
-                }
-            } else {
-#pragma unroll
-                for (int i = 0; i < 16; ++i) kw[i] = 0u;
+            for (int i = 0; i < 4; ++i) {
+                const uint4 w = scq[i];
+                scw[4 * i] = w.x; scw[4 * i + 1] = w.y; scw[4 * i + 2] = w.z; scw[4 * i + 3] = w.w;
             }
+#pragma unroll
+            for (int m = 0; m < 16; ++m) {
+                const uint32_t nib = ((m < 8 ? kc.x : kc.y) >> (4 * (m & 7))) & 15u;
+                const uint32_t sel = ((nib & 3u) | ((nib & 12u) << 6)) * 0x22u + 0x1010u;
+                kw[m] = hmul2_bits(__byte_perm(lv01, lv23, sel), scw[m]);
+            }
+        };
+        auto k_store = [&](int r, int j, const uint32_t (&kw)[16]) {
             unsigned char* kdst = sK + (j >> 1) * kChunkT;
 #pragma unroll
             for (int i = 0; i < 4; ++i)
                 *reinterpret_cast<uint4*>(kdst + sw128(r, (j & 1) * 64 + 16 * i)) =
                     make_uint4(kw[4 * i], kw[4 * i + 1], kw[4 * i + 2], kw[4 * i + 3]);
+        };
+        if (plain) {
+#pragma unroll
+            for (int it = tid; it < kRowsT * (D / 32); it += kThreadsT) {
+                const int r = it / (D / 32), j = it - r * (D / 32);   // cell, 32-dim slice
+                uint32_t kw[16];
+                k_bulk(r, j, kw);
+                k_store(r, j, kw);
+            }
+        } else {
+            for (int it = tid; it < kRowsT * (D / 32); it += kThreadsT) {
+                const int r = it / (D / 32), j = it - r * (D / 32);
+                uint32_t kw[16];
+                if (r < nt) {
+                    const int64_t slot = overlay_slot(t0 + r, p.c);
+                    if (slot >= 0) {
+                        // exact fp16 copy
+                        const uint4* kwin =
+                            reinterpret_cast<const uint4*>(p.k_win + (seq * p.c.slots + slot) * D + 32 * j);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const uint4 a = __ldg(kwin + i);
+                            kw[4 * i] = a.x; kw[4 * i + 1] = a.y; kw[4 * i + 2] = a.z; kw[4 * i + 3] = a.w;
+                        }
+                    } else {
+                        k_bulk(r, j, kw);
+                    }
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) kw[i] = 0u;
+                }
+                k_store(r, j, kw);
+            }
         }
         fence_async_smem();
         tc_before();
@@ -704,43 +720,59 @@ __global__ void __launch_bounds__(kThreadsT, 1) k2v4_tc_kernel(K2V4DecodeParams 
             // ---- V of the tile to f16, warps 4-7, overlapping the score MMAs
             // and the softmax, once the previous context MMAs released sV ----
             if (t > 0) mbar_wait(&bars[1], (uint32_t)(t - 1) & 1u, sAbort);
-            for (int it = tid - 128; it < kRowsT * (D / 32); it += kThreadsT - 128) {
-                const int r = it / (D / 32), j = it - r * (D / 32);
-                uint32_t vw[16];
-                if (r < nt) {
-                    const int64_t slot = overlay_slot(t0 + r, p.c);
-                    if (slot >= 0) {
-                        const uint4* vwin =
-                            reinterpret_cast<const uint4*>(p.v_win + (seq * p.c.slots + slot) * D + 32 * j);
+            auto v_bulk = [&](int r, int j, uint32_t (&vw)[16]) {
+                // q4_0 block (d, then 16 bytes: element e in the low nibble of
+                // byte e, e + 16 in the high nibble)
+                const uint16_t* blk = reinterpret_cast<const uint16_t*>(raw_vb + (r * (D / 32) + j) * 18);
+                const uint32_t d2 = (uint32_t)blk[0] * 0x10001u;
 #pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            const uint4 c = __ldg(vwin + i);
-                            vw[4 * i] = c.x; vw[4 * i + 1] = c.y; vw[4 * i + 2] = c.z; vw[4 * i + 3] = c.w;
-                        }
-                    } else {
-                        // q4_0 block (d, then 16 bytes: element e in the low nibble of
-                        // byte e, e + 16 in the high nibble)
-                        const uint16_t* blk = reinterpret_cast<const uint16_t*>(raw_vb + (r * (D / 32) + j) * 18);
-                        const uint32_t d2 = (uint32_t)blk[0] * 0x10001u;
-#pragma unroll
-                        for (int m = 0; m < 4; ++m) {
-                            const uint32_t w = (uint32_t)blk[1 + 2 * m] | ((uint32_t)blk[2 + 2 * m] << 16);
-                            const uint32_t p01 = __byte_perm(w, 0u, 0x4140u), p23 = __byte_perm(w, 0u, 0x4342u);
-                            vw[2 * m] = q4_pair(p01 & 0x000F000Fu, d2);
-                            vw[2 * m + 1] = q4_pair(p23 & 0x000F000Fu, d2);
-                            vw[8 + 2 * m] = q4_pair((p01 >> 4) & 0x000F000Fu, d2);
-                            vw[9 + 2 * m] = q4_pair((p23 >> 4) & 0x000F000Fu, d2);
-                        }
-                    }
-                } else {
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) vw[i] = 0u;
+                for (int m = 0; m < 4; ++m) {
+                    const uint32_t w = (uint32_t)blk[1 + 2 * m] | ((uint32_t)blk[2 + 2 * m] << 16);
+                    const uint32_t p01 = __byte_perm(w, 0u, 0x4140u), p23 = __byte_perm(w, 0u, 0x4342u);
+                    vw[2 * m] = q4_pair(p01 & 0x000F000Fu, d2);
+                    vw[2 * m + 1] = q4_pair(p23 & 0x000F000Fu, d2);
+                    vw[8 + 2 * m] = q4_pair((p01 >> 4) & 0x000F000Fu, d2);
+                    vw[9 + 2 * m] = q4_pair((p23 >> 4) & 0x000F000Fu, d2);
                 }
+            };
+            auto v_store = [&](int r, int j, const uint32_t (&vw)[16]) {
                 unsigned char* vdst = sV + (j >> 1) * kChunkT;
 #pragma unroll
                 for (int i = 0; i < 4; ++i)
                     *reinterpret_cast<uint4*>(vdst + sw128(r, (j & 1) * 64 + 16 * i)) =
                         make_uint4(vw[4 * i], vw[4 * i + 1], vw[4 * i + 2], vw[4 * i + 3]);
+            };
+            if (plain) {
+#pragma unroll 4
+                for (int it = tid - 128; it < kRowsT * (D / 32); it += kThreadsT - 128) {
+                    const int r = it / (D / 32), j = it - r * (D / 32);
+                    uint32_t vw[16];
+                    v_bulk(r, j, vw);
+                    v_store(r, j, vw);
+                }
+            } else {
+                for (int it = tid - 128; it < kRowsT * (D / 32); it += kThreadsT - 128) {
+                    const int r = it / (D / 32), j = it - r * (D / 32);
+                    uint32_t vw[16];
+                    if (r < nt) {
+                        const int64_t slot = overlay_slot(t0 + r, p.c);
+                        if (slot >= 0) {
+                            const uint4* vwin =
+                                reinterpret_cast<const uint4*>(p.v_win + (seq * p.c.slots + slot) * D + 32 * j);
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) {
+                                const uint4 c = __ldg(vwin + i);
+                                vw[4 * i] = c.x; vw[4 * i + 1] = c.y; vw[4 * i + 2] = c.z; vw[4 * i + 3] = c.w;
+                            }
+                        } else {
+                            v_bulk(r, j, vw);
+                        }
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) vw[i] = 0u;
+                    }
+                    v_store(r, j, vw);
+                }
             }
         } else {
             // ---- softmax: warps 0-3, thread = cell (TMEM lane), the group's
