@@ -248,8 +248,9 @@ def run_ours(args, rank, world):
     line = {
         "metric": METRIC, "value": round(gbs, 3), "unit": "GB/s", "n_gpus": world, "steps": K,
         "warmup": max(args.warmup, 3), "ms_per_step": round(step_ms, 5), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "e4m3 codes, f16 tensor-core operands, f32 accumulate" if used_path == "tensor"
-        else "e4m3 codes, f32 accumulate",
+        "scaling": "weak", "vs_baseline": None, "dtype": "f16" if used_path == "tensor" else "f32",
+        "precision": "e4m3 codes dequantized to f16 tensor-core operands, f32 accumulation and softmax"
+        if used_path == "tensor" else "e4m3 codes dequantized to f32, f32 accumulation and softmax",
         "data": "synthetic (seeded N(0,1) x log-normal channel gains; bf16 queries)",
         "config": {"workload": WORKLOAD, "batch": B, "seq_len": T, "heads": H, "row_bytes": ROW_BYTES,
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
@@ -316,7 +317,7 @@ def run_reference(args, rank, world):
     gbs = T * ROW_BYTES * (8 / H) / step_s / 1e9
     return {"impl": "reference", "metric": METRIC, "value": round(gbs, 6), "unit": "GB/s", "n_gpus": 1, "steps": K,
             "warmup": W, "ms_per_step": round(step_s * 1e3, 3), "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "f64 (oracle)", "data": "synthetic",
+            "vs_baseline": None, "dtype": "f64", "precision": "the oracle: f32 codecs, f64 attention", "data": "synthetic",
             "config": {"workload": WORKLOAD + " (each step: one sequence of the batch, 8 of 128 heads)", "batch": B,
                        "seq_len": T, "heads": H},
             "cpu_baseline": {"value": round(gbs, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",
