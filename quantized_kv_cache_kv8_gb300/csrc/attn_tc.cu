@@ -382,30 +382,34 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnParams p) {
         tc_after();
         float z[32];
         {
-            uint32_t sl[32], sr[32];
-            tmem_ld32(tmem + lane_base + kColSL + 32 * hq, sl);
-            tmem_ld32(tmem + lane_base + kColSR + 32 * hq, sr);
-            tmem_wait_ld();
-            float fl[32], fr[32];
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                fl[j] = __uint_as_float(sl[j]);
-                fr[j] = __uint_as_float(sr[j]);
-            }
-            if (has_lo) {
-                tmem_ld32(tmem + lane_base + kColSL + kHC + 32 * hq, sl);
-                tmem_ld32(tmem + lane_base + kColSR + kHC + 32 * hq, sr);
-                tmem_wait_ld();
-#pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    fl[j] += __uint_as_float(sl[j]);
-                    fr[j] += __uint_as_float(sr[j]);
-                }
-            }
             const float a = my_sl * cz, bb = my_sr * cz;
             const bool row_ok = srow < nt;
+            // 16 columns at a time keeps the peak register count under the cap
 #pragma unroll
-            for (int j = 0; j < 32; ++j) z[j] = row_ok ? fmaf(fl[j], a, fr[j] * bb) : -INFINITY;
+            for (int c = 0; c < 2; ++c) {
+                uint32_t sl[16], sr[16];
+                tmem_ld16(tmem + lane_base + kColSL + 32 * hq + 16 * c, sl);
+                tmem_ld16(tmem + lane_base + kColSR + 32 * hq + 16 * c, sr);
+                tmem_wait_ld();
+                float fl[16], fr[16];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    fl[j] = __uint_as_float(sl[j]);
+                    fr[j] = __uint_as_float(sr[j]);
+                }
+                if (has_lo) {
+                    tmem_ld16(tmem + lane_base + kColSL + kHC + 32 * hq + 16 * c, sl);
+                    tmem_ld16(tmem + lane_base + kColSR + kHC + 32 * hq + 16 * c, sr);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        fl[j] += __uint_as_float(sl[j]);
+                        fr[j] += __uint_as_float(sr[j]);
+                    }
+                }
+#pragma unroll
+                for (int j = 0; j < 16; ++j) z[16 * c + j] = row_ok ? fmaf(fl[j], a, fr[j] * bb) : -INFINITY;
+            }
         }
         bool flag = false;
 #pragma unroll
@@ -433,17 +437,17 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnParams p) {
             }
             worker_sync();
             if (o_init) {
-#pragma unroll
+#pragma unroll 1
                 for (int bi = 0; bi < 2; ++bi)
-#pragma unroll
-                    for (int c = 0; c < 2; ++c) {
-                        const uint32_t ta = tmem + lane_base + kColO + 64 * (2 * hq + bi) + 32 * c;
-                        uint32_t v[32];
-                        tmem_ld32(ta, v);
+#pragma unroll 1
+                    for (int c = 0; c < 4; ++c) {
+                        const uint32_t ta = tmem + lane_base + kColO + 64 * (2 * hq + bi) + 16 * c;
+                        uint32_t v[16];
+                        tmem_ld16(ta, v);
                         tmem_wait_ld();
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) * sAlpha[32 * c + j]);
-                        tmem_st32(ta, v);
+                        for (int j = 0; j < 16; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) * sAlpha[16 * c + j]);
+                        tmem_st16(ta, v);
                     }
                 tmem_wait_st();
             }

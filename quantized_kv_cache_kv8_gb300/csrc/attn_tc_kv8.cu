@@ -462,24 +462,22 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kv8_kernel(AttnParams p) 
         const float za = my_sl * cz, zb = my_sr * cz;
         const bool row_ok = srow < nt;
         auto load_z = [&]() {
-            uint32_t s32[32];
-            tmem_ld32(tmem + lane_base + kColSR + 32 * hq, s32);
-            tmem_wait_ld();
+            // 16 columns at a time keeps the peak register count under the cap
 #pragma unroll
-            for (int j = 0; j < 32; ++j) z[j] = __uint_as_float(s32[j]) * zb;
-            tmem_ld32(tmem + lane_base + kColSL + 32 * hq, s32);
-            tmem_wait_ld();
+            for (int c = 0; c < 2; ++c) {
+                uint32_t s16[16];
+                tmem_ld16(tmem + lane_base + kColSR + 32 * hq + 16 * c, s16);
+                tmem_wait_ld();
 #pragma unroll
-            for (int j = 0; j < 32; ++j) z[j] = row_ok ? fmaf(__uint_as_float(s32[j]), za, z[j]) : -INFINITY;
+                for (int j = 0; j < 16; ++j) z[16 * c + j] = __uint_as_float(s16[j]) * zb;
+                tmem_ld16(tmem + lane_base + kColSL + 32 * hq + 16 * c, s16);
+                tmem_wait_ld();
+#pragma unroll
+                for (int j = 0; j < 16; ++j)
+                    z[16 * c + j] = row_ok ? fmaf(__uint_as_float(s16[j]), za, z[16 * c + j]) : -INFINITY;
+            }
         };
         load_z();
-        // the rest of tile t+1 is requested while the tensor cores are idle
-        // (their operand reads compete with these loads for the SM's memory pipe)
-        if (!GATHER && t + 1 < n_tiles) {
-            load_group<APPEND, GATHER>(rawB, p.codes, t1, nt1, 1, warp, lane, rn, sNew, nullptr);
-            load_rope<APPEND, GATHER>(rawC, p.codes, t1, nt1, tid, rn, sNew, nullptr);
-            load_scales(t1, nt1);
-        }
         bool flag = *sAbort != 0;
 #pragma unroll
         for (int j = 0; j < 32; ++j) flag |= z[j] > sM[32 * hq + j] + kLagLog2;
@@ -523,6 +521,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kv8_kernel(AttnParams p) 
             }
             lcol *= sAlpha[32 * hq + lane];
             load_z();   // the reduction consumed z
+        }
+        // the rest of tile t+1 is requested once the running max is settled:
+        // held across the max pass above, these 40 registers spilled
+        if (!GATHER && t + 1 < n_tiles) {
+            load_group<APPEND, GATHER>(rawB, p.codes, t1, nt1, 1, warp, lane, rn, sNew, nullptr);
+            load_rope<APPEND, GATHER>(rawC, p.codes, t1, nt1, tid, rn, sNew, nullptr);
+            load_scales(t1, nt1);
         }
         {
             const float wrow = my_sl * inv_s_ref;
