@@ -642,23 +642,30 @@ __global__ void __launch_bounds__(kThreadsT, 1) k2v4_tc_kernel(K2V4DecodeParams 
         // takes a branch-free loop whose unrolled iterations interleave: with
         // one CTA of 8 warps per SM little else hides their latency.
         const bool plain = nt == kRowsT && t0 >= p.c.n_sink && t0 + kRowsT <= p.c.T - p.c.n_window;
-        auto k_bulk = [&](int r, int j, uint32_t (&kw)[16]) {
-            // 2-bit codes (32 dims = 8 bytes; dims 2m, 2m+1 in bits 4m..4m+3)
-            // times the group's per-dim fp16 scales, pairwise in f16
-            const uint2 kc = *reinterpret_cast<const uint2*>(raw_kc + r * (D / 4) + 8 * j);
-            const uint4* scq = reinterpret_cast<const uint4*>(raw_ks + (r / kG) * D + 32 * j);
-            uint32_t scw[16];
+        // the fp16 scales of dims 32j .. 32j + 31 in the K scale group g
+        auto k_scales = [&](int g, int j, uint32_t (&scw)[16]) {
+            const uint4* scq = reinterpret_cast<const uint4*>(raw_ks + g * D + 32 * j);
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const uint4 w = scq[i];
                 scw[4 * i] = w.x; scw[4 * i + 1] = w.y; scw[4 * i + 2] = w.z; scw[4 * i + 3] = w.w;
             }
+        };
+        // 2-bit codes (32 dims = 8 bytes; dims 2m, 2m+1 in bits 4m..4m+3)
+        // times the group's per-dim fp16 scales, pairwise in f16
+        auto k_dec = [&](int r, int j, const uint32_t (&scw)[16], uint32_t (&kw)[16]) {
+            const uint2 kc = *reinterpret_cast<const uint2*>(raw_kc + r * (D / 4) + 8 * j);
 #pragma unroll
             for (int m = 0; m < 16; ++m) {
                 const uint32_t nib = ((m < 8 ? kc.x : kc.y) >> (4 * (m & 7))) & 15u;
                 const uint32_t sel = ((nib & 3u) | ((nib & 12u) << 6)) * 0x22u + 0x1010u;
                 kw[m] = hmul2_bits(__byte_perm(lv01, lv23, sel), scw[m]);
             }
+        };
+        auto k_bulk = [&](int r, int j, uint32_t (&kw)[16]) {
+            uint32_t scw[16];
+            k_scales(r / kG, j, scw);
+            k_dec(r, j, scw, kw);
         };
         auto k_store = [&](int r, int j, const uint32_t (&kw)[16]) {
             unsigned char* kdst = sK + (j >> 1) * kChunkT;
@@ -668,11 +675,18 @@ __global__ void __launch_bounds__(kThreadsT, 1) k2v4_tc_kernel(K2V4DecodeParams 
                     make_uint4(kw[4 * i], kw[4 * i + 1], kw[4 * i + 2], kw[4 * i + 3]);
         };
         if (plain) {
+            // warp w takes cells 16w .. 16w + 15 (one scale group) and every
+            // 32-dim slice; a thread keeps one slice, so its scales load once,
+            // and each step covers consecutive cells (conflict-free code loads)
+            constexpr int kS = D / 32, kQ = 32 / kS;
+            const int j = lane % kS, q = lane / kS;
+            uint32_t scw[16];
+            k_scales((16 * warp) / kG, j, scw);
 #pragma unroll
-            for (int it = tid; it < kRowsT * (D / 32); it += kThreadsT) {
-                const int r = it / (D / 32), j = it - r * (D / 32);   // cell, 32-dim slice
+            for (int k = 0; k < 16 / kQ; ++k) {
+                const int r = 16 * warp + q + kQ * k;
                 uint32_t kw[16];
-                k_bulk(r, j, kw);
+                k_dec(r, j, scw, kw);
                 k_store(r, j, kw);
             }
         } else {
@@ -735,6 +749,45 @@ __global__ void __launch_bounds__(kThreadsT, 1) k2v4_tc_kernel(K2V4DecodeParams 
                     vw[9 + 2 * m] = q4_pair((p23 >> 4) & 0x000F000Fu, d2);
                 }
             };
+            // four consecutive q4_0 blocks (72 bytes, 8-byte aligned: a cell's
+            // blocks are contiguous and D / 32 of them take 9 D / 16 bytes)
+            // read as nine 8-byte words; block jj's scale and nibbles sit at
+            // byte 18 jj and 18 jj + 2
+            auto v_quad = [&](int r, int u, auto&& emit) {
+                const uint2* src = reinterpret_cast<const uint2*>(raw_vb + (r * (D / 32) + 4 * u) * 18);
+                uint32_t w[18];
+#pragma unroll
+                for (int i = 0; i < 9; ++i) {
+                    const uint2 x = src[i];
+                    w[2 * i] = x.x;
+                    w[2 * i + 1] = x.y;
+                }
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj) {
+                    const int b = 9 * jj / 2;   // first word of the block (18 jj / 4)
+                    uint32_t d16, nb[4];
+                    if ((jj & 1) == 0) {
+                        d16 = w[b] & 0xffffu;
+#pragma unroll
+                        for (int m = 0; m < 4; ++m) nb[m] = __funnelshift_r(w[b + m], w[b + m + 1], 16);
+                    } else {
+                        d16 = w[b] >> 16;
+#pragma unroll
+                        for (int m = 0; m < 4; ++m) nb[m] = w[b + 1 + m];
+                    }
+                    const uint32_t d2 = d16 * 0x10001u;
+                    uint32_t vw[16];
+#pragma unroll
+                    for (int m = 0; m < 4; ++m) {
+                        const uint32_t p01 = __byte_perm(nb[m], 0u, 0x4140u), p23 = __byte_perm(nb[m], 0u, 0x4342u);
+                        vw[2 * m] = q4_pair(p01 & 0x000F000Fu, d2);
+                        vw[2 * m + 1] = q4_pair(p23 & 0x000F000Fu, d2);
+                        vw[8 + 2 * m] = q4_pair((p01 >> 4) & 0x000F000Fu, d2);
+                        vw[9 + 2 * m] = q4_pair((p23 >> 4) & 0x000F000Fu, d2);
+                    }
+                    emit(4 * u + jj, vw);
+                }
+            };
             auto v_store = [&](int r, int j, const uint32_t (&vw)[16]) {
                 unsigned char* vdst = sV + (j >> 1) * kChunkT;
 #pragma unroll
@@ -743,12 +796,10 @@ __global__ void __launch_bounds__(kThreadsT, 1) k2v4_tc_kernel(K2V4DecodeParams 
                         make_uint4(vw[4 * i], vw[4 * i + 1], vw[4 * i + 2], vw[4 * i + 3]);
             };
             if (plain) {
-#pragma unroll 4
-                for (int it = tid - 128; it < kRowsT * (D / 32); it += kThreadsT - 128) {
-                    const int r = it / (D / 32), j = it - r * (D / 32);
-                    uint32_t vw[16];
-                    v_bulk(r, j, vw);
-                    v_store(r, j, vw);
+#pragma unroll
+                for (int it = tid - 128; it < kRowsT * (D / 128); it += kThreadsT - 128) {
+                    const int r = it / (D / 128), u = it - r * (D / 128);   // cell, run of 4 blocks
+                    v_quad(r, u, [&](int j, const uint32_t (&vw)[16]) { v_store(r, j, vw); });
                 }
             } else {
                 for (int it = tid - 128; it < kRowsT * (D / 32); it += kThreadsT - 128) {
