@@ -349,7 +349,8 @@ size_t kv_attn_decode_k2v4_workspace_size(const kvq_k2v4_layout* layout, int32_t
 /* GQA decode over the K2/V4 cache: q head h reads kv head h / (n_q_heads /
  * n_kv_heads); cells in the overlay read fp16 exactly, the rest the bulk.
  * n_cells may end inside a 32-cell group (after appends); capacity is a
- * multiple of 32.
+ * multiple of 32.  k_codes, k_scales and v_blocks are 16-byte aligned
+ * (KVQ_ERR_ARG otherwise): tiles are staged by bulk copies of whole groups.
  *   q    [batch][n_q_heads][head_dim] f32;  out [batch][n_q_heads][head_dim] f32 */
 kvq_status kv_attn_decode_k2v4(const kvq_k2v4_layout* layout, const float* q, int32_t batch,
                                int32_t n_q_heads, int64_t n_cells, int64_t capacity,

@@ -439,6 +439,9 @@ kvq_status kv_attn_decode_k2v4(const kvq_k2v4_layout* layout, const float* q, in
     if (batch == 0 || n_q_heads == 0) return KVQ_OK;
     if (!q || !out || (n_cells > 0 && (!k_codes || !k_scales || !v_blocks))) return KVQ_ERR_ARG;
     if ((layout->n_sink + layout->n_window) > 0 && (!k_win || !v_win)) return KVQ_ERR_ARG;
+    // the tile staging copies whole 32-cell groups of each pool in 16-byte units
+    if (n_cells > 0 && (!aligned(k_codes, 16) || !aligned(k_scales, 16) || !aligned(v_blocks, 16)))
+        return KVQ_ERR_ARG;
     if (!isfinite(sm_scale)) return KVQ_ERR_ARG;
     const size_t need = kv_attn_decode_k2v4_workspace_size(layout, batch, n_q_heads, n_cells, path);
     if (!workspace || workspace_bytes < need) return KVQ_ERR_WORKSPACE;

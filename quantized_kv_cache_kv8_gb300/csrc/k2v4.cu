@@ -503,34 +503,30 @@ __device__ __forceinline__ uint32_t q4_pair(uint32_t codes2, uint32_t d2) {
 // 32-cell groups, into `dst` with 16-byte cp.async (t0 a multiple of 32; each
 // piece is contiguous and 16-byte aligned in the cache).  One commit group per
 // call.
+// One thread stages a tile's raw bytes with three bulk copies (the TMA
+// engine, no per-thread copy instructions) that complete on the buffer's
+// mbarrier: K codes, K scales and V blocks of whole 32-cell groups.  A
+// sequence may end inside its last group (after appends); the cells past its
+// end lie inside the pool (capacities are multiples of 32, every size and
+// source offset a multiple of 16 bytes) and are masked by the caller.
 template <int D>
 __device__ __forceinline__ void stage_tile(const K2V4DecodeParams& p, int64_t seq, int64_t t0, int nt,
-                                           unsigned char* dst, int tid) {
+                                           unsigned char* dst, uint64_t* bar) {
     using SM = SmemT<D>;
-    // whole 32-cell groups: a sequence may end inside its last group (after
-    // appends); the cells past its end lie inside the pool (capacities are
-    // multiples of 32) and are zeroed and masked by the caller
     const int ns = (nt + kG - 1) / kG * kG;
-    const int n_kc = ns * (D / 4) / 16, n_ks = (ns / kG) * 2 * D / 16, n_vb = ns * (D / 32) * 18 / 16;
+    const uint32_t b_kc = ns * (D / 4), b_ks = (ns / kG) * 2 * D, b_vb = ns * (D / 32) * 18;
     const unsigned char* kc = p.k_codes + (seq * p.c.cap + t0) * (D / 4);
     const unsigned char* ks = reinterpret_cast<const unsigned char*>(p.k_scales + (seq * (p.c.cap / kG) + t0 / kG) * D);
     const unsigned char* vb = p.v_blocks + (seq * p.c.cap + t0) * (D / 32) * 18;
-    for (int i = tid; i < n_kc + n_ks + n_vb; i += kThreadsT) {
-        const unsigned char* src;
-        unsigned char* d;
-        if (i < n_kc) {
-            src = kc + 16 * i;
-            d = dst + 16 * i;
-        } else if (i < n_kc + n_ks) {
-            src = ks + 16 * (i - n_kc);
-            d = dst + SM::kRawKc + 16 * (i - n_kc);
-        } else {
-            src = vb + 16 * (i - n_kc - n_ks);
-            d = dst + SM::kRawKc + SM::kRawKs + 16 * (i - n_kc - n_ks);
-        }
-        cp_async16(d, src);
-    }
-    cp_async_commit();
+    const uint32_t mb = smem_u32(bar);
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(mb), "r"(b_kc + b_ks + b_vb) : "memory");
+    const unsigned char* src[3] = {kc, ks, vb};
+    const uint32_t off[3] = {0u, SM::kRawKc, SM::kRawKc + SM::kRawKs}, bytes[3] = {b_kc, b_ks, b_vb};
+#pragma unroll
+    for (int i = 0; i < 3; ++i)
+        asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                     ::"r"(smem_u32(dst + off[i])), "l"(src[i]), "r"(bytes[i]), "r"(mb)
+                     : "memory");
 }
 
 template <int D>
@@ -548,7 +544,7 @@ __global__ void __launch_bounds__(kThreadsT, 1) k2v4_tc_kernel(K2V4DecodeParams 
     float* sL = sM + 8;
     float* sQmax = sL + 8;
     float* sLv = sQmax + 8;   // the 4 K levels
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem_raw + SM::kOffBar);   // 0 score, 1 context
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem_raw + SM::kOffBar);   // 0 score, 1 context, 2-3 raw buffers
     volatile int* sAbort = reinterpret_cast<volatile int*>(smem_raw + SM::kOffMisc);
     uint32_t* sTmem = reinterpret_cast<uint32_t*>(smem_raw + SM::kOffMisc + 4);
     unsigned char* sRaw = smem_raw + SM::kOffRaw;   // [2][kRawBytes]
@@ -560,7 +556,6 @@ __global__ void __launch_bounds__(kThreadsT, 1) k2v4_tc_kernel(K2V4DecodeParams 
     const int64_t c1 = min(c0 + p.chunk, p.c.T);
     const int n_tiles = (int)((c1 - c0 + kRowsT - 1) / kRowsT);
     const int grp = p.grp;
-    if (n_tiles > 0) stage_tile<D>(p, seq, c0, (int)min((int64_t)kRowsT, c1 - c0), sRaw, tid);
 
     if (warp == 0) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(sTmem)),
@@ -568,10 +563,11 @@ __global__ void __launch_bounds__(kThreadsT, 1) k2v4_tc_kernel(K2V4DecodeParams 
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
     }
     if (tid == 32) {
-        for (int i = 0; i < 2; ++i)
+        for (int i = 0; i < 4; ++i)
             asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(&bars[i])), "r"(1u));
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         *sAbort = smem_u32(smem_raw) & 1023u ? 1 : 0;   // the swizzled operands need a 1024-byte base
+        if (n_tiles > 0) stage_tile<D>(p, seq, c0, (int)min((int64_t)kRowsT, c1 - c0), sRaw, &bars[2]);
     }
     if (tid < 8) {
         sM[tid] = -INFINITY;
@@ -622,15 +618,13 @@ __global__ void __launch_bounds__(kThreadsT, 1) k2v4_tc_kernel(K2V4DecodeParams 
     for (int t = 0; t < n_tiles; ++t) {
         const int64_t t0 = c0 + (int64_t)t * kRowsT;
         const int nt = (int)min((int64_t)kRowsT, c1 - t0);
-        // the next tile's bytes stream in while this one is processed
-        if (t + 1 < n_tiles) {
+        // the next tile's bytes stream in while this one is processed; its
+        // buffer was last read by tile t - 1, whose reads every thread fenced
+        // against the async proxy before the barrier that closed that tile
+        if (tid == 0 && t + 1 < n_tiles)
             stage_tile<D>(p, seq, t0 + kRowsT, (int)min((int64_t)kRowsT, c1 - t0 - kRowsT),
-                          sRaw + ((t + 1) & 1) * SM::kRawBytes, tid);
-            cp_async_wait<1>();
-        } else {
-            cp_async_wait<0>();
-        }
-        __syncthreads();
+                          sRaw + ((t + 1) & 1) * SM::kRawBytes, &bars[2 + ((t + 1) & 1)]);
+        mbar_wait(&bars[2 + (t & 1)], (uint32_t)(t >> 1) & 1u, sAbort);
         const unsigned char* raw = sRaw + (t & 1) * SM::kRawBytes;
         const unsigned char* raw_kc = raw;
         const uint16_t* raw_ks = reinterpret_cast<const uint16_t*>(raw + SM::kRawKc);
@@ -911,6 +905,11 @@ __global__ void __launch_bounds__(kThreadsT, 1) k2v4_tc_kernel(K2V4DecodeParams 
     if (n_tiles > 0) {
         volatile int never = 0;
         if (!mbar_wait(&bars[1], (uint32_t)(n_tiles - 1) & 1u, &never)) *sAbort = 1;
+        // after an abort the loop stopped waiting for its raw tiles: the
+        // bulk copies still in flight land before the CTA leaves
+        if (tid == 0)
+            for (int t = max(0, n_tiles - 2); t < n_tiles; ++t)
+                if (!mbar_wait(&bars[2 + (t & 1)], (uint32_t)(t >> 1) & 1u, &never)) *sAbort = 1;
     }
     tc_after();
     if (*sAbort) {

@@ -179,3 +179,16 @@ def test_k2v4_append_validates_before_launch(kvq):
     assert L.k2v4_append(C.byref(lay), None, d, 1, 0, 10, 64, d, d, d, d, d, None) == 1
     assert L.k2v4_append(C.byref(lay), d, d, 1, 0, 10, 64, d, d, d, None, d, None) == 1  # overlay pools
     assert L.k2v4_append(C.byref(lay), None, None, 1, 5, 0, 64, None, None, None, None, None, None) == 0
+
+
+def test_k2v4_decode_refuses_unaligned_pools(kvq):
+    """Refused on the host before any launch: a K2/V4 pool that is not 16-byte
+    aligned (the decode stages whole cell groups by 16-byte bulk copies)."""
+    L = kvq.lib()
+    lay = kvq.k2v4_layout()
+    d = C.c_void_p(256)     # dummy device addresses, never dereferenced
+    odd = C.c_void_p(264)
+    ws = C.c_void_p(4096)
+    for kc, ks, vb in ((odd, d, d), (d, odd, d), (d, d, odd)):
+        assert L.kv_attn_decode_k2v4(C.byref(lay), d, 1, 16, 64, 64, kc, ks, vb, d, d, 0.1, d, ws, 1 << 30,
+                                     kvq.PATH_TENSOR, None) == 1
