@@ -32,7 +32,8 @@
  *     sticky: it keeps the first error of any call until read with `clear`,
  *     and a decode/prefill workspace must start with it zero (allocate the
  *     workspace zeroed, or clear it once with kvq_read_device_error).
- *   - The library keeps no global state; calls on different streams with
+ *   - The library keeps no global state besides the opt-in launch timing
+ *     (kvq_timing_enable, off by default); calls on different streams with
  *     different workspaces are independent.
  *   - Encoders are bit-exact by construction: IEEE f32 arithmetic in a fixed
  *     order, no fast-math, no fused multiply-add except where the definition
@@ -276,6 +277,26 @@ kvq_status kv_attn_prefill(kvq_format fmt, const kvq_mla_layout* layout,
                            int64_t n_past, int64_t n_new, int32_t n_heads,
                            uint8_t* codes, float* scales, float sm_scale, float* out,
                            void* workspace, size_t workspace_bytes, kvq_path path, void* stream);
+
+/* Opt-in launch timing, for kernel-level rooflines (instrumentation, not part
+ * of the pages' method).  With capacity > 0, every kv_attn_decode,
+ * kv_attn_decode_append, kv_attn_decode_gather, kv_attn_prefill and
+ * kv_attn_decode_k2v4 call records three CUDA events on its stream -- before
+ * its partial kernel, before its merge, after its merge -- into the next of
+ * `capacity` slots (a ring: older calls are overwritten); capacity 0 turns it
+ * off and frees the events.  The record between the two kernels ends the
+ * merge's programmatic overlap with the partial kernel, so timed calls run a
+ * little slower than untimed ones.  Process-wide state, not thread-safe.
+ * Returns KVQ_ERR_ARG for a negative capacity, KVQ_ERR_CUDA if the events
+ * cannot be created (then timing is off). */
+kvq_status kvq_timing_enable(int32_t capacity);
+
+/* Waits for the recorded calls and returns the summed milliseconds of their
+ * partial kernels (from the first record to the second: launch to end of the
+ * partial kernel, and for the fused append the row encoding inside it) and of
+ * their merges, and how many calls were complete; then empties the ring.
+ * KVQ_ERR_ARG for a null pointer, KVQ_ERR_CUDA if an event query fails. */
+kvq_status kvq_timing_read(double* partial_ms, double* merge_ms, int32_t* n_calls);
 
 /* Reads the device error word of a decode/prefill workspace (synchronizes
  * `stream`).  Returns 0 when clear, else the kvq_status value of the first

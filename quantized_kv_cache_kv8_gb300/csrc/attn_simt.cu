@@ -443,6 +443,7 @@ cudaError_t launch_attn_simt(kvq_format fmt, const kvq_mla_layout& L, const void
     p.sel = sel;
     p.pool_rows = pool_rows;
     const int groups = (n_heads + kHG - 1) / kHG;
+    timing_mark(stream, 0);
     cudaError_t e;
     if (fmt == KVQ_KV8)
         e = qdt == KVQ_BF16 ? launch_partial<KVQ_KV8, true>(p, plan.max_items, groups, stream)
@@ -468,8 +469,11 @@ cudaError_t launch_attn_merge(kvq_format fmt, const AttnParams& p, float* out, c
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (fmt == KVQ_KV8) return cudaLaunchKernelEx(&cfg, attn_merge_kernel<KVQ_KV8>, p, out);
-    return cudaLaunchKernelEx(&cfg, attn_merge_kernel<KVQ_TQ4>, p, out);
+    timing_mark(stream, 1);
+    const cudaError_t e = fmt == KVQ_KV8 ? cudaLaunchKernelEx(&cfg, attn_merge_kernel<KVQ_KV8>, p, out)
+                                         : cudaLaunchKernelEx(&cfg, attn_merge_kernel<KVQ_TQ4>, p, out);
+    timing_mark(stream, 2);
+    return e;
 }
 
 }  // namespace kvq

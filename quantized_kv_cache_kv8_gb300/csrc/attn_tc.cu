@@ -615,6 +615,7 @@ cudaError_t launch_attn_tc(kvq_format fmt, const kvq_mla_layout& L, const void* 
     // only the KV8 / bf16-query kernel reads rows through an index table
     if (sel && !(fmt == KVQ_KV8 && qdt == KVQ_BF16)) return cudaErrorNotSupported;
     const int groups = n_heads / kHC;
+    timing_mark(stream, 0);
     cudaError_t e;
     if (fmt == KVQ_KV8)
         e = qdt == KVQ_BF16 ? launch_attn_tc_kv8_bf16(p, plan.max_items, groups, stream)
@@ -638,6 +639,7 @@ cudaError_t launch_attn_tc_kv8_append(const kvq_mla_layout& L, const float* x_ne
     p.scales_out = scales;
     p.bd0 = L.block_dim[0];
     p.bd1 = L.n_blocks > 1 ? L.block_dim[1] : 0;
+    timing_mark(stream, 0);
     const cudaError_t e = launch_attn_tc_kv8_bf16_append(p, plan.max_items, n_heads / kHC, stream);
     if (e != cudaSuccess) return e;
     return launch_attn_merge(KVQ_KV8, p, out, stream);

@@ -442,7 +442,10 @@ cudaError_t launch_k2v4_merge(const K2V4DecodeParams& p, float* out, cudaStream_
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, k2v4_merge_kernel, p, out);
+    timing_mark(stream, 1);
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, k2v4_merge_kernel, p, out);
+    timing_mark(stream, 2);
+    return e;
 }
 
 // ---------------------------------------------------------------------------
@@ -1043,6 +1046,7 @@ cudaError_t launch_k2v4_decode(const kvq_k2v4_layout& L, const float* q, int32_t
     p.ws_ml = p.ws_o + (size_t)batch * n_q_heads * plan.n_chunks * L.head_dim;
     const dim3 grid(plan.n_chunks, L.n_kv_heads, batch);
     cudaError_t e = cudaSuccess;
+    timing_mark(stream, 0);
     if (plan.tensor) {
         switch (L.head_dim) {
 #define KVQ_TC_CASE(DD)                                                                                 \

@@ -20,6 +20,10 @@ namespace kvq {
 
 constexpr unsigned kFull = 0xffffffffu;
 
+// Opt-in launch timing (timing.cu): phase 0 before a call's partial kernel,
+// 1 before its merge, 2 after it; a no-op unless kvq_timing_enable is on.
+void timing_mark(cudaStream_t stream, int phase);
+
 // N(0,1) Lloyd-Max codebooks as f32 bit patterns (levels ascending, then the
 // decision thresholds = f64 midpoints of adjacent levels rounded to f32).
 // Derived by gen_codebook.py (root finding on the centroid and midpoint

@@ -104,6 +104,10 @@ def _declare(L):
     L.kv_attn_prefill.argtypes = [C.c_int, pl, P, P, C.c_int, I64, I64, I32, P, P, C.c_float, P, P, S, C.c_int, P]
     L.kvq_read_device_error.restype = I32
     L.kvq_read_device_error.argtypes = [P, I32, P]
+    L.kvq_timing_enable.restype = C.c_int
+    L.kvq_timing_enable.argtypes = [I32]
+    L.kvq_timing_read.restype = C.c_int
+    L.kvq_timing_read.argtypes = [C.POINTER(C.c_double), C.POINTER(C.c_double), C.POINTER(I32)]
     L.k2v4_encode.restype = C.c_int
     L.k2v4_encode.argtypes = [pk, P, P, I32, I64, I64, P, P, P, P, P, P]
     L.k2v4_append.restype = C.c_int
@@ -283,6 +287,20 @@ def kv_attn_prefill(fmt: int, x_new, q, codes, scales, n_past: int, out, workspa
 
 def read_device_error(workspace, clear: bool = True, stream=None) -> int:
     return lib().kvq_read_device_error(_ptr(workspace, torch.uint8, "workspace"), int(clear), _stream(stream))
+
+
+def timing_enable(capacity: int) -> None:
+    """Opt-in launch timing of the attention calls (events before the partial
+    kernel, before and after the merge); 0 turns it off."""
+    _ok(lib().kvq_timing_enable(int(capacity)), "kvq_timing_enable")
+
+
+def timing_read() -> tuple[float, float, int]:
+    """(partial kernel ms, merge ms, calls) summed over the recorded calls;
+    waits for them and empties the record."""
+    a, b, n = C.c_double(), C.c_double(), C.c_int32()
+    _ok(lib().kvq_timing_read(C.byref(a), C.byref(b), C.byref(n)), "kvq_timing_read")
+    return a.value, b.value, n.value
 
 
 # -- K2/V4 -------------------------------------------------------------------
