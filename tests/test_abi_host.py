@@ -192,3 +192,15 @@ def test_k2v4_decode_refuses_unaligned_pools(kvq):
     for kc, ks, vb in ((odd, d, d), (d, odd, d), (d, d, odd)):
         assert L.kv_attn_decode_k2v4(C.byref(lay), d, 1, 16, 64, 64, kc, ks, vb, d, d, 0.1, d, ws, 1 << 30,
                                      kvq.PATH_TENSOR, None) == 1
+
+
+def test_timing_hook_host_side(kvq):
+    """The launch timing hook: off by default (an empty read), a negative
+    capacity and null outputs refused, capacity 0 always accepted."""
+    L = kvq.lib()
+    a, b, n = C.c_double(1.0), C.c_double(1.0), C.c_int32(7)
+    assert L.kvq_timing_read(C.byref(a), C.byref(b), C.byref(n)) == 0
+    assert (a.value, b.value, n.value) == (0.0, 0.0, 0)
+    assert L.kvq_timing_enable(-1) == 1
+    assert L.kvq_timing_read(None, C.byref(b), C.byref(n)) == 1
+    assert L.kvq_timing_enable(0) == 0
