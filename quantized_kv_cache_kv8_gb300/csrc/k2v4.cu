@@ -502,16 +502,14 @@ __device__ __forceinline__ uint32_t q4_pair(uint32_t codes2, uint32_t d2) {
     return hmul2_bits(hsub2_bits(codes2 | 0x64006400u, 0x64086408u), d2);
 }
 
-// Copies the raw bytes of the tile at cells [t0, t0 + nt), rounded up to whole
-// 32-cell groups, into `dst` with 16-byte cp.async (t0 a multiple of 32; each
-// piece is contiguous and 16-byte aligned in the cache).  One commit group per
-// call.
-// One thread stages a tile's raw bytes with three bulk copies (the TMA
-// engine, no per-thread copy instructions) that complete on the buffer's
-// mbarrier: K codes, K scales and V blocks of whole 32-cell groups.  A
-// sequence may end inside its last group (after appends); the cells past its
-// end lie inside the pool (capacities are multiples of 32, every size and
-// source offset a multiple of 16 bytes) and are masked by the caller.
+// Stages the raw bytes of the tile at cells [t0, t0 + nt), rounded up to
+// whole 32-cell groups (t0 a multiple of 32), into `dst`: one thread issues
+// three bulk copies (the TMA engine, no per-thread copy instructions) of the
+// K codes, K scales and V blocks, each contiguous in the cache, completing on
+// the buffer's mbarrier.  A sequence may end inside its last group (after
+// appends); the cells past its end lie inside the pool (capacities are
+// multiples of 32, every size and source offset a multiple of 16 bytes) and
+// are masked by the caller.
 template <int D>
 __device__ __forceinline__ void stage_tile(const K2V4DecodeParams& p, int64_t seq, int64_t t0, int nt,
                                            unsigned char* dst, uint64_t* bar) {
