@@ -1,4 +1,4 @@
-"""Derivation of the codebook constants hard-coded in ``kvq_codebooks.cuh``.
+"""Derivation of the codebook constants hard-coded in ``kvq_internal.cuh`` (kTq4LevelBits, kTq4ThreshBits, kK2LevelBits, kK2ThreshBits).
 
 The TQ4 codec uses the 16-level, and the K2 codec the 4-level, minimum-MSE
 (Lloyd-Max) quantizer of N(0,1).  The library stores them as f32 bit patterns;

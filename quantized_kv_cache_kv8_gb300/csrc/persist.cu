@@ -23,6 +23,8 @@
 //           of 512 + 64 dims, 296 for TQ4), so rows append in place
 #include "kvq_internal.cuh"
 
+#include <stdint.h>
+
 #include <stdio.h>
 #include <string.h>
 #include <unistd.h>
@@ -117,6 +119,12 @@ kvq_status read_header(FILE* f, Header* H, int64_t* file_bytes, char* msg, size_
     if (h[0] < 0 || h[1] <= 0 || (h[2] != 1 && h[2] != 2) || h[3] <= 0 || h[4] < 0 || h[3] + h[4] != h[1] ||
         (h[2] == 2) != (h[4] > 0) || h[5] <= 0 || h[5] > h[1]) {
         put_msg(msg, msg_len, "corrupt quantized cache header");
+        return KVQ_ERR_IO;
+    }
+    // sizes computed from the header stay inside int64: a row dimension of at
+    // most 2^20 and no more rows than the largest file could hold
+    if (h[1] > (int64_t(1) << 20) || h[0] > (INT64_MAX - kHeaderBytes) / payload_row_bytes(*H)) {
+        put_msg(msg, msg_len, "corrupt quantized cache header (sizes out of range)");
         return KVQ_ERR_IO;
     }
     if (fseek(f, 0, SEEK_END) != 0) return KVQ_ERR_IO;

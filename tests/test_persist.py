@@ -146,3 +146,21 @@ def test_append_in_place_and_self_heal(kvq, oracle, tmp_path):
     with pytest.raises(kvq.CacheFileError) as e:                          # appends check the mode too
         kvq.cache_append(path, TQ4, codes[:1, :288], scales[:1], lay)
     assert e.value.status == MISMATCH
+
+
+@pytest.mark.parametrize("rows", [-5, 2 ** 62, 2 ** 63 - 1])
+def test_header_row_count_out_of_range_is_refused(kvq, oracle, tmp_path, rows):
+    """A header whose row count is negative, or so large that the file size it
+    implies overflows, is refused as corrupt by every reader, never misread."""
+    codes, scales = pool(oracle, KV8, 4)
+    path = str(tmp_path / "kv.bin")
+    lay = kvq.mla_layout(seed=3)
+    kvq.cache_save(path, KV8, codes, scales, lay)
+    raw = bytearray(open(path, "rb").read())
+    raw[8:16] = np.array([rows], np.int64).tobytes()
+    open(path, "wb").write(bytes(raw))
+    for call in (lambda: kvq.cache_info(path), lambda: kvq.cache_load(path, KV8, 8, lay),
+                 lambda: kvq.cache_append(path, KV8, codes, scales, lay)):
+        with pytest.raises(kvq.CacheFileError) as e:
+            call()
+        assert e.value.status == IO
