@@ -58,7 +58,12 @@ typedef enum kvq_status {
     KVQ_ERR_UNSUPPORTED = 5,  /* valid arguments this build has no kernel for */
     KVQ_ERR_DEVICE = 6,       /* the device error word was set (see kvq_read_device_error) */
     KVQ_ERR_MISMATCH = 7,     /* cache file of another tier, codec, bit width or layout: refused */
-    KVQ_ERR_IO = 8            /* cache file missing, unreadable, corrupt or of the wrong size */
+    KVQ_ERR_IO = 8,           /* cache file missing, unreadable, corrupt or of the wrong size */
+    KVQ_ERR_NONFINITE = 9,    /* device word: an encoder met a NaN or infinite value (or an
+                                 infinite TQ4 radius); that row's codes and scale are unspecified */
+    KVQ_ERR_TIMEOUT = 10      /* device word: a bounded wait inside a kernel ran out; the kernel
+                                 drained its tensor-core work, freed its tensor memory and wrote
+                                 no result for its work item */
 } kvq_status;
 
 typedef enum kvq_format { KVQ_KV8 = 1, KVQ_TQ4 = 2 } kvq_format;
@@ -109,9 +114,15 @@ kvq_status kvq_codebook(int32_t which, float* levels, float* thresholds);
  *             sequence, each at the end of its own range)
  *   codes     pool [*][D] bytes (e4m3 bit patterns), rows written
  *   scales    pool [*][n_blocks] f32, rows written
+ *   err_word  NULL, or a device int32 error word (for instance the first 4
+ *             bytes of an attention workspace): a row holding a NaN or an
+ *             infinity sets it to KVQ_ERR_NONFINITE if it is still 0 (the
+ *             pages define no code for such values; that row's codes and
+ *             scales are then unspecified, the other rows are unaffected)
  * Any block widths with D <= 4096.  n_rows == 0 is a no-op. */
 kvq_status kv8_encode(const float* x, int64_t n_rows, const kvq_mla_layout* layout,
-                      const int64_t* dst_rows, uint8_t* codes, float* scales, void* stream);
+                      const int64_t* dst_rows, uint8_t* codes, float* scales, int32_t* err_word,
+                      void* stream);
 
 /* TQ4 (rotated-int4) encode ([P1] "Why rotated-int4 for the 4-bit tier";
  * [P2] "What's in it").  Per block of n dims (a power of two, 2..1024):
@@ -127,11 +138,15 @@ kvq_status kv8_encode(const float* x, int64_t n_rows, const kvq_mla_layout* layo
  *   dst_rows  NULL, or device int64 [n_rows] destination pool rows (as kv8_encode)
  *   packed    pool [*][D/2] bytes, rows written (block 0 first)
  *   scales    pool [*][n_blocks] f32, rows written
+ *   err_word  NULL, or a device int32 error word set to KVQ_ERR_NONFINITE
+ *             (if still 0) by a block whose sum of squares is not finite (a
+ *             NaN or infinite input, or a radius past the f32 range)
  * Returns KVQ_ERR_SHAPE for a width that is not a power of two >= 2 ([P1]
  * rebase comment and [P2] review-pass item 1: such rows would all become
  * inert, so the codec refuses). */
 kvq_status tq4_encode(const float* x, int64_t n_rows, const kvq_mla_layout* layout,
-                      const int64_t* dst_rows, uint8_t* packed, float* scales, void* stream);
+                      const int64_t* dst_rows, uint8_t* packed, float* scales, int32_t* err_word,
+                      void* stream);
 
 /* The TQ4 rotation applied to whole vectors, f32 ([P1] "Ready for review"
  * comment, finding 2: rotate the query once per head, unrotate the
@@ -244,10 +259,13 @@ kvq_status kv_attn_decode_gather(kvq_format fmt, const kvq_mla_layout* layout,
  * request whose kv_attn_workspace_size exceeds 32 MiB returns
  * KVQ_ERR_WORKSPACE and launches nothing (the scratch grows with the number
  * of sequences, not their length: 32 MiB covers 128 heads for batches of up
- * to 76 sequences (KV8) or 114 (TQ4) of any length on the tensor-core path).  The first call on each device
- * looks up the array's device address (cudaGetSymbolAddress, which may load
- * the library's device code); make that first call before any stream
- * capture.  All calls share the one array, which keeps the last call's
+ * to 76 sequences (KV8) or 114 (TQ4) of any length on the tensor-core path).
+ * The first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress, which may load the library's device code), and so
+ * does the first call after the device's context was re-created (a device
+ * reset loads the library's device code anew); make that first call before
+ * any stream capture.  Argument checks and their statuses are those of
+ * kv_attn_decode, made before the size check.  All calls share the one array, which keeps the last call's
  * contents: calls that can overlap on the GPU (other streams, other host
  * threads) race and must be serialized by the caller.  The device error word
  * of kv_attn_decode is not readable here; a ragged batch larger than
@@ -303,6 +321,28 @@ kvq_status kvq_timing_read(double* partial_ms, double* merge_ms, int32_t* n_call
  * error recorded since it was last cleared; clears it when `clear` is
  * non-zero. */
 int32_t kvq_read_device_error(void* workspace, int32_t clear, void* stream);
+
+/* Diagnostic of the tensor-core attention kernels: how many tiles after the
+ * first of a work item took the exact path of the lagged running maxima (a
+ * score passing the running reference by more than the lag: column maxima,
+ * then the context accumulator rescaled in tensor memory) since the counter
+ * was last cleared.  The counter is bytes 16..19 of a decode/prefill
+ * workspace (zero in a zeroed workspace; wraps at 2^32).  Synchronizes
+ * `stream`; clears the counter when `clear` is non-zero.  Returns -1 for a
+ * null workspace or a failed copy. */
+int64_t kvq_read_exact_rescales(void* workspace, int32_t clear, void* stream);
+
+/* Testing hook for the timeout path of the tensor-core attention kernels (the
+ * KV8, KV8 f32-query and TQ4 decode/prefill kernels).  Process-wide, not
+ * thread-safe, off by default.  With polls > 0, every later launch of those
+ * kernels first waits, for at most `polls` polls, on a barrier that nothing
+ * arrives on, and its other tile-loop waits give up after `polls` polls too:
+ * the wait runs out, the kernel leaves its tile loop, waits (with the normal
+ * bound) for the tensor-core operations it issued, frees its tensor memory
+ * and sets KVQ_ERR_TIMEOUT in the workspace's error word; no partial result
+ * of that launch is meaningful.  polls = 0 restores normal operation.
+ * Returns KVQ_ERR_ARG for a negative count. */
+kvq_status kvq_test_stall_waits(int64_t polls);
 
 /* ------------------------------------------------------------------------ */
 /* K2/V4 GQA cache with an exact FP16 window ([P3])                          */

@@ -121,6 +121,8 @@ const char* kvq_status_string(kvq_status s) {
         case KVQ_ERR_DEVICE: return "device error word set";
         case KVQ_ERR_MISMATCH: return "cache file of another tier, codec, bit width or layout: refused";
         case KVQ_ERR_IO: return "cache file missing, unreadable, corrupt or of the wrong size";
+        case KVQ_ERR_NONFINITE: return "an encoder met a NaN or infinite value (device error word)";
+        case KVQ_ERR_TIMEOUT: return "a bounded wait inside a kernel ran out (device error word)";
     }
     return "unknown status";
 }
@@ -145,23 +147,24 @@ kvq_status kvq_codebook(int32_t which, float* levels, float* thresholds) {
 }
 
 kvq_status kv8_encode(const float* x, int64_t n_rows, const kvq_mla_layout* layout, const int64_t* dst_rows,
-                      uint8_t* codes, float* scales, void* stream) {
+                      uint8_t* codes, float* scales, int32_t* err_word, void* stream) {
     kvq_status s = check_layout(layout);
     if (s != KVQ_OK) return s;
     if (n_rows < 0) return KVQ_ERR_ARG;
     if (n_rows == 0) return KVQ_OK;
     if (!x || !codes || !scales) return KVQ_ERR_ARG;
-    return cuda_status(launch_kv8_encode(x, n_rows, *layout, dst_rows, codes, scales, (cudaStream_t)stream));
+    return cuda_status(launch_kv8_encode(x, n_rows, *layout, dst_rows, codes, scales, err_word, (cudaStream_t)stream));
 }
 
 kvq_status tq4_encode(const float* x, int64_t n_rows, const kvq_mla_layout* layout, const int64_t* dst_rows,
-                      uint8_t* packed, float* scales, void* stream) {
+                      uint8_t* packed, float* scales, int32_t* err_word, void* stream) {
     kvq_status s = check_tq4_layout(layout);
     if (s != KVQ_OK) return s;
     if (n_rows < 0) return KVQ_ERR_ARG;
     if (n_rows == 0) return KVQ_OK;
     if (!x || !packed || !scales) return KVQ_ERR_ARG;
-    return cuda_status(launch_tq4_encode(x, n_rows, *layout, dst_rows, packed, scales, (cudaStream_t)stream));
+    return cuda_status(
+        launch_tq4_encode(x, n_rows, *layout, dst_rows, packed, scales, err_word, (cudaStream_t)stream));
 }
 
 kvq_status tq4_rotate(const void* in, kvq_dtype in_dtype, int64_t n_vecs, const kvq_mla_layout* layout,
@@ -261,8 +264,9 @@ kvq_status kv_attn_decode_append(kvq_format fmt, const kvq_mla_layout* layout, c
                                                      cu_seqlens, pl, sm_scale, out, workspace, st));
     }
     // other formats and paths: the encoder launch, then the decode
-    const cudaError_t e = fmt == KVQ_KV8 ? launch_kv8_encode(x_new, batch, *layout, dst_rows, codes, scales, st)
-                                         : launch_tq4_encode(x_new, batch, *layout, dst_rows, codes, scales, st);
+    int32_t* err = static_cast<int32_t*>(workspace);
+    const cudaError_t e = fmt == KVQ_KV8 ? launch_kv8_encode(x_new, batch, *layout, dst_rows, codes, scales, err, st)
+                                         : launch_tq4_encode(x_new, batch, *layout, dst_rows, codes, scales, err, st);
     if (e != cudaSuccess) return KVQ_ERR_CUDA;
     return kv_attn_decode(fmt, layout, q, q_dtype, batch, n_heads, codes, scales, cu_seqlens, max_total_rows,
                           sm_scale, out, workspace, workspace_bytes, path, stream);
@@ -357,10 +361,10 @@ kvq_status kv_attn_prefill(kvq_format fmt, const kvq_mla_layout* layout, const f
     cudaError_t e;
     if (fmt == KVQ_KV8)
         e = launch_kv8_encode(x_new, n_new, *layout, nullptr, codes + n_past * row_bytes,
-                              scales + n_past * layout->n_blocks, st);
+                              scales + n_past * layout->n_blocks, static_cast<int32_t*>(workspace), st);
     else
         e = launch_tq4_encode(x_new, n_new, *layout, nullptr, codes + n_past * row_bytes,
-                              scales + n_past * layout->n_blocks, st);
+                              scales + n_past * layout->n_blocks, static_cast<int32_t*>(workspace), st);
     if (e != cudaSuccess) return KVQ_ERR_CUDA;
     const AttnPlan pl = plan_prefill(n_past, n_new);
     if (rp == KVQ_PATH_TENSOR)
@@ -380,6 +384,23 @@ int32_t kvq_read_device_error(void* workspace, int32_t clear, void* stream) {
         if (cudaMemsetAsync(workspace, 0, sizeof(int32_t), st) != cudaSuccess) return KVQ_ERR_CUDA;
     }
     return v;
+}
+
+kvq_status kvq_test_stall_waits(int64_t polls) {
+    if (polls < 0) return KVQ_ERR_ARG;
+    kvq::set_test_stall_polls(polls);
+    return KVQ_OK;
+}
+
+int64_t kvq_read_exact_rescales(void* workspace, int32_t clear, void* stream) {
+    if (!workspace) return -1;
+    cudaStream_t st = (cudaStream_t)stream;
+    uint32_t* counter = reinterpret_cast<uint32_t*>(static_cast<char*>(workspace) + 16);
+    uint32_t v = 0;
+    if (cudaMemcpyAsync(&v, counter, sizeof v, cudaMemcpyDeviceToHost, st) != cudaSuccess) return -1;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return -1;
+    if (clear && v != 0 && cudaMemsetAsync(counter, 0, sizeof v, st) != cudaSuccess) return -1;
+    return (int64_t)v;
 }
 
 kvq_status k2v4_encode(const kvq_k2v4_layout* layout, const float* k, const float* v, int32_t batch,

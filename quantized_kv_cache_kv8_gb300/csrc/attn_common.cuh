@@ -33,6 +33,14 @@ struct AttnParams {
     float* ws_o;            // [max_items][n_heads][512]
     float* ws_ml;           // [max_items][n_heads][2]
     int32_t* err;
+    // tensor-core kernels: tiles after a chunk's first that took the exact
+    // rescale path of the lagged running maxima (a diagnostic counter in the
+    // workspace header)
+    uint32_t* exact_count;
+    // bounded waits: the tile-loop limit (try_wait polls) and the testing
+    // hook's stall (> 0: first wait on a barrier nothing arrives on)
+    int64_t wait_limit;
+    int64_t stall_polls;
     SignWords signs;
     float kn[2];
     float lv[16];

@@ -417,6 +417,9 @@ AttnParams make_attn_params(kvq_format fmt, const kvq_mla_layout& L, const void*
     char* ws = static_cast<char*>(workspace);
     p.err = reinterpret_cast<int32_t*>(ws);
     p.ws_chunk = reinterpret_cast<int64_t*>(ws + 8);
+    p.exact_count = reinterpret_cast<uint32_t*>(ws + 16);
+    p.stall_polls = test_stall_polls();
+    p.wait_limit = p.stall_polls > 0 ? p.stall_polls : kWaitLimit;
     p.ws_o = reinterpret_cast<float*>(ws + kWsHeader);
     p.ws_ml = p.ws_o + (size_t)plan.max_items * n_heads * kMlaDV;
     if (fmt == KVQ_TQ4) {

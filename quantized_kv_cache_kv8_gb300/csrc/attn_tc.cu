@@ -26,13 +26,18 @@
 // TMEM, which is why a CTA serves 64 heads and two CTAs share each chunk.
 //
 // Softmax in this layout: a thread owns one row (a TMEM lane) and 32 heads.
-// The running max per head is lagged: rows are exponentiated against the max
-// of the previous tiles and a tile takes an exact slow path (column max over
-// the tile, rescale of O^T in TMEM) only when some score exceeds that max by
-// more than 2^14 (weights and their f16 copies then stay below 2^14).  Row
-// sums are accumulated per thread and reduced across the 128 rows once per
-// chunk.  The partial state written for the merge is the
-// same as the SIMT path's, in natural-log units.
+// In log2 units, per head: m is a lagged running maximum of the scores z and
+// the row sums take p = 2^(z - m); R is the largest y = z + log2 s_L of the
+// tiles that set the references, and the context takes the f16 weight
+// w = p s_L E with E = 2^(m - R - 3) -- relative to the largest p * s_L of the
+// chunk (which weighs 2^-3), so a row whose latent scale is small keeps f16
+// precision when it carries the attention.  A tile takes an exact slow path
+// (column maxima of z and y over the tile, new m, R, E, rescale of O^T in TMEM
+// by (E_new / E_old) 2^(m_old - m_new) and of the row sums by
+// 2^(m_old - m_new)) only when some z exceeds m by more than 2^14 or a row's
+// latent scale exceeds 3.5 / max_h E (then p <= 2^14, w <= 3.5 * 2^14).  Row sums are accumulated per thread
+// and reduced across the 128 rows once per chunk.  The partial state written
+// for the merge is the SIMT path's, in natural-log units: (m, sum p, O^T / E).
 #include "tc_common.cuh"
 
 #include <algorithm>
@@ -53,9 +58,14 @@ constexpr uint32_t kQChunkBytes = 2 * kHC * 128;
 constexpr uint32_t kOffQ = 0;
 constexpr uint32_t kOffSlot = kOffQ + 9 * kQChunkBytes;
 constexpr uint32_t kOffP = kOffSlot + kSlots * kSlotBytes;
-constexpr uint32_t kOffM = kOffP + kRows * 128;
-constexpr uint32_t kOffAlpha = kOffM + kHC * 4;
-constexpr uint32_t kOffBar = kOffAlpha + kHC * 4;
+constexpr uint32_t kOffM = kOffP + kRows * 128;          // m: running max of z per head
+constexpr uint32_t kOffR = kOffM + kHC * 4;               // R: reference of z + log2 s_L
+constexpr uint32_t kOffE = kOffR + kHC * 4;               // E = 2^(m - R - 3)
+constexpr uint32_t kOffF = kOffE + kHC * 4;               // 1 / E
+constexpr uint32_t kOffAlpha = kOffF + kHC * 4;           // O^T rescale, then the row sums
+constexpr uint32_t kOffAlphaM = kOffAlpha + kHC * 4;      // row-sum rescale
+constexpr uint32_t kOffEmax = kOffAlphaM + kHC * 4;       // max E of each 32 heads
+constexpr uint32_t kOffBar = kOffEmax + 16;
 constexpr uint32_t kOffMisc = kOffBar + 16 * 8;   // abort flag, TMEM base, residual flag, item info, reductions
 constexpr uint32_t kSmemUsed = kOffMisc + 160;
 constexpr size_t kSmemAlloc = kSmemUsed;          // the base is 1024-aligned (checked at run time)
@@ -66,8 +76,11 @@ static_assert(kSmemAlloc <= 232448, "shared memory budget");
 constexpr uint32_t kColO = 0, kColSL = 256, kColSR = 384, kTmemCols = 512;
 
 // mbarriers: slot full (256 worker arrivals), slot empty (MMA commit), score
-// done, context done (MMA commits), P^T ready (256 worker arrivals)
-enum { kBarFull0 = 0, kBarEmpty0 = 4, kBarScore = 8, kBarCtx = 9, kBarP = 10, kNumBars = 11 };
+// done, context done (MMA commits), P^T ready (256 worker arrivals), every MMA
+// of the CTA complete (the MMA warp's last commit, also after an abort), and
+// one that nothing arrives on (the testing hook's stall)
+enum { kBarFull0 = 0, kBarEmpty0 = 4, kBarScore = 8, kBarCtx = 9, kBarP = 10, kBarDone = 11, kBarNever = 12,
+       kNumBars = 13 };
 
 using namespace tc;
 constexpr uint32_t kIdescScore = idesc_f16(128, kHC, false, false);
@@ -135,7 +148,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnParams p) {
     unsigned char* sSlot = sm + kOffSlot;
     unsigned char* sP = sm + kOffP;
     float* sM = reinterpret_cast<float*>(sm + kOffM);
+    float* sR = reinterpret_cast<float*>(sm + kOffR);
+    float* sE = reinterpret_cast<float*>(sm + kOffE);
+    float* sF = reinterpret_cast<float*>(sm + kOffF);
+    float* sEmax = reinterpret_cast<float*>(sm + kOffEmax);
     float* sAlpha = reinterpret_cast<float*>(sm + kOffAlpha);
+    float* sAlphaM = reinterpret_cast<float*>(sm + kOffAlphaM);
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kOffBar);
     volatile int* sAbort = reinterpret_cast<volatile int*>(sm + kOffMisc);
     uint32_t* sTmem = reinterpret_cast<uint32_t*>(sm + kOffMisc + 4);
@@ -184,7 +202,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnParams p) {
         *sAbort = 0;
         *sHasLo = 0;
     }
-    if (tid < kHC) sM[tid] = -INFINITY;
+    if (tid < kHC) {
+        sM[tid] = -INFINITY;
+        sR[tid] = -INFINITY;
+        sE[tid] = 0.0f;
+        sF[tid] = 0.0f;
+    }
 
     const int wt = tid < kWorkers ? tid : 0;
     int64_t step = 0;
@@ -206,8 +229,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnParams p) {
     constexpr int kQVec = 4;                               // f32 values per 16-byte load
     constexpr int kQLoads = kHC * kMlaD / kQVec;           // 16-byte loads covering the 64 heads
     // largest |q| (with the bound 24 max|q| >= ||q|| that the other kernels
-    // use for rotated queries) and the largest latent scale of the chunk
-    float qmax = 0.0f, smax = 0.0f;
+    // use for rotated queries)
+    float qmax = 0.0f;
     if (tid < kWorkers) {
         const uint4* qv = reinterpret_cast<const uint4*>(reinterpret_cast<const float*>(p.q) + qbase);
         constexpr int kPer = kQLoads / kWorkers;           // 36: all in flight at once
@@ -224,30 +247,18 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnParams p) {
                 for (int k = 0; k < 4; ++k) qmax = fmaxf(qmax, fabsf(__uint_as_float(in[k])));
             }
         }
-        for (int64_t r = row0 + tid; r < row1; r += kWorkers) smax = fmaxf(smax, p.scales[r * p.n_blocks]);
         qmax = warp_max(qmax);
-        smax = warp_max(smax);
-        if (lane == 0) {
-            sRed[warp] = qmax;
-            sRed[8 + warp] = smax;
-        }
+        if (lane == 0) sRed[warp] = qmax;
     }
     tc_before();
     __syncthreads();
     tc_after();
-    float q_max = 0.0f, s_max = 0.0f;
-    for (int i = 0; i < 8; ++i) {
-        q_max = fmaxf(q_max, sRed[i]);
-        s_max = fmaxf(s_max, sRed[8 + i]);
-    }
+    float q_max = 0.0f;
+    for (int i = 0; i < 8; ++i) q_max = fmaxf(q_max, sRed[i]);
     const float q_bound = 24.0f * q_max;
-    int e_s = 0, e_q = 0;
-    if (s_max > 0.0f) frexpf(s_max, &e_s);
+    int e_q = 0;
     if (q_bound > 0.0f) frexpf(q_bound, &e_q);
-    // context weights p * s_L / S_ref stay within f16 range; queries scaled so
-    // every f16 element stays below 2^14
-    const float s_ref = s_max > 0.0f ? ldexpf(1.0f, e_s) : 1.0f;
-    const float inv_s_ref = s_max > 0.0f ? ldexpf(1.0f, -e_s) : 1.0f;
+    // queries scaled so every f16 element stays below 2^14
     const float q_scale = q_bound > 0.0f ? ldexpf(1.0f, 14 - e_q) : 1.0f;
     const float cz = p.sm_scale * kLog2e * (q_bound > 0.0f ? ldexpf(1.0f, e_q - 14) : 1.0f);
     const uint32_t tmem = *sTmem;
@@ -300,10 +311,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnParams p) {
             constexpr uint64_t kQStep = kQChunkBytes >> 4, kSlotStep = kSlotBytes >> 4;
             uint32_t fills[kSlots] = {0u, 0u, 0u, 0u};
             bool o_init = false, ok = true;
+            if (p.stall_polls > 0) ok = mbar_wait(&bars[kBarNever], 0u, sAbort, p.stall_polls);
             for (int tile = 0; tile < n_tiles && ok; ++tile) {
                 for (int kc = 0; kc < 9 && ok; ++kc) {
                     const int s = kc & 3;
-                    ok = mbar_wait(&bars[kBarFull0 + s], fills[s] & 1, sAbort);
+                    ok = mbar_wait(&bars[kBarFull0 + s], fills[s] & 1, sAbort, p.wait_limit);
                     ++fills[s];
                     tc_after();
                     const uint32_t d = tmem + (kc < 8 ? kColSL : kColSR);
@@ -314,12 +326,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnParams p) {
                     umma_commit(&bars[kBarEmpty0 + s]);
                     if (kc == 8) umma_commit(&bars[kBarScore]);
                 }
-                ok = ok && mbar_wait(&bars[kBarP], tile & 1, sAbort);
+                ok = ok && mbar_wait(&bars[kBarP], tile & 1, sAbort, p.wait_limit);
                 tc_after();
                 for (int db = 0; db < 4 && ok; ++db) {
                     const int s0 = (db & 1) * 2;
-                    ok = mbar_wait(&bars[kBarFull0 + s0], fills[s0] & 1, sAbort) &&
-                         mbar_wait(&bars[kBarFull0 + s0 + 1], fills[s0 + 1] & 1, sAbort);
+                    ok = mbar_wait(&bars[kBarFull0 + s0], fills[s0] & 1, sAbort, p.wait_limit) &&
+                         mbar_wait(&bars[kBarFull0 + s0 + 1], fills[s0 + 1] & 1, sAbort, p.wait_limit);
                     ++fills[s0];
                     ++fills[s0 + 1];
                     tc_after();
@@ -334,6 +346,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnParams p) {
                 }
                 o_init = true;
             }
+            umma_commit(&bars[kBarDone]);
         }
         return;
     }
@@ -348,6 +361,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnParams p) {
     uint32_t uses[kSlots] = {0u, 0u, 0u, 0u};
     bool o_init = false;
     int tile = 0;
+    float s_lim = 0.0f;   // latent scales above this take the exact path (3.5 / max_h E)
 
     for (; tile < n_tiles; ++tile) {
         if (worker_any(*sAbort != 0)) break;
@@ -368,7 +382,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnParams p) {
         // ---- score chunks: 9 chunks of 64 dims (8 latent, 1 rope) ----
         for (int kc = 0; kc < 9; ++kc) {
             const int s = kc & 3;
-            if (uses[s] > 0) mbar_wait(&bars[kBarEmpty0 + s], (uses[s] - 1) & 1, sAbort);
+            if (uses[s] > 0) mbar_wait(&bars[kBarEmpty0 + s], (uses[s] - 1) & 1, sAbort, p.wait_limit);
             RawChunk rc;
             KVQ_NEXT_CHUNK(rc);
             store_chunk(rc, valid, sSlot + s * kSlotBytes, tid);
@@ -377,8 +391,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnParams p) {
             ++uses[s];
         }
         // ---- softmax of the tile (thread = row, 32 heads) ----
-        mbar_wait(&bars[kBarScore], tile & 1, sAbort);
-        if (tile > 0) mbar_wait(&bars[kBarCtx], (tile - 1) & 1, sAbort);
+        mbar_wait(&bars[kBarScore], tile & 1, sAbort, p.wait_limit);
+        if (tile > 0) mbar_wait(&bars[kBarCtx], (tile - 1) & 1, sAbort, p.wait_limit);
         tc_after();
         float z[32];
         {
@@ -411,31 +425,57 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnParams p) {
                 for (int j = 0; j < 16; ++j) z[16 * c + j] = row_ok ? fmaf(fl[j], a, fr[j] * bb) : -INFINITY;
             }
         }
-        bool flag = false;
+        bool flag = my_sl > s_lim;
 #pragma unroll
         for (int j = 0; j < 32; ++j) flag |= z[j] > sM[32 * hq + j] + 14.0f;
         if (worker_any(flag)) {
-            // exact column max of the tile, new running max, rescale factors
-            float* zbuf = reinterpret_cast<float*>(sSlot);   // 128 x 64 f32 over slots 0-1 (idle now)
+            const float ls = my_sl > 0.0f ? __log2f(my_sl) : -INFINITY;   // -inf: an inert latent block
+            // exact column maxima of z and of y = z + log2 s_L over the tile,
+            // new running maxima, rescale factors
+            float* zbuf = reinterpret_cast<float*>(sSlot);                   // 128 x 64 f32, slots 0-1
+            float* ybuf = reinterpret_cast<float*>(sSlot + 2 * kSlotBytes);  // slots 2-3 (all idle now)
 #pragma unroll
-            for (int j = 0; j < 32; ++j) zbuf[srow * kHC + 32 * hq + j] = z[j];
+            for (int j = 0; j < 32; ++j) {
+                zbuf[srow * kHC + 32 * hq + j] = z[j];
+                ybuf[srow * kHC + 32 * hq + j] = z[j] + ls;
+            }
             worker_sync();
             {
                 const int col = tid & (kHC - 1), quarter = tid >> 6;
-                float cm = -INFINITY;
+                float cm = -INFINITY, cy = -INFINITY;
 #pragma unroll 8
-                for (int r = 32 * quarter; r < 32 * quarter + 32; ++r) cm = fmaxf(cm, zbuf[r * kHC + col]);
+                for (int r = 32 * quarter; r < 32 * quarter + 32; ++r) {
+                    cm = fmaxf(cm, zbuf[r * kHC + col]);
+                    cy = fmaxf(cy, ybuf[r * kHC + col]);
+                }
                 float* part = reinterpret_cast<float*>(sP);   // P^T is rewritten after this
                 part[quarter * kHC + col] = cm;
+                part[4 * kHC + quarter * kHC + col] = cy;
                 worker_sync();
                 if (tid < kHC) {
+                    const float* py = part + 4 * kHC;
                     const float c4 = fmaxf(fmaxf(part[tid], part[kHC + tid]), fmaxf(part[2 * kHC + tid], part[3 * kHC + tid]));
+                    const float y4 = fmaxf(fmaxf(py[tid], py[kHC + tid]), fmaxf(py[2 * kHC + tid], py[3 * kHC + tid]));
                     const float mo = sM[tid], mn = fmaxf(mo, c4);
-                    sAlpha[tid] = mo == -INFINITY ? 0.0f : exp2f(mo - mn);
+                    const float ro = sR[tid], rn = fmaxf(ro, y4);
+                    const float dn = fminf(mn - rn - 3.0f, 120.0f), d_old = fminf(mo - ro - 3.0f, 120.0f);
+                    sAlphaM[tid] = mo == -INFINITY ? 0.0f : exp2f(mo - mn);
+                    sAlpha[tid] = ro == -INFINITY ? 0.0f : exp2f(dn - d_old + (mo - mn));
                     sM[tid] = mn;
+                    sR[tid] = rn;
+                    const float e = rn == -INFINITY ? 0.0f : exp2f(dn);   // R = -inf: only inert latent blocks
+                    sE[tid] = e;
+                    sF[tid] = rn == -INFINITY ? 0.0f : exp2f(-dn);
+                    const float em = warp_max(e);
+                    if ((tid & 31) == 0) sEmax[tid >> 5] = em;
+                    if (tile > 0 && tid == 0) atomicAdd(p.exact_count, 1u);
                 }
             }
             worker_sync();
+            {
+                const float em = fmaxf(sEmax[0], sEmax[1]);
+                s_lim = em > 0.0f ? 3.5f / em : 0.0f;
+            }
             if (o_init) {
 #pragma unroll 1
                 for (int bi = 0; bi < 2; ++bi)
@@ -452,10 +492,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnParams p) {
                 tmem_wait_st();
             }
 #pragma unroll
-            for (int j = 0; j < 32; ++j) lsum[j] *= sAlpha[32 * hq + j];
+            for (int j = 0; j < 32; ++j) lsum[j] *= sAlphaM[32 * hq + j];
         }
         {
-            const float wrow = my_sl * inv_s_ref;
+            // row-sum weights p = 2^(z - m), f16 context weights w = p s_L E
             uint32_t pk[16];
 #pragma unroll
             for (int j = 0; j < 32; j += 2) {
@@ -463,7 +503,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnParams p) {
                 const float p1 = exp2f(z[j + 1] - sM[32 * hq + j + 1]);
                 lsum[j] += p0;
                 lsum[j + 1] += p1;
-                const __half2 h2 = __floats2half2_rn(p0 * wrow, p1 * wrow);
+                const __half2 h2 = __floats2half2_rn(p0 * sE[32 * hq + j] * my_sl, p1 * sE[32 * hq + j + 1] * my_sl);
                 pk[j / 2] = *reinterpret_cast<const uint32_t*>(&h2);
             }
             // slow path: every column max must be read before P^T overwrites the partials
@@ -479,8 +519,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnParams p) {
         // ---- context chunks: 4 blocks of 128 dims (2 chunks each) ----
         for (int db = 0; db < 4; ++db) {
             const int s0 = (db & 1) * 2;
-            if (uses[s0] > 0) mbar_wait(&bars[kBarEmpty0 + s0], (uses[s0] - 1) & 1, sAbort);
-            if (uses[s0 + 1] > 0) mbar_wait(&bars[kBarEmpty0 + s0 + 1], (uses[s0 + 1] - 1) & 1, sAbort);
+            if (uses[s0] > 0) mbar_wait(&bars[kBarEmpty0 + s0], (uses[s0] - 1) & 1, sAbort, p.wait_limit);
+            if (uses[s0 + 1] > 0) mbar_wait(&bars[kBarEmpty0 + s0 + 1], (uses[s0 + 1] - 1) & 1, sAbort, p.wait_limit);
             RawChunk r0c, r1c;
             KVQ_NEXT_CHUNK(r0c);
             KVQ_NEXT_CHUNK(r1c);
@@ -497,7 +537,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnParams p) {
 #undef KVQ_NEXT_CHUNK
 
     // ---- epilogue: row sums, O^T -> partial state ----
-    if (tile > 0) mbar_wait(&bars[kBarCtx], (tile - 1) & 1, sAbort);
+    {
+        // bounded, and not cut short by the abort flag: TMEM is released only
+        // after the MMAs in flight have completed
+        volatile int never = 0;
+        if (!mbar_wait(&bars[kBarDone], 0u, &never)) *sAbort = 1;
+    }
     tc_after();
     {
         float* lbuf = reinterpret_cast<float*>(sSlot);
@@ -515,9 +560,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnParams p) {
         if (tid < kHC) sAlpha[tid] = (part[tid] + part[kHC + tid]) + (part[2 * kHC + tid] + part[3 * kHC + tid]);
         worker_sync();
     }
-    const bool aborted = *sAbort != 0 || tile < n_tiles;
+    const bool aborted = worker_any(*sAbort != 0 || tile < n_tiles);
     if (aborted) {
-        if (tid == 0) set_err(p.err, KVQ_ERR_DEVICE);
+        if (tid == 0) set_err(p.err, KVQ_ERR_TIMEOUT);
     } else {
         const int64_t unit = blockIdx.x;
         const int64_t item = unit / (p.n_heads / kHC);
@@ -535,7 +580,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnParams p) {
                 for (int j = 0; j < 32; ++j) {
                     const int h = hbase + 32 * c + j;
                     p.ws_o[(item * p.n_heads + h) * kMlaDV + dim] =
-                        o_init ? __uint_as_float(v[j]) * s_ref : 0.0f;
+                        o_init ? __uint_as_float(v[j]) * sF[32 * c + j] : 0.0f;
                 }
             }
         }

@@ -36,8 +36,19 @@
 //
 // The row scales factor out of both sums ([P2] "What's in it"; [P1] "Ready for
 // review" comment, finding 2): z = sm * (s_L * S_L + s_R * S_R), and the
-// context weight is p * s_L (divided by a power of two S_ref that keeps it in
-// f16 range and multiplied back in the epilogue).
+// context weight of row t is p_t * s_L,t.  In log2 units, per head: m is a
+// lagged running maximum of the scores and the row sums take p = 2^(z - m);
+// R is the largest y = z + log2 s_L of the tiles that set the references, and
+// the context takes the f16 weight w = p * s_L * E with E = 2^(m - R - 3):
+// weights relative to the largest p * s_L (which weighs 2^-3), so rows whose
+// latent scale is small keep f16 precision whenever they carry the attention.
+// A tile takes the exact path when a score passes m by more than 2^14 or a
+// row's latent scale passes 3.5 / max_h E (about 28 times the scale of the
+// row that set a head's reference); below both, p <= 2^14 and
+// w <= 3.5 * 2^14 < 65504, the f16 maximum.  The exact path takes the column
+// maxima of z and y over the tile, sets m, R and E, and rescales O^T in TMEM
+// by (E_new / E_old) 2^(m_old - m_new) and the row sums by 2^(m_old - m_new).
+// The partial state is (m, sum p, O^T / E).
 #include "tc_common.cuh"
 
 #include <math.h>
@@ -56,10 +67,15 @@ constexpr uint32_t kSlotBytes = kRows * 128;       // 128 rows x 64 f16
 constexpr uint32_t kQChunkBytes = kHC * 128;       // 64 heads x 64 f16
 constexpr uint32_t kOffQ = 0;
 constexpr uint32_t kOffSlot = kOffQ + kChunks * kQChunkBytes;
-constexpr uint32_t kOffM = kOffSlot + kChunks * kSlotBytes;
-constexpr uint32_t kOffAlpha = kOffM + kHC * 4;
-constexpr uint32_t kOffRed = kOffAlpha + kHC * 4;   // 4 quadrants x 64 heads of f32
-constexpr uint32_t kOffBar = kOffRed + 4 * kHC * 4;
+constexpr uint32_t kOffM = kOffSlot + kChunks * kSlotBytes;   // m: running max of z per head
+constexpr uint32_t kOffR = kOffM + kHC * 4;                    // R: reference of z + log2 s_L
+constexpr uint32_t kOffE = kOffR + kHC * 4;                    // E = 2^(m - R - kHeadroom)
+constexpr uint32_t kOffF = kOffE + kHC * 4;                    // 1 / E
+constexpr uint32_t kOffAlpha = kOffF + kHC * 4;                // O^T rescale, then the row sums
+constexpr uint32_t kOffAlphaM = kOffAlpha + kHC * 4;           // row-sum rescale 2^(m_old - m_new)
+constexpr uint32_t kOffEmax = kOffAlphaM + kHC * 4;            // max E of each 32 heads
+constexpr uint32_t kOffRed = kOffEmax + 16;   // 2 x 4 quadrants x 64 heads of f32
+constexpr uint32_t kOffBar = kOffRed + 2 * 4 * kHC * 4;
 constexpr uint32_t kOffMisc = kOffBar + 16 * 8;      // abort flag, TMEM base, item info
 constexpr uint32_t kOffNew = kOffMisc + 32;          // appended row: 576 codes, 2 scales, row index
 constexpr uint32_t kOffRowIdx = kOffNew + 576 + 16;   // gather: pool rows of 2 tiles (int64)
@@ -74,12 +90,18 @@ constexpr uint32_t kColO = 0, kColSL = 256, kColSR = 320, kTmemCols = 512;
 // C = the rope chunk), slot pair db released by the context (MMA commit; the
 // last pair also releases the rope/P^T slot), score complete (MMA commit), P^T
 // written (256 arrivals), every MMA of the CTA complete (the MMA warp's last
-// commit, also after an abort)
-enum { kBarFull0 = 0, kBarFree0 = 3, kBarScore = 7, kBarP = 8, kBarDone = 9, kNumBars = 10 };
+// commit, also after an abort), and one that nothing arrives on (the testing
+// hook's stall)
+enum { kBarFull0 = 0, kBarFree0 = 3, kBarScore = 7, kBarP = 8, kBarDone = 9, kBarNever = 10, kNumBars = 11 };
 
-// The running max may lag the true one by up to 2^14: softmax weights stay
-// below 2^14 and their f16 copies (times s_L / S_ref <= 1) below 65504.
+// A score may pass m by up to 2^14 without the exact path (p <= 2^14), a
+// latent scale up to 3.5 / max_h E (w <= 3.5 * 2^14); the largest p * s_L of a
+// reference tile weighs 2^-kHeadroom; log2 E is capped so that E and 1 / E
+// stay finite in f32 (any E is exact: the epilogue divides it out).
 constexpr float kLagLog2 = 14.0f;
+constexpr float kScaleLim = 3.5f;
+constexpr float kHeadroom = 3.0f;
+constexpr float kLogEmax = 120.0f;
 
 constexpr uint32_t kIdescScore = idesc_f16(128, kHC, false, false);
 constexpr uint32_t kIdescCtx = idesc_f16(128, kHC, true, true);
@@ -163,8 +185,93 @@ __device__ __forceinline__ float warp_columns(float (&v)[32], int lane) {
     return v[0];
 }
 
+// The exact path of a tile (see the top of the file), by every worker thread
+// with its row's scores in TMEM: column maxima of z and of y = z + log2 s_L
+// over the tile (16 heads at a time, straight from TMEM), new m, R and E per
+// head, the rescale of O^T in TMEM after the first tile; returns this thread's
+// row sum rescaled.  Out of line: the path is rare, and kept out of the tile
+// loop it leaves the loop's registers alone.
+__device__ __noinline__ float exact_path(unsigned char* sm, uint32_t tmem, uint32_t lane_base, int hq, bool row_ok,
+                                         float za, float zb, float my_sl, int lane, int warp, int tid, int t,
+                                         uint32_t* exact_count, float lcol) {
+    float* sM = reinterpret_cast<float*>(sm + kOffM);
+    float* sR = reinterpret_cast<float*>(sm + kOffR);
+    float* sE = reinterpret_cast<float*>(sm + kOffE);
+    float* sF = reinterpret_cast<float*>(sm + kOffF);
+    float* sAlpha = reinterpret_cast<float*>(sm + kOffAlpha);
+    float* sAlphaM = reinterpret_cast<float*>(sm + kOffAlphaM);
+    float* sEmax = reinterpret_cast<float*>(sm + kOffEmax);
+    float* sRed = reinterpret_cast<float*>(sm + kOffRed);
+            // exact column maxima of z and of y = z + log2 s_L over the tile
+            {
+                float v[32];
+                auto load_v = [&](float add) {
+#pragma unroll
+                    for (int c = 0; c < 2; ++c) {
+                        uint32_t s16[16];
+                        tmem_ld16(tmem + lane_base + kColSR + 32 * hq + 16 * c, s16);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) v[16 * c + j] = __uint_as_float(s16[j]) * zb;
+                        tmem_ld16(tmem + lane_base + kColSL + 32 * hq + 16 * c, s16);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int j = 0; j < 16; ++j)
+                            v[16 * c + j] = row_ok ? fmaf(__uint_as_float(s16[j]), za, v[16 * c + j]) + add : -INFINITY;
+                    }
+                };
+                load_v(0.0f);
+                sRed[(warp & 3) * kHC + 32 * hq + lane] = warp_columns<true>(v, lane);
+                load_v(my_sl > 0.0f ? __log2f(my_sl) : -INFINITY);   // -inf: an inert latent block
+                sRed[4 * kHC + (warp & 3) * kHC + 32 * hq + lane] = warp_columns<true>(v, lane);
+            }
+            worker_sync();
+            if (tid < kHC) {
+                const float* ry = sRed + 4 * kHC;
+                const float c4 = fmaxf(fmaxf(sRed[tid], sRed[kHC + tid]), fmaxf(sRed[2 * kHC + tid], sRed[3 * kHC + tid]));
+                const float y4 = fmaxf(fmaxf(ry[tid], ry[kHC + tid]), fmaxf(ry[2 * kHC + tid], ry[3 * kHC + tid]));
+                const float mo = sM[tid], mn = fmaxf(mo, c4);
+                const float ro = sR[tid], rn2 = fmaxf(ro, y4);
+                // log2 E = m - R - kHeadroom (capped); R = -inf: every row so far
+                // has an inert latent block (E = 0 keeps their weights 0 and
+                // makes any later latent scale take this path)
+                const float dn = fminf(mn - rn2 - kHeadroom, kLogEmax), d_old = fminf(mo - ro - kHeadroom, kLogEmax);
+                sAlphaM[tid] = mo == -INFINITY ? 0.0f : ex2(mo - mn);
+                // O^T holds sum p s_L E c: rescaled by (E_new / E_old) 2^(m_old - m_new)
+                sAlpha[tid] = ro == -INFINITY ? 0.0f : ex2(dn - d_old + (mo - mn));
+                sM[tid] = mn;
+                sR[tid] = rn2;
+                const float e = rn2 == -INFINITY ? 0.0f : ex2(dn);
+                sE[tid] = e;
+                sF[tid] = rn2 == -INFINITY ? 0.0f : ex2(-dn);
+                const float em = warp_max(rn2 == -INFINITY ? INFINITY : e);
+                if (lane == 0) sEmax[tid >> 5] = em;
+                if (t > 0 && tid == 0) atomicAdd(exact_count, 1u);
+            }
+            worker_sync();
+            if (t > 0) {
+                // O^T is stable: the score commit of this tile follows every
+                // context MMA of the previous one
+#pragma unroll 1
+                for (int bi = 0; bi < 2; ++bi)
+#pragma unroll 1
+                    for (int c = 0; c < 2; ++c) {
+                        const uint32_t ta = tmem + lane_base + kColO + 64 * (2 * hq + bi) + 32 * c;
+                        uint32_t o[32];
+                        tmem_ld32(ta, o);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * sAlpha[32 * c + j]);
+                        tmem_st32(ta, o);
+                    }
+                tmem_wait_st();
+            }
+    return lcol * sAlphaM[32 * hq + lane];
+}
+
 template <bool APPEND, bool GATHER>
 __global__ void __launch_bounds__(kThreads, 1) attn_tc_kv8_kernel(AttnParams p) {
+    const int64_t wl = p.wait_limit;
     launch_dependents();
     const int64_t w = blockIdx.x;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -173,7 +280,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kv8_kernel(AttnParams p) 
     unsigned char* sSlot = sm + kOffSlot;
     unsigned char* sP = sSlot + kRope * kSlotBytes;
     float* sM = reinterpret_cast<float*>(sm + kOffM);
+    float* sR = reinterpret_cast<float*>(sm + kOffR);
+    float* sE = reinterpret_cast<float*>(sm + kOffE);
+    float* sF = reinterpret_cast<float*>(sm + kOffF);
     float* sAlpha = reinterpret_cast<float*>(sm + kOffAlpha);
+    float* sEmax = reinterpret_cast<float*>(sm + kOffEmax);
     float* sRed = reinterpret_cast<float*>(sm + kOffRed);
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kOffBar);
     volatile int* sAbort = reinterpret_cast<volatile int*>(sm + kOffMisc);
@@ -235,7 +346,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kv8_kernel(AttnParams p) 
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         *sAbort = 0;
     }
-    if (tid < kHC) sM[tid] = -INFINITY;
+    if (tid < kHC) {
+        sM[tid] = -INFINITY;
+        sR[tid] = -INFINITY;
+        sE[tid] = 0.0f;
+        sF[tid] = 0.0f;
+        if (tid < kHC / 32) sEmax[tid] = INFINITY;
+    }
     if (!GATHER && tid == 0) {
         const int64_t n = min((int64_t)kRows, row1 - row0);
         prefetch_l2(p.codes + row0 * kMlaD, (uint32_t)(n * kMlaD));
@@ -256,7 +373,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kv8_kernel(AttnParams p) 
                 if ((d < s0 || d >= s1) && row0 == s0 && group == 0) set_err(p.err, KVQ_ERR_ARG);
             }
             if (rn >= 0) {
-                kv8_encode_row_warp(p.x_new + (int64_t)b * kMlaD, p.n_blocks, p.bd0, p.bd1, sNew, sNewScale, lane);
+                kv8_encode_row_warp(p.x_new + (int64_t)b * kMlaD, p.n_blocks, p.bd0, p.bd1, sNew, sNewScale, lane,
+                                    group == 0 ? p.err : nullptr);
                 __syncwarp();
                 if (group == 0) {
                     for (int i = lane; i < kMlaD / 16; i += 32)
@@ -268,19 +386,16 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kv8_kernel(AttnParams p) 
     }
 
     // ---- query: 64 heads x 576 bf16, 18 16-byte loads per worker held in
-    // registers; largest |q| and largest latent scale of the chunk ----
+    // registers; largest |q| ----
     const int64_t qbase = ((int64_t)b * p.n_heads + hbase) * kMlaD;
     constexpr int kQPer = kHC * kMlaD / 8 / kWorkers;   // 18
     static_assert(kHC * kMlaD / 8 == kQPer * kWorkers, "query loads per worker");
     uint4 qraw[kQPer];
     if (tid < kWorkers) {
         const uint4* qv = reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(p.q) + qbase);
-        float qmax = 0.0f, smax = 0.0f;
+        float qmax = 0.0f;
 #pragma unroll
         for (int i = 0; i < kQPer; ++i) qraw[i] = __ldg(qv + tid + i * kWorkers);
-#pragma unroll 4
-        for (int64_t r = row0 + tid; r < row1; r += kWorkers)
-            if (!APPEND || r != rn) smax = fmaxf(smax, p.scales[(GATHER ? gather_row(p, r) : r) * p.n_blocks]);
 #pragma unroll
         for (int i = 0; i < kQPer; ++i) {
             const uint32_t in[4] = {qraw[i].x, qraw[i].y, qraw[i].z, qraw[i].w};
@@ -291,29 +406,18 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kv8_kernel(AttnParams p) 
             }
         }
         qmax = warp_max(qmax);
-        smax = warp_max(smax);
-        if (lane == 0) {
-            sRed[warp] = qmax;
-            sRed[8 + warp] = smax;
-        }
+        if (lane == 0) sRed[warp] = qmax;
     }
     __syncthreads();
-    float q_max = 0.0f, s_max = 0.0f;
+    float q_max = 0.0f;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        q_max = fmaxf(q_max, sRed[i]);
-        s_max = fmaxf(s_max, sRed[8 + i]);
-    }
-    if (APPEND && rn >= 0) s_max = fmaxf(s_max, sNewScale[0]);
-    int e_s = 0, e_q = 0;
-    if (s_max > 0.0f) frexpf(s_max, &e_s);
+    for (int i = 0; i < 8; ++i) q_max = fmaxf(q_max, sRed[i]);
+    int e_q = 0;
     if (q_max > 0.0f) frexpf(q_max, &e_q);
     // |q| * q_scale < 2^14: every product with a code (|c| <= 448) and every
     // 576-term sum stays finite in f32, and a bf16 value scaled by a power of
     // two is exact in f16 unless it is below 2^-17 of the scaled maximum range
     // (its residual, under 2^-24 after scaling, is dropped)
-    const float s_ref = s_max > 0.0f ? ldexpf(1.0f, e_s) : 1.0f;
-    const float inv_s_ref = s_max > 0.0f ? ldexpf(1.0f, -e_s) : 1.0f;
     const float q_scale = q_max > 0.0f ? ldexpf(1.0f, 14 - e_q) : 1.0f;
     const float cz = p.sm_scale * kLog2e * (q_max > 0.0f ? ldexpf(1.0f, e_q - 14) : 1.0f);
 
@@ -349,12 +453,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kv8_kernel(AttnParams p) 
             const uint64_t dp = umma_desc(smem_u32(sP), kSlotBytes, 1024);
             constexpr uint64_t kQStep = kQChunkBytes >> 4, kSlotStep = kSlotBytes >> 4;
             bool ok = true;
+            if (p.stall_polls > 0) ok = mbar_wait(&bars[kBarNever], 0u, sAbort, p.stall_polls);
             for (int t = 0; t < n_tiles && ok; ++t) {
                 const uint32_t par = (uint32_t)t & 1u;
 #pragma unroll 1
                 for (int kc = 0; kc < kChunks && ok; ++kc) {
                     if ((kc & 3) == 0) {
-                        ok = mbar_wait(&bars[kBarFull0 + (kc >> 2)], par, sAbort);
+                        ok = mbar_wait(&bars[kBarFull0 + (kc >> 2)], par, sAbort, wl);
                         tc_after();
                     }
                     const uint32_t d = tmem + (kc < kRope ? kColSL : kColSR);
@@ -365,7 +470,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kv8_kernel(AttnParams p) 
                         umma_f16(d, a + 2 * ks, bq + 2 * ks, kIdescScore, (first && ks == 0) ? 0u : 1u);
                 }
                 umma_commit(&bars[kBarScore]);
-                ok = ok && mbar_wait(&bars[kBarP], par, sAbort);
+                ok = ok && mbar_wait(&bars[kBarP], par, sAbort, wl);
                 tc_after();
 #pragma unroll 1
                 for (int db = 0; db < 4 && ok; ++db) {
@@ -432,8 +537,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kv8_kernel(AttnParams p) 
 #pragma unroll
             for (int g = 0; g < 2; ++g) {
                 if (t > 0) {
-                    mbar_wait(&bars[kBarFree0 + 2 * g], prev, sAbort);
-                    mbar_wait(&bars[kBarFree0 + 2 * g + 1], prev, sAbort);
+                    mbar_wait(&bars[kBarFree0 + 2 * g], prev, sAbort, wl);
+                    mbar_wait(&bars[kBarFree0 + 2 * g + 1], prev, sAbort, wl);
                 }
                 unsigned char* slot = sSlot + (4 * g + cg) * kSlotBytes;
 #pragma unroll
@@ -455,7 +560,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kv8_kernel(AttnParams p) 
         if (!GATHER && t + 1 < n_tiles) load_group<APPEND, GATHER>(rawA, p.codes, t1, nt1, 0, warp, lane, rn, sNew, nullptr);
 
         // ---- softmax of the tile: thread = row srow, 32 heads ----
-        mbar_wait(&bars[kBarScore], (uint32_t)t & 1u, sAbort);
+        mbar_wait(&bars[kBarScore], (uint32_t)t & 1u, sAbort, wl);
         tc_after();
         // z = sm log2(e) (s_L S_L + s_R S_R) for this row's 32 heads, read from TMEM
         float z[32];
@@ -478,7 +583,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kv8_kernel(AttnParams p) 
             }
         };
         load_z();
-        bool flag = *sAbort != 0;
+        // a latent scale with s_L max_h E > kScaleLim takes the exact path
+        // (max_h E is +inf while only inert latent blocks have been met)
+        bool flag = (*sAbort != 0) | (my_sl * fmaxf(sEmax[0], sEmax[1]) > kScaleLim);
 #pragma unroll
         for (int j = 0; j < 32; ++j) flag |= z[j] > sM[32 * hq + j] + kLagLog2;
         const bool any_flag = worker_any(flag);
@@ -492,35 +599,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kv8_kernel(AttnParams p) 
         }
         if (any_flag) {
             if (worker_any(*sAbort != 0)) break;
-            // exact column max of the tile, new running max, rescale factors
-            sRed[(warp & 3) * kHC + 32 * hq + lane] = warp_columns<true>(z, lane);
-            worker_sync();
-            if (tid < kHC) {
-                const float c4 = fmaxf(fmaxf(sRed[tid], sRed[kHC + tid]), fmaxf(sRed[2 * kHC + tid], sRed[3 * kHC + tid]));
-                const float mo = sM[tid], mn = fmaxf(mo, c4);
-                sAlpha[tid] = mo == -INFINITY ? 0.0f : ex2(mo - mn);
-                sM[tid] = mn;
-            }
-            worker_sync();
-            if (t > 0) {
-                // O^T is stable: the score commit of this tile follows every
-                // context MMA of the previous one
-#pragma unroll 1
-                for (int bi = 0; bi < 2; ++bi)
-#pragma unroll 1
-                    for (int c = 0; c < 2; ++c) {
-                        const uint32_t ta = tmem + lane_base + kColO + 64 * (2 * hq + bi) + 32 * c;
-                        uint32_t o[32];
-                        tmem_ld32(ta, o);
-                        tmem_wait_ld();
-#pragma unroll
-                        for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * sAlpha[32 * c + j]);
-                        tmem_st32(ta, o);
-                    }
-                tmem_wait_st();
-            }
-            lcol *= sAlpha[32 * hq + lane];
-            load_z();   // the reduction consumed z
+            lcol = exact_path(sm, tmem, lane_base, hq, row_ok, za, zb, my_sl, lane, warp, tid, t, p.exact_count,
+                              lcol);
+            load_z();   // refreshed after the rescale path
         }
         // the rest of tile t+1 is requested once the running max is settled:
         // held across the max pass above, these 40 registers spilled
@@ -530,13 +611,14 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kv8_kernel(AttnParams p) 
             load_scales(t1, nt1);
         }
         {
-            const float wrow = my_sl * inv_s_ref;
+            // row-sum weights p = 2^(z - m), f16 context weights w = p s_L E
             uint32_t pk[16];
 #pragma unroll
             for (int j = 0; j < 32; j += 2) {
                 z[j] = ex2(z[j] - sM[32 * hq + j]);
                 z[j + 1] = ex2(z[j + 1] - sM[32 * hq + j + 1]);
-                const __half2 h2 = __floats2half2_rn(z[j] * wrow, z[j + 1] * wrow);
+                const __half2 h2 =
+                    __floats2half2_rn(z[j] * sE[32 * hq + j] * my_sl, z[j + 1] * sE[32 * hq + j + 1] * my_sl);
                 pk[j / 2] = *reinterpret_cast<const uint32_t*>(&h2);
             }
 #pragma unroll
@@ -567,7 +649,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kv8_kernel(AttnParams p) 
         worker_sync();
     }
     if (aborted) {
-        if (tid == 0) set_err(p.err, KVQ_ERR_DEVICE);
+        if (tid == 0) set_err(p.err, KVQ_ERR_TIMEOUT);
     } else {
         const int64_t unit = blockIdx.x;
         const int64_t item = unit / (p.n_heads / kHC);
@@ -584,7 +666,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kv8_kernel(AttnParams p) 
 #pragma unroll
                 for (int j = 0; j < 32; ++j) {
                     const int h = hbase + 32 * c + j;
-                    p.ws_o[(item * p.n_heads + h) * kMlaDV + dim] = n_tiles > 0 ? __uint_as_float(v[j]) * s_ref : 0.0f;
+                    p.ws_o[(item * p.n_heads + h) * kMlaDV + dim] =
+                        n_tiles > 0 ? __uint_as_float(v[j]) * sF[32 * c + j] : 0.0f;
                 }
             }
         }

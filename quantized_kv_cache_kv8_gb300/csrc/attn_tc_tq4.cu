@@ -16,6 +16,13 @@
 //     of f16; divided out of scores and context);
 //   - P is stored K-major (heads on rows) so that N = 32 needs no padding.
 // The context accumulates in the rotated domain; the merge unrotates it.
+// Softmax weights as in the KV8 kernel: the row sums take p = 2^(z - m) (m a
+// lagged running maximum of the scores), the context the f16 weight
+// w = p s_L E with E = 2^(m - R - 3) per head, R the largest z + log2 s_L of
+// the tiles that set the references, so that the context weights are relative
+// to the largest p * s_L of the chunk (which weighs 2^-3); the exact path runs
+// when a score passes m by 2^14 or a latent scale passes 3.5 / max_h E; the
+// partial state is (m, sum p, O^T / E).
 #include "tc_common.cuh"
 
 #include <math.h>
@@ -37,10 +44,15 @@ constexpr uint32_t kPChunkBytes = kHC * 128;       // P: 32 head rows x 64 cells
 constexpr uint32_t kOffQ = 0;
 constexpr uint32_t kOffSlot = kOffQ + kChunks * kQChunkBytes;
 constexpr uint32_t kOffLevels = kOffSlot + kChunks * kSlotBytes;   // LevelBytes: 32 bytes
-constexpr uint32_t kOffM = kOffLevels + 32;
-constexpr uint32_t kOffAlpha = kOffM + kHC * 4;
-constexpr uint32_t kOffRed = kOffAlpha + kHC * 4;   // 4 quadrants x 32 heads
-constexpr uint32_t kOffBar = kOffRed + 4 * kHC * 4;
+constexpr uint32_t kOffM = kOffLevels + 32;             // m: running max of z per head
+constexpr uint32_t kOffR = kOffM + kHC * 4;              // R: reference of z + log2 s_L
+constexpr uint32_t kOffE = kOffR + kHC * 4;              // E = 2^(m - R - kHeadroom)
+constexpr uint32_t kOffF = kOffE + kHC * 4;              // 1 / E
+constexpr uint32_t kOffAlpha = kOffF + kHC * 4;          // O^T rescale
+constexpr uint32_t kOffAlphaM = kOffAlpha + kHC * 4;     // row-sum rescale 2^(m_old - m_new)
+constexpr uint32_t kOffEmax = kOffAlphaM + kHC * 4;      // max E over the heads
+constexpr uint32_t kOffRed = kOffEmax + 16;          // 2 x 4 quadrants x 32 heads
+constexpr uint32_t kOffBar = kOffRed + 2 * 4 * kHC * 4;
 constexpr uint32_t kOffMisc = kOffBar + 16 * 8;
 constexpr uint32_t kSmemUsed = kOffMisc + 32;
 static_assert(kOffSlot % 1024 == 0, "swizzled operands need 1024-byte alignment");
@@ -49,9 +61,12 @@ static_assert(kSmemUsed <= 232448, "shared memory budget");
 // TMEM: O^T 4 blocks x 32 columns, S_L^T and S_R^T 64 columns each (values, residuals)
 constexpr uint32_t kColO = 0, kColSL = 128, kColSR = 192, kTmemCols = 256;
 
-enum { kBarFull0 = 0, kBarFree0 = 3, kBarScore = 7, kBarP = 8, kBarDone = 9, kNumBars = 10 };
+// (the same barriers as the KV8 kernel, the last one for the testing hook's stall)
+enum { kBarFull0 = 0, kBarFree0 = 3, kBarScore = 7, kBarP = 8, kBarDone = 9, kBarNever = 10, kNumBars = 11 };
 
-constexpr float kLagLog2 = 14.0f;
+constexpr float kLagLog2 = 14.0f;   // p <= 2^14, w <= 3.5 * 2^14 without the exact path
+constexpr float kHeadroom = 3.0f;   // the largest p * s_L of a reference tile weighs 2^-3
+constexpr float kLogEmax = 120.0f;  // cap of log2 E (E and 1 / E finite in f32)
 // TQ4 levels in f16: the 16 Lloyd-Max levels times kTq4Gamma round to f16 with
 // a relative error of at most 9.3e-5 (2^-13.4), against 3.2e-4 unscaled; the
 // value comes from a search over scales in [1, 2) (csrc/gen_codebook.py
@@ -119,29 +134,6 @@ __device__ __forceinline__ void store32(unsigned char* slot, const uint4& c, int
     }
 }
 
-// In-warp transpose-reduce of 16 columns over 32 lanes: lane j's result is
-// column j % 16 reduced over all lanes.  31 shuffles.
-template <bool MAX>
-__device__ __forceinline__ float warp_columns16(float (&v)[16], int lane) {
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-        const float got = __shfl_xor_sync(kFull, v[i], 16);
-        v[i] = MAX ? fmaxf(v[i], got) : v[i] + got;
-    }
-#pragma unroll
-    for (int s = 8; s >= 1; s >>= 1) {
-        const bool upper = (lane & s) != 0;
-#pragma unroll
-        for (int i = 0; i < s; ++i) {
-            const float send = upper ? v[i] : v[i + s];
-            const float keep = upper ? v[i + s] : v[i];
-            const float got = __shfl_xor_sync(kFull, send, s);
-            v[i] = MAX ? fmaxf(keep, got) : keep + got;
-        }
-    }
-    return v[0];
-}
-
 template <bool QBF16>
 __global__ void __launch_bounds__(kThreads, 1) attn_tc_tq4_kernel(AttnParams p) {
     launch_dependents();
@@ -153,7 +145,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_tq4_kernel(AttnParams p) 
     unsigned char* sP = sSlot + kRope * kSlotBytes;
     unsigned char* sLevels = sm + kOffLevels;
     float* sM = reinterpret_cast<float*>(sm + kOffM);
+    float* sR = reinterpret_cast<float*>(sm + kOffR);
+    float* sE = reinterpret_cast<float*>(sm + kOffE);
+    float* sF = reinterpret_cast<float*>(sm + kOffF);
+    float* sEmax = reinterpret_cast<float*>(sm + kOffEmax);
     float* sAlpha = reinterpret_cast<float*>(sm + kOffAlpha);
+    float* sAlphaM = reinterpret_cast<float*>(sm + kOffAlphaM);
     float* sRed = reinterpret_cast<float*>(sm + kOffRed);
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kOffBar);
     volatile int* sAbort = reinterpret_cast<volatile int*>(sm + kOffMisc);
@@ -210,12 +207,16 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_tq4_kernel(AttnParams p) 
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         *sAbort = 0;
     }
-    if (tid < kHC) sM[tid] = -INFINITY;
+    if (tid < kHC) {
+        sM[tid] = -INFINITY;
+        sR[tid] = -INFINITY;
+        sE[tid] = 0.0f;
+        sF[tid] = 0.0f;
+    }
     if (tid == 0) {
-        // one thread, constant level indices: written by 16 threads with a
-        // per-thread index into the parameter block, these planes read back
-        // wrong on the device (found by comparing them with planes built in
-        // registers), while this form matches
+        // one thread builds both planes in registers and stores each as one
+        // 16-byte word, so no word of them is written by two threads; the
+        // barrier after the prologue orders these stores before every reader
         uint32_t lo[4] = {0u, 0u, 0u, 0u}, hi[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
         for (int k = 0; k < 16; ++k) {
@@ -236,7 +237,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_tq4_kernel(AttnParams p) 
     // power of two that keeps every element below 2^14 ----
     const int64_t qbase = ((int64_t)b * p.n_heads + hbase) * kMlaD;
     float qv[4][18];
-    float smax = 0.0f;
     if (tid < kWorkers) {
         float qmax = 0.0f;
 #pragma unroll
@@ -250,29 +250,17 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_tq4_kernel(AttnParams p) 
                 qmax = fmaxf(qmax, fabsf(qv[hh][k]));
             }
         }
-#pragma unroll 4
-        for (int64_t r = row0 + tid; r < row1; r += kWorkers) smax = fmaxf(smax, p.scales[r * p.n_blocks]);
         qmax = warp_max(qmax);
-        smax = warp_max(smax);
-        if (lane == 0) {
-            sRed[warp] = qmax;
-            sRed[8 + warp] = smax;
-        }
+        if (lane == 0) sRed[warp] = qmax;
     }
     __syncthreads();
-    float q_max = 0.0f, s_max = 0.0f;
+    float q_max = 0.0f;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        q_max = fmaxf(q_max, sRed[i]);
-        s_max = fmaxf(s_max, sRed[8 + i]);
-    }
+    for (int i = 0; i < 8; ++i) q_max = fmaxf(q_max, sRed[i]);
     // |q'_i| <= ||q|| <= 24 max|q| for the rotated query
     const float q_bound = 24.0f * q_max;
-    int e_s = 0, e_q = 0;
-    if (s_max > 0.0f) frexpf(s_max, &e_s);
+    int e_q = 0;
     if (q_bound > 0.0f) frexpf(q_bound, &e_q);
-    const float s_ref = s_max > 0.0f ? ldexpf(1.0f, e_s) : 1.0f;
-    const float inv_s_ref = s_max > 0.0f ? ldexpf(1.0f, -e_s) : 1.0f;
     const float q_scale = q_bound > 0.0f ? ldexpf(1.0f, 14 - e_q) : 1.0f;
     const float cz = p.sm_scale * kLog2e * (q_bound > 0.0f ? ldexpf(1.0f, e_q - 14) : 1.0f) * kTq4InvGamma;
     if (tid < kWorkers) {
@@ -319,12 +307,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_tq4_kernel(AttnParams p) 
             const uint64_t dp = umma_desc(smem_u32(sP), 16, 1024);
             constexpr uint64_t kQStep = kQChunkBytes >> 4, kSlotStep = kSlotBytes >> 4, kPStep = kPChunkBytes >> 4;
             bool ok = true;
+            if (p.stall_polls > 0) ok = mbar_wait(&bars[kBarNever], 0u, sAbort, p.stall_polls);
             for (int t = 0; t < n_tiles && ok; ++t) {
                 const uint32_t par = (uint32_t)t & 1u;
 #pragma unroll 1
                 for (int kc = 0; kc < kChunks && ok; ++kc) {
                     if ((kc & 3) == 0) {
-                        ok = mbar_wait(&bars[kBarFull0 + (kc >> 2)], par, sAbort);
+                        ok = mbar_wait(&bars[kBarFull0 + (kc >> 2)], par, sAbort, p.wait_limit);
                         tc_after();
                     }
                     const uint32_t d = tmem + (kc < kRope ? kColSL : kColSR);
@@ -335,7 +324,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_tq4_kernel(AttnParams p) 
                         umma_f16(d, a + 2 * ks, bq + 2 * ks, kIdescScore, (first && ks == 0) ? 0u : 1u);
                 }
                 umma_commit(&bars[kBarScore]);
-                ok = ok && mbar_wait(&bars[kBarP], par, sAbort);
+                ok = ok && mbar_wait(&bars[kBarP], par, sAbort, p.wait_limit);
                 tc_after();
 #pragma unroll 1
                 for (int db = 0; db < 4 && ok; ++db) {
@@ -358,6 +347,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_tq4_kernel(AttnParams p) 
     const int hq = warp >> 2;                            // softmax: heads 16 hq .. 16 hq + 15
     const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
     float lcol = 0.0f;   // row sum of head 16 hq + lane % 16 over this quadrant (lanes 0-15)
+    float s_lim = 0.0f;  // latent scales above this take the exact path (3.5 / max_h E)
 
     float sl_next = 0.0f, sr_next = 0.0f;
     auto load_scales = [&](int64_t t0n, int ntn) {
@@ -404,8 +394,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_tq4_kernel(AttnParams p) 
 #pragma unroll
             for (int g = 0; g < 2; ++g) {
                 if (t > 0) {
-                    mbar_wait(&bars[kBarFree0 + 2 * g], prev, sAbort);
-                    mbar_wait(&bars[kBarFree0 + 2 * g + 1], prev, sAbort);
+                    mbar_wait(&bars[kBarFree0 + 2 * g], prev, sAbort, p.wait_limit);
+                    mbar_wait(&bars[kBarFree0 + 2 * g + 1], prev, sAbort, p.wait_limit);
                 }
                 unsigned char* slot = sSlot + (4 * g + cg) * kSlotBytes;
                 const RawGroup& rg = g == 0 ? rawA : rawB;
@@ -423,7 +413,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_tq4_kernel(AttnParams p) 
         if (t + 1 < n_tiles) load_group(rawA, p.codes, t1, nt1, 0, warp, lane);
 
         // ---- softmax of the tile: thread = row srow, 16 heads ----
-        mbar_wait(&bars[kBarScore], (uint32_t)t & 1u, sAbort);
+        mbar_wait(&bars[kBarScore], (uint32_t)t & 1u, sAbort, p.wait_limit);
         tc_after();
         float z[16];
         const float za = my_sl * cz, zb = my_sr * cz;
@@ -448,21 +438,49 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_tq4_kernel(AttnParams p) 
             rawC = load_rope(p.codes, t1, nt1, warp, lane);
             load_scales(t1, nt1);
         }
-        bool flag = *sAbort != 0;
+        bool flag = (*sAbort != 0) | (my_sl > s_lim);
 #pragma unroll
         for (int j = 0; j < 16; ++j) flag |= z[j] > sM[16 * hq + j] + kLagLog2;
         if (worker_any(flag)) {
             if (worker_any(*sAbort != 0)) break;
-            const float cm = warp_columns16<true>(z, lane);
-            if (lane < 16) sRed[(warp & 3) * kHC + 16 * hq + lane] = cm;
-            worker_sync();
-            if (tid < kHC) {
-                const float c4 = fmaxf(fmaxf(sRed[tid], sRed[kHC + tid]), fmaxf(sRed[2 * kHC + tid], sRed[3 * kHC + tid]));
-                const float mo = sM[tid], mn = fmaxf(mo, c4);
-                sAlpha[tid] = mo == -INFINITY ? 0.0f : ex2(mo - mn);
-                sM[tid] = mn;
+            // exact column maxima of z and of y = z + log2 s_L, new running
+            // maxima, rescale factors
+            {
+                const float cm = warp_columns16<true>(z, lane);
+                if (lane < 16) sRed[(warp & 3) * kHC + 16 * hq + lane] = cm;
+            }
+            load_z();
+            const float ls = my_sl > 0.0f ? __log2f(my_sl) : -INFINITY;   // -inf: an inert latent block
+#pragma unroll
+            for (int j = 0; j < 16; ++j) z[j] += ls;
+            {
+                const float cm = warp_columns16<true>(z, lane);
+                if (lane < 16) sRed[4 * kHC + (warp & 3) * kHC + 16 * hq + lane] = cm;
             }
             worker_sync();
+            if (tid < kHC) {
+                const float* rz = sRed;
+                const float* ry = sRed + 4 * kHC;
+                const float cz4 = fmaxf(fmaxf(rz[tid], rz[kHC + tid]), fmaxf(rz[2 * kHC + tid], rz[3 * kHC + tid]));
+                const float cy4 = fmaxf(fmaxf(ry[tid], ry[kHC + tid]), fmaxf(ry[2 * kHC + tid], ry[3 * kHC + tid]));
+                const float mo = sM[tid], mn = fmaxf(mo, cz4);
+                const float ro = sR[tid], rn = fmaxf(ro, cy4);
+                const float dn = fminf(mn - rn - kHeadroom, kLogEmax), d_old = fminf(mo - ro - kHeadroom, kLogEmax);
+                sAlphaM[tid] = mo == -INFINITY ? 0.0f : ex2(mo - mn);
+                sAlpha[tid] = ro == -INFINITY ? 0.0f : ex2(dn - d_old + (mo - mn));   // E_new / E_old x 2^(m_old - m_new)
+                sM[tid] = mn;
+                sR[tid] = rn;
+                const float e = rn == -INFINITY ? 0.0f : ex2(dn);   // R = -inf: only inert latent blocks so far
+                sE[tid] = e;
+                sF[tid] = rn == -INFINITY ? 0.0f : ex2(-dn);
+                const float em = warp_max(e);
+                if (tid == 0) {
+                    sEmax[0] = em;
+                    if (t > 0) atomicAdd(p.exact_count, 1u);
+                }
+            }
+            worker_sync();
+            s_lim = sEmax[0] > 0.0f ? 3.5f / sEmax[0] : 0.0f;
             if (t > 0) {
                 // O^T (lanes = dims, columns = heads) is stable: the score commit
                 // of this tile follows every context MMA of the previous one
@@ -478,17 +496,17 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_tq4_kernel(AttnParams p) 
                 }
                 tmem_wait_st();
             }
-            if (lane < 16) lcol *= sAlpha[16 * hq + lane];
+            if (lane < 16) lcol *= sAlphaM[16 * hq + lane];
             load_z();
         }
         {
-            const float wrow = my_sl * inv_s_ref;
+            // row-sum weights p = 2^(z - m), f16 context weights w = p s_L E
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
-                z[j] = ex2(z[j] - sM[16 * hq + j]);
                 const int h = 16 * hq + j;
+                z[j] = ex2(z[j] - sM[h]);
                 *reinterpret_cast<__half*>(sP + (srow >> 6) * kPChunkBytes + sw128(h, (srow & 63) * 2)) =
-                    __float2half_rn(z[j] * wrow);
+                    __float2half_rn(z[j] * sE[h] * my_sl);
             }
         }
         fence_async_smem();
@@ -515,12 +533,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_tq4_kernel(AttnParams p) 
         worker_sync();
     }
     if (aborted) {
-        if (tid == 0) set_err(p.err, KVQ_ERR_DEVICE);
+        if (tid == 0) set_err(p.err, KVQ_ERR_TIMEOUT);
     } else {
         const int64_t unit = blockIdx.x;
         const int64_t item = unit / (p.n_heads / kHC);
         const int hbase = (int)(unit % (p.n_heads / kHC)) * kHC;
-        const float o_scale = s_ref * kTq4InvGamma;
+        const float o_scale = kTq4InvGamma;
 #pragma unroll
         for (int bi = 0; bi < 2; ++bi) {
             const int db = 2 * hq + bi;
@@ -531,7 +549,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_tq4_kernel(AttnParams p) 
 #pragma unroll
             for (int j = 0; j < 32; ++j) {
                 const int h = hbase + j;
-                p.ws_o[(item * p.n_heads + h) * kMlaDV + dim] = n_tiles > 0 ? __uint_as_float(v[j]) * o_scale : 0.0f;
+                p.ws_o[(item * p.n_heads + h) * kMlaDV + dim] =
+                    n_tiles > 0 ? __uint_as_float(v[j]) * (sF[j] * o_scale) : 0.0f;
             }
         }
         if (tid < kHC) {

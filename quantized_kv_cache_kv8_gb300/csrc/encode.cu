@@ -56,17 +56,18 @@ struct Kv8Params {
 
 __global__ void __launch_bounds__(256) kv8_encode_kernel(const float* __restrict__ x, int64_t n_rows, Kv8Params p,
                                                          const int64_t* __restrict__ dst_rows,
-                                                         uint8_t* __restrict__ codes, float* __restrict__ scales) {
+                                                         uint8_t* __restrict__ codes, float* __restrict__ scales,
+                                                         int32_t* err) {
     const int lane = threadIdx.x & 31;
     const int64_t src = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     if (src >= n_rows) return;
     const int64_t row = dst_rows ? dst_rows[src] : src;
     kv8_encode_row_warp(x + src * p.D, p.n_blocks, p.bd[0], p.bd[1], codes + row * p.D, scales + row * p.n_blocks,
-                        lane);
+                        lane, err);
 }
 
 cudaError_t launch_kv8_encode(const float* x, int64_t n_rows, const kvq_mla_layout& L, const int64_t* dst_rows,
-                              uint8_t* codes, float* scales, cudaStream_t stream) {
+                              uint8_t* codes, float* scales, int32_t* err, cudaStream_t stream) {
     if (n_rows == 0) return cudaSuccess;
     Kv8Params p{};
     p.n_blocks = L.n_blocks;
@@ -75,7 +76,7 @@ cudaError_t launch_kv8_encode(const float* x, int64_t n_rows, const kvq_mla_layo
     p.D = p.bd[0] + p.bd[1];
     const int warps = 8;
     const int64_t grid = (n_rows + warps - 1) / warps;
-    kv8_encode_kernel<<<(unsigned)grid, warps * 32, 0, stream>>>(x, n_rows, p, dst_rows, codes, scales);
+    kv8_encode_kernel<<<(unsigned)grid, warps * 32, 0, stream>>>(x, n_rows, p, dst_rows, codes, scales, err);
     return cudaGetLastError();
 }
 
@@ -92,7 +93,8 @@ struct Tq4Params {
 
 template <int N>
 __device__ __forceinline__ void tq4_encode_block(const float* __restrict__ xb, int lane, const Tq4Params& p, int blk,
-                                                 const float* th, uint8_t* __restrict__ out, float* scale_out) {
+                                                 const float* th, uint8_t* __restrict__ out, float* scale_out,
+                                                 int32_t* err) {
     constexpr int K = N >= 32 ? N / 32 : 1;
     const bool active = (N >= 32) || (lane < N);
     float x[K], v[K];
@@ -107,6 +109,8 @@ __device__ __forceinline__ void tq4_encode_block(const float* __restrict__ xb, i
 #pragma unroll
     for (int k = 0; k < K; ++k) ss = __fmaf_rn(x[k], x[k], ss);
     ss = warp_sum(ss);
+    // a NaN or infinite input, or a radius past the f32 range: no code exists
+    if (!(ss <= 3.402823466e38f) && lane == 0 && err) atomicCAS(err, 0, (int32_t)KVQ_ERR_NONFINITE);
     const float s = __fdiv_rn(__fsqrt_rn(ss), p.sqrtn[blk]);
     warp_fwht<N>(v, lane);
     const float kn = p.kn[blk];
@@ -142,7 +146,8 @@ __device__ __forceinline__ void tq4_rotate_block(float* v, int lane, const Tq4Pa
 
 __global__ void __launch_bounds__(256) tq4_encode_kernel(const float* __restrict__ x, int64_t n_rows, Tq4Params p,
                                                          const int64_t* __restrict__ dst_rows,
-                                                         uint8_t* __restrict__ packed, float* __restrict__ scales) {
+                                                         uint8_t* __restrict__ packed, float* __restrict__ scales,
+                                                         int32_t* err) {
     __shared__ float th[16];
     if (threadIdx.x < 16) th[threadIdx.x] = p.cb.th[threadIdx.x];
     __syncthreads();
@@ -157,7 +162,7 @@ __global__ void __launch_bounds__(256) tq4_encode_kernel(const float* __restrict
         float* so = scales + row * p.n_blocks + b;
         switch (p.bd[b]) {
 #define KVQ_CASE(n) \
-    case n: tq4_encode_block<n>(xb, lane, p, b, th, ob, so); break;
+    case n: tq4_encode_block<n>(xb, lane, p, b, th, ob, so, err); break;
             KVQ_POW2_CASES(KVQ_CASE)
 #undef KVQ_CASE
             default: break;
@@ -226,12 +231,12 @@ static Tq4Params make_tq4_params(const kvq_mla_layout& L) {
 }
 
 cudaError_t launch_tq4_encode(const float* x, int64_t n_rows, const kvq_mla_layout& L, const int64_t* dst_rows,
-                              uint8_t* packed, float* scales, cudaStream_t stream) {
+                              uint8_t* packed, float* scales, int32_t* err, cudaStream_t stream) {
     if (n_rows == 0) return cudaSuccess;
     const Tq4Params p = make_tq4_params(L);
     const int warps = 8;
     const int64_t grid = (n_rows + warps - 1) / warps;
-    tq4_encode_kernel<<<(unsigned)grid, warps * 32, 0, stream>>>(x, n_rows, p, dst_rows, packed, scales);
+    tq4_encode_kernel<<<(unsigned)grid, warps * 32, 0, stream>>>(x, n_rows, p, dst_rows, packed, scales, err);
     return cudaGetLastError();
 }
 

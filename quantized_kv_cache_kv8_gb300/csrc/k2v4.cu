@@ -234,6 +234,7 @@ struct K2V4DecodeParams {
     float* ws_o;   // [batch][Hq][n_chunks][D]
     float* ws_ml;  // [batch][Hq][n_chunks][2]
     int32_t* err;  // the workspace's error word
+    int64_t wait_limit;   // try_wait polls of the tensor-core kernel's tile-loop waits
 };
 
 constexpr int kHQ = 8;   // query heads per CTA (one kv group)
@@ -567,7 +568,9 @@ __global__ void __launch_bounds__(kThreadsT, 1) k2v4_tc_kernel(K2V4DecodeParams 
         for (int i = 0; i < 4; ++i)
             asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(&bars[i])), "r"(1u));
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-        *sAbort = smem_u32(smem_raw) & 1023u ? 1 : 0;   // the swizzled operands need a 1024-byte base
+        // the swizzled operands need a 1024-byte base (2: refused; a wait that
+        // runs out raises the flag to 1)
+        *sAbort = smem_u32(smem_raw) & 1023u ? 2 : 0;
         if (n_tiles > 0) stage_tile<D>(p, seq, c0, (int)min((int64_t)kRowsT, c1 - c0), sRaw, &bars[2]);
     }
     if (tid < 8) {
@@ -625,7 +628,7 @@ __global__ void __launch_bounds__(kThreadsT, 1) k2v4_tc_kernel(K2V4DecodeParams 
         if (tid == 0 && t + 1 < n_tiles)
             stage_tile<D>(p, seq, t0 + kRowsT, (int)min((int64_t)kRowsT, c1 - t0 - kRowsT),
                           sRaw + ((t + 1) & 1) * SM::kRawBytes, &bars[2 + ((t + 1) & 1)]);
-        mbar_wait(&bars[2 + (t & 1)], (uint32_t)(t >> 1) & 1u, sAbort);
+        mbar_wait(&bars[2 + (t & 1)], (uint32_t)(t >> 1) & 1u, sAbort, p.wait_limit);
         const unsigned char* raw = sRaw + (t & 1) * SM::kRawBytes;
         const unsigned char* raw_kc = raw;
         const uint16_t* raw_ks = reinterpret_cast<const uint16_t*>(raw + SM::kRawKc);
@@ -728,7 +731,7 @@ __global__ void __launch_bounds__(kThreadsT, 1) k2v4_tc_kernel(K2V4DecodeParams 
         if (warp >= 4) {
             // ---- V of the tile to f16, warps 4-7, overlapping the score MMAs
             // and the softmax, once the previous context MMAs released sV ----
-            if (t > 0) mbar_wait(&bars[1], (uint32_t)(t - 1) & 1u, sAbort);
+            if (t > 0) mbar_wait(&bars[1], (uint32_t)(t - 1) & 1u, sAbort, p.wait_limit);
             auto v_bulk = [&](int r, int j, uint32_t (&vw)[16]) {
                 // q4_0 block (d, then 16 bytes: element e in the low nibble of
                 // byte e, e + 16 in the high nibble)
@@ -824,7 +827,7 @@ __global__ void __launch_bounds__(kThreadsT, 1) k2v4_tc_kernel(K2V4DecodeParams 
             // ---- softmax: warps 0-3, thread = cell (TMEM lane), the group's
             // heads.  The score commit covers the previous context MMAs too, so
             // P^T and O^T are free once it has arrived.
-            mbar_wait(&bars[0], (uint32_t)t & 1u, sAbort);
+            mbar_wait(&bars[0], (uint32_t)t & 1u, sAbort, p.wait_limit);
             tc_after();
             uint32_t sv[16];
             tmem_ld16(tmem + lane_base + kColS, sv);
@@ -914,7 +917,7 @@ __global__ void __launch_bounds__(kThreadsT, 1) k2v4_tc_kernel(K2V4DecodeParams 
     }
     tc_after();
     if (*sAbort) {
-        if (tid == 0) atomicCAS(p.err, 0, KVQ_ERR_DEVICE);
+        if (tid == 0) atomicCAS(p.err, 0, *sAbort == 2 ? (int32_t)KVQ_ERR_DEVICE : (int32_t)KVQ_ERR_TIMEOUT);
     } else if (warp < 4) {
 #pragma unroll
         for (int m = 0; m < D / 128; ++m) {
@@ -1039,6 +1042,7 @@ cudaError_t launch_k2v4_decode(const kvq_k2v4_layout& L, const float* q, int32_t
     p.k_win = k_win;
     p.v_win = v_win;
     p.err = static_cast<int32_t*>(workspace);
+    p.wait_limit = kWaitLimit;
     char* ws = static_cast<char*>(workspace) + kWsHeader;
     p.ws_o = reinterpret_cast<float*>(ws);
     p.ws_ml = p.ws_o + (size_t)batch * n_q_heads * plan.n_chunks * L.head_dim;

@@ -24,6 +24,12 @@ constexpr unsigned kFull = 0xffffffffu;
 // 1 before its merge, 2 after it; a no-op unless kvq_timing_enable is on.
 void timing_mark(cudaStream_t stream, int phase);
 
+// Bounded waits of the tensor-core kernels: try_wait polls before a wait
+// gives up, and the testing hook's stall (kvq_test_stall_waits; 0 = off).
+constexpr long long kWaitLimit = 1ll << 22;
+int64_t test_stall_polls();
+void set_test_stall_polls(int64_t polls);
+
 // N(0,1) Lloyd-Max codebooks as f32 bit patterns (levels ascending, then the
 // decision thresholds = f64 midpoints of adjacent levels rounded to f32).
 // Derived by gen_codebook.py (root finding on the centroid and midpoint
@@ -78,13 +84,21 @@ __device__ __forceinline__ float warp_max(float v) {
 // e4m3_rn_satfinite(x / s); a block with s == 0 stores s = 0 and codes 0.
 // Lane 0 writes the block scales to sr[0 .. n_blocks).  The encoder kernel and
 // the decode kernel that appends rows both call this, so their bytes agree.
+// With CHECK, a NaN or an infinity in the row sets *err (if given and still
+// 0) to KVQ_ERR_NONFINITE; the pages define no code for such values.
+template <bool CHECK = true>
 __device__ __forceinline__ void kv8_encode_row_warp(const float* __restrict__ xr, int n_blocks, int bd0, int bd1,
-                                                    uint8_t* cr, float* sr, int lane) {
+                                                    uint8_t* cr, float* sr, int lane, int32_t* err) {
     int off = 0;
+    bool bad = false;
     for (int b = 0; b < n_blocks; ++b) {
         const int n = b == 0 ? bd0 : bd1;
         float amax = 0.0f;
-        for (int i = lane; i < n; i += 32) amax = fmaxf(amax, fabsf(__ldg(xr + off + i)));
+        for (int i = lane; i < n; i += 32) {
+            const float a = fabsf(__ldg(xr + off + i));
+            if (CHECK) bad |= !(a <= 3.402823466e38f);
+            amax = fmaxf(amax, a);
+        }
         amax = warp_max(amax);
         const float s = __fdiv_rn(amax, 448.0f);
         if (lane == 0) sr[b] = s;
@@ -96,7 +110,9 @@ __device__ __forceinline__ void kv8_encode_row_warp(const float* __restrict__ xr
         }
         off += n;
     }
+    if (CHECK && __any_sync(kFull, bad) && lane == 0 && err) atomicCAS(err, 0, (int32_t)KVQ_ERR_NONFINITE);
 }
+
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
     for (int o = 16; o >= 1; o >>= 1) v = __fadd_rn(v, __shfl_xor_sync(kFull, v, o));
@@ -157,10 +173,11 @@ __device__ __forceinline__ bool sign_neg(const SignWords& s, int block, int i) {
 // Launchers (all asynchronous on `stream`; return cudaGetLastError()).
 // ---------------------------------------------------------------------------
 // dst_rows (device, may be null): input row i goes to pool row dst_rows[i].
+// err (device, may be null): the error word a non-finite row sets.
 cudaError_t launch_kv8_encode(const float* x, int64_t n_rows, const kvq_mla_layout& L, const int64_t* dst_rows,
-                              uint8_t* codes, float* scales, cudaStream_t stream);
+                              uint8_t* codes, float* scales, int32_t* err, cudaStream_t stream);
 cudaError_t launch_tq4_encode(const float* x, int64_t n_rows, const kvq_mla_layout& L, const int64_t* dst_rows,
-                              uint8_t* packed, float* scales, cudaStream_t stream);
+                              uint8_t* packed, float* scales, int32_t* err, cudaStream_t stream);
 cudaError_t launch_tq4_rotate(const void* in, kvq_dtype dt, int64_t n_vecs, const kvq_mla_layout& L, int inverse,
                               float* out, cudaStream_t stream);
 
@@ -175,7 +192,8 @@ struct AttnPlan {
 };
 AttnPlan plan_decode_simt(int32_t batch, int32_t n_heads, int64_t max_total_rows);
 size_t partial_bytes(int64_t max_items, int32_t n_heads, int32_t v_dim);
-constexpr size_t kWsHeader = 256;   // error word, device-chosen chunk, padding
+// error word (bytes 0..3), device-chosen chunk (8..15), exact-path counter (16..19), padding
+constexpr size_t kWsHeader = 256;
 
 cudaError_t launch_attn_simt(kvq_format fmt, const kvq_mla_layout& L, const void* q, kvq_dtype qdt, int32_t n_seq,
                              int32_t n_heads, const uint8_t* codes, const float* scales, const int64_t* cu_seqlens,

@@ -12,7 +12,6 @@ namespace tc {
 
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
-constexpr long long kWaitLimit = 1ll << 22;   // try_wait polls before a wait gives up
 
 __host__ __device__ constexpr uint32_t idesc_f16(int M, int N, bool a_mn, bool b_mn) {
     // D f32 (bit 4), A and B f16 (format 0), operand majors, N>>3 at 17, M>>4 at 24
@@ -51,12 +50,15 @@ static __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.
 static __device__ __forceinline__ void tc_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 static __device__ __forceinline__ void tc_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
-// Bounded wait on an mbarrier phase.  Returns false (and raises the CTA's
-// abort flag) when the limit is reached; later waits then return at once.
-static __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+// Bounded wait on an mbarrier phase: at most `limit` try_wait polls.  Returns
+// false (and raises the CTA's abort flag) when the limit is reached; it also
+// gives up, every 64 polls, once another thread has raised the flag, and later
+// waits then return at once.
+static __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                                 long long limit = kWaitLimit) {
     if (*abort_flag) return false;
     const uint32_t a = smem_u32(bar);
-    for (long long i = 0; i < kWaitLimit; ++i) {
+    for (long long i = 0; i < limit; ++i) {
         uint32_t ok;
         asm volatile(
             "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
@@ -64,21 +66,48 @@ static __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
             : "r"(a), "r"(parity)
             : "memory");
         if (ok) return true;
+        if ((i & 63) == 63 && *abort_flag) return false;
     }
     *abort_flag = 1;
     return false;
 }
 
-// Named barrier 1 among the 256 worker threads of a CTA (its MMA warp never joins it).
-static __device__ __forceinline__ void worker_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+// Named barrier 1 among the N worker threads of a CTA (its MMA warp never joins it).
+template <int N = 256>
+static __device__ __forceinline__ void worker_sync() { asm volatile("bar.sync 1, %0;" ::"n"(N) : "memory"); }
+template <int N = 256>
 static __device__ __forceinline__ bool worker_any(bool v) {
     uint32_t r;
     asm volatile(
-        "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.or.pred q, 1, 256, p;\n selp.u32 %0, 1, 0, q;\n}\n"
+        "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.or.pred q, 1, %2, p;\n selp.u32 %0, 1, 0, q;\n}\n"
         : "=r"(r)
-        : "r"((uint32_t)v)
+        : "r"((uint32_t)v), "n"(N)
         : "memory");
     return r != 0;
+}
+
+// In-warp transpose-reduce of 16 columns over 32 lanes: on entry each lane
+// holds 16 values (columns 0..15 of its row); on return lane j's v[0] is
+// column j % 16 reduced over all 32 lanes.  31 shuffles.
+template <bool MAX>
+static __device__ __forceinline__ float warp_columns16(float (&v)[16], int lane) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        const float got = __shfl_xor_sync(0xffffffffu, v[i], 16);
+        v[i] = MAX ? fmaxf(v[i], got) : v[i] + got;
+    }
+#pragma unroll
+    for (int s = 8; s >= 1; s >>= 1) {
+        const bool upper = (lane & s) != 0;
+#pragma unroll
+        for (int i = 0; i < s; ++i) {
+            const float send = upper ? v[i] : v[i + s];
+            const float keep = upper ? v[i + s] : v[i];
+            const float got = __shfl_xor_sync(0xffffffffu, send, s);
+            v[i] = MAX ? fmaxf(keep, got) : keep + got;
+        }
+    }
+    return v[0];
 }
 static __device__ __forceinline__ void cp_async16(void* smem_dst, const void* gmem_src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem_dst)), "l"(gmem_src) : "memory");

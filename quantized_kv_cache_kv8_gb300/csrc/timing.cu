@@ -7,6 +7,9 @@
 // the two kernels ends the programmatic overlap of the merge with the partial
 // kernel's tail, so a timed run with this on is a separate measurement from an
 // untimed one.
+//
+// Also the testing hook of the kernels' bounded waits (kvq_test_stall_waits):
+// a process-wide poll count that the tensor-core attention launches read.
 #include <vector>
 
 #include "kvq_internal.cuh"
@@ -20,6 +23,7 @@ struct LaunchTiming {
     int32_t cap = 0, next = 0, cur = -1;
 };
 LaunchTiming g_timing;
+int64_t g_stall_polls = 0;
 
 void timing_free() {
     for (cudaEvent_t e : g_timing.ev) cudaEventDestroy(e);
@@ -31,6 +35,9 @@ void timing_free() {
 }
 
 }  // namespace
+
+int64_t test_stall_polls() { return g_stall_polls; }
+void set_test_stall_polls(int64_t polls) { g_stall_polls = polls; }
 
 void timing_mark(cudaStream_t stream, int phase) {
     LaunchTiming& t = g_timing;

@@ -70,9 +70,11 @@ def _declare(L):
     L.kvq_codebook.restype = C.c_int
     L.kvq_codebook.argtypes = [I32, P, P]
     L.kv8_encode.restype = C.c_int
-    L.kv8_encode.argtypes = [P, I64, pl, P, P, P, P]
+    L.kv8_encode.argtypes = [P, I64, pl, P, P, P, P, P]
     L.tq4_encode.restype = C.c_int
-    L.tq4_encode.argtypes = [P, I64, pl, P, P, P, P]
+    L.tq4_encode.argtypes = [P, I64, pl, P, P, P, P, P]
+    L.kvq_test_stall_waits.restype = C.c_int
+    L.kvq_test_stall_waits.argtypes = [I64]
     L.tq4_rotate.restype = C.c_int
     L.tq4_rotate.argtypes = [P, C.c_int, I64, pl, I32, P, P]
     L.kv_attn_workspace_size.restype = S
@@ -104,6 +106,8 @@ def _declare(L):
     L.kv_attn_prefill.argtypes = [C.c_int, pl, P, P, C.c_int, I64, I64, I32, P, P, C.c_float, P, P, S, C.c_int, P]
     L.kvq_read_device_error.restype = I32
     L.kvq_read_device_error.argtypes = [P, I32, P]
+    L.kvq_read_exact_rescales.restype = I64
+    L.kvq_read_exact_rescales.argtypes = [P, I32, P]
     L.kvq_timing_enable.restype = C.c_int
     L.kvq_timing_enable.argtypes = [I32]
     L.kvq_timing_read.restype = C.c_int
@@ -167,24 +171,40 @@ def codebook(which: int):
 
 # -- producers ---------------------------------------------------------------
 
-def kv8_encode(x, codes, scales, layout: MLALayout | None = None, dst_rows=None, stream=None):
-    """Encode rows of x into the pool; row i goes to pool row dst_rows[i] (or i)."""
+def _err_ptr(err_word):
+    """A device int32 error word: an int32 tensor, or a uint8 workspace (its first 4 bytes)."""
+    if err_word is None:
+        return None
+    if err_word.dtype not in (torch.int32, torch.uint8):
+        raise ValueError("err_word must be an int32 tensor or a uint8 workspace")
+    return _ptr(err_word, None, "err_word")
+
+
+def kv8_encode(x, codes, scales, layout: MLALayout | None = None, dst_rows=None, stream=None, err_word=None):
+    """Encode rows of x into the pool; row i goes to pool row dst_rows[i] (or i).
+    A non-finite row sets err_word (if given) to KVQ_ERR_NONFINITE."""
     layout = layout or mla_layout()
     _ok(lib().kv8_encode(_ptr(x, torch.float32, "x"), x.shape[0], C.byref(layout),
                          _ptr(dst_rows, torch.int64, "dst_rows"), _ptr(codes, torch.uint8, "codes"),
-                         _ptr(scales, torch.float32, "scales"), _stream(stream)), "kv8_encode")
+                         _ptr(scales, torch.float32, "scales"), _err_ptr(err_word), _stream(stream)), "kv8_encode")
 
 
-def tq4_encode(x, packed, scales, layout: MLALayout | None = None, dst_rows=None, stream=None):
+def tq4_encode(x, packed, scales, layout: MLALayout | None = None, dst_rows=None, stream=None, err_word=None):
     layout = layout or mla_layout()
     _ok(lib().tq4_encode(_ptr(x, torch.float32, "x"), x.shape[0], C.byref(layout),
                          _ptr(dst_rows, torch.int64, "dst_rows"), _ptr(packed, torch.uint8, "packed"),
-                         _ptr(scales, torch.float32, "scales"), _stream(stream)), "tq4_encode")
+                         _ptr(scales, torch.float32, "scales"), _err_ptr(err_word), _stream(stream)), "tq4_encode")
 
 
 def tq4_encode_status(x, packed, scales, layout: MLALayout, stream=None) -> int:
     return lib().tq4_encode(_ptr(x, torch.float32, "x"), x.shape[0], C.byref(layout), None, _ptr(packed),
-                            _ptr(scales), _stream(stream))
+                            _ptr(scales), None, _stream(stream))
+
+
+def test_stall_waits(polls: int) -> None:
+    """Testing hook: later tensor-core attention launches stall on a barrier
+    nothing arrives on for `polls` polls (then report KVQ_ERR_TIMEOUT); 0 = off."""
+    _ok(lib().kvq_test_stall_waits(int(polls)), "kvq_test_stall_waits")
 
 
 def tq4_rotate(inp, out, layout: MLALayout | None = None, inverse=False, stream=None):
@@ -287,6 +307,15 @@ def kv_attn_prefill(fmt: int, x_new, q, codes, scales, n_past: int, out, workspa
 
 def read_device_error(workspace, clear: bool = True, stream=None) -> int:
     return lib().kvq_read_device_error(_ptr(workspace, torch.uint8, "workspace"), int(clear), _stream(stream))
+
+
+def read_exact_rescales(workspace, clear: bool = True, stream=None) -> int:
+    """Tiles after a work item's first that took the tensor kernels' exact
+    rescale path since the counter was last cleared."""
+    v = lib().kvq_read_exact_rescales(_ptr(workspace, torch.uint8, "workspace"), int(clear), _stream(stream))
+    if v < 0:
+        raise KvqError(4, "kvq_read_exact_rescales")
+    return v
 
 
 def timing_enable(capacity: int) -> None:

@@ -35,7 +35,7 @@ def test_every_declared_symbol_is_exported(kvq):
 
 def test_status_strings_and_version(kvq):
     assert kvq.version() == "0.1.0"
-    for s in range(9):
+    for s in range(11):
         assert kvq.status_string(s)
 
 
@@ -54,7 +54,7 @@ def test_tq4_refuses_non_power_of_two_before_launch(kvq):
     L = kvq.lib()
     for bd in [(576,), (500, 76), (512, 60)]:
         lay = kvq.mla_layout(bd, v_dim=min(bd[0], 512))
-        assert L.tq4_encode(None, 4, C.byref(lay), None, None, None, None) == 2
+        assert L.tq4_encode(None, 4, C.byref(lay), None, None, None, None, None) == 2
         assert L.tq4_rotate(None, 0, 4, C.byref(lay), 0, None, None) == 2
         assert L.kv_attn_workspace_size(2, C.byref(lay), 1, 16, 100, 0) == 0
         assert L.kv_attn_decode(2, C.byref(lay), None, 0, 1, 16, None, None, None, 100, 0.1, None, None, 0, 0,
@@ -64,10 +64,10 @@ def test_tq4_refuses_non_power_of_two_before_launch(kvq):
 def test_argument_validation(kvq):
     L = kvq.lib()
     lay = kvq.mla_layout()
-    assert L.kv8_encode(None, -1, C.byref(lay), None, None, None, None) == 1
-    assert L.kv8_encode(None, 0, C.byref(lay), None, None, None, None) == 0    # empty is a no-op
-    assert L.kv8_encode(None, 3, C.byref(lay), None, None, None, None) == 1    # null pointers
-    assert L.kv8_encode(None, 3, None, None, None, None, None) == 1
+    assert L.kv8_encode(None, -1, C.byref(lay), None, None, None, None, None) == 1
+    assert L.kv8_encode(None, 0, C.byref(lay), None, None, None, None, None) == 0    # empty is a no-op
+    assert L.kv8_encode(None, 3, C.byref(lay), None, None, None, None, None) == 1    # null pointers
+    assert L.kv8_encode(None, 3, None, None, None, None, None, None) == 1
     # workspace too small is reported before any launch
     need = kvq.kv_attn_workspace_size(1, 8, 128, 32768)
     assert need > 0
@@ -204,3 +204,14 @@ def test_timing_hook_host_side(kvq):
     assert L.kvq_timing_enable(-1) == 1
     assert L.kvq_timing_read(None, C.byref(b), C.byref(n)) == 1
     assert L.kvq_timing_enable(0) == 0
+
+
+def test_stall_hook_rejects_a_negative_count(kvq):
+    L = kvq.lib()
+    assert L.kvq_test_stall_waits(-1) == 1
+    assert L.kvq_test_stall_waits(0) == 0
+
+
+def test_new_status_strings(kvq):
+    assert "NaN" in kvq.status_string(9)
+    assert "wait" in kvq.status_string(10)
