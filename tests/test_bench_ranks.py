@@ -42,8 +42,10 @@ def test_max_over_ranks_and_job_rate_with_two_gloo_ranks():
     import sys
     sys.path.insert(0, ROOT)
     import bench
-    rows = bench.B * bench.T
-    assert bench.job_rate_gbs(rows, world, 2.0) == pytest.approx(2 * rows * bench.ROW_BYTES / 2e-3 / 1e9)
+    rows = int(bench.ragged_layout()[1][-1])
+    assert rows == 2256568
+    assert bench.job_rate_gbs(rows, world, 2.0) == pytest.approx(2 * rows * 584 / 2e-3 / 1e9)
+    assert bench.job_rate_gbs(rows, world, 2.0, 296) == pytest.approx(2 * rows * 296 / 2e-3 / 1e9)
     assert bench.job_rate_gbs(rows, 1, 2.0) * 2 == pytest.approx(bench.job_rate_gbs(rows, 2, 2.0))
 
 
