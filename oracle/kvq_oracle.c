@@ -3,7 +3,8 @@
  *
  * A plain, slow CPU statement of what the quantized-KV MLA path computes: the
  * KV8 and TQ4 row codecs, the K2/V4 GQA codec with its FP16 window overlay, and
- * softmax attention over the reconstructed rows in double precision.  Only the
+ * softmax attention over the reconstructed rows in double precision, and the
+ * PolarQuant codec of the TQ tier.  Only the
  * test suite, the smoke check and the benchmark's CPU-baseline leg may load it.
  * It shares no code, header, table or constant with the CUDA library: every
  * constant it needs (the Lloyd-Max codebooks, the e4m3 and fp16 grids, the
@@ -40,6 +41,15 @@
  *                              orthogonality identities of [P1]/[P2])
  *   K2/V4 codec + overlay ... pinned (byte counts and overlay footprint from
  *                              [P3], q4_0 nibble order fixture, gain property)
+ *   PolarQuant codebooks .... pinned (closed-form centroid conditions for
+ *                              k = 2 and 3, symmetry, Panter-Dite MSE limit,
+ *                              sampled angle densities)
+ *   PolarQuant codec ........ pinned (exact polar round trips, closed-form
+ *                              angles of basis and constant vectors, codes =
+ *                              nearest centroid by atan2 away from cell
+ *                              edges, distortion = the sum of the levels'
+ *                              quantizer MSE); its distortion at 4 bits does
+ *                              not reproduce the pages' ~0.147 (reported)
  *   K2/V4 append ............ pinned (whole groups = the encoder, constant-
  *                              magnitude closed forms of the partial-group
  *                              rule, one call = two calls split at a group
@@ -194,7 +204,7 @@ int kvqo_lloyd_max_gaussian(int levels, double* c, double* mse_out)
     for (int k = 0; k < levels; ++k)                       /* symmetric uniform start */
         c[k] = ((double)k - 0.5 * (levels - 1)) * (4.0 / levels);
     int it;
-    for (it = 1; it <= 1000000; ++it) {
+    for (it = 1; it <= 400000; ++it) {
         t[0] = -INFINITY;
         for (int k = 1; k < levels; ++k) t[k] = 0.5 * (c[k - 1] + c[k]);
         if (levels % 2 == 0) t[levels / 2] = 0.0;
@@ -475,6 +485,517 @@ int kvqo_tq4_decode(const uint8_t* packed, const float* scales, int64_t n_rows, 
         kvqo_tq4_rotate(chat, xhat + t * D, 1, n_blocks, bdims, seed, 1);
     }
     free(chat);
+    return KVQO_OK;
+}
+
+/* ------------------------------------------------------------------------ */
+/* PolarQuant row codec (codec 0 of the TQ tier).  [P1] Summary names it    */
+/* ("PolarQuant, arXiv 2502.02617, variable 2-6 bit"), [P1] Commits item 6   */
+/* gives its shape ("randomized-Hadamard rotation + recursive polar") and    */
+/* [P2] "What's in it" its bit widths (KV_TQ = 2|3|5|6, or 4 with            */
+/* KV_TQ_POLAR = 1).  The steps follow the published method (Han et al.,     */
+/* "PolarQuant: Quantizing KV Caches with Polar Transformation", 2025):      */
+/*                                                                           */
+/*   1. rotate the block as TQ4 does: y = (1/sqrt n) H_n (sigma . x), f32;   */
+/*   2. level 1: each pair (y_2j, y_2j+1) becomes a radius and an angle in   */
+/*      [0, 2 pi); level l >= 2: each pair of level-(l-1) radii (lo, hi)     */
+/*      becomes sqrt(lo^2 + hi^2) and the angle atan2(hi, lo) in [0, pi/2];  */
+/*      log2(n) levels leave one radius R, stored as the block's f32 scale;  */
+/*   3. every angle is quantized to b bits with the level's own codebook:    */
+/*      level 1 is uniform on the circle (its angle is uniform after the     */
+/*      rotation), level l >= 2 is the Lloyd-Max quantizer of the angle's    */
+/*      density, proportional to sin(2 psi)^(k-1) with k = 2^(l-1) (the      */
+/*      angle between two independent k-dimensional Gaussian halves);        */
+/*   4. reconstruction runs the tree back down from R with the cells'        */
+/*      centroids, then unrotates.                                            */
+/* Readings where the pages are silent (each also in the design notes):      */
+/*   * one width b for every angle of every level, the recursion run to a   */
+/*     single radius: the pages' "variable 2-6 bit" names one width per     */
+/*     tier, and at b = 4 the row is then 296 bytes like TQ4's (the paper's  */
+/*     own 4-level, 4/2/2/2-bit split with fp16 radii is another reading);   */
+/*   * pairing of consecutive elements, angles stored level by level (level */
+/*     1 first, in pair order), b bits each, least significant bit first,   */
+/*     ceil(n b / 8) bytes per block;                                        */
+/*   * level-1 cells [2 pi j / 2^b, 2 pi (j+1) / 2^b), reconstructed at     */
+/*     their centres;                                                        */
+/*   * the quantizer decisions are taken in f32 without computing an angle: */
+/*     psi > t  <=>  hi * (float)cos t > lo * (float)sin t (products rounded */
+/*     once each), after turning a level-1 pair into its quadrant by exact  */
+/*     sign swaps; a tie goes to the lower cell and a zero pair to code 0;  */
+/*   * radii as sqrtf(lo*lo + hi*hi), each operation rounded in f32.        */
+/* The pages' distortion figure for 4 bits (~0.147 rel-L2, [P1] "Why        */
+/* rotated-int4") is not reproduced by this reading (0.120 on Gaussian rows):*/
+/* it is reported, not pinned.  Pins: closed forms of the k = 2 and k = 3   */
+/* codebooks, the angle densities against sampled Gaussian vectors, exact   */
+/* round trips of the polar transform, and invariants of the codec.         */
+/* ------------------------------------------------------------------------ */
+
+#define PQ_MAX_LEVEL 10   /* blocks up to 1024 */
+#define PQ_MAX_BITS 8
+
+/* Gauss-Legendre nodes and weights on [-1, 1]: Newton's method on P_n from
+ * the usual cosine starting points, P_n and P_n' by the three-term recurrence. */
+#define GL_N 10
+static double gl_x[GL_N], gl_w[GL_N];
+static int gl_ready = 0;
+static void gl_init(void)
+{
+    if (gl_ready) return;
+    for (int i = 0; i < GL_N; ++i) {
+        double x = cos(M_PI * (i + 0.75) / (GL_N + 0.5)), dp = 1.0;
+        for (int it = 0; it < 100; ++it) {
+            double p0 = 1.0, p1 = x;
+            for (int j = 2; j <= GL_N; ++j) {
+                double p2 = ((2.0 * j - 1.0) * x * p1 - (j - 1.0) * p0) / j;
+                p0 = p1;
+                p1 = p2;
+            }
+            dp = GL_N * (x * p1 - p0) / (x * x - 1.0);
+            double dx = p1 / dp;
+            x -= dx;
+            if (fabs(dx) < 1e-16) break;
+        }
+        gl_x[i] = x;
+        gl_w[i] = 2.0 / ((1.0 - x * x) * dp * dp);
+    }
+    gl_ready = 1;
+}
+
+/* density of a level-l angle (l >= 2), unnormalized: sin(2 psi)^(k-1) */
+static double pq_density(double psi, int k)
+{
+    double s = sin(2.0 * psi);
+    return s > 0.0 ? pow(s, (double)(k - 1)) : 0.0;
+}
+
+/* integrals of f and psi*f over [a, b] by one Gauss-Legendre rule */
+static void gl_cell(double a, double b, int k, double* F, double* M)
+{
+    double h = 0.5 * (b - a), m = 0.5 * (a + b), f = 0.0, g = 0.0;
+    for (int i = 0; i < GL_N; ++i) {
+        double t = m + h * gl_x[i], d = pq_density(t, k) * gl_w[i];
+        f += d;
+        g += t * d;
+    }
+    *F = h * f;
+    *M = h * g;
+}
+
+/* Integrals of f and psi*f over each of G equal panels of [0, pi/2]; the
+ * integral over a cell [a, b] adds the panels inside it and one rule over
+ * each part-panel at its ends (no differences of large cumulative sums, so
+ * the far-tail cells keep their relative accuracy). */
+#define PQ_GRID 16384
+typedef struct { int k; double pf[PQ_GRID], pm[PQ_GRID]; } pq_panels;
+
+static void pq_panels_build(pq_panels* c, int k)
+{
+    const double h = (M_PI / 2) / PQ_GRID;
+    c->k = k;
+    for (int i = 0; i < PQ_GRID; ++i) gl_cell(i * h, (i + 1) * h, k, &c->pf[i], &c->pm[i]);
+}
+
+static void pq_cell(const pq_panels* c, double a, double b, double* F, double* M)
+{
+    const double h = (M_PI / 2) / PQ_GRID;
+    int ia = (int)(a / h), ib = (int)(b / h);
+    if (ia > PQ_GRID - 1) ia = PQ_GRID - 1;
+    if (ib > PQ_GRID) ib = PQ_GRID;
+    if (ia >= ib) { gl_cell(a, b, c->k, F, M); return; }
+    double f, m, sf, sm;
+    gl_cell(a, (ia + 1) * h, c->k, &sf, &sm);
+    for (int i = ia + 1; i < ib; ++i) { sf += c->pf[i]; sm += c->pm[i]; }
+    if (ib < PQ_GRID && b > ib * h) {
+        gl_cell(ib * h, b, c->k, &f, &m);
+        sf += f;
+        sm += m;
+    }
+    *F = sf;
+    *M = sm;
+}
+
+/* Lloyd-Max quantizer with L levels for the level-l angle density (k =
+ * 2^(l-1)): a fixed point of the two optimality conditions (thresholds at
+ * the midpoints of adjacent levels, each level the centroid of its cell).
+ * Lloyd's alternation from the quantiles of f^(1/3) brings the levels within
+ * 1e-9 rad; Newton's method on the same conditions (a tridiagonal system:
+ * centroid q moves with thresholds q-1 and q, d mu/d b = f(b)(b - mu)/mass)
+ * then settles them.  Returns 0, or -1 if the residual stays above 1e-13. */
+static int pq_lloyd(int k, int L, double* lv, double* th, double* mse_out)
+{
+    gl_init();
+    pq_panels* c = (pq_panels*)malloc(sizeof(pq_panels));
+    pq_panels_build(c, k);
+    /* start: quantiles of f^(1/3), by the trapezoid rule on a fine grid */
+    {
+        const int G = 200000;
+        double* cw = (double*)malloc(sizeof(double) * (G + 1));
+        cw[0] = 0.0;
+        double prev = 0.0;
+        for (int i = 1; i <= G; ++i) {
+            double t = (M_PI / 2) * i / G, w = cbrt(pq_density(t, k));
+            cw[i] = cw[i - 1] + 0.5 * (prev + w);
+            prev = w;
+        }
+        int j = 0;
+        for (int q = 0; q < L; ++q) {
+            double target = cw[G] * (q + 0.5) / L;
+            while (j < G && cw[j + 1] < target) ++j;
+            double frac = (target - cw[j]) / (cw[j + 1] - cw[j]);
+            lv[q] = (M_PI / 2) * (j + frac) / G;
+        }
+        free(cw);
+    }
+    double* mass = (double*)malloc(sizeof(double) * (size_t)L);
+    double* mu = (double*)malloc(sizeof(double) * (size_t)L);
+    double* dl = (double*)malloc(sizeof(double) * (size_t)L);
+    double* dd = (double*)malloc(sizeof(double) * (size_t)L);
+    double* du = (double*)malloc(sizeof(double) * (size_t)L);
+    double* rhs = (double*)malloc(sizeof(double) * (size_t)L);
+    int ok = 0;
+    for (int it = 0; it < 200000; ++it) {           /* Lloyd */
+        double move = 0.0;
+        for (int q = 0; q + 1 < L; ++q) th[q] = 0.5 * (lv[q] + lv[q + 1]);
+        for (int q = 0; q < L; ++q) {
+            double F, M;
+            pq_cell(c, q ? th[q - 1] : 0.0, q + 1 < L ? th[q] : M_PI / 2, &F, &M);
+            double nv = M / F;
+            if (fabs(nv - lv[q]) > move) move = fabs(nv - lv[q]);
+            lv[q] = nv;
+        }
+        if (move <= 1e-9) break;
+    }
+    for (int it = 0; it < 60; ++it) {               /* Newton */
+        for (int q = 0; q + 1 < L; ++q) th[q] = 0.5 * (lv[q] + lv[q + 1]);
+        double resid = 0.0;
+        for (int q = 0; q < L; ++q) {
+            double F, M;
+            pq_cell(c, q ? th[q - 1] : 0.0, q + 1 < L ? th[q] : M_PI / 2, &F, &M);
+            mass[q] = F;
+            mu[q] = M / F;
+            rhs[q] = -(mu[q] - lv[q]);
+            if (fabs(rhs[q]) > resid) resid = fabs(rhs[q]);
+        }
+        if (resid <= 1e-15) { ok = 1; break; }
+        for (int q = 0; q < L; ++q) {
+            double da = 0.0, db = 0.0;   /* d mu_q / d (lower, upper edge) */
+            if (q > 0) da = pq_density(th[q - 1], k) * (mu[q] - th[q - 1]) / mass[q];
+            if (q + 1 < L) db = pq_density(th[q], k) * (th[q] - mu[q]) / mass[q];
+            dl[q] = 0.5 * da;
+            du[q] = 0.5 * db;
+            dd[q] = 0.5 * (da + db) - 1.0;
+        }
+        /* Thomas algorithm on (dl, dd, du) x = rhs */
+        for (int q = 1; q < L; ++q) {
+            double w = dl[q] / dd[q - 1];
+            dd[q] -= w * du[q - 1];
+            rhs[q] -= w * rhs[q - 1];
+        }
+        rhs[L - 1] /= dd[L - 1];
+        for (int q = L - 2; q >= 0; --q) rhs[q] = (rhs[q] - du[q] * rhs[q + 1]) / dd[q];
+        for (int q = 0; q < L; ++q) lv[q] += rhs[q];
+        if (it == 59 && resid <= 1e-13) ok = 1;
+    }
+    for (int q = 0; q + 1 < L; ++q) th[q] = 0.5 * (lv[q] + lv[q + 1]);
+    free(rhs); free(du); free(dd); free(dl); free(mu); free(mass);
+    if (mse_out) {
+        /* E[(psi - level)^2] over the normalized density, cell by cell */
+        double tot = 0.0, z = 0.0;
+        for (int i = 0; i < PQ_GRID; ++i) z += c->pf[i];
+        for (int q = 0; q < L; ++q) {
+            double a = q ? th[q - 1] : 0.0, b = q + 1 < L ? th[q] : M_PI / 2;
+            const int S = 64;
+            for (int s = 0; s < S; ++s) {
+                double lo = a + (b - a) * s / S, hi = a + (b - a) * (s + 1) / S, hh = 0.5 * (hi - lo),
+                       mm = 0.5 * (hi + lo), acc = 0.0;
+                for (int i = 0; i < GL_N; ++i) {
+                    double t = mm + hh * gl_x[i];
+                    acc += gl_w[i] * pq_density(t, k) * (t - lv[q]) * (t - lv[q]);
+                }
+                tot += hh * acc;
+            }
+        }
+        *mse_out = tot / z;
+    }
+    free(c);
+    return ok ? 0 : -1;
+}
+
+/* The codebook of one level and width, memoized: centroids (2^b) and
+ * thresholds (2^b - 1) in radians.  Level 1: uniform cells of the circle. */
+static double pq_books_lv[PQ_MAX_LEVEL + 1][PQ_MAX_BITS + 1][1 << PQ_MAX_BITS];
+static double pq_books_th[PQ_MAX_LEVEL + 1][PQ_MAX_BITS + 1][1 << PQ_MAX_BITS];
+static double pq_books_mse[PQ_MAX_LEVEL + 1][PQ_MAX_BITS + 1];
+static int pq_books_have[PQ_MAX_LEVEL + 1][PQ_MAX_BITS + 1];
+
+int kvqo_pq_codebook(int level, int bits, double* centroids, double* thresholds, double* mse)
+{
+    if (level < 1 || level > PQ_MAX_LEVEL || bits < 1 || bits > PQ_MAX_BITS) return KVQO_ERR_ARG;
+    const int L = 1 << bits;
+    if (!pq_books_have[level][bits]) {
+        double* lv = pq_books_lv[level][bits];
+        double* th = pq_books_th[level][bits];
+        if (level == 1) {
+            const double step = 2.0 * M_PI / L;
+            for (int q = 0; q < L; ++q) lv[q] = (q + 0.5) * step;
+            for (int q = 1; q < L; ++q) th[q - 1] = q * step;
+            pq_books_mse[level][bits] = step * step / 12.0;
+        } else if (pq_lloyd(1 << (level - 1), L, lv, th, &pq_books_mse[level][bits]) < 0) {
+            return KVQO_ERR_ARG;
+        }
+        pq_books_have[level][bits] = 1;
+    }
+    if (centroids) memcpy(centroids, pq_books_lv[level][bits], sizeof(double) * (size_t)L);
+    if (thresholds) memcpy(thresholds, pq_books_th[level][bits], sizeof(double) * (size_t)(L - 1));
+    if (mse) *mse = pq_books_mse[level][bits];
+    return KVQO_OK;
+}
+
+static int ilog2(int n) { int l = 0; while ((1 << l) < n) ++l; return l; }
+
+/* Bytes of one block's angle stream and of a whole row. */
+int64_t kvqo_pq_block_bytes(int n, int bits) { return ((int64_t)n * bits + 7) / 8; }
+int64_t kvqo_pq_row_bytes(int n_blocks, const int* bdims, int bits)
+{
+    int64_t s = 0;
+    for (int b = 0; b < n_blocks; ++b) s += kvqo_pq_block_bytes(bdims[b], bits);
+    return s;
+}
+
+/* The f32 decision tables: for level 1 the 2^(b-2) - 1 in-quadrant
+ * thresholds j pi / 2^(b-1) (j >= 1), for level l >= 2 the codebook's
+ * thresholds; each as the f32 roundings of its cosine and sine. */
+static int pq_decision_table(int level, int bits, float* ct, float* st)
+{
+    if (level == 1) {
+        const int nq = (1 << bits) / 4;
+        for (int j = 1; j < nq; ++j) {
+            double t = j * M_PI / (1 << (bits - 1));
+            ct[j - 1] = (float)cos(t);
+            st[j - 1] = (float)sin(t);
+        }
+        return nq - 1;
+    }
+    double th[1 << PQ_MAX_BITS];
+    if (kvqo_pq_codebook(level, bits, NULL, th, NULL) != KVQO_OK) return -1;
+    for (int j = 0; j + 1 < (1 << bits); ++j) {
+        ct[j] = (float)cos(th[j]);
+        st[j] = (float)sin(th[j]);
+    }
+    return (1 << bits) - 1;
+}
+
+int kvqo_pq_decision_table(int level, int bits, float* ct, float* st)
+{
+    return pq_decision_table(level, bits, ct, st);
+}
+
+/* number of thresholds t with psi > t, psi the angle of (lo, hi) in [0, pi/2] */
+static unsigned pq_count(float lo, float hi, const float* ct, const float* st, int n_th)
+{
+    unsigned c = 0;
+    for (int j = 0; j < n_th; ++j)
+        if (hi * ct[j] > lo * st[j]) ++c;
+    return c;
+}
+
+/* code of a level-1 pair (a, c): quadrant by exact sign swaps, then the
+ * in-quadrant cells */
+static unsigned pq_code1(float a, float c, int bits, const float* ct, const float* st, int n_th)
+{
+    unsigned q;
+    float u, w;
+    if (a > 0.0f && c >= 0.0f)      { q = 0; u = a;  w = c;  }
+    else if (a <= 0.0f && c > 0.0f) { q = 1; u = c;  w = -a; }
+    else if (a < 0.0f && c <= 0.0f) { q = 2; u = -a; w = -c; }
+    else if (a >= 0.0f && c < 0.0f) { q = 3; u = -c; w = a;  }
+    else return 0;                                   /* a zero pair */
+    return q * (unsigned)(1 << (bits - 2)) + pq_count(u, w, ct, st, n_th);
+}
+
+static void put_bits(uint8_t* s, int64_t pos, unsigned v, int bits)
+{
+    for (int i = 0; i < bits; ++i)
+        if ((v >> i) & 1u) s[(pos + i) >> 3] |= (uint8_t)(1u << ((pos + i) & 7));
+}
+
+static unsigned get_bits(const uint8_t* s, int64_t pos, int bits)
+{
+    unsigned v = 0;
+    for (int i = 0; i < bits; ++i) v |= (unsigned)((s[(pos + i) >> 3] >> ((pos + i) & 7)) & 1u) << i;
+    return v;
+}
+
+/* Encode.  codes [n_rows][row_bytes], radii [n_rows][n_blocks] f32.  A block
+ * whose radius is not finite (a NaN or infinite input, or squares past the
+ * f32 range) makes the call return KVQO_NONFINITE; its codes are then
+ * whatever the steps gave, and the other rows are encoded as usual. */
+#define KVQO_NONFINITE 3
+int kvqo_pq_encode(const float* x, int64_t n_rows, int n_blocks, const int* bdims, uint64_t seed, int bits,
+                   uint8_t* codes, float* radii)
+{
+    if (n_blocks < 1 || n_blocks > 8 || bits < 2 || bits > 6) return KVQO_ERR_ARG;
+    for (int b = 0; b < n_blocks; ++b)
+        if (!is_pow2_ge2(bdims[b]) || bdims[b] > (1 << PQ_MAX_LEVEL)) return KVQO_ERR_SHAPE;
+    const int D = row_dim(n_blocks, bdims);
+    const int64_t RB = kvqo_pq_row_bytes(n_blocks, bdims, bits);
+    int8_t* sigma = (int8_t*)malloc((size_t)D);
+    float* v = (float*)malloc(sizeof(float) * (size_t)D);
+    float* rad = (float*)malloc(sizeof(float) * (size_t)D);
+    float ct[PQ_MAX_LEVEL + 1][1 << 6], st[PQ_MAX_LEVEL + 1][1 << 6];
+    int nth[PQ_MAX_LEVEL + 1];
+    int maxl = 0;
+    for (int b = 0; b < n_blocks; ++b) if (ilog2(bdims[b]) > maxl) maxl = ilog2(bdims[b]);
+    for (int l = 1; l <= maxl; ++l) {
+        nth[l] = pq_decision_table(l, bits, ct[l], st[l]);
+        if (nth[l] < 0) { free(rad); free(v); free(sigma); return KVQO_ERR_ARG; }
+    }
+    kvqo_tq4_signs(seed, n_blocks, bdims, sigma);
+    int status = KVQO_OK;
+    memset(codes, 0, (size_t)(RB * n_rows));
+    for (int64_t t = 0; t < n_rows; ++t) {
+        const float* xr = x + t * D;
+        uint8_t* cr = codes + t * RB;
+        int off = 0;
+        int64_t boff = 0;
+        for (int b = 0; b < n_blocks; ++b) {
+            const int n = bdims[b], L = ilog2(n);
+            const float kn = (float)(1.0 / sqrt((double)n));
+            for (int i = 0; i < n; ++i) v[i] = sigma[off + i] < 0 ? -xr[off + i] : xr[off + i];
+            kvqo_fwht_f32(v, n);
+            for (int i = 0; i < n; ++i) v[i] = v[i] * kn;
+            uint8_t* s = cr + boff;
+            int64_t pos = 0;
+            /* level 1 */
+            for (int j = 0; j < n / 2; ++j) {
+                const float a = v[2 * j], c = v[2 * j + 1];
+                put_bits(s, pos, pq_code1(a, c, bits, ct[1], st[1], nth[1]), bits);
+                pos += bits;
+                rad[j] = sqrtf(a * a + c * c);
+            }
+            /* levels 2 .. L */
+            for (int l = 2, m = n / 4; l <= L; ++l, m /= 2) {
+                for (int j = 0; j < m; ++j) {
+                    const float lo = rad[2 * j], hi = rad[2 * j + 1];
+                    put_bits(s, pos, pq_count(lo, hi, ct[l], st[l], nth[l]), bits);
+                    pos += bits;
+                    rad[j] = sqrtf(lo * lo + hi * hi);
+                }
+            }
+            radii[t * n_blocks + b] = rad[0];
+            if (!isfinite(rad[0])) status = KVQO_NONFINITE;
+            off += n;
+            boff += kvqo_pq_block_bytes(n, bits);
+        }
+    }
+    free(rad);
+    free(v);
+    free(sigma);
+    return status;
+}
+
+/* Reconstruction in binary64 from the centroids: y_hat by the tree from R
+ * down, then (unless rotated != 0) x_hat = unrotate(y_hat). */
+int kvqo_pq_decode(const uint8_t* codes, const float* radii, int64_t n_rows, int n_blocks, const int* bdims,
+                   uint64_t seed, int bits, int rotated, double* xhat)
+{
+    if (n_blocks < 1 || n_blocks > 8 || bits < 2 || bits > 6) return KVQO_ERR_ARG;
+    for (int b = 0; b < n_blocks; ++b)
+        if (!is_pow2_ge2(bdims[b]) || bdims[b] > (1 << PQ_MAX_LEVEL)) return KVQO_ERR_SHAPE;
+    const int D = row_dim(n_blocks, bdims);
+    const int64_t RB = kvqo_pq_row_bytes(n_blocks, bdims, bits);
+    double* y = (double*)malloc(sizeof(double) * (size_t)D);
+    double* r = (double*)malloc(sizeof(double) * (size_t)D);
+    double* nx = (double*)malloc(sizeof(double) * (size_t)D);
+    double lv[PQ_MAX_LEVEL + 1][1 << 6];
+    int maxl = 0;
+    for (int b = 0; b < n_blocks; ++b) if (ilog2(bdims[b]) > maxl) maxl = ilog2(bdims[b]);
+    for (int l = 1; l <= maxl; ++l)
+        if (kvqo_pq_codebook(l, bits, lv[l], NULL, NULL) != KVQO_OK) { free(nx); free(r); free(y); return KVQO_ERR_ARG; }
+    for (int64_t t = 0; t < n_rows; ++t) {
+        const uint8_t* cr = codes + t * RB;
+        int off = 0;
+        int64_t boff = 0;
+        for (int b = 0; b < n_blocks; ++b) {
+            const int n = bdims[b], L = ilog2(n);
+            const uint8_t* s = cr + boff;
+            /* stream offset (in angles) of each level's first angle */
+            int64_t first[PQ_MAX_LEVEL + 2];
+            first[1] = 0;
+            for (int l = 2; l <= L; ++l) first[l] = first[l - 1] + (n >> (l - 1));
+            r[0] = (double)radii[t * n_blocks + b];
+            for (int l = L, m = 1; l >= 2; --l, m *= 2) {
+                for (int j = 0; j < m; ++j) {
+                    const double psi = lv[l][get_bits(s, (first[l] + j) * bits, bits)];
+                    nx[2 * j] = r[j] * cos(psi);
+                    nx[2 * j + 1] = r[j] * sin(psi);
+                }
+                memcpy(r, nx, sizeof(double) * (size_t)(2 * m));
+            }
+            for (int j = 0; j < n / 2; ++j) {
+                const double psi = lv[1][get_bits(s, j * bits, bits)];
+                y[off + 2 * j] = r[j] * cos(psi);
+                y[off + 2 * j + 1] = r[j] * sin(psi);
+            }
+            off += n;
+            boff += kvqo_pq_block_bytes(n, bits);
+        }
+        if (rotated) memcpy(xhat + t * D, y, sizeof(double) * (size_t)D);
+        else kvqo_tq4_rotate(y, xhat + t * D, 1, n_blocks, bdims, seed, 1);
+    }
+    free(nx);
+    free(r);
+    free(y);
+    return KVQO_OK;
+}
+
+/* The polar transform itself in binary64, without quantization: angles
+ * (level 1 first, n - 1 of them, level-1 angles in [0, 2 pi)) and the radius
+ * of each block of v, and its inverse.  Test support for the round trips. */
+int kvqo_polar_forward(const double* v, int n, double* angles, double* radius)
+{
+    if (!is_pow2_ge2(n) || n > (1 << PQ_MAX_LEVEL)) return KVQO_ERR_SHAPE;
+    double* r = (double*)malloc(sizeof(double) * (size_t)n);
+    int64_t pos = 0;
+    for (int j = 0; j < n / 2; ++j) {
+        double a = atan2(v[2 * j + 1], v[2 * j]);
+        angles[pos++] = a < 0.0 ? a + 2.0 * M_PI : a;
+        r[j] = sqrt(v[2 * j] * v[2 * j] + v[2 * j + 1] * v[2 * j + 1]);
+    }
+    for (int m = n / 4; m >= 1; m /= 2) {
+        for (int j = 0; j < m; ++j) {
+            angles[pos++] = atan2(r[2 * j + 1], r[2 * j]);
+            r[j] = sqrt(r[2 * j] * r[2 * j] + r[2 * j + 1] * r[2 * j + 1]);
+        }
+    }
+    *radius = r[0];
+    free(r);
+    return KVQO_OK;
+}
+
+int kvqo_polar_inverse(const double* angles, double radius, int n, double* v)
+{
+    if (!is_pow2_ge2(n) || n > (1 << PQ_MAX_LEVEL)) return KVQO_ERR_SHAPE;
+    double* r = (double*)malloc(sizeof(double) * (size_t)n);
+    double* nx = (double*)malloc(sizeof(double) * (size_t)n);
+    int L = ilog2(n);
+    int64_t first[PQ_MAX_LEVEL + 2];
+    first[1] = 0;
+    for (int l = 2; l <= L; ++l) first[l] = first[l - 1] + (n >> (l - 1));
+    r[0] = radius;
+    for (int l = L, m = 1; l >= 2; --l, m *= 2) {
+        for (int j = 0; j < m; ++j) {
+            nx[2 * j] = r[j] * cos(angles[first[l] + j]);
+            nx[2 * j + 1] = r[j] * sin(angles[first[l] + j]);
+        }
+        memcpy(r, nx, sizeof(double) * (size_t)(2 * m));
+    }
+    for (int j = 0; j < n / 2; ++j) {
+        v[2 * j] = r[j] * cos(angles[j]);
+        v[2 * j + 1] = r[j] * sin(angles[j]);
+    }
+    free(nx);
+    free(r);
     return KVQO_OK;
 }
 

@@ -101,6 +101,20 @@ def _declare(L):
     L.kvqo_k2v4_encode.argtypes = [P, P, C.c_int64, C.c_int64, C.POINTER(K2V4Layout), P, P, P, P, P]
     L.kvqo_k2v4_append.restype = C.c_int
     L.kvqo_k2v4_append.argtypes = [P, P, C.c_int64, C.c_int64, C.c_int64, C.POINTER(K2V4Layout), P, P, P, P, P]
+    L.kvqo_pq_codebook.restype = C.c_int
+    L.kvqo_pq_codebook.argtypes = [C.c_int, C.c_int, P, P, P]
+    L.kvqo_pq_decision_table.restype = C.c_int
+    L.kvqo_pq_decision_table.argtypes = [C.c_int, C.c_int, P, P]
+    L.kvqo_pq_row_bytes.restype = C.c_int64
+    L.kvqo_pq_row_bytes.argtypes = [C.c_int, P, C.c_int]
+    L.kvqo_pq_encode.restype = C.c_int
+    L.kvqo_pq_encode.argtypes = [P, C.c_int64, C.c_int, P, C.c_uint64, C.c_int, P, P]
+    L.kvqo_pq_decode.restype = C.c_int
+    L.kvqo_pq_decode.argtypes = [P, P, C.c_int64, C.c_int, P, C.c_uint64, C.c_int, C.c_int, P]
+    L.kvqo_polar_forward.restype = C.c_int
+    L.kvqo_polar_forward.argtypes = [P, C.c_int, P, P]
+    L.kvqo_polar_inverse.restype = C.c_int
+    L.kvqo_polar_inverse.argtypes = [P, C.c_double, C.c_int, P]
     L.kvqo_k2v4_reconstruct.restype = C.c_int
     L.kvqo_k2v4_reconstruct.argtypes = [P, P, P, P, P, C.c_int64, C.c_int64, C.POINTER(K2V4Layout),
                                         C.c_int, P, P]
@@ -249,8 +263,90 @@ def tq4_rotate(v: np.ndarray, bdims=(512, 64), seed: int = 0, inverse: bool = Fa
     return out
 
 
+# -- PolarQuant (codec 0 of the TQ tier) ------------------------------------
+
+NONFINITE = 3   # kvqo_pq_encode: some block's radius is not finite
+
+
+def pq_format(bits: int) -> int:
+    """Format number of the PolarQuant tier at ``bits`` bits per angle."""
+    return 10 + bits
+
+
+def pq_bits(fmt: int) -> int:
+    return fmt - 10 if 12 <= fmt <= 16 else 0
+
+
+def pq_codebook(level: int, bits: int):
+    """Centroids (2^bits) and thresholds (2^bits - 1) of one level's angle
+    quantizer in radians, and its mean squared error (rad^2)."""
+    lv = np.empty(1 << bits, np.float64)
+    th = np.empty((1 << bits) - 1, np.float64)
+    mse = C.c_double()
+    _check(lib().kvqo_pq_codebook(level, bits, _p(lv), _p(th), C.byref(mse)), "pq_codebook")
+    return lv, th, mse.value
+
+
+def pq_decision_table(level: int, bits: int):
+    """f32 cosines and sines of the thresholds the encoder compares against
+    (level 1: the in-quadrant thresholds)."""
+    ct = np.zeros(64, np.float32)
+    st = np.zeros(64, np.float32)
+    n = lib().kvqo_pq_decision_table(level, bits, _p(ct), _p(st))
+    if n < 0:
+        raise ValueError("oracle pq_decision_table failed")
+    return ct[:n].copy(), st[:n].copy()
+
+
+def pq_row_bytes(bits: int, bdims=(512, 64)) -> int:
+    d = _dims(bdims)
+    return int(lib().kvqo_pq_row_bytes(d.size, _p(d), bits))
+
+
+def pq_encode(x: np.ndarray, bits: int, bdims=(512, 64), seed: int = 0, allow_nonfinite: bool = False):
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    d = _dims(bdims)
+    n = x.shape[0]
+    codes = np.zeros((n, pq_row_bytes(bits, bdims)), np.uint8)
+    radii = np.zeros((n, d.size), np.float32)
+    rc = lib().kvqo_pq_encode(_p(x), n, d.size, _p(d), seed, bits, _p(codes), _p(radii))
+    if not (rc == 0 or (allow_nonfinite and rc == NONFINITE)):
+        _check(rc, "pq_encode")
+    return codes, radii
+
+
+def pq_decode(codes, radii, bits: int, bdims=(512, 64), seed: int = 0, rotated: bool = False) -> np.ndarray:
+    codes = np.ascontiguousarray(codes, np.uint8)
+    radii = np.ascontiguousarray(radii, np.float32)
+    d = _dims(bdims)
+    out = np.empty((codes.shape[0], int(d.sum())), np.float64)
+    _check(lib().kvqo_pq_decode(_p(codes), _p(radii), codes.shape[0], d.size, _p(d), seed, bits, int(rotated),
+                                _p(out)), "pq_decode")
+    return out
+
+
+def polar_forward(v: np.ndarray):
+    """Angles (level 1 first) and radius of the exact polar transform of v."""
+    v = np.ascontiguousarray(v, np.float64)
+    ang = np.empty(v.size - 1, np.float64)
+    r = C.c_double()
+    _check(lib().kvqo_polar_forward(_p(v), v.size, _p(ang), C.byref(r)), "polar_forward")
+    return ang, r.value
+
+
+def polar_inverse(angles: np.ndarray, radius: float) -> np.ndarray:
+    angles = np.ascontiguousarray(angles, np.float64)
+    out = np.empty(angles.size + 1, np.float64)
+    _check(lib().kvqo_polar_inverse(_p(angles), float(radius), out.size, _p(out)), "polar_inverse")
+    return out
+
+
 def reconstruct(fmt: int, codes, scales, bdims=(512, 64), seed: int = 0) -> np.ndarray:
-    return kv8_decode(codes, scales, bdims) if fmt == KV8 else tq4_decode(codes, scales, bdims, seed)
+    if fmt == KV8:
+        return kv8_decode(codes, scales, bdims)
+    if fmt == TQ4:
+        return tq4_decode(codes, scales, bdims, seed)
+    return pq_decode(codes, scales, pq_bits(fmt), bdims, seed)
 
 
 # -- attention ---------------------------------------------------------------
