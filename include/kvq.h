@@ -66,7 +66,20 @@ typedef enum kvq_status {
                                  no result for its work item */
 } kvq_status;
 
-typedef enum kvq_format { KVQ_KV8 = 1, KVQ_TQ4 = 2 } kvq_format;
+/* Row codecs of the MLA cache.  KV8: fp8 e4m3 codes + f32 scale per block.
+ * TQ4: rotated-int4 (codec 1 of the TQ tier).  KVQ_PQ2 .. KVQ_PQ6: PolarQuant
+ * (codec 0 of the TQ tier) with b = 2 .. 6 bits per angle ([P1] Summary:
+ * "PolarQuant ... variable 2-6 bit"; [P2] "What's in it": KV_TQ = 2|3|5|6, or
+ * 4 with KV_TQ_POLAR = 1); the format value is 10 + b. */
+typedef enum kvq_format {
+    KVQ_KV8 = 1,
+    KVQ_TQ4 = 2,
+    KVQ_PQ2 = 12,
+    KVQ_PQ3 = 13,
+    KVQ_PQ4 = 14,
+    KVQ_PQ5 = 15,
+    KVQ_PQ6 = 16
+} kvq_format;
 typedef enum kvq_dtype { KVQ_F32 = 0, KVQ_BF16 = 1 } kvq_dtype;
 
 /* Which attention kernel family runs.  AUTO picks the fastest available;
@@ -156,6 +169,55 @@ kvq_status tq4_encode(const float* x, int64_t n_rows, const kvq_mla_layout* layo
 kvq_status tq4_rotate(const void* in, kvq_dtype in_dtype, int64_t n_vecs, const kvq_mla_layout* layout,
                       int32_t inverse, float* out, void* stream);
 
+/* PolarQuant encode (codec 0 of the TQ tier; [P1] Summary and Commits item
+ * 6: "randomized-Hadamard rotation + recursive polar"; the steps of the
+ * published method, Han et al. 2025).  fmt = KVQ_PQ2 .. KVQ_PQ6 gives the
+ * width b.  Per block of n dims (a power of two, 2..1024):
+ *   y = (1/sqrt n) H_n (sigma . x)       (the TQ4 rotation, same signs)
+ *   level 1: pair j = (y_2j, y_2j+1) -> radius sqrtf(a*a + c*c) and an angle
+ *            in [0, 2 pi), coded into 2^b uniform cells [2 pi k / 2^b, ...)
+ *   level l = 2 .. log2 n: pair (lo, hi) of level-(l-1) radii -> radius
+ *            sqrtf(lo*lo + hi*hi) and the angle atan2(hi, lo) in [0, pi/2],
+ *            coded with the level's Lloyd-Max codebook for the density
+ *            sin(2 psi)^(2^(l-1) - 1)
+ *   radii     the one radius left (f32) -> radii[row][block]
+ *   codes     the n - 1 angle codes, level 1 first, b bits each, least
+ *             significant bit first: ceil(n b / 8) bytes per block, blocks in
+ *             order (72 b bytes for the 512 + 64 row; 288 + 8 at b = 4, the
+ *             TQ4 footprint)
+ * Each decision is taken in f32 without an angle: psi > t when
+ * hi * cos(t) > lo * sin(t) (f32 products of the tables' f32 cos and sin),
+ * after turning a level-1 pair into its quadrant by exact sign swaps; a tie
+ * goes to the lower cell, a zero pair to code 0.  An all-zero block stores
+ * radius 0 and codes 0.
+ *   x, dst_rows, err_word   as tq4_encode (err_word: KVQ_ERR_NONFINITE for a
+ *                           block whose radius is not finite)
+ *   codes     pool [*][kvq_row_bytes(fmt, layout)] bytes, rows written
+ *   radii     pool [*][n_blocks] f32, rows written
+ * KVQ_ERR_SHAPE for a width that is not a power of two >= 2; KVQ_ERR_ARG for
+ * a format that is not PolarQuant. */
+kvq_status pq_encode(kvq_format fmt, const float* x, int64_t n_rows, const kvq_mla_layout* layout,
+                     const int64_t* dst_rows, uint8_t* codes, float* radii, int32_t* err_word, void* stream);
+
+/* PolarQuant decode (the dequantizing consumer): each row rebuilt from its
+ * radius down the tree with the cells' centroids, in f32; rotated != 0 leaves
+ * it in the rotated domain, else it is unrotated (sigma . (1/sqrt n) H_n y).
+ *   codes, radii  as written by pq_encode;  out  [n_rows][D] f32 (device). */
+kvq_status pq_decode(kvq_format fmt, const uint8_t* codes, const float* radii, int64_t n_rows,
+                     const kvq_mla_layout* layout, int32_t rotated, float* out, void* stream);
+
+/* Bytes of one encoded row (the scales or radii excluded): KV8 D, TQ4 D/2,
+ * PolarQuant the sum over blocks of ceil(n b / 8).  0 for an invalid format
+ * or layout.  Host call. */
+int64_t kvq_row_bytes(kvq_format fmt, const kvq_mla_layout* layout);
+
+/* Copies the f32 PolarQuant tables the kernels use for width bits (2..6) and
+ * level (1..10): centroids [2^bits][2] (cos, sin of each cell's centroid) and
+ * thresholds [2^bits - 1][2] (cos, sin of each decision threshold; level 1:
+ * the 2^(bits-2) - 1 in-quadrant thresholds j pi / 2^(bits-1), the rest left
+ * untouched).  Host memory, host call, no GPU needed. */
+kvq_status kvq_pq_codebook(int32_t bits, int32_t level, float* centroids, float* thresholds);
+
 /* ------------------------------------------------------------------------ */
 /* Consumers                                                                */
 /* ------------------------------------------------------------------------ */
@@ -177,13 +239,18 @@ size_t kv_attn_workspace_size(kvq_format fmt, const kvq_mla_layout* layout, int3
  * sequences are split into chunks whose partial softmax states are merged
  * (split-T).  An empty sequence yields zeros.
  *   q           [batch][n_heads][D] in q_dtype
- *   codes       packed row pool: KV8 [rows][D] bytes, TQ4 [rows][D/2] bytes
- *   scales      [rows][n_blocks] f32
+ *   codes       packed row pool: KV8 [rows][D] bytes, TQ4 [rows][D/2] bytes,
+ *               PolarQuant [rows][kvq_row_bytes(fmt, layout)] bytes
+ *   scales      [rows][n_blocks] f32 (PolarQuant: the block radii)
  *   cu_seqlens  [batch+1] int64, device, non-decreasing, cu[0] = 0
  *   max_total_rows  host-side bound on cu_seqlens[batch] (sizes the launch)
  *   out         [batch][n_heads][v_dim] f32, written
  * Supported attention layout: D = 576 as blocks (512, 64) or (576) for KV8,
- * (512, 64) for TQ4; v_dim = 512.  Others return KVQ_ERR_UNSUPPORTED. */
+ * (512, 64) for TQ4 and PolarQuant; v_dim = 512.  Others return
+ * KVQ_ERR_UNSUPPORTED.  PolarQuant runs on the fp32 path only (it rebuilds
+ * each row's tree in the rotated domain in shared memory, tile by tile, and
+ * unrotates the context once as TQ4 does); KVQ_PATH_TENSOR with a PolarQuant
+ * format returns KVQ_ERR_UNSUPPORTED. */
 kvq_status kv_attn_decode(kvq_format fmt, const kvq_mla_layout* layout,
                           const void* q, kvq_dtype q_dtype, int32_t batch, int32_t n_heads,
                           const uint8_t* codes, const float* scales, const int64_t* cu_seqlens,
@@ -426,16 +493,17 @@ kvq_status kv_attn_decode_k2v4(const kvq_k2v4_layout* layout, const float* q, in
 /* ------------------------------------------------------------------------ */
 
 /* Files are versioned by their magic, which names the tier: "COLIKV" (v1,
- * f32 rows), "COLIKV2" (v2, KV8 codes), "COLIKV3" (v3, TQ4 codes); eight int64
+ * f32 rows), "COLIKV2" (v2, KV8 codes), "COLIKV3" (v3, TQ codes); eight int64
  * header words follow: rows, row dimension, scale blocks, the two block dims,
  * v_dim, the TQ sign seed and, in h[7], codec << 8 | bits (TQ4: codec 1, 4
- * bits).  Then one record per row: its codes, then its f32 scales (v1: its f32
- * values).  All pointers here are HOST pointers; copy device pools to the host
+ * bits; PolarQuant: codec 0, 2..6 bits, [P1] Commits item 6: "COLIKV3,
+ * h[7]=codec<<8|bits").  Then one record per row: its codes, then its f32
+ * scales or radii (v1: its f32 values).  All pointers here are HOST pointers; copy device pools to the host
  * first.  Files are written to "<path>.tmp" and renamed over `path`.
  * `msg` (optional, msg_len bytes) receives the reason of a refusal. */
 
-/* Writes a KV8 or TQ4 pool of n_rows rows (codes [n][row_bytes], scales
- * [n][n_blocks]). */
+/* Writes a KV8, TQ4 or PolarQuant pool of n_rows rows (codes
+ * [n][kvq_row_bytes(fmt, layout)], scales [n][n_blocks]). */
 kvq_status kvq_cache_save(const char* path, kvq_format fmt, const kvq_mla_layout* layout, int64_t n_rows,
                           const uint8_t* codes, const float* scales);
 

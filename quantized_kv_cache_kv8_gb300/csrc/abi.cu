@@ -4,6 +4,7 @@
 // failed check returns a status and launches nothing.  No call allocates or
 // frees device memory.
 #include "kvq_internal.cuh"
+#include "pq_common.cuh"
 
 #include <algorithm>
 #include <math.h>
@@ -50,14 +51,31 @@ static bool attn_pointers_aligned(const void* q, const uint8_t* codes, const flo
     return aligned(q, 16) && aligned(codes, 32) && aligned(scales, 8) && aligned(cu, 8) && aligned(out, 16);
 }
 
+bool is_tq(kvq_format fmt) { return fmt == KVQ_TQ4 || is_pq(fmt); }
+
 kvq_status check_attn_layout(kvq_format fmt, const kvq_mla_layout* L) {
-    kvq_status s = fmt == KVQ_TQ4 ? check_tq4_layout(L) : (fmt == KVQ_KV8 ? check_layout(L) : KVQ_ERR_ARG);
+    kvq_status s = is_tq(fmt) ? check_tq4_layout(L) : (fmt == KVQ_KV8 ? check_layout(L) : KVQ_ERR_ARG);
     if (s != KVQ_OK) return s;
     if (L->v_dim != 512) return KVQ_ERR_UNSUPPORTED;
     const bool two = L->n_blocks == 2 && L->block_dim[0] == 512 && L->block_dim[1] == 64;
     const bool one = L->n_blocks == 1 && L->block_dim[0] == 576;
-    if (fmt == KVQ_TQ4 ? !two : !(two || one)) return KVQ_ERR_UNSUPPORTED;
+    if (is_tq(fmt) ? !two : !(two || one)) return KVQ_ERR_UNSUPPORTED;
     return KVQ_OK;
+}
+
+// The encoder of a format (err: the error word a non-finite row sets).
+cudaError_t launch_encode(kvq_format fmt, const float* x, int64_t n_rows, const kvq_mla_layout& L,
+                          const int64_t* dst_rows, uint8_t* codes, float* scales, int32_t* err, cudaStream_t st) {
+    if (fmt == KVQ_KV8) return launch_kv8_encode(x, n_rows, L, dst_rows, codes, scales, err, st);
+    if (fmt == KVQ_TQ4) return launch_tq4_encode(x, n_rows, L, dst_rows, codes, scales, err, st);
+    return launch_pq_encode(pq_bits_of(fmt), x, n_rows, L, dst_rows, codes, scales, err, st);
+}
+
+int64_t format_row_bytes(kvq_format fmt, const kvq_mla_layout& L) {
+    const int D = L.block_dim[0] + (L.n_blocks > 1 ? L.block_dim[1] : 0);
+    if (fmt == KVQ_KV8) return D;
+    if (fmt == KVQ_TQ4) return D / 2;
+    return pq_row_bytes(pq_bits_of(fmt), L);
 }
 
 kvq_status cuda_status(cudaError_t e) { return e == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA; }
@@ -68,13 +86,14 @@ kvq_status check_path(kvq_path path) {
 }
 
 // The attention family that runs: AUTO takes the tensor-core kernel when it
-// supports the head count, else the SIMT kernel.  K2/V4 has only SIMT.
-kvq_status resolve_path(kvq_path path, const kvq_mla_layout* L, int32_t n_heads, kvq_path* out) {
+// supports the format and head count, else the SIMT kernel.  PolarQuant has
+// only the SIMT consumer.
+kvq_status resolve_path(kvq_format fmt, kvq_path path, const kvq_mla_layout* L, int32_t n_heads, kvq_path* out) {
     if (path == KVQ_PATH_SIMT) {
         *out = KVQ_PATH_SIMT;
         return KVQ_OK;
     }
-    const bool tc = tc_supported(*L, n_heads);
+    const bool tc = !is_pq(fmt) && tc_supported(*L, n_heads);
     if (path == KVQ_PATH_TENSOR && !tc) return KVQ_ERR_UNSUPPORTED;
     *out = tc ? KVQ_PATH_TENSOR : KVQ_PATH_SIMT;
     return KVQ_OK;
@@ -167,6 +186,46 @@ kvq_status tq4_encode(const float* x, int64_t n_rows, const kvq_mla_layout* layo
         launch_tq4_encode(x, n_rows, *layout, dst_rows, packed, scales, err_word, (cudaStream_t)stream));
 }
 
+kvq_status pq_encode(kvq_format fmt, const float* x, int64_t n_rows, const kvq_mla_layout* layout,
+                     const int64_t* dst_rows, uint8_t* codes, float* radii, int32_t* err_word, void* stream) {
+    if (!is_pq(fmt)) return KVQ_ERR_ARG;
+    kvq_status s = check_tq4_layout(layout);
+    if (s != KVQ_OK) return s;
+    if (n_rows < 0) return KVQ_ERR_ARG;
+    if (n_rows == 0) return KVQ_OK;
+    if (!x || !codes || !radii) return KVQ_ERR_ARG;
+    return cuda_status(launch_pq_encode(pq_bits_of(fmt), x, n_rows, *layout, dst_rows, codes, radii, err_word,
+                                        (cudaStream_t)stream));
+}
+
+kvq_status pq_decode(kvq_format fmt, const uint8_t* codes, const float* radii, int64_t n_rows,
+                     const kvq_mla_layout* layout, int32_t rotated, float* out, void* stream) {
+    if (!is_pq(fmt)) return KVQ_ERR_ARG;
+    kvq_status s = check_tq4_layout(layout);
+    if (s != KVQ_OK) return s;
+    if (n_rows < 0) return KVQ_ERR_ARG;
+    if (n_rows == 0) return KVQ_OK;
+    if (!codes || !radii || !out) return KVQ_ERR_ARG;
+    return cuda_status(
+        launch_pq_decode(pq_bits_of(fmt), codes, radii, n_rows, *layout, rotated != 0, out, (cudaStream_t)stream));
+}
+
+int64_t kvq_row_bytes(kvq_format fmt, const kvq_mla_layout* layout) {
+    if (fmt == KVQ_KV8) {
+        if (check_layout(layout) != KVQ_OK) return 0;
+    } else if (is_tq(fmt)) {
+        if (check_tq4_layout(layout) != KVQ_OK) return 0;
+    } else {
+        return 0;
+    }
+    return format_row_bytes(fmt, *layout);
+}
+
+kvq_status kvq_pq_codebook(int32_t bits, int32_t level, float* centroids, float* thresholds) {
+    if (!centroids || !thresholds) return KVQ_ERR_ARG;
+    return pq_host_codebook(bits, level, centroids, thresholds) ? KVQ_OK : KVQ_ERR_ARG;
+}
+
 kvq_status tq4_rotate(const void* in, kvq_dtype in_dtype, int64_t n_vecs, const kvq_mla_layout* layout,
                       int32_t inverse, float* out, void* stream) {
     kvq_status s = check_tq4_layout(layout);
@@ -186,7 +245,7 @@ size_t attn_workspace_size_waves(kvq_format fmt, const kvq_mla_layout* layout, i
     if (check_attn_layout(fmt, layout) != KVQ_OK || check_path(path) != KVQ_OK) return 0;
     if (batch < 0 || n_heads < 0 || max_total_rows < 0) return 0;
     kvq_path rp;
-    if (resolve_path(path, layout, n_heads, &rp) != KVQ_OK) return 0;
+    if (resolve_path(fmt, path, layout, n_heads, &rp) != KVQ_OK) return 0;
     const AttnPlan pl = plan_decode(fmt, rp, batch, n_heads, max_total_rows, waves);
     return kWsHeader + partial_bytes(pl.max_items, n_heads, layout->v_dim);
 }
@@ -203,7 +262,7 @@ kvq_status attn_decode_waves(kvq_format fmt, const kvq_mla_layout* layout, const
     if (batch > 65535 || n_heads > 65535) return KVQ_ERR_UNSUPPORTED;
     if (batch == 0 || n_heads == 0) return KVQ_OK;
     kvq_path rp;
-    if ((s = resolve_path(path, layout, n_heads, &rp)) != KVQ_OK) return s;
+    if ((s = resolve_path(fmt, path, layout, n_heads, &rp)) != KVQ_OK) return s;
     if (!q || !cu_seqlens || !out) return KVQ_ERR_ARG;
     if (max_total_rows > 0 && (!codes || !scales)) return KVQ_ERR_ARG;
     if (!attn_pointers_aligned(q, codes, scales, cu_seqlens, out)) return KVQ_ERR_ARG;
@@ -249,7 +308,7 @@ kvq_status kv_attn_decode_append(kvq_format fmt, const kvq_mla_layout* layout, c
     if (batch > 65535 || n_heads > 65535) return KVQ_ERR_UNSUPPORTED;
     if (batch == 0 || n_heads == 0) return KVQ_OK;
     kvq_path rp;
-    if ((s = resolve_path(path, layout, n_heads, &rp)) != KVQ_OK) return s;
+    if ((s = resolve_path(fmt, path, layout, n_heads, &rp)) != KVQ_OK) return s;
     if (!x_new || !dst_rows || !q || !cu_seqlens || !out || !codes || !scales) return KVQ_ERR_ARG;
     if (!attn_pointers_aligned(q, codes, scales, cu_seqlens, out) || !aligned(x_new, 16) || !aligned(dst_rows, 8))
         return KVQ_ERR_ARG;
@@ -265,8 +324,7 @@ kvq_status kv_attn_decode_append(kvq_format fmt, const kvq_mla_layout* layout, c
     }
     // other formats and paths: the encoder launch, then the decode
     int32_t* err = static_cast<int32_t*>(workspace);
-    const cudaError_t e = fmt == KVQ_KV8 ? launch_kv8_encode(x_new, batch, *layout, dst_rows, codes, scales, err, st)
-                                         : launch_tq4_encode(x_new, batch, *layout, dst_rows, codes, scales, err, st);
+    const cudaError_t e = launch_encode(fmt, x_new, batch, *layout, dst_rows, codes, scales, err, st);
     if (e != cudaSuccess) return KVQ_ERR_CUDA;
     return kv_attn_decode(fmt, layout, q, q_dtype, batch, n_heads, codes, scales, cu_seqlens, max_total_rows,
                           sm_scale, out, workspace, workspace_bytes, path, stream);
@@ -349,22 +407,16 @@ kvq_status kv_attn_prefill(kvq_format fmt, const kvq_mla_layout* layout, const f
     if (n_new > 65535 || n_heads > 65535) return KVQ_ERR_UNSUPPORTED;
     if (n_new == 0 || n_heads == 0) return KVQ_OK;
     kvq_path rp;
-    if ((s = resolve_path(path, layout, n_heads, &rp)) != KVQ_OK) return s;
+    if ((s = resolve_path(fmt, path, layout, n_heads, &rp)) != KVQ_OK) return s;
     if (!x_new || !q || !codes || !scales || !out) return KVQ_ERR_ARG;
     if (!attn_pointers_aligned(q, codes, scales, nullptr, out) || !aligned(x_new, 16)) return KVQ_ERR_ARG;
     if (!isfinite(sm_scale)) return KVQ_ERR_ARG;
     const size_t need = kv_attn_prefill_workspace_size(fmt, layout, n_heads, n_past, n_new, path);
     if (!workspace || workspace_bytes < need) return KVQ_ERR_WORKSPACE;
     cudaStream_t st = (cudaStream_t)stream;
-    const int D = row_dim(layout);
-    const int64_t row_bytes = fmt == KVQ_KV8 ? D : D / 2;
-    cudaError_t e;
-    if (fmt == KVQ_KV8)
-        e = launch_kv8_encode(x_new, n_new, *layout, nullptr, codes + n_past * row_bytes,
-                              scales + n_past * layout->n_blocks, static_cast<int32_t*>(workspace), st);
-    else
-        e = launch_tq4_encode(x_new, n_new, *layout, nullptr, codes + n_past * row_bytes,
-                              scales + n_past * layout->n_blocks, static_cast<int32_t*>(workspace), st);
+    const int64_t row_bytes = format_row_bytes(fmt, *layout);
+    const cudaError_t e = launch_encode(fmt, x_new, n_new, *layout, nullptr, codes + n_past * row_bytes,
+                                        scales + n_past * layout->n_blocks, static_cast<int32_t*>(workspace), st);
     if (e != cudaSuccess) return KVQ_ERR_CUDA;
     const AttnPlan pl = plan_prefill(n_past, n_new);
     if (rp == KVQ_PATH_TENSOR)

@@ -44,6 +44,10 @@ struct AttnParams {
     SignWords signs;
     float kn[2];
     float lv[16];
+    // PolarQuant rows (fp32 consumer): width, row bytes, byte offset of the
+    // rope block's stream, device centroids of the width ([level 1..10][2^b])
+    int32_t pq_bits, pq_row_bytes, pq_boff1;
+    const float2* pq_cent;
     // decode with rows appended in the same launch (tensor-core KV8 kernel):
     // x_new[b] is encoded into pool row dst_rows[b], inside [cu[b], cu[b+1])
     const float* x_new;

@@ -10,13 +10,16 @@
 // device from cu_seqlens, so nothing is synchronized with the host.
 //
 // Inside a CTA the consumer never reconstructs a row ([P2] "What's in it"):
-// a tile of 16 rows is decoded to the codes' values only (e4m3 value or TQ4
-// codebook level) and the per-row scales stay separate.  The score of head h
+// a tile of 16 rows is decoded to the codes' values only (e4m3 value, TQ4
+// codebook level, or the PolarQuant tree's leaves under a unit radius) and the
+// per-row scales (radii) stay separate.  The score of head h
 // and row t is sm_scale * (s_L * (q_L . c_L) + s_R * (q_R . c_R)) and the
 // context weight of row t is p_t * s_L: the scale is factored out of both sums.
-// For TQ4 the query is rotated in shared memory first ([P1] "Ready for
-// review" comment, finding 2).
+// For TQ4 and PolarQuant the query is rotated in shared memory first ([P1]
+// "Ready for review" comment, finding 2: the rotation is orthogonal, so
+// q . x_hat = rotate(q) . y_hat and the context unrotates once).
 #include "attn_common.cuh"
+#include "pq_common.cuh"
 
 #include <algorithm>
 #include <math.h>
@@ -33,8 +36,11 @@ constexpr int kXS = 580;  // shared-memory row stride in floats (bank spread)
 constexpr int kSmSMs = 152;
 
 // shared floats: queries, tile, row scales, weights, rescale factors, TQ4 levels (16),
-// item info (4 int64), the pool rows of a gather tile (kTR int64)
-constexpr size_t kSmemFloats = (size_t)kHG * kXS + (size_t)kTR * kXS + kTR * 2 + kTR * kHG + kHG + 16 + 8 + 2 * kTR;
+// item info (4 int64), the pool rows of a gather tile (kTR int64), the
+// PolarQuant centroids of levels 1..9 (up to 64 (cos, sin) pairs each)
+constexpr int kPqCentPairs = 9 * 64;
+constexpr size_t kSmemFloats =
+    (size_t)kHG * kXS + (size_t)kTR * kXS + kTR * 2 + kTR * kHG + kHG + 16 + 8 + 2 * kTR + 2 * kPqCentPairs;
 
 template <int FMT, bool QBF16, bool GATHER>
 __global__ void __launch_bounds__(kNT, 2) attn_partial_kernel(AttnParams p) {
@@ -48,6 +54,7 @@ __global__ void __launch_bounds__(kNT, 2) attn_partial_kernel(AttnParams p) {
     float* lvs = alpha + kHG;
     int64_t* info = reinterpret_cast<int64_t*>(lvs + 16);
     int64_t* prow = info + 4;   // gather: the pool rows of the tile
+    float2* pqc = reinterpret_cast<float2*>(prow + kTR);   // PolarQuant centroids
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int64_t item = blockIdx.x;
@@ -62,6 +69,8 @@ __global__ void __launch_bounds__(kNT, 2) attn_partial_kernel(AttnParams p) {
         }
     }
     if (tid < 16) lvs[tid] = p.lv[tid];
+    if (FMT == kFmtPolar)
+        for (int i = tid; i < (9 << p.pq_bits); i += kNT) pqc[i] = p.pq_cent[i];
     __syncthreads();
     const int b = (int)info[0];
     if (b < 0) return;
@@ -75,7 +84,7 @@ __global__ void __launch_bounds__(kNT, 2) attn_partial_kernel(AttnParams p) {
         qs[h * kXS + d] = v;
     }
     __syncthreads();
-    if (FMT == KVQ_TQ4) {
+    if (FMT != KVQ_KV8) {
         // rotate each head's query once: latent block (512) and rope block (64)
         for (int hh = warp; hh < kHG; hh += kNT / 32) {
             float* qh = qs + hh * kXS;
@@ -137,6 +146,19 @@ __global__ void __launch_bounds__(kNT, 2) attn_partial_kernel(AttnParams p) {
                     f = make_float4(a.x, a.y, c.x, c.y);
                 }
                 *reinterpret_cast<float4*>(xs + r * kXS + c4) = f;
+            }
+        } else if (FMT == kFmtPolar) {
+            // each warp rebuilds whole rows: the latent and rope trees with unit
+            // top radius, in the rotated domain (the radii stay in sc)
+            for (int r = warp; r < kTR; r += kNT / 32) {
+                float* xr = xs + r * kXS;
+                if (r < nt) {
+                    const uint8_t* cr = p.codes + (GATHER ? prow[r] : t0 + r) * p.pq_row_bytes;
+                    pq_expand_block(cr, kDL, 9, p.pq_bits, 1.0f, pqc, xr, lane);
+                    pq_expand_block(cr + p.pq_boff1, kMlaDR, 6, p.pq_bits, 1.0f, pqc, xr + kDL, lane);
+                } else {
+                    for (int i = lane; i < kD; i += 32) xr[i] = 0.0f;
+                }
             }
         } else {
             const uint32_t* src = reinterpret_cast<const uint32_t*>(p.codes + t0 * (kD / 2));
@@ -422,12 +444,18 @@ AttnParams make_attn_params(kvq_format fmt, const kvq_mla_layout& L, const void*
     p.wait_limit = p.stall_polls > 0 ? p.stall_polls : kWaitLimit;
     p.ws_o = reinterpret_cast<float*>(ws + kWsHeader);
     p.ws_ml = p.ws_o + (size_t)plan.max_items * n_heads * kMlaDV;
-    if (fmt == KVQ_TQ4) {
+    if (fmt != KVQ_KV8) {
         p.signs = tq4_sign_words(L);
         p.kn[0] = (float)(1.0 / sqrt((double)L.block_dim[0]));
         p.kn[1] = (float)(1.0 / sqrt((double)L.block_dim[1]));
         const Codebook16 cb = tq4_codebook();
         for (int k = 0; k < 16; ++k) p.lv[k] = cb.lv[k];
+    }
+    if (is_pq(fmt)) {
+        p.pq_bits = pq_bits_of(fmt);
+        p.pq_boff1 = (int32_t)pq_block_bytes(L.block_dim[0], p.pq_bits);
+        p.pq_row_bytes = (int32_t)pq_row_bytes(p.pq_bits, L);
+        p.pq_cent = pq_device_centroids(p.pq_bits);
     }
     return p;
 }
@@ -451,6 +479,10 @@ cudaError_t launch_attn_simt(kvq_format fmt, const kvq_mla_layout& L, const void
     if (fmt == KVQ_KV8)
         e = qdt == KVQ_BF16 ? launch_partial<KVQ_KV8, true>(p, plan.max_items, groups, stream)
                             : launch_partial<KVQ_KV8, false>(p, plan.max_items, groups, stream);
+    else if (is_pq(fmt))
+        e = !p.pq_cent ? cudaErrorInvalidSymbol
+            : qdt == KVQ_BF16 ? launch_partial<kFmtPolar, true>(p, plan.max_items, groups, stream)
+                              : launch_partial<kFmtPolar, false>(p, plan.max_items, groups, stream);
     else
         e = qdt == KVQ_BF16 ? launch_partial<KVQ_TQ4, true>(p, plan.max_items, groups, stream)
                             : launch_partial<KVQ_TQ4, false>(p, plan.max_items, groups, stream);

@@ -180,6 +180,14 @@ cudaError_t launch_tq4_encode(const float* x, int64_t n_rows, const kvq_mla_layo
                               uint8_t* packed, float* scales, int32_t* err, cudaStream_t stream);
 cudaError_t launch_tq4_rotate(const void* in, kvq_dtype dt, int64_t n_vecs, const kvq_mla_layout& L, int inverse,
                               float* out, cudaStream_t stream);
+// PolarQuant (pq.cu): b = bits per angle; codes [*][pq_row_bytes], radii [*][n_blocks]
+cudaError_t launch_pq_encode(int bits, const float* x, int64_t n_rows, const kvq_mla_layout& L,
+                             const int64_t* dst_rows, uint8_t* codes, float* radii, int32_t* err,
+                             cudaStream_t stream);
+cudaError_t launch_pq_decode(int bits, const uint8_t* codes, const float* radii, int64_t n_rows,
+                             const kvq_mla_layout& L, int rotated, float* out, cudaStream_t stream);
+int64_t pq_row_bytes(int bits, const kvq_mla_layout& L);
+bool pq_host_codebook(int bits, int level, float* centroids, float* thresholds);
 
 // SIMT attention over the 576 = 512 + 64 latent layout.
 struct AttnPlan {

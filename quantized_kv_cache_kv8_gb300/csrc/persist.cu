@@ -17,10 +17,13 @@
 //   magic   8 bytes: "COLIKV\0\0" | "COLIKV2\0" | "COLIKV3\0"
 //   h[0..7] 8 x int64: rows, row dimension D, number of scale blocks, block
 //           dims (2), v_dim, TQ sign seed (0 for KV8 and f32), codec << 8 | bits
-//           (TQ: codec 1 = rotated-int4, 4 bits; 0 otherwise)
-//   payload one record per row -- v1: D f32; v2/v3: the row's codes
-//           (row_bytes) then its n_blocks f32 scales (584 bytes for a KV8 row
-//           of 512 + 64 dims, 296 for TQ4), so rows append in place
+//           (TQ: codec 1 = rotated-int4 at 4 bits, codec 0 = PolarQuant at
+//           2..6 bits; 0 for KV8 and f32)
+//   payload one record per row -- v1: D f32; v2/v3: the row's codes then its
+//           n_blocks f32 scales (584 bytes for a KV8 row of 512 + 64 dims, 296
+//           for TQ4, 72 b + 8 for PolarQuant at b bits), so rows append in
+//           place.  A v3 record's code bytes follow from h[7]: D b / 8 for
+//           codec 1, the sum over blocks of ceil(n b / 8) for codec 0.
 #include "kvq_internal.cuh"
 
 #include <stdint.h>
@@ -36,7 +39,22 @@ namespace {
 
 constexpr int kHeaderWords = 8;
 constexpr int64_t kHeaderBytes = 8 + kHeaderWords * 8;
-constexpr int32_t kTq4Codec = 1, kTq4Bits = 4;
+constexpr int32_t kTq4Codec = 1, kTq4Bits = 4, kPolarCodec = 0;
+
+// The tier (file version) and the TQ codec word of a format.
+struct Mode {
+    int version;
+    int64_t codec_bits;   // h[7]
+};
+
+bool is_pq_format(kvq_format f) { return f >= KVQ_PQ2 && f <= KVQ_PQ6; }
+bool format_ok(kvq_format f) { return f == KVQ_KV8 || f == KVQ_TQ4 || is_pq_format(f); }
+
+Mode mode_of(kvq_format fmt) {
+    if (fmt == KVQ_KV8) return {2, 0};
+    if (fmt == KVQ_TQ4) return {3, (int64_t)kTq4Codec << 8 | kTq4Bits};
+    return {3, (int64_t)kPolarCodec << 8 | ((int)fmt - 10)};
+}
 
 const char* magic_of(int version) {
     switch (version) {
@@ -56,12 +74,18 @@ const char* tier_name(int version) {
     return version == 1 ? "f32" : version == 2 ? "fp8 (KV8)" : "KV_TQ";
 }
 
-int version_of_format(kvq_format fmt) { return fmt == KVQ_KV8 ? 2 : 3; }
-
 int64_t row_dim(const kvq_mla_layout& L) { return L.block_dim[0] + (L.n_blocks > 1 ? L.block_dim[1] : 0); }
 
+// code bytes of one row of a TQ codec word (codec << 8 | bits)
+int64_t tq_code_bytes(int64_t codec_bits, int64_t d0, int64_t d1) {
+    const int64_t codec = codec_bits >> 8, bits = codec_bits & 255;
+    if (codec == kPolarCodec) return (d0 * bits + 7) / 8 + (d1 * bits + 7) / 8;
+    return (d0 + d1) * bits / 8;
+}
+
 int64_t row_bytes(kvq_format fmt, const kvq_mla_layout& L) {
-    return fmt == KVQ_KV8 ? row_dim(L) : row_dim(L) / 2;
+    if (fmt == KVQ_KV8) return row_dim(L);
+    return tq_code_bytes(mode_of(fmt).codec_bits, L.block_dim[0], L.n_blocks > 1 ? L.block_dim[1] : 0);
 }
 
 void put_msg(char* msg, size_t len, const std::string& s) {
@@ -80,7 +104,8 @@ struct Header {
     int64_t h[kHeaderWords];
 };
 
-void fill_header(Header* H, int version, const kvq_mla_layout& L, int64_t rows) {
+void fill_header(Header* H, Mode m, const kvq_mla_layout& L, int64_t rows) {
+    const int version = m.version;
     H->version = version;
     H->h[0] = rows;
     H->h[1] = row_dim(L);
@@ -89,12 +114,12 @@ void fill_header(Header* H, int version, const kvq_mla_layout& L, int64_t rows) 
     H->h[4] = L.n_blocks > 1 ? L.block_dim[1] : 0;
     H->h[5] = L.v_dim;
     H->h[6] = version == 3 ? (int64_t)L.seed : 0;
-    H->h[7] = version == 3 ? ((int64_t)kTq4Codec << 8 | kTq4Bits) : 0;
+    H->h[7] = version == 3 ? m.codec_bits : 0;
 }
 
 int64_t payload_row_bytes(const Header& H) {
     if (H.version == 1) return H.h[1] * 4;
-    const int64_t codes = H.version == 2 ? H.h[1] : H.h[1] / 2;
+    const int64_t codes = H.version == 2 ? H.h[1] : tq_code_bytes(H.h[7], H.h[3], H.h[4]);
     return codes + H.h[2] * 4;
 }
 
@@ -117,7 +142,8 @@ kvq_status read_header(FILE* f, Header* H, int64_t* file_bytes, char* msg, size_
     }
     const int64_t* h = H->h;
     if (h[0] < 0 || h[1] <= 0 || (h[2] != 1 && h[2] != 2) || h[3] <= 0 || h[4] < 0 || h[3] + h[4] != h[1] ||
-        (h[2] == 2) != (h[4] > 0) || h[5] <= 0 || h[5] > h[1]) {
+        (h[2] == 2) != (h[4] > 0) || h[5] <= 0 || h[5] > h[1] ||
+        (H->version == 3 && ((h[7] & 255) < 1 || (h[7] & 255) > 16 || (h[7] >> 8) < 0 || (h[7] >> 8) > 255))) {
         put_msg(msg, msg_len, "corrupt quantized cache header");
         return KVQ_ERR_IO;
     }
@@ -147,14 +173,15 @@ kvq_status open_checked(const char* path, FILE** f, Header* H, int64_t* file_byt
 }
 
 // The stored tier, codec and layout against the caller's; explains a refusal.
-kvq_status check_mode(const Header& H, int want_version, const kvq_mla_layout& L, char* msg, size_t msg_len) {
+kvq_status check_mode(const Header& H, Mode want_mode, const kvq_mla_layout& L, char* msg, size_t msg_len) {
+    const int want_version = want_mode.version;
     if (H.version != want_version) {
         put_msg(msg, msg_len, std::string("file is ") + tier_name(H.version) + ", current mode is " +
                                   tier_name(want_version) + ": refused");
         return KVQ_ERR_MISMATCH;
     }
     Header want;
-    fill_header(&want, want_version, L, 0);
+    fill_header(&want, want_mode, L, 0);
     if (want_version == 3 && H.h[7] != want.h[7]) {
         char b[160];
         snprintf(b, sizeof b, "file is KV_TQ (codec %lld, %lld-bit), current is KV_TQ (codec %lld, %lld-bit): refused",
@@ -217,17 +244,17 @@ extern "C" {
 
 kvq_status kvq_cache_save(const char* path, kvq_format fmt, const kvq_mla_layout* layout, int64_t n_rows,
                           const uint8_t* codes, const float* scales) {
-    if (!path || !layout_ok(layout) || (fmt != KVQ_KV8 && fmt != KVQ_TQ4) || n_rows < 0) return KVQ_ERR_ARG;
+    if (!path || !layout_ok(layout) || !format_ok(fmt) || n_rows < 0) return KVQ_ERR_ARG;
     if (n_rows > 0 && (!codes || !scales)) return KVQ_ERR_ARG;
     Header H;
-    fill_header(&H, version_of_format(fmt), *layout, n_rows);
+    fill_header(&H, mode_of(fmt), *layout, n_rows);
     return write_file(path, H, n_rows, row_bytes(fmt, *layout), layout->n_blocks * 4, codes, scales);
 }
 
 kvq_status kvq_cache_save_f32(const char* path, const kvq_mla_layout* layout, int64_t n_rows, const float* rows) {
     if (!path || !layout_ok(layout) || n_rows < 0 || (n_rows > 0 && !rows)) return KVQ_ERR_ARG;
     Header H;
-    fill_header(&H, 1, *layout, n_rows);
+    fill_header(&H, Mode{1, 0}, *layout, n_rows);
     return write_file(path, H, n_rows, row_dim(*layout) * 4, 0, rows, nullptr);
 }
 
@@ -247,12 +274,12 @@ kvq_status kvq_cache_info(const char* path, int32_t* version, int64_t* n_rows, i
 }
 
 // Shared by the two loaders: open, check the mode, check the byte count.
-static kvq_status open_for_load(const char* path, int version, const kvq_mla_layout& L, int64_t capacity, FILE** f,
+static kvq_status open_for_load(const char* path, Mode mode, const kvq_mla_layout& L, int64_t capacity, FILE** f,
                                 Header* H, char* msg, size_t msg_len) {
     int64_t bytes = 0;
     kvq_status s = open_checked(path, f, H, &bytes, msg, msg_len);
     if (s != KVQ_OK) return s;
-    if ((s = check_mode(*H, version, L, msg, msg_len)) != KVQ_OK) {
+    if ((s = check_mode(*H, mode, L, msg, msg_len)) != KVQ_OK) {
         fclose(*f);
         return s;
     }
@@ -271,11 +298,11 @@ static kvq_status open_for_load(const char* path, int version, const kvq_mla_lay
 
 kvq_status kvq_cache_load(const char* path, kvq_format fmt, const kvq_mla_layout* layout, int64_t capacity,
                           uint8_t* codes, float* scales, int64_t* n_rows, char* msg, size_t msg_len) {
-    if (!path || !layout_ok(layout) || (fmt != KVQ_KV8 && fmt != KVQ_TQ4) || capacity < 0 || !n_rows)
+    if (!path || !layout_ok(layout) || !format_ok(fmt) || capacity < 0 || !n_rows)
         return KVQ_ERR_ARG;
     FILE* f;
     Header H;
-    kvq_status s = open_for_load(path, version_of_format(fmt), *layout, capacity, &f, &H, msg, msg_len);
+    kvq_status s = open_for_load(path, mode_of(fmt), *layout, capacity, &f, &H, msg, msg_len);
     if (s != KVQ_OK) return s;
     const int64_t n = H.h[0];
     const bool ok = (n == 0 || (codes && scales)) &&
@@ -291,7 +318,7 @@ kvq_status kvq_cache_load_f32(const char* path, const kvq_mla_layout* layout, in
     if (!path || !layout_ok(layout) || capacity < 0 || !n_rows) return KVQ_ERR_ARG;
     FILE* f;
     Header H;
-    kvq_status s = open_for_load(path, 1, *layout, capacity, &f, &H, msg, msg_len);
+    kvq_status s = open_for_load(path, Mode{1, 0}, *layout, capacity, &f, &H, msg, msg_len);
     if (s != KVQ_OK) return s;
     const int64_t n = H.h[0];
     const bool ok = (n == 0 || rows) && read_records(f, n, row_dim(*layout) * 4, 0, rows, nullptr);
@@ -303,7 +330,7 @@ kvq_status kvq_cache_load_f32(const char* path, const kvq_mla_layout* layout, in
 
 kvq_status kvq_cache_append(const char* path, kvq_format fmt, const kvq_mla_layout* layout, int64_t n_new,
                             const uint8_t* codes, const float* scales, int64_t* n_rows, char* msg, size_t msg_len) {
-    if (!path || !layout_ok(layout) || (fmt != KVQ_KV8 && fmt != KVQ_TQ4) || n_new < 0) return KVQ_ERR_ARG;
+    if (!path || !layout_ok(layout) || !format_ok(fmt) || n_new < 0) return KVQ_ERR_ARG;
     if (n_new > 0 && (!codes || !scales)) return KVQ_ERR_ARG;
     FILE* f;
     Header H;
@@ -311,7 +338,7 @@ kvq_status kvq_cache_append(const char* path, kvq_format fmt, const kvq_mla_layo
     kvq_status s = open_checked(path, &f, &H, &bytes, msg, msg_len);
     if (s != KVQ_OK) return s;
     fclose(f);
-    if ((s = check_mode(H, version_of_format(fmt), *layout, msg, msg_len)) != KVQ_OK) return s;
+    if ((s = check_mode(H, mode_of(fmt), *layout, msg, msg_len)) != KVQ_OK) return s;
     const int64_t rec = payload_row_bytes(H), committed = kHeaderBytes + H.h[0] * rec;
     if (bytes < committed) {
         put_msg(msg, msg_len, "file is shorter than its header says: refused");

@@ -16,6 +16,7 @@ import torch
 from . import build as _build
 
 KVQ_KV8, KVQ_TQ4 = 1, 2
+KVQ_PQ2, KVQ_PQ3, KVQ_PQ4, KVQ_PQ5, KVQ_PQ6 = 12, 13, 14, 15, 16   # PolarQuant, 10 + bits
 KVQ_F32, KVQ_BF16 = 0, 1
 PATH_AUTO, PATH_SIMT, PATH_TENSOR = 0, 1, 2
 SM_SCALE_MLA = 1.0 / math.sqrt(192.0)
@@ -75,6 +76,14 @@ def _declare(L):
     L.tq4_encode.argtypes = [P, I64, pl, P, P, P, P, P]
     L.kvq_test_stall_waits.restype = C.c_int
     L.kvq_test_stall_waits.argtypes = [I64]
+    L.pq_encode.restype = C.c_int
+    L.pq_encode.argtypes = [C.c_int, P, I64, pl, P, P, P, P, P]
+    L.pq_decode.restype = C.c_int
+    L.pq_decode.argtypes = [C.c_int, P, P, I64, pl, I32, P, P]
+    L.kvq_row_bytes.restype = I64
+    L.kvq_row_bytes.argtypes = [C.c_int, pl]
+    L.kvq_pq_codebook.restype = C.c_int
+    L.kvq_pq_codebook.argtypes = [I32, I32, P, P]
     L.tq4_rotate.restype = C.c_int
     L.tq4_rotate.argtypes = [P, C.c_int, I64, pl, I32, P, P]
     L.kv_attn_workspace_size.restype = S
@@ -199,6 +208,53 @@ def tq4_encode(x, packed, scales, layout: MLALayout | None = None, dst_rows=None
 def tq4_encode_status(x, packed, scales, layout: MLALayout, stream=None) -> int:
     return lib().tq4_encode(_ptr(x, torch.float32, "x"), x.shape[0], C.byref(layout), None, _ptr(packed),
                             _ptr(scales), None, _stream(stream))
+
+
+def pq_format(bits: int) -> int:
+    """The PolarQuant format at `bits` (2..6) bits per angle."""
+    if not 2 <= bits <= 6:
+        raise ValueError("PolarQuant widths are 2..6 bits")
+    return 10 + bits
+
+
+def row_bytes(fmt: int, layout: MLALayout | None = None) -> int:
+    """Code bytes of one row of `fmt` (scales excluded); raises for an invalid pair."""
+    layout = layout or mla_layout()
+    n = lib().kvq_row_bytes(fmt, C.byref(layout))
+    if n <= 0:
+        raise KvqError(1, "kvq_row_bytes")
+    return n
+
+
+def pq_codebook(bits: int, level: int):
+    """The library's f32 PolarQuant tables of one width and level: centroids
+    [2^bits][2] and thresholds [2^bits - 1][2] (cos, sin); level 1 gives its
+    2^(bits-2) - 1 in-quadrant thresholds."""
+    import numpy as np
+    n = 1 << bits
+    c = np.zeros((n, 2), np.float32)
+    t = np.zeros((n - 1, 2), np.float32)
+    _ok(lib().kvq_pq_codebook(bits, level, c.ctypes.data_as(C.c_void_p), t.ctypes.data_as(C.c_void_p)),
+        "kvq_pq_codebook")
+    return c, (t[: n // 4 - 1] if level == 1 else t)
+
+
+def pq_encode(fmt: int, x, codes, radii, layout: MLALayout | None = None, dst_rows=None, stream=None,
+              err_word=None):
+    """PolarQuant-encode rows of x into the pool (codes [*][row_bytes], radii
+    [*][n_blocks]); row i goes to pool row dst_rows[i] (or i)."""
+    layout = layout or mla_layout()
+    _ok(lib().pq_encode(fmt, _ptr(x, torch.float32, "x"), x.shape[0], C.byref(layout),
+                        _ptr(dst_rows, torch.int64, "dst_rows"), _ptr(codes, torch.uint8, "codes"),
+                        _ptr(radii, torch.float32, "radii"), _err_ptr(err_word), _stream(stream)), "pq_encode")
+
+
+def pq_decode(fmt: int, codes, radii, out, layout: MLALayout | None = None, rotated: bool = False, stream=None):
+    """Rebuild PolarQuant rows as f32 (unrotated, or in the rotated domain)."""
+    layout = layout or mla_layout()
+    _ok(lib().pq_decode(fmt, _ptr(codes, torch.uint8, "codes"), _ptr(radii, torch.float32, "radii"),
+                        codes.shape[0], C.byref(layout), int(rotated), _ptr(out, torch.float32, "out"),
+                        _stream(stream)), "pq_decode")
 
 
 def test_stall_waits(polls: int) -> None:
@@ -392,8 +448,7 @@ def _np_ptr(a):
 
 
 def _row_bytes(fmt: int, layout: MLALayout) -> int:
-    D = sum(layout.block_dim[b] for b in range(layout.n_blocks))
-    return D if fmt == KVQ_KV8 else D // 2
+    return row_bytes(fmt, layout)
 
 
 def cache_save(path: str, fmt: int, codes, scales, layout: MLALayout | None = None):

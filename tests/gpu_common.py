@@ -53,12 +53,14 @@ def gpu_encode(kvq, fmt, x: np.ndarray, layout):
     D = x.shape[1]
     n = x.shape[0]
     nb = layout.n_blocks
-    row = D if fmt == kvq.KVQ_KV8 else D // 2
+    row = kvq.row_bytes(fmt, layout)
     codes = torch.empty((n, row), dtype=torch.uint8, device="cuda")
     scales = torch.empty((n, nb), dtype=torch.float32, device="cuda")
     xt = to_dev(x)
     if fmt == kvq.KVQ_KV8:
         kvq.kv8_encode(xt, codes, scales, layout)
-    else:
+    elif fmt == kvq.KVQ_TQ4:
         kvq.tq4_encode(xt, codes, scales, layout)
+    else:
+        kvq.pq_encode(fmt, xt, codes, scales, layout)
     return codes, scales

@@ -215,3 +215,47 @@ def test_stall_hook_rejects_a_negative_count(kvq):
 def test_new_status_strings(kvq):
     assert "NaN" in kvq.status_string(9)
     assert "wait" in kvq.status_string(10)
+
+
+def test_polar_tables_equal_the_oracle(kvq, oracle):
+    """The f32 cos/sin tables compiled into the library (derived by
+    csrc/gen_pq_codebook.py) against the oracle's own codebooks, bit for bit:
+    centroids as f32(cos), f32(sin) of the oracle's f64 centroids, thresholds
+    as the oracle's f32 decision tables."""
+    for bits in range(2, 7):
+        for level in range(1, 11):
+            c, t = kvq.pq_codebook(bits, level)
+            lv, _, _ = oracle.pq_codebook(level, bits)
+            want = np.stack([np.cos(lv), np.sin(lv)], 1).astype(np.float32)
+            np.testing.assert_array_equal(c.view(np.uint32), want.view(np.uint32))
+            ct, st = oracle.pq_decision_table(level, bits)
+            np.testing.assert_array_equal(t[:, 0].view(np.uint32), ct.view(np.uint32))
+            np.testing.assert_array_equal(t[:, 1].view(np.uint32), st.view(np.uint32))
+
+
+def test_polar_row_bytes_and_validation(kvq, oracle):
+    L = kvq.lib()
+    lay = kvq.mla_layout()
+    for bits in range(2, 7):
+        fmt = kvq.pq_format(bits)
+        assert kvq.row_bytes(fmt) == 72 * bits == oracle.pq_row_bytes(bits)
+        for bd in [(64,), (2,), (1024,), (16, 32)]:
+            lo = kvq.mla_layout(bd, v_dim=bd[0])
+            assert kvq.row_bytes(fmt, lo) == oracle.pq_row_bytes(bits, bd)
+    assert kvq.row_bytes(kvq.KVQ_KV8) == 576 and kvq.row_bytes(kvq.KVQ_TQ4) == 288
+    assert L.kvq_row_bytes(11, C.byref(lay)) == 0 and L.kvq_row_bytes(17, C.byref(lay)) == 0
+    d = C.c_void_p(256)
+    assert L.pq_encode(kvq.KVQ_TQ4, d, 4, C.byref(lay), None, d, d, None, None) == 1     # not a PolarQuant format
+    assert L.pq_encode(14, None, 0, C.byref(lay), None, None, None, None, None) == 0       # empty
+    assert L.pq_encode(14, None, 4, C.byref(lay), None, d, d, None, None) == 1             # null x
+    odd = kvq.mla_layout((500, 76), v_dim=500)
+    assert L.pq_encode(14, d, 4, C.byref(odd), None, d, d, None, None) == 2
+    assert L.pq_decode(14, d, d, 4, C.byref(odd), 0, d, None) == 2
+    assert L.pq_decode(2, d, d, 4, C.byref(lay), 0, d, None) == 1
+    # attention: the fp32 path serves PolarQuant, the tensor path refuses it
+    assert kvq.kv_attn_workspace_size(14, 8, 128, 32768) == kvq.kv_attn_workspace_size(14, 8, 128, 32768,
+                                                                                        path=kvq.PATH_SIMT) > 0
+    assert kvq.kv_attn_workspace_size(14, 8, 128, 32768, path=kvq.PATH_TENSOR) == 0
+    ws = C.c_void_p(1 << 21)
+    assert L.kv_attn_decode(14, C.byref(lay), d, 1, 2, 128, d, d, d, 10, 0.1, d, ws, 1 << 30, kvq.PATH_TENSOR,
+                            None) == 5

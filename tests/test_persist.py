@@ -164,3 +164,44 @@ def test_header_row_count_out_of_range_is_refused(kvq, oracle, tmp_path, rows):
         with pytest.raises(kvq.CacheFileError) as e:
             call()
         assert e.value.status == IO
+
+
+@pytest.mark.parametrize("bits", [2, 3, 4, 5, 6])
+def test_polar_pools_round_trip_under_codec_0(kvq, oracle, tmp_path, bits):
+    """PolarQuant pools persist in the TQ tier (COLIKV3) with h[7] = 0 << 8 | b
+    and records of 72 b code bytes + 8 radius bytes."""
+    x = synth.mla_rows(9, 23)
+    codes, radii = oracle.pq_encode(x, bits, seed=4)
+    fmt = 10 + bits
+    lay = kvq.mla_layout(seed=4)
+    path = str(tmp_path / f"pq{bits}")
+    kvq.cache_save(path, fmt, codes, radii, lay)
+    raw = open(path, "rb").read()
+    assert raw[:8] == b"COLIKV3\0" and len(raw) == 72 + 23 * (72 * bits + 8)
+    h = np.frombuffer(raw[8:72], np.int64)
+    assert h[7] == bits and h[6] == 4
+    c2, r2 = kvq.cache_load(path, fmt, 30, lay)
+    np.testing.assert_array_equal(c2, codes)
+    np.testing.assert_array_equal(r2.view(np.uint32), radii.view(np.uint32))
+    kvq.cache_append(path, fmt, codes[:3], radii[:3], lay)
+    c3, _ = kvq.cache_load(path, fmt, 30, lay)
+    np.testing.assert_array_equal(c3[23:], codes[:3])
+
+
+def test_polar_and_rotated_int4_refuse_each_other(kvq, oracle, tmp_path):
+    lay = kvq.mla_layout(seed=4)
+    x = synth.mla_rows(10, 5)
+    pq, pr = oracle.pq_encode(x, 4, seed=4)
+    tq, ts = oracle.tq4_encode(x, seed=4)
+    p_pq, p_tq = str(tmp_path / "pq"), str(tmp_path / "tq")
+    kvq.cache_save(p_pq, 14, pq, pr, lay)
+    kvq.cache_save(p_tq, TQ4, tq, ts, lay)
+    with pytest.raises(kvq.CacheFileError) as e:
+        kvq.cache_load(p_pq, TQ4, 10, lay)
+    assert e.value.status == MISMATCH and "codec 0, 4-bit" in e.value.msg and "codec 1, 4-bit" in e.value.msg
+    with pytest.raises(kvq.CacheFileError) as e:
+        kvq.cache_load(p_tq, 14, 10, lay)
+    assert e.value.status == MISMATCH
+    with pytest.raises(kvq.CacheFileError) as e:
+        kvq.cache_load(p_pq, 13, 10, lay)
+    assert e.value.status == MISMATCH and "codec 0, 3-bit" in e.value.msg
