@@ -14,13 +14,15 @@
 // chunks, as the MN-major A operand of the context.  P^T takes the rope
 // chunk's slot once the score of the tile has completed.
 //
-// Pipeline per tile t (8 worker warps, 1 MMA warp):
+// Pipeline per tile t (8 worker warps, 1 MMA warp; the MMA warp's warpgroup,
+// padded with three idle warps, hands its registers to the workers):
 //   workers: decode the tile in three groups -- chunks 0-3 (row bytes
 //            0..255), chunks 4-7 (256..511), the rope chunk 8 (512..575) --
 //            each as soon as the context of tile t-1 has released its slots,
 //            then the softmax of tile t (thread = row, 32 heads), then P^T.
-//            The raw bytes of tile t+1 are loaded into registers during tile t
-//            (group A before the softmax, groups B and C after P^T).
+//            The raw bytes of tile t+1 are loaded into registers during tile t,
+//            all three groups before the softmax (they stay live across it in
+//            the workers' 232 registers).
 //   MMA:     score of tile t group by group, commit; once P^T(t) is written,
 //            the 4 context blocks, each committed to its slot pair's barrier.
 // The decode of tile t+1 thus overlaps the context MMAs of tile t, and the
@@ -60,7 +62,13 @@ using namespace tc;
 constexpr int kRows = 128;      // rows per tile
 constexpr int kHC = 64;         // heads per CTA
 constexpr int kWorkers = 256;
-constexpr int kThreads = kWorkers + 32;
+// warpgroup 2 holds the MMA-issuing warp and three idle warps: after the
+// prologue it gives its registers to the eight worker warps (setmaxnreg), so
+// the tile loop runs with kRegsWorker registers per thread instead of the
+// 168 a 384-thread launch allows
+constexpr int kThreads = kWorkers + 128;
+constexpr int kRegsLaunch = 168, kRegsWorker = 232, kRegsMma = 40;
+static_assert(kWorkers * kRegsWorker + 128 * kRegsMma <= kThreads * kRegsLaunch, "register split");
 constexpr int kChunks = 9;      // 64-dim chunks of a row: 8 latent + 1 rope
 constexpr int kRope = 8;        // the rope chunk's slot, reused for P^T
 constexpr uint32_t kSlotBytes = kRows * 128;       // 128 rows x 64 f16
@@ -444,9 +452,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kv8_kernel(AttnParams p) 
     tc_after();
     const uint32_t tmem = *sTmem;
 
-    if (warp == kWorkers / 32) {
+    if (warp >= kWorkers / 32) {
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsMma));
         // ================= MMA warp: lane 0 issues =================
-        if (lane == 0) {
+        if (warp == kWorkers / 32 && lane == 0) {
             const uint64_t dq0 = umma_desc(smem_u32(sQ), 16, 1024);
             const uint64_t dslot0 = umma_desc(smem_u32(sSlot), 16, 1024);
             const uint64_t dpair0 = umma_desc(smem_u32(sSlot), kSlotBytes, 1024);
@@ -488,6 +497,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kv8_kernel(AttnParams p) 
     }
 
     // ================= workers =================
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsWorker));
     const int srow = 32 * (warp & 3) + lane;            // softmax: TMEM lane / row
     const int hq = warp >> 2;                            // softmax: heads 32 hq .. 32 hq + 31
     const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
@@ -557,7 +567,14 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kv8_kernel(AttnParams p) 
         }
         const int64_t t1 = t0 + kRows;
         const int nt1 = (int)min((int64_t)kRows, row1 - t1);
-        if (!GATHER && t + 1 < n_tiles) load_group<APPEND, GATHER>(rawA, p.codes, t1, nt1, 0, warp, lane, rn, sNew, nullptr);
+        // all of tile t+1 is requested before the softmax (its raw codes stay in
+        // registers across it: the worker warps' share of the register split)
+        if (!GATHER && t + 1 < n_tiles) {
+            load_group<APPEND, GATHER>(rawA, p.codes, t1, nt1, 0, warp, lane, rn, sNew, nullptr);
+            load_group<APPEND, GATHER>(rawB, p.codes, t1, nt1, 1, warp, lane, rn, sNew, nullptr);
+            load_rope<APPEND, GATHER>(rawC, p.codes, t1, nt1, tid, rn, sNew, nullptr);
+            load_scales(t1, nt1);
+        }
 
         // ---- softmax of the tile: thread = row srow, 32 heads ----
         mbar_wait(&bars[kBarScore], (uint32_t)t & 1u, sAbort, wl);
@@ -602,13 +619,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kv8_kernel(AttnParams p) 
             lcol = exact_path(sm, tmem, lane_base, hq, row_ok, za, zb, my_sl, lane, warp, tid, t, p.exact_count,
                               lcol);
             load_z();   // refreshed after the rescale path
-        }
-        // the rest of tile t+1 is requested once the running max is settled:
-        // held across the max pass above, these 40 registers spilled
-        if (!GATHER && t + 1 < n_tiles) {
-            load_group<APPEND, GATHER>(rawB, p.codes, t1, nt1, 1, warp, lane, rn, sNew, nullptr);
-            load_rope<APPEND, GATHER>(rawC, p.codes, t1, nt1, tid, rn, sNew, nullptr);
-            load_scales(t1, nt1);
         }
         {
             // row-sum weights p = 2^(z - m), f16 context weights w = p s_L E
@@ -688,8 +698,14 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kv8_kernel(AttnParams p) 
 namespace {
 template <bool APPEND, bool GATHER>
 cudaError_t launch_kv8(const AttnParams& p, int64_t grid_x, int groups, cudaStream_t stream) {
-    cudaError_t e = cudaFuncSetAttribute(attn_tc_kv8_kernel<APPEND, GATHER>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemUsed);
+    // the worker warps' setmaxnreg.inc waits for registers the other warpgroup
+    // released: launch only if the split adds up against the launch's own count
+    cudaFuncAttributes fa{};
+    cudaError_t e = cudaFuncGetAttributes(&fa, attn_tc_kv8_kernel<APPEND, GATHER>);
+    if (e != cudaSuccess) return e;
+    if (kWorkers * kRegsWorker + 128 * kRegsMma > kThreads * fa.numRegs) return cudaErrorInvalidConfiguration;
+    e = cudaFuncSetAttribute(attn_tc_kv8_kernel<APPEND, GATHER>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kSmemUsed);
     if (e != cudaSuccess) return e;
     attn_tc_kv8_kernel<APPEND, GATHER><<<dim3((unsigned)(grid_x * groups)), kThreads, kSmemUsed, stream>>>(p);
     return cudaGetLastError();
