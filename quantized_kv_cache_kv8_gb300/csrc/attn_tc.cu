@@ -49,7 +49,11 @@ namespace {
 constexpr int kRows = 128;      // rows per tile: the score's M, the context's K
 constexpr int kHC = 64;         // heads per CTA: the MMA N
 constexpr int kWorkers = 256;   // 8 warps: conversion, softmax, epilogue
-constexpr int kThreads = kWorkers + 32;   // + 1 warp whose lane 0 issues every MMA
+// + warpgroup 2: one warp whose lane 0 issues every MMA and three idle warps;
+// after the prologue it gives its registers to the workers (setmaxnreg)
+constexpr int kThreads = kWorkers + 128;
+constexpr int kRegsLaunch = 168, kRegsWorker = 232, kRegsMma = 40;
+static_assert(kWorkers * kRegsWorker + 128 * kRegsMma <= kThreads * kRegsLaunch, "register split");
 constexpr int kSlots = 4;       // f16 staging slots of 128 rows x 64 dims
 constexpr uint32_t kSlotBytes = kRows * 128;
 // query chunk kc (64 dims): rows 0..63 = f16(q) of the 64 heads, rows 64..127 =
@@ -300,9 +304,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnParams p) {
     // a query exact in f16 needs only the first 64 rows
     const bool has_lo = *sHasLo != 0;
 
-    if (warp == kWorkers / 32) {
+    if (warp >= kWorkers / 32) {
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsMma));
         // ================= MMA warp: lane 0 issues, the rest idle =================
-        if (lane == 0) {
+        if (warp == kWorkers / 32 && lane == 0) {
             const uint32_t id_score = has_lo ? kIdescScore2 : kIdescScore;
             const uint64_t dq0 = umma_desc(smem_u32(sQ), 16, 1024);
             const uint64_t dslot0 = umma_desc(smem_u32(sSlot), 16, 1024);
@@ -352,6 +357,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnParams p) {
     }
 
     // ================= workers: conversion, softmax, epilogue =================
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsWorker));
     const int srow = 32 * (warp & 3) + lane;   // TMEM lane owned in the softmax
     const int hq = warp >> 2;                   // heads 32 hq .. 32 hq + 31
     const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
@@ -597,7 +603,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnParams p) {
 }
 
 cudaError_t launch_tc_kv8_f32(const AttnParams& p, int64_t grid_x, int groups, cudaStream_t stream) {
-    cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemAlloc);
+    // the workers' setmaxnreg.inc waits for registers the other warpgroup
+    // released: launch only if the split adds up against the launch's count
+    cudaFuncAttributes fa{};
+    cudaError_t e = cudaFuncGetAttributes(&fa, attn_tc_kernel);
+    if (e != cudaSuccess) return e;
+    if (kWorkers * kRegsWorker + 128 * kRegsMma > kThreads * fa.numRegs) return cudaErrorInvalidConfiguration;
+    e = cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemAlloc);
     if (e != cudaSuccess) return e;
     attn_tc_kernel<<<dim3((unsigned)(grid_x * groups)), kThreads, kSmemAlloc, stream>>>(p);
     return cudaGetLastError();

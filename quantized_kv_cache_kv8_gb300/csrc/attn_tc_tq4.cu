@@ -34,7 +34,11 @@ using namespace tc;
 constexpr int kRows = 128;      // rows per tile
 constexpr int kHC = 32;         // heads per CTA
 constexpr int kWorkers = 256;
-constexpr int kThreads = kWorkers + 32;
+// warpgroup 2 (the MMA-issuing warp and three idle warps) gives its registers
+// to the eight worker warps after the prologue (setmaxnreg)
+constexpr int kThreads = kWorkers + 128;
+constexpr int kRegsLaunch = 168, kRegsWorker = 232, kRegsMma = 40;
+static_assert(kWorkers * kRegsWorker + 128 * kRegsMma <= kThreads * kRegsLaunch, "register split");
 constexpr int kChunks = 9;      // 64-dim chunks: 8 latent + 1 rope
 constexpr int kRope = 8;
 constexpr int kRowBytes = kMlaD / 2;                // 288 code bytes per row
@@ -298,9 +302,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_tq4_kernel(AttnParams p) 
     tc_after();
     const uint32_t tmem = *sTmem;
 
-    if (warp == kWorkers / 32) {
+    if (warp >= kWorkers / 32) {
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsMma));
         // ================= MMA warp: lane 0 issues =================
-        if (lane == 0) {
+        if (warp == kWorkers / 32 && lane == 0) {
             const uint64_t dq0 = umma_desc(smem_u32(sQ), 16, 1024);
             const uint64_t dslot0 = umma_desc(smem_u32(sSlot), 16, 1024);
             const uint64_t dpair0 = umma_desc(smem_u32(sSlot), kSlotBytes, 1024);
@@ -343,6 +348,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_tq4_kernel(AttnParams p) 
     }
 
     // ================= workers =================
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsWorker));
     const int srow = 32 * (warp & 3) + lane;            // softmax: TMEM lane / row
     const int hq = warp >> 2;                            // softmax: heads 16 hq .. 16 hq + 15
     const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
@@ -410,7 +416,14 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_tq4_kernel(AttnParams p) 
         }
         const int64_t t1 = t0 + kRows;
         const int nt1 = (int)min((int64_t)kRows, row1 - t1);
-        if (t + 1 < n_tiles) load_group(rawA, p.codes, t1, nt1, 0, warp, lane);
+        // all of tile t+1 is requested before the softmax (the raw codes stay in
+        // registers across it: the workers' share of the register split)
+        if (t + 1 < n_tiles) {
+            load_group(rawA, p.codes, t1, nt1, 0, warp, lane);
+            load_group(rawB, p.codes, t1, nt1, 1, warp, lane);
+            rawC = load_rope(p.codes, t1, nt1, warp, lane);
+            load_scales(t1, nt1);
+        }
 
         // ---- softmax of the tile: thread = row srow, 16 heads ----
         mbar_wait(&bars[kBarScore], (uint32_t)t & 1u, sAbort, p.wait_limit);
@@ -433,11 +446,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_tq4_kernel(AttnParams p) 
                 z[j] = row_ok ? fmaf(__uint_as_float(a[j]) + __uint_as_float(c[j]), za, z[j]) : -INFINITY;
         };
         load_z();
-        if (t + 1 < n_tiles) {
-            load_group(rawB, p.codes, t1, nt1, 1, warp, lane);
-            rawC = load_rope(p.codes, t1, nt1, warp, lane);
-            load_scales(t1, nt1);
-        }
         bool flag = (*sAbort != 0) | (my_sl > s_lim);
 #pragma unroll
         for (int j = 0; j < 16; ++j) flag |= z[j] > sM[16 * hq + j] + kLagLog2;
@@ -567,8 +575,14 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_tq4_kernel(AttnParams p) 
 
 template <bool QBF16>
 cudaError_t launch_tq4(const AttnParams& p, int64_t grid_x, int groups, cudaStream_t stream) {
-    cudaError_t e = cudaFuncSetAttribute(attn_tc_tq4_kernel<QBF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)kSmemUsed);
+    // the workers' setmaxnreg.inc waits for registers the other warpgroup
+    // released: launch only if the split adds up against the launch's count
+    cudaFuncAttributes fa{};
+    cudaError_t e = cudaFuncGetAttributes(&fa, attn_tc_tq4_kernel<QBF16>);
+    if (e != cudaSuccess) return e;
+    if (kWorkers * kRegsWorker + 128 * kRegsMma > kThreads * fa.numRegs) return cudaErrorInvalidConfiguration;
+    e = cudaFuncSetAttribute(attn_tc_tq4_kernel<QBF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kSmemUsed);
     if (e != cudaSuccess) return e;
     attn_tc_tq4_kernel<QBF16><<<dim3((unsigned)(grid_x * groups)), kThreads, kSmemUsed, stream>>>(p);
     return cudaGetLastError();
