@@ -196,12 +196,12 @@ __device__ __forceinline__ float warp_columns(float (&v)[32], int lane) {
 // The exact path of a tile (see the top of the file), by every worker thread
 // with its row's scores in TMEM: column maxima of z and of y = z + log2 s_L
 // over the tile (16 heads at a time, straight from TMEM), new m, R and E per
-// head, the rescale of O^T in TMEM after the first tile; returns this thread's
-// row sum rescaled.  Out of line: the path is rare, and kept out of the tile
-// loop it leaves the loop's registers alone.
-__device__ __noinline__ float exact_path(unsigned char* sm, uint32_t tmem, uint32_t lane_base, int hq, bool row_ok,
-                                         float za, float zb, float my_sl, int lane, int warp, int tid, int t,
-                                         uint32_t* exact_count, float lcol) {
+// head (sAlphaM: the row-sum rescale), the rescale of O^T in TMEM after the
+// first tile.  Out of line: the path is rare, and kept out of the tile loop it
+// leaves the loop's registers alone.
+__device__ __noinline__ void exact_path(unsigned char* sm, uint32_t tmem, uint32_t lane_base, int hq, bool row_ok,
+                                        float za, float zb, float my_sl, int lane, int warp, int tid, int t,
+                                        uint32_t* exact_count) {
     float* sM = reinterpret_cast<float*>(sm + kOffM);
     float* sR = reinterpret_cast<float*>(sm + kOffR);
     float* sE = reinterpret_cast<float*>(sm + kOffE);
@@ -274,7 +274,6 @@ __device__ __noinline__ float exact_path(unsigned char* sm, uint32_t tmem, uint3
                     }
                 tmem_wait_st();
             }
-    return lcol * sAlphaM[32 * hq + lane];
 }
 
 template <bool APPEND, bool GATHER>
@@ -292,6 +291,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kv8_kernel(AttnParams p) 
     float* sE = reinterpret_cast<float*>(sm + kOffE);
     float* sF = reinterpret_cast<float*>(sm + kOffF);
     float* sAlpha = reinterpret_cast<float*>(sm + kOffAlpha);
+    float* sAlphaM = reinterpret_cast<float*>(sm + kOffAlphaM);
     float* sEmax = reinterpret_cast<float*>(sm + kOffEmax);
     float* sRed = reinterpret_cast<float*>(sm + kOffRed);
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kOffBar);
@@ -502,7 +502,21 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kv8_kernel(AttnParams p) 
     const int hq = warp >> 2;                            // softmax: heads 32 hq .. 32 hq + 31
     const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
     // running row sum of head 32 hq + lane over the rows of quadrant (warp & 3)
-    float lcol = 0.0f;
+    // this thread's row: sums of p for its 32 heads, over every tile so far
+    // (reduced over the rows once, in the epilogue); m and E of its heads,
+    // refreshed after each exact path
+    float lsum[32], mreg[32], ereg[32], emax = 0.0f;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) lsum[j] = 0.0f;
+    auto load_state = [&]() {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            mreg[j] = sM[32 * hq + j];
+            ereg[j] = sE[32 * hq + j];
+        }
+        emax = fmaxf(sEmax[0], sEmax[1]);
+    };
+    load_state();
 
     // this thread's softmax row scales, one tile ahead
     float sl_next = 0.0f, sr_next = 0.0f;
@@ -599,12 +613,21 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kv8_kernel(AttnParams p) 
                     z[16 * c + j] = row_ok ? fmaf(__uint_as_float(s16[j]), za, z[16 * c + j]) : -INFINITY;
             }
         };
-        load_z();
-        // a latent scale with s_L max_h E > kScaleLim takes the exact path
-        // (max_h E is +inf while only inert latent blocks have been met)
-        bool flag = (*sAbort != 0) | (my_sl * fmaxf(sEmax[0], sEmax[1]) > kScaleLim);
+        // d = z - m: the lag test below and the weights 2^d after it
+        auto load_d = [&]() {
+            load_z();
 #pragma unroll
-        for (int j = 0; j < 32; ++j) flag |= z[j] > sM[32 * hq + j] + kLagLog2;
+            for (int j = 0; j < 32; ++j) z[j] -= mreg[j];
+        };
+        load_d();
+        // a latent scale with s_L max_h E > kScaleLim takes the exact path
+        // (max_h E is +inf while only inert latent blocks have been met); so
+        // does a score past m by more than the lag (m = -inf before the first
+        // exact path: d = +inf, or NaN on a row past the tile's end, which the
+        // valid rows outvote)
+        bool flag = (*sAbort != 0) | (my_sl * emax > kScaleLim);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) flag |= z[j] > kLagLog2;
         const bool any_flag = worker_any(flag);
         if (GATHER && t + 1 < n_tiles) {
             // the barrier above made the next tile's index table visible
@@ -616,19 +639,20 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kv8_kernel(AttnParams p) 
         }
         if (any_flag) {
             if (worker_any(*sAbort != 0)) break;
-            lcol = exact_path(sm, tmem, lane_base, hq, row_ok, za, zb, my_sl, lane, warp, tid, t, p.exact_count,
-                              lcol);
-            load_z();   // refreshed after the rescale path
+            exact_path(sm, tmem, lane_base, hq, row_ok, za, zb, my_sl, lane, warp, tid, t, p.exact_count);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) lsum[j] *= sAlphaM[32 * hq + j];
+            load_state();
+            load_d();   // refreshed after the rescale path
         }
         {
             // row-sum weights p = 2^(z - m), f16 context weights w = p s_L E
             uint32_t pk[16];
 #pragma unroll
             for (int j = 0; j < 32; j += 2) {
-                z[j] = ex2(z[j] - sM[32 * hq + j]);
-                z[j + 1] = ex2(z[j + 1] - sM[32 * hq + j + 1]);
-                const __half2 h2 =
-                    __floats2half2_rn(z[j] * sE[32 * hq + j] * my_sl, z[j + 1] * sE[32 * hq + j + 1] * my_sl);
+                z[j] = ex2(z[j]);
+                z[j + 1] = ex2(z[j + 1]);
+                const __half2 h2 = __floats2half2_rn(z[j] * ereg[j] * my_sl, z[j + 1] * ereg[j + 1] * my_sl);
                 pk[j / 2] = *reinterpret_cast<const uint32_t*>(&h2);
             }
 #pragma unroll
@@ -639,7 +663,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kv8_kernel(AttnParams p) 
         fence_async_smem();
         tc_before();
         mbar_arrive(&bars[kBarP]);
-        lcol += warp_columns<false>(z, lane);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) lsum[j] += z[j];
     }
 
     // ---- epilogue: wait for every MMA, row sums, O^T -> partial state ----
@@ -653,7 +678,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kv8_kernel(AttnParams p) 
     const bool aborted = worker_any(*sAbort != 0 || t < n_tiles);
     {
         worker_sync();   // sRed may still be read by the last exact-max pass
-        sRed[(warp & 3) * kHC + 32 * hq + lane] = lcol;
+        sRed[(warp & 3) * kHC + 32 * hq + lane] = warp_columns<false>(lsum, lane);
         worker_sync();
         if (tid < kHC) sAlpha[tid] = (sRed[tid] + sRed[kHC + tid]) + (sRed[2 * kHC + tid] + sRed[3 * kHC + tid]);
         worker_sync();

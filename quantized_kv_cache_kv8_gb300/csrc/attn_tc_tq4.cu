@@ -352,7 +352,20 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_tq4_kernel(AttnParams p) 
     const int srow = 32 * (warp & 3) + lane;            // softmax: TMEM lane / row
     const int hq = warp >> 2;                            // softmax: heads 16 hq .. 16 hq + 15
     const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
-    float lcol = 0.0f;   // row sum of head 16 hq + lane % 16 over this quadrant (lanes 0-15)
+    // this thread's row: sums of p for its 16 heads over every tile so far
+    // (reduced over the rows once, in the epilogue); m and E of its heads,
+    // refreshed after each exact path
+    float lsum[16], mreg[16], ereg[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) lsum[j] = 0.0f;
+    auto load_state = [&]() {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            mreg[j] = sM[16 * hq + j];
+            ereg[j] = sE[16 * hq + j];
+        }
+    };
+    load_state();
     float s_lim = 0.0f;  // latent scales above this take the exact path (3.5 / max_h E)
 
     float sl_next = 0.0f, sr_next = 0.0f;
@@ -446,13 +459,19 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_tq4_kernel(AttnParams p) 
                 z[j] = row_ok ? fmaf(__uint_as_float(a[j]) + __uint_as_float(c[j]), za, z[j]) : -INFINITY;
         };
         load_z();
+        // d = z - m: the lag test and the weights 2^d (m = -inf before the first
+        // exact path: d = +inf, or NaN on a row past the tile's end, which the
+        // valid rows outvote)
+#pragma unroll
+        for (int j = 0; j < 16; ++j) z[j] -= mreg[j];
         bool flag = (*sAbort != 0) | (my_sl > s_lim);
 #pragma unroll
-        for (int j = 0; j < 16; ++j) flag |= z[j] > sM[16 * hq + j] + kLagLog2;
+        for (int j = 0; j < 16; ++j) flag |= z[j] > kLagLog2;
         if (worker_any(flag)) {
             if (worker_any(*sAbort != 0)) break;
             // exact column maxima of z and of y = z + log2 s_L, new running
             // maxima, rescale factors
+            load_z();
             {
                 const float cm = warp_columns16<true>(z, lane);
                 if (lane < 16) sRed[(warp & 3) * kHC + 16 * hq + lane] = cm;
@@ -504,26 +523,28 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_tq4_kernel(AttnParams p) 
                 }
                 tmem_wait_st();
             }
-            if (lane < 16) lcol *= sAlphaM[16 * hq + lane];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) lsum[j] *= sAlphaM[16 * hq + j];
+            load_state();
             load_z();
+#pragma unroll
+            for (int j = 0; j < 16; ++j) z[j] -= mreg[j];
         }
         {
             // row-sum weights p = 2^(z - m), f16 context weights w = p s_L E
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
                 const int h = 16 * hq + j;
-                z[j] = ex2(z[j] - sM[h]);
+                z[j] = ex2(z[j]);
                 *reinterpret_cast<__half*>(sP + (srow >> 6) * kPChunkBytes + sw128(h, (srow & 63) * 2)) =
-                    __float2half_rn(z[j] * sE[h] * my_sl);
+                    __float2half_rn(z[j] * ereg[j] * my_sl);
             }
         }
         fence_async_smem();
         tc_before();
         mbar_arrive(&bars[kBarP]);
-        {
-            const float l = warp_columns16<false>(z, lane);
-            if (lane < 16) lcol += l;
-        }
+#pragma unroll
+        for (int j = 0; j < 16; ++j) lsum[j] += z[j];
     }
 
     // ---- epilogue: wait for every MMA, row sums, O^T -> partial state ----
@@ -535,6 +556,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_tq4_kernel(AttnParams p) 
     const bool aborted = worker_any(*sAbort != 0 || t < n_tiles);
     {
         worker_sync();
+        const float lcol = warp_columns16<false>(lsum, lane);
         if (lane < 16) sRed[(warp & 3) * kHC + 16 * hq + lane] = lcol;
         worker_sync();
         if (tid < kHC) sAlpha[tid] = (sRed[tid] + sRed[kHC + tid]) + (sRed[2 * kHC + tid] + sRed[3 * kHC + tid]);
