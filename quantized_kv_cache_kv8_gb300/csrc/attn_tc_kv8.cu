@@ -364,6 +364,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kv8_kernel(AttnParams p) 
     if (!GATHER && tid == 0) {
         const int64_t n = min((int64_t)kRows, row1 - row0);
         prefetch_l2(p.codes + row0 * kMlaD, (uint32_t)(n * kMlaD));
+        // the second tile too: the loop keeps the L2 prefetch two tiles ahead
+        if (row0 + kRows < row1)
+            prefetch_l2(p.codes + (row0 + kRows) * kMlaD, (uint32_t)(min((int64_t)kRows, row1 - row0 - kRows) * kMlaD));
     }
     if (GATHER && tid < kRows) sRowIdx[tid] = row0 + tid < row1 ? gather_row(p, row0 + tid) : 0;
 
@@ -546,9 +549,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kv8_kernel(AttnParams p) 
     for (; t < n_tiles; ++t) {
         const int64_t t0 = row0 + (int64_t)t * kRows;
         const int nt = (int)min((int64_t)kRows, row1 - t0);
-        if (!GATHER && tid == 0 && t0 + kRows < row1) {
-            const int64_t n = min((int64_t)kRows, row1 - (t0 + kRows));
-            prefetch_l2(p.codes + (t0 + kRows) * kMlaD, (uint32_t)(n * kMlaD));
+        if (!GATHER && tid == 0 && t0 + 2 * kRows < row1) {
+            const int64_t n = min((int64_t)kRows, row1 - (t0 + 2 * kRows));
+            prefetch_l2(p.codes + (t0 + 2 * kRows) * kMlaD, (uint32_t)(n * kMlaD));
         }
         // gather: the next tile's pool rows, read after the softmax's first barrier
         if (GATHER && tid < kRows && t0 + kRows < row1)
@@ -598,19 +601,18 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kv8_kernel(AttnParams p) 
         const float za = my_sl * cz, zb = my_sr * cz;
         const bool row_ok = srow < nt;
         auto load_z = [&]() {
-            // 16 columns at a time keeps the peak register count under the cap
+            // 16 heads at a time: their rope and latent columns go out together,
+            // then one wait (all four at once made the appending kernel spill)
 #pragma unroll
             for (int c = 0; c < 2; ++c) {
-                uint32_t s16[16];
-                tmem_ld16(tmem + lane_base + kColSR + 32 * hq + 16 * c, s16);
-                tmem_wait_ld();
-#pragma unroll
-                for (int j = 0; j < 16; ++j) z[16 * c + j] = __uint_as_float(s16[j]) * zb;
-                tmem_ld16(tmem + lane_base + kColSL + 32 * hq + 16 * c, s16);
+                uint32_t r[16], l[16];
+                tmem_ld16(tmem + lane_base + kColSR + 32 * hq + 16 * c, r);
+                tmem_ld16(tmem + lane_base + kColSL + 32 * hq + 16 * c, l);
                 tmem_wait_ld();
 #pragma unroll
                 for (int j = 0; j < 16; ++j)
-                    z[16 * c + j] = row_ok ? fmaf(__uint_as_float(s16[j]), za, z[16 * c + j]) : -INFINITY;
+                    z[16 * c + j] =
+                        row_ok ? fmaf(__uint_as_float(l[j]), za, __uint_as_float(r[j]) * zb) : -INFINITY;
             }
         };
         // d = z - m: the lag test below and the weights 2^d after it

@@ -234,6 +234,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_tq4_kernel(AttnParams p) 
     if (tid == 0) {
         const int64_t n = min((int64_t)kRows, row1 - row0);
         prefetch_l2(p.codes + row0 * kRowBytes, (uint32_t)(n * kRowBytes));
+        // the second tile too: the loop keeps the L2 prefetch two tiles ahead
+        if (row0 + kRows < row1)
+            prefetch_l2(p.codes + (row0 + kRows) * kRowBytes, (uint32_t)(min((int64_t)kRows, row1 - row0 - kRows) * kRowBytes));
     }
 
     // ---- query: 32 heads, 4 per worker warp, rotated once (sign flip, FWHT of
@@ -390,9 +393,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_tq4_kernel(AttnParams p) 
     for (; t < n_tiles; ++t) {
         const int64_t t0 = row0 + (int64_t)t * kRows;
         const int nt = (int)min((int64_t)kRows, row1 - t0);
-        if (tid == 0 && t0 + kRows < row1) {
-            const int64_t n = min((int64_t)kRows, row1 - (t0 + kRows));
-            prefetch_l2(p.codes + (t0 + kRows) * kRowBytes, (uint32_t)(n * kRowBytes));
+        if (tid == 0 && t0 + 2 * kRows < row1) {
+            const int64_t n = min((int64_t)kRows, row1 - (t0 + 2 * kRows));
+            prefetch_l2(p.codes + (t0 + 2 * kRows) * kRowBytes, (uint32_t)(n * kRowBytes));
         }
         const float my_sl = sl_next, my_sr = sr_next;
         // ---- decode the tile: groups A (chunks 0-3), B (4-7), C (rope) ----
@@ -445,18 +448,18 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_tq4_kernel(AttnParams p) 
         const float za = my_sl * cz, zb = my_sr * cz;
         const bool row_ok = srow < nt;
         auto load_z = [&]() {
-            uint32_t a[16], c[16];
+            // the four 16-column loads go out together, then one wait
+            uint32_t a[16], c[16], e[16], f[16];
             tmem_ld16(tmem + lane_base + kColSR + 16 * hq, a);            // rope, values
             tmem_ld16(tmem + lane_base + kColSR + kHC + 16 * hq, c);      // rope, residuals
-            tmem_wait_ld();
-#pragma unroll
-            for (int j = 0; j < 16; ++j) z[j] = (__uint_as_float(a[j]) + __uint_as_float(c[j])) * zb;
-            tmem_ld16(tmem + lane_base + kColSL + 16 * hq, a);
-            tmem_ld16(tmem + lane_base + kColSL + kHC + 16 * hq, c);
+            tmem_ld16(tmem + lane_base + kColSL + 16 * hq, e);
+            tmem_ld16(tmem + lane_base + kColSL + kHC + 16 * hq, f);
             tmem_wait_ld();
 #pragma unroll
             for (int j = 0; j < 16; ++j)
-                z[j] = row_ok ? fmaf(__uint_as_float(a[j]) + __uint_as_float(c[j]), za, z[j]) : -INFINITY;
+                z[j] = row_ok ? fmaf(__uint_as_float(e[j]) + __uint_as_float(f[j]), za,
+                                     (__uint_as_float(a[j]) + __uint_as_float(c[j])) * zb)
+                              : -INFINITY;
         };
         load_z();
         // d = z - m: the lag test and the weights 2^d (m = -inf before the first
