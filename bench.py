@@ -20,7 +20,13 @@ The same JSON line carries, under ``workloads``, the other timed workloads:
                    encoded and appended to a 124 x 1024 = 126,976-row cache,
                    then 2048 tokens x 128 heads attend rows [0, P + j];
 * ``kv8_8x4096``   decode of 8 sequences x 4096 rows (19 MB, fits in L2:
-                   a 256 MB buffer is written between timed steps).
+                   a 256 MB buffer is written between timed steps);
+* ``pq4_8x4096``   the same short decode step on a PolarQuant 4-bit cache (296
+                   B/row), on the fp32 consumer (the only PolarQuant consumer);
+* ``k2v4_4x32768`` the K2/V4 GQA decode: 4 sequences x 32768 cells, 2 kv
+                   heads x 256 dims, 16 query heads, sinks 8 + window 256 in
+                   the fp16 overlay, K gain 1.10 (60.4 MB, fits in L2: flushed
+                   between steps); its roofline is HBM (36 flop per byte).
 
 Inputs are synthetic and seeded (quantized_kv_cache_kv8_gb300.synth): latent
 rows N(0,1) x per-channel log-normal gains, N(0,1) queries rounded to bf16.
@@ -55,7 +61,8 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 H, D, DV = 128, 576, 512
-ROW_BYTES = {1: 576 + 2 * 4, 2: 288 + 2 * 4}          # KV8, TQ4
+ROW_BYTES = {1: 576 + 2 * 4, 2: 288 + 2 * 4, 14: 288 + 2 * 4}   # KV8, TQ4, PolarQuant 4-bit
+FORMAT_NAMES = {1: "KV8", 2: "TQ4", 14: "PolarQuant-4"}
 FLOPS_PER_ROW = H * (D + DV) * 2
 SM_SCALE = 1.0 / math.sqrt(192.0)
 METRIC = "quantized-KV MLA decode attn: cache GB/s & % of HBM roofline; rows/s"
@@ -66,6 +73,8 @@ RAGGED_SEED, RAGGED_B, RAGGED_LO, RAGGED_HI, MASTER = 4, 32, 1024, 131072, 13107
 PREFILL_PAST, PREFILL_NEW = 124 * 1024, 2048
 # short decode (fits in L2)
 SHORT_B, SHORT_T, SHORT_SEED = 8, 4096, 2
+# K2/V4 GQA decode
+K2_B, K2_H, K2_T, K2_D, K2_HQ, K2_SINK, K2_WINDOW, K2_SLACK, K2_GAIN, K2_SEED = 4, 2, 32768, 256, 16, 8, 256, 16, 1.10, 5
 
 WORKLOAD_NAMES = {
     "kv8_ragged": "ragged decode, KV8: 32 seqs, lengths U[1024,131072] (seed 4), 128 heads, 576-dim latent "
@@ -77,8 +86,13 @@ WORKLOAD_NAMES = {
     "tq4_prefill": "chunked causal prefill, TQ4: 2048 new rows encoded onto 126976 cached rows, "
                    "2048 tokens x 128 heads, bf16 query",
     "kv8_8x4096": "decode, KV8: 8 seqs x 4096 rows, 128 heads, bf16 query, the step's 8 new rows appended",
+    "pq4_8x4096": "decode, PolarQuant 4-bit: 8 seqs x 4096 rows, 128 heads, bf16 query, the step's 8 new rows "
+                  "appended (fp32 consumer)",
+    "k2v4_4x32768": "GQA decode, K2/V4: 4 seqs x 32768 cells, 2 kv heads x 256, 16 query heads, f32 query, "
+                    "sinks 8 + window 256 fp16, K gain 1.10",
 }
-DEFAULT_WORKLOADS = ["kv8_ragged", "tq4_ragged", "kv8_prefill", "tq4_prefill", "kv8_8x4096"]
+DEFAULT_WORKLOADS = ["kv8_ragged", "tq4_ragged", "kv8_prefill", "tq4_prefill", "kv8_8x4096", "pq4_8x4096",
+                     "k2v4_4x32768"]
 
 # profile summaries holding the ncu DRAM traffic of a dominant kernel, keyed by workload
 PROFILE_FOR = {"kv8_ragged": "decode_tc_kv8_ragged_b32_h128.md", "tq4_ragged": "decode_tc_tq4_ragged_b32_h128.md",
@@ -235,9 +249,14 @@ class Ctx:
     def encode(self, fmt, x_dev, layout):
         torch, kvq = self.torch, self.kvq
         n = x_dev.shape[0]
-        codes = torch.empty((n, 576 if fmt == 1 else 288), dtype=torch.uint8, device=self.dev)
+        codes = torch.empty((n, kvq.row_bytes(fmt, layout)), dtype=torch.uint8, device=self.dev)
         scales = torch.empty((n, 2), dtype=torch.float32, device=self.dev)
-        (kvq.kv8_encode if fmt == 1 else kvq.tq4_encode)(x_dev, codes, scales, layout)
+        if fmt == 1:
+            kvq.kv8_encode(x_dev, codes, scales, layout)
+        elif fmt == 2:
+            kvq.tq4_encode(x_dev, codes, scales, layout)
+        else:
+            kvq.pq_encode(fmt, x_dev, codes, scales, layout)
         return codes, scales
 
 
@@ -324,6 +343,8 @@ def setup_decode(ctx, fmt, workload):
 
 def used_path(ctx, fmt):
     kvq = ctx.kvq
+    if fmt not in (1, 2):
+        return "simt"   # PolarQuant has only the fp32 consumer
     return "tensor" if (ctx.path == kvq.PATH_TENSOR or (ctx.path == kvq.PATH_AUTO and H % 64 == 0)) else "simt"
 
 
@@ -336,7 +357,7 @@ def roofline(ctx, peaks, src, fmt, workload, rows, kernel_ms, sustained=False, k
         return {"bound": "alu", "achieved": round(achieved, 3), "peak": round(peak, 2), "unit": "TFLOP/s",
                 "frac": round(achieved / peak, 4), "traffic": None,
                 "peak_source": "derived: 152 SMs x 128 fp32 lanes x 2 x max SM clock (MEASURED_PEAKS sm_max_mhz)",
-                "kernel": "attn_partial_kernel (fp32 split-T partials)"}
+                "kernel": kernel_name or "attn_partial_kernel (fp32 split-T partials)"}
     key = "bf16_tflops_sustained" if sustained else "bf16_tflops"
     peak = peaks.get(key, peaks["bf16_tflops"])
     traffic, tsrc = profiled_traffic(workload, fmt)
@@ -351,7 +372,7 @@ def run_decode(ctx, fmt, workload, K, W, peaks, src, sampler, world, dist, e2e=F
     torch, kvq = ctx.torch, ctx.kvq
     d = setup_decode(ctx, fmt, workload)
     flush = None
-    if workload == "kv8_8x4096":
+    if workload.endswith("8x4096"):
         flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=ctx.dev)
     for _ in range(max(W, 3)):
         d["step"]()
@@ -380,10 +401,11 @@ def run_decode(ctx, fmt, workload, K, W, peaks, src, sampler, world, dist, e2e=F
     step_ms, part_ms, merge_ms, e2e_ms_m = vals
     rows, B = d["total"], d["B"]
     path = used_path(ctx, fmt)
-    kname = ("attn_tc_kv8_kernel<APPEND> (tcgen05 split-T partials with the row append)" if fmt == 1
-             else "attn_tc_tq4_kernel (tcgen05 split-T partials, query rotated in the prologue)")
+    kname = {1: "attn_tc_kv8_kernel<APPEND> (tcgen05 split-T partials with the row append)",
+             2: "attn_tc_tq4_kernel (tcgen05 split-T partials, query rotated in the prologue)",
+             14: "attn_partial_kernel<PolarQuant> (fp32 split-T partials, rows rebuilt per tile)"}[fmt]
     res = {
-        "workload": WORKLOAD_NAMES[workload], "format": "KV8" if fmt == 1 else "TQ4", "path": path,
+        "workload": WORKLOAD_NAMES[workload], "format": FORMAT_NAMES[fmt], "path": path,
         "rows": rows, "row_bytes": ROW_BYTES[fmt], "ms_per_step": round(step_ms, 5),
         "value": round(job_rate_gbs(rows, world, step_ms, ROW_BYTES[fmt]), 3), "unit": "GB/s",
         "rows_per_s": round(rows * world / (step_ms * 1e-3), 1),
@@ -405,6 +427,75 @@ def run_decode(ctx, fmt, workload, K, W, peaks, src, sampler, world, dist, e2e=F
                       "h2d_bytes_per_step": int(B * D * 4 + B * H * D * 2),
                       "d2h_bytes_per_step": int(B * H * DV * 4)}
     del d
+    torch.cuda.empty_cache()
+    return res
+
+
+def k2v4_bytes():
+    """Bytes a K2/V4 decode reads: bulk cells' K codes and V blocks, every K
+    scale group, and the overlay cells' fp16 K and V."""
+    ov = K2_SINK + K2_WINDOW
+    bulk = K2_T - ov
+    per = bulk * (K2_D // 4 + (K2_D // 32) * 18) + ov * 4 * K2_D + (K2_T // 32) * K2_D * 2
+    return K2_B * K2_H * per
+
+
+def run_k2v4(ctx, workload, K, W, peaks, sampler, world, dist):
+    torch, kvq = ctx.torch, ctx.kvq
+    from quantized_kv_cache_kv8_gb300 import synth
+    layout = kvq.k2v4_layout(K2_H, K2_D, K2_GAIN, K2_SINK, K2_WINDOW, K2_SLACK)
+    k, v = synth.gqa_kv(K2_SEED, K2_B, K2_H, K2_T, K2_D)
+    slots = K2_SINK + K2_WINDOW + K2_SLACK
+    dev = ctx.dev
+    kc = torch.zeros((K2_B, K2_H, K2_T, K2_D // 4), dtype=torch.uint8, device=dev)
+    ks = torch.zeros((K2_B, K2_H, K2_T // 32, K2_D), dtype=torch.int16, device=dev)
+    vb = torch.zeros((K2_B, K2_H, K2_T, K2_D // 32, 18), dtype=torch.uint8, device=dev)
+    kw = torch.zeros((K2_B, K2_H, slots, K2_D), dtype=torch.int16, device=dev)
+    vw = torch.zeros((K2_B, K2_H, slots, K2_D), dtype=torch.int16, device=dev)
+    kvq.k2v4_encode(layout, torch.from_numpy(k).to(dev), torch.from_numpy(v).to(dev), kc, ks, vb, kw, vw)
+    del k, v
+    q = torch.from_numpy(synth.queries(K2_SEED + 1, (K2_B, K2_HQ, K2_D))).to(dev)
+    out = torch.empty((K2_B, K2_HQ, K2_D), dtype=torch.float32, device=dev)
+    pth = ctx.path if ctx.path != kvq.PATH_AUTO else kvq.PATH_AUTO
+    ws = torch.zeros(kvq.kv_attn_decode_k2v4_workspace_size(layout, K2_B, K2_HQ, K2_T, pth), dtype=torch.uint8,
+                     device=dev)
+    sm = 1.0 / math.sqrt(K2_D)
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+
+    def step():
+        kvq.kv_attn_decode_k2v4(layout, q, K2_T, kc, ks, vb, kw, vw, out, ws, sm, path=pth)
+    for _ in range(max(W, 3)):
+        step()
+        flush.zero_()
+    torch.cuda.synchronize()
+    if kvq.read_device_error(ws) != 0:
+        raise RuntimeError(f"{workload}: device error word set during warm-up")
+    if dist:
+        dist.barrier()
+    step_ms = timed_loop(torch, step, K, ctx.stream, flush, sampler)
+    part_ms, merge_ms = kernel_timing(kvq, torch, step, K, flush)
+    if kvq.read_device_error(ws) != 0:
+        raise RuntimeError(f"{workload}: device error word set")
+    step_ms, part_ms, merge_ms = max_over_ranks([step_ms, part_ms, merge_ms], dist, ctx.dev)
+    nbytes = k2v4_bytes()
+    tensor = ctx.path != kvq.PATH_SIMT
+    achieved = nbytes / (part_ms * 1e-3) / 1e9
+    res = {
+        "workload": WORKLOAD_NAMES[workload], "format": "K2/V4", "path": "tensor" if tensor else "simt",
+        "ms_per_step": round(step_ms, 5), "value": round(nbytes * world / (step_ms * 1e-3) / 1e9, 3), "unit": "GB/s",
+        "bytes_per_step": nbytes,
+        "timing": {"partial_ms": round(part_ms, 5), "merge_ms": round(merge_ms, 5),
+                   "how": "CUDA events recorded by the library around the partial kernel and the merge"},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": None,
+                     "traffic_source": "no capture for this workload", "algorithmic_bytes": nbytes,
+                     "peak_source": "hbm_gbs (measured)",
+                     "kernel": "k2v4_tc_kernel<256> (tcgen05, tiles dequantized to f16 in shared memory)"
+                     if tensor else "k2v4_partial_kernel (fp32)"},
+        "gpu_launches_per_step": 2,
+        "l2": "256 MB buffer written between timed steps (outside the events)",
+    }
+    del kc, ks, vb, kw, vw, q, out, ws, flush
     torch.cuda.empty_cache()
     return res
 
@@ -495,8 +586,10 @@ def run_ours(args, rank, world):
     Kp = max(1, min(K, args.prefill_steps))
     results = {}
     for w in workloads:
-        fmt = 1 if w.startswith("kv8") else 2
-        if w.endswith("prefill"):
+        fmt = 1 if w.startswith("kv8") else (14 if w.startswith("pq4") else 2)
+        if w.startswith("k2v4"):
+            results[w] = run_k2v4(ctx, w, K, W, peaks, sampler, world, dist)
+        elif w.endswith("prefill"):
             results[w] = run_prefill(ctx, fmt, w, Kp, W, peaks, src, sampler, world, dist)
         else:
             results[w] = run_decode(ctx, fmt, w, K, W, peaks, src, sampler, world, dist, e2e=(w == head))
