@@ -21,8 +21,9 @@ The same JSON line carries, under ``workloads``, the other timed workloads:
                    then 2048 tokens x 128 heads attend rows [0, P + j];
 * ``kv8_8x4096``   decode of 8 sequences x 4096 rows (19 MB, fits in L2:
                    a 256 MB buffer is written between timed steps);
-* ``pq4_8x4096``   the same short decode step on a PolarQuant 4-bit cache (296
-                   B/row), on the fp32 consumer (the only PolarQuant consumer);
+* ``pq4_8x4096`` / ``pq4t_8x4096``  the same short decode step on a PolarQuant
+                   4-bit cache (296 B/row), on the fp32 consumer (the default
+                   path for PolarQuant) and on the tensor-core consumer;
 * ``k2v4_4x32768`` the K2/V4 GQA decode: 4 sequences x 32768 cells, 2 kv
                    heads x 256 dims, 16 query heads, sinks 8 + window 256 in
                    the fp16 overlay, K gain 1.10 (60.4 MB, fits in L2: flushed
@@ -87,12 +88,14 @@ WORKLOAD_NAMES = {
                    "2048 tokens x 128 heads, bf16 query",
     "kv8_8x4096": "decode, KV8: 8 seqs x 4096 rows, 128 heads, bf16 query, the step's 8 new rows appended",
     "pq4_8x4096": "decode, PolarQuant 4-bit: 8 seqs x 4096 rows, 128 heads, bf16 query, the step's 8 new rows "
-                  "appended (fp32 consumer)",
+                  "appended (fp32 consumer, the default path)",
+    "pq4t_8x4096": "decode, PolarQuant 4-bit: 8 seqs x 4096 rows, 128 heads, bf16 query, the step's 8 new rows "
+                   "appended (tensor-core consumer, KVQ_PATH_TENSOR)",
     "k2v4_4x32768": "GQA decode, K2/V4: 4 seqs x 32768 cells, 2 kv heads x 256, 16 query heads, f32 query, "
                     "sinks 8 + window 256 fp16, K gain 1.10",
 }
 DEFAULT_WORKLOADS = ["kv8_ragged", "tq4_ragged", "kv8_prefill", "tq4_prefill", "kv8_8x4096", "pq4_8x4096",
-                     "k2v4_4x32768"]
+                     "pq4t_8x4096", "k2v4_4x32768"]
 
 # profile summaries holding the ncu DRAM traffic of a dominant kernel, keyed by workload
 PROFILE_FOR = {"kv8_ragged": "decode_tc_kv8_ragged_b32_h128.md", "tq4_ragged": "decode_tc_tq4_ragged_b32_h128.md",
@@ -344,7 +347,8 @@ def setup_decode(ctx, fmt, workload):
 def used_path(ctx, fmt):
     kvq = ctx.kvq
     if fmt not in (1, 2):
-        return "simt"   # PolarQuant has only the fp32 consumer
+        # PolarQuant: the fp32 consumer unless the tensor path is asked for (4 bits)
+        return "tensor" if (fmt == 14 and ctx.path == kvq.PATH_TENSOR) else "simt"
     return "tensor" if (ctx.path == kvq.PATH_TENSOR or (ctx.path == kvq.PATH_AUTO and H % 64 == 0)) else "simt"
 
 
@@ -403,7 +407,9 @@ def run_decode(ctx, fmt, workload, K, W, peaks, src, sampler, world, dist, e2e=F
     path = used_path(ctx, fmt)
     kname = {1: "attn_tc_kv8_kernel<APPEND> (tcgen05 split-T partials with the row append)",
              2: "attn_tc_tq4_kernel (tcgen05 split-T partials, query rotated in the prologue)",
-             14: "attn_partial_kernel<PolarQuant> (fp32 split-T partials, rows rebuilt per tile)"}[fmt]
+             14: "attn_tc_tq4_kernel<PQ> (tcgen05 split-T partials, PolarQuant trees rebuilt into f16 operands)"
+             if path == "tensor" else
+             "attn_partial_kernel<PolarQuant> (fp32 split-T partials, rows rebuilt per tile)"}[fmt]
     res = {
         "workload": WORKLOAD_NAMES[workload], "format": FORMAT_NAMES[fmt], "path": path,
         "rows": rows, "row_bytes": ROW_BYTES[fmt], "ms_per_step": round(step_ms, 5),
@@ -587,12 +593,16 @@ def run_ours(args, rank, world):
     results = {}
     for w in workloads:
         fmt = 1 if w.startswith("kv8") else (14 if w.startswith("pq4") else 2)
+        saved = ctx.path
+        if w.startswith("pq4t"):
+            ctx.path = ctx.kvq.PATH_TENSOR
         if w.startswith("k2v4"):
             results[w] = run_k2v4(ctx, w, K, W, peaks, sampler, world, dist)
         elif w.endswith("prefill"):
             results[w] = run_prefill(ctx, fmt, w, Kp, W, peaks, src, sampler, world, dist)
         else:
             results[w] = run_decode(ctx, fmt, w, K, W, peaks, src, sampler, world, dist, e2e=(w == head))
+        ctx.path = saved
     sampler.stop()
     if rank != 0:
         return None

@@ -247,10 +247,13 @@ size_t kv_attn_workspace_size(kvq_format fmt, const kvq_mla_layout* layout, int3
  *   out         [batch][n_heads][v_dim] f32, written
  * Supported attention layout: D = 576 as blocks (512, 64) or (576) for KV8,
  * (512, 64) for TQ4 and PolarQuant; v_dim = 512.  Others return
- * KVQ_ERR_UNSUPPORTED.  PolarQuant runs on the fp32 path only (it rebuilds
- * each row's tree in the rotated domain in shared memory, tile by tile, and
- * unrotates the context once as TQ4 does); KVQ_PATH_TENSOR with a PolarQuant
- * format returns KVQ_ERR_UNSUPPORTED. */
+ * KVQ_ERR_UNSUPPORTED.  PolarQuant runs on the fp32 path under KVQ_PATH_AUTO
+ * (it rebuilds each row's tree in the rotated domain in shared memory, tile by
+ * tile, and unrotates the context once as TQ4 does).  KVQ_PATH_TENSOR with
+ * KVQ_PQ4 runs the tensor-core consumer: the trees are rebuilt into f16
+ * operands, each leaf rounded once (up to 2^-11 relative), so its outputs are
+ * within 4e-3 rather than 2e-3; KVQ_PATH_TENSOR with another PolarQuant width
+ * returns KVQ_ERR_UNSUPPORTED. */
 kvq_status kv_attn_decode(kvq_format fmt, const kvq_mla_layout* layout,
                           const void* q, kvq_dtype q_dtype, int32_t batch, int32_t n_heads,
                           const uint8_t* codes, const float* scales, const int64_t* cu_seqlens,

@@ -86,14 +86,15 @@ kvq_status check_path(kvq_path path) {
 }
 
 // The attention family that runs: AUTO takes the tensor-core kernel when it
-// supports the format and head count, else the SIMT kernel.  PolarQuant has
-// only the SIMT consumer.
+// supports the format and head count, else the SIMT kernel.  PolarQuant runs
+// on the SIMT kernel unless the tensor path is asked for, which serves 4-bit
+// rows (its f16 leaves carry a looser bound than the other tensor paths).
 kvq_status resolve_path(kvq_format fmt, kvq_path path, const kvq_mla_layout* L, int32_t n_heads, kvq_path* out) {
-    if (path == KVQ_PATH_SIMT) {
+    if (path == KVQ_PATH_SIMT || (path == KVQ_PATH_AUTO && is_pq(fmt))) {
         *out = KVQ_PATH_SIMT;
         return KVQ_OK;
     }
-    const bool tc = !is_pq(fmt) && tc_supported(*L, n_heads);
+    const bool tc = (!is_pq(fmt) || fmt == KVQ_PQ4) && tc_supported(*L, n_heads);
     if (path == KVQ_PATH_TENSOR && !tc) return KVQ_ERR_UNSUPPORTED;
     *out = tc ? KVQ_PATH_TENSOR : KVQ_PATH_SIMT;
     return KVQ_OK;

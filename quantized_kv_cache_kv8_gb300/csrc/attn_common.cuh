@@ -361,7 +361,9 @@ cudaError_t launch_attn_tc_kv8_bf16(const AttnParams& p, int64_t grid_x, int gro
 cudaError_t launch_attn_tc_kv8_bf16_append(const AttnParams& p, int64_t grid_x, int groups, cudaStream_t stream);
 // Tensor-core partial kernel for TQ4 rows (bf16 or f32 queries, rotated in the
 // kernel); grid = work items x head groups of 32.
-cudaError_t launch_attn_tc_tq4(const AttnParams& p, bool q_bf16, int64_t grid_x, int n_heads, cudaStream_t stream);
+// TQ4 rows, or (pq) PolarQuant rows at 4 bits
+cudaError_t launch_attn_tc_tq4(const AttnParams& p, bool q_bf16, bool pq, int64_t grid_x, int n_heads,
+                               cudaStream_t stream);
 
 // LSE merge of the chunk partials into out[n_seq][n_heads][512] (TQ4: unrotated).
 cudaError_t launch_attn_merge(kvq_format fmt, const AttnParams& p, float* out, cudaStream_t stream);

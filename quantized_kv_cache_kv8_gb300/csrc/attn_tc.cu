@@ -624,7 +624,7 @@ bool tc_supported(const kvq_mla_layout& L, int32_t n_heads) {
 
 AttnPlan plan_decode_tc(kvq_format fmt, int32_t batch, int32_t n_heads, int64_t max_total_rows, int waves) {
     AttnPlan pl{};
-    pl.heads_per_cta = fmt == KVQ_TQ4 ? kHC / 2 : kHC;
+    pl.heads_per_cta = (fmt == KVQ_TQ4 || fmt == KVQ_PQ4) ? kHC / 2 : kHC;
     const int64_t groups = std::max<int64_t>(1, n_heads / pl.heads_per_cta);
     const int64_t target_items = std::max<int64_t>(1, 152 / groups);
     int64_t chunk = (std::max<int64_t>(max_total_rows, 1) + target_items - 1) / target_items;
@@ -678,7 +678,7 @@ cudaError_t launch_attn_tc(kvq_format fmt, const kvq_mla_layout& L, const void* 
         e = qdt == KVQ_BF16 ? launch_attn_tc_kv8_bf16(p, plan.max_items, groups, stream)
                             : launch_tc_kv8_f32(p, plan.max_items, groups, stream);
     else
-        e = launch_attn_tc_tq4(p, qdt == KVQ_BF16, plan.max_items, n_heads, stream);
+        e = launch_attn_tc_tq4(p, qdt == KVQ_BF16, fmt == KVQ_PQ4, plan.max_items, n_heads, stream);
     if (e != cudaSuccess) return e;
     return launch_attn_merge(fmt, p, out, stream);
 }

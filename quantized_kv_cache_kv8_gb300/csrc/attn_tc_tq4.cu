@@ -16,6 +16,11 @@
 //     of f16; divided out of scores and context);
 //   - P is stored K-major (heads on rows) so that N = 32 needs no padding.
 // The context accumulates in the rotated domain; the merge unrotates it.
+// The same kernel serves PolarQuant rows at 4 bits (PQ = true; codec 0 of the
+// TQ tier, 288 code bytes per row like TQ4): each row's tree is rebuilt from
+// a unit top radius, the block radius riding the row scale as TQ4's does; two
+// threads rebuild a row, one per half of its latent and rope blocks, with the
+// level centroids' (cos, sin) in shared memory and the leaves written as f16.
 // Softmax weights as in the KV8 kernel: the row sums take p = 2^(z - m) (m a
 // lagged running maximum of the scores), the context the f16 weight
 // w = p s_L E with E = 2^(m - R - 3) per head, R the largest z + log2 s_L of
@@ -58,7 +63,8 @@ constexpr uint32_t kOffEmax = kOffAlphaM + kHC * 4;      // max E over the heads
 constexpr uint32_t kOffRed = kOffEmax + 16;          // 2 x 4 quadrants x 32 heads
 constexpr uint32_t kOffBar = kOffRed + 2 * 4 * kHC * 4;
 constexpr uint32_t kOffMisc = kOffBar + 16 * 8;
-constexpr uint32_t kSmemUsed = kOffMisc + 32;
+constexpr uint32_t kOffCent = kOffMisc + 32;             // PolarQuant: [level 1..9][16] (cos, sin)
+constexpr uint32_t kSmemUsed = kOffCent + 9 * 16 * 8;
 static_assert(kOffSlot % 1024 == 0, "swizzled operands need 1024-byte alignment");
 static_assert(kSmemUsed <= 232448, "shared memory budget");
 
@@ -125,6 +131,134 @@ __device__ __forceinline__ void levels4(const LevelBytes& t, uint32_t s, uint32_
     w1 = __byte_perm(l, h, 0x7362u);
 }
 
+// PolarQuant, 4 bits: a worker's raw share of a tile is half of one row --
+// row 32 (warp / 2) + lane, half h = warp % 2 -- as the byte ranges holding the
+// angles of that half: latent level 1 (bytes 64 h .. + 63), level 2
+// (128 + 32 h .. + 31), level 3 (192 + 16 h .. + 15), levels 4-9 of both halves
+// (bytes 224 .. 255) and the whole rope block (256 .. 287).  Angle a of a
+// block is nibble a of its stream (level 1 first); level l starts at angle
+// n - n / 2^(l-1).
+struct RawPQ {
+    uint4 l1[4], l2[2], l3, tail[2], rope[2];
+};
+
+__device__ __forceinline__ void load_pq(RawPQ& r, const uint8_t* __restrict__ codes, int64_t t0, int nt, int warp,
+                                        int lane) {
+    const int row = 32 * (warp >> 1) + lane, h = warp & 1;
+    const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+    const uint4* base = reinterpret_cast<const uint4*>(codes + (t0 + row) * kRowBytes);
+    const bool ok = row < nt;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) r.l1[i] = ok ? __ldg(base + 4 * h + i) : z;
+#pragma unroll
+    for (int i = 0; i < 2; ++i) r.l2[i] = ok ? __ldg(base + 8 + 2 * h + i) : z;
+    r.l3 = ok ? __ldg(base + 12 + h) : z;
+#pragma unroll
+    for (int i = 0; i < 2; ++i) r.tail[i] = ok ? __ldg(base + 14 + i) : z;
+#pragma unroll
+    for (int i = 0; i < 2; ++i) r.rope[i] = ok ? __ldg(base + 16 + i) : z;
+}
+
+template <int N>
+__device__ __forceinline__ void words_of(const uint4 (&v)[N], uint32_t (&w)[4 * N]) {
+#pragma unroll
+    for (int i = 0; i < N; ++i) {
+        w[4 * i] = v[i].x;
+        w[4 * i + 1] = v[i].y;
+        w[4 * i + 2] = v[i].z;
+        w[4 * i + 3] = v[i].w;
+    }
+}
+
+// nibble i of a word array (i a compile-time index after unrolling)
+template <int W>
+__device__ __forceinline__ uint32_t nib(const uint32_t (&w)[W], int i) {
+    return (w[i >> 3] >> (4 * (i & 7))) & 15u;
+}
+
+// children of node radius r under the angle with code c at level l: (r cos, r sin)
+__device__ __forceinline__ void split(const float2* cent, int level, uint32_t c, float r, float& a, float& b) {
+    const float2 cs = cent[(level - 1) * 16 + c];
+    a = __fmul_rn(r, cs.x);
+    b = __fmul_rn(r, cs.y);
+}
+
+__device__ __forceinline__ uint32_t pack_h2(float a, float b) {
+    const __half2 h2 = __floats2half2_rn(a, b);
+    return *reinterpret_cast<const uint32_t*>(&h2);
+}
+
+// Latent half h of a row: its 256 leaves (unit top radius) as f16 into
+// chunks 4 h .. 4 h + 3 of swizzled row `row`.  h is a template argument so
+// that every nibble index is a constant (the code words stay in registers).
+template <int h>
+__device__ __forceinline__ void pq_latent_half(const RawPQ& r, int row, const float2* cent, unsigned char* sSlot) {
+    uint32_t T[8], L3[4], L2[8], L1[16];
+    words_of(r.tail, T);
+    L3[0] = r.l3.x; L3[1] = r.l3.y; L3[2] = r.l3.z; L3[3] = r.l3.w;
+    words_of(r.l2, L2);
+    words_of(r.l1, L1);
+    // levels 9 .. 5: angles 510, 508 + h, 504 + 2h + j, 496 + 4h + j, 480 + 8h + j
+    // (tail nibbles 62, 60 + h, 56 + 2h + j, 48 + 4h + j, 32 + 8h + j)
+    float a9, b9;
+    split(cent, 9, nib(T, 62), 1.0f, a9, b9);
+    const float r8 = h ? b9 : a9;
+    float r7[2], r6[4], r5[8], r4[16];
+    split(cent, 8, nib(T, 60 + h), r8, r7[0], r7[1]);
+#pragma unroll
+    for (int j = 0; j < 2; ++j) split(cent, 7, nib(T, 56 + 2 * h + j), r7[j], r6[2 * j], r6[2 * j + 1]);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) split(cent, 6, nib(T, 48 + 4 * h + j), r6[j], r5[2 * j], r5[2 * j + 1]);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) split(cent, 5, nib(T, 32 + 8 * h + j), r5[j], r4[2 * j], r4[2 * j + 1]);
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+        // the 16-leaf subtree k: level 4 (tail nibble 16 h + k), level 3 (l3
+        // nibbles 2k, 2k + 1), level 2 (l2 nibbles 4k ..), level 1 (l1 nibbles 8k ..)
+        float r3[2], r2[4], r1[8], x[16];
+        split(cent, 4, nib(T, 16 * h + k), r4[k], r3[0], r3[1]);
+#pragma unroll
+        for (int i = 0; i < 2; ++i) split(cent, 3, nib(L3, 2 * k + i), r3[i], r2[2 * i], r2[2 * i + 1]);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) split(cent, 2, nib(L2, 4 * k + i), r2[i], r1[2 * i], r1[2 * i + 1]);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) split(cent, 1, nib(L1, 8 * k + i), r1[i], x[2 * i], x[2 * i + 1]);
+        unsigned char* slot = sSlot + (4 * h + (k >> 2)) * kSlotBytes;
+#pragma unroll
+        for (int q = 0; q < 2; ++q)
+            *reinterpret_cast<uint4*>(slot + sw128(row, 32 * (k & 3) + 16 * q)) =
+                make_uint4(pack_h2(x[8 * q], x[8 * q + 1]), pack_h2(x[8 * q + 2], x[8 * q + 3]),
+                           pack_h2(x[8 * q + 4], x[8 * q + 5]), pack_h2(x[8 * q + 6], x[8 * q + 7]));
+    }
+}
+
+// Rope half h of a row (64 dims, 6 levels): leaves 32 h .. 32 h + 31 into the
+// rope chunk's slot, bytes 64 h .. 64 h + 63 of swizzled row `row`.
+template <int h>
+__device__ __forceinline__ void pq_rope_half(const RawPQ& r, int row, const float2* cent, unsigned char* sRopeSlot) {
+    uint32_t R[8];
+    words_of(r.rope, R);
+    // levels 6 .. 1 of the rope block start at angles 62, 60, 56, 48, 32, 0
+    float a6, b6;
+    split(cent, 6, nib(R, 62), 1.0f, a6, b6);
+    const float r5 = h ? b6 : a6;
+    float r4[2], r3[4], r2[8], r1[16], x[32];
+    split(cent, 5, nib(R, 60 + h), r5, r4[0], r4[1]);
+#pragma unroll
+    for (int j = 0; j < 2; ++j) split(cent, 4, nib(R, 56 + 2 * h + j), r4[j], r3[2 * j], r3[2 * j + 1]);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) split(cent, 3, nib(R, 48 + 4 * h + j), r3[j], r2[2 * j], r2[2 * j + 1]);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) split(cent, 2, nib(R, 32 + 8 * h + j), r2[j], r1[2 * j], r1[2 * j + 1]);
+#pragma unroll
+    for (int j = 0; j < 16; ++j) split(cent, 1, nib(R, 16 * h + j), r1[j], x[2 * j], x[2 * j + 1]);
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+        *reinterpret_cast<uint4*>(sRopeSlot + sw128(row, 64 * h + 16 * q)) =
+            make_uint4(pack_h2(x[8 * q], x[8 * q + 1]), pack_h2(x[8 * q + 2], x[8 * q + 3]),
+                       pack_h2(x[8 * q + 4], x[8 * q + 5]), pack_h2(x[8 * q + 6], x[8 * q + 7]));
+}
+
 // 16 code bytes (32 codes) -> 32 f16 levels at byte offset `b` (64 bytes) of
 // swizzled row `row`.
 __device__ __forceinline__ void store32(unsigned char* slot, const uint4& c, int row, int b, const LevelBytes& t) {
@@ -138,7 +272,7 @@ __device__ __forceinline__ void store32(unsigned char* slot, const uint4& c, int
     }
 }
 
-template <bool QBF16>
+template <bool QBF16, bool PQ>
 __global__ void __launch_bounds__(kThreads, 1) attn_tc_tq4_kernel(AttnParams p) {
     launch_dependents();
     const int64_t w = blockIdx.x;
@@ -148,6 +282,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_tq4_kernel(AttnParams p) 
     unsigned char* sSlot = sm + kOffSlot;
     unsigned char* sP = sSlot + kRope * kSlotBytes;
     unsigned char* sLevels = sm + kOffLevels;
+    float2* sCent = reinterpret_cast<float2*>(sm + kOffCent);
     float* sM = reinterpret_cast<float*>(sm + kOffM);
     float* sR = reinterpret_cast<float*>(sm + kOffR);
     float* sE = reinterpret_cast<float*>(sm + kOffE);
@@ -205,7 +340,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_tq4_kernel(AttnParams p) 
     }
     if (tid == 64) {
         for (int i = 0; i < kNumBars; ++i) {
-            const uint32_t count = (i < kBarFree0 || i == kBarP) ? (uint32_t)kWorkers : 1u;
+            // PolarQuant: each latent group comes from the 128 threads of one half
+            const uint32_t count = (i < kBarFree0 || i == kBarP)
+                                       ? ((PQ && i < kBarFull0 + 2) ? (uint32_t)kWorkers / 2 : (uint32_t)kWorkers)
+                                       : 1u;
             asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(&bars[i])), "r"(count));
         }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -217,7 +355,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_tq4_kernel(AttnParams p) 
         sE[tid] = 0.0f;
         sF[tid] = 0.0f;
     }
-    if (tid == 0) {
+    if (PQ)
+        for (int i = tid; i < 9 * 16; i += kThreads) sCent[i] = p.pq_cent[i];
+    if (!PQ && tid == 0) {
         // one thread builds both planes in registers and stores each as one
         // 16-byte word, so no word of them is written by two threads; the
         // barrier after the prologue orders these stores before every reader
@@ -269,7 +409,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_tq4_kernel(AttnParams p) 
     int e_q = 0;
     if (q_bound > 0.0f) frexpf(q_bound, &e_q);
     const float q_scale = q_bound > 0.0f ? ldexpf(1.0f, 14 - e_q) : 1.0f;
-    const float cz = p.sm_scale * kLog2e * (q_bound > 0.0f ? ldexpf(1.0f, e_q - 14) : 1.0f) * kTq4InvGamma;
+    const float cz = p.sm_scale * kLog2e * (q_bound > 0.0f ? ldexpf(1.0f, e_q - 14) : 1.0f) * (PQ ? 1.0f : kTq4InvGamma);
     if (tid < kWorkers) {
 #pragma unroll
         for (int hh = 0; hh < 4; ++hh) {
@@ -382,13 +522,18 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_tq4_kernel(AttnParams p) 
     };
     RawGroup rawA, rawB;
     uint4 rawC;
-    {
-        const int nt0 = (int)min((int64_t)kRows, row1 - row0);
-        load_group(rawA, p.codes, row0, nt0, 0, warp, lane);
-        load_group(rawB, p.codes, row0, nt0, 1, warp, lane);
-        rawC = load_rope(p.codes, row0, nt0, warp, lane);
-        load_scales(row0, nt0);
-    }
+    RawPQ rawP;
+    auto load_tile = [&](int64_t t0n, int ntn) {
+        if constexpr (PQ) {
+            load_pq(rawP, p.codes, t0n, ntn, warp, lane);
+        } else {
+            load_group(rawA, p.codes, t0n, ntn, 0, warp, lane);
+            load_group(rawB, p.codes, t0n, ntn, 1, warp, lane);
+            rawC = load_rope(p.codes, t0n, ntn, warp, lane);
+        }
+        load_scales(t0n, ntn);
+    };
+    load_tile(row0, (int)min((int64_t)kRows, row1 - row0));
     int t = 0;
     for (; t < n_tiles; ++t) {
         const int64_t t0 = row0 + (int64_t)t * kRows;
@@ -400,7 +545,24 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_tq4_kernel(AttnParams p) 
         const float my_sl = sl_next, my_sr = sr_next;
         // ---- decode the tile: groups A (chunks 0-3), B (4-7), C (rope) ----
         const uint32_t prev = (uint32_t)(t - 1) & 1u;
-        {
+        if constexpr (PQ) {
+            // half h of row 32 (warp / 2) + lane: latent chunks 4h .. 4h + 3
+            // (group A or B), then half of the rope chunk (group C)
+            const int h = warp & 1, row = 32 * (warp >> 1) + lane;
+            if (t > 0) {
+                mbar_wait(&bars[kBarFree0 + 2 * h], prev, sAbort, p.wait_limit);
+                mbar_wait(&bars[kBarFree0 + 2 * h + 1], prev, sAbort, p.wait_limit);
+            }
+            if (h) pq_latent_half<1>(rawP, row, sCent, sSlot);
+            else pq_latent_half<0>(rawP, row, sCent, sSlot);
+            fence_async_smem();
+            mbar_arrive(&bars[kBarFull0 + h]);
+            if (t > 0 && h == 0) mbar_wait(&bars[kBarFree0 + 3], prev, sAbort, p.wait_limit);
+            if (h) pq_rope_half<1>(rawP, row, sCent, sSlot + kRope * kSlotBytes);
+            else pq_rope_half<0>(rawP, row, sCent, sSlot + kRope * kSlotBytes);
+            fence_async_smem();
+            mbar_arrive(&bars[kBarFull0 + 2]);
+        } else {
             // the level byte planes, re-read per tile (asm volatile: not kept
             // in registers across the softmax)
             LevelBytes lvb;
@@ -434,12 +596,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_tq4_kernel(AttnParams p) 
         const int nt1 = (int)min((int64_t)kRows, row1 - t1);
         // all of tile t+1 is requested before the softmax (the raw codes stay in
         // registers across it: the workers' share of the register split)
-        if (t + 1 < n_tiles) {
-            load_group(rawA, p.codes, t1, nt1, 0, warp, lane);
-            load_group(rawB, p.codes, t1, nt1, 1, warp, lane);
-            rawC = load_rope(p.codes, t1, nt1, warp, lane);
-            load_scales(t1, nt1);
-        }
+        if (t + 1 < n_tiles) load_tile(t1, nt1);
 
         // ---- softmax of the tile: thread = row srow, 16 heads ----
         mbar_wait(&bars[kBarScore], (uint32_t)t & 1u, sAbort, p.wait_limit);
@@ -571,7 +728,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_tq4_kernel(AttnParams p) 
         const int64_t unit = blockIdx.x;
         const int64_t item = unit / (p.n_heads / kHC);
         const int hbase = (int)(unit % (p.n_heads / kHC)) * kHC;
-        const float o_scale = kTq4InvGamma;
+        const float o_scale = PQ ? 1.0f : kTq4InvGamma;
 #pragma unroll
         for (int bi = 0; bi < 2; ++bi) {
             const int db = 2 * hq + bi;
@@ -598,26 +755,29 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_tq4_kernel(AttnParams p) 
     if (warp == 1) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols));
 }
 
-template <bool QBF16>
+template <bool QBF16, bool PQ>
 cudaError_t launch_tq4(const AttnParams& p, int64_t grid_x, int groups, cudaStream_t stream) {
     // the workers' setmaxnreg.inc waits for registers the other warpgroup
     // released: launch only if the split adds up against the launch's count
     cudaFuncAttributes fa{};
-    cudaError_t e = cudaFuncGetAttributes(&fa, attn_tc_tq4_kernel<QBF16>);
+    cudaError_t e = cudaFuncGetAttributes(&fa, attn_tc_tq4_kernel<QBF16, PQ>);
     if (e != cudaSuccess) return e;
     if (kWorkers * kRegsWorker + 128 * kRegsMma > kThreads * fa.numRegs) return cudaErrorInvalidConfiguration;
-    e = cudaFuncSetAttribute(attn_tc_tq4_kernel<QBF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (PQ && !p.pq_cent) return cudaErrorInvalidSymbol;
+    e = cudaFuncSetAttribute(attn_tc_tq4_kernel<QBF16, PQ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)kSmemUsed);
     if (e != cudaSuccess) return e;
-    attn_tc_tq4_kernel<QBF16><<<dim3((unsigned)(grid_x * groups)), kThreads, kSmemUsed, stream>>>(p);
+    attn_tc_tq4_kernel<QBF16, PQ><<<dim3((unsigned)(grid_x * groups)), kThreads, kSmemUsed, stream>>>(p);
     return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_attn_tc_tq4(const AttnParams& p, bool q_bf16, int64_t grid_x, int n_heads, cudaStream_t stream) {
-    return q_bf16 ? launch_tq4<true>(p, grid_x, n_heads / kHC, stream)
-                  : launch_tq4<false>(p, grid_x, n_heads / kHC, stream);
+cudaError_t launch_attn_tc_tq4(const AttnParams& p, bool q_bf16, bool pq, int64_t grid_x, int n_heads,
+                               cudaStream_t stream) {
+    const int g = n_heads / kHC;
+    if (pq) return q_bf16 ? launch_tq4<true, true>(p, grid_x, g, stream) : launch_tq4<false, true>(p, grid_x, g, stream);
+    return q_bf16 ? launch_tq4<true, false>(p, grid_x, g, stream) : launch_tq4<false, false>(p, grid_x, g, stream);
 }
 
 }  // namespace kvq

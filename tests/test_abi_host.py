@@ -252,10 +252,14 @@ def test_polar_row_bytes_and_validation(kvq, oracle):
     assert L.pq_encode(14, d, 4, C.byref(odd), None, d, d, None, None) == 2
     assert L.pq_decode(14, d, d, 4, C.byref(odd), 0, d, None) == 2
     assert L.pq_decode(2, d, d, 4, C.byref(lay), 0, d, None) == 1
-    # attention: the fp32 path serves PolarQuant, the tensor path refuses it
-    assert kvq.kv_attn_workspace_size(14, 8, 128, 32768) == kvq.kv_attn_workspace_size(14, 8, 128, 32768,
+    # attention: the fp32 path serves every PolarQuant width, the tensor path 4 bits only
+    assert kvq.kv_attn_workspace_size(13, 8, 128, 32768) == kvq.kv_attn_workspace_size(13, 8, 128, 32768,
                                                                                         path=kvq.PATH_SIMT) > 0
-    assert kvq.kv_attn_workspace_size(14, 8, 128, 32768, path=kvq.PATH_TENSOR) == 0
+    assert kvq.kv_attn_workspace_size(13, 8, 128, 32768, path=kvq.PATH_TENSOR) == 0
+    assert kvq.kv_attn_workspace_size(14, 8, 128, 32768, path=kvq.PATH_TENSOR) == \
+        kvq.kv_attn_workspace_size(2, 8, 128, 32768, path=kvq.PATH_TENSOR) > 0
+    assert kvq.kv_attn_workspace_size(14, 8, 128, 32768) == kvq.kv_attn_workspace_size(14, 8, 128, 32768,
+                                                                                        path=kvq.PATH_SIMT)
     ws = C.c_void_p(1 << 21)
-    assert L.kv_attn_decode(14, C.byref(lay), d, 1, 2, 128, d, d, d, 10, 0.1, d, ws, 1 << 30, kvq.PATH_TENSOR,
+    assert L.kv_attn_decode(12, C.byref(lay), d, 1, 2, 128, d, d, d, 10, 0.1, d, ws, 1 << 30, kvq.PATH_TENSOR,
                             None) == 5

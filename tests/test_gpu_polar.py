@@ -9,7 +9,13 @@
   the context unrotated once) within the fp32 bound 1e-5 of exact attention
   over the oracle's reconstruction: ragged decode with empty and one-row
   sequences, bf16 and f32 queries, the append step, the gather decode and a
-  small chunked prefill.
+  small chunked prefill;
+* the tensor-core consumer of 4-bit rows (the TQ4 kernel with the trees
+  rebuilt into f16 operands; KVQ_PATH_TENSOR only) within 4e-3: each leaf is
+  an f32 product rounded once to f16 (up to 2^-11 relative, about five times
+  the 9.3e-5 of TQ4's scaled levels), so the bound is twice the 2e-3 of the
+  KV8/TQ4 tensor path (worst measured 2.7e-3, on 300- and 900-row sequences):
+  the same ragged decode, the append step at the benchmark's size, a prefill.
 """
 import math
 
@@ -17,11 +23,12 @@ import numpy as np
 import pytest
 import torch
 
-from gpu_common import SIMT_TOL, gpu_encode, kvq_module, queries, rel_err, to_dev
+from gpu_common import SIMT_TOL, TENSOR_TOL, gpu_encode, kvq_module, queries, rel_err, to_dev
 from quantized_kv_cache_kv8_gb300 import synth
 
 pytestmark = pytest.mark.gpu
 SM = 1.0 / math.sqrt(192.0)
+PQ_TENSOR_TOL = 2 * TENSOR_TOL
 NONFINITE = 9
 
 
@@ -140,8 +147,9 @@ def test_ragged_decode_against_oracle(kvq, oracle, bits, bf16):
     codes, radii = gpu_encode(kvq, fmt, x, layout)
     q_dev, q = queries(21 + bits, (B, H, 576), bf16)
     out = torch.full((B, H, 512), float("nan"), device="cuda")
-    ws = torch.zeros(kvq.kv_attn_workspace_size(fmt, B, H, int(cu[-1]), layout), dtype=torch.uint8, device="cuda")
-    kvq.kv_attn_decode(fmt, q_dev, codes, radii, to_dev(cu), out, ws, int(cu[-1]), SM, layout)
+    S = kvq.PATH_SIMT
+    ws = torch.zeros(kvq.kv_attn_workspace_size(fmt, B, H, int(cu[-1]), layout, S), dtype=torch.uint8, device="cuda")
+    kvq.kv_attn_decode(fmt, q_dev, codes, radii, to_dev(cu), out, ws, int(cu[-1]), SM, layout, S)
     torch.cuda.synchronize()
     assert kvq.read_device_error(ws) == 0
     oc, orr = oracle.pq_encode(x, bits, seed=6)
@@ -153,9 +161,14 @@ def test_ragged_decode_against_oracle(kvq, oracle, bits, bf16):
             assert rel_err(got[b, h], ref[h]) <= SIMT_TOL, (b, h)
 
 
-def test_tensor_path_is_refused(kvq):
+def test_tensor_path_serves_four_bits_only(kvq):
     layout = kvq.mla_layout()
-    assert kvq.kv_attn_workspace_size(14, 2, 128, 100, layout, path=kvq.PATH_TENSOR) == 0
+    for bits in (2, 3, 5, 6):
+        assert kvq.kv_attn_workspace_size(kvq.pq_format(bits), 2, 128, 100, layout, path=kvq.PATH_TENSOR) == 0
+    assert kvq.kv_attn_workspace_size(14, 2, 128, 100, layout, path=kvq.PATH_TENSOR) > 0
+    # AUTO keeps PolarQuant on the fp32 consumer
+    assert kvq.kv_attn_workspace_size(14, 2, 128, 100, layout) == \
+        kvq.kv_attn_workspace_size(14, 2, 128, 100, layout, path=kvq.PATH_SIMT)
 
 
 def test_append_step_and_gather(kvq, oracle):
@@ -168,9 +181,10 @@ def test_append_step_and_gather(kvq, oracle):
     dst = (cu[1:] - 1).astype(np.int64)
     q_dev, q = queries(32, (B, H, 576), True)
     out = torch.empty((B, H, 512), device="cuda")
-    ws = torch.zeros(kvq.kv_attn_workspace_size(14, B, H, int(cu[-1]), layout), dtype=torch.uint8, device="cuda")
+    S = kvq.PATH_SIMT
+    ws = torch.zeros(kvq.kv_attn_workspace_size(14, B, H, int(cu[-1]), layout, S), dtype=torch.uint8, device="cuda")
     kvq.kv_attn_decode_append(14, to_dev(x_new), to_dev(dst), q_dev, codes, radii, to_dev(cu), out, ws, int(cu[-1]),
-                              SM, layout)
+                              SM, layout, S)
     torch.cuda.synchronize()
     assert kvq.read_device_error(ws) == 0
     xa = x.copy()
@@ -222,3 +236,127 @@ def test_small_prefill(kvq, oracle):
         ref = oracle.attn_dense(np.ascontiguousarray(xh[:P + j + 1]), np.ascontiguousarray(q[j]), SM, 512)
         for h in range(H):
             assert rel_err(got[j, h], ref[h]) <= SIMT_TOL, (j, h)
+
+
+def test_bench_step_at_full_size(kvq, oracle):
+    """The PolarQuant-4 step the benchmark times (8 x 4096 rows, 128 heads,
+    bf16 queries, the step's 8 rows appended; fp32 consumer), every
+    (sequence, head) against the oracle."""
+    B, T, H = 8, 4096, 128
+    layout = kvq.mla_layout(seed=4)
+    x = synth.mla_rows(2, B * T)
+    codes, radii = gpu_encode(kvq, 14, x, layout)
+    cu = synth.cu_seqlens([T] * B)
+    dst = (cu[1:] - 1).astype(np.int64)
+    x_new = synth.mla_rows(102, B)
+    q_dev, q = queries(3, (B, H, 576), True)
+    out = torch.full((B, H, 512), float("nan"), device="cuda")
+    S = kvq.PATH_SIMT
+    ws = torch.zeros(kvq.kv_attn_workspace_size(14, B, H, B * T, layout, S), dtype=torch.uint8, device="cuda")
+    kvq.kv_attn_decode_append(14, to_dev(x_new), to_dev(dst), q_dev, codes, radii, to_dev(cu), out, ws, B * T, SM,
+                              layout, S)
+    torch.cuda.synchronize()
+    assert kvq.read_device_error(ws) == 0
+    xa = x.copy()
+    xa[dst] = x_new
+    oc, orr = oracle.pq_encode(xa, 4, seed=4)
+    np.testing.assert_array_equal(codes.cpu().numpy(), oc)
+    np.testing.assert_array_equal(radii.cpu().numpy().view(np.uint32), orr.view(np.uint32))
+    xh = oracle.pq_decode(oc, orr, 4, seed=4)
+    got = out.cpu().numpy()
+    for b in range(B):
+        ref = oracle.attn_dense(np.ascontiguousarray(xh[cu[b]:cu[b + 1]]), np.ascontiguousarray(q[b]), SM, 512)
+        for h in range(H):
+            assert rel_err(got[b, h], ref[h]) <= SIMT_TOL, (b, h)
+
+
+@pytest.mark.parametrize("bits", [2, 6])
+def test_encode_at_ragged_pool_scale(kvq, oracle, bits):
+    """An encode of the ragged workload's 131072-row master block; 3000
+    sampled rows bit for bit against the oracle."""
+    layout = kvq.mla_layout(seed=4)
+    x = synth.mla_rows(4, 131072)
+    codes, radii = gpu_encode(kvq, kvq.pq_format(bits), x, layout)
+    rows = np.sort(np.random.default_rng(bits).choice(131072, 3000, replace=False))
+    oc, orr = oracle.pq_encode(np.ascontiguousarray(x[rows]), bits, seed=4)
+    np.testing.assert_array_equal(codes.cpu().numpy()[rows], oc)
+    np.testing.assert_array_equal(radii.cpu().numpy()[rows].view(np.uint32), orr.view(np.uint32))
+
+
+@pytest.mark.parametrize("bf16", [True, False], ids=["bf16", "f32"])
+def test_tensor_ragged_decode_against_oracle(kvq, oracle, bf16):
+    lengths = [0, 1, 17, 300, 1000, 129, 2048]
+    x, cu = ragged_case(60, lengths)
+    B, H = len(lengths), 128
+    layout = kvq.mla_layout(seed=6)
+    codes, radii = gpu_encode(kvq, 14, x, layout)
+    q_dev, q = queries(61, (B, H, 576), bf16)
+    out = torch.full((B, H, 512), float("nan"), device="cuda")
+    ws = torch.zeros(kvq.kv_attn_workspace_size(14, B, H, int(cu[-1]), layout, kvq.PATH_TENSOR), dtype=torch.uint8,
+                     device="cuda")
+    kvq.kv_attn_decode(14, q_dev, codes, radii, to_dev(cu), out, ws, int(cu[-1]), SM, layout, kvq.PATH_TENSOR)
+    torch.cuda.synchronize()
+    assert kvq.read_device_error(ws) == 0
+    oc, orr = oracle.pq_encode(x, 4, seed=6)
+    xh = oracle.pq_decode(oc, orr, 4, seed=6)
+    got = out.cpu().numpy()
+    for b in range(B):
+        ref = oracle.attn_dense(np.ascontiguousarray(xh[cu[b]:cu[b + 1]]), np.ascontiguousarray(q[b]), SM, 512)
+        for h in range(H):
+            assert rel_err(got[b, h], ref[h]) <= PQ_TENSOR_TOL, (b, h)
+
+
+def test_tensor_bench_step_at_full_size(kvq, oracle):
+    """The benchmark's PolarQuant-4 step (8 x 4096 rows, 128 heads, bf16, the
+    step's rows appended) on the tensor-core path, every (sequence, head)."""
+    B, T, H = 8, 4096, 128
+    layout = kvq.mla_layout(seed=4)
+    x = synth.mla_rows(2, B * T)
+    codes, radii = gpu_encode(kvq, 14, x, layout)
+    cu = synth.cu_seqlens([T] * B)
+    dst = (cu[1:] - 1).astype(np.int64)
+    x_new = synth.mla_rows(102, B)
+    q_dev, q = queries(3, (B, H, 576), True)
+    out = torch.full((B, H, 512), float("nan"), device="cuda")
+    ws = torch.zeros(kvq.kv_attn_workspace_size(14, B, H, B * T, layout, kvq.PATH_TENSOR), dtype=torch.uint8,
+                     device="cuda")
+    kvq.kv_attn_decode_append(14, to_dev(x_new), to_dev(dst), q_dev, codes, radii, to_dev(cu), out, ws, B * T, SM,
+                              layout, kvq.PATH_TENSOR)
+    torch.cuda.synchronize()
+    assert kvq.read_device_error(ws) == 0
+    xa = x.copy()
+    xa[dst] = x_new
+    oc, orr = oracle.pq_encode(xa, 4, seed=4)
+    np.testing.assert_array_equal(codes.cpu().numpy(), oc)
+    xh = oracle.pq_decode(oc, orr, 4, seed=4)
+    got = out.cpu().numpy()
+    for b in range(B):
+        ref = oracle.attn_dense(np.ascontiguousarray(xh[cu[b]:cu[b + 1]]), np.ascontiguousarray(q[b]), SM, 512)
+        for h in range(H):
+            assert rel_err(got[b, h], ref[h]) <= PQ_TENSOR_TOL, (b, h)
+
+
+def test_tensor_prefill(kvq, oracle):
+    P, N, H = 900, 20, 64
+    layout = kvq.mla_layout(seed=9)
+    x = synth.mla_rows(62, P + N)
+    rb = kvq.row_bytes(14)
+    codes = torch.zeros((P + N, rb), dtype=torch.uint8, device="cuda")
+    radii = torch.zeros((P + N, 2), dtype=torch.float32, device="cuda")
+    pc, pr = gpu_encode(kvq, 14, x[:P], layout)
+    codes[:P], radii[:P] = pc, pr
+    q_dev, q = queries(63, (N, H, 576), True)
+    out = torch.empty((N, H, 512), device="cuda")
+    ws = torch.zeros(kvq.kv_attn_prefill_workspace_size(14, H, P, N, layout, kvq.PATH_TENSOR), dtype=torch.uint8,
+                     device="cuda")
+    kvq.kv_attn_prefill(14, to_dev(x[P:]), q_dev, codes, radii, P, out, ws, SM, layout, kvq.PATH_TENSOR)
+    torch.cuda.synchronize()
+    assert kvq.read_device_error(ws) == 0
+    oc, orr = oracle.pq_encode(x, 4, seed=9)
+    np.testing.assert_array_equal(codes.cpu().numpy(), oc)
+    xh = oracle.pq_decode(oc, orr, 4, seed=9)
+    got = out.cpu().numpy()
+    for j in range(N):
+        ref = oracle.attn_dense(np.ascontiguousarray(xh[:P + j + 1]), np.ascontiguousarray(q[j]), SM, 512)
+        for h in range(H):
+            assert rel_err(got[j, h], ref[h]) <= PQ_TENSOR_TOL, (j, h)
