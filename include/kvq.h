@@ -442,12 +442,16 @@ typedef struct kvq_k2v4_layout {
  *   k_scales  [batch][n_kv_heads][capacity/32][head_dim] fp16 bits
  *   v_blocks  [batch][n_kv_heads][capacity][head_dim/32][18] bytes (q4_0)
  *   k_win, v_win [batch][n_kv_heads][n_sink+n_window+n_slack][head_dim] fp16
+ *   err_word  NULL, or a device int32 error word set to KVQ_ERR_NONFINITE (if
+ *             still 0) by a NaN or infinite K or V value (or K squares past
+ *             the f32 range); the codes of the group or block holding it are
+ *             then unspecified, the others are encoded as usual
  * Overlay slot of cell c: c < n_sink -> c; c >= n_cells - n_window ->
  * n_sink + c mod (n_window + n_slack). */
 kvq_status k2v4_encode(const kvq_k2v4_layout* layout, const float* k, const float* v,
                        int32_t batch, int64_t n_cells, int64_t capacity,
                        uint8_t* k_codes, uint16_t* k_scales, uint8_t* v_blocks,
-                       uint16_t* k_win, uint16_t* v_win, void* stream);
+                       uint16_t* k_win, uint16_t* v_win, int32_t* err_word, void* stream);
 
 /* Appends n_new cells to every sequence at cells n_past .. n_past + n_new - 1
  * (the engine's append patterns of [P3] "Attention error under the engine's
@@ -468,11 +472,11 @@ kvq_status k2v4_encode(const kvq_k2v4_layout* layout, const float* k, const floa
  * Stored scale fp16(k_gain * s), codes against s, as in the encoder.  V and
  * the overlay of the new cells as in the encoder, the window taken at
  * n_past + n_new.  Requires n_past + n_new <= capacity (a multiple of 32);
- * returns KVQ_ERR_ARG otherwise. */
+ * returns KVQ_ERR_ARG otherwise.  err_word as for k2v4_encode. */
 kvq_status k2v4_append(const kvq_k2v4_layout* layout, const float* k_new, const float* v_new,
                        int32_t batch, int64_t n_past, int64_t n_new, int64_t capacity,
                        uint8_t* k_codes, uint16_t* k_scales, uint8_t* v_blocks,
-                       uint16_t* k_win, uint16_t* v_win, void* stream);
+                       uint16_t* k_win, uint16_t* v_win, int32_t* err_word, void* stream);
 
 size_t kv_attn_decode_k2v4_workspace_size(const kvq_k2v4_layout* layout, int32_t batch,
                                           int32_t n_q_heads, int64_t n_cells, kvq_path path);

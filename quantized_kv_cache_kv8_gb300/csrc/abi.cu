@@ -458,7 +458,7 @@ int64_t kvq_read_exact_rescales(void* workspace, int32_t clear, void* stream) {
 
 kvq_status k2v4_encode(const kvq_k2v4_layout* layout, const float* k, const float* v, int32_t batch,
                        int64_t n_cells, int64_t capacity, uint8_t* k_codes, uint16_t* k_scales, uint8_t* v_blocks,
-                       uint16_t* k_win, uint16_t* v_win, void* stream) {
+                       uint16_t* k_win, uint16_t* v_win, int32_t* err_word, void* stream) {
     kvq_status s = check_k2v4(layout);
     if (s != KVQ_OK) return s;
     if (batch < 0 || n_cells < 0 || capacity < n_cells) return KVQ_ERR_ARG;
@@ -468,12 +468,12 @@ kvq_status k2v4_encode(const kvq_k2v4_layout* layout, const float* k, const floa
     if (!k || !v || !k_codes || !k_scales || !v_blocks) return KVQ_ERR_ARG;
     if ((layout->n_sink + layout->n_window) > 0 && (!k_win || !v_win)) return KVQ_ERR_ARG;
     return cuda_status(launch_k2v4_encode(*layout, k, v, batch, n_cells, capacity, k_codes, k_scales, v_blocks, k_win,
-                                          v_win, (cudaStream_t)stream));
+                                          v_win, err_word, (cudaStream_t)stream));
 }
 
 kvq_status k2v4_append(const kvq_k2v4_layout* layout, const float* k_new, const float* v_new, int32_t batch,
                        int64_t n_past, int64_t n_new, int64_t capacity, uint8_t* k_codes, uint16_t* k_scales,
-                       uint8_t* v_blocks, uint16_t* k_win, uint16_t* v_win, void* stream) {
+                       uint8_t* v_blocks, uint16_t* k_win, uint16_t* v_win, int32_t* err_word, void* stream) {
     kvq_status s = check_k2v4(layout);
     if (s != KVQ_OK) return s;
     if (batch < 0 || n_past < 0 || n_new < 0 || capacity < 0 || n_past > capacity - n_new) return KVQ_ERR_ARG;
@@ -483,7 +483,7 @@ kvq_status k2v4_append(const kvq_k2v4_layout* layout, const float* k_new, const 
     if (!k_new || !v_new || !k_codes || !k_scales || !v_blocks) return KVQ_ERR_ARG;
     if ((layout->n_sink + layout->n_window) > 0 && (!k_win || !v_win)) return KVQ_ERR_ARG;
     return cuda_status(launch_k2v4_append(*layout, k_new, v_new, batch, n_past, n_new, capacity, k_codes, k_scales,
-                                          v_blocks, k_win, v_win, (cudaStream_t)stream));
+                                          v_blocks, k_win, v_win, err_word, (cudaStream_t)stream));
 }
 
 size_t kv_attn_decode_k2v4_workspace_size(const kvq_k2v4_layout* layout, int32_t batch, int32_t n_q_heads,

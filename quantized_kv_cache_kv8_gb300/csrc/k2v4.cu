@@ -47,7 +47,7 @@ __device__ __forceinline__ int64_t overlay_slot(int64_t c, const K2V4Params& p) 
 // grid: (groups, H, batch), block: D threads (one per channel)
 __global__ void __launch_bounds__(kMaxD) k2_encode_kernel(const float* __restrict__ k, K2V4Params p,
                                                           uint8_t* __restrict__ k_codes,
-                                                          uint16_t* __restrict__ k_scales) {
+                                                          uint16_t* __restrict__ k_scales, int32_t* err) {
     const int d = threadIdx.x;
     const int64_t gi = blockIdx.x;
     const int g = blockIdx.y, b = blockIdx.z;
@@ -63,6 +63,8 @@ __global__ void __launch_bounds__(kMaxD) k2_encode_kernel(const float* __restric
     for (int off = 16; off >= 1; off >>= 1)
 #pragma unroll
         for (int j = 0; j < off; ++j) ps[j] = __fadd_rn(ps[j], ps[j + off]);
+    // a NaN or infinite K value (or squares past the f32 range): no code exists
+    if (!(ps[0] <= 3.402823466e38f) && err) atomicCAS(err, 0, (int32_t)KVQ_ERR_NONFINITE);
     const float s_rule = __fsqrt_rn(__fdiv_rn(ps[0], 32.0f));
     k_scales[(seq * (p.cap / kG) + gi) * p.D + d] = __half_as_ushort(__float2half_rn(__fmul_rn(p.k_gain, s_rule)));
     const int lane = threadIdx.x & 31;
@@ -96,7 +98,7 @@ __global__ void __launch_bounds__(kMaxD) k2_encode_kernel(const float* __restric
 __global__ void __launch_bounds__(kMaxD) k2_append_kernel(const float* __restrict__ k_new, K2V4Params p,
                                                           int64_t t_old, int64_t n_new,
                                                           uint8_t* __restrict__ k_codes,
-                                                          uint16_t* __restrict__ k_scales) {
+                                                          uint16_t* __restrict__ k_scales, int32_t* err) {
     const int d = threadIdx.x, lane = threadIdx.x & 31;
     const int64_t gi = t_old / kG + blockIdx.x;
     const int h = blockIdx.y, b = blockIdx.z;
@@ -110,6 +112,12 @@ __global__ void __launch_bounds__(kMaxD) k2_append_kernel(const float* __restric
     float x[kG];
 #pragma unroll
     for (int j = 0; j < kG; ++j) x[j] = j < n ? __ldg(col + (int64_t)j * p.D) : 0.0f;
+    {
+        bool bad = false;
+#pragma unroll
+        for (int j = 0; j < kG; ++j) bad |= !(fabsf(x[j]) <= 3.402823466e38f);
+        if (bad && err) atomicCAS(err, 0, (int32_t)KVQ_ERR_NONFINITE);
+    }
     float s_rule;
     if (fresh) {
         float ps[kG];
@@ -175,7 +183,8 @@ __global__ void __launch_bounds__(kMaxD) k2_append_kernel(const float* __restric
 __global__ void __launch_bounds__(kMaxD) v4_encode_kernel(const float* __restrict__ k, const float* __restrict__ v,
                                                           K2V4Params p, int64_t src_cells, int64_t cell0,
                                                           uint8_t* __restrict__ v_blocks,
-                                                          uint16_t* __restrict__ k_win, uint16_t* __restrict__ v_win) {
+                                                          uint16_t* __restrict__ k_win, uint16_t* __restrict__ v_win,
+                                                          int32_t* err) {
     const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
     const int64_t cell = cell0 + blockIdx.x;
     const int g = blockIdx.y, b = blockIdx.z;
@@ -184,6 +193,9 @@ __global__ void __launch_bounds__(kMaxD) v4_encode_kernel(const float* __restric
     const float x = __ldg(v + src);
     const float ax = fabsf(x);
     const float amax = warp_max(ax);
+    // a NaN or infinite V value (a vote: the max above passes over NaNs)
+    if (__any_sync(kFull, !(ax <= 3.402823466e38f)) && lane == 0 && err)
+        atomicCAS(err, 0, (int32_t)KVQ_ERR_NONFINITE);
     float m = 0.0f;
     const unsigned at = __ballot_sync(kFull, ax == amax);
     if (amax > 0.0f) m = __shfl_sync(kFull, x, __ffs(at) - 1);   // first element of largest magnitude
@@ -967,29 +979,31 @@ K2V4Params make_params(const kvq_k2v4_layout& L, int64_t T, int64_t cap) {
 
 cudaError_t launch_k2v4_encode(const kvq_k2v4_layout& L, const float* k, const float* v, int32_t batch,
                                int64_t n_cells, int64_t cap, uint8_t* k_codes, uint16_t* k_scales,
-                               uint8_t* v_blocks, uint16_t* k_win, uint16_t* v_win, cudaStream_t stream) {
+                               uint8_t* v_blocks, uint16_t* k_win, uint16_t* v_win, int32_t* err,
+                               cudaStream_t stream) {
     if (batch == 0 || n_cells == 0) return cudaSuccess;
     const K2V4Params p = make_params(L, n_cells, cap);
-    k2_encode_kernel<<<dim3((unsigned)(n_cells / kG), p.H, batch), p.D, 0, stream>>>(k, p, k_codes, k_scales);
+    k2_encode_kernel<<<dim3((unsigned)(n_cells / kG), p.H, batch), p.D, 0, stream>>>(k, p, k_codes, k_scales, err);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     v4_encode_kernel<<<dim3((unsigned)n_cells, p.H, batch), p.D, 0, stream>>>(k, v, p, n_cells, 0, v_blocks, k_win,
-                                                                              v_win);
+                                                                              v_win, err);
     return cudaGetLastError();
 }
 
 cudaError_t launch_k2v4_append(const kvq_k2v4_layout& L, const float* k_new, const float* v_new, int32_t batch,
                                int64_t n_past, int64_t n_new, int64_t cap, uint8_t* k_codes, uint16_t* k_scales,
-                               uint8_t* v_blocks, uint16_t* k_win, uint16_t* v_win, cudaStream_t stream) {
+                               uint8_t* v_blocks, uint16_t* k_win, uint16_t* v_win, int32_t* err,
+                               cudaStream_t stream) {
     if (batch == 0 || n_new == 0) return cudaSuccess;
     const K2V4Params p = make_params(L, n_past + n_new, cap);   // overlay window at the new length
     const int64_t groups = (n_past + n_new - 1) / kG - n_past / kG + 1;
     k2_append_kernel<<<dim3((unsigned)groups, p.H, batch), p.D, 0, stream>>>(k_new, p, n_past, n_new, k_codes,
-                                                                            k_scales);
+                                                                            k_scales, err);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     v4_encode_kernel<<<dim3((unsigned)n_new, p.H, batch), p.D, 0, stream>>>(k_new, v_new, p, n_new, n_past,
-                                                                            v_blocks, k_win, v_win);
+                                                                            v_blocks, k_win, v_win, err);
     return cudaGetLastError();
 }
 

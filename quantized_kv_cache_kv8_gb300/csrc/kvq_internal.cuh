@@ -237,12 +237,14 @@ cudaError_t launch_attn_tc(kvq_format fmt, const kvq_mla_layout& L, const void* 
 // K2/V4
 cudaError_t launch_k2v4_encode(const kvq_k2v4_layout& L, const float* k, const float* v, int32_t batch,
                                int64_t n_cells, int64_t cap, uint8_t* k_codes, uint16_t* k_scales,
-                               uint8_t* v_blocks, uint16_t* k_win, uint16_t* v_win, cudaStream_t stream);
+                               uint8_t* v_blocks, uint16_t* k_win, uint16_t* v_win, int32_t* err,
+                               cudaStream_t stream);
 // n_new cells per sequence appended at cells n_past .. n_past + n_new - 1
 // (k_new, v_new [batch][Hkv][n_new][D]), with the partial-group scale rule.
 cudaError_t launch_k2v4_append(const kvq_k2v4_layout& L, const float* k_new, const float* v_new, int32_t batch,
                                int64_t n_past, int64_t n_new, int64_t cap, uint8_t* k_codes, uint16_t* k_scales,
-                               uint8_t* v_blocks, uint16_t* k_win, uint16_t* v_win, cudaStream_t stream);
+                               uint8_t* v_blocks, uint16_t* k_win, uint16_t* v_win, int32_t* err,
+                               cudaStream_t stream);
 struct K2V4Plan {
     int64_t chunk;
     int32_t n_chunks;

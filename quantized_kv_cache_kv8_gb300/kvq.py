@@ -122,9 +122,9 @@ def _declare(L):
     L.kvq_timing_read.restype = C.c_int
     L.kvq_timing_read.argtypes = [C.POINTER(C.c_double), C.POINTER(C.c_double), C.POINTER(I32)]
     L.k2v4_encode.restype = C.c_int
-    L.k2v4_encode.argtypes = [pk, P, P, I32, I64, I64, P, P, P, P, P, P]
+    L.k2v4_encode.argtypes = [pk, P, P, I32, I64, I64, P, P, P, P, P, P, P]
     L.k2v4_append.restype = C.c_int
-    L.k2v4_append.argtypes = [pk, P, P, I32, I64, I64, I64, P, P, P, P, P, P]
+    L.k2v4_append.argtypes = [pk, P, P, I32, I64, I64, I64, P, P, P, P, P, P, P]
     L.kv_attn_decode_k2v4_workspace_size.restype = S
     L.kv_attn_decode_k2v4_workspace_size.argtypes = [pk, I32, I32, I64, C.c_int]
     L.kv_attn_decode_k2v4.restype = C.c_int
@@ -391,17 +391,17 @@ def timing_read() -> tuple[float, float, int]:
 # -- K2/V4 -------------------------------------------------------------------
 
 def k2v4_encode(layout: K2V4Layout, k, v, k_codes, k_scales, v_blocks, k_win, v_win, capacity: int | None = None,
-                stream=None):
+                stream=None, err_word=None):
     B, H, T, D = k.shape
     cap = T if capacity is None else capacity
     _ok(lib().k2v4_encode(C.byref(layout), _ptr(k, torch.float32, "k"), _ptr(v, torch.float32, "v"), B, T, cap,
                           _ptr(k_codes, torch.uint8, "k_codes"), _ptr(k_scales, torch.int16, "k_scales"),
                           _ptr(v_blocks, torch.uint8, "v_blocks"), _ptr(k_win, torch.int16, "k_win"),
-                          _ptr(v_win, torch.int16, "v_win"), _stream(stream)), "k2v4_encode")
+                          _ptr(v_win, torch.int16, "v_win"), _err_ptr(err_word), _stream(stream)), "k2v4_encode")
 
 
 def k2v4_append(layout: K2V4Layout, k_new, v_new, n_past: int, k_codes, k_scales, v_blocks, k_win, v_win,
-                stream=None):
+                stream=None, err_word=None):
     """Append k_new, v_new ([B, Hkv, n_new, D] f32) at cells n_past .. n_past + n_new - 1 of every
     sequence; the pools' capacity is their cell dimension."""
     B, H, n_new, D = k_new.shape
@@ -409,7 +409,8 @@ def k2v4_append(layout: K2V4Layout, k_new, v_new, n_past: int, k_codes, k_scales
     _ok(lib().k2v4_append(C.byref(layout), _ptr(k_new, torch.float32, "k_new"), _ptr(v_new, torch.float32, "v_new"),
                           B, n_past, n_new, cap, _ptr(k_codes, torch.uint8, "k_codes"),
                           _ptr(k_scales, torch.int16, "k_scales"), _ptr(v_blocks, torch.uint8, "v_blocks"),
-                          _ptr(k_win, torch.int16, "k_win"), _ptr(v_win, torch.int16, "v_win"), _stream(stream)),
+                          _ptr(k_win, torch.int16, "k_win"), _ptr(v_win, torch.int16, "v_win"), _err_ptr(err_word),
+                          _stream(stream)),
         "k2v4_append")
 
 

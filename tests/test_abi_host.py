@@ -78,7 +78,7 @@ def test_argument_validation(kvq):
     assert kvq.kv_attn_workspace_size(1, 1, 16, 100, layout=odd) == 0
     k2 = kvq.k2v4_layout()
     k2.group = 16
-    assert L.k2v4_encode(C.byref(k2), None, None, 1, 64, 64, None, None, None, None, None, None) == 5
+    assert L.k2v4_encode(C.byref(k2), None, None, 1, 64, 64, None, None, None, None, None, None, None) == 5
 
 
 def test_workspace_sizes_grow_with_work(kvq):
@@ -173,12 +173,12 @@ def test_k2v4_append_validates_before_launch(kvq):
     L = kvq.lib()
     lay = kvq.k2v4_layout()
     d = C.c_void_p(256)
-    assert L.k2v4_append(C.byref(lay), d, d, 1, 60, 10, 64, d, d, d, d, d, None) == 1      # 70 > 64 cells
-    assert L.k2v4_append(C.byref(lay), d, d, 1, -1, 10, 64, d, d, d, d, d, None) == 1
-    assert L.k2v4_append(C.byref(lay), d, d, 1, 0, 10, 40, d, d, d, d, d, None) == 5       # capacity 40
-    assert L.k2v4_append(C.byref(lay), None, d, 1, 0, 10, 64, d, d, d, d, d, None) == 1
-    assert L.k2v4_append(C.byref(lay), d, d, 1, 0, 10, 64, d, d, d, None, d, None) == 1  # overlay pools
-    assert L.k2v4_append(C.byref(lay), None, None, 1, 5, 0, 64, None, None, None, None, None, None) == 0
+    assert L.k2v4_append(C.byref(lay), d, d, 1, 60, 10, 64, d, d, d, d, d, None, None) == 1      # 70 > 64 cells
+    assert L.k2v4_append(C.byref(lay), d, d, 1, -1, 10, 64, d, d, d, d, d, None, None) == 1
+    assert L.k2v4_append(C.byref(lay), d, d, 1, 0, 10, 40, d, d, d, d, d, None, None) == 5       # capacity 40
+    assert L.k2v4_append(C.byref(lay), None, d, 1, 0, 10, 64, d, d, d, d, d, None, None) == 1
+    assert L.k2v4_append(C.byref(lay), d, d, 1, 0, 10, 64, d, d, d, None, d, None, None) == 1  # overlay pools
+    assert L.k2v4_append(C.byref(lay), None, None, 1, 5, 0, 64, None, None, None, None, None, None, None) == 0
 
 
 def test_k2v4_decode_refuses_unaligned_pools(kvq):

@@ -148,3 +148,48 @@ def test_a_wait_that_runs_out_reports_timeout_and_the_next_call_runs(kvq, oracle
         for i, h in enumerate(heads):
             assert rel_err(got[b, h], ref[i]) <= TENSOR_TOL, (b, h)
 
+
+
+def test_k2v4_producers_flag_non_finite_values(kvq, oracle):
+    """The K2/V4 encoder and append report a NaN in K or an infinity in V through
+    the error word; a sequence without one is encoded exactly as the oracle
+    encodes it; clean calls leave the word at 0."""
+    B, H, T, D = 2, 2, 64, 128
+    layout = kvq.k2v4_layout(H, D, 1.10, 4, 16, 16)
+    OL = oracle.k2v4_layout(H, D, 1.10, 4, 16, 16)
+    k, v = synth.gqa_kv(71, B, H, T, D)
+    slots = 4 + 16 + 16
+
+    def pools():
+        return (torch.zeros((B, H, T, D // 4), dtype=torch.uint8, device="cuda"),
+                torch.zeros((B, H, T // 32, D), dtype=torch.int16, device="cuda"),
+                torch.zeros((B, H, T, D // 32, 18), dtype=torch.uint8, device="cuda"),
+                torch.zeros((B, H, slots, D), dtype=torch.int16, device="cuda"),
+                torch.zeros((B, H, slots, D), dtype=torch.int16, device="cuda"))
+    for case in ("k_nan", "v_inf", "v_nan"):
+        kb, vb = k.copy(), v.copy()
+        if case == "k_nan":
+            kb[1, 0, 40, 7] = np.nan
+        elif case == "v_inf":
+            vb[1, 1, 50, 3] = np.inf
+        else:
+            vb[1, 0, 20, 100] = np.nan
+        err = torch.zeros(1, dtype=torch.int32, device="cuda")
+        enc = pools()
+        kvq.k2v4_encode(layout, to_dev(kb), to_dev(vb), *enc, err_word=err)
+        torch.cuda.synchronize()
+        assert int(err.item()) == NONFINITE
+        oenc = oracle.k2v4_encode(k[0], v[0], OL)
+        for g, o in zip(enc, oenc):
+            np.testing.assert_array_equal(g[0].cpu().numpy().view(o.dtype), o)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    enc = pools()
+    kvq.k2v4_encode(layout, to_dev(k), to_dev(v), *enc, err_word=err)
+    k_new, v_new = synth.gqa_kv(72, B, H, 8, D)
+    kvq.k2v4_append(layout, to_dev(k_new), to_dev(v_new), 32, *enc, err_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    k_new[0, 1, 3, 9] = np.inf
+    kvq.k2v4_append(layout, to_dev(k_new), to_dev(v_new), 40, *enc, err_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == NONFINITE
