@@ -15,8 +15,9 @@
 // dequantized to f16 in shared memory and both products run as tcgen05 MMAs
 // with the cells on M: S^T = K Q^T (N = 16: the query heads as f16 and as
 // their f16 residuals) and O^T += V^T P^T (N = 16, heads past the group are
-// zero).  Both paths write the same chunk partials; a merge kernel combines
-// them by log-sum-exp.
+// zero).  A CTA runs two such pipelines, each on its own chunk.  Both paths
+// write the same chunk partials; a merge kernel combines them by
+// log-sum-exp.
 #include "tc_common.cuh"
 
 #include <algorithm>
@@ -402,53 +403,62 @@ __global__ void __launch_bounds__(kNT) k2v4_partial_kernel(K2V4DecodeParams p) {
     }
 }
 
-// One pass over the chunk partials of (sequence, query head), 8 chunks at a
-// time with their loads in flight together, combined by an online
-// log-sum-exp; launched as a programmatic dependent of the partial kernel.
-__global__ void __launch_bounds__(256) k2v4_merge_kernel(K2V4DecodeParams p, float* __restrict__ out) {
+// Combines the chunk partials of (sequence, query head) by log-sum-exp;
+// launched as a programmatic dependent of the partial kernel.  The chunk
+// weights exp(m_c - M) and the total L = sum_c w_c l_c are formed once, in
+// shared memory; then 1024 threads take the D dims 1024 / D ways over the
+// chunks, each with its loads in flight together, and one shared-memory pass
+// adds the ways.
+constexpr int kMergeThreads = 1024;
+__global__ void __launch_bounds__(kMergeThreads) k2v4_merge_kernel(K2V4DecodeParams p, float* __restrict__ out) {
     grid_dependency_wait();
-    const int hq = blockIdx.x, b = blockIdx.y;
-    const int D = p.c.D;
-    const int64_t base = ((int64_t)b * p.Hq + hq) * p.n_chunks;
-    constexpr int kBatch = 8;
-    for (int d = threadIdx.x; d < D; d += blockDim.x) {
-        float M = -INFINITY, L = 0.0f, acc = 0.0f;
-        for (int c0 = 0; c0 < p.n_chunks; c0 += kBatch) {
-            float mv[kBatch], lw[kBatch], ov[kBatch];
+    extern __shared__ float smw[];   // [n_chunks] weights
+    __shared__ float red[kMergeThreads];
+    __shared__ float wred[32];
+    const int hq = blockIdx.x, b = blockIdx.y, t = threadIdx.x, lane = t & 31, warp = t >> 5;
+    const int D = p.c.D, n = p.n_chunks;
+    const int64_t base = ((int64_t)b * p.Hq + hq) * n;
+    float mloc = -INFINITY;
+    for (int c = t; c < n; c += kMergeThreads) mloc = fmaxf(mloc, p.ws_ml[(base + c) * 2]);
+    mloc = warp_max(mloc);
+    if (lane == 0) wred[warp] = mloc;
+    __syncthreads();
+    float M = -INFINITY;
+    for (int i = 0; i < kMergeThreads / 32; ++i) M = fmaxf(M, wred[i]);
+    float lloc = 0.0f;
+    for (int c = t; c < n; c += kMergeThreads) {
+        const float2 ml = *reinterpret_cast<const float2*>(p.ws_ml + (base + c) * 2);
+        const float w = ml.x == -INFINITY ? 0.0f : expf(ml.x - M);
+        smw[c] = w;
+        lloc = fmaf(w, ml.y, lloc);
+    }
 #pragma unroll
-            for (int k = 0; k < kBatch; ++k) {
-                mv[k] = -INFINITY;
-                lw[k] = ov[k] = 0.0f;
-                if (c0 + k < p.n_chunks) {
-                    const float2 ml = *reinterpret_cast<const float2*>(p.ws_ml + (base + c0 + k) * 2);
-                    mv[k] = ml.x;
-                    lw[k] = ml.y;
-                    ov[k] = p.ws_o[(base + c0 + k) * D + d];
-                }
-            }
-            float mb = M;
-#pragma unroll
-            for (int k = 0; k < kBatch; ++k) mb = fmaxf(mb, mv[k]);
-            if (mb == -INFINITY) continue;
-            const float keep = M == -INFINITY ? 0.0f : expf(M - mb);
-            L *= keep;
-            acc *= keep;
-#pragma unroll
-            for (int k = 0; k < kBatch; ++k) {
-                const float w = mv[k] == -INFINITY ? 0.0f : expf(mv[k] - mb);
-                L = fmaf(w, lw[k], L);
-                acc = fmaf(w, ov[k], acc);
-            }
-            M = mb;
-        }
-        out[((int64_t)b * p.Hq + hq) * D + d] = L > 0.0f ? acc / L : 0.0f;
+    for (int o = 16; o >= 1; o >>= 1) lloc += __shfl_xor_sync(0xffffffffu, lloc, o);
+    __syncthreads();   // every warp has read wred; the weights are stored
+    if (lane == 0) wred[warp] = lloc;
+    __syncthreads();
+    float L = 0.0f;
+    for (int i = 0; i < kMergeThreads / 32; ++i) L += wred[i];
+    const int ways = kMergeThreads / D, d = t % D, way = t / D;
+    float acc = 0.0f;
+    if (way < ways) {
+#pragma unroll 16
+        for (int c = way; c < n; c += ways) acc = fmaf(smw[c], p.ws_o[(base + c) * D + d], acc);
+    }
+    red[t] = acc;
+    __syncthreads();
+    if (t < D) {
+        float sum = 0.0f;
+        for (int k = 0; k < ways; ++k) sum += red[k * D + t];
+        out[((int64_t)b * p.Hq + hq) * D + t] = L > 0.0f ? sum / L : 0.0f;
     }
 }
 
 cudaError_t launch_k2v4_merge(const K2V4DecodeParams& p, float* out, cudaStream_t stream) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)p.Hq, (unsigned)p.batch);
-    cfg.blockDim = dim3(256);
+    cfg.blockDim = dim3(kMergeThreads);
+    cfg.dynamicSmemBytes = (size_t)p.n_chunks * sizeof(float);
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -473,21 +483,28 @@ constexpr uint32_t kChunkT = kRowsT * 128;   // 128 cells x 64 dims f16, 128-byt
 template <int D>
 struct SmemT {
     static constexpr int kChunks = D / 64;
+    // one f16 operand region: K for the score, then (once the score MMAs have
+    // read it) V for the context; at about 105 KB in all for D = 256, two
+    // pipelines share a CTA (and an SM), each one's serial steps hiding
+    // behind the other's
     static constexpr uint32_t kOffK = 0;
-    static constexpr uint32_t kOffV = kOffK + kChunks * kChunkT;
-    static constexpr uint32_t kOffQ = kOffV + kChunks * kChunkT;     // kChunks x (16 rows x 128 B)
+    static constexpr uint32_t kOffV = kOffK;
+    static constexpr uint32_t kOffQ = kOffK + kChunks * kChunkT;     // kChunks x (16 rows x 128 B)
     static constexpr uint32_t kOffP = kOffQ + kChunks * kNq * 128;    // 2 x (16 rows x 128 B): P^T by 64 cells
     static constexpr uint32_t kOffRed = kOffP + 2 * kNq * 128;        // [4 warps][8] max, [4][8] sums
     static constexpr uint32_t kOffState = kOffRed + 2 * 4 * 8 * 4;    // running max, sum, qmax (8 each), levels (4)
     static constexpr uint32_t kOffBar = kOffState + 3 * 8 * 4 + 16;
     static constexpr uint32_t kOffMisc = kOffBar + 4 * 8;             // abort flag, TMEM base
-    // raw bytes of a tile, double-buffered: K codes (128 x D/4), the 4 groups'
-    // K scales (4 x D fp16), V blocks (128 x D/32 x 18)
+    // raw bytes of a tile: K codes (128 x D/4) and the 4 groups' K scales
+    // (4 x D fp16) in one buffer, V blocks (128 x D/32 x 18) in another, each
+    // refilled for the next tile as soon as its own dequantization is done
     static constexpr uint32_t kRawKc = kRowsT * D / 4, kRawKs = 4 * 2 * D, kRawVb = kRowsT * (D / 32) * 18;
-    static constexpr uint32_t kRawBytes = kRawKc + kRawKs + kRawVb;
-    static constexpr uint32_t kOffRaw = (kOffMisc + 16 + 127) / 128 * 128;
-    static constexpr uint32_t kBytes = kOffRaw + 2 * kRawBytes;
+    static constexpr uint32_t kOffRawK = (kOffMisc + 16 + 127) / 128 * 128;
+    static constexpr uint32_t kOffRawV = kOffRawK + kRawKc + kRawKs;
+    static constexpr uint32_t kBytes = kOffRawV + kRawVb;
+    static constexpr uint32_t kStride = (kBytes + 1023) / 1024 * 1024;   // one pipeline's region
 };
+static_assert(2 * SmemT<256>::kStride <= 232448, "two pipelines per CTA");
 
 constexpr uint32_t kColS = 0, kColO = 32, kTmemColsT = 64;
 constexpr uint32_t kIdescK2Score = idesc_f16(128, kNq, false, false);
@@ -516,38 +533,55 @@ __device__ __forceinline__ uint32_t q4_pair(uint32_t codes2, uint32_t d2) {
 }
 
 // Stages the raw bytes of the tile at cells [t0, t0 + nt), rounded up to
-// whole 32-cell groups (t0 a multiple of 32), into `dst`: one thread issues
-// three bulk copies (the TMA engine, no per-thread copy instructions) of the
-// K codes, K scales and V blocks, each contiguous in the cache, completing on
-// the buffer's mbarrier.  A sequence may end inside its last group (after
-// appends); the cells past its end lie inside the pool (capacities are
-// multiples of 32, every size and source offset a multiple of 16 bytes) and
-// are masked by the caller.
-template <int D>
+// whole 32-cell groups (t0 a multiple of 32): the K codes and K scales (two
+// bulk copies into the K buffer) or the V blocks (one into the V buffer), each
+// contiguous in the cache, issued by one thread on the TMA engine and
+// completing on the buffer's mbarrier.  A sequence may end inside its last
+// group (after appends); the cells past its end lie inside the pool
+// (capacities are multiples of 32, every size and source offset a multiple of
+// 16 bytes) and are masked by the caller.
+template <int D, bool V>
 __device__ __forceinline__ void stage_tile(const K2V4DecodeParams& p, int64_t seq, int64_t t0, int nt,
                                            unsigned char* dst, uint64_t* bar) {
-    using SM = SmemT<D>;
     const int ns = (nt + kG - 1) / kG * kG;
-    const uint32_t b_kc = ns * (D / 4), b_ks = (ns / kG) * 2 * D, b_vb = ns * (D / 32) * 18;
-    const unsigned char* kc = p.k_codes + (seq * p.c.cap + t0) * (D / 4);
-    const unsigned char* ks = reinterpret_cast<const unsigned char*>(p.k_scales + (seq * (p.c.cap / kG) + t0 / kG) * D);
-    const unsigned char* vb = p.v_blocks + (seq * p.c.cap + t0) * (D / 32) * 18;
     const uint32_t mb = smem_u32(bar);
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(mb), "r"(b_kc + b_ks + b_vb) : "memory");
-    const unsigned char* src[3] = {kc, ks, vb};
-    const uint32_t off[3] = {0u, SM::kRawKc, SM::kRawKc + SM::kRawKs}, bytes[3] = {b_kc, b_ks, b_vb};
-#pragma unroll
-    for (int i = 0; i < 3; ++i)
+    const unsigned char* src[2];
+    uint32_t off[2], bytes[2];
+    int n;
+    if (V) {
+        src[0] = p.v_blocks + (seq * p.c.cap + t0) * (D / 32) * 18;
+        off[0] = 0;
+        bytes[0] = ns * (D / 32) * 18;
+        n = 1;
+    } else {
+        src[0] = p.k_codes + (seq * p.c.cap + t0) * (D / 4);
+        src[1] = reinterpret_cast<const unsigned char*>(p.k_scales + (seq * (p.c.cap / kG) + t0 / kG) * D);
+        off[0] = 0;
+        off[1] = SmemT<D>::kRawKc;
+        bytes[0] = ns * (D / 4);
+        bytes[1] = (ns / kG) * 2 * D;
+        n = 2;
+    }
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(mb),
+                 "r"(n == 1 ? bytes[0] : bytes[0] + bytes[1])
+                 : "memory");
+    for (int i = 0; i < n; ++i)
         asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
                      ::"r"(smem_u32(dst + off[i])), "l"(src[i]), "r"(bytes[i]), "r"(mb)
                      : "memory");
 }
 
+// Named barrier `id` of pipeline `half` (ids 1-3 and 4-6; 0 is the CTA's).
+__device__ __forceinline__ void pipe_bar(int half, int id, int n) {
+    asm volatile("bar.sync %0, %1;" ::"r"(3 * half + id), "r"(n) : "memory");
+}
+
+// One decode pipeline: 256 threads (local `tid`) over chunk `chunk_id` with
+// their own shared-memory region, TMEM columns, mbarriers and named barriers.
 template <int D>
-__global__ void __launch_bounds__(kThreadsT, 1) k2v4_tc_kernel(K2V4DecodeParams p) {
-    launch_dependents();
+__device__ __forceinline__ void k2v4_tc_pipe(const K2V4DecodeParams& p, unsigned char* smem_raw, uint32_t tmem,
+                                             int tid, int half, int chunk_id) {
     using SM = SmemT<D>;
-    extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char* sK = smem_raw + SM::kOffK;
     unsigned char* sV = smem_raw + SM::kOffV;
     unsigned char* sQ = smem_raw + SM::kOffQ;
@@ -558,24 +592,19 @@ __global__ void __launch_bounds__(kThreadsT, 1) k2v4_tc_kernel(K2V4DecodeParams 
     float* sL = sM + 8;
     float* sQmax = sL + 8;
     float* sLv = sQmax + 8;   // the 4 K levels
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem_raw + SM::kOffBar);   // 0 score, 1 context, 2-3 raw buffers
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem_raw + SM::kOffBar);   // 0 score, 1 context, 2 raw K, 3 raw V
     volatile int* sAbort = reinterpret_cast<volatile int*>(smem_raw + SM::kOffMisc);
-    uint32_t* sTmem = reinterpret_cast<uint32_t*>(smem_raw + SM::kOffMisc + 4);
-    unsigned char* sRaw = smem_raw + SM::kOffRaw;   // [2][kRawBytes]
+    unsigned char* sRawK = smem_raw + SM::kOffRawK;
+    unsigned char* sRawV = smem_raw + SM::kOffRawV;
 
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int chunk_id = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+    const int lane = tid & 31, warp = tid >> 5;
+    const int g = blockIdx.y, b = blockIdx.z;
     const int64_t seq = (int64_t)b * p.c.H + g;
     const int64_t c0 = (int64_t)chunk_id * p.chunk;
     const int64_t c1 = min(c0 + p.chunk, p.c.T);
     const int n_tiles = (int)((c1 - c0 + kRowsT - 1) / kRowsT);
     const int grp = p.grp;
 
-    if (warp == 0) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(sTmem)),
-                     "r"(kTmemColsT));
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
-    }
     if (tid == 32) {
         for (int i = 0; i < 4; ++i)
             asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(&bars[i])), "r"(1u));
@@ -583,7 +612,10 @@ __global__ void __launch_bounds__(kThreadsT, 1) k2v4_tc_kernel(K2V4DecodeParams 
         // the swizzled operands need a 1024-byte base (2: refused; a wait that
         // runs out raises the flag to 1)
         *sAbort = smem_u32(smem_raw) & 1023u ? 2 : 0;
-        if (n_tiles > 0) stage_tile<D>(p, seq, c0, (int)min((int64_t)kRowsT, c1 - c0), sRaw, &bars[2]);
+        if (n_tiles > 0) {
+            stage_tile<D, false>(p, seq, c0, (int)min((int64_t)kRowsT, c1 - c0), sRawK, &bars[2]);
+            stage_tile<D, true>(p, seq, c0, (int)min((int64_t)kRowsT, c1 - c0), sRawV, &bars[3]);
+        }
     }
     if (tid < 8) {
         sM[tid] = -INFINITY;
@@ -600,7 +632,7 @@ __global__ void __launch_bounds__(kThreadsT, 1) k2v4_tc_kernel(K2V4DecodeParams 
     for (int i = tid; i < grp * D; i += kThreadsT) qmax = fmaxf(qmax, fabsf(qg[i]));
     qmax = warp_max(qmax);
     if (lane == 0) sQmax[warp] = qmax;
-    __syncthreads();
+    pipe_bar(half, 1, kThreadsT);
     float q_max = 0.0f;
     for (int i = 0; i < 8; ++i) q_max = fmaxf(q_max, sQmax[i]);
     int e_q = 0;
@@ -626,31 +658,29 @@ __global__ void __launch_bounds__(kThreadsT, 1) k2v4_tc_kernel(K2V4DecodeParams 
         *reinterpret_cast<__half*>(chunk + sw128(8 + h, (d & 63) * 2)) = lo;
     }
     tc_before();
-    __syncthreads();
+    pipe_bar(half, 1, kThreadsT);
     tc_after();
-    const uint32_t tmem = *sTmem;
 
     const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
+    // the raw copy of each buffer that its issuing thread (0 for K, 128 for
+    // V) has not yet seen land: copy t is waited for before copy t + 1 is
+    // issued into the same buffer, and one still pending when the loop ends
+    // (after an abort) is waited for before the CTA leaves
+    int pend_k = n_tiles > 0 ? 0 : -1, pend_v = pend_k;
     for (int t = 0; t < n_tiles; ++t) {
         const int64_t t0 = c0 + (int64_t)t * kRowsT;
         const int nt = (int)min((int64_t)kRowsT, c1 - t0);
-        // the next tile's bytes stream in while this one is processed; its
-        // buffer was last read by tile t - 1, whose reads every thread fenced
-        // against the async proxy before the barrier that closed that tile
-        if (tid == 0 && t + 1 < n_tiles)
-            stage_tile<D>(p, seq, t0 + kRowsT, (int)min((int64_t)kRowsT, c1 - t0 - kRowsT),
-                          sRaw + ((t + 1) & 1) * SM::kRawBytes, &bars[2 + ((t + 1) & 1)]);
-        mbar_wait(&bars[2 + (t & 1)], (uint32_t)(t >> 1) & 1u, sAbort, p.wait_limit);
-        const unsigned char* raw = sRaw + (t & 1) * SM::kRawBytes;
-        const unsigned char* raw_kc = raw;
-        const uint16_t* raw_ks = reinterpret_cast<const uint16_t*>(raw + SM::kRawKc);
-        const unsigned char* raw_vb = raw + SM::kRawKc + SM::kRawKs;
+        if (mbar_wait(&bars[2], (uint32_t)t & 1u, sAbort, p.wait_limit) && pend_k == t) pend_k = -1;
+        // the f16 region holds the previous tile's V until its context MMAs
+        // have read it
+        if (t > 0) mbar_wait(&bars[1], (uint32_t)(t - 1) & 1u, sAbort, p.wait_limit);
+        const unsigned char* raw_kc = sRawK;
+        const uint16_t* raw_ks = reinterpret_cast<const uint16_t*>(sRawK + SM::kRawKc);
+        const unsigned char* raw_vb = sRawV;
         // ---- K of the tile to f16 (cells on rows, 64 dims per chunk), all
-        // warps.  sK is free: the previous tile's softmax waited for its score;
-        // the previous context MMAs, which read sV and P^T only, may still run.
-        // A whole tile of bulk cells (no sink or window cell, the usual case)
-        // takes a branch-free loop whose unrolled iterations interleave: with
-        // one CTA of 8 warps per SM little else hides their latency.
+        // warps.  A whole tile of bulk cells (no sink or window cell, the
+        // usual case) takes a branch-free loop whose unrolled iterations
+        // interleave.
         const bool plain = nt == kRowsT && t0 >= p.c.n_sink && t0 + kRowsT <= p.c.T - p.c.n_window;
         // the fp16 scales of dims 32j .. 32j + 31 in the K scale group g
         auto k_scales = [&](int g, int j, uint32_t (&scw)[16]) {
@@ -686,10 +716,14 @@ __global__ void __launch_bounds__(kThreadsT, 1) k2v4_tc_kernel(K2V4DecodeParams 
         };
         if (plain) {
             // warp w takes cells 16w .. 16w + 15 (one scale group) and every
-            // 32-dim slice; a thread keeps one slice, so its scales load once,
-            // and each step covers consecutive cells (conflict-free code loads)
+            // 32-dim slice; a thread keeps one slice, so its scales load once
+            // A 16-byte store is served 8 lanes at a time, and the lanes of
+            // one such phase must cover the 8 swizzled 16-byte units of a
+            // row: lanes 8p .. 8p + 7 take kQ consecutive cells (distinct
+            // swizzle phases) and 8 / kQ slices (the two halves of a chunk
+            // row when kQ = 4), where one cell and 8 slices hit 2 units 4 ways
             constexpr int kS = D / 32, kQ = 32 / kS;
-            const int j = lane % kS, q = lane / kS;
+            const int q = lane % kQ, j = lane / kQ;
             uint32_t scw[16];
             k_scales((16 * warp) / kG, j, scw);
 #pragma unroll
@@ -726,7 +760,7 @@ __global__ void __launch_bounds__(kThreadsT, 1) k2v4_tc_kernel(K2V4DecodeParams 
         }
         fence_async_smem();
         tc_before();
-        __syncthreads();
+        pipe_bar(half, 1, kThreadsT);
         tc_after();
         // ---- score MMAs (issued after the previous context MMAs: its commit
         // covers both) ----
@@ -740,10 +774,17 @@ __global__ void __launch_bounds__(kThreadsT, 1) k2v4_tc_kernel(K2V4DecodeParams 
                              kIdescK2Score, (c | ks) ? 1u : 0u);
             umma_commit(&bars[0]);
         }
+        // the raw K buffer is free (every thread fenced its reads before the
+        // barrier): the next tile's K streams in during this one
+        if (tid == 0 && pend_k < 0 && t + 1 < n_tiles && !*sAbort) {
+            stage_tile<D, false>(p, seq, t0 + kRowsT, (int)min((int64_t)kRowsT, c1 - t0 - kRowsT), sRawK, &bars[2]);
+            pend_k = t + 1;
+        }
         if (warp >= 4) {
-            // ---- V of the tile to f16, warps 4-7, overlapping the score MMAs
-            // and the softmax, once the previous context MMAs released sV ----
-            if (t > 0) mbar_wait(&bars[1], (uint32_t)(t - 1) & 1u, sAbort, p.wait_limit);
+            // ---- V of the tile to f16, warps 4-7, alongside the softmax, once
+            // the score MMAs have read K out of the shared f16 region ----
+            mbar_wait(&bars[0], (uint32_t)t & 1u, sAbort, p.wait_limit);
+            if (mbar_wait(&bars[3], (uint32_t)t & 1u, sAbort, p.wait_limit) && pend_v == t) pend_v = -1;
             auto v_bulk = [&](int r, int j, uint32_t (&vw)[16]) {
                 // q4_0 block (d, then 16 bytes: element e in the low nibble of
                 // byte e, e + 16 in the high nibble)
@@ -808,7 +849,10 @@ __global__ void __launch_bounds__(kThreadsT, 1) k2v4_tc_kernel(K2V4DecodeParams 
             if (plain) {
 #pragma unroll
                 for (int it = tid - 128; it < kRowsT * (D / 128); it += kThreadsT - 128) {
-                    const int r = it / (D / 128), u = it - r * (D / 128);   // cell, run of 4 blocks
+                    // cell and run of 4 blocks: each 8-lane store phase takes 8
+                    // consecutive cells (8 distinct swizzle phases) of one run
+                    const int r = D == 256 ? (it & 7) + 8 * (it >> 4) : it;
+                    const int u = D == 256 ? (it >> 3) & 1 : 0;
                     v_quad(r, u, [&](int j, const uint32_t (&vw)[16]) { v_store(r, j, vw); });
                 }
             } else {
@@ -835,6 +879,14 @@ __global__ void __launch_bounds__(kThreadsT, 1) k2v4_tc_kernel(K2V4DecodeParams 
                     v_store(r, j, vw);
                 }
             }
+            // the raw V buffer is free once warps 4-7 have fenced their reads
+            fence_async_smem();
+            pipe_bar(half, 3, 128);
+            if (tid == 128 && pend_v < 0 && t + 1 < n_tiles && !*sAbort) {
+                stage_tile<D, true>(p, seq, t0 + kRowsT, (int)min((int64_t)kRowsT, c1 - t0 - kRowsT), sRawV,
+                                    &bars[3]);
+                pend_v = t + 1;
+            }
         } else {
             // ---- softmax: warps 0-3, thread = cell (TMEM lane), the group's
             // heads.  The score commit covers the previous context MMAs too, so
@@ -856,7 +908,7 @@ __global__ void __launch_bounds__(kThreadsT, 1) k2v4_tc_kernel(K2V4DecodeParams 
                 const float m = warp_max(z[h]);
                 if (lane == 0) sRedM[warp * 8 + h] = m;
             }
-            asm volatile("bar.sync 2, 128;" ::: "memory");
+            pipe_bar(half, 2, 128);
             float mnew[8], alpha[8], pv[8];
 #pragma unroll
             for (int h = 0; h < 8; ++h) {
@@ -888,7 +940,7 @@ __global__ void __launch_bounds__(kThreadsT, 1) k2v4_tc_kernel(K2V4DecodeParams 
                 }
                 tmem_wait_st();
             }
-            asm volatile("bar.sync 2, 128;" ::: "memory");
+            pipe_bar(half, 2, 128);
             if (tid < 8) {
                 float a = 0.0f, mn = 0.0f;
 #pragma unroll
@@ -903,7 +955,7 @@ __global__ void __launch_bounds__(kThreadsT, 1) k2v4_tc_kernel(K2V4DecodeParams 
         }
         fence_async_smem();
         tc_before();
-        __syncthreads();
+        pipe_bar(half, 1, kThreadsT);
         tc_after();
         // ---- context MMAs ----
         if (tid == 0 && !*sAbort) {
@@ -921,11 +973,10 @@ __global__ void __launch_bounds__(kThreadsT, 1) k2v4_tc_kernel(K2V4DecodeParams 
     if (n_tiles > 0) {
         volatile int never = 0;
         if (!mbar_wait(&bars[1], (uint32_t)(n_tiles - 1) & 1u, &never)) *sAbort = 1;
-        // after an abort the loop stopped waiting for its raw tiles: the
-        // bulk copies still in flight land before the CTA leaves
-        if (tid == 0)
-            for (int t = max(0, n_tiles - 2); t < n_tiles; ++t)
-                if (!mbar_wait(&bars[2 + (t & 1)], (uint32_t)(t >> 1) & 1u, &never)) *sAbort = 1;
+        // after an abort the loop stopped waiting for its raw tiles: a bulk
+        // copy still in flight lands before the CTA leaves
+        if (tid == 0 && pend_k >= 0 && !mbar_wait(&bars[2], (uint32_t)pend_k & 1u, &never)) *sAbort = 1;
+        if (tid == 128 && pend_v >= 0 && !mbar_wait(&bars[3], (uint32_t)pend_v & 1u, &never)) *sAbort = 1;
     }
     tc_after();
     if (*sAbort) {
@@ -950,10 +1001,36 @@ __global__ void __launch_bounds__(kThreadsT, 1) k2v4_tc_kernel(K2V4DecodeParams 
             p.ws_ml[slot * 2 + 1] = sL[tid];
         }
     }
+}
+
+// Two pipelines per CTA, each on its own chunk: a kernel that allocates TMEM
+// runs one CTA per SM, and one pipeline's serial steps (dequantization, MMA
+// waits, softmax) leave most of the SM idle; the second fills it.
+template <int D>
+__global__ void __launch_bounds__(2 * kThreadsT, 1) k2v4_tc_kernel(K2V4DecodeParams p) {
+    launch_dependents();
+    extern __shared__ __align__(1024) unsigned char smem_all[];
+    const int half = threadIdx.x / kThreadsT;
+    // the TMEM base goes to a word of pipeline 0's region that it never uses
+    uint32_t* slot = reinterpret_cast<uint32_t*>(smem_all + SmemT<D>::kOffMisc + 4);
+    if (threadIdx.x < 32) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(slot)),
+                     "r"(2 * kTmemColsT));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
     tc_before();
     __syncthreads();
     tc_after();
-    if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemColsT));
+    const uint32_t base = *slot;
+    const int chunk_id = 2 * (int)blockIdx.x + half;
+    if (chunk_id < p.n_chunks)
+        k2v4_tc_pipe<D>(p, smem_all + half * SmemT<D>::kStride, base + half * kTmemColsT, (int)threadIdx.x % kThreadsT,
+                        half, chunk_id);
+    tc_before();
+    __syncthreads();
+    tc_after();
+    if (threadIdx.x < 32)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(base), "r"(2 * kTmemColsT));
 }
 
 K2V4Params make_params(const kvq_k2v4_layout& L, int64_t T, int64_t cap) {
@@ -1013,9 +1090,10 @@ K2V4Plan plan_k2v4(const kvq_k2v4_layout& L, int32_t batch, int32_t, int64_t n_c
     K2V4Plan pl{};
     pl.tensor = tensor;
     if (tensor) {
-        // about one CTA per SM, chunks of whole 128-cell tiles
+        // about one CTA (two pipelines, a chunk each) per SM, chunks of whole
+        // 128-cell tiles
         const int64_t per = std::max<int64_t>(1, (int64_t)batch * L.n_kv_heads);
-        const int64_t target = std::max<int64_t>(1, (int64_t)kSmSMs / per);
+        const int64_t target = std::max<int64_t>(1, (int64_t)kSmSMs * 2 / per);
         int64_t chunk = (std::max<int64_t>(n_cells, 1) + target - 1) / target;
         chunk = std::max<int64_t>(kRowsT, (chunk + kRowsT - 1) / kRowsT * kRowsT);
         pl.chunk = chunk;
@@ -1068,9 +1146,10 @@ cudaError_t launch_k2v4_decode(const kvq_k2v4_layout& L, const float* q, int32_t
 #define KVQ_TC_CASE(DD)                                                                                 \
     case DD: {                                                                                          \
         e = cudaFuncSetAttribute(k2v4_tc_kernel<DD>, cudaFuncAttributeMaxDynamicSharedMemorySize,      \
-                                 (int)SmemT<DD>::kBytes);                                              \
+                                 (int)(2 * SmemT<DD>::kStride));                                       \
         if (e != cudaSuccess) return e;                                                                 \
-        k2v4_tc_kernel<DD><<<grid, kThreadsT, SmemT<DD>::kBytes, stream>>>(p);                         \
+        k2v4_tc_kernel<DD><<<dim3((plan.n_chunks + 1) / 2, L.n_kv_heads, batch), 2 * kThreadsT,        \
+                             2 * SmemT<DD>::kStride, stream>>>(p);                                      \
         break;                                                                                          \
     }
             KVQ_TC_CASE(128)
