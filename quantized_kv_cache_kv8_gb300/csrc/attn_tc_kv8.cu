@@ -29,8 +29,8 @@
 // score MMAs of tile t+1 follow the decode group by group.
 //
 // Loads are laid out so that each warp instruction reads whole rows: in groups
-// A and B a half-warp reads the 256 contiguous bytes of one row (2 rows per
-// instruction, 4 cache lines), in group C 8 rows of 64 bytes.
+// A and B the 256 contiguous bytes of two rows (lanes alternate between them
+// in fours), in group C 8 rows of 64 bytes.
 //
 // Reductions over the 128 rows of a tile (column max in the softmax's exact
 // path, the row sums at the end) run as a 31-shuffle transpose-reduce within
@@ -115,9 +115,13 @@ constexpr uint32_t kIdescScore = idesc_f16(128, kHC, false, false);
 constexpr uint32_t kIdescCtx = idesc_f16(128, kHC, true, true);
 
 // A worker's raw share of a tile.  Groups A and B: 8 pieces of 16 bytes, piece
-// i at row 2 (warp + 8 i) + lane / 16, bytes 16 (lane % 16) of the group's 256
-// (so the thread always serves chunk 4 g + (lane % 16) / 4, 16 dims at
-// 16 (lane % 4)).  Group C: 2 pieces, piece i at row (tid + 256 i) / 4, bytes
+// i at row 2 (warp + 8 i) + (lane / 4) % 2, bytes 64 (lane / 8) + 16 (lane % 4)
+// of the group's 256 (so the thread always serves chunk 4 g + lane / 8, 16
+// dims at 16 (lane % 4)).  A 16-byte shared-memory store is served 8 lanes at
+// a time: lanes 8p .. 8p + 3 and 8p + 4 .. 8p + 7 write the same chunk of two
+// adjacent rows, whose 128-byte swizzle phases differ in their low bit, so the
+// 8 lanes cover 8 distinct 16-byte units (one row across two chunks hit 4
+// units twice).  Group C: 2 pieces, piece i at row (tid + 256 i) / 4, bytes
 // 16 (tid % 4) of the rope chunk.
 struct RawGroup {
     uint4 v[8];
@@ -145,8 +149,9 @@ __device__ __forceinline__ void load_group(RawGroup& r, const uint8_t* __restric
                                            const int64_t* prow) {
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-        const int row = 2 * (warp + 8 * i) + (lane >> 4);
-        r.v[i] = row < nt ? load16<APPEND>(codes, pool_row<GATHER>(t0, row, prow), 256 * g + 16 * (lane & 15), rn, snew)
+        const int row = 2 * (warp + 8 * i) + ((lane >> 2) & 1);
+        r.v[i] = row < nt ? load16<APPEND>(codes, pool_row<GATHER>(t0, row, prow),
+                                           256 * g + 64 * (lane >> 3) + 16 * (lane & 3), rn, snew)
                           : make_uint4(0u, 0u, 0u, 0u);
     }
 }
@@ -560,7 +565,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kv8_kernel(AttnParams p) 
         // ---- decode the tile: groups A (chunks 0-3), B (4-7), C (rope) ----
         const uint32_t prev = (uint32_t)(t - 1) & 1u;
         {
-            const int q4 = lane & 3, cg = (lane & 15) >> 2;
+            const int q4 = lane & 3, cg = lane >> 3;
 #pragma unroll
             for (int g = 0; g < 2; ++g) {
                 if (t > 0) {
@@ -570,7 +575,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kv8_kernel(AttnParams p) 
                 unsigned char* slot = sSlot + (4 * g + cg) * kSlotBytes;
 #pragma unroll
                 for (int i = 0; i < 8; ++i)
-                    store16(slot, g == 0 ? rawA.v[i] : rawB.v[i], 2 * (warp + 8 * i) + (lane >> 4), 32 * q4);
+                    store16(slot, g == 0 ? rawA.v[i] : rawB.v[i], 2 * (warp + 8 * i) + ((lane >> 2) & 1), 32 * q4);
                 fence_async_smem();
                 mbar_arrive(&bars[kBarFull0 + g]);
             }

@@ -87,10 +87,14 @@ constexpr uint32_t kIdescScore = idesc_f16(128, 2 * kHC, false, false);
 constexpr uint32_t kIdescCtx = idesc_f16(128, kHC, true, false);
 
 // A worker's raw share of a tile.  Groups A and B (code bytes 128 g .. + 127):
-// 4 pieces, piece i at row 4 (warp + 8 i) + lane / 8, bytes 16 (lane % 8) of
-// the group -- chunk 4 g + (lane % 8) / 2, dims 32 (lane % 2) of it.  Group C
-// (the rope chunk, bytes 256..287): 1 piece at row 16 warp + lane / 2, bytes
-// 16 (lane % 2).
+// 4 pieces, piece i at row 4 (warp + 8 i) + (lane / 2) % 4, bytes
+// 32 (lane / 8) + 16 (lane % 2) of the group -- chunk 4 g + lane / 8, dims
+// 32 (lane % 2) of it.  A 16-byte shared-memory store is served 8 lanes at a
+// time: lanes 8p .. 8p + 7 write 4 rows x 2 halves of one chunk, and 4
+// consecutive rows' 128-byte swizzle phases map a half's units {i, 4 + i} onto
+// 8 distinct 16-byte units (one row across four chunks hit 2 units 4 ways).
+// Group C (the rope chunk, bytes 256..287): 1 piece at row 16 warp + lane / 2,
+// bytes 16 (lane % 2).
 struct RawGroup {
     uint4 v[4];
 };
@@ -99,8 +103,9 @@ __device__ __forceinline__ void load_group(RawGroup& r, const uint8_t* __restric
                                            int warp, int lane) {
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-        const int row = 4 * (warp + 8 * i) + (lane >> 3);
-        r.v[i] = row < nt ? __ldg(reinterpret_cast<const uint4*>(codes + (t0 + row) * kRowBytes + 128 * g + 16 * (lane & 7)))
+        const int row = 4 * (warp + 8 * i) + ((lane >> 1) & 3);
+        r.v[i] = row < nt ? __ldg(reinterpret_cast<const uint4*>(codes + (t0 + row) * kRowBytes + 128 * g +
+                                                                 32 * (lane >> 3) + 16 * (lane & 1)))
                           : make_uint4(0u, 0u, 0u, 0u);
     }
 }
@@ -574,7 +579,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_tq4_kernel(AttnParams p) 
                          : "=r"(lvb.hi[0]), "=r"(lvb.hi[1]), "=r"(lvb.hi[2]), "=r"(lvb.hi[3])
                          : "r"(smem_u32(sLevels + 16))
                          : "memory");
-            const int half = lane & 1, cg = (lane & 7) >> 1;
+            const int half = lane & 1, cg = lane >> 3;
 #pragma unroll
             for (int g = 0; g < 2; ++g) {
                 if (t > 0) {
@@ -584,7 +589,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_tq4_kernel(AttnParams p) 
                 unsigned char* slot = sSlot + (4 * g + cg) * kSlotBytes;
                 const RawGroup& rg = g == 0 ? rawA : rawB;
 #pragma unroll
-                for (int i = 0; i < 4; ++i) store32(slot, rg.v[i], 4 * (warp + 8 * i) + (lane >> 3), 64 * half, lvb);
+                for (int i = 0; i < 4; ++i)
+                    store32(slot, rg.v[i], 4 * (warp + 8 * i) + ((lane >> 1) & 3), 64 * half, lvb);
                 fence_async_smem();
                 mbar_arrive(&bars[kBarFull0 + g]);
             }
