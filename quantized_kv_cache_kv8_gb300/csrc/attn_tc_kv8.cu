@@ -632,9 +632,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kv8_kernel(AttnParams p) 
         // does a score past m by more than the lag (m = -inf before the first
         // exact path: d = +inf, or NaN on a row past the tile's end, which the
         // valid rows outvote)
-        bool flag = (*sAbort != 0) | (my_sl * emax > kScaleLim);
+        // one maximum over the heads, then one test (fmaxf passes over NaN, as
+        // a comparison per head would)
+        float dmax = z[0];
 #pragma unroll
-        for (int j = 0; j < 32; ++j) flag |= z[j] > kLagLog2;
+        for (int j = 1; j < 32; ++j) dmax = fmaxf(dmax, z[j]);
+        const bool flag = (*sAbort != 0) | (my_sl * emax > kScaleLim) | (dmax > kLagLog2);
         const bool any_flag = worker_any(flag);
         if (GATHER && t + 1 < n_tiles) {
             // the barrier above made the next tile's index table visible

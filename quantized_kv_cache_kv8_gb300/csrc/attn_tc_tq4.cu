@@ -630,9 +630,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_tq4_kernel(AttnParams p) 
         // valid rows outvote)
 #pragma unroll
         for (int j = 0; j < 16; ++j) z[j] -= mreg[j];
-        bool flag = (*sAbort != 0) | (my_sl > s_lim);
+        // one maximum over the heads, then one test (fmaxf passes over NaN, as
+        // a comparison per head would)
+        float dmax = z[0];
 #pragma unroll
-        for (int j = 0; j < 16; ++j) flag |= z[j] > kLagLog2;
+        for (int j = 1; j < 16; ++j) dmax = fmaxf(dmax, z[j]);
+        const bool flag = (*sAbort != 0) | (my_sl > s_lim) | (dmax > kLagLog2);
         if (worker_any(flag)) {
             if (worker_any(*sAbort != 0)) break;
             // exact column maxima of z and of y = z + log2 s_L, new running

@@ -77,6 +77,15 @@ def test_k2v4_half_group_and_tail_tile(kvq, oracle, path):
     run_case(kvq, oracle, B=1, H=2, T=416, D=256, Hq=8, sink=8, window=64, seed=53, path=path)
 
 
+def test_k2v4_tensor_odd_chunk_counts(kvq, oracle):
+    """The tensor kernel runs two chunks per CTA.  320 cells of one kv head
+    make 3 chunks of one tile (the second CTA's second pipeline has no chunk;
+    the last tile holds 64 cells); 40000 cells at head_dim 128 make 157 chunks
+    of two tiles each (every pipeline refills its raw K and V buffers)."""
+    run_case(kvq, oracle, B=1, H=1, T=320, D=256, Hq=8, sink=8, window=32, seed=57, path="tensor")
+    run_case(kvq, oracle, B=1, H=1, T=40000, D=128, Hq=8, sink=8, window=256, seed=58, path="tensor")
+
+
 @pytest.mark.parametrize("path", ["simt", "tensor"])
 def test_k2v4_window_covers_all(kvq, oracle, path):
     """Every cell inside the overlay: output equals attention over fp16 K/V."""
