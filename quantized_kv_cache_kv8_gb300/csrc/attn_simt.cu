@@ -141,9 +141,7 @@ __global__ void __launch_bounds__(kNT, 2) attn_partial_kernel(AttnParams p) {
                 if (r < nt) {
                     const uint32_t u = GATHER ? __ldg(reinterpret_cast<const uint32_t*>(p.codes + prow[r] * kD) + c4 / 4)
                                               : __ldg(src + w);
-                    const float2 a = e4m3x2_to_float2((uint16_t)(u & 0xffffu));
-                    const float2 c = e4m3x2_to_float2((uint16_t)(u >> 16));
-                    f = make_float4(a.x, a.y, c.x, c.y);
+                    f = e4m3x4_to_float4(u);
                 }
                 *reinterpret_cast<float4*>(xs + r * kXS + c4) = f;
             }

@@ -129,10 +129,7 @@ __device__ __forceinline__ void store_chunk(const RawChunk& c, bool valid, unsig
     if (valid) {
         const uint32_t in[8] = {c.a.x, c.a.y, c.a.z, c.a.w, c.b.x, c.b.y, c.b.z, c.b.w};
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            w[2 * i] = e4m3x2_to_half2_bits(in[i] & 0xffffu);
-            w[2 * i + 1] = e4m3x2_to_half2_bits(in[i] >> 16);
-        }
+        for (int i = 0; i < 8; ++i) e4m3x4_to_half2x2(in[i], w[2 * i], w[2 * i + 1]);
     } else {
 #pragma unroll
         for (int i = 0; i < 16; ++i) w[i] = 0u;

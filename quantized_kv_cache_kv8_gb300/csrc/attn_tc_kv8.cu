@@ -171,10 +171,7 @@ __device__ __forceinline__ void store16(unsigned char* slot, const uint4& c, int
     const uint32_t in[4] = {c.x, c.y, c.z, c.w};
     uint32_t w[8];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        w[2 * i] = e4m3x2_to_half2_bits(in[i] & 0xffffu);
-        w[2 * i + 1] = e4m3x2_to_half2_bits(in[i] >> 16);
-    }
+    for (int i = 0; i < 4; ++i) e4m3x4_to_half2x2(in[i], w[2 * i], w[2 * i + 1]);
     *reinterpret_cast<uint4*>(slot + sw128(row, b)) = make_uint4(w[0], w[1], w[2], w[3]);
     *reinterpret_cast<uint4*>(slot + sw128(row, b + 16)) = make_uint4(w[4], w[5], w[6], w[7]);
 }

@@ -128,11 +128,24 @@ __device__ __forceinline__ int code16(float u, const float* th) {
     return c;
 }
 
-// e4m3 byte -> f32 (exact).  The NaN pattern S.1111.111 is never stored by the
-// encoder; it would read back as NaN here.
-__device__ __forceinline__ float2 e4m3x2_to_float2(uint16_t two) {
-    __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)two, __NV_E4M3);
-    return __half22float2(*reinterpret_cast<__half2*>(&h));
+// 4 e4m3 codes (one word, code k in byte k) -> their f16 values (exact) as two
+// f16x2 words (codes 0, 1 and 2, 3): each 16-bit half of the word feeds one
+// pair conversion in place, with no unpacking or repacking around it.  The
+// NaN pattern S.1111.111 is never stored by the encoder; it would read back
+// as NaN.
+__device__ __forceinline__ void e4m3x4_to_half2x2(uint32_t in, uint32_t& w0, uint32_t& w1) {
+    asm("{\n .reg .b16 lo, hi;\n mov.b32 {lo, hi}, %2;\n"
+        " cvt.rn.f16x2.e4m3x2 %0, lo;\n cvt.rn.f16x2.e4m3x2 %1, hi;\n}\n"
+        : "=r"(w0), "=r"(w1)
+        : "r"(in));
+}
+// The same 4 codes as f32 (exact).
+__device__ __forceinline__ float4 e4m3x4_to_float4(uint32_t in) {
+    uint32_t w0, w1;
+    e4m3x4_to_half2x2(in, w0, w1);
+    const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&w0));
+    const float2 c = __half22float2(*reinterpret_cast<const __half2*>(&w1));
+    return make_float4(a.x, a.y, c.x, c.y);
 }
 
 // Warp-held radix-2 FWHT of an n-point block (n a power of two, 2..1024).

@@ -165,10 +165,6 @@ static __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t 
 static __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 static __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
-static __device__ __forceinline__ uint32_t e4m3x2_to_half2_bits(uint32_t two) {
-    __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)two, __NV_E4M3);
-    return (uint32_t)h.x | ((uint32_t)h.y << 16);
-}
 
 
 // 2^x on the SFU (ex2.approx, relative error about 2^-22; 2^-inf = 0).
