@@ -100,10 +100,12 @@ DEFAULT_WORKLOADS = ["kv8_ragged", "tq4_ragged", "kv8_prefill", "tq4_prefill", "
 # profile summaries holding the ncu DRAM traffic of a dominant kernel, keyed by workload
 PROFILE_FOR = {"kv8_ragged": "decode_tc_kv8_ragged_b32_h128.md", "tq4_ragged": "decode_tc_tq4_ragged_b32_h128.md",
                "kv8_prefill": "prefill_tc_kv8_p126976_n2048_h128.md",
-               "tq4_prefill": "prefill_tc_tq4_p126976_n2048_h128.md"}
+               "tq4_prefill": "prefill_tc_tq4_p126976_n2048_h128.md",
+               "k2v4_4x32768": "decode_tc_k2v4_b4_t32768.md"}
 # the sources whose hash a traffic figure is tied to (the kernel changed => no figure)
-KERNEL_SOURCES = {1: ["attn_tc_kv8.cu", "tc_common.cuh", "attn_common.cuh"],
-                  2: ["attn_tc_tq4.cu", "tc_common.cuh", "attn_common.cuh"]}
+KERNEL_SOURCES = {1: ["attn_tc_kv8.cu", "tc_common.cuh", "attn_common.cuh", "kvq_internal.cuh"],
+                  2: ["attn_tc_tq4.cu", "tc_common.cuh", "attn_common.cuh", "kvq_internal.cuh"],
+                  "k2v4": ["k2v4.cu", "tc_common.cuh", "attn_common.cuh", "kvq_internal.cuh"]}
 
 
 def load_peaks():
@@ -485,6 +487,7 @@ def run_k2v4(ctx, workload, K, W, peaks, sampler, world, dist):
     step_ms, part_ms, merge_ms = max_over_ranks([step_ms, part_ms, merge_ms], dist, ctx.dev)
     nbytes = k2v4_bytes()
     tensor = ctx.path != kvq.PATH_SIMT
+    traffic, tsrc = profiled_traffic(workload, "k2v4") if tensor else (None, "no capture for the fp32 kernel")
     achieved = nbytes / (part_ms * 1e-3) / 1e9
     res = {
         "workload": WORKLOAD_NAMES[workload], "format": "K2/V4", "path": "tensor" if tensor else "simt",
@@ -493,8 +496,8 @@ def run_k2v4(ctx, workload, K, W, peaks, sampler, world, dist):
         "timing": {"partial_ms": round(part_ms, 5), "merge_ms": round(merge_ms, 5),
                    "how": "CUDA events recorded by the library around the partial kernel and the merge"},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                     "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": None,
-                     "traffic_source": "no capture for this workload", "algorithmic_bytes": nbytes,
+                     "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": traffic,
+                     "traffic_source": tsrc, "algorithmic_bytes": nbytes,
                      "peak_source": "hbm_gbs (measured)",
                      "kernel": "k2v4_tc_kernel<256> (tcgen05, tiles dequantized to f16 in shared memory)"
                      if tensor else "k2v4_partial_kernel (fp32)"},
