@@ -86,14 +86,19 @@ def test_fused_kv8_equals_encode_then_decode(kvq, oracle):
     np.testing.assert_array_equal(pools[0][0], oc)          # the appended rows, bit-exact
 
 
-def test_fused_config2_step(kvq):
-    """The decode step of the benchmark: 8 x 4096 rows, the new row last."""
+def test_fused_config2_step(kvq, oracle):
+    """The decode step of the benchmark: 8 x 4096 rows, the new row last; the
+    one-launch kernel against the two-call path (bit for bit) and, on sampled
+    (sequence, head) pairs, against the oracle; the appended rows bit-exact."""
     lens = [4096] * 8
     cu = synth.cu_seqlens(lens)
-    _, _, _, outs, pools = run_both(kvq, 1, lens, list(cu[1:] - 1), 2, 128, kvq.PATH_TENSOR)
+    cu, x_all, qv, outs, pools = run_both(kvq, 1, lens, list(cu[1:] - 1), 2, 128, kvq.PATH_TENSOR)
     np.testing.assert_array_equal(pools[0][0], pools[1][0])
     np.testing.assert_array_equal(outs[0], outs[1])
     assert np.all(np.isfinite(outs[0]))
+    pairs = [(b, h) for b in (0, 3, 7) for h in (0, 64, 127)]
+    oc, os_ = check_oracle(oracle, 1, x_all, cu, qv, outs[0], 2, TENSOR_TOL, pairs)
+    np.testing.assert_array_equal(pools[0][0], oc)
 
 
 @pytest.mark.parametrize("fmt,path,bf16", [(2, "tensor", True), (1, "simt", True), (1, "tensor", False)])

@@ -89,6 +89,56 @@ def test_config4_ragged_decode(kvq, oracle, ragged_inputs, fmt, path):
             assert e <= tol, (b, h, int(lens[b]), e)
 
 
+@pytest.mark.parametrize("fmt", [1, 2])
+def test_config4_ragged_decode_append(kvq, oracle, ragged_inputs, fmt):
+    """The step the benchmark times: kv_attn_decode_append on the tensor path
+    over the ragged batch, each sequence's new row written at its last
+    position (KV8: encoded inside the decode launch).  The appended rows are
+    bit-exact against the oracle's encoding; sampled outputs are checked
+    against the oracle over the master rows plus the new row."""
+    d = ragged_inputs
+    lens, cu, offs, x = d["lens"], d["cu"], d["offs"], d["x"]
+    seed = 4
+    layout = kvq.mla_layout(seed=seed)
+    mc, ms = gpu_encode(kvq, fmt, x, layout)
+    idx = np.concatenate([(o + np.arange(T, dtype=np.int64)) % MASTER for o, T in zip(offs, lens)])
+    idx_t = torch.from_numpy(idx).cuda()
+    codes = mc[idx_t].contiguous()
+    scales = ms[idx_t].contiguous()
+    del idx_t, mc, ms
+    total = int(cu[-1])
+    x_new = synth.mla_rows(7, B)
+    dst = (cu[1:] - 1).astype(np.int64)
+    out = torch.full((B, H, 512), float("nan"), device="cuda")
+    ws = torch.zeros(kvq.kv_attn_workspace_size(fmt, B, H, total, layout, kvq.PATH_TENSOR), dtype=torch.uint8,
+                     device="cuda")
+    kvq.kv_attn_decode_append(fmt, to_dev(x_new), to_dev(dst), _bf16_dev(d["q_bits"]), codes, scales, to_dev(cu),
+                              out, ws, total, SM, layout, kvq.PATH_TENSOR)
+    torch.cuda.synchronize()
+    assert kvq.read_device_error(ws) == 0
+    got = out.cpu().numpy()
+    assert np.all(np.isfinite(got))
+    if fmt == 1:
+        oc, os_ = oracle.kv8_encode(x)
+        nc, ns = oracle.kv8_encode(x_new)
+    else:
+        oc, os_ = oracle.tq4_encode(x, seed=seed)
+        nc, ns = oracle.tq4_encode(x_new, seed=seed)
+    np.testing.assert_array_equal(codes[torch.from_numpy(dst).cuda()].cpu().numpy(), nc)
+    np.testing.assert_array_equal(scales[torch.from_numpy(dst).cuda()].cpu().numpy().view(np.uint32),
+                                  ns.view(np.uint32))
+    seqs = sorted({int(np.argmax(lens)), int(np.argmin(lens)), 0, 21})
+    for b in seqs:
+        rows = (offs[b] + np.arange(lens[b] - 1, dtype=np.int64)) % MASTER
+        xh = np.concatenate([oracle.reconstruct(fmt, oc[rows], os_[rows], seed=seed),
+                             oracle.reconstruct(fmt, nc[b:b + 1], ns[b:b + 1], seed=seed)])
+        heads = [0, 63, 64, 127]
+        ref = oracle.attn_dense(xh, d["q"][b, heads], SM, 512)
+        for i, h in enumerate(heads):
+            e = rel_err(got[b, h], ref[i])
+            assert e <= TENSOR_TOL, (b, h, int(lens[b]), e)
+
+
 @pytest.fixture(scope="module")
 def prefill_inputs():
     n_past, n_new = 124 * 1024, 2048
