@@ -19,8 +19,9 @@ The same JSON line carries, under ``workloads``, the other timed workloads:
 * ``kv8_prefill`` / ``tq4_prefill``  chunked causal prefill: 2048 new rows
                    encoded and appended to a 124 x 1024 = 126,976-row cache,
                    then 2048 tokens x 128 heads attend rows [0, P + j];
-* ``kv8_8x4096``   decode of 8 sequences x 4096 rows (19 MB, fits in L2:
-                   a 256 MB buffer is written between timed steps);
+* ``kv8_8x4096`` / ``tq4_8x4096``  decode of 8 sequences x 4096 rows (KV8
+                   19 MB, TQ4 9.7 MB, both fit in L2: a 256 MB buffer is
+                   written between timed steps);
 * ``pq4_8x4096`` / ``pq4t_8x4096``  the same short decode step on a PolarQuant
                    4-bit cache (296 B/row), on the fp32 consumer (the default
                    path for PolarQuant) and on the tensor-core consumer;
@@ -87,6 +88,7 @@ WORKLOAD_NAMES = {
     "tq4_prefill": "chunked causal prefill, TQ4: 2048 new rows encoded onto 126976 cached rows, "
                    "2048 tokens x 128 heads, bf16 query",
     "kv8_8x4096": "decode, KV8: 8 seqs x 4096 rows, 128 heads, bf16 query, the step's 8 new rows appended",
+    "tq4_8x4096": "decode, TQ4: 8 seqs x 4096 rows, 128 heads, bf16 query, the step's 8 new rows appended",
     "pq4_8x4096": "decode, PolarQuant 4-bit: 8 seqs x 4096 rows, 128 heads, bf16 query, the step's 8 new rows "
                   "appended (fp32 consumer, the default path)",
     "pq4t_8x4096": "decode, PolarQuant 4-bit: 8 seqs x 4096 rows, 128 heads, bf16 query, the step's 8 new rows "
@@ -94,14 +96,15 @@ WORKLOAD_NAMES = {
     "k2v4_4x32768": "GQA decode, K2/V4: 4 seqs x 32768 cells, 2 kv heads x 256, 16 query heads, f32 query, "
                     "sinks 8 + window 256 fp16, K gain 1.10",
 }
-DEFAULT_WORKLOADS = ["kv8_ragged", "tq4_ragged", "kv8_prefill", "tq4_prefill", "kv8_8x4096", "pq4_8x4096",
-                     "pq4t_8x4096", "k2v4_4x32768"]
+DEFAULT_WORKLOADS = ["kv8_ragged", "tq4_ragged", "kv8_prefill", "tq4_prefill", "kv8_8x4096", "tq4_8x4096",
+                     "pq4_8x4096", "pq4t_8x4096", "k2v4_4x32768"]
 
 # profile summaries holding the ncu DRAM traffic of a dominant kernel, keyed by workload
 PROFILE_FOR = {"kv8_ragged": "decode_tc_kv8_ragged_b32_h128.md", "tq4_ragged": "decode_tc_tq4_ragged_b32_h128.md",
                "kv8_prefill": "prefill_tc_kv8_p126976_n2048_h128.md",
                "tq4_prefill": "prefill_tc_tq4_p126976_n2048_h128.md",
-               "k2v4_4x32768": "decode_tc_k2v4_b4_t32768.md"}
+               "k2v4_4x32768": "decode_tc_k2v4_b4_t32768.md",
+               "kv8_8x4096": "decode_tc_kv8_b8_t4096_h128.md", "tq4_8x4096": "decode_tc_tq4_b8_t4096_h128.md"}
 # the sources whose hash a traffic figure is tied to (the kernel changed => no figure)
 KERNEL_SOURCES = {1: ["attn_tc_kv8.cu", "tc_common.cuh", "attn_common.cuh", "kvq_internal.cuh"],
                   2: ["attn_tc_tq4.cu", "tc_common.cuh", "attn_common.cuh", "kvq_internal.cuh"],
