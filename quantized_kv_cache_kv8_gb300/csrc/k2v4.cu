@@ -692,14 +692,21 @@ __device__ __forceinline__ void k2v4_tc_pipe(const K2V4DecodeParams& p, unsigned
             }
         };
         // 2-bit codes (32 dims = 8 bytes; dims 2m, 2m+1 in bits 4m..4m+3)
-        // times the group's per-dim fp16 scales, pairwise in f16
+        // times the group's per-dim fp16 scales, pairwise in f16.  A code
+        // byte (dims 4q .. 4q+3) is spread to one code per byte by two masked
+        // multiplies (even codes, odd codes: no carries cross a byte), then
+        // x * 0x22 + 0x10 turns each code c into the byte-permute selector
+        // nibbles (2c, 2c + 1) of its f16 level: the low half selects the pair
+        // of dims 4q, 4q+1, the high half the pair 4q+2, 4q+3
         auto k_dec = [&](int r, int j, const uint32_t (&scw)[16], uint32_t (&kw)[16]) {
             const uint2 kc = *reinterpret_cast<const uint2*>(raw_kc + r * (D / 4) + 8 * j);
 #pragma unroll
-            for (int m = 0; m < 16; ++m) {
-                const uint32_t nib = ((m < 8 ? kc.x : kc.y) >> (4 * (m & 7))) & 15u;
-                const uint32_t sel = ((nib & 3u) | ((nib & 12u) << 6)) * 0x22u + 0x1010u;
-                kw[m] = hmul2_bits(__byte_perm(lv01, lv23, sel), scw[m]);
+            for (int q = 0; q < 8; ++q) {
+                const uint32_t t = (q < 4 ? kc.x : kc.y) >> (8 * (q & 3));
+                const uint32_t x = (((t & 0x33u) * 0x1001u) | ((t & 0xCCu) * 0x40040u)) & 0x03030303u;
+                const uint32_t sel = x * 0x22u + 0x10101010u;
+                kw[2 * q] = hmul2_bits(__byte_perm(lv01, lv23, sel), scw[2 * q]);
+                kw[2 * q + 1] = hmul2_bits(__byte_perm(lv01, lv23, sel >> 16), scw[2 * q + 1]);
             }
         };
         auto k_bulk = [&](int r, int j, uint32_t (&kw)[16]) {
