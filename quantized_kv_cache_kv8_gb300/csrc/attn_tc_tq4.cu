@@ -11,7 +11,7 @@
 //     value and the f16 residual of every head; to leave room for the retained
 //     chunks a CTA serves 32 heads: the score runs with N = 64 (32 values + 32
 //     residuals), the context with N = 32;
-//   - codes are nibbles: byte permutes over the 16 f16 levels (levels4) turn
+//   - codes are nibbles: byte permutes over the 16 f16 levels (store32) turn
 //     them into f16 operands, the levels scaled by kTq4Gamma (within 9.3e-5
 //     of f16; divided out of scores and context);
 //   - P is stored K-major (heads on rows) so that N = 32 needs no padding.
@@ -121,20 +121,6 @@ struct LevelBytes {
     uint32_t lo[4], hi[4];
 };
 
-// The 4 codes in the low 16 bits of s (one per nibble, dims in order) -> their
-// f16 levels as two f16x2 words, by byte permutes: the low 3 bits of each
-// code pick a byte from levels 0-7 and from levels 8-15, bit 3 picks between
-// the two, then the low and high byte planes are interleaved.  No shared
-// memory access (a 256-entry table in shared memory took ~4k bank-conflicted
-// wavefronts per tile on the port the MMAs read their operands through).
-__device__ __forceinline__ void levels4(const LevelBytes& t, uint32_t s, uint32_t& w0, uint32_t& w1) {
-    const uint32_t sel = s & 0x7777u;
-    const uint32_t pick = ((s >> 1) & 0x4444u) | 0x3210u;
-    const uint32_t l = __byte_perm(__byte_perm(t.lo[0], t.lo[1], sel), __byte_perm(t.lo[2], t.lo[3], sel), pick);
-    const uint32_t h = __byte_perm(__byte_perm(t.hi[0], t.hi[1], sel), __byte_perm(t.hi[2], t.hi[3], sel), pick);
-    w0 = __byte_perm(l, h, 0x5140u);
-    w1 = __byte_perm(l, h, 0x7362u);
-}
 
 // PolarQuant, 4 bits: a worker's raw share of a tile is half of one row --
 // row 32 (warp / 2) + lane, half h = warp % 2 -- as the byte ranges holding the
@@ -264,16 +250,31 @@ __device__ __forceinline__ void pq_rope_half(const RawPQ& r, int row, const floa
                        pack_h2(x[8 * q + 4], x[8 * q + 5]), pack_h2(x[8 * q + 6], x[8 * q + 7]));
 }
 
-// 16 code bytes (32 codes) -> 32 f16 levels at byte offset `b` (64 bytes) of
-// swizzled row `row`.
+// 16 code bytes (32 codes, one per nibble, dims in order) -> 32 f16 levels at
+// byte offset `b` (64 bytes) of swizzled row `row`, by byte permutes: the low
+// 3 bits of each code pick a byte from levels 0-7 and from levels 8-15, bit 3
+// picks between the two, then the low and high byte planes are interleaved.
+// The selector and pick words are formed once per code word (8 codes) and
+// shifted for its upper four codes (a byte permute reads only the low 16 bits
+// of its selector).  No shared memory access (a 256-entry table in shared
+// memory took ~4k bank-conflicted wavefronts per tile on the port the MMAs
+// read their operands through).
 __device__ __forceinline__ void store32(unsigned char* slot, const uint4& c, int row, int b, const LevelBytes& t) {
     const uint32_t in[4] = {c.x, c.y, c.z, c.w};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-        uint32_t w0, w1, w2, w3;
-        levels4(t, in[i], w0, w1);
-        levels4(t, in[i] >> 16, w2, w3);
-        *reinterpret_cast<uint4*>(slot + sw128(row, b + 16 * i)) = make_uint4(w0, w1, w2, w3);
+        const uint32_t sel = in[i] & 0x77777777u;
+        const uint32_t pick = ((in[i] >> 1) & 0x44444444u) | 0x32103210u;
+        uint32_t w[4];
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+            const uint32_t sl = hh ? sel >> 16 : sel, pk = hh ? pick >> 16 : pick;
+            const uint32_t l = __byte_perm(__byte_perm(t.lo[0], t.lo[1], sl), __byte_perm(t.lo[2], t.lo[3], sl), pk);
+            const uint32_t h = __byte_perm(__byte_perm(t.hi[0], t.hi[1], sl), __byte_perm(t.hi[2], t.hi[3], sl), pk);
+            w[2 * hh] = __byte_perm(l, h, 0x5140u);
+            w[2 * hh + 1] = __byte_perm(l, h, 0x7362u);
+        }
+        *reinterpret_cast<uint4*>(slot + sw128(row, b + 16 * i)) = make_uint4(w[0], w[1], w[2], w[3]);
     }
 }
 
