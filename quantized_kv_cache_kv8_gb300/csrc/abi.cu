@@ -385,7 +385,6 @@ static AttnPlan plan_prefill(int64_t n_past, int64_t n_new) {
     AttnPlan pl{};
     pl.chunk = std::max<int64_t>(1, n_past + n_new);
     pl.max_items = n_new;
-    pl.heads_per_cta = 16;
     return pl;
 }
 

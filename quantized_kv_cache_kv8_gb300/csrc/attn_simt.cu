@@ -3,7 +3,7 @@
 //
 // Work decomposition (split-T, [P1] Commits item 2: split-T kernels): the rows
 // of every sequence are cut into chunks of `chunk` rows; one CTA handles one
-// (chunk, group of 16 heads) and leaves a partial softmax state (running max
+// (chunk, group of 32 heads) and leaves a partial softmax state (running max
 // m, running sum l, unnormalized context o[512]) per head in the workspace.  A
 // second kernel merges the chunks of each (sequence, head) by log-sum-exp and,
 // for TQ4, unrotates the context once.  Ragged sequences are found on the
@@ -28,10 +28,10 @@ namespace kvq {
 namespace {
 
 constexpr int kD = kMlaD, kDL = kMlaDL, kDV = kMlaDV;
-constexpr int kHG = 16;   // heads per CTA
+constexpr int kHG = 32;   // heads per CTA: each tile is decoded (a PolarQuant row rebuilt) once for them
 constexpr int kTR = 16;   // rows per tile
 constexpr int kFlushTiles = 64;   // tiles per block sum (1024 rows)
-constexpr int kNT = 256;  // threads per CTA
+constexpr int kNT = 512;  // threads per CTA: a score (head, row) and a 4-head x 8-dim context share each
 constexpr int kXS = 580;  // shared-memory row stride in floats (bank spread)
 constexpr int kSmSMs = 152;
 
@@ -43,7 +43,7 @@ constexpr size_t kSmemFloats =
     (size_t)kHG * kXS + (size_t)kTR * kXS + kTR * 2 + kTR * kHG + kHG + 16 + 8 + 2 * kTR + 2 * kPqCentPairs;
 
 template <int FMT, bool QBF16, bool GATHER>
-__global__ void __launch_bounds__(kNT, 2) attn_partial_kernel(AttnParams p) {
+__global__ void __launch_bounds__(kNT, 1) attn_partial_kernel(AttnParams p) {
     launch_dependents();
     extern __shared__ float4 smem4[];
     float* qs = reinterpret_cast<float*>(smem4);
