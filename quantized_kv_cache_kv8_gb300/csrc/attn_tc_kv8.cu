@@ -165,6 +165,20 @@ __device__ __forceinline__ void load_rope(RawRope& r, const uint8_t* __restrict_
                           : make_uint4(0u, 0u, 0u, 0u);
     }
 }
+// The same three groups for a full tile of contiguous rows that does not hold
+// the appended row: no per-piece row tests, one base address per group.
+__device__ __forceinline__ void load_tile_full(RawGroup& a, RawGroup& b, RawRope& c,
+                                               const uint8_t* __restrict__ codes, int64_t t0, int warp, int lane,
+                                               int tid) {
+    const uint8_t* ga = codes + (t0 + 2 * warp + ((lane >> 2) & 1)) * kMlaD + 64 * (lane >> 3) + 16 * (lane & 3);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) a.v[i] = __ldg(reinterpret_cast<const uint4*>(ga + i * 16 * kMlaD));
+#pragma unroll
+    for (int i = 0; i < 8; ++i) b.v[i] = __ldg(reinterpret_cast<const uint4*>(ga + i * 16 * kMlaD + 256));
+    const uint8_t* gc = codes + (t0 + (tid >> 2)) * kMlaD + 512 + 16 * (tid & 3);
+#pragma unroll
+    for (int i = 0; i < 2; ++i) c.v[i] = __ldg(reinterpret_cast<const uint4*>(gc + i * (kWorkers / 4) * kMlaD));
+}
 
 // 16 e4m3 codes -> 16 f16 values (exact) at byte offset `b` of swizzled row `row`.
 __device__ __forceinline__ void store16(unsigned char* slot, const uint4& c, int row, int b) {
@@ -589,20 +603,27 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kv8_kernel(AttnParams p) 
         // all of tile t+1 is requested before the softmax (its raw codes stay in
         // registers across it: the worker warps' share of the register split)
         if (!GATHER && t + 1 < n_tiles) {
-            load_group<APPEND, GATHER>(rawA, p.codes, t1, nt1, 0, warp, lane, rn, sNew, nullptr);
-            load_group<APPEND, GATHER>(rawB, p.codes, t1, nt1, 1, warp, lane, rn, sNew, nullptr);
-            load_rope<APPEND, GATHER>(rawC, p.codes, t1, nt1, tid, rn, sNew, nullptr);
+            if (nt1 == kRows && !(APPEND && rn >= t1 && rn < t1 + kRows)) {
+                load_tile_full(rawA, rawB, rawC, p.codes, t1, warp, lane, tid);
+            } else {
+                load_group<APPEND, GATHER>(rawA, p.codes, t1, nt1, 0, warp, lane, rn, sNew, nullptr);
+                load_group<APPEND, GATHER>(rawB, p.codes, t1, nt1, 1, warp, lane, rn, sNew, nullptr);
+                load_rope<APPEND, GATHER>(rawC, p.codes, t1, nt1, tid, rn, sNew, nullptr);
+            }
             load_scales(t1, nt1);
         }
 
         // ---- softmax of the tile: thread = row srow, 32 heads ----
-        mbar_wait(&bars[kBarScore], (uint32_t)t & 1u, sAbort, wl);
+        // one warp polls; the others wait on the named barrier, issuing nothing
+        if (warp == 1) mbar_wait(&bars[kBarScore], (uint32_t)t & 1u, sAbort, wl);
+        worker_sync();
         tc_after();
-        // z = sm log2(e) (s_L S_L + s_R S_R) for this row's 32 heads, read from TMEM
+        // d = z - m with z = sm log2(e) (s_L S_L + s_R S_R), for this row's 32
+        // heads read from TMEM: the lag test below and the weights 2^d after it
         float z[32];
         const float za = my_sl * cz, zb = my_sr * cz;
         const bool row_ok = srow < nt;
-        auto load_z = [&]() {
+        auto load_d = [&]() {
             // 16 heads at a time: their rope and latent columns go out together,
             // then one wait (all four at once made the appending kernel spill)
 #pragma unroll
@@ -613,27 +634,21 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kv8_kernel(AttnParams p) 
                 tmem_wait_ld();
 #pragma unroll
                 for (int j = 0; j < 16; ++j)
-                    z[16 * c + j] =
-                        row_ok ? fmaf(__uint_as_float(l[j]), za, __uint_as_float(r[j]) * zb) : -INFINITY;
+                    z[16 * c + j] = row_ok ? fmaf(__uint_as_float(l[j]), za,
+                                                  fmaf(__uint_as_float(r[j]), zb, -mreg[16 * c + j]))
+                                           : -INFINITY;
             }
-        };
-        // d = z - m: the lag test below and the weights 2^d after it
-        auto load_d = [&]() {
-            load_z();
-#pragma unroll
-            for (int j = 0; j < 32; ++j) z[j] -= mreg[j];
         };
         load_d();
         // a latent scale with s_L max_h E > kScaleLim takes the exact path
         // (max_h E is +inf while only inert latent blocks have been met); so
         // does a score past m by more than the lag (m = -inf before the first
-        // exact path: d = +inf, or NaN on a row past the tile's end, which the
-        // valid rows outvote)
-        // one maximum over the heads, then one test (fmaxf passes over NaN, as
-        // a comparison per head would)
-        float dmax = z[0];
+        // exact path: d = +inf on every row of the tile)
+        // one maximum over the heads, then one test
+        float dm[4] = {z[0], z[1], z[2], z[3]};
 #pragma unroll
-        for (int j = 1; j < 32; ++j) dmax = fmaxf(dmax, z[j]);
+        for (int j = 4; j < 32; ++j) dm[j & 3] = fmaxf(dm[j & 3], z[j]);
+        const float dmax = fmaxf(fmaxf(dm[0], dm[1]), fmaxf(dm[2], dm[3]));
         const bool flag = (*sAbort != 0) | (my_sl * emax > kScaleLim) | (dmax > kLagLog2);
         const bool any_flag = worker_any(flag);
         if (GATHER && t + 1 < n_tiles) {

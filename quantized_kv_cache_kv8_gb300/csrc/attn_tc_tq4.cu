@@ -606,7 +606,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_tq4_kernel(AttnParams p) 
         if (t + 1 < n_tiles) load_tile(t1, nt1);
 
         // ---- softmax of the tile: thread = row srow, 16 heads ----
-        mbar_wait(&bars[kBarScore], (uint32_t)t & 1u, sAbort, p.wait_limit);
+        // one warp polls; the others wait on the named barrier, issuing nothing
+        if (warp == 1) mbar_wait(&bars[kBarScore], (uint32_t)t & 1u, sAbort, p.wait_limit);
+        worker_sync();
         tc_after();
         float z[16];
         const float za = my_sl * cz, zb = my_sr * cz;
@@ -625,17 +627,27 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_tq4_kernel(AttnParams p) 
                                      (__uint_as_float(a[j]) + __uint_as_float(c[j])) * zb)
                               : -INFINITY;
         };
-        load_z();
         // d = z - m: the lag test and the weights 2^d (m = -inf before the first
-        // exact path: d = +inf, or NaN on a row past the tile's end, which the
-        // valid rows outvote)
+        // exact path: d = +inf on every row of the tile)
+        auto load_d = [&]() {
+            uint32_t a[16], c[16], e[16], f[16];
+            tmem_ld16(tmem + lane_base + kColSR + 16 * hq, a);
+            tmem_ld16(tmem + lane_base + kColSR + kHC + 16 * hq, c);
+            tmem_ld16(tmem + lane_base + kColSL + 16 * hq, e);
+            tmem_ld16(tmem + lane_base + kColSL + kHC + 16 * hq, f);
+            tmem_wait_ld();
 #pragma unroll
-        for (int j = 0; j < 16; ++j) z[j] -= mreg[j];
-        // one maximum over the heads, then one test (fmaxf passes over NaN, as
-        // a comparison per head would)
-        float dmax = z[0];
+            for (int j = 0; j < 16; ++j)
+                z[j] = row_ok ? fmaf(__uint_as_float(e[j]) + __uint_as_float(f[j]), za,
+                                     fmaf(__uint_as_float(a[j]) + __uint_as_float(c[j]), zb, -mreg[j]))
+                              : -INFINITY;
+        };
+        load_d();
+        // one maximum over the heads, then one test
+        float dm[4] = {z[0], z[1], z[2], z[3]};
 #pragma unroll
-        for (int j = 1; j < 16; ++j) dmax = fmaxf(dmax, z[j]);
+        for (int j = 4; j < 16; ++j) dm[j & 3] = fmaxf(dm[j & 3], z[j]);
+        const float dmax = fmaxf(fmaxf(dm[0], dm[1]), fmaxf(dm[2], dm[3]));
         const bool flag = (*sAbort != 0) | (my_sl > s_lim) | (dmax > kLagLog2);
         if (worker_any(flag)) {
             if (worker_any(*sAbort != 0)) break;
@@ -696,9 +708,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_tq4_kernel(AttnParams p) 
 #pragma unroll
             for (int j = 0; j < 16; ++j) lsum[j] *= sAlphaM[16 * hq + j];
             load_state();
-            load_z();
-#pragma unroll
-            for (int j = 0; j < 16; ++j) z[j] -= mreg[j];
+            load_d();
         }
         {
             // row-sum weights p = 2^(z - m), f16 context weights w = p s_L E
