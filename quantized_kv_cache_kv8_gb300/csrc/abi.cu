@@ -111,7 +111,7 @@ static kvq_status resolve_k2v4_path(kvq_path path, const kvq_k2v4_layout* L, boo
 }
 
 AttnPlan plan_decode(kvq_format fmt, kvq_path resolved, int32_t batch, int32_t n_heads, int64_t max_total_rows,
-                     int waves = kDecodeWaves) {
+                     int waves) {
     return resolved == KVQ_PATH_TENSOR ? plan_decode_tc(fmt, batch, n_heads, max_total_rows, waves)
                                        : plan_decode_simt(batch, n_heads, max_total_rows);
 }
@@ -285,7 +285,7 @@ extern "C" {
 
 size_t kv_attn_workspace_size(kvq_format fmt, const kvq_mla_layout* layout, int32_t batch, int32_t n_heads,
                               int64_t max_total_rows, kvq_path path) {
-    return attn_workspace_size_waves(fmt, layout, batch, n_heads, max_total_rows, path, kDecodeWaves);
+    return attn_workspace_size_waves(fmt, layout, batch, n_heads, max_total_rows, path, decode_waves(fmt));
 }
 
 kvq_status kv_attn_decode(kvq_format fmt, const kvq_mla_layout* layout, const void* q, kvq_dtype q_dtype,
@@ -293,7 +293,7 @@ kvq_status kv_attn_decode(kvq_format fmt, const kvq_mla_layout* layout, const vo
                           const int64_t* cu_seqlens, int64_t max_total_rows, float sm_scale, float* out,
                           void* workspace, size_t workspace_bytes, kvq_path path, void* stream) {
     return attn_decode_waves(fmt, layout, q, q_dtype, batch, n_heads, codes, scales, cu_seqlens, max_total_rows,
-                             sm_scale, out, workspace, workspace_bytes, path, stream, kDecodeWaves);
+                             sm_scale, out, workspace, workspace_bytes, path, stream, decode_waves(fmt));
 }
 
 kvq_status kv_attn_decode_append(kvq_format fmt, const kvq_mla_layout* layout, const float* x_new,
@@ -319,7 +319,7 @@ kvq_status kv_attn_decode_append(kvq_format fmt, const kvq_mla_layout* layout, c
     if (!workspace || workspace_bytes < need) return KVQ_ERR_WORKSPACE;
     cudaStream_t st = (cudaStream_t)stream;
     if (rp == KVQ_PATH_TENSOR && fmt == KVQ_KV8 && q_dtype == KVQ_BF16) {
-        const AttnPlan pl = plan_decode(fmt, rp, batch, n_heads, max_total_rows);
+        const AttnPlan pl = plan_decode(fmt, rp, batch, n_heads, max_total_rows, decode_waves(fmt));
         return cuda_status(launch_attn_tc_kv8_append(*layout, x_new, dst_rows, q, batch, n_heads, codes, scales,
                                                      cu_seqlens, pl, sm_scale, out, workspace, st));
     }
@@ -347,7 +347,7 @@ size_t kv_attn_gather_workspace_size(kvq_format fmt, const kvq_mla_layout* layou
     if (batch < 0 || n_heads < 0 || max_total_selected < 0 || (q_dtype != KVQ_F32 && q_dtype != KVQ_BF16)) return 0;
     kvq_path rp;
     if (resolve_gather_path(fmt, q_dtype, path, layout, n_heads, &rp) != KVQ_OK) return 0;
-    const AttnPlan pl = plan_decode(fmt, rp, batch, n_heads, max_total_selected);
+    const AttnPlan pl = plan_decode(fmt, rp, batch, n_heads, max_total_selected, decode_waves(fmt));
     return kWsHeader + partial_bytes(pl.max_items, n_heads, layout->v_dim);
 }
 
@@ -373,7 +373,7 @@ kvq_status kv_attn_decode_gather(kvq_format fmt, const kvq_mla_layout* layout, c
     const size_t need = kv_attn_gather_workspace_size(fmt, layout, q_dtype, batch, n_heads, max_total_selected, path);
     if (!workspace || workspace_bytes < need) return KVQ_ERR_WORKSPACE;
     cudaStream_t st = (cudaStream_t)stream;
-    const AttnPlan pl = plan_decode(fmt, rp, batch, n_heads, max_total_selected);
+    const AttnPlan pl = plan_decode(fmt, rp, batch, n_heads, max_total_selected, decode_waves(fmt));
     if (rp == KVQ_PATH_TENSOR)
         return cuda_status(launch_attn_tc(fmt, *layout, q, q_dtype, batch, n_heads, codes, scales, cu_sel, -1, pl,
                                           sm_scale, out, workspace, st, sel_rows, pool_rows));

@@ -225,8 +225,10 @@ cudaError_t launch_attn_simt(kvq_format fmt, const kvq_mla_layout& L, const void
 // Tensor-core attention (tcgen05; 64 heads per CTA for KV8, 32 for TQ4).
 bool tc_supported(const kvq_mla_layout& L, int32_t n_heads);
 // Waves of work items a decode workspace is sized for (the device picks
-// 1 .. waves from the actual lengths).
-constexpr int kDecodeWaves = 4;
+// 1 .. waves from the actual lengths): 4 for KV8's 64-head CTAs, 6 for the
+// 32-head CTAs of TQ4 and PolarQuant (on the 32-sequence ragged decode KV8
+// took 1.003 ms at 4 waves and 1.007 ms at 6, TQ4 2.442 ms and 2.399 ms).
+constexpr int decode_waves(kvq_format fmt) { return fmt == KVQ_KV8 ? 4 : 6; }
 AttnPlan plan_decode_tc(kvq_format fmt, int32_t batch, int32_t n_heads, int64_t max_total_rows, int waves);
 // kv_attn_workspace_size / kv_attn_decode with a given wave budget (the
 // no-allocation entry takes fewer waves to fit its fixed scratch).

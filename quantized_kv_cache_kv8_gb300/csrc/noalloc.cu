@@ -102,10 +102,10 @@ extern "C" kvq_status kv_attn_decode_noalloc(kvq_format fmt, const kvq_mla_layou
     // valid (and KVQ_OK for an empty batch), launching nothing either way
     const kvq_status pre = kvq::attn_decode_waves(fmt, layout, q, q_dtype, batch, n_heads, codes, scales, cu_seqlens,
                                                   max_total_rows, sm_scale, out, nullptr, 0, path, stream,
-                                                  kvq::kDecodeWaves);
+                                                  kvq::decode_waves(fmt));
     if (pre != KVQ_ERR_WORKSPACE) return pre;
     // the largest wave budget whose workspace fits the scratch
-    int waves = kvq::kDecodeWaves;
+    int waves = kvq::decode_waves(fmt);
     size_t need = kvq::attn_workspace_size_waves(fmt, layout, batch, n_heads, max_total_rows, path, waves);
     while (need > kNoAllocScratchBytes && waves > 1)
         need = kvq::attn_workspace_size_waves(fmt, layout, batch, n_heads, max_total_rows, path, --waves);

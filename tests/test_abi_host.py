@@ -89,11 +89,12 @@ def test_workspace_sizes_grow_with_work(kvq):
     # tensor-core split: a host chunk when it guarantees one wave (76 items of
     # 64 heads per wave for KV8) near the ideal size: 8 x 4096 rows -> 512-row
     # chunks, 64 + 8 items; otherwise the device balances items over at most
-    # 4 waves (38 items of 32 heads per wave for TQ4; whole waves per 76 / 38
-    # sequences), never more than one per 128-row tile plus one per sequence
+    # 4 waves for KV8 and 6 for TQ4 (76 items of 64 heads, 38 items of 32
+    # heads per wave; whole waves per 76 / 38 sequences), never more than one
+    # per 128-row tile plus one per sequence
     assert a == 256 + (64 + 8) * item
     assert b == 256 + 4 * 76 * item
-    assert kvq.kv_attn_workspace_size(2, 8, 128, 32768) == 256 + 4 * 38 * item
+    assert kvq.kv_attn_workspace_size(2, 8, 128, 32768) == 256 + 6 * 38 * item
     assert kvq.kv_attn_workspace_size(1, 8, 128, 1000) == 256 + (8 + 8) * item
     assert kvq.kv_attn_workspace_size(1, 100, 128, 10**6) == 256 + 4 * 152 * item
     # the SIMT split grows with the rows
