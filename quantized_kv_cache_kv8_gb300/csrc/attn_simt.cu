@@ -42,6 +42,53 @@ constexpr int kPqCentPairs = 9 * 64;
 constexpr size_t kSmemFloats =
     (size_t)kHG * kXS + (size_t)kTR * kXS + kTR * 2 + kTR * kHG + kHG + 16 + 8 + 2 * kTR + 2 * kPqCentPairs;
 
+// One PolarQuant block of n = 32 Q leaves (2^L, unit top radius) rebuilt by
+// one warp in registers and stored to y[0 .. n).  Lane k owns the subtree of
+// node k at level log2(Q): its radius is the product of the factors on its
+// path from the root (each lane reads the top L - log2(Q) angles of that
+// path), then the lane expands its Q leaves level by level.  Node j of level
+// l is the right child (factor sin) when j is odd.  The products are taken in
+// the in-place expansion's order (root to leaf, each rounded once), so the
+// leaves are bit-identical to it, without its strided shared-memory accesses
+// (2- to 16-way bank conflicts at every level).
+template <int Q, int L>
+__device__ __forceinline__ void pq_expand_regs(const uint8_t* __restrict__ stream, int b, const float2* cent, float* y,
+                                               int lane) {
+    constexpr int n = 32 * Q;
+    constexpr int Lb = Q == 16 ? 4 : Q == 8 ? 3 : Q == 4 ? 2 : Q == 2 ? 1 : 0;
+    static_assert((1 << Lb) == Q && n == (1 << L), "block shape");
+    float v = 1.0f;
+#pragma unroll
+    for (int l = L; l > Lb; --l) {
+        const int j = lane >> (l - Lb);            // the path's node at level l
+        const int first = n - (n >> (l - 1));      // stream index of level l's first angle
+        const float2 cs = cent[((l - 1) << b) + pq_get_bits(stream, (int64_t)(first + j) * b, b)];
+        v = __fmul_rn(v, ((lane >> (l - 1 - Lb)) & 1) ? cs.y : cs.x);
+    }
+    float t[Q];
+    t[0] = v;
+#pragma unroll
+    for (int l = Lb; l >= 1; --l) {
+        const int first = n - (n >> (l - 1));
+#pragma unroll
+        for (int jj = 0; jj < (Q >> l); ++jj) {
+            const int j = (lane << (Lb - l)) + jj;
+            const float2 cs = cent[((l - 1) << b) + pq_get_bits(stream, (int64_t)(first + j) * b, b)];
+            const float r = t[jj << l];
+            t[jj << l] = __fmul_rn(r, cs.x);
+            t[(jj << l) + (1 << (l - 1))] = __fmul_rn(r, cs.y);
+        }
+    }
+    if constexpr (Q % 4 == 0) {
+#pragma unroll
+        for (int i = 0; i < Q; i += 4)
+            *reinterpret_cast<float4*>(y + Q * lane + i) = make_float4(t[i], t[i + 1], t[i + 2], t[i + 3]);
+    } else {
+        static_assert(Q == 2, "leaves per lane");
+        *reinterpret_cast<float2*>(y + 2 * lane) = make_float2(t[0], t[1]);
+    }
+}
+
 template <int FMT, bool QBF16, bool GATHER>
 __global__ void __launch_bounds__(kNT, 1) attn_partial_kernel(AttnParams p) {
     launch_dependents();
@@ -152,8 +199,8 @@ __global__ void __launch_bounds__(kNT, 1) attn_partial_kernel(AttnParams p) {
                 float* xr = xs + r * kXS;
                 if (r < nt) {
                     const uint8_t* cr = p.codes + (GATHER ? prow[r] : t0 + r) * p.pq_row_bytes;
-                    pq_expand_block(cr, kDL, 9, p.pq_bits, 1.0f, pqc, xr, lane);
-                    pq_expand_block(cr + p.pq_boff1, kMlaDR, 6, p.pq_bits, 1.0f, pqc, xr + kDL, lane);
+                    pq_expand_regs<kDL / 32, 9>(cr, p.pq_bits, pqc, xr, lane);
+                    pq_expand_regs<kMlaDR / 32, 6>(cr + p.pq_boff1, p.pq_bits, pqc, xr + kDL, lane);
                 } else {
                     for (int i = lane; i < kD; i += 32) xr[i] = 0.0f;
                 }
