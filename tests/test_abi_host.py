@@ -95,6 +95,10 @@ def test_workspace_sizes_grow_with_work(kvq):
     assert a == 256 + (64 + 8) * item
     assert b == 256 + 4 * 76 * item
     assert kvq.kv_attn_workspace_size(2, 8, 128, 32768) == 256 + 6 * 38 * item
+    # the PolarQuant-4 tensor consumer runs the TQ4 kernel's 32-head CTAs
+    assert kvq.kv_attn_workspace_size(kvq.KVQ_PQ4, 8, 128, 32768, path=kvq.PATH_TENSOR) == 256 + 6 * 38 * item
+    # a ragged batch of 32 sequences: one wave holds 38 of them, so 6 waves of 38
+    assert kvq.kv_attn_workspace_size(2, 32, 128, 2_100_000) == 256 + 6 * 38 * item
     assert kvq.kv_attn_workspace_size(1, 8, 128, 1000) == 256 + (8 + 8) * item
     assert kvq.kv_attn_workspace_size(1, 100, 128, 10**6) == 256 + 4 * 152 * item
     # the SIMT split grows with the rows
